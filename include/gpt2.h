@@ -1,0 +1,206 @@
+/*
+ * gpt2.h -- C ABI of the B300-native GPT-2 training step (libgpt2.so).
+ *
+ * The library computes one GPT-2 training step -- forward pass with the
+ * mean cross-entropy loss, backward pass, AdamW update -- over memory it
+ * allocates once at build time, the design of llm.c as described in
+ * QbitAI, "OpenAI founder hand-writes a thousand lines of C to train GPT"
+ * (section "Manually implementing each layer's forward/backward pass": all
+ * memory is allocated at the start as one 1-D block and stays constant while
+ * batches stream through) and in InfoQ, "Real men program in C: a large
+ * model hand-built from 1000 lines of C" (the layer list: encoder,
+ * layernorm, matmul, self-attention, gelu, residual, softmax, cross-entropy;
+ * the forward / zero-grad / backward / update loop).
+ *
+ * Every stage runs in the library's own sm_103a CUDA kernels.  There is no
+ * CPU fallback: a call that cannot run on the GPU returns an error.
+ *
+ * Conventions for every function below
+ *   - Return value: GPT2_OK (0) or one of the negative GPT2_ERR_* codes.
+ *     No function aborts, throws or traps; gpt2_last_error() gives text.
+ *   - A gpt2_model is used by one host thread at a time; calls are not
+ *     re-entrant.  Work is enqueued on the model's stream (gpt2_set_stream)
+ *     and is asynchronous unless the function says it synchronises.
+ *   - "device pointer" = CUDA global memory on the model's device;
+ *     "host pointer" = ordinary (optionally pinned) host memory.
+ *   - All floating-point tensors are row-major and contiguous.
+ */
+#ifndef GPT2_H
+#define GPT2_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GPT2_API __attribute__((visibility("default")))
+#else
+#define GPT2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ codes */
+#define GPT2_OK 0
+#define GPT2_ERR_ARG (-1)       /* null pointer, bad shape, bad argument value    */
+#define GPT2_ERR_OOM (-2)       /* a device allocation at build time failed       */
+#define GPT2_ERR_CUDA (-3)      /* a CUDA runtime/driver call failed              */
+#define GPT2_ERR_STATE (-4)     /* call-order violation (e.g. backward w/o loss)  */
+#define GPT2_ERR_TOKEN (-5)     /* a token or target id outside [0, V)            */
+#define GPT2_ERR_TIMEOUT (-6)   /* a bounded device-side wait expired             */
+#define GPT2_ERR_NONFINITE (-7) /* the loss is NaN or infinite                    */
+
+/* Arithmetic of the step.
+ *   GPT2_FP32: every product and sum in fp32 (SIMT FFMA; no TF32, no bf16).
+ *   GPT2_BF16: fp32 master weights, Adam moments and gradients; the matmul and
+ *              attention operands are bf16 (a bf16 copy of the weights is
+ *              refreshed by every AdamW step) with fp32 accumulation on the
+ *              tcgen05 tensor cores; the residual stream, LayerNorm
+ *              statistics, softmax statistics and losses stay fp32. */
+typedef enum { GPT2_FP32 = 0, GPT2_BF16 = 1 } gpt2_precision;
+
+/* Model shape and the batch shape the buffers are sized for.  The fields
+ * named after the run log's header block (max_seq_len, vocab_size,
+ * num_layers, num_heads, channels) mean what they mean there.
+ * Constraints (checked by gpt2_build, GPT2_ERR_ARG otherwise):
+ *   num_layers >= 1; channels % num_heads == 0; channels % 8 == 0;
+ *   head size channels/num_heads in {16, 32, 64, 128};
+ *   vocab_size <= padded_vocab_size and padded_vocab_size % 8 == 0;
+ *   1 <= seq_len <= max_seq_len <= 4096; batch_size >= 1;
+ *   batch_size * seq_len <= 32768. */
+typedef struct gpt2_config {
+  int32_t max_seq_len;       /* maxT: rows of the position embedding          */
+  int32_t vocab_size;        /* V: real vocabulary, the softmax's width       */
+  int32_t padded_vocab_size; /* Vp: rows of the token embedding (pad rows 0)  */
+  int32_t num_layers;        /* L                                              */
+  int32_t num_heads;         /* NH                                             */
+  int32_t channels;          /* C                                              */
+  int32_t batch_size;        /* B                                              */
+  int32_t seq_len;           /* T                                              */
+  int32_t precision;         /* gpt2_precision                                 */
+} gpt2_config;
+
+/* Opaque model: owns every device buffer (parameter, gradient, AdamW m and
+ * v arrays, the bf16 weight copy, the activations, the scratch). */
+typedef struct gpt2_model gpt2_model;
+
+/* The four fp32 arrays that share the parameter layout (gpt2_tensor_info). */
+typedef enum {
+  GPT2_PARAMS = 0, GPT2_GRADS = 1, GPT2_ADAM_M = 2, GPT2_ADAM_V = 3
+} gpt2_arena;
+
+/* Allocate every buffer once on the current CUDA device and draw the
+ * initial parameters on the device:
+ *   N(0, 0.02) for wte rows < V, wpe and the qkv / attproj / fc / fcproj
+ *   weights, attproj and fcproj further scaled by 1/sqrt(2 L); all biases 0;
+ *   LayerNorm gamma 1, beta 0; wte pad rows 0.
+ * The normal draw for parameter-array element e: Philox4x32-10 (Salmon et
+ * al., SC'11) at counter (e/2 low word, e/2 high word, 0, 0), key (seed low
+ * word, seed high word); u1 = (word0 + 1) / 2^32, u2 = word1 / 2^32;
+ * sqrt(-2 ln u1) * cos(2 pi u2) for even e, * sin(2 pi u2) for odd e.
+ * Gradients and Adam moments start at zero.  Synchronises.
+ *   cfg: host pointer, read only during the call.
+ *   out: host pointer that receives the model (NULL on failure).
+ * Errors: GPT2_ERR_ARG (bad shape), GPT2_ERR_OOM, GPT2_ERR_CUDA. */
+GPT2_API int gpt2_build(const gpt2_config* cfg, uint64_t seed, gpt2_model** out);
+
+/* Release every buffer of the model; NULL is allowed.  Synchronises. */
+GPT2_API void gpt2_free(gpt2_model* m);
+
+/* Enqueue all later work on this stream (a cudaStream_t, e.g. a torch
+ * stream's handle; NULL = the legacy default stream).  The caller keeps the
+ * stream alive while the model uses it. */
+GPT2_API int gpt2_set_stream(gpt2_model* m, void* cuda_stream);
+
+/* Forward pass over one batch.
+ *   tokens:  device pointer, int32 [B, T], ids in [0, V).
+ *   targets: device pointer, int32 [B, T] next-token ids in [0, V), or NULL
+ *            for logits only (then gpt2_backward returns GPT2_ERR_STATE and
+ *            gpt2_copy_logits_out becomes valid).
+ *   mean_loss: host pointer or NULL.  If non-NULL the call synchronises and
+ *            writes the mean over the B*T positions of -log softmax(logits)
+ *            [target]; it then also reports device-side errors (out-of-range
+ *            ids: GPT2_ERR_TOKEN; NaN/Inf loss: GPT2_ERR_NONFINITE).  If NULL
+ *            the call is asynchronous; errors surface at the next
+ *            synchronising call.
+ * The ids are copied into the model, so the caller may reuse the buffers
+ * once the stream has passed this call.  With targets, the softmax-minus-
+ * one-hot gradient of the loss is computed in the same pass, ready for
+ * gpt2_backward. */
+GPT2_API int gpt2_forward(gpt2_model* m, const int32_t* tokens, const int32_t* targets,
+                 float* mean_loss);
+
+/* As gpt2_forward, with tokens and targets in host memory (pinned memory
+ * makes the copy asynchronous); the host-to-device copies are enqueued on
+ * the model's stream before the forward pass. */
+GPT2_API int gpt2_forward_host(gpt2_model* m, const int32_t* host_tokens,
+                      const int32_t* host_targets, float* mean_loss);
+
+/* Set every gradient to zero (the gradient array is accumulated into). */
+GPT2_API int gpt2_zero_grad(gpt2_model* m);
+
+/* Backward pass of the last forward (which must have had targets):
+ * gradients of the mean loss with respect to every parameter are ADDED to
+ * the gradient array.  Asynchronous. */
+GPT2_API int gpt2_backward(gpt2_model* m);
+
+/* One AdamW update of every parameter, t = 1-based step number:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g^2;
+ *   p = p - lr * ( (m/(1-b1^t)) / (sqrt(v/(1-b2^t)) + eps) + wd * p ).
+ * Also refreshes the bf16 weight copy (bf16 mode).  Asynchronous.
+ * Errors: GPT2_ERR_ARG for t < 1 or a non-finite hyper-parameter. */
+GPT2_API int gpt2_adamw_step(gpt2_model* m, float lr, float beta1, float beta2,
+                    float eps, float weight_decay, int32_t t);
+
+/* Wait for all enqueued work; report device-side errors recorded since the
+ * last synchronising call (GPT2_ERR_TOKEN, GPT2_ERR_TIMEOUT). */
+GPT2_API int gpt2_synchronize(gpt2_model* m);
+
+/* The configuration the model was built with. */
+GPT2_API int gpt2_get_config(const gpt2_model* m, gpt2_config* out);
+
+/* Number of fp32 elements in the parameter array (Vp rows of wte). */
+GPT2_API int gpt2_num_params(const gpt2_model* m, int64_t* n);
+
+/* Number of parameter tensors (16) and, for 0 <= idx < that number, the
+ * name, element offset and element count of tensor idx in the parameter
+ * array.  Order: wte[Vp,C], wpe[maxT,C], ln1w[L,C], ln1b[L,C],
+ * qkvw[L,3C,C], qkvb[L,3C], attprojw[L,C,C], attprojb[L,C], ln2w[L,C],
+ * ln2b[L,C], fcw[L,4C,C], fcb[L,4C], fcprojw[L,C,4C], fcprojb[L,C],
+ * lnfw[C], lnfb[C].  A Linear's weight is [out, in]: y = x W^T + b.
+ * *name points to static storage. */
+GPT2_API int gpt2_num_tensors(const gpt2_model* m, int32_t* n);
+GPT2_API int gpt2_tensor_info(const gpt2_model* m, int32_t idx, const char** name,
+                     int64_t* offset, int64_t* numel);
+
+/* Copy one fp32 array (gpt2_arena) out to / in from host memory of
+ * gpt2_num_params floats.  Synchronises.  Copying parameters in also
+ * refreshes the bf16 weight copy. */
+GPT2_API int gpt2_copy_out(gpt2_model* m, int32_t arena, float* host_dst);
+GPT2_API int gpt2_copy_in(gpt2_model* m, int32_t arena, const float* host_src);
+
+/* Per-position losses [B*T] of the last forward with targets.  Synchronises. */
+GPT2_API int gpt2_copy_losses_out(gpt2_model* m, float* host_dst);
+
+/* Logits [B*T, Vp] (as fp32; pad columns are 0 * lnf = 0) of the last
+ * forward WITHOUT targets.  Synchronises.  GPT2_ERR_STATE otherwise. */
+GPT2_API int gpt2_copy_logits_out(gpt2_model* m, float* host_dst);
+
+/* The fp32 residual stream [B*T, C] entering block `layer` of the last
+ * forward: layer 0 is the encoder output wte[token] + wpe[position],
+ * layer L the input of the final LayerNorm.  Synchronises.
+ * Errors: GPT2_ERR_ARG (layer outside [0, L]), GPT2_ERR_STATE (no forward). */
+GPT2_API int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* host_dst);
+
+/* Number of kernel launches the library made since the model was built
+ * (a plain host-side counter). */
+GPT2_API int gpt2_launch_count(const gpt2_model* m, int64_t* n);
+
+/* Text of the last error on this model (or of the last failed gpt2_build
+ * when m is NULL).  Static or model-owned storage; never NULL. */
+GPT2_API const char* gpt2_last_error(const gpt2_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT2_H */

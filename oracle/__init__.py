@@ -48,6 +48,8 @@ def lib():
             f = getattr(L, "oracle_fwdbwd_" + suf)
             f.argtypes = [_i32p, fp, _i32p, vp, vp, vp, vp]
             f.restype = ctypes.c_double
+        L.oracle_residuals_f32.argtypes = [_i32p, _f32p, _i32p, _f32p]
+        L.oracle_residuals_f32.restype = ctypes.c_int
         flt, dbl = ctypes.c_float, ctypes.c_double
         L.oracle_adamw_f32.argtypes = [_i64, _f32p, _f32p, _f32p, _f32p, flt, flt, flt, flt, flt, ctypes.c_int]
         L.oracle_adamw_f64.argtypes = [_i64, _f64p, _f64p, _f64p, _f64p, dbl, dbl, dbl, dbl, dbl, ctypes.c_int]
@@ -136,6 +138,15 @@ def fwdbwd(cfg, params, tokens, targets=None, want_grads=True, want_logits=False
     loss = f(cfg, params, tokens, _ptr(tg), _ptr(grads), _ptr(losses), _ptr(logits))
     return dict(loss=loss, losses=losses, grads=grads,
                 logits=None if logits is None else logits.reshape(B * T, V))
+
+
+def residuals_f32(cfg, params, tokens):
+    """fp32 residual streams [(L+1), B*T, C] of a forward pass."""
+    L, C, B, T = int(cfg[0]), int(cfg[1]), int(cfg[6]), int(cfg[7])
+    out = np.zeros((L + 1, B * T, C), np.float32)
+    assert lib().oracle_residuals_f32(cfg, np.ascontiguousarray(params, np.float32),
+                                      np.ascontiguousarray(tokens, np.int32).reshape(-1), out) == 0
+    return out
 
 
 def adamw(params, grads, m, v, lr, b1, b2, eps, wd, t):

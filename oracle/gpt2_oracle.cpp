@@ -721,6 +721,19 @@ double oracle_fwdbwd_f32(const int32_t* cfg8, const float* params, const int32_t
                          const int32_t* tgt, float* grads, float* losses, float* logits) {
   return fwdbwd<float>(cfg8, params, tok, tgt, grads, losses, logits);
 }
+// The residual streams of a forward pass: out[(L+1), B*T, C]; stream 0 is the
+// encoder output, stream l the output of block l-1.
+int oracle_residuals_f32(const int32_t* cfg8, const float* params, const int32_t* tok, float* out) {
+  Shape s = shape_from(cfg8);
+  if (!shape_ok(s)) return -1;
+  Model<float> m(s);
+  m.forward(params, tok, nullptr);
+  Tensors<float> A(m.acts.data(), m.asz, NUM_ACTS);
+  const int64_t n = s.B * s.T * s.C;
+  std::memcpy(out, A[ENCODED], sizeof(float) * n);
+  for (int64_t l = 0; l < s.L; l++) std::memcpy(out + (l + 1) * n, A[RESIDUAL3] + l * n, sizeof(float) * n);
+  return 0;
+}
 double oracle_fwdbwd_f64(const int32_t* cfg8, const double* params, const int32_t* tok,
                          const int32_t* tgt, double* grads, double* losses, double* logits) {
   return fwdbwd<double>(cfg8, params, tok, tgt, grads, losses, logits);

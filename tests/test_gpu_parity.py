@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded
+inputs, through the C ABI.  Shapes are the method's configurations (tiny,
+char-level, GPT-2 124M / 350M) plus ragged ones that leave partial tiles in
+every dimension.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_lm_step_gpt_b300 import GPT2Error, GRADS, PARAMS, Model, synthetic
+from parity_util import TOL, assert_parity, cuda_ids, per_tensor_errors, rel_l2, run_steps
+
+pytestmark = pytest.mark.gpu
+
+TINY = (2, 64, 4, 256, 256, 32, 4, 32)          # L C NH V Vp maxT B T
+CHAR = (8, 128, 8, 1000, 1000, 64, 32, 64)
+RAGGED = (2, 64, 4, 250, 256, 64, 3, 50)        # M=150, V<Vp, T=50, hs=16
+RAGGED64 = (1, 128, 2, 1000, 1000, 96, 2, 80)   # hs=64, M=160, T=80
+GPT2_124M = (12, 768, 12, 50257, 50304, 1024)
+
+
+def test_init_matches_oracle_generator():
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    m = Model(L, C, NH, 250, Vp, maxT, B, T, precision="fp32", seed=4242)
+    got = m.copy_out(PARAMS).astype(np.float64)
+    want = oracle.init_params(oracle.cfg8(L, C, NH, 250, Vp, maxT, B, T), 4242)
+    np.testing.assert_allclose(got, want.astype(np.float32), rtol=1e-6, atol=1e-9)
+    tab = dict((n, (o, k)) for n, o, k in m.tensor_table())
+    o, k = tab["wte"]
+    assert np.all(got[o + 250 * C:o + k] == 0)
+
+
+def test_encoder_gather_bit_exact():
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    for prec in ("fp32", "bf16"):
+        m = Model(L, C, NH, V, Vp, maxT, B, T, precision=prec, seed=7)
+        p = synthetic.params(m.tensor_table(), L, C, V, 7, kind="perturbed")
+        m.copy_in(p)
+        tok, _ = synthetic.batch(8, B, T, V, "zipf")
+        m.forward(cuda_ids(tok), None)
+        ref = oracle.residuals_f32(oracle.cfg8(*TINY), p, tok)
+        assert np.array_equal(m.residual(0), ref[0])  # bit for bit
+        if prec == "fp32":
+            for l in range(1, L + 1):
+                assert rel_l2(m.residual(l), ref[l]) < 1e-5
+
+
+def test_forward_logits_fp32():
+    L, C, NH, V, Vp, maxT, B, T = RAGGED
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="fp32", seed=3)
+    p = synthetic.params(m.tensor_table(), L, C, V, 3, kind="perturbed")
+    m.copy_in(p)
+    tok, _ = synthetic.batch(4, B, T, V)
+    m.forward(cuda_ids(tok), None)
+    got = m.logits()
+    ref = oracle.fwdbwd(oracle.cfg8(*RAGGED), p, tok, None, want_grads=False, want_logits=True)["logits"]
+    assert rel_l2(got[:, :V], ref) < 1e-5
+    assert np.all(got[:, V:] == 0)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_config_tiny_one_step(prec):
+    res = run_steps(TINY, prec, 1, 1e-4, 0.9, 0.999, 1e-8, 0.0, "uniform", seed=11)
+    assert_parity(res, TINY, prec)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_config_char_ten_steps(prec):
+    res = run_steps(CHAR, prec, 10, 3e-4, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=12)
+    assert_parity(res, CHAR, prec)
+    # the loss curve goes down on a fixed-distribution stream
+    assert res["loss_gpu"][-1] < res["loss_gpu"][0]
+
+
+@pytest.mark.parametrize("shape", [RAGGED, RAGGED64])
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_ragged_shapes(shape, prec):
+    res = run_steps(shape, prec, 2, 1e-3, 0.9, 0.95, 1e-8, 0.1, "zipf", seed=13,
+                    check_grads_every_step=True)
+    assert_parity(res, shape, prec)
+
+
+def test_gpt2_124m_shapes_short_sequence_bf16():
+    """Every weight at its full 124M size (all tiles of the 50304-wide head),
+    on a batch the oracle can finish in seconds."""
+    shape = GPT2_124M + (1, 64)
+    res = run_steps(shape, "bf16", 1, 6e-4, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=14)
+    assert_parity(res, shape, "bf16")
+
+
+def _prefix_losses(shape, prec, rows, tprefix, dist, seed):
+    """Full-size step on the GPU; the per-position losses of the first
+    `tprefix` positions of `rows` rows depend only on those positions (causal
+    mask), so the oracle checks them on the truncated batch."""
+    L, C, NH, V, Vp, maxT, B, T = shape
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision=prec, seed=seed)
+    tok, tgt = synthetic.batch(seed + 1, B, T, V, dist)
+    p0 = m.copy_out(PARAMS)
+    loss = m.forward(cuda_ids(tok), cuda_ids(tgt))
+    got = m.losses().reshape(B, T)[:rows, :tprefix]
+    m.zero_grad()
+    m.backward()
+    g = m.copy_out(GRADS)
+    m.adamw_step(6e-4, 0.9, 0.999, 1e-8, 0.1, 1)
+    p1 = m.copy_out(PARAMS)
+    cfg = oracle.cfg8(L, C, NH, V, Vp, maxT, rows, tprefix)
+    ref = oracle.fwdbwd(cfg, p0, tok[:rows, :tprefix], tgt[:rows, :tprefix], want_grads=False)["losses"]
+    return loss, got.reshape(-1), ref, g, p0, p1, m
+
+
+@pytest.mark.parametrize("shape,rows,tp,dist", [
+    (GPT2_124M + (4, 1024), 4, 48, "uniform"),    # 124M, B=4 single step
+    (GPT2_124M + (16, 1024), 2, 32, "zipf"),      # 124M throughput shape
+    ((24, 1024, 16, 50257, 50304, 1024, 8, 1024), 2, 24, "uniform"),  # 350M
+])
+def test_full_size_sampled(shape, rows, tp, dist):
+    L, C, NH, V, Vp, maxT, B, T = shape
+    loss, got, ref, g, p0, p1, m = _prefix_losses(shape, "bf16", rows, tp, dist, seed=21)
+    np.testing.assert_allclose(got, ref, atol=TOL["bf16"]["loss"] * 3, rtol=0)
+    assert abs(float(np.mean(got)) - float(np.mean(ref))) <= TOL["bf16"]["loss"]
+    # at init the logits are ~N(0, C * 0.02^2) (unit-variance LN output times
+    # std-0.02 embedding rows), so E[loss] ~ ln V + C * 0.02^2 / 2
+    assert abs(loss - (math.log(V) + C * 0.02 ** 2 / 2)) < 0.05
+    assert np.all(np.isfinite(g))
+    # AdamW at t = 1: |m_hat / (sqrt(v_hat) + eps)| <= 1, so every parameter
+    # moves by at most lr beyond its decay
+    lr, wd = 6e-4, 0.1
+    assert np.max(np.abs(p1 - p0 * (1 - lr * wd))) <= lr * (1 + 1e-5) + 1e-7
+    tab = dict((n, (o, k)) for n, o, k in m.tensor_table())
+    o, k = tab["wte"]
+    assert np.all(p1[o + V * C:o + k] == 0)
+
+
+def test_errors_are_reported():
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=1)
+    with pytest.raises(GPT2Error) as e:
+        m.backward()
+    assert e.value.code == -4  # GPT2_ERR_STATE
+    with pytest.raises(GPT2Error) as e:
+        m.adamw_step(1e-3, 0.9, 0.999, 1e-8, 0.0, 0)
+    assert e.value.code == -1
+    tok, tgt = synthetic.batch(2, B, T, V)
+    bad = tok.copy()
+    bad[1, 3] = V + 5
+    with pytest.raises(GPT2Error) as e:
+        m.forward(cuda_ids(bad), cuda_ids(tgt))
+    assert e.value.code == -5  # GPT2_ERR_TOKEN
+    badt = tgt.copy()
+    badt[0, 0] = -1
+    with pytest.raises(GPT2Error) as e:
+        m.forward(cuda_ids(tok), cuda_ids(badt))
+    assert e.value.code == -5
+    # the model stays usable after a reported error
+    loss = m.forward(cuda_ids(tok), cuda_ids(tgt))
+    assert math.isfinite(loss)
+    with pytest.raises(GPT2Error) as e:
+        m.residual(L + 1)
+    assert e.value.code == -1
+
+
+def test_host_entry_point_matches_device_entry_point():
+    L, C, NH, V, Vp, maxT, B, T = RAGGED
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=5)
+    tok, tgt = synthetic.batch(6, B, T, V)
+    a = m.forward(cuda_ids(tok), cuda_ids(tgt))
+    ht = torch.from_numpy(tok).pin_memory()
+    hg = torch.from_numpy(tgt).pin_memory()
+    b = m.forward_host(ht, hg)
+    assert a == b
+
+
+def test_step_is_deterministic():
+    L, C, NH, V, Vp, maxT, B, T = CHAR
+    out = []
+    for _ in range(2):
+        m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=9)
+        tok, tgt = synthetic.batch(10, B, T, V, "zipf")
+        m.forward(cuda_ids(tok), cuda_ids(tgt))
+        m.zero_grad()
+        m.backward()
+        out.append(m.copy_out(GRADS))
+        m.close()
+    assert np.array_equal(out[0], out[1])
+
+
+def test_stream_is_honoured():
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    s = torch.cuda.Stream()
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=3, stream=s)
+    tok, tgt = synthetic.batch(2, B, T, V)
+    with torch.cuda.stream(s):
+        t1, t2 = cuda_ids(tok), cuda_ids(tgt)
+    loss = m.forward(t1, t2)
+    assert math.isfinite(loss)

@@ -1,1 +1,219 @@
-"""B300-native GPT-2 training step (binding placeholder; filled in with the C ABI)."""
+"""B300-native GPT-2 training step: Python binding of libgpt2.so.
+
+A thin ctypes layer over the C ABI in ``include/gpt2.h``: it marshals
+arguments and raises :class:`GPT2Error` on a non-zero status.  Every step of
+the computation runs in the library's CUDA kernels; there is no Python or CPU
+fallback -- if ``libgpt2.so`` is missing or fails to load, using the binding
+raises immediately.  PyTorch is used only for device memory of the token
+buffers and for streams.
+
+    from transformer_lm_step_gpt_b300 import Model
+    m = Model(L=12, C=768, NH=12, V=50257, Vp=50304, maxT=1024, B=16, T=1024,
+              precision="bf16", seed=1337)
+    loss = m.forward(tokens, targets)        # int32 CUDA tensors [B, T]
+    m.zero_grad(); m.backward(); m.adamw_step(6e-4, 0.9, 0.999, 1e-8, 0.1, t=1)
+"""
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = ["Model", "GPT2Error", "library_path", "load_library", "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgpt2.so")
+_lib = None
+
+PARAMS, GRADS, ADAM_M, ADAM_V = 0, 1, 2, 3
+FP32, BF16 = 0, 1
+
+ERRORS = {0: "OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_OOM", -3: "GPT2_ERR_CUDA", -4: "GPT2_ERR_STATE",
+          -5: "GPT2_ERR_TOKEN", -6: "GPT2_ERR_TIMEOUT", -7: "GPT2_ERR_NONFINITE"}
+
+
+class GPT2Error(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__("%s (%d): %s" % (ERRORS.get(code, "?"), code, msg))
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("max_seq_len", ctypes.c_int32), ("vocab_size", ctypes.c_int32),
+                ("padded_vocab_size", ctypes.c_int32), ("num_layers", ctypes.c_int32),
+                ("num_heads", ctypes.c_int32), ("channels", ctypes.c_int32),
+                ("batch_size", ctypes.c_int32), ("seq_len", ctypes.c_int32),
+                ("precision", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libgpt2.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError("libgpt2.so is not built; run `python -m transformer_lm_step_gpt_b300.build` "
+                           "(there is no CPU fallback)")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    sig = {
+        "gpt2_build": ([ctypes.POINTER(Config), ctypes.c_uint64, ctypes.POINTER(vp)], ctypes.c_int),
+        "gpt2_free": ([vp], None),
+        "gpt2_set_stream": ([vp, vp], ctypes.c_int),
+        "gpt2_forward": ([vp, vp, vp, vp], ctypes.c_int),
+        "gpt2_forward_host": ([vp, vp, vp, vp], ctypes.c_int),
+        "gpt2_zero_grad": ([vp], ctypes.c_int),
+        "gpt2_backward": ([vp], ctypes.c_int),
+        "gpt2_adamw_step": ([vp, f32, f32, f32, f32, f32, i32], ctypes.c_int),
+        "gpt2_synchronize": ([vp], ctypes.c_int),
+        "gpt2_get_config": ([vp, ctypes.POINTER(Config)], ctypes.c_int),
+        "gpt2_num_params": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
+        "gpt2_num_tensors": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
+        "gpt2_tensor_info": ([vp, i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(i64),
+                              ctypes.POINTER(i64)], ctypes.c_int),
+        "gpt2_copy_out": ([vp, i32, vp], ctypes.c_int),
+        "gpt2_copy_in": ([vp, i32, vp], ctypes.c_int),
+        "gpt2_copy_losses_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_logits_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_residual_out": ([vp, i32, vp], ctypes.c_int),
+        "gpt2_launch_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
+        "gpt2_last_error": ([vp], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _ptr(x):
+    """Address of a torch tensor, numpy array or raw int (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data
+    raise TypeError(type(x))
+
+
+class Model:
+    """One GPT-2 model with all of its device memory (see include/gpt2.h)."""
+
+    def __init__(self, L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=1337, stream=None):
+        self._lib = load_library()
+        self.cfg = Config(maxT, V, Vp, L, NH, C, B, T, BF16 if precision == "bf16" else FP32)
+        self.L, self.C, self.NH, self.V, self.Vp, self.maxT, self.B, self.T = L, C, NH, V, Vp, maxT, B, T
+        self.precision = precision
+        h = ctypes.c_void_p()
+        rc = self._lib.gpt2_build(ctypes.byref(self.cfg), ctypes.c_uint64(seed), ctypes.byref(h))
+        if rc != 0:
+            raise GPT2Error(rc, self._lib.gpt2_last_error(None).decode())
+        self._h = h
+        if stream is not None:
+            self.set_stream(stream)
+
+    # -- lifetime --------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.gpt2_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, rc):
+        if rc != 0:
+            raise GPT2Error(rc, self._lib.gpt2_last_error(self._h).decode())
+
+    # -- the step ----------------------------------------------------------
+    def set_stream(self, stream):
+        """stream: a torch.cuda.Stream, a raw cudaStream_t int, or None."""
+        s = getattr(stream, "cuda_stream", stream)
+        self._check(self._lib.gpt2_set_stream(self._h, s))
+
+    def forward(self, tokens, targets=None, sync=True):
+        """tokens/targets: int32 device tensors [B, T].  Returns the mean loss
+        (a float) when sync and targets are given, else None."""
+        loss = ctypes.c_float(float("nan"))
+        self._check(self._lib.gpt2_forward(self._h, _ptr(tokens), _ptr(targets),
+                                           ctypes.byref(loss) if sync else None))
+        return loss.value if (sync and targets is not None) else None
+
+    def forward_host(self, tokens, targets=None, sync=True):
+        """As forward, with host (ideally pinned) int32 buffers."""
+        loss = ctypes.c_float(float("nan"))
+        self._check(self._lib.gpt2_forward_host(self._h, _ptr(tokens), _ptr(targets),
+                                                ctypes.byref(loss) if sync else None))
+        return loss.value if (sync and targets is not None) else None
+
+    def zero_grad(self):
+        self._check(self._lib.gpt2_zero_grad(self._h))
+
+    def backward(self):
+        self._check(self._lib.gpt2_backward(self._h))
+
+    def adamw_step(self, lr, beta1, beta2, eps, weight_decay, t):
+        self._check(self._lib.gpt2_adamw_step(self._h, lr, beta1, beta2, eps, weight_decay, int(t)))
+
+    def synchronize(self):
+        self._check(self._lib.gpt2_synchronize(self._h))
+
+    # -- inspection -------------------------------------------------------
+    @property
+    def num_params(self) -> int:
+        n = ctypes.c_int64()
+        self._check(self._lib.gpt2_num_params(self._h, ctypes.byref(n)))
+        return n.value
+
+    def tensor_table(self):
+        n = ctypes.c_int32()
+        self._check(self._lib.gpt2_num_tensors(self._h, ctypes.byref(n)))
+        out = []
+        for i in range(n.value):
+            name, off, cnt = ctypes.c_char_p(), ctypes.c_int64(), ctypes.c_int64()
+            self._check(self._lib.gpt2_tensor_info(self._h, i, ctypes.byref(name), ctypes.byref(off),
+                                                   ctypes.byref(cnt)))
+            out.append((name.value.decode(), off.value, cnt.value))
+        return out
+
+    def copy_out(self, arena=PARAMS) -> np.ndarray:
+        a = np.empty(self.num_params, np.float32)
+        self._check(self._lib.gpt2_copy_out(self._h, arena, a.ctypes.data))
+        return a
+
+    def copy_in(self, arr, arena=PARAMS):
+        a = np.ascontiguousarray(arr, dtype=np.float32)
+        assert a.size == self.num_params
+        self._check(self._lib.gpt2_copy_in(self._h, arena, a.ctypes.data))
+
+    def losses(self) -> np.ndarray:
+        a = np.empty(self.B * self.T, np.float32)
+        self._check(self._lib.gpt2_copy_losses_out(self._h, a.ctypes.data))
+        return a
+
+    def logits(self) -> np.ndarray:
+        a = np.empty((self.B * self.T, self.Vp), np.float32)
+        self._check(self._lib.gpt2_copy_logits_out(self._h, a.ctypes.data))
+        return a
+
+    def residual(self, layer) -> np.ndarray:
+        """fp32 residual stream [B*T, C] entering block `layer` (0 = encoder output)."""
+        a = np.empty((self.B * self.T, self.C), np.float32)
+        self._check(self._lib.gpt2_copy_residual_out(self._h, int(layer), a.ctypes.data))
+        return a
+
+    @property
+    def launch_count(self) -> int:
+        n = ctypes.c_int64()
+        self._check(self._lib.gpt2_launch_count(self._h, ctypes.byref(n)))
+        return n.value

@@ -1,0 +1,642 @@
+// gpt2.cu -- the model object, its single device allocation, the step's
+// launch sequence, and the C ABI declared in include/gpt2.h.
+//
+// Memory (QbitAI, section "Manually implementing each layer's forward/
+// backward pass": everything is allocated once, as one 1-D block, and
+// pointers are carved out of it): one cudaMalloc at build time holds the
+// fp32 parameter / gradient / AdamW m / AdamW v arrays (same layout), the
+// bf16 copy of the weights, every saved activation of every layer and the
+// backward's scratch.  Nothing is allocated or freed afterwards.
+//
+// The step (InfoQ's layer list; GeekNews, "The Transformer core" for the
+// block order):
+//   forward   encoder -> L x [LN1 -> QKV -> attention -> proj + residual ->
+//             LN2 -> fc + GELU -> fcproj + residual] -> LN_f -> tied head ->
+//             softmax cross-entropy (dlogits computed in the same pass)
+//   backward  head dgrad/wgrad -> LN_f -> L x reversed block -> encoder
+//   update    one fused AdamW pass over the whole parameter array
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/gpt2.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+enum { WTE = 0, WPE, LN1W, LN1B, QKVW, QKVB, ATTPROJW, ATTPROJB, LN2W, LN2B, FCW, FCB,
+       FCPROJW, FCPROJB, LNFW, LNFB, NT };
+const char* kTensorNames[NT] = {"wte", "wpe", "ln1w", "ln1b", "qkvw", "qkvb", "attprojw",
+                                "attprojb", "ln2w", "ln2b", "fcw", "fcb", "fcprojw",
+                                "fcprojb", "lnfw", "lnfb"};
+
+thread_local std::string g_build_error = "no error";
+
+struct Bump {
+  char* base;
+  size_t off = 0;
+  explicit Bump(char* b) : base(b) {}
+  template <typename T>
+  T* take(size_t n) {
+    off = (off + 255) & ~(size_t)255;
+    T* p = reinterpret_cast<T*>(base + off);
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+}  // namespace
+
+struct gpt2_model {
+  gpt2_config cfg;
+  int L, C, NH, V, Vp, maxT, B, T, M;
+  bool bf;      // bf16 mode
+  size_t act;   // bytes per stored activation element (2 or 4)
+  int device = 0, num_sms = 148;
+  cudaStream_t stream = nullptr;
+  int64_t n_params = 0;
+  int64_t off[NT + 1];
+  char* block = nullptr;
+  size_t block_bytes = 0;
+  // fp32 arrays sharing the parameter layout
+  float *params, *grads, *adam_m, *adam_v;
+  bf16* wb = nullptr;  // bf16 copy of the parameters (bf16 mode)
+  // inputs of the last forward
+  int32_t *tok, *tgt;
+  // activations (act = bf16 or fp32 per mode; residual stream fp32)
+  std::vector<float*> res;  // L+1 residual streams [M,C]; res[0] = encoder output
+  std::vector<float*> mid;  // L after-attention residuals [M,C]
+  char *ln1, *qkv, *atty, *ln2, *fch, *fcg, *lnf, *logits;
+  float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lse, *lnf_mean, *lnf_rstd;
+  float *losses, *loss;
+  // backward scratch
+  float* dres;
+  char* dres_act;  // bf16 copy of dres (bf16 mode); == dres in fp32 mode
+  float* dln;
+  char *dbig, *datty;
+  float *dsum, *ln_partial, *cs_partial, *splitk;
+  int64_t splitk_floats;
+  uint32_t* enc_sorted;
+  float* enc_partial;
+  int* err;
+  int64_t launches = 0;
+  bool have_fwd = false, fwd_targets = false;
+  std::string last_error = "no error";
+
+  int64_t tensor(int t) const { return off[t]; }
+  float* P(int t) const { return params + off[t]; }
+  float* G(int t) const { return grads + off[t]; }
+  const void* W(int t) const {  // matmul operand copy of a weight
+    return bf ? static_cast<const void*>(wb + off[t]) : static_cast<const void*>(params + off[t]);
+  }
+  template <typename X = char>
+  X* A(char* base, int l, int64_t per) const {  // per-layer slice of an activation array
+    return reinterpret_cast<X*>(base + (size_t)l * per * act);
+  }
+};
+
+namespace {
+
+int fail(gpt2_model* m, int code, const std::string& msg) {
+  if (m) m->last_error = msg;
+  else g_build_error = msg;
+  return code;
+}
+
+int cuda_fail(gpt2_model* m, cudaError_t e, const char* where) {
+  return fail(m, GPT2_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+LaunchCtx ctx(gpt2_model* m) {
+  LaunchCtx c;
+  c.stream = m->stream;
+  c.err = m->err;
+  c.launches = &m->launches;
+  c.num_sms = m->num_sms;
+  c.host_fail = 0;
+  return c;
+}
+
+int after_launches(gpt2_model* m, LaunchCtx& c, const char* where) {
+  if (c.host_fail) return fail(m, GPT2_ERR_CUDA, std::string(where) + ": a kernel could not be enqueued");
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(m, e, where);
+  return GPT2_OK;
+}
+
+// Read and clear the device error word (synchronises the stream first).
+int check_device(gpt2_model* m, const char* where) {
+  cudaError_t e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, where);
+  int w = 0;
+  e = cudaMemcpy(&w, m->err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(m, e, where);
+  if (w) {
+    cudaMemset(m->err, 0, sizeof(int));
+    if (w & DEVERR_TIMEOUT) return fail(m, GPT2_ERR_TIMEOUT, std::string(where) + ": a bounded device wait expired");
+    if (w & DEVERR_TOKEN) return fail(m, GPT2_ERR_TOKEN, std::string(where) + ": token or target id outside [0, V)");
+  }
+  return GPT2_OK;
+}
+
+void param_sizes(const gpt2_model* m, int64_t n[NT]) {
+  const int64_t L = m->L, C = m->C;
+  n[WTE] = (int64_t)m->Vp * C; n[WPE] = (int64_t)m->maxT * C;
+  n[LN1W] = L * C; n[LN1B] = L * C; n[QKVW] = L * 3 * C * C; n[QKVB] = L * 3 * C;
+  n[ATTPROJW] = L * C * C; n[ATTPROJB] = L * C; n[LN2W] = L * C; n[LN2B] = L * C;
+  n[FCW] = L * 4 * C * C; n[FCB] = L * 4 * C; n[FCPROJW] = L * C * 4 * C; n[FCPROJB] = L * C;
+  n[LNFW] = C; n[LNFB] = C;
+}
+
+// Carve every buffer out of one block (base == nullptr: measure only).
+size_t layout(gpt2_model* m, char* base) {
+  Bump b(base);
+  const int64_t M = m->M, C = m->C, L = m->L, n = m->n_params;
+  const size_t a = m->act;
+  m->params = b.take<float>(n);
+  m->grads = b.take<float>(n);
+  m->adam_m = b.take<float>(n);
+  m->adam_v = b.take<float>(n);
+  m->wb = m->bf ? b.take<bf16>(n) : nullptr;
+  m->tok = b.take<int32_t>(M);
+  m->tgt = b.take<int32_t>(M);
+  m->res.assign(L + 1, nullptr);
+  m->mid.assign(L, nullptr);
+  for (int l = 0; l <= L; l++) m->res[l] = b.take<float>(M * C);
+  for (int l = 0; l < L; l++) m->mid[l] = b.take<float>(M * C);
+  m->ln1 = b.take<char>(L * M * C * a);
+  m->qkv = b.take<char>(L * M * 3 * C * a);
+  m->atty = b.take<char>(L * M * C * a);
+  m->ln2 = b.take<char>(L * M * C * a);
+  m->fch = b.take<char>(L * M * 4 * C * a);
+  m->fcg = b.take<char>(L * M * 4 * C * a);
+  m->lnf = b.take<char>(M * C * a);
+  m->logits = b.take<char>(M * (int64_t)m->Vp * a);
+  m->ln1_mean = b.take<float>(L * M);
+  m->ln1_rstd = b.take<float>(L * M);
+  m->ln2_mean = b.take<float>(L * M);
+  m->ln2_rstd = b.take<float>(L * M);
+  m->lse = b.take<float>(L * (int64_t)m->B * m->NH * m->T);
+  m->lnf_mean = b.take<float>(M);
+  m->lnf_rstd = b.take<float>(M);
+  m->losses = b.take<float>(M);
+  m->loss = b.take<float>(1);
+  m->dres = b.take<float>(M * C);
+  m->dres_act = m->bf ? b.take<char>(M * C * a) : reinterpret_cast<char*>(m->dres);
+  m->dln = b.take<float>(M * C);
+  m->dbig = b.take<char>(M * 4 * C * a);
+  m->datty = b.take<char>(M * C * a);
+  m->dsum = b.take<float>((int64_t)m->B * m->NH * m->T);
+  m->ln_partial = b.take<float>(ln_partial_floats(m->M, m->C));
+  m->cs_partial = b.take<float>(colsum_partial_floats(m->M, 4 * m->C));
+  m->splitk_floats = m->bf ? 16 * C * C : 0;
+  m->splitk = b.take<float>(m->splitk_floats);
+  m->enc_sorted = b.take<uint32_t>(M);
+  m->enc_partial = b.take<float>(M * C);
+  m->err = b.take<int>(1);
+  return b.off + 256;
+}
+
+GemmArgs gemm(int M, int N, int K, const void* A, int64_t lda, bool ak, const void* B,
+              int64_t ldb, bool bk, int epi, void* out, int64_t ldo, bool out_f32) {
+  GemmArgs g;
+  std::memset(&g, 0, sizeof(g));
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.a_kmajor = ak;
+  g.B = B; g.ldb = ldb; g.b_kmajor = bk;
+  g.epi = epi; g.out = out; g.ldo = ldo; g.out_f32 = out_f32;
+  return g;
+}
+
+void run_gemm(gpt2_model* m, LaunchCtx& c, GemmArgs g) {
+  if (m->bf) {
+    g.splitk_scratch = m->splitk;
+    g.splitk_scratch_floats = m->splitk_floats;
+    launch_gemm_bf16(c, g);
+  } else {
+    launch_gemm_f32(c, g);
+  }
+}
+
+template <typename ActT>
+void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
+  const int M = m->M, C = m->C, L = m->L, B = m->B, T = m->T, NH = m->NH;
+  const bool f32 = !m->bf;
+  launch_encoder_fwd(c, m->res[0], m->tok, m->P(WTE), m->P(WPE), B, T, C, m->V);
+  const int64_t WS = sizeof(ActT) == 2 ? 2 : 4;
+  auto w = [&](int t, int64_t o) {
+    return static_cast<const void*>(static_cast<const char*>(m->W(t)) + o * WS);
+  };
+  for (int l = 0; l < L; l++) {
+    ActT* ln1 = m->A<ActT>(m->ln1, l, (int64_t)M * C);
+    ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
+    ActT* atty = m->A<ActT>(m->atty, l, (int64_t)M * C);
+    ActT* ln2 = m->A<ActT>(m->ln2, l, (int64_t)M * C);
+    ActT* fch = m->A<ActT>(m->fch, l, (int64_t)M * 4 * C);
+    ActT* fcg = m->A<ActT>(m->fcg, l, (int64_t)M * 4 * C);
+    float* lse = m->lse + (int64_t)l * B * NH * T;
+    launch_layernorm_fwd<ActT>(c, ln1, m->ln1_mean + (int64_t)l * M, m->ln1_rstd + (int64_t)l * M,
+                               m->res[l], m->P(LN1W) + l * C, m->P(LN1B) + l * C, M, C);
+    GemmArgs g = gemm(M, 3 * C, C, ln1, C, true, w(QKVW, (int64_t)l * 3 * C * C), C, true,
+                      EPI_STORE, qkv, 3 * C, f32);
+    g.bias = m->P(QKVB) + (int64_t)l * 3 * C;
+    run_gemm(m, c, g);
+    if (f32) launch_attention_fwd_simt<ActT>(c, atty, lse, qkv, B, T, C, NH);
+    else launch_attention_fwd_bf16(c, reinterpret_cast<bf16*>(atty), lse, reinterpret_cast<const bf16*>(qkv), B, T, C, NH);
+    g = gemm(M, C, C, atty, C, true, w(ATTPROJW, (int64_t)l * C * C), C, true, EPI_RESIDUAL,
+             m->mid[l], C, true);
+    g.bias = m->P(ATTPROJB) + (int64_t)l * C;
+    g.aux = m->res[l];
+    run_gemm(m, c, g);
+    launch_layernorm_fwd<ActT>(c, ln2, m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
+                               m->mid[l], m->P(LN2W) + l * C, m->P(LN2B) + l * C, M, C);
+    g = gemm(M, 4 * C, C, ln2, C, true, w(FCW, (int64_t)l * 4 * C * C), C, true, EPI_BIAS_GELU,
+             fch, 4 * C, f32);
+    g.bias = m->P(FCB) + (int64_t)l * 4 * C;
+    g.out2 = fcg;
+    run_gemm(m, c, g);
+    g = gemm(M, C, 4 * C, fcg, 4 * C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C, true,
+             EPI_RESIDUAL, m->res[l + 1], C, true);
+    g.bias = m->P(FCPROJB) + (int64_t)l * C;
+    g.aux = m->mid[l];
+    run_gemm(m, c, g);
+  }
+  ActT* lnf = reinterpret_cast<ActT*>(m->lnf);
+  launch_layernorm_fwd<ActT>(c, lnf, m->lnf_mean, m->lnf_rstd, m->res[L], m->P(LNFW), m->P(LNFB), M, C);
+  ActT* logits = reinterpret_cast<ActT*>(m->logits);
+  run_gemm(m, c, gemm(M, m->Vp, C, lnf, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32));
+  launch_crossentropy<ActT>(c, logits, m->losses, with_targets ? m->tgt : nullptr, M, m->V, m->Vp,
+                            1.f / (float)M, with_targets);
+  if (with_targets) launch_mean(c, m->loss, m->losses, M);
+}
+
+template <typename ActT>
+void backward_layers(gpt2_model* m, LaunchCtx& c) {
+  const int M = m->M, C = m->C, L = m->L, B = m->B, T = m->T, NH = m->NH;
+  const int Vp = m->Vp;
+  const int64_t WS = sizeof(ActT) == 2 ? 2 : 4;
+  auto w = [&](int t, int64_t o) {
+    return static_cast<const void*>(static_cast<const char*>(m->W(t)) + o * WS);
+  };
+  const bool f32 = !m->bf;
+  ActT* dlogits = reinterpret_cast<ActT*>(m->logits);
+  ActT* lnf = reinterpret_cast<ActT*>(m->lnf);
+  ActT* dres_act = reinterpret_cast<ActT*>(m->dres_act);
+  ActT* dres_act_out = f32 ? nullptr : dres_act;  // fp32 mode: dres itself is the operand
+  ActT* dbig = reinterpret_cast<ActT*>(m->dbig);
+  ActT* datty = reinterpret_cast<ActT*>(m->datty);
+  // tied head: logits = lnf wte^T
+  run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, m->dln, C, true));
+  run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true));
+  launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB), m->dln, m->res[L],
+                             m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
+  for (int l = L - 1; l >= 0; l--) {
+    ActT* ln1 = m->A<ActT>(m->ln1, l, (int64_t)M * C);
+    ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
+    ActT* atty = m->A<ActT>(m->atty, l, (int64_t)M * C);
+    ActT* ln2 = m->A<ActT>(m->ln2, l, (int64_t)M * C);
+    ActT* fch = m->A<ActT>(m->fch, l, (int64_t)M * 4 * C);
+    ActT* fcg = m->A<ActT>(m->fcg, l, (int64_t)M * 4 * C);
+    float* lse = m->lse + (int64_t)l * B * NH * T;
+    // fcproj: res[l+1] = mid + fcg Wfcproj^T + b
+    GemmArgs g = gemm(M, 4 * C, C, dres_act, C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C,
+                      false, EPI_GELU_BWD, dbig, 4 * C, f32);
+    g.aux = fch;
+    run_gemm(m, c, g);
+    run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
+                        m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true));
+    launch_colsum<float>(c, m->G(FCPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    // fc: fch = ln2 Wfc^T + b
+    run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
+                        EPI_STORE, m->dln, C, true));
+    run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,
+                        m->G(FCW) + (int64_t)l * 4 * C * C, C, true));
+    launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
+    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
+                               m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
+                               m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+    // attproj: mid = res[l] + atty Wproj^T + b
+    run_gemm(m, c, gemm(M, C, C, dres_act, C, true, w(ATTPROJW, (int64_t)l * C * C), C, false,
+                        EPI_STORE, datty, C, f32));
+    run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
+                        m->G(ATTPROJW) + (int64_t)l * C * C, C, true));
+    launch_colsum<float>(c, m->G(ATTPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    // attention
+    if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
+    else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
+                                   reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
+                                   lse, m->dsum, B, T, C, NH);
+    // qkv: qkv = ln1 Wqkv^T + b
+    run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
+                        EPI_STORE, m->dln, C, true));
+    run_gemm(m, c, gemm(3 * C, C, M, dbig, 3 * C, false, ln1, C, false, EPI_ACCUM,
+                        m->G(QKVW) + (int64_t)l * 3 * C * C, C, true));
+    launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
+                               m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
+                               m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+  }
+  launch_encoder_bwd(c, m->G(WTE), m->G(WPE), m->dres, m->tok, B, T, C, Vp, m->enc_sorted,
+                     m->enc_partial);
+}
+
+int forward_common(gpt2_model* m, bool with_targets, float* mean_loss) {
+  LaunchCtx c = ctx(m);
+  if (m->bf) forward_layers<bf16>(m, c, with_targets);
+  else forward_layers<float>(m, c, with_targets);
+  int rc = after_launches(m, c, "gpt2_forward");
+  if (rc) return rc;
+  m->have_fwd = true;
+  m->fwd_targets = with_targets;
+  if (mean_loss) {
+    rc = check_device(m, "gpt2_forward");
+    if (rc) return rc;
+    if (with_targets) {
+      cudaError_t e = cudaMemcpy(mean_loss, m->loss, sizeof(float), cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_forward");
+      if (!std::isfinite(*mean_loss)) return fail(m, GPT2_ERR_NONFINITE, "gpt2_forward: loss is not finite");
+    } else {
+      *mean_loss = NAN;
+    }
+  }
+  return GPT2_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+int gpt2_build(const gpt2_config* cfg, uint64_t seed, gpt2_model** out) {
+  if (!out) return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: out is NULL");
+  *out = nullptr;
+  if (!cfg) return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: cfg is NULL");
+  const gpt2_config& k = *cfg;
+  const int hs = k.num_heads > 0 ? k.channels / k.num_heads : 0;
+  if (k.num_layers < 1 || k.num_heads < 1 || k.channels < 8 || k.channels % k.num_heads != 0 ||
+      k.channels % 8 != 0 || !(hs == 16 || hs == 32 || hs == 64 || hs == 128))
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need L>=1, C%NH==0, C%8==0, head size in {16,32,64,128}");
+  if (k.vocab_size < 1 || k.padded_vocab_size < k.vocab_size || k.padded_vocab_size % 8 != 0)
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need 1 <= V <= Vp and Vp % 8 == 0");
+  if (k.seq_len < 1 || k.seq_len > k.max_seq_len || k.max_seq_len > 4096 || k.batch_size < 1 ||
+      (int64_t)k.batch_size * k.seq_len > 32768)
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need 1 <= T <= maxT <= 4096, B >= 1, B*T <= 32768");
+  if ((uint64_t)k.padded_vocab_size * (uint64_t)k.batch_size * (uint64_t)k.seq_len >= (1ull << 32))
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: Vp * B * T must be below 2^32");
+  if (k.precision != GPT2_FP32 && k.precision != GPT2_BF16)
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: unknown precision");
+  if (k.precision == GPT2_BF16 && !gemm_bf16_init())
+    return fail(nullptr, GPT2_ERR_CUDA, "gpt2_build: the driver's tensor-map encoder is unavailable");
+
+  gpt2_model* m = new gpt2_model();
+  m->cfg = k;
+  m->L = k.num_layers; m->C = k.channels; m->NH = k.num_heads; m->V = k.vocab_size;
+  m->Vp = k.padded_vocab_size; m->maxT = k.max_seq_len; m->B = k.batch_size; m->T = k.seq_len;
+  m->M = m->B * m->T;
+  m->bf = k.precision == GPT2_BF16;
+  m->act = m->bf ? 2 : 4;
+  cudaError_t e = cudaGetDevice(&m->device);
+  if (e != cudaSuccess) { delete m; return cuda_fail(nullptr, e, "gpt2_build: cudaGetDevice"); }
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, m->device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, m->device);
+  cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+  if (major != 10 || minor != 3) {
+    delete m;
+    return fail(nullptr, GPT2_ERR_CUDA, "gpt2_build: this library is built for sm_103 (B300) only");
+  }
+  int64_t n[NT];
+  param_sizes(m, n);
+  m->off[0] = 0;
+  for (int t = 0; t < NT; t++) m->off[t + 1] = m->off[t] + n[t];
+  m->n_params = m->off[NT];
+  m->block_bytes = layout(m, nullptr);
+  e = cudaMalloc(&m->block, m->block_bytes);
+  if (e != cudaSuccess) {
+    delete m;
+    cudaGetLastError();
+    return fail(nullptr, GPT2_ERR_OOM, "gpt2_build: cudaMalloc of the model block failed");
+  }
+  layout(m, m->block);
+  cudaMemset(m->grads, 0, sizeof(float) * m->n_params);
+  cudaMemset(m->adam_m, 0, sizeof(float) * m->n_params);
+  cudaMemset(m->adam_v, 0, sizeof(float) * m->n_params);
+  cudaMemset(m->err, 0, sizeof(int));
+  LaunchCtx c = ctx(m);
+  InitSpec s;
+  for (int t = 0; t <= NT; t++) s.off[t] = m->off[t];
+  s.L = m->L; s.C = m->C; s.V = m->V; s.seed = seed;
+  launch_init_params(c, m->params, s);
+  if (m->bf) launch_f32_to_bf16(c, m->wb, m->params, m->n_params);
+  int rc = after_launches(m, c, "gpt2_build");
+  if (rc == GPT2_OK) rc = check_device(m, "gpt2_build");
+  if (rc != GPT2_OK) {
+    g_build_error = m->last_error;
+    cudaFree(m->block);
+    delete m;
+    return rc;
+  }
+  *out = m;
+  return GPT2_OK;
+}
+
+void gpt2_free(gpt2_model* m) {
+  if (!m) return;
+  cudaSetDevice(m->device);
+  cudaStreamSynchronize(m->stream);
+  cudaFree(m->block);
+  delete m;
+}
+
+int gpt2_set_stream(gpt2_model* m, void* s) {
+  if (!m) return GPT2_ERR_ARG;
+  m->stream = static_cast<cudaStream_t>(s);
+  return GPT2_OK;
+}
+
+int gpt2_forward(gpt2_model* m, const int32_t* tokens, const int32_t* targets, float* mean_loss) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!tokens) return fail(m, GPT2_ERR_ARG, "gpt2_forward: tokens is NULL");
+  cudaSetDevice(m->device);
+  cudaError_t e = cudaMemcpyAsync(m->tok, tokens, sizeof(int32_t) * m->M, cudaMemcpyDeviceToDevice, m->stream);
+  if (e == cudaSuccess && targets)
+    e = cudaMemcpyAsync(m->tgt, targets, sizeof(int32_t) * m->M, cudaMemcpyDeviceToDevice, m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_forward: copying ids");
+  return forward_common(m, targets != nullptr, mean_loss);
+}
+
+int gpt2_forward_host(gpt2_model* m, const int32_t* tokens, const int32_t* targets, float* mean_loss) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!tokens) return fail(m, GPT2_ERR_ARG, "gpt2_forward_host: tokens is NULL");
+  cudaSetDevice(m->device);
+  cudaError_t e = cudaMemcpyAsync(m->tok, tokens, sizeof(int32_t) * m->M, cudaMemcpyHostToDevice, m->stream);
+  if (e == cudaSuccess && targets)
+    e = cudaMemcpyAsync(m->tgt, targets, sizeof(int32_t) * m->M, cudaMemcpyHostToDevice, m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_forward_host: copying ids");
+  return forward_common(m, targets != nullptr, mean_loss);
+}
+
+int gpt2_zero_grad(gpt2_model* m) {
+  if (!m) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  cudaError_t e = cudaMemsetAsync(m->grads, 0, sizeof(float) * m->n_params, m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_zero_grad");
+  return GPT2_OK;
+}
+
+int gpt2_backward(gpt2_model* m) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!m->have_fwd || !m->fwd_targets)
+    return fail(m, GPT2_ERR_STATE, "gpt2_backward: needs a preceding forward with targets");
+  cudaSetDevice(m->device);
+  LaunchCtx c = ctx(m);
+  if (m->bf) backward_layers<bf16>(m, c);
+  else backward_layers<float>(m, c);
+  m->have_fwd = false;  // the dlogits buffer has been consumed
+  return after_launches(m, c, "gpt2_backward");
+}
+
+int gpt2_adamw_step(gpt2_model* m, float lr, float b1, float b2, float eps, float wd, int32_t t) {
+  if (!m) return GPT2_ERR_ARG;
+  if (t < 1) return fail(m, GPT2_ERR_ARG, "gpt2_adamw_step: t must be >= 1");
+  if (!std::isfinite(lr) || !std::isfinite(b1) || !std::isfinite(b2) || !std::isfinite(eps) ||
+      !std::isfinite(wd))
+    return fail(m, GPT2_ERR_ARG, "gpt2_adamw_step: non-finite hyper-parameter");
+  cudaSetDevice(m->device);
+  LaunchCtx c = ctx(m);
+  const float c1 = 1.f - powf(b1, (float)t), c2 = 1.f - powf(b2, (float)t);
+  launch_adamw(c, m->params, m->grads, m->adam_m, m->adam_v, m->bf ? m->wb : nullptr, m->n_params,
+               lr, b1, b2, eps, wd, c1, c2);
+  return after_launches(m, c, "gpt2_adamw_step");
+}
+
+int gpt2_synchronize(gpt2_model* m) {
+  if (!m) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  return check_device(m, "gpt2_synchronize");
+}
+
+int gpt2_get_config(const gpt2_model* m, gpt2_config* out) {
+  if (!m || !out) return GPT2_ERR_ARG;
+  *out = m->cfg;
+  return GPT2_OK;
+}
+
+int gpt2_num_params(const gpt2_model* m, int64_t* n) {
+  if (!m || !n) return GPT2_ERR_ARG;
+  *n = m->n_params;
+  return GPT2_OK;
+}
+
+int gpt2_num_tensors(const gpt2_model* m, int32_t* n) {
+  if (!m || !n) return GPT2_ERR_ARG;
+  *n = NT;
+  return GPT2_OK;
+}
+
+int gpt2_tensor_info(const gpt2_model* m, int32_t idx, const char** name, int64_t* offset,
+                     int64_t* numel) {
+  if (!m || idx < 0 || idx >= NT) return GPT2_ERR_ARG;
+  if (name) *name = kTensorNames[idx];
+  if (offset) *offset = m->off[idx];
+  if (numel) *numel = m->off[idx + 1] - m->off[idx];
+  return GPT2_OK;
+}
+
+static float* arena_ptr(gpt2_model* m, int32_t a) {
+  switch (a) {
+    case GPT2_PARAMS: return m->params;
+    case GPT2_GRADS: return m->grads;
+    case GPT2_ADAM_M: return m->adam_m;
+    case GPT2_ADAM_V: return m->adam_v;
+  }
+  return nullptr;
+}
+
+int gpt2_copy_out(gpt2_model* m, int32_t arena, float* dst) {
+  if (!m) return GPT2_ERR_ARG;
+  float* src = arena_ptr(m, arena);
+  if (!src || !dst) return fail(m, GPT2_ERR_ARG, "gpt2_copy_out: bad arena or NULL destination");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_copy_out");
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpy(dst, src, sizeof(float) * m->n_params, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_out");
+}
+
+int gpt2_copy_in(gpt2_model* m, int32_t arena, const float* srch) {
+  if (!m) return GPT2_ERR_ARG;
+  float* dst = arena_ptr(m, arena);
+  if (!dst || !srch) return fail(m, GPT2_ERR_ARG, "gpt2_copy_in: bad arena or NULL source");
+  cudaSetDevice(m->device);
+  cudaError_t e = cudaStreamSynchronize(m->stream);
+  if (e == cudaSuccess) e = cudaMemcpy(dst, srch, sizeof(float) * m->n_params, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_copy_in");
+  if (arena == GPT2_PARAMS && m->bf) {
+    LaunchCtx c = ctx(m);
+    launch_f32_to_bf16(c, m->wb, m->params, m->n_params);
+    int rc = after_launches(m, c, "gpt2_copy_in");
+    if (rc) return rc;
+  }
+  return check_device(m, "gpt2_copy_in");
+}
+
+int gpt2_copy_losses_out(gpt2_model* m, float* dst) {
+  if (!m || !dst) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_copy_losses_out");
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpy(dst, m->losses, sizeof(float) * m->M, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_losses_out");
+}
+
+int gpt2_copy_logits_out(gpt2_model* m, float* dst) {
+  if (!m || !dst) return GPT2_ERR_ARG;
+  if (!m->have_fwd || m->fwd_targets)
+    return fail(m, GPT2_ERR_STATE, "gpt2_copy_logits_out: needs a preceding forward without targets");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_copy_logits_out");
+  if (rc) return rc;
+  const size_t n = (size_t)m->M * m->Vp;
+  if (!m->bf) {
+    cudaError_t e = cudaMemcpy(dst, m->logits, sizeof(float) * n, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_logits_out");
+  }
+  std::vector<uint16_t> tmp(n);
+  cudaError_t e = cudaMemcpy(tmp.data(), m->logits, 2 * n, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_copy_logits_out");
+  for (size_t i = 0; i < n; i++) {
+    uint32_t u = (uint32_t)tmp[i] << 16;
+    std::memcpy(&dst[i], &u, 4);
+  }
+  return GPT2_OK;
+}
+
+int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* dst) {
+  if (!m || !dst) return GPT2_ERR_ARG;
+  if (layer < 0 || layer > m->L) return fail(m, GPT2_ERR_ARG, "gpt2_copy_residual_out: layer outside [0, L]");
+  if (!m->have_fwd) return fail(m, GPT2_ERR_STATE, "gpt2_copy_residual_out: no forward to read");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_copy_residual_out");
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpy(dst, m->res[layer], sizeof(float) * (size_t)m->M * m->C, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_residual_out");
+}
+
+int gpt2_launch_count(const gpt2_model* m, int64_t* n) {
+  if (!m || !n) return GPT2_ERR_ARG;
+  *n = m->launches;
+  return GPT2_OK;
+}
+
+const char* gpt2_last_error(const gpt2_model* m) {
+  return m ? m->last_error.c_str() : g_build_error.c_str();
+}
+
+}  // extern "C"

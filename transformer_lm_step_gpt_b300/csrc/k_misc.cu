@@ -1,0 +1,581 @@
+// k_misc.cu -- the bandwidth-bound kernels of the step.
+//
+//  - parameter initialisation (Philox4x32-10 + Box-Muller, on the device)
+//  - encoder forward / backward (token + position embedding; InfoQ's layer
+//    list "encoder")
+//  - LayerNorm forward / backward (QbitAI's worked example; GeekNews,
+//    "Implementing the neural-network layers")
+//  - bias-gradient column sums, fused softmax + cross-entropy (InfoQ's
+//    layer list), mean loss, AdamW (InfoQ: "Adam lr 1e-4")
+//
+// All of them are HBM-bound: each reads its inputs once with 16-byte vector
+// loads, reduces rows with warp shuffles and writes its outputs once.  Every
+// reduction runs in a fixed order, so results repeat bit for bit.
+#include <cstdio>
+
+#include "common.cuh"
+#include "kernels.h"
+
+#define LAUNCH_CHECK(c) \
+  do { (*(c).launches)++; } while (0)
+
+static inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+// ============================================================ init
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; r++) {
+    if (r > 0) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+    const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+    const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+    c[0] = n0; c[1] = lo1; c[2] = n2; c[3] = lo0;
+  }
+}
+
+__global__ void init_params_kernel(float* p, InitSpec s) {
+  const int64_t total = s.off[16];
+  const double sd = 0.02, sdr = 0.02 / sqrt(2.0 * (double)(s.L > 0 ? s.L : 1));
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
+       e += (int64_t)gridDim.x * blockDim.x) {
+    int t = 0;
+    while (t < 15 && e >= s.off[t + 1]) t++;
+    // tensor ids: 0 wte 1 wpe 2 ln1w 3 ln1b 4 qkvw 5 qkvb 6 attprojw 7 attprojb
+    //             8 ln2w 9 ln2b 10 fcw 11 fcb 12 fcprojw 13 fcprojb 14 lnfw 15 lnfb
+    double scale = 0.0;
+    bool draw = false;
+    if (t == 0) { draw = (e - s.off[0]) / s.C < s.V; scale = sd; }
+    else if (t == 1 || t == 4 || t == 10) { draw = true; scale = sd; }
+    else if (t == 6 || t == 12) { draw = true; scale = sdr; }
+    float v = (t == 2 || t == 8 || t == 14) ? 1.f : 0.f;
+    if (draw) {
+      const uint64_t pair = (uint64_t)e >> 1;
+      uint32_t c[4] = {(uint32_t)pair, (uint32_t)(pair >> 32), 0u, 0u};
+      philox4x32_10(c, (uint32_t)s.seed, (uint32_t)(s.seed >> 32));
+      const double u1 = ((double)c[0] + 1.0) / 4294967296.0;
+      const double u2 = (double)c[1] / 4294967296.0;
+      const double r = sqrt(-2.0 * log(u1));
+      const double th = 6.283185307179586476925 * u2;
+      v = (float)(scale * ((e & 1) ? r * sin(th) : r * cos(th)));
+    }
+    p[e] = v;
+  }
+}
+
+void launch_init_params(LaunchCtx& c, float* params, const InitSpec& s) {
+  init_params_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(params, s);
+  LAUNCH_CHECK(c);
+}
+
+__global__ void f32_to_bf16_kernel(bf16* out, const float* in, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = __float2bfloat16_rn(in[i]);
+}
+void launch_f32_to_bf16(LaunchCtx& c, bf16* out, const float* in, int64_t n) {
+  f32_to_bf16_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(out, in, n);
+  LAUNCH_CHECK(c);
+}
+
+// ============================================================ encoder
+__global__ void encoder_fwd_kernel(float* out, const int32_t* tok, const float* wte,
+                                   const float* wpe, int B, int T, int C, int V, int* err) {
+  const int C4 = C / 4;
+  const int64_t n = (int64_t)B * T * C4;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = idx / C4;
+    const int c4 = (int)(idx % C4);
+    const int t = (int)(i % T);
+    int id = tok[i];
+    if (id < 0 || id >= V) {
+      if (c4 == 0) record_error(err, DEVERR_TOKEN);
+      id = 0;
+    }
+    const float4 a = reinterpret_cast<const float4*>(wte + (int64_t)id * C)[c4];
+    const float4 b = reinterpret_cast<const float4*>(wpe + (int64_t)t * C)[c4];
+    reinterpret_cast<float4*>(out + i * C)[c4] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+  }
+}
+
+void launch_encoder_fwd(LaunchCtx& c, float* out, const int32_t* tok, const float* wte,
+                        const float* wpe, int B, int T, int C, int V) {
+  const int64_t n = (int64_t)B * T * (C / 4);
+  int grid = (int)std::min<int64_t>(cdiv(n, 256), (int64_t)c.num_sms * 16);
+  encoder_fwd_kernel<<<grid, 256, 0, c.stream>>>(out, tok, wte, wpe, B, T, C, V, c.err);
+  LAUNCH_CHECK(c);
+}
+
+// dwpe[t, c] += sum_b dout[b, t, c], b in order.
+__global__ void encoder_bwd_wpe_kernel(float* dwpe, const float* dout, int B, int T, int C) {
+  const int64_t n = (int64_t)T * C;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / C), ch = (int)(idx % C);
+    float s = 0.f;
+    for (int b = 0; b < B; b++) s += dout[((int64_t)b * T + t) * C + ch];
+    dwpe[idx] += s;
+  }
+}
+
+// Sort the keys tok*M + position (one block, bitonic sort in shared memory);
+// equal tokens end up adjacent, in position order.
+__global__ void encoder_sort_kernel(uint32_t* sorted, const int32_t* tok, int M, int Vp, int P) {
+  extern __shared__ uint32_t keys[];
+  for (int i = threadIdx.x; i < P; i += blockDim.x) {
+    uint32_t k = 0xFFFFFFFFu;
+    if (i < M) {
+      int id = tok[i];
+      id = id < 0 ? 0 : (id >= Vp ? Vp - 1 : id);
+      k = (uint32_t)id * (uint32_t)M + (uint32_t)i;
+    }
+    keys[i] = k;
+  }
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = (lo & size) == 0;
+        const uint32_t a = keys[lo], b = keys[hi];
+        if ((a > b) == up) { keys[lo] = b; keys[hi] = a; }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < M; i += blockDim.x) sorted[i] = keys[i];
+}
+
+__device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_t key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+#define ENC_PIECE 64
+// One block per sorted index; blocks at a piece start (segment start, or 64
+// rows into a segment) sum their piece's rows in order.  Single-piece
+// segments add straight into dwte; longer ones leave a partial per piece.
+__global__ void encoder_bwd_piece_kernel(float* dwte, float* partial, const float* dout,
+                                         const uint32_t* sorted, int M, int C) {
+  const int i = blockIdx.x;
+  const uint32_t key = sorted[i];
+  const uint32_t id = key / (uint32_t)M;
+  const int seg0 = lower_bound_u32(sorted, M, id * (uint32_t)M);
+  if ((i - seg0) % ENC_PIECE != 0) return;
+  const int seg1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
+  const int end = min(seg1, i + ENC_PIECE);
+  const int C4 = C / 4;
+  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = i; j < end; j++) {
+      const uint32_t pos = sorted[j] % (uint32_t)M;
+      const float4 v = reinterpret_cast<const float4*>(dout + (int64_t)pos * C)[c4];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    if (seg1 - seg0 <= ENC_PIECE) {
+      float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
+      float4 o = *d;
+      o.x += s.x; o.y += s.y; o.z += s.z; o.w += s.w;
+      *d = o;
+    } else {
+      reinterpret_cast<float4*>(partial + (int64_t)i * C)[c4] = s;
+    }
+  }
+}
+
+__global__ void encoder_bwd_combine_kernel(float* dwte, const float* partial,
+                                           const uint32_t* sorted, int M, int C) {
+  const int i = blockIdx.x;
+  const uint32_t id = sorted[i] / (uint32_t)M;
+  if (i > 0 && sorted[i - 1] / (uint32_t)M == id) return;  // not a segment start
+  const int seg1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
+  if (seg1 - i <= ENC_PIECE) return;
+  const int C4 = C / 4;
+  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = i; j < seg1; j += ENC_PIECE) {
+      const float4 v = reinterpret_cast<const float4*>(partial + (int64_t)j * C)[c4];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
+    float4 o = *d;
+    o.x += s.x; o.y += s.y; o.z += s.z; o.w += s.w;
+    *d = o;
+  }
+}
+
+void launch_encoder_bwd(LaunchCtx& c, float* dwte, float* dwpe, const float* dout,
+                        const int32_t* tok, int B, int T, int C, int Vp, uint32_t* sorted,
+                        float* partial) {
+  const int M = B * T;
+  {
+    const int64_t n = (int64_t)T * C;
+    int grid = (int)std::min<int64_t>(cdiv(n, 256), (int64_t)c.num_sms * 8);
+    encoder_bwd_wpe_kernel<<<grid, 256, 0, c.stream>>>(dwpe, dout, B, T, C);
+    LAUNCH_CHECK(c);
+  }
+  int P = 1;
+  while (P < M) P <<= 1;
+  const size_t smem = (size_t)P * sizeof(uint32_t);
+  cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  encoder_sort_kernel<<<1, 1024, smem, c.stream>>>(sorted, tok, M, Vp, P);
+  LAUNCH_CHECK(c);
+  const int threads = std::min(1024, std::max(32, ((C / 4) + 31) / 32 * 32));
+  encoder_bwd_piece_kernel<<<M, threads, 0, c.stream>>>(dwte, partial, dout, sorted, M, C);
+  LAUNCH_CHECK(c);
+  encoder_bwd_combine_kernel<<<M, threads, 0, c.stream>>>(dwte, partial, sorted, M, C);
+  LAUNCH_CHECK(c);
+}
+
+// ============================================================ LayerNorm
+template <typename OutT>
+__device__ __forceinline__ void store4(OutT* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<bf16>(bf16* p, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+template <typename T>
+__device__ __forceinline__ float4 load4(const T* p);
+template <>
+__device__ __forceinline__ float4 load4<float>(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 load4<bf16>(const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  const float2 a = __bfloat1622float2(lo), b = __bfloat1622float2(hi);
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// One warp per row: mean, then variance about the mean (two passes; the row
+// stays in L1), then y = (x - mean) * rstd * w + b.
+template <typename OutT>
+__global__ void layernorm_fwd_kernel(OutT* out, float* mean, float* rstd, const float* inp,
+                                     const float* w, const float* b, int N, int C) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (row >= N) return;
+  const float* x = inp + (int64_t)row * C;
+  float s = 0.f;
+  for (int c = lane * 4; c < C; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(x + c);
+    s += (v.x + v.y) + (v.z + v.w);
+  }
+  const float m = warp_sum(s) / (float)C;
+  float q = 0.f;
+  for (int c = lane * 4; c < C; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(x + c);
+    const float a = v.x - m, bb = v.y - m, cc = v.z - m, d = v.w - m;
+    q += (a * a + bb * bb) + (cc * cc + d * d);
+  }
+  const float var = warp_sum(q) / (float)C;
+  const float r = 1.f / sqrtf(var + 1e-5f);
+  OutT* y = out + (int64_t)row * C;
+  for (int c = lane * 4; c < C; c += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(x + c);
+    const float4 ww = *reinterpret_cast<const float4*>(w + c);
+    const float4 bb = *reinterpret_cast<const float4*>(b + c);
+    store4<OutT>(y + c, (v.x - m) * r * ww.x + bb.x, (v.y - m) * r * ww.y + bb.y,
+                 (v.z - m) * r * ww.z + bb.z, (v.w - m) * r * ww.w + bb.w);
+  }
+  if (lane == 0) { mean[row] = m; rstd[row] = r; }
+}
+
+template <typename OutT>
+void launch_layernorm_fwd(LaunchCtx& c, OutT* out, float* mean, float* rstd, const float* inp,
+                          const float* w, const float* b, int N, int C) {
+  layernorm_fwd_kernel<OutT><<<cdiv(N, 8), 256, 0, c.stream>>>(out, mean, rstd, inp, w, b, N, C);
+  LAUNCH_CHECK(c);
+}
+template void launch_layernorm_fwd<float>(LaunchCtx&, float*, float*, float*, const float*,
+                                          const float*, const float*, int, int);
+template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, const float*,
+                                         const float*, const float*, int, int);
+
+#define LNB_WARPS 8
+#define LNB_ROWS 64  // rows per block (8 per warp)
+
+int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS) * 2 * C; }
+
+// One warp per row; gamma/beta gradient partials per warp in shared memory,
+// combined over the block's warps in warp order into one partial per block.
+template <typename ActT>
+__global__ void layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
+                                     const float* inp, const float* w, const float* mean,
+                                     const float* rstd, int N, int C, int accumulate) {
+  extern __shared__ float sm[];  // [LNB_WARPS][2][C]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float* sdw = sm + (int64_t)warp * 2 * C;
+  float* sdb = sdw + C;
+  for (int c = lane; c < C; c += 32) { sdw[c] = 0.f; sdb[c] = 0.f; }
+  __syncwarp();
+  const int row0 = blockIdx.x * LNB_ROWS + warp * (LNB_ROWS / LNB_WARPS);
+  for (int rr = 0; rr < LNB_ROWS / LNB_WARPS; rr++) {
+    const int row = row0 + rr;
+    if (row >= N) break;
+    const float* x = inp + (int64_t)row * C;
+    const float* g = dy + (int64_t)row * C;
+    const float m = mean[row], r = rstd[row];
+    float s1 = 0.f, s2 = 0.f;
+    for (int c = lane * 4; c < C; c += 128) {
+      const float4 xv = *reinterpret_cast<const float4*>(x + c);
+      const float4 gv = *reinterpret_cast<const float4*>(g + c);
+      const float4 wv = *reinterpret_cast<const float4*>(w + c);
+      const float h0 = gv.x * wv.x, h1 = gv.y * wv.y, h2 = gv.z * wv.z, h3 = gv.w * wv.w;
+      s1 += (h0 + h1) + (h2 + h3);
+      s2 += (h0 * (xv.x - m) * r + h1 * (xv.y - m) * r) + (h2 * (xv.z - m) * r + h3 * (xv.w - m) * r);
+    }
+    const float mg = warp_sum(s1) / (float)C;
+    const float mgx = warp_sum(s2) / (float)C;
+    float* dr = dres + (int64_t)row * C;
+    for (int c = lane * 4; c < C; c += 128) {
+      const float4 xv = *reinterpret_cast<const float4*>(x + c);
+      const float4 gv = *reinterpret_cast<const float4*>(g + c);
+      const float4 wv = *reinterpret_cast<const float4*>(w + c);
+      const float x0 = (xv.x - m) * r, x1 = (xv.y - m) * r, x2 = (xv.z - m) * r, x3 = (xv.w - m) * r;
+      float4 d;
+      d.x = r * (gv.x * wv.x - mg - x0 * mgx);
+      d.y = r * (gv.y * wv.y - mg - x1 * mgx);
+      d.z = r * (gv.z * wv.z - mg - x2 * mgx);
+      d.w = r * (gv.w * wv.w - mg - x3 * mgx);
+      if (accumulate) {
+        const float4 o = *reinterpret_cast<const float4*>(dr + c);
+        d.x += o.x; d.y += o.y; d.z += o.z; d.w += o.w;
+      }
+      *reinterpret_cast<float4*>(dr + c) = d;
+      if (dres_act) store4<ActT>(dres_act + (int64_t)row * C + c, d.x, d.y, d.z, d.w);
+      sdw[c] += gv.x * x0; sdw[c + 1] += gv.y * x1; sdw[c + 2] += gv.z * x2; sdw[c + 3] += gv.w * x3;
+      sdb[c] += gv.x; sdb[c + 1] += gv.y; sdb[c + 2] += gv.z; sdb[c + 3] += gv.w;
+    }
+  }
+  __syncthreads();
+  float* out = partial + (int64_t)blockIdx.x * 2 * C;
+  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+    float s = 0.f;
+    for (int wv = 0; wv < LNB_WARPS; wv++) s += sm[(int64_t)wv * 2 * C + c];
+    out[c] = s;
+  }
+}
+
+// Sum nb partial rows of width W in row order and add into dst[0:W]
+// (dst may be split: first half into d0, second half into d1).
+__global__ void reduce_partials_kernel(float* d0, float* d1, const float* partial, int nb, int W,
+                                       int half) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= W) return;
+  float s = 0.f;
+  for (int b = 0; b < nb; b++) s += partial[(int64_t)b * W + c];
+  if (c < half) d0[c] += s; else d1[c - half] += s;
+}
+
+template <typename ActT>
+void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
+                          const float* dy, const float* inp, const float* w, const float* mean,
+                          const float* rstd, int N, int C, bool accumulate, float* partial) {
+  const int nb = cdiv(N, LNB_ROWS);
+  const size_t smem = (size_t)LNB_WARPS * 2 * C * sizeof(float);
+  cudaFuncSetAttribute(layernorm_bwd_kernel<ActT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  layernorm_bwd_kernel<ActT><<<nb, LNB_WARPS * 32, smem, c.stream>>>(
+      dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
+  LAUNCH_CHECK(c);
+  reduce_partials_kernel<<<cdiv(2 * C, 256), 256, 0, c.stream>>>(dw, db, partial, nb, 2 * C, C);
+  LAUNCH_CHECK(c);
+}
+template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, const float*,
+                                          const float*, const float*, const float*, const float*,
+                                          int, int, bool, float*);
+template void launch_layernorm_bwd<bf16>(LaunchCtx&, float*, bf16*, float*, float*, const float*,
+                                         const float*, const float*, const float*, const float*,
+                                         int, int, bool, float*);
+
+// ============================================================ column sums
+#define CS_CHUNKS 64
+int64_t colsum_partial_floats(int M, int N) { return (int64_t)CS_CHUNKS * N; }
+
+// grid (ceil(N/256), CS_CHUNKS); 64 threads x 4 columns; rows of one chunk in order.
+template <typename T>
+__global__ void colsum_partial_kernel(float* partial, const T* x, int M, int N, int64_t ld) {
+  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int rows = (M + CS_CHUNKS - 1) / CS_CHUNKS;
+  const int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
+  if (col >= N) return;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = r0; r < r1; r++) {
+    const float4 v = load4<T>(x + (int64_t)r * ld + col);
+    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  }
+  *reinterpret_cast<float4*>(partial + (int64_t)blockIdx.y * N + col) = s;
+}
+
+template <typename T>
+void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
+  dim3 grid(cdiv(N, 256), CS_CHUNKS);
+  colsum_partial_kernel<T><<<grid, 64, 0, c.stream>>>(partial, x, M, N, ld);
+  LAUNCH_CHECK(c);
+  reduce_partials_kernel<<<cdiv(N, 256), 256, 0, c.stream>>>(db, db, partial, CS_CHUNKS, N, N);
+  LAUNCH_CHECK(c);
+}
+template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);
+template void launch_colsum<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t, float*);
+
+// ============================================================ softmax + cross-entropy
+__device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) return;
+  s = s * expf(m - mm) + s2 * expf(m2 - mm);
+  m = mm;
+}
+
+// One block per row.  Pass 1: per-thread online (max, sum exp) over the V
+// real columns, then a block reduction.  Pass 2 (the row is now in L2):
+// dlogits = (exp(l - lse) - onehot) * dscale, pad columns 0, written in place.
+template <typename T>
+__global__ void crossentropy_kernel(T* logits, float* losses, const int32_t* targets, int V,
+                                    int Vp, float dscale, int write_dlogits, int* err) {
+  __shared__ float sm_m[32], sm_s[32];
+  const int64_t row = blockIdx.x;
+  T* l = logits + row * Vp;
+  float m = -INFINITY, s = 0.f;
+  for (int j = threadIdx.x * 4; j < V; j += blockDim.x * 4) {
+    const float4 v = load4<T>(l + j);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      if (j + q < V) {
+        const float x = vv[q];
+        if (x > m) { s = s * expf(m - x) + 1.f; m = x; }
+        else s += expf(x - m);
+      }
+    }
+  }
+  // warp then block reduction of (m, s)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_combine(m, s, m2, s2);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (lane == 0) { sm_m[warp] = m; sm_s[warp] = s; }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < nw ? sm_m[lane] : -INFINITY;
+    s = lane < nw ? sm_s[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_combine(m, s, m2, s2);
+    }
+    if (lane == 0) { sm_m[0] = m; sm_s[0] = s; }
+  }
+  __syncthreads();
+  const float lse = sm_m[0] + logf(sm_s[0]);
+  int tg = targets ? targets[row] : -1;
+  if (targets && (tg < 0 || tg >= V)) {
+    if (threadIdx.x == 0) record_error(err, DEVERR_TOKEN);
+    tg = 0;
+  }
+  __syncthreads();  // every thread has read its target logit source before overwriting
+  float lt = 0.f;
+  if (targets) lt = to_f(l[tg]);
+  __syncthreads();
+  if (threadIdx.x == 0 && targets) losses[row] = lse - lt;
+  if (!write_dlogits) return;
+  for (int j = threadIdx.x * 4; j < Vp; j += blockDim.x * 4) {
+    const float4 v = load4<T>(l + j);
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    float o[4];
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const int jj = j + q;
+      o[q] = jj < V ? (expf(vv[q] - lse) - (jj == tg ? 1.f : 0.f)) * dscale : 0.f;
+    }
+    store4<T>(l + j, o[0], o[1], o[2], o[3]);
+  }
+}
+
+template <typename T>
+void launch_crossentropy(LaunchCtx& c, T* logits, float* losses, const int32_t* targets, int M,
+                         int V, int Vp, float dscale, bool dlogits) {
+  crossentropy_kernel<T><<<M, 512, 0, c.stream>>>(logits, losses, targets, V, Vp, dscale,
+                                                  dlogits ? 1 : 0, c.err);
+  LAUNCH_CHECK(c);
+}
+template void launch_crossentropy<float>(LaunchCtx&, float*, float*, const int32_t*, int, int, int,
+                                         float, bool);
+template void launch_crossentropy<bf16>(LaunchCtx&, bf16*, float*, const int32_t*, int, int, int,
+                                        float, bool);
+
+__global__ void mean_kernel(float* out, const float* x, int M) {
+  __shared__ float sm[32];
+  float s = 0.f;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) s += x[i];
+  s = warp_sum(s);
+  if ((threadIdx.x & 31) == 0) sm[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    s = threadIdx.x < (blockDim.x >> 5) ? sm[threadIdx.x] : 0.f;
+    s = warp_sum(s);
+    if (threadIdx.x == 0) out[0] = s / (float)M;
+  }
+}
+void launch_mean(LaunchCtx& c, float* out, const float* losses, int M) {
+  mean_kernel<<<1, 1024, 0, c.stream>>>(out, losses, M);
+  LAUNCH_CHECK(c);
+}
+
+// ============================================================ AdamW
+__global__ void adamw_kernel(float* p, const float* g, float* m, float* v, bf16* shadow, int64_t n4,
+                             float lr, float b1, float b2, float eps, float wd, float c1,
+                             float c2) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 pp = reinterpret_cast<float4*>(p)[i];
+    const float4 gg = reinterpret_cast<const float4*>(g)[i];
+    float4 mm = reinterpret_cast<float4*>(m)[i];
+    float4 vv = reinterpret_cast<float4*>(v)[i];
+    float* P = &pp.x;
+    const float* G = &gg.x;
+    float* Mm = &mm.x;
+    float* Vv = &vv.x;
+#pragma unroll
+    for (int q = 0; q < 4; q++) {
+      const float mi = b1 * Mm[q] + (1.f - b1) * G[q];
+      const float vi = b2 * Vv[q] + (1.f - b2) * G[q] * G[q];
+      Mm[q] = mi;
+      Vv[q] = vi;
+      const float mh = mi / c1, vh = vi / c2;
+      P[q] = P[q] - lr * (mh / (sqrtf(vh) + eps) + wd * P[q]);
+    }
+    reinterpret_cast<float4*>(p)[i] = pp;
+    reinterpret_cast<float4*>(m)[i] = mm;
+    reinterpret_cast<float4*>(v)[i] = vv;
+    if (shadow) store4<bf16>(shadow + i * 4, pp.x, pp.y, pp.z, pp.w);
+  }
+}
+
+void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf16* shadow,
+                  int64_t n, float lr, float b1, float b2, float eps, float wd, float c1,
+                  float c2) {
+  const int64_t n4 = n / 4;  // the parameter count is a multiple of 4 (C % 8 == 0)
+  int grid = (int)std::min<int64_t>(cdiv(n4, 256), (int64_t)c.num_sms * 16);
+  adamw_kernel<<<grid, 256, 0, c.stream>>>(p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
+  LAUNCH_CHECK(c);
+}

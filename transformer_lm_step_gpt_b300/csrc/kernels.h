@@ -1,0 +1,119 @@
+// kernels.h -- host-side launchers of every kernel in libgpt2.so.
+//
+// Each launcher takes raw device pointers, sizes and a LaunchCtx (stream,
+// device error word, launch counter) and enqueues its kernel(s); none
+// allocates memory or synchronises.  Scratch buffers are passed in by the
+// caller (the model owns them).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+typedef __nv_bfloat16 bf16;
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  int* err;           // device error word (DEVERR_* bits)
+  int64_t* launches;  // host-side count of kernel launches
+  int num_sms;
+  int host_fail;      // set by a launcher that could not enqueue its kernel
+};
+
+// ---------------------------------------------------------------- init
+struct InitSpec {
+  int64_t off[17];  // start of each of the 16 parameter tensors, off[16] = total
+  int L, C, V;
+  uint64_t seed;
+};
+void launch_init_params(LaunchCtx& c, float* params, const InitSpec& s);
+void launch_f32_to_bf16(LaunchCtx& c, bf16* out, const float* in, int64_t n);
+
+// ---------------------------------------------------------------- encoder
+// out[b,t,:] = wte[tok[b,t],:] + wpe[t,:]; ids outside [0,V) set DEVERR_TOKEN
+// and read row 0 instead.
+void launch_encoder_fwd(LaunchCtx& c, float* out, const int32_t* tok, const float* wte,
+                        const float* wpe, int B, int T, int C, int V);
+// dwte[tok[i]] += dout[i], dwpe[t] += sum_b dout[b,t]; deterministic.
+// scratch: keys (uint32 [M]), piece partials (float [M*C]).
+void launch_encoder_bwd(LaunchCtx& c, float* dwte, float* dwpe, const float* dout,
+                        const int32_t* tok, int B, int T, int C, int Vp, uint32_t* sorted,
+                        float* partial);
+
+// ---------------------------------------------------------------- LayerNorm
+template <typename OutT>
+void launch_layernorm_fwd(LaunchCtx& c, OutT* out, float* mean, float* rstd, const float* inp,
+                          const float* w, const float* b, int N, int C);
+// dres (+)= dx; dres_act = dres in ActT (if non-null); dw, db += column
+// sums via partials (float [ln_partial_floats(N, C)]).
+template <typename ActT>
+void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
+                          const float* dy, const float* inp, const float* w, const float* mean,
+                          const float* rstd, int N, int C, bool accumulate, float* partial);
+int64_t ln_partial_floats(int N, int C);
+
+// ---------------------------------------------------------------- column sums
+// db[j] += sum_i x[i*ld + j], i < M, j < N.  partial: float [colsum_partial_floats]
+template <typename T>
+void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial);
+int64_t colsum_partial_floats(int M, int N);
+
+// ---------------------------------------------------------------- softmax + CE
+// Per row i < M of logits [M, Vp]: loss_i = logsumexp(l[0:V]) - l[target];
+// if dlogits: logits row <- (softmax - onehot(target)) * dscale (pad cols 0).
+template <typename T>
+void launch_crossentropy(LaunchCtx& c, T* logits, float* losses, const int32_t* targets, int M,
+                         int V, int Vp, float dscale, bool dlogits);
+// out[0] = mean of losses[0:M] (fixed-order reduction)
+void launch_mean(LaunchCtx& c, float* out, const float* losses, int M);
+
+// ---------------------------------------------------------------- AdamW
+void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf16* shadow,
+                  int64_t n, float lr, float b1, float b2, float eps, float wd, float c1,
+                  float c2);
+
+// ---------------------------------------------------------------- GEMM
+// out[m, n] = sum_k A(m,k) * B(n,k) with
+//   A(m,k) = A[m*lda + k] (a_kmajor) or A[k*lda + m] (M-major)
+//   B(n,k) = B[n*ldb + k] (b_kmajor) or B[k*ldb + n] (N-major)
+enum GemmEpi {
+  EPI_STORE = 0,     // out = acc (+ bias)                          out: act or f32
+  EPI_BIAS_GELU,     // out = acc + bias (pre-activation), out2 = gelu(out)  both act
+  EPI_RESIDUAL,      // out(f32) = aux(f32) + acc + bias
+  EPI_GELU_BWD,      // out(act) = acc * gelu'(aux(act))
+  EPI_ACCUM,         // out(f32) += acc
+};
+struct GemmArgs {
+  int M, N, K;
+  const void* A; int64_t lda; bool a_kmajor;
+  const void* B; int64_t ldb; bool b_kmajor;
+  int epi;
+  void* out; int64_t ldo; bool out_f32;
+  const float* bias;  // [N] or null
+  void* out2;         // EPI_BIAS_GELU
+  const void* aux;    // EPI_RESIDUAL (f32, ldo) / EPI_GELU_BWD (act, ldo)
+  float* splitk_scratch;  // EPI_ACCUM with split-K (tensor-core path)
+  int64_t splitk_scratch_floats;
+};
+// fp32 operands, SIMT FFMA (no TF32)
+void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
+// bf16 operands on tcgen05 tensor cores, fp32 accumulation in TMEM
+void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g);
+bool gemm_bf16_init();  // resolves the driver's tensor-map encoder; false on failure
+
+// ---------------------------------------------------------------- attention
+// qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T] (natural-log logsumexp of the
+// scaled, masked scores of each query row).
+template <typename T>
+void launch_attention_fwd_simt(LaunchCtx& c, T* y, float* lse, const T* qkv, int B, int T_,
+                               int C, int NH);
+template <typename T>
+void launch_attention_bwd_simt(LaunchCtx& c, T* dqkv, const T* dy, const T* y, const T* qkv,
+                               const float* lse, float* dsum, int B, int T_, int C, int NH,
+                               float* scratch);
+int64_t attention_simt_scratch_floats(int B, int T_, int NH);
+void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T_,
+                               int C, int NH);
+void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+                               const bf16* qkv, const float* lse, float* dsum, int B, int T_,
+                               int C, int NH);
