@@ -192,6 +192,28 @@ GPT2_API int gpt2_copy_logits_out(gpt2_model* m, float* host_dst);
  * Errors: GPT2_ERR_ARG (layer outside [0, L]), GPT2_ERR_STATE (no forward). */
 GPT2_API int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* host_dst);
 
+/* Mean loss of the last forward with targets, copied to host memory.
+ * Synchronises; reports device-side errors like gpt2_synchronize and
+ * GPT2_ERR_NONFINITE for a NaN/Inf loss. */
+GPT2_API int gpt2_read_loss(gpt2_model* m, float* host_loss);
+
+/* Kernel timing with CUDA events recorded on the model's stream around
+ * every launch of the selected kernel classes (bit i of class_mask selects
+ * class i; 0 turns timing off).  Each class also accumulates the
+ * algorithmic work of its launches: FLOPs of the matmuls / attention
+ * contractions (2*M*N*K; causal attention counts only the unmasked half) or
+ * the minimum bytes a memory-bound kernel must move (each input read once,
+ * each output written once).  gpt2_profile_read synchronises and returns,
+ * for class cls: its name, the unit of `work` ("flop" or "byte"), the
+ * number of launches, their summed duration in milliseconds and their
+ * summed work, since the last reset.  Names and units are static strings. */
+GPT2_API int gpt2_profile_num_classes(int32_t* n);
+GPT2_API int gpt2_profile_enable(gpt2_model* m, uint32_t class_mask);
+GPT2_API int gpt2_profile_reset(gpt2_model* m);
+GPT2_API int gpt2_profile_read(gpt2_model* m, int32_t cls, const char** name,
+                               const char** unit, int64_t* launches,
+                               double* total_ms, double* work);
+
 /* Number of kernel launches the library made since the model was built
  * (a plain host-side counter). */
 GPT2_API int gpt2_launch_count(const gpt2_model* m, int64_t* n);

@@ -79,6 +79,13 @@ def load_library():
         "gpt2_copy_losses_out": ([vp, vp], ctypes.c_int),
         "gpt2_copy_logits_out": ([vp, vp], ctypes.c_int),
         "gpt2_copy_residual_out": ([vp, i32, vp], ctypes.c_int),
+        "gpt2_read_loss": ([vp, ctypes.POINTER(f32)], ctypes.c_int),
+        "gpt2_profile_num_classes": ([ctypes.POINTER(i32)], ctypes.c_int),
+        "gpt2_profile_enable": ([vp, ctypes.c_uint32], ctypes.c_int),
+        "gpt2_profile_reset": ([vp], ctypes.c_int),
+        "gpt2_profile_read": ([vp, i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_char_p),
+                               ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_double)], ctypes.c_int),
         "gpt2_launch_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_last_error": ([vp], ctypes.c_char_p),
     }
@@ -211,6 +218,42 @@ class Model:
         a = np.empty((self.B * self.T, self.C), np.float32)
         self._check(self._lib.gpt2_copy_residual_out(self._h, int(layer), a.ctypes.data))
         return a
+
+    def read_loss(self) -> float:
+        """Mean loss of the last forward with targets (synchronises)."""
+        x = ctypes.c_float()
+        self._check(self._lib.gpt2_read_loss(self._h, ctypes.byref(x)))
+        return x.value
+
+    def profile_enable(self, classes="all"):
+        """Time the named kernel classes with CUDA events (None/[] = off)."""
+        n = ctypes.c_int32()
+        self._check(self._lib.gpt2_profile_num_classes(ctypes.byref(n)))
+        mask = 0
+        if classes == "all":
+            mask = (1 << n.value) - 1
+        elif classes:
+            names = [r["name"] for r in self.profile_read()]
+            for c in classes:
+                mask |= 1 << names.index(c)
+        self._check(self._lib.gpt2_profile_enable(self._h, mask))
+
+    def profile_reset(self):
+        self._check(self._lib.gpt2_profile_reset(self._h))
+
+    def profile_read(self):
+        """[{name, unit, launches, ms, work}] per kernel class (synchronises)."""
+        n = ctypes.c_int32()
+        self._check(self._lib.gpt2_profile_num_classes(ctypes.byref(n)))
+        out = []
+        for i in range(n.value):
+            name, unit = ctypes.c_char_p(), ctypes.c_char_p()
+            cnt, ms, work = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+            self._check(self._lib.gpt2_profile_read(self._h, i, ctypes.byref(name), ctypes.byref(unit),
+                                                    ctypes.byref(cnt), ctypes.byref(ms), ctypes.byref(work)))
+            out.append(dict(name=name.value.decode(), unit=unit.value.decode(), launches=cnt.value,
+                            ms=ms.value, work=work.value))
+        return out
 
     @property
     def launch_count(self) -> int:

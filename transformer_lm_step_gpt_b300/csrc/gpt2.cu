@@ -38,6 +38,24 @@ const char* kTensorNames[NT] = {"wte", "wpe", "ln1w", "ln1b", "qkvw", "qkvb", "a
 
 thread_local std::string g_build_error = "no error";
 
+// Kernel classes timed by gpt2_profile_*; work unit per class.
+enum ProfClass { PC_GEMM_FWD = 0, PC_GEMM_DGRAD, PC_GEMM_WGRAD, PC_ATTN_FWD, PC_ATTN_BWD,
+                 PC_LN_FWD, PC_LN_BWD, PC_CE, PC_BIAS_GRAD, PC_ENC_FWD, PC_ENC_BWD, PC_ADAMW,
+                 PC_ZERO_GRAD, PC_N };
+const char* kProfNames[PC_N] = {"gemm_fwd", "gemm_dgrad", "gemm_wgrad", "attention_fwd",
+                                "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy",
+                                "bias_grad", "encoder_fwd", "encoder_bwd", "adamw", "zero_grad"};
+const char* kProfUnits[PC_N] = {"flop", "flop", "flop", "flop", "flop", "byte", "byte",
+                                "byte", "byte", "byte", "byte", "byte", "byte"};
+
+struct ProfState {
+  uint32_t mask = 0;
+  int64_t launches[PC_N] = {};
+  double work[PC_N] = {}, ms[PC_N] = {};
+  std::vector<std::pair<int, std::pair<cudaEvent_t, cudaEvent_t>>> pending;
+  std::vector<cudaEvent_t> pool;
+};
+
 struct Bump {
   char* base;
   size_t off = 0;
@@ -86,6 +104,7 @@ struct gpt2_model {
   float* enc_partial;
   int* err;
   int64_t launches = 0;
+  ProfState prof;
   bool have_fwd = false, fwd_targets = false;
   std::string last_error = "no error";
 
@@ -102,6 +121,39 @@ struct gpt2_model {
 };
 
 namespace {
+
+cudaEvent_t take_event(gpt2_model* m) {
+  if (!m->prof.pool.empty()) {
+    cudaEvent_t e = m->prof.pool.back();
+    m->prof.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Records an event pair around the launches made in its scope when the
+// class is selected; accounts the launch and its algorithmic work.
+struct ProfScope {
+  gpt2_model* m = nullptr;
+  int cls;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  ProfScope(gpt2_model* mm, int c, double work) : cls(c) {
+    if (!(mm->prof.mask & (1u << c))) return;
+    m = mm;
+    e0 = take_event(m);
+    e1 = take_event(m);
+    cudaEventRecord(e0, m->stream);
+    m->prof.launches[c]++;
+    m->prof.work[c] += work;
+  }
+  ~ProfScope() {
+    if (!m) return;
+    cudaEventRecord(e1, m->stream);
+    m->prof.pending.push_back({cls, {e0, e1}});
+  }
+};
 
 int fail(gpt2_model* m, int code, const std::string& msg) {
   if (m) m->last_error = msg;
@@ -215,6 +267,8 @@ GemmArgs gemm(int M, int N, int K, const void* A, int64_t lda, bool ak, const vo
 }
 
 void run_gemm(gpt2_model* m, LaunchCtx& c, GemmArgs g) {
+  const int cls = g.a_kmajor ? (g.b_kmajor ? PC_GEMM_FWD : PC_GEMM_DGRAD) : PC_GEMM_WGRAD;
+  ProfScope ps(m, cls, 2.0 * g.M * (double)g.N * g.K);
   if (m->bf) {
     g.splitk_scratch = m->splitk;
     g.splitk_scratch_floats = m->splitk_floats;
@@ -228,7 +282,12 @@ template <typename ActT>
 void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
   const int M = m->M, C = m->C, L = m->L, B = m->B, T = m->T, NH = m->NH;
   const bool f32 = !m->bf;
-  launch_encoder_fwd(c, m->res[0], m->tok, m->P(WTE), m->P(WPE), B, T, C, m->V);
+  const double a = (double)sizeof(ActT);
+  const double attn_flop = 4.0 * B * NH * (double)(C / NH) * (T * (T + 1.0) / 2.0);
+  {
+    ProfScope ps(m, PC_ENC_FWD, 12.0 * M * C);
+    launch_encoder_fwd(c, m->res[0], m->tok, m->P(WTE), m->P(WPE), B, T, C, m->V);
+  }
   const int64_t WS = sizeof(ActT) == 2 ? 2 : 4;
   auto w = [&](int t, int64_t o) {
     return static_cast<const void*>(static_cast<const char*>(m->W(t)) + o * WS);
@@ -241,21 +300,30 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
     ActT* fch = m->A<ActT>(m->fch, l, (int64_t)M * 4 * C);
     ActT* fcg = m->A<ActT>(m->fcg, l, (int64_t)M * 4 * C);
     float* lse = m->lse + (int64_t)l * B * NH * T;
-    launch_layernorm_fwd<ActT>(c, ln1, m->ln1_mean + (int64_t)l * M, m->ln1_rstd + (int64_t)l * M,
-                               m->res[l], m->P(LN1W) + l * C, m->P(LN1B) + l * C, M, C);
+    {
+      ProfScope ps(m, PC_LN_FWD, (double)M * C * (4 + a) + 8.0 * M);
+      launch_layernorm_fwd<ActT>(c, ln1, m->ln1_mean + (int64_t)l * M, m->ln1_rstd + (int64_t)l * M,
+                                 m->res[l], m->P(LN1W) + l * C, m->P(LN1B) + l * C, M, C);
+    }
     GemmArgs g = gemm(M, 3 * C, C, ln1, C, true, w(QKVW, (int64_t)l * 3 * C * C), C, true,
                       EPI_STORE, qkv, 3 * C, f32);
     g.bias = m->P(QKVB) + (int64_t)l * 3 * C;
     run_gemm(m, c, g);
-    if (f32) launch_attention_fwd_simt<ActT>(c, atty, lse, qkv, B, T, C, NH);
-    else launch_attention_fwd_bf16(c, reinterpret_cast<bf16*>(atty), lse, reinterpret_cast<const bf16*>(qkv), B, T, C, NH);
+    {
+      ProfScope ps(m, PC_ATTN_FWD, attn_flop);
+      if (f32) launch_attention_fwd_simt<ActT>(c, atty, lse, qkv, B, T, C, NH);
+      else launch_attention_fwd_bf16(c, reinterpret_cast<bf16*>(atty), lse, reinterpret_cast<const bf16*>(qkv), B, T, C, NH);
+    }
     g = gemm(M, C, C, atty, C, true, w(ATTPROJW, (int64_t)l * C * C), C, true, EPI_RESIDUAL,
              m->mid[l], C, true);
     g.bias = m->P(ATTPROJB) + (int64_t)l * C;
     g.aux = m->res[l];
     run_gemm(m, c, g);
-    launch_layernorm_fwd<ActT>(c, ln2, m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
-                               m->mid[l], m->P(LN2W) + l * C, m->P(LN2B) + l * C, M, C);
+    {
+      ProfScope ps(m, PC_LN_FWD, (double)M * C * (4 + a) + 8.0 * M);
+      launch_layernorm_fwd<ActT>(c, ln2, m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
+                                 m->mid[l], m->P(LN2W) + l * C, m->P(LN2B) + l * C, M, C);
+    }
     g = gemm(M, 4 * C, C, ln2, C, true, w(FCW, (int64_t)l * 4 * C * C), C, true, EPI_BIAS_GELU,
              fch, 4 * C, f32);
     g.bias = m->P(FCB) + (int64_t)l * 4 * C;
@@ -268,11 +336,17 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
     run_gemm(m, c, g);
   }
   ActT* lnf = reinterpret_cast<ActT*>(m->lnf);
-  launch_layernorm_fwd<ActT>(c, lnf, m->lnf_mean, m->lnf_rstd, m->res[L], m->P(LNFW), m->P(LNFB), M, C);
+  {
+    ProfScope ps(m, PC_LN_FWD, (double)M * C * (4 + a) + 8.0 * M);
+    launch_layernorm_fwd<ActT>(c, lnf, m->lnf_mean, m->lnf_rstd, m->res[L], m->P(LNFW), m->P(LNFB), M, C);
+  }
   ActT* logits = reinterpret_cast<ActT*>(m->logits);
   run_gemm(m, c, gemm(M, m->Vp, C, lnf, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32));
-  launch_crossentropy<ActT>(c, logits, m->losses, with_targets ? m->tgt : nullptr, M, m->V, m->Vp,
-                            1.f / (float)M, with_targets);
+  {
+    ProfScope ps(m, PC_CE, (with_targets ? 2.0 : 1.0) * M * (double)m->Vp * a + 4.0 * M);
+    launch_crossentropy<ActT>(c, logits, m->losses, with_targets ? m->tgt : nullptr, M, m->V, m->Vp,
+                              1.f / (float)M, with_targets);
+  }
   if (with_targets) launch_mean(c, m->loss, m->losses, M);
 }
 
@@ -285,6 +359,9 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     return static_cast<const void*>(static_cast<const char*>(m->W(t)) + o * WS);
   };
   const bool f32 = !m->bf;
+  const double a = (double)sizeof(ActT);
+  const double lnb_bytes = (double)M * C * (16.0 + (f32 ? 0.0 : a)) + 8.0 * M;
+  const double attn_flop = 8.0 * B * NH * (double)(C / NH) * (T * (T + 1.0) / 2.0);
   ActT* dlogits = reinterpret_cast<ActT*>(m->logits);
   ActT* lnf = reinterpret_cast<ActT*>(m->lnf);
   ActT* dres_act = reinterpret_cast<ActT*>(m->dres_act);
@@ -294,8 +371,11 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
   // tied head: logits = lnf wte^T
   run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, m->dln, C, true));
   run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true));
-  launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB), m->dln, m->res[L],
-                             m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
+  {
+    ProfScope ps(m, PC_LN_BWD, lnb_bytes - 4.0 * M * C);
+    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB), m->dln, m->res[L],
+                               m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
+  }
   for (int l = L - 1; l >= 0; l--) {
     ActT* ln1 = m->A<ActT>(m->ln1, l, (int64_t)M * C);
     ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
@@ -311,39 +391,63 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, g);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
                         m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true));
-    launch_colsum<float>(c, m->G(FCPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    {
+      ProfScope ps(m, PC_BIAS_GRAD, 4.0 * M * C);
+      launch_colsum<float>(c, m->G(FCPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    }
     // fc: fch = ln2 Wfc^T + b
     run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
                         EPI_STORE, m->dln, C, true));
     run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,
                         m->G(FCW) + (int64_t)l * 4 * C * C, C, true));
-    launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
-    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
-                               m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
-                               m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+    {
+      ProfScope ps(m, PC_BIAS_GRAD, a * M * 4.0 * C);
+      launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
+    }
+    {
+      ProfScope ps(m, PC_LN_BWD, lnb_bytes);
+      launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
+                                 m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
+                                 m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+    }
     // attproj: mid = res[l] + atty Wproj^T + b
     run_gemm(m, c, gemm(M, C, C, dres_act, C, true, w(ATTPROJW, (int64_t)l * C * C), C, false,
                         EPI_STORE, datty, C, f32));
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true));
-    launch_colsum<float>(c, m->G(ATTPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    {
+      ProfScope ps(m, PC_BIAS_GRAD, 4.0 * M * C);
+      launch_colsum<float>(c, m->G(ATTPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
+    }
     // attention
-    if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
-    else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
-                                   reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                   lse, m->dsum, B, T, C, NH);
+    {
+      ProfScope ps(m, PC_ATTN_BWD, attn_flop);
+      if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
+      else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
+                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
+                                     lse, m->dsum, B, T, C, NH);
+    }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
                         EPI_STORE, m->dln, C, true));
     run_gemm(m, c, gemm(3 * C, C, M, dbig, 3 * C, false, ln1, C, false, EPI_ACCUM,
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true));
-    launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
-    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
-                               m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
-                               m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+    {
+      ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
+      launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+    }
+    {
+      ProfScope ps(m, PC_LN_BWD, lnb_bytes);
+      launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
+                                 m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
+                                 m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+    }
   }
-  launch_encoder_bwd(c, m->G(WTE), m->G(WPE), m->dres, m->tok, B, T, C, Vp, m->enc_sorted,
-                     m->enc_partial);
+  {
+    ProfScope ps(m, PC_ENC_BWD, 4.0 * M * C + 8.0 * T * C);
+    launch_encoder_bwd(c, m->G(WTE), m->G(WPE), m->dres, m->tok, B, T, C, Vp, m->enc_sorted,
+                       m->enc_partial);
+  }
 }
 
 int forward_common(gpt2_model* m, bool with_targets, float* mean_loss) {
@@ -450,6 +554,8 @@ void gpt2_free(gpt2_model* m) {
   if (!m) return;
   cudaSetDevice(m->device);
   cudaStreamSynchronize(m->stream);
+  for (auto& p : m->prof.pending) { cudaEventDestroy(p.second.first); cudaEventDestroy(p.second.second); }
+  for (cudaEvent_t e : m->prof.pool) cudaEventDestroy(e);
   cudaFree(m->block);
   delete m;
 }
@@ -485,7 +591,11 @@ int gpt2_forward_host(gpt2_model* m, const int32_t* tokens, const int32_t* targe
 int gpt2_zero_grad(gpt2_model* m) {
   if (!m) return GPT2_ERR_ARG;
   cudaSetDevice(m->device);
-  cudaError_t e = cudaMemsetAsync(m->grads, 0, sizeof(float) * m->n_params, m->stream);
+  cudaError_t e;
+  {
+    ProfScope ps(m, PC_ZERO_GRAD, 4.0 * m->n_params);
+    e = cudaMemsetAsync(m->grads, 0, sizeof(float) * m->n_params, m->stream);
+  }
   if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_zero_grad");
   return GPT2_OK;
 }
@@ -511,8 +621,11 @@ int gpt2_adamw_step(gpt2_model* m, float lr, float b1, float b2, float eps, floa
   cudaSetDevice(m->device);
   LaunchCtx c = ctx(m);
   const float c1 = 1.f - powf(b1, (float)t), c2 = 1.f - powf(b2, (float)t);
-  launch_adamw(c, m->params, m->grads, m->adam_m, m->adam_v, m->bf ? m->wb : nullptr, m->n_params,
-               lr, b1, b2, eps, wd, c1, c2);
+  {
+    ProfScope ps(m, PC_ADAMW, (28.0 + (m->bf ? 2.0 : 0.0)) * m->n_params);
+    launch_adamw(c, m->params, m->grads, m->adam_m, m->adam_v, m->bf ? m->wb : nullptr, m->n_params,
+                 lr, b1, b2, eps, wd, c1, c2);
+  }
   return after_launches(m, c, "gpt2_adamw_step");
 }
 
@@ -627,6 +740,65 @@ int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* dst) {
   if (rc) return rc;
   cudaError_t e = cudaMemcpy(dst, m->res[layer], sizeof(float) * (size_t)m->M * m->C, cudaMemcpyDeviceToHost);
   return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_residual_out");
+}
+
+int gpt2_read_loss(gpt2_model* m, float* host_loss) {
+  if (!m || !host_loss) return GPT2_ERR_ARG;
+  if (!m->fwd_targets) return fail(m, GPT2_ERR_STATE, "gpt2_read_loss: no forward with targets");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_read_loss");
+  if (rc) return rc;
+  cudaError_t e = cudaMemcpy(host_loss, m->loss, sizeof(float), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_read_loss");
+  if (!std::isfinite(*host_loss)) return fail(m, GPT2_ERR_NONFINITE, "gpt2_read_loss: loss is not finite");
+  return GPT2_OK;
+}
+
+int gpt2_profile_num_classes(int32_t* n) {
+  if (!n) return GPT2_ERR_ARG;
+  *n = PC_N;
+  return GPT2_OK;
+}
+
+int gpt2_profile_enable(gpt2_model* m, uint32_t mask) {
+  if (!m) return GPT2_ERR_ARG;
+  m->prof.mask = mask & ((1u << PC_N) - 1u);
+  return GPT2_OK;
+}
+
+static int profile_collect(gpt2_model* m) {
+  cudaError_t e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_profile_read");
+  for (auto& p : m->prof.pending) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p.second.first, p.second.second) == cudaSuccess) m->prof.ms[p.first] += ms;
+    m->prof.pool.push_back(p.second.first);
+    m->prof.pool.push_back(p.second.second);
+  }
+  m->prof.pending.clear();
+  return GPT2_OK;
+}
+
+int gpt2_profile_reset(gpt2_model* m) {
+  if (!m) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  int rc = profile_collect(m);
+  for (int i = 0; i < PC_N; i++) { m->prof.launches[i] = 0; m->prof.work[i] = 0; m->prof.ms[i] = 0; }
+  return rc;
+}
+
+int gpt2_profile_read(gpt2_model* m, int32_t cls, const char** name, const char** unit,
+                      int64_t* launches, double* total_ms, double* work) {
+  if (!m || cls < 0 || cls >= PC_N) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  int rc = profile_collect(m);
+  if (rc) return rc;
+  if (name) *name = kProfNames[cls];
+  if (unit) *unit = kProfUnits[cls];
+  if (launches) *launches = m->prof.launches[cls];
+  if (total_ms) *total_ms = m->prof.ms[cls];
+  if (work) *work = m->prof.work[cls];
+  return GPT2_OK;
 }
 
 int gpt2_launch_count(const gpt2_model* m, int64_t* n) {

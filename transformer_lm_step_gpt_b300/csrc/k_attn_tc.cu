@@ -1,15 +1,622 @@
-// k_attn_tc.cu -- bf16 causal attention entry points.
-// Bring-up version: routes to the CUDA-core kernels of k_attn_simt.cu.
+// k_attn_tc.cu -- causal multi-head self-attention on the tcgen05 tensor cores.
+//
+// GeekNews, "A GPT-2-based ChatGPT clone in 3000 bytes of C", section "The
+// Transformer core": per head, S = q k^T (scaled by 1/sqrt(hs)), the lower-
+// triangular causal mask, softmax over each query row, times v.  Here the
+// T x T score matrix is never stored: it is computed one 128 x 128 tile at a
+// time in TMEM and folded into an online softmax (forward) or recomputed from
+// the saved row logsumexp (backward).
+//
+// Head size 64.  Every tile of q, k, v, dy is one TMA box [128 rows x 64]
+// of a 3-D tensor map over [B, T, width] (rows past T read as zero), landing
+// 128-byte-swizzled in shared memory, where a tcgen05 descriptor can read it
+// either as a K-major operand (rows = M or N) or as an MN-major one (rows =
+// K) -- so S = q k^T, P v, dV = P^T dy, dK = dS^T q and dQ = dS k all read the
+// same tiles.  P and dS are written to shared memory in the same swizzled
+// K-major layout by the softmax threads.
+//
+//   forward   one CTA per (128-query block, batch*head), 4 warps: S -> TMEM,
+//             row max / exp / row sum from TMEM (thread = query row), P -> smem,
+//             O_blk = P v -> TMEM, O accumulated in registers with the
+//             online-softmax rescale.  Saves lse = max + log(sum).
+//   backward  D = rowsum(dy * y); one CTA per (128-key block, b*h) for dK, dV
+//             (S^T, dP^T recomputed, dV += P^T dy, dK += dS^T q accumulated in
+//             TMEM); one CTA per (128-query block, b*h) for dQ (dQ += dS k).
+//             No atomics: every output element is written by one CTA, so the
+//             result is deterministic.
+// All mbarrier waits are bounded (common.cuh); a wait that gives up records
+// a timeout and the kernel runs to completion without trapping.
+#include <cuda.h>
+
+#include <cstdio>
+
 #include "common.cuh"
 #include "kernels.h"
 
+typedef CUresult (*EncodeTiledFnA)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFnA encoder_fn() {
+  static EncodeTiledFnA fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFnA>(p);
+  }
+  return fn;
+}
+
+// [B][T][W] bf16 tensor, box {64, 128, 1}, 128-byte swizzle, rows past T zero.
+static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W) {
+  EncodeTiledFnA f = encoder_fn();
+  if (!f) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)B};
+  cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)T * W * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#define AT_BLK 128
+#define AT_HS 64
+#define AT_TILE 16384u  // bytes of one [128 x 64] bf16 tile
+
+// descriptors of a [128 rows x 64] tile read as a K-major operand (rows = M
+// or N, K = 64 head dims) at K-step kk (16 dims), or as an MN-major operand
+// (rows = K, 64 columns = N) at K-step kk (16 rows)
+__device__ __forceinline__ uint64_t kmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 32, 16, 1024); }
+__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, 8192, 1024); }
+// descriptor of a [128 rows x 128] K-major operand stored as two 64-wide atoms
+__device__ __forceinline__ uint64_t kmaj2(uint32_t buf, int kk) {
+  return sw128_desc(buf + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024);
+}
+
+// Write 8 consecutive bf16 values (columns c8*8 .. c8*8+7) of row r into a
+// [128 x 128] K-major swizzled buffer (two 64-column atoms).
+__device__ __forceinline__ void st_swz8(uint8_t* buf, int r, int c8, const float* v) {
+  const int atom = c8 >> 3, chunk = (c8 & 7) ^ (r & 7);
+  uint4 u;
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&t0);
+  u.y = *reinterpret_cast<uint32_t*>(&t1);
+  u.z = *reinterpret_cast<uint32_t*>(&t2);
+  u.w = *reinterpret_cast<uint32_t*>(&t3);
+  *reinterpret_cast<uint4*>(buf + atom * AT_TILE + r * 128 + chunk * 16) = u;
+}
+
+__device__ __forceinline__ void store_row64_bf16(bf16* dst, const float* v, float mul) {
+#pragma unroll
+  for (int i = 0; i < 64; i += 8) {
+    uint4 u;
+    __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i] * mul, v[i + 1] * mul);
+    __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2] * mul, v[i + 3] * mul);
+    __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4] * mul, v[i + 5] * mul);
+    __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6] * mul, v[i + 7] * mul);
+    u.x = *reinterpret_cast<uint32_t*>(&t0);
+    u.y = *reinterpret_cast<uint32_t*>(&t1);
+    u.z = *reinterpret_cast<uint32_t*>(&t2);
+    u.w = *reinterpret_cast<uint32_t*>(&t3);
+    *reinterpret_cast<uint4*>(dst + i) = u;
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+// ============================================================ forward
+// smem: Q | K0 K1 | V0 V1 | P (2 atoms) | barriers
+#define AF_SMEM (1024 + 7 * AT_TILE + 256)
+
+__global__ void __launch_bounds__(128, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* y, float* lse, int T,
+                       int C, int NH, float scale, int* err) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sQ = sm;
+  uint8_t* sK = sm + AT_TILE;        // 2 stages
+  uint8_t* sV = sm + 3 * AT_TILE;    // 2 stages
+  uint8_t* sP = sm + 5 * AT_TILE;    // 2 atoms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 7 * AT_TILE);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;  // [2]
+  uint64_t* s_done = bars + 3;
+  uint64_t* o_done = bars + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+
+  const int nqb = gridDim.x;
+  const int qb = nqb - 1 - blockIdx.x;  // longest rows first
+  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  const int q0 = qb * AT_BLK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = warp * 32 + lane, q = q0 + row;
+  const int nkb = qb + 1;
+
+  if (tid == 0) {
+    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+  }
+  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t tS = tm, tO = tm + 128;
+  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(q_full, AT_TILE);
+    tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+    for (int s = 0; s < 2 && s < nkb; s++) {
+      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
+      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, s * AT_BLK, b);
+      tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, s * AT_BLK, b);
+    }
+  }
+  const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
+  float m = -INFINITY, l = 0.f;
+  float o[64];
+#pragma unroll
+  for (int i = 0; i < 64; i++) o[i] = 0.f;
+  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+
+  for (int kb = 0; kb < nkb; kb++) {
+    const int st = kb & 1;
+    const uint32_t ph = (uint32_t)(kb >> 1) & 1u;
+    if (tid == 0) {
+      if (kb == 0) mbar_wait(q_full, 0, err);
+      mbar_wait(&kv_full[st], ph, err);
+      tc_fence_after();
+      const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+      tc_commit(s_done);
+    }
+    mbar_wait(s_done, (uint32_t)kb & 1u, err);
+    tc_fence_after();
+    const bool diag = kb == qb;
+    const int k0 = kb * AT_BLK;
+    // pass 1: row max of this tile
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+      uint32_t r[32];
+      tmem_ld32(tS + lanebase + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j++) {
+        const float s = __uint_as_float(r[j]);
+        if (!diag || k0 + c * 32 + j <= q) mx = fmaxf(mx, s);
+      }
+    }
+    const float mnew = fmaxf(m, mx);
+    const float alpha = exp2f((m - mnew) * sl2);
+    const float mo = mnew * sl2;
+    // pass 2: P = exp(scale (s - mnew)), row sum, P -> smem (bf16)
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+      uint32_t r[32];
+      tmem_ld32(tS + lanebase + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float p[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const int kc = c * 32 + g * 8 + j;
+          const float s = __uint_as_float(r[g * 8 + j]);
+          p[j] = (!diag || k0 + kc <= q) ? exp2f(s * sl2 - mo) : 0.f;
+          sum += p[j];
+        }
+        st_swz8(sP, row, c * 4 + g, p);
+      }
+    }
+    l = l * alpha + sum;
+    m = mnew;
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t aP = smem_u32(sP), bV = smem_u32(sV + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tO, kmaj2(aP, kk), mnmaj(bV, kk), idO, kk > 0);
+      tc_commit(o_done);
+    }
+    mbar_wait(o_done, (uint32_t)kb & 1u, err);
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+      uint32_t r[32];
+      tmem_ld32(tO + lanebase + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j++) o[c * 32 + j] = o[c * 32 + j] * alpha + __uint_as_float(r[j]);
+    }
+    if (tid == 0 && kb + 2 < nkb) {
+      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_TILE);
+      tma_load_3d(sK + st * AT_TILE, &tm_qkv, &kv_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
+      tma_load_3d(sV + st * AT_TILE, &tm_qkv, &kv_full[st], 2 * C + h * AT_HS, (kb + 2) * AT_BLK, b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (q < T) {
+    store_row64_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS, o, 1.f / l);
+    lse[(int64_t)bh * T + q] = m * scale + logf(l);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
+}
+
+// ============================================================ backward: D
+// D[b,h,t] = sum_i dy[b,t,h*64+i] * y[b,t,h*64+i]
+__global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y, int B, int T,
+                                     int C, int NH) {
+  const int64_t n = (int64_t)B * T * NH;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int h = (int)(i % NH);
+    const int64_t bt = i / NH;
+    const int t = (int)(bt % T), b = (int)(bt / T);
+    const uint4* a = reinterpret_cast<const uint4*>(dy + bt * C + h * AT_HS);
+    const uint4* c = reinterpret_cast<const uint4*>(y + bt * C + h * AT_HS);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const uint4 ua = a[k], uc = c[k];
+      const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wc[4] = {uc.x, uc.y, uc.z, uc.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[j]));
+        const float2 fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wc[j]));
+        s += fa.x * fc.x + fa.y * fc.y;
+      }
+    }
+    dsum[((int64_t)b * NH + h) * T + t] = s;
+  }
+}
+
+// ============================================================ backward: dK, dV
+// smem: K | V | Q0 Q1 | dO0 dO1 | P^T (2 atoms) | dS^T (2 atoms) | lse[128] D[128] | bars
+#define AKV_SMEM (1024 + 10 * AT_TILE + 1024 + 256)
+
+__global__ void __launch_bounds__(128, 1)
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                           const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
+                           const float* dsum, int T, int C, int NH, float scale, int* err) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sK = sm;
+  uint8_t* sV = sm + AT_TILE;
+  uint8_t* sQ = sm + 2 * AT_TILE;   // 2 stages
+  uint8_t* sD = sm + 4 * AT_TILE;   // dO, 2 stages
+  uint8_t* sP = sm + 6 * AT_TILE;   // P^T, 2 atoms
+  uint8_t* sS = sm + 8 * AT_TILE;   // dS^T, 2 atoms
+  float* sl = reinterpret_cast<float*>(sm + 10 * AT_TILE);  // lse[128]
+  float* sdd = sl + 128;                                   // D[128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 10 * AT_TILE + 1024);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;  // [2]
+  uint64_t* s_done = bars + 3;
+  uint64_t* o_done = bars + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+
+  const int nb = gridDim.x;
+  const int kb = blockIdx.x;  // key block
+  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  const int k0 = kb * AT_BLK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = warp * 32 + lane, key = k0 + row;
+  const int nq = nb - kb;  // query blocks kb .. nb-1
+
+  if (tid == 0) {
+    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_dy);
+  }
+  if (warp == 0) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t tS = tm, tdP = tm + 128, tdV = tm + 256, tdK = tm + 320;
+  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
+    tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, k0, b);
+    tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, k0, b);
+    for (int s = 0; s < 2 && s < nq; s++) {
+      mbar_arrive_expect_tx(&q_full[s], 2 * AT_TILE);
+      tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &q_full[s], h * AT_HS, (kb + s) * AT_BLK, b);
+      tma_load_3d(sD + s * AT_TILE, &tm_dy, &q_full[s], h * AT_HS, (kb + s) * AT_BLK, b);
+    }
+  }
+  const float sl2 = scale * 1.4426950408889634f;
+  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+
+  for (int it = 0; it < nq; it++) {
+    const int qb = kb + it, q0 = qb * AT_BLK;
+    const int st = it & 1;
+    const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+    {  // this query block's lse (log2 units) and D
+      const int qq = q0 + row;
+      sl[row] = qq < T ? lse[(int64_t)bh * T + qq] * 1.4426950408889634f : INFINITY;
+      sdd[row] = qq < T ? dsum[(int64_t)bh * T + qq] : 0.f;
+    }
+    if (tid == 0) {
+      if (it == 0) mbar_wait(kv_full, 0, err);
+      mbar_wait(&q_full[st], ph, err);
+      tc_fence_after();
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      const uint32_t bQ = smem_u32(sQ + st * AT_TILE), bD = smem_u32(sD + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
+      tc_commit(s_done);
+    }
+    __syncthreads();  // lse / D of this block visible
+    mbar_wait(s_done, (uint32_t)it & 1u, err);
+    tc_fence_after();
+    const bool diag = it == 0;
+#pragma unroll 1
+    for (int c = 0; c < 4; c++) {
+      uint32_t rs[32], rd[32];
+      tmem_ld32(tS + lanebase + c * 32, rs);
+      tmem_ld32(tdP + lanebase + c * 32, rd);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float p[8], ds[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const int qc = c * 32 + g * 8 + j;
+          const bool ok = !diag || q0 + qc >= key;
+          const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - sl[qc]) : 0.f;
+          p[j] = pv;
+          ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - sdd[qc]);
+        }
+        st_swz8(sP, row, c * 4 + g, p);
+        st_swz8(sS, row, c * 4 + g, ds);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t aP = smem_u32(sP), aS = smem_u32(sS);
+      const uint32_t bQ = smem_u32(sQ + st * AT_TILE), bD = smem_u32(sD + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdV, kmaj2(aP, kk), mnmaj(bD, kk), idO, (it > 0 || kk > 0));
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdK, kmaj2(aS, kk), mnmaj(bQ, kk), idO, (it > 0 || kk > 0));
+      tc_commit(o_done);
+    }
+    mbar_wait(o_done, (uint32_t)it & 1u, err);
+    tc_fence_after();
+    if (tid == 0 && it + 2 < nq) {
+      mbar_arrive_expect_tx(&q_full[st], 2 * AT_TILE);
+      tma_load_3d(sQ + st * AT_TILE, &tm_qkv, &q_full[st], h * AT_HS, (qb + 2) * AT_BLK, b);
+      tma_load_3d(sD + st * AT_TILE, &tm_dy, &q_full[st], h * AT_HS, (qb + 2) * AT_BLK, b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  float v[64];
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    uint32_t r[32];
+    tmem_ld32(tdV + lanebase + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
+  }
+  const int64_t C3 = 3 * (int64_t)C;
+  if (key < T) store_row64_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS, v, 1.f);
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    uint32_t r[32];
+    tmem_ld32(tdK + lanebase + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
+  }
+  if (key < T) store_row64_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS, v, scale);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
+}
+
+// ============================================================ backward: dQ
+// smem: Q | dO | K0 K1 | V0 V1 | dS (2 atoms) | bars
+#define AQ_SMEM (1024 + 8 * AT_TILE + 256)
+
+__global__ void __launch_bounds__(128, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                          const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
+                          const float* dsum, int T, int C, int NH, float scale, int* err) {
+  extern __shared__ uint8_t smraw[];
+  uint8_t* sm = align1024(smraw);
+  uint8_t* sQ = sm;
+  uint8_t* sD = sm + AT_TILE;
+  uint8_t* sK = sm + 2 * AT_TILE;  // 2 stages
+  uint8_t* sV = sm + 4 * AT_TILE;  // 2 stages
+  uint8_t* sS = sm + 6 * AT_TILE;  // dS, 2 atoms
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 8 * AT_TILE);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;  // [2]
+  uint64_t* s_done = bars + 3;
+  uint64_t* o_done = bars + 4;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+
+  const int nqb = gridDim.x;
+  const int qb = nqb - 1 - blockIdx.x;
+  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  const int q0 = qb * AT_BLK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = warp * 32 + lane, q = q0 + row;
+  const int nkb = qb + 1;
+
+  if (tid == 0) {
+    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_dy);
+  }
+  if (warp == 0) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  const uint32_t tS = tm, tdP = tm + 128, tdQ = tm + 256;
+  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
+    tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+    tma_load_3d(sD, &tm_dy, q_full, h * AT_HS, q0, b);
+    for (int s = 0; s < 2 && s < nkb; s++) {
+      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
+      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, s * AT_BLK, b);
+      tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, s * AT_BLK, b);
+    }
+  }
+  const float sl2 = scale * 1.4426950408889634f;
+  const float my_lse = q < T ? lse[(int64_t)bh * T + q] * 1.4426950408889634f : INFINITY;
+  const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+
+  for (int kb = 0; kb < nkb; kb++) {
+    const int st = kb & 1;
+    const uint32_t ph = (uint32_t)(kb >> 1) & 1u;
+    if (tid == 0) {
+      if (kb == 0) mbar_wait(q_full, 0, err);
+      mbar_wait(&kv_full[st], ph, err);
+      tc_fence_after();
+      const uint32_t aQ = smem_u32(sQ), aD = smem_u32(sD);
+      const uint32_t bK = smem_u32(sK + st * AT_TILE), bV = smem_u32(sV + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aD, kk), kmaj(bV, kk), idS, kk > 0);
+      tc_commit(s_done);
+    }
+    mbar_wait(s_done, (uint32_t)kb & 1u, err);
+    tc_fence_after();
+    const bool diag = kb == qb;
+    const int k0 = kb * AT_BLK;
+#pragma unroll 1
+    for (int c = 0; c < 4; c++) {
+      uint32_t rs[32], rd[32];
+      tmem_ld32(tS + lanebase + c * 32, rs);
+      tmem_ld32(tdP + lanebase + c * 32, rd);
+      tmem_ld_wait();
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float ds[8];
+#pragma unroll
+        for (int j = 0; j < 8; j++) {
+          const int kc = c * 32 + g * 8 + j;
+          const bool ok = !diag || k0 + kc <= q;
+          const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - my_lse) : 0.f;
+          ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - my_d);
+        }
+        st_swz8(sS, row, c * 4 + g, ds);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t aS = smem_u32(sS), bK = smem_u32(sK + st * AT_TILE);
+#pragma unroll
+      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdQ, kmaj2(aS, kk), mnmaj(bK, kk), idO, (kb > 0 || kk > 0));
+      tc_commit(o_done);
+    }
+    mbar_wait(o_done, (uint32_t)kb & 1u, err);
+    tc_fence_after();
+    if (tid == 0 && kb + 2 < nkb) {
+      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_TILE);
+      tma_load_3d(sK + st * AT_TILE, &tm_qkv, &kv_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
+      tma_load_3d(sV + st * AT_TILE, &tm_qkv, &kv_full[st], 2 * C + h * AT_HS, (kb + 2) * AT_BLK, b);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  float v[64];
+#pragma unroll
+  for (int c = 0; c < 2; c++) {
+    uint32_t r[32];
+    tmem_ld32(tdQ + lanebase + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
+  }
+  if (q < T) store_row64_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS, v, scale);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
+}
+
+// ============================================================ launchers
 void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T,
                                int C, int NH) {
-  launch_attention_fwd_simt<bf16>(c, y, lse, qkv, B, T, C, NH);
+  if (C / NH != AT_HS) {
+    launch_attention_fwd_simt<bf16>(c, y, lse, qkv, B, T, C, NH);
+    return;
+  }
+  CUtensorMap tq;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C)) { c.host_fail = 1; return; }
+  dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
+  cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
+  attn_fwd_tc_kernel<<<grid, 128, AF_SMEM, c.stream>>>(tq, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
+  (*c.launches)++;
 }
 
 void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T,
                                int C, int NH) {
-  launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
+  if (C / NH != AT_HS) {
+    launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
+    return;
+  }
+  CUtensorMap tq, td;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C)) {
+    c.host_fail = 1;
+    return;
+  }
+  const int64_t n = (int64_t)B * T * NH;
+  attn_bwd_dsum_kernel<<<(int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16), 256, 0,
+                         c.stream>>>(dsum, dy, y, B, T, C, NH);
+  (*c.launches)++;
+  const float scale = 1.f / sqrtf((float)AT_HS);
+  dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
+  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AKV_SMEM);
+  attn_bwd_dkv_tc_kernel<<<grid, 128, AKV_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  (*c.launches)++;
+  cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
+  attn_bwd_dq_tc_kernel<<<grid, 128, AQ_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  (*c.launches)++;
 }

@@ -70,24 +70,8 @@ struct TcCfg {
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
 };
 
-// tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
-//   K-major operand: 8-row groups 1024 B apart (SBO); LBO unused.
-//   MN-major operand: 64-element MN blocks LBO apart, 8-row K groups 1024 B
-//   apart (SBO).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor of kind::f16: D f32, A and B bf16, M = 128, N = BN.
 __host__ __device__ constexpr uint32_t tc_idesc(int N, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_BM >> 4) << 24);
+  return tc_idesc_bf16(TC_BM, N, a_mn, b_mn);
 }
 
 __device__ __forceinline__ void store8_bf16(bf16* p, const float* v) {
