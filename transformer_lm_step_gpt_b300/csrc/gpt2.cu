@@ -373,7 +373,8 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
   run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true));
   {
     ProfScope ps(m, PC_LN_BWD, lnb_bytes - 4.0 * M * C);
-    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB), m->dln, m->res[L],
+    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB),
+                               m->G(FCPROJB) + (int64_t)(L - 1) * C, m->dln, m->res[L],
                                m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
   }
   for (int l = L - 1; l >= 0; l--) {
@@ -391,10 +392,8 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, g);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
                         m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true));
-    {
-      ProfScope ps(m, PC_BIAS_GRAD, 4.0 * M * C);
-      launch_colsum<float>(c, m->G(FCPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
-    }
+    // fcproj bias gradient: column sums of dres, taken by the LayerNorm
+    // backward that produced dres (LN_f or the next block's LN1)
     // fc: fch = ln2 Wfc^T + b
     run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
                         EPI_STORE, m->dln, C, true));
@@ -407,7 +406,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
       launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
-                                 m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
+                                 m->G(ATTPROJB) + (int64_t)l * C, m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
                                  m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
     }
     // attproj: mid = res[l] + atty Wproj^T + b
@@ -415,10 +414,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         EPI_STORE, datty, C, f32));
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true));
-    {
-      ProfScope ps(m, PC_BIAS_GRAD, 4.0 * M * C);
-      launch_colsum<float>(c, m->G(ATTPROJB) + (int64_t)l * C, m->dres, M, C, C, m->cs_partial);
-    }
+    // attproj bias gradient: taken by the LN2 backward above
     // attention
     {
       ProfScope ps(m, PC_ATTN_BWD, attn_flop);
@@ -439,7 +435,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
       launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
-                                 m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
+                                 l > 0 ? m->G(FCPROJB) + (int64_t)(l - 1) * C : nullptr, m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
                                  m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
     }
   }

@@ -67,7 +67,7 @@ struct TcCfg {
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
   static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;  // + align + barriers
 };
 
 __host__ __device__ constexpr uint32_t tc_idesc(int N, bool a_mn, bool b_mn) {
@@ -181,33 +181,63 @@ __device__ __forceinline__ void epi8(const GemmArgs& g, float* v, int m, int n, 
   }
 }
 
+// Persistent kernel: one CTA per SM walks the output tiles (split, m-tile,
+// n-tile) in a grouped raster (GROUP_M m-tiles per column sweep, so the
+// concurrently resident tiles share A and B tiles in L2).  Two TMEM
+// accumulators let the epilogue of one tile run while the MMAs of the next
+// one are issued.
+//   warp 0      TMA producer (one thread)
+//   warp 1      TMEM allocation + MMA issuer (one thread)
+//   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4, column half
+//               (w - 2) / 4 of the tile
+#define GROUP_M 8
+#define EPI_WARPS 8
+#define TC_THREADS (64 + 32 * EPI_WARPS)
+
+struct TileCoord {
+  int split, mt, nt;
+};
+__device__ __forceinline__ TileCoord tile_coord(int t, int mtiles, int ntiles) {
+  TileCoord c;
+  const int per = mtiles * ntiles;
+  c.split = t / per;
+  const int r = t - c.split * per;
+  const int group = r / (GROUP_M * ntiles);
+  const int first_m = group * GROUP_M;
+  const int gsize = min(mtiles - first_m, GROUP_M);
+  const int idx = r - group * GROUP_M * ntiles;
+  c.mt = first_m + idx % gsize;
+  c.nt = idx / gsize;
+  return c;
+}
+
 template <int BN, bool A_K, bool B_K>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   GemmArgs g, int k_tiles, int k_per_split, float* partial, int* err) {
+                   GemmArgs g, int k_tiles, int k_per_split, int splits, float* partial, int* err) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::STAGE_BYTES);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* acc_full = empty + S;   // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * TC_BM;
-  const int kt0 = blockIdx.z * k_per_split;
-  const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
+  const int mtiles = (g.M + TC_BM - 1) / TC_BM, ntiles = (g.N + BN - 1) / BN;
+  const int total = splits * mtiles * ntiles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    mbar_init(accf, 1);
+    for (int a = 0; a < 2; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], EPI_WARPS); }
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, 2 * BN);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -217,59 +247,80 @@ __global__ void __launch_bounds__(192, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int i = 0; i < nkt; i++) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, err)) break;
-        uint8_t* sa = smem + (size_t)s * Cfg::STAGE_BYTES;
-        uint8_t* sb = sa + Cfg::A_BYTES;
-        mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
-        const int k = (kt0 + i) * TC_BK;
-        if (A_K) {
-          tma_load_2d(sa, &tmA, &full[s], k, m0);
-        } else {
-          tma_load_2d(sa, &tmA, &full[s], m0, k);
-          tma_load_2d(sa + 8192, &tmA, &full[s], m0 + 64, k);
-        }
-        if (B_K) {
-          tma_load_2d(sb, &tmB, &full[s], k, n0);
-        } else {
+      int it = 0;  // running k-tile counter over all tiles of this CTA
+      for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        const TileCoord tc = tile_coord(t, mtiles, ntiles);
+        const int m0 = tc.mt * TC_BM, n0 = tc.nt * BN;
+        const int kt0 = tc.split * k_per_split;
+        const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
+        for (int i = 0; i < nkt; i++, it++) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          mbar_wait(&empty[s], ph ^ 1u, err);
+          uint8_t* sa = smem + (size_t)s * Cfg::STAGE_BYTES;
+          uint8_t* sb = sa + Cfg::A_BYTES;
+          mbar_arrive_expect_tx(&full[s], Cfg::STAGE_BYTES);
+          const int k = (kt0 + i) * TC_BK;
+          if (A_K) {
+            tma_load_2d(sa, &tmA, &full[s], k, m0);
+          } else {
+            tma_load_2d(sa, &tmA, &full[s], m0, k);
+            tma_load_2d(sa + 8192, &tmA, &full[s], m0 + 64, k);
+          }
+          if (B_K) {
+            tma_load_2d(sb, &tmB, &full[s], k, n0);
+          } else {
 #pragma unroll
-          for (int j = 0; j < BN / 64; j++) tma_load_2d(sb + j * 8192, &tmB, &full[s], n0 + 64 * j, k);
+            for (int j = 0; j < BN / 64; j++) tma_load_2d(sb + j * 8192, &tmB, &full[s], n0 + 64 * j, k);
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = tc_idesc(BN, !A_K, !B_K);
-      for (int i = 0; i < nkt; i++) {
-        const int s = i % S;
-        const uint32_t ph = (uint32_t)(i / S) & 1u;
-        if (!mbar_wait(&full[s], ph, err)) break;
+      int it = 0, ti = 0;
+      for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
+        const TileCoord tc = tile_coord(t, mtiles, ntiles);
+        const int kt0 = tc.split * k_per_split;
+        const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
+        const int a = ti & 1;
+        mbar_wait(&acc_empty[a], ((uint32_t)(ti >> 1) & 1u) ^ 1u, err);
         tc_fence_after();
-        const uint32_t a0 = smem_u32(smem + (size_t)s * Cfg::STAGE_BYTES);
-        const uint32_t b0 = a0 + Cfg::A_BYTES;
+        const uint32_t acc = tmem + (uint32_t)(a * BN);
+        for (int i = 0; i < nkt; i++, it++) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          mbar_wait(&full[s], ph, err);
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + (size_t)s * Cfg::STAGE_BYTES);
+          const uint32_t b0 = a0 + Cfg::A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < TC_BK / 16; kk++) {
-          const uint64_t ad = A_K ? sw128_desc(a0 + kk * 32, 16, 1024) : sw128_desc(a0 + kk * 2048, 8192, 1024);
-          const uint64_t bd = B_K ? sw128_desc(b0 + kk * 32, 16, 1024) : sw128_desc(b0 + kk * 2048, 8192, 1024);
-          tc_mma_bf16(tmem, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < TC_BK / 16; kk++) {
+            const uint64_t ad = A_K ? sw128_desc(a0 + kk * 32, 16, 1024) : sw128_desc(a0 + kk * 2048, 8192, 1024);
+            const uint64_t bd = B_K ? sw128_desc(b0 + kk * 32, 16, 1024) : sw128_desc(b0 + kk * 2048, 8192, 1024);
+            tc_mma_bf16(acc, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
         }
-        tc_commit(&empty[s]);
+        tc_commit(&acc_full[a]);
       }
-      tc_commit(accf);
     }
   } else {
-    const int quarter = warp & 3;
-    const int m = m0 + quarter * 32 + lane;
-    const bool got = mbar_wait(accf, 0, err);
-    tc_fence_after();
-    if (got && nkt > 0) {
-      float* part = partial ? partial + (size_t)blockIdx.z * (size_t)g.M * (size_t)g.N : nullptr;
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    int ti = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
+      const TileCoord tc = tile_coord(t, mtiles, ntiles);
+      const int m0 = tc.mt * TC_BM, n0 = tc.nt * BN;
+      const int a = ti & 1;
+      mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
+      tc_fence_after();
+      const int m = m0 + quarter * 32 + lane;
+      float* part = partial ? partial + (size_t)tc.split * (size_t)g.M * (size_t)g.N : nullptr;
 #pragma unroll 1
-      for (int cc = 0; cc < BN; cc += 32) {
+      for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 32) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cc, r);
+        tmem_ld32(tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cc, r);
         tmem_ld_wait();
         if (m < g.M && n0 + cc < g.N) {
 #pragma unroll
@@ -283,13 +334,16 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[a]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -330,10 +384,11 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
   const int kps = (k_tiles + splits - 1) / splits;
   const int zs = (k_tiles + kps - 1) / kps;
-  dim3 grid((g.N + BN - 1) / BN, (g.M + TC_BM - 1) / TC_BM, zs);
+  const int tiles = zs * ((g.N + BN - 1) / BN) * ((g.M + TC_BM - 1) / TC_BM);
+  const int grid = std::min(tiles, c.num_sms);
   auto kern = gemm_tc_kernel<BN, A_K, B_K>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM);
-  kern<<<grid, 192, TcCfg<BN>::SMEM, c.stream>>>(ta, tb, g, k_tiles, kps, zs > 1 ? partial : nullptr, c.err);
+  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, c.stream>>>(ta, tb, g, k_tiles, kps, zs, zs > 1 ? partial : nullptr, c.err);
   (*c.launches)++;
   if (zs > 1) {
     const int64_t n4 = (int64_t)g.M * g.N / 4;
@@ -344,7 +399,7 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
 }
 
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
-  const int BN = g.N >= 1024 ? 256 : 128;
+  const int BN = g.N >= 256 ? 256 : 128;
   const int tiles = ((g.N + BN - 1) / BN) * ((g.M + TC_BM - 1) / TC_BM);
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
   int splits = 1;

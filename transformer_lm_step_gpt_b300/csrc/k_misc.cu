@@ -310,19 +310,21 @@ template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, cons
 #define LNB_WARPS 8
 #define LNB_ROWS 64  // rows per block (8 per warp)
 
-int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS) * 2 * C; }
+int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS) * 3 * C; }
 
-// One warp per row; gamma/beta gradient partials per warp in shared memory,
-// combined over the block's warps in warp order into one partial per block.
+// One warp per row; gamma/beta gradient partials (and, when asked, the column
+// sums of the updated residual gradient) per warp in shared memory, combined
+// over the block's warps in warp order into one partial per block.
 template <typename ActT>
 __global__ void layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
                                      const float* inp, const float* w, const float* mean,
                                      const float* rstd, int N, int C, int accumulate) {
-  extern __shared__ float sm[];  // [LNB_WARPS][2][C]
+  extern __shared__ float sm[];  // [LNB_WARPS][3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sdw = sm + (int64_t)warp * 2 * C;
+  float* sdw = sm + (int64_t)warp * 3 * C;
   float* sdb = sdw + C;
-  for (int c = lane; c < C; c += 32) { sdw[c] = 0.f; sdb[c] = 0.f; }
+  float* sdr = sdb + C;
+  for (int c = lane; c < C; c += 32) { sdw[c] = 0.f; sdb[c] = 0.f; sdr[c] = 0.f; }
   __syncwarp();
   const int row0 = blockIdx.x * LNB_ROWS + warp * (LNB_ROWS / LNB_WARPS);
   for (int rr = 0; rr < LNB_ROWS / LNB_WARPS; rr++) {
@@ -361,74 +363,92 @@ __global__ void layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial
       if (dres_act) store4<ActT>(dres_act + (int64_t)row * C + c, d.x, d.y, d.z, d.w);
       sdw[c] += gv.x * x0; sdw[c + 1] += gv.y * x1; sdw[c + 2] += gv.z * x2; sdw[c + 3] += gv.w * x3;
       sdb[c] += gv.x; sdb[c + 1] += gv.y; sdb[c + 2] += gv.z; sdb[c + 3] += gv.w;
+      sdr[c] += d.x; sdr[c + 1] += d.y; sdr[c + 2] += d.z; sdr[c + 3] += d.w;
     }
   }
   __syncthreads();
-  float* out = partial + (int64_t)blockIdx.x * 2 * C;
-  for (int c = threadIdx.x; c < 2 * C; c += blockDim.x) {
+  float* out = partial + (int64_t)blockIdx.x * 3 * C;
+  for (int c = threadIdx.x; c < 3 * C; c += blockDim.x) {
     float s = 0.f;
-    for (int wv = 0; wv < LNB_WARPS; wv++) s += sm[(int64_t)wv * 2 * C + c];
+    for (int wv = 0; wv < LNB_WARPS; wv++) s += sm[(int64_t)wv * 3 * C + c];
     out[c] = s;
   }
 }
 
-// Sum nb partial rows of width W in row order and add into dst[0:W]
-// (dst may be split: first half into d0, second half into d1).
-__global__ void reduce_partials_kernel(float* d0, float* d1, const float* partial, int nb, int W,
-                                       int half) {
+// Sum nb partial rows of width W = parts * seg in row order and add segment
+// i into d[i][0:seg] (a null d[i] is skipped).
+__global__ void reduce_partials_kernel(float* d0, float* d1, float* d2, const float* partial, int nb,
+                                       int W, int seg) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= W) return;
+  float* d = c < seg ? d0 : (c < 2 * seg ? d1 : d2);
+  if (!d) return;
   float s = 0.f;
   for (int b = 0; b < nb; b++) s += partial[(int64_t)b * W + c];
-  if (c < half) d0[c] += s; else d1[c - half] += s;
+  d[c % seg] += s;
 }
 
 template <typename ActT>
 void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
-                          const float* dy, const float* inp, const float* w, const float* mean,
-                          const float* rstd, int N, int C, bool accumulate, float* partial) {
+                          float* dres_colsum, const float* dy, const float* inp, const float* w,
+                          const float* mean, const float* rstd, int N, int C, bool accumulate,
+                          float* partial) {
   const int nb = cdiv(N, LNB_ROWS);
-  const size_t smem = (size_t)LNB_WARPS * 2 * C * sizeof(float);
+  const size_t smem = (size_t)LNB_WARPS * 3 * C * sizeof(float);
   cudaFuncSetAttribute(layernorm_bwd_kernel<ActT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   layernorm_bwd_kernel<ActT><<<nb, LNB_WARPS * 32, smem, c.stream>>>(
       dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
   LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(2 * C, 256), 256, 0, c.stream>>>(dw, db, partial, nb, 2 * C, C);
+  reduce_partials_kernel<<<cdiv(3 * C, 256), 256, 0, c.stream>>>(dw, db, dres_colsum, partial, nb,
+                                                                   3 * C, C);
   LAUNCH_CHECK(c);
 }
-template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, const float*,
+template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
                                           const float*, const float*, const float*, const float*,
-                                          int, int, bool, float*);
-template void launch_layernorm_bwd<bf16>(LaunchCtx&, float*, bf16*, float*, float*, const float*,
+                                          const float*, int, int, bool, float*);
+template void launch_layernorm_bwd<bf16>(LaunchCtx&, float*, bf16*, float*, float*, float*,
                                          const float*, const float*, const float*, const float*,
-                                         int, int, bool, float*);
+                                         const float*, int, int, bool, float*);
 
 // ============================================================ column sums
-#define CS_CHUNKS 64
+#define CS_CHUNKS 128
 int64_t colsum_partial_floats(int M, int N) { return (int64_t)CS_CHUNKS * N; }
 
-// grid (ceil(N/256), CS_CHUNKS); 64 threads x 4 columns; rows of one chunk in order.
+// grid (ceil(N/256), CS_CHUNKS), 256 threads: 4 row groups x 64 threads x 4
+// columns.  Group g sums rows r0+g, r0+g+4, ... of the chunk in order; the 4
+// group sums are added in group order.
 template <typename T>
 __global__ void colsum_partial_kernel(float* partial, const T* x, int M, int N, int64_t ld) {
-  const int col = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  __shared__ float4 sg[4][64];
+  const int grp = threadIdx.x >> 6, t = threadIdx.x & 63;
+  const int col = (blockIdx.x * 64 + t) * 4;
   const int rows = (M + CS_CHUNKS - 1) / CS_CHUNKS;
   const int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
-  if (col >= N) return;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int r = r0; r < r1; r++) {
-    const float4 v = load4<T>(x + (int64_t)r * ld + col);
-    s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  if (col < N) {
+#pragma unroll 4
+    for (int r = r0 + grp; r < r1; r += 4) {
+      const float4 v = load4<T>(x + (int64_t)r * ld + col);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
   }
-  *reinterpret_cast<float4*>(partial + (int64_t)blockIdx.y * N + col) = s;
+  sg[grp][t] = s;
+  __syncthreads();
+  if (grp == 0 && col < N) {
+    float4 o = sg[0][t];
+#pragma unroll
+    for (int q = 1; q < 4; q++) { o.x += sg[q][t].x; o.y += sg[q][t].y; o.z += sg[q][t].z; o.w += sg[q][t].w; }
+    *reinterpret_cast<float4*>(partial + (int64_t)blockIdx.y * N + col) = o;
+  }
 }
 
 template <typename T>
 void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
   dim3 grid(cdiv(N, 256), CS_CHUNKS);
-  colsum_partial_kernel<T><<<grid, 64, 0, c.stream>>>(partial, x, M, N, ld);
+  colsum_partial_kernel<T><<<grid, 256, 0, c.stream>>>(partial, x, M, N, ld);
   LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(N, 256), 256, 0, c.stream>>>(db, db, partial, CS_CHUNKS, N, N);
+  reduce_partials_kernel<<<cdiv(N, 256), 256, 0, c.stream>>>(db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
   LAUNCH_CHECK(c);
 }
 template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);
