@@ -49,6 +49,9 @@ WORKLOADS = {
                                dist="uniform", lr=6e-4, wd=0.1),
     "gpt2-350M-B8-T1024": dict(L=24, C=1024, NH=16, V=50257, Vp=50304, maxT=1024, B=8, T=1024,
                                dist="uniform", lr=6e-4, wd=0.1),
+    # the 124M model on a small batch: the size used for ncu captures
+    "gpt2-124M-B2-T1024": dict(L=12, C=768, NH=12, V=50257, Vp=50304, maxT=1024, B=2, T=1024,
+                               dist="zipf", lr=6e-4, wd=0.1),
 }
 DEFAULT_WORKLOAD = "gpt2-124M-B16-T1024"
 BETAS, EPS = (0.9, 0.999), 1e-8

@@ -62,6 +62,22 @@ __device__ __forceinline__ float gelu_grad_f(float x) {
   return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * GELU_S * (1.f + 3.f * GELU_A * x * x);
 }
 
+// The same two functions with the hardware tanh approximation (PTX
+// tanh.approx.f32, relative error about 2^-11), for results that are
+// rounded to bf16 anyway.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_hw(float x) {
+  return 0.5f * x * (1.f + tanh_hw(GELU_S * (x + GELU_A * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_hw(float x) {
+  const float th = tanh_hw(GELU_S * (x + GELU_A * x * x * x));
+  return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * GELU_S * (1.f + 3.f * GELU_A * x * x);
+}
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -188,6 +204,32 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, uint64_
       "l"(tmap), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+
+// TMA store / reduce-add of a shared-memory box into a 2-D or 3-D tensor
+// (bulk-group completion), and the waits on outstanding groups.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until the shared-memory sources of all committed groups have been read
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until all committed groups have completed
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand
 // whose swizzle atoms (8 rows x 128 B) start on 1024-byte boundaries.

@@ -39,14 +39,24 @@ const char* kTensorNames[NT] = {"wte", "wpe", "ln1w", "ln1b", "qkvw", "qkvb", "a
 thread_local std::string g_build_error = "no error";
 
 // Kernel classes timed by gpt2_profile_*; work unit per class.
-enum ProfClass { PC_GEMM_FWD = 0, PC_GEMM_DGRAD, PC_GEMM_WGRAD, PC_ATTN_FWD, PC_ATTN_BWD,
-                 PC_LN_FWD, PC_LN_BWD, PC_CE, PC_BIAS_GRAD, PC_ENC_FWD, PC_ENC_BWD, PC_ADAMW,
-                 PC_ZERO_GRAD, PC_N };
-const char* kProfNames[PC_N] = {"gemm_fwd", "gemm_dgrad", "gemm_wgrad", "attention_fwd",
-                                "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy",
-                                "bias_grad", "encoder_fwd", "encoder_bwd", "adamw", "zero_grad"};
-const char* kProfUnits[PC_N] = {"flop", "flop", "flop", "flop", "flop", "byte", "byte",
-                                "byte", "byte", "byte", "byte", "byte", "byte"};
+// Matmul classes are per Linear (qkv, attproj, fc, fcproj, the tied head)
+// and per pass (forward, data gradient, weight gradient).
+enum GemmSite { GS_QKV = 0, GS_ATTPROJ, GS_FC, GS_FCPROJ, GS_HEAD, GS_N };
+enum GemmPass { GP_FWD = 0, GP_DGRAD, GP_WGRAD };
+enum ProfClass { PC_GEMM0 = 0, PC_ATTN_FWD = 3 * GS_N, PC_ATTN_BWD, PC_LN_FWD, PC_LN_BWD, PC_CE,
+                 PC_BIAS_GRAD, PC_ENC_FWD, PC_ENC_BWD, PC_ADAMW, PC_ZERO_GRAD, PC_N };
+const char* kProfNames[PC_N] = {
+    "gemm_qkv_fwd", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
+    "gemm_attproj_fwd", "gemm_attproj_dgrad", "gemm_attproj_wgrad",
+    "gemm_fc_fwd", "gemm_fc_dgrad", "gemm_fc_wgrad",
+    "gemm_fcproj_fwd", "gemm_fcproj_dgrad", "gemm_fcproj_wgrad",
+    "gemm_head_fwd", "gemm_head_dgrad", "gemm_head_wgrad",
+    "attention_fwd", "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy",
+    "bias_grad", "encoder_fwd", "encoder_bwd", "adamw", "zero_grad"};
+const char* kProfUnits[PC_N] = {
+    "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop",
+    "flop", "flop", "flop", "flop", "flop", "flop", "byte", "byte", "byte", "byte", "byte",
+    "byte", "byte", "byte"};
 
 struct ProfState {
   uint32_t mask = 0;
@@ -266,9 +276,9 @@ GemmArgs gemm(int M, int N, int K, const void* A, int64_t lda, bool ak, const vo
   return g;
 }
 
-void run_gemm(gpt2_model* m, LaunchCtx& c, GemmArgs g) {
-  const int cls = g.a_kmajor ? (g.b_kmajor ? PC_GEMM_FWD : PC_GEMM_DGRAD) : PC_GEMM_WGRAD;
-  ProfScope ps(m, cls, 2.0 * g.M * (double)g.N * g.K);
+void run_gemm(gpt2_model* m, LaunchCtx& c, GemmArgs g, int site) {
+  const int pass = g.a_kmajor ? (g.b_kmajor ? GP_FWD : GP_DGRAD) : GP_WGRAD;
+  ProfScope ps(m, PC_GEMM0 + 3 * site + pass, 2.0 * g.M * (double)g.N * g.K);
   if (m->bf) {
     g.splitk_scratch = m->splitk;
     g.splitk_scratch_floats = m->splitk_floats;
@@ -308,7 +318,7 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
     GemmArgs g = gemm(M, 3 * C, C, ln1, C, true, w(QKVW, (int64_t)l * 3 * C * C), C, true,
                       EPI_STORE, qkv, 3 * C, f32);
     g.bias = m->P(QKVB) + (int64_t)l * 3 * C;
-    run_gemm(m, c, g);
+    run_gemm(m, c, g, GS_QKV);
     {
       ProfScope ps(m, PC_ATTN_FWD, attn_flop);
       if (f32) launch_attention_fwd_simt<ActT>(c, atty, lse, qkv, B, T, C, NH);
@@ -318,7 +328,7 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
              m->mid[l], C, true);
     g.bias = m->P(ATTPROJB) + (int64_t)l * C;
     g.aux = m->res[l];
-    run_gemm(m, c, g);
+    run_gemm(m, c, g, GS_ATTPROJ);
     {
       ProfScope ps(m, PC_LN_FWD, (double)M * C * (4 + a) + 8.0 * M);
       launch_layernorm_fwd<ActT>(c, ln2, m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
@@ -328,12 +338,12 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
              fch, 4 * C, f32);
     g.bias = m->P(FCB) + (int64_t)l * 4 * C;
     g.out2 = fcg;
-    run_gemm(m, c, g);
+    run_gemm(m, c, g, GS_FC);
     g = gemm(M, C, 4 * C, fcg, 4 * C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C, true,
              EPI_RESIDUAL, m->res[l + 1], C, true);
     g.bias = m->P(FCPROJB) + (int64_t)l * C;
     g.aux = m->mid[l];
-    run_gemm(m, c, g);
+    run_gemm(m, c, g, GS_FCPROJ);
   }
   ActT* lnf = reinterpret_cast<ActT*>(m->lnf);
   {
@@ -341,7 +351,7 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
     launch_layernorm_fwd<ActT>(c, lnf, m->lnf_mean, m->lnf_rstd, m->res[L], m->P(LNFW), m->P(LNFB), M, C);
   }
   ActT* logits = reinterpret_cast<ActT*>(m->logits);
-  run_gemm(m, c, gemm(M, m->Vp, C, lnf, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32));
+  run_gemm(m, c, gemm(M, m->Vp, C, lnf, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32), GS_HEAD);
   {
     ProfScope ps(m, PC_CE, (with_targets ? 2.0 : 1.0) * M * (double)m->Vp * a + 4.0 * M);
     launch_crossentropy<ActT>(c, logits, m->losses, with_targets ? m->tgt : nullptr, M, m->V, m->Vp,
@@ -369,8 +379,8 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
   ActT* dbig = reinterpret_cast<ActT*>(m->dbig);
   ActT* datty = reinterpret_cast<ActT*>(m->datty);
   // tied head: logits = lnf wte^T
-  run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, m->dln, C, true));
-  run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true));
+  run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, m->dln, C, true), GS_HEAD);
+  run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true), GS_HEAD);
   {
     ProfScope ps(m, PC_LN_BWD, lnb_bytes - 4.0 * M * C);
     launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB),
@@ -389,16 +399,16 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     GemmArgs g = gemm(M, 4 * C, C, dres_act, C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C,
                       false, EPI_GELU_BWD, dbig, 4 * C, f32);
     g.aux = fch;
-    run_gemm(m, c, g);
+    run_gemm(m, c, g, GS_FCPROJ);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
-                        m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true));
+                        m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true), GS_FCPROJ);
     // fcproj bias gradient: column sums of dres, taken by the LayerNorm
     // backward that produced dres (LN_f or the next block's LN1)
     // fc: fch = ln2 Wfc^T + b
     run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
-                        EPI_STORE, m->dln, C, true));
+                        EPI_STORE, m->dln, C, true), GS_FC);
     run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,
-                        m->G(FCW) + (int64_t)l * 4 * C * C, C, true));
+                        m->G(FCW) + (int64_t)l * 4 * C * C, C, true), GS_FC);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 4.0 * C);
       launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
@@ -411,9 +421,9 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     }
     // attproj: mid = res[l] + atty Wproj^T + b
     run_gemm(m, c, gemm(M, C, C, dres_act, C, true, w(ATTPROJW, (int64_t)l * C * C), C, false,
-                        EPI_STORE, datty, C, f32));
+                        EPI_STORE, datty, C, f32), GS_ATTPROJ);
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
-                        m->G(ATTPROJW) + (int64_t)l * C * C, C, true));
+                        m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
     // attention
     {
@@ -425,9 +435,9 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
-                        EPI_STORE, m->dln, C, true));
+                        EPI_STORE, m->dln, C, true), GS_QKV);
     run_gemm(m, c, gemm(3 * C, C, M, dbig, 3 * C, false, ln1, C, false, EPI_ACCUM,
-                        m->G(QKVW) + (int64_t)l * 3 * C * C, C, true));
+                        m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
       launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);

@@ -15,7 +15,7 @@
 // same tiles.  P and dS are written to shared memory in the same swizzled
 // K-major layout by the softmax threads.
 //
-//   forward   one CTA per (128-query block, batch*head), 4 warps: S -> TMEM,
+//   forward   one CTA per (128-query block, batch*head), 8 warps: S -> TMEM,
 //             row max / exp / row sum from TMEM (thread = query row), P -> smem,
 //             O_blk = P v -> TMEM, O accumulated in registers with the
 //             online-softmax rescale.  Saves lse = max + log(sum).
@@ -112,36 +112,61 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
 }
 
-// ============================================================ forward
-// smem: Q | K0 K1 | V0 V1 | P (2 atoms) | barriers
-#define AF_SMEM (1024 + 7 * AT_TILE + 256)
+__device__ __forceinline__ void store_row32_bf16(bf16* dst, const float* v, float mul) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    uint4 u;
+    __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i] * mul, v[i + 1] * mul);
+    __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2] * mul, v[i + 3] * mul);
+    __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4] * mul, v[i + 5] * mul);
+    __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6] * mul, v[i + 7] * mul);
+    u.x = *reinterpret_cast<uint32_t*>(&t0);
+    u.y = *reinterpret_cast<uint32_t*>(&t1);
+    u.z = *reinterpret_cast<uint32_t*>(&t2);
+    u.w = *reinterpret_cast<uint32_t*>(&t3);
+    *reinterpret_cast<uint4*>(dst + i) = u;
+  }
+}
 
-__global__ void __launch_bounds__(128, 1)
+// 8 warps: warps w and w+4 read the same TMEM lane quarter (w % 4, i.e. the
+// same 32 query or key rows) and split the 128 score columns (half = w / 4
+// takes columns 64*half .. 64*half+63) and the 64 output head dims
+// (32*half .. 32*half+31).
+#define AT_THREADS 256
+
+// ============================================================ forward
+// smem: Q | K0 K1 | V | P (2 atoms) | row-max exchange [2][128] | barriers
+#define AF_SMEM (1024 + 6 * AT_TILE + 1024 + 256)
+
+__global__ void __launch_bounds__(AT_THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* y, float* lse, int T,
                        int C, int NH, float scale, int* err) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
-  uint8_t* sK = sm + AT_TILE;        // 2 stages
-  uint8_t* sV = sm + 3 * AT_TILE;    // 2 stages
-  uint8_t* sP = sm + 5 * AT_TILE;    // 2 atoms
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 7 * AT_TILE);
+  uint8_t* sK = sm + AT_TILE;      // 2 stages
+  uint8_t* sV = sm + 3 * AT_TILE;  // 1 stage
+  uint8_t* sP = sm + 4 * AT_TILE;  // 2 atoms
+  float* red = reinterpret_cast<float*>(sm + 6 * AT_TILE);  // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 6 * AT_TILE + 1024);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;  // [2]
-  uint64_t* s_done = bars + 3;
-  uint64_t* o_done = bars + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  uint64_t* k_full = bars + 1;  // [2]
+  uint64_t* v_full = bars + 3;
+  uint64_t* s_done = bars + 4;
+  uint64_t* o_done = bars + 5;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
 
   const int nqb = gridDim.x;
   const int qb = nqb - 1 - blockIdx.x;  // longest rows first
   const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = warp * 32 + lane, q = q0 + row;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane, q = q0 + row;
   const int nkb = qb + 1;
 
   if (tid == 0) {
-    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 6; i++) mbar_init(&bars[i], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
   }
@@ -151,31 +176,31 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tm = *tslot;
   const uint32_t tS = tm, tO = tm + 128;
-  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
   if (tid == 0) {
     mbar_arrive_expect_tx(q_full, AT_TILE);
     tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+    mbar_arrive_expect_tx(v_full, AT_TILE);
+    tma_load_3d(sV, &tm_qkv, v_full, 2 * C + h * AT_HS, 0, b);
     for (int s = 0; s < 2 && s < nkb; s++) {
-      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
-      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, s * AT_BLK, b);
-      tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, s * AT_BLK, b);
+      mbar_arrive_expect_tx(&k_full[s], AT_TILE);
+      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, s * AT_BLK, b);
     }
   }
   const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
-  float m = -INFINITY, l = 0.f;
-  float o[64];
+  float m = -INFINITY, lpart = 0.f;
+  float o[32];
 #pragma unroll
-  for (int i = 0; i < 64; i++) o[i] = 0.f;
+  for (int i = 0; i < 32; i++) o[i] = 0.f;
   const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
   const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
   for (int kb = 0; kb < nkb; kb++) {
     const int st = kb & 1;
-    const uint32_t ph = (uint32_t)(kb >> 1) & 1u;
     if (tid == 0) {
       if (kb == 0) mbar_wait(q_full, 0, err);
-      mbar_wait(&kv_full[st], ph, err);
+      mbar_wait(&k_full[st], (uint32_t)(kb >> 1) & 1u, err);
       tc_fence_after();
       const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + st * AT_TILE);
 #pragma unroll
@@ -186,10 +211,11 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const bool diag = kb == qb;
     const int k0 = kb * AT_BLK;
-    // pass 1: row max of this tile
+    // pass 1: max over this half's 64 columns, exchanged with the partner warp
     float mx = -INFINITY;
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
+#pragma unroll 1
+    for (int cc = 0; cc < 2; cc++) {
+      const int c = half * 2 + cc;
       uint32_t r[32];
       tmem_ld32(tS + lanebase + c * 32, r);
       tmem_ld_wait();
@@ -199,13 +225,17 @@ __global__ void __launch_bounds__(128, 1)
         if (!diag || k0 + c * 32 + j <= q) mx = fmaxf(mx, s);
       }
     }
-    const float mnew = fmaxf(m, mx);
+    red[half * 128 + row] = mx;
+    tc_fence_before();
+    __syncthreads();
+    const float mnew = fmaxf(m, fmaxf(red[row], red[128 + row]));
     const float alpha = exp2f((m - mnew) * sl2);
     const float mo = mnew * sl2;
-    // pass 2: P = exp(scale (s - mnew)), row sum, P -> smem (bf16)
+    // pass 2: P = exp(scale (s - mnew)) -> smem (bf16), partial row sum
     float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; c++) {
+#pragma unroll 1
+    for (int cc = 0; cc < 2; cc++) {
+      const int c = half * 2 + cc;
       uint32_t r[32];
       tmem_ld32(tS + lanebase + c * 32, r);
       tmem_ld_wait();
@@ -222,40 +252,47 @@ __global__ void __launch_bounds__(128, 1)
         st_swz8(sP, row, c * 4 + g, p);
       }
     }
-    l = l * alpha + sum;
+    lpart = lpart * alpha + sum;
     m = mnew;
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t aP = smem_u32(sP), bV = smem_u32(sV + st * AT_TILE);
+      mbar_wait(v_full, (uint32_t)kb & 1u, err);
+      const uint32_t aP = smem_u32(sP), bV = smem_u32(sV);
 #pragma unroll
       for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tO, kmaj2(aP, kk), mnmaj(bV, kk), idO, kk > 0);
       tc_commit(o_done);
     }
     mbar_wait(o_done, (uint32_t)kb & 1u, err);
     tc_fence_after();
-#pragma unroll
-    for (int c = 0; c < 2; c++) {
+    {
       uint32_t r[32];
-      tmem_ld32(tO + lanebase + c * 32, r);
+      tmem_ld32(tO + lanebase + half * 32, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; j++) o[c * 32 + j] = o[c * 32 + j] * alpha + __uint_as_float(r[j]);
+      for (int j = 0; j < 32; j++) o[j] = o[j] * alpha + __uint_as_float(r[j]);
     }
-    if (tid == 0 && kb + 2 < nkb) {
-      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_TILE);
-      tma_load_3d(sK + st * AT_TILE, &tm_qkv, &kv_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
-      tma_load_3d(sV + st * AT_TILE, &tm_qkv, &kv_full[st], 2 * C + h * AT_HS, (kb + 2) * AT_BLK, b);
+    if (tid == 0) {  // both MMAs of block kb are done: V and K stage st are free
+      if (kb + 1 < nkb) {
+        mbar_arrive_expect_tx(v_full, AT_TILE);
+        tma_load_3d(sV, &tm_qkv, v_full, 2 * C + h * AT_HS, (kb + 1) * AT_BLK, b);
+      }
+      if (kb + 2 < nkb) {
+        mbar_arrive_expect_tx(&k_full[st], AT_TILE);
+        tma_load_3d(sK + st * AT_TILE, &tm_qkv, &k_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
+      }
     }
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
+  __syncthreads();
+  red[half * 128 + row] = lpart;
+  __syncthreads();
+  const float l = red[row] + red[128 + row];
   if (q < T) {
-    store_row64_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS, o, 1.f / l);
-    lse[(int64_t)bh * T + q] = m * scale + logf(l);
+    store_row32_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS + half * 32, o, 1.f / l);
+    if (half == 0) lse[(int64_t)bh * T + q] = m * scale + logf(l);
   }
   tc_fence_before();
   __syncthreads();
@@ -294,7 +331,7 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 // smem: K | V | Q0 Q1 | dO0 dO1 | P^T (2 atoms) | dS^T (2 atoms) | lse[128] D[128] | bars
 #define AKV_SMEM (1024 + 10 * AT_TILE + 1024 + 256)
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(AT_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                            const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
                            const float* dsum, int T, int C, int NH, float scale, int* err) {
@@ -306,7 +343,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* sD = sm + 4 * AT_TILE;   // dO, 2 stages
   uint8_t* sP = sm + 6 * AT_TILE;   // P^T, 2 atoms
   uint8_t* sS = sm + 8 * AT_TILE;   // dS^T, 2 atoms
-  float* sl = reinterpret_cast<float*>(sm + 10 * AT_TILE);  // lse[128]
+  float* sl = reinterpret_cast<float*>(sm + 10 * AT_TILE);  // lse[128] (log2 units)
   float* sdd = sl + 128;                                   // D[128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 10 * AT_TILE + 1024);
   uint64_t* kv_full = bars;
@@ -320,7 +357,8 @@ __global__ void __launch_bounds__(128, 1)
   const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
   const int k0 = kb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = warp * 32 + lane, key = k0 + row;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane, key = k0 + row;
   const int nq = nb - kb;  // query blocks kb .. nb-1
 
   if (tid == 0) {
@@ -335,7 +373,7 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tm = *tslot;
   const uint32_t tS = tm, tdP = tm + 128, tdV = tm + 256, tdK = tm + 320;
-  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
   if (tid == 0) {
     mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
@@ -355,10 +393,10 @@ __global__ void __launch_bounds__(128, 1)
     const int qb = kb + it, q0 = qb * AT_BLK;
     const int st = it & 1;
     const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-    {  // this query block's lse (log2 units) and D
-      const int qq = q0 + row;
-      sl[row] = qq < T ? lse[(int64_t)bh * T + qq] * 1.4426950408889634f : INFINITY;
-      sdd[row] = qq < T ? dsum[(int64_t)bh * T + qq] : 0.f;
+    if (tid < 128) {  // this query block's lse (log2 units) and D
+      const int qq = q0 + tid;
+      sl[tid] = qq < T ? lse[(int64_t)bh * T + qq] * 1.4426950408889634f : INFINITY;
+      sdd[tid] = qq < T ? dsum[(int64_t)bh * T + qq] : 0.f;
     }
     if (tid == 0) {
       if (it == 0) mbar_wait(kv_full, 0, err);
@@ -377,7 +415,8 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const bool diag = it == 0;
 #pragma unroll 1
-    for (int c = 0; c < 4; c++) {
+    for (int cc = 0; cc < 2; cc++) {
+      const int c = half * 2 + cc;
       uint32_t rs[32], rd[32];
       tmem_ld32(tS + lanebase + c * 32, rs);
       tmem_ld32(tdP + lanebase + c * 32, rd);
@@ -421,26 +460,24 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
   }
-  float v[64];
-#pragma unroll
-  for (int c = 0; c < 2; c++) {
-    uint32_t r[32];
-    tmem_ld32(tdV + lanebase + c * 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
-  }
   const int64_t C3 = 3 * (int64_t)C;
-  if (key < T) store_row64_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS, v, 1.f);
-#pragma unroll
-  for (int c = 0; c < 2; c++) {
+  float v[32];
+  {
     uint32_t r[32];
-    tmem_ld32(tdK + lanebase + c * 32, r);
+    tmem_ld32(tdV + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
   }
-  if (key < T) store_row64_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS, v, scale);
+  if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS + half * 32, v, 1.f);
+  {
+    uint32_t r[32];
+    tmem_ld32(tdK + lanebase + half * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+  }
+  if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
@@ -450,7 +487,7 @@ __global__ void __launch_bounds__(128, 1)
 // smem: Q | dO | K0 K1 | V0 V1 | dS (2 atoms) | bars
 #define AQ_SMEM (1024 + 8 * AT_TILE + 256)
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(AT_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
                           const float* dsum, int T, int C, int NH, float scale, int* err) {
@@ -473,7 +510,8 @@ __global__ void __launch_bounds__(128, 1)
   const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = warp * 32 + lane, q = q0 + row;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int row = quarter * 32 + lane, q = q0 + row;
   const int nkb = qb + 1;
 
   if (tid == 0) {
@@ -488,7 +526,7 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tm = *tslot;
   const uint32_t tS = tm, tdP = tm + 128, tdQ = tm + 256;
-  const uint32_t lanebase = (uint32_t)(warp * 32) << 16;
+  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
   if (tid == 0) {
     mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
@@ -526,7 +564,8 @@ __global__ void __launch_bounds__(128, 1)
     const bool diag = kb == qb;
     const int k0 = kb * AT_BLK;
 #pragma unroll 1
-    for (int c = 0; c < 4; c++) {
+    for (int cc = 0; cc < 2; cc++) {
+      const int c = half * 2 + cc;
       uint32_t rs[32], rd[32];
       tmem_ld32(tS + lanebase + c * 32, rs);
       tmem_ld32(tdP + lanebase + c * 32, rd);
@@ -565,16 +604,15 @@ __global__ void __launch_bounds__(128, 1)
     __syncthreads();
     tc_fence_after();
   }
-  float v[64];
-#pragma unroll
-  for (int c = 0; c < 2; c++) {
+  float v[32];
+  {
     uint32_t r[32];
-    tmem_ld32(tdQ + lanebase + c * 32, r);
+    tmem_ld32(tdQ + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[c * 32 + j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
   }
-  if (q < T) store_row64_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS, v, scale);
+  if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
@@ -591,7 +629,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
   if (!make_tmap_btw(&tq, qkv, B, T, 3 * C)) { c.host_fail = 1; return; }
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
-  attn_fwd_tc_kernel<<<grid, 128, AF_SMEM, c.stream>>>(tq, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
+  attn_fwd_tc_kernel<<<grid, AT_THREADS, AF_SMEM, c.stream>>>(tq, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
   (*c.launches)++;
 }
 
@@ -614,9 +652,9 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
   const float scale = 1.f / sqrtf((float)AT_HS);
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AKV_SMEM);
-  attn_bwd_dkv_tc_kernel<<<grid, 128, AKV_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  attn_bwd_dkv_tc_kernel<<<grid, AT_THREADS, AKV_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
   (*c.launches)++;
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  attn_bwd_dq_tc_kernel<<<grid, 128, AQ_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  attn_bwd_dq_tc_kernel<<<grid, AT_THREADS, AQ_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
   (*c.launches)++;
 }

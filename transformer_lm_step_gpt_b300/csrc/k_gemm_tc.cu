@@ -1,27 +1,36 @@
 // k_gemm_tc.cu -- bf16 matmul on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
 //
 // out[m, n] = sum_k A(m,k) B(n,k), fp32 accumulation, the three layouts of a
-// Linear layer's forward (x W^T), data gradient (dy W) and weight gradient
-// (dy^T x) served by one kernel: each operand is either K-major or
-// M/N-major in global memory and is copied as-is by TMA into 128-byte-
-// swizzled shared memory, where the tcgen05 matrix descriptor states its
-// major-ness -- no transposed copies are ever made.
+// Linear layer (GeekNews, "Implementing the neural-network layers": a matrix
+// product plus a bias tiled over the rows): forward x W^T, data gradient
+// dy W, weight gradient dy^T x.  Each operand is K-major or M/N-major in
+// global memory and is copied as-is by TMA into 128-byte-swizzled shared
+// memory, where the tcgen05 matrix descriptor states its major-ness -- no
+// transposed copies are ever made.
 //
-// One CTA computes one 128 x BN output tile (BN = 128 or 256) over a range
-// of K (the whole K, or one split of it for the weight gradient):
-//   warp 0      TMA producer: a ring of STAGES shared-memory stages,
-//               64 K-elements per stage, full/empty mbarriers;
-//   warp 1      allocates BN TMEM columns, then one elected thread issues
-//               tcgen05.mma (M=128, N=BN, K=16, four per stage) and commits
-//               each stage back to the producer;
-//   warps 2..5  epilogue: tcgen05.ld 32 rows x 32 columns at a time from the
-//               warp's TMEM lane quarter, apply the fused epilogue (bias,
-//               GELU, residual, GELU backward, accumulate) and store.
-// Every mbarrier wait is bounded (see common.cuh); nothing traps.
+// Persistent kernel: one CTA per SM walks the output tiles (split, m-tile,
+// n-tile) of 128 x BN (BN = 128 or 256) in a grouped raster (GROUP_M m-tiles
+// per sweep over n, so concurrently resident tiles share operands in L2).
+//   warp 0      TMA producer: a ring of STAGES stages of 64 K-elements,
+//               full/empty mbarriers
+//   warp 1      allocates 2 x BN TMEM columns (two accumulators), one thread
+//               issues tcgen05.mma (M=128, N=BN, K=16) and commits each stage
+//               back to the producer and each finished tile to the epilogue
+//   warps 2..9  epilogue, overlapping the next tile's MMAs: warp w reads its
+//               TMEM lane quarter (w % 4: 32 rows) and column half
+//               ((w-2)/4), 32-row x 128-byte chunks at a time.  Every global
+//               byte of the epilogue moves by TMA: the chunk's auxiliary
+//               input (residual stream, pre-GELU activation) is TMA-loaded
+//               into a 128B-swizzled staging buffer, each thread (one row)
+//               applies the fused epilogue from registers, writes the result
+//               back into the staging buffer and one lane TMA-stores it (or
+//               TMA-reduce-adds it, for the weight gradient's dW += ...).
+// Every mbarrier wait is bounded (common.cuh); nothing traps.
 #include <cuda.h>
 
 #include <algorithm>
 #include <cstdio>
+#include <cstring>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -44,22 +53,30 @@ bool gemm_bf16_init() {
   return true;
 }
 
-// 2-D bf16 tensor [outer][inner] with row stride ld elements; box
-// {box_inner, box_outer}; 128-byte swizzle; out-of-range elements read 0.
-static bool make_tmap(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                      uint64_t ld, uint32_t box_inner, uint32_t box_outer) {
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+// 2-D tensor [outer][inner] (fp32 or bf16, row stride ld elements) or, with
+// d2 > 1, 3-D [d2][outer][inner] (plane stride outer*ld); box {box_inner,
+// box_outer, 1}; 128-byte swizzle; out-of-range reads are 0 and
+// out-of-range writes are dropped.
+static bool make_tmap(CUtensorMap* m, const void* base, bool f32, uint64_t inner, uint64_t outer,
+                      uint64_t ld, uint32_t box_inner, uint32_t box_outer, uint64_t d2 = 1) {
+  const uint64_t esz = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {inner, outer, d2};
+  cuuint64_t strides[2] = {ld * esz, outer * ld * esz};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  d2 > 1 ? 3 : 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 #define TC_BM 128
 #define TC_BK 64
+#define GROUP_M 8
+#define EPI_WARPS 8
+#define TC_THREADS (64 + 32 * EPI_WARPS)
+#define STG_BYTES 4096  // one epilogue chunk: 32 rows x 128 bytes, swizzled
 
 template <int BN>
 struct TcCfg {
@@ -67,132 +84,13 @@ struct TcCfg {
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;
   static constexpr uint32_t B_BYTES = BN * TC_BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;  // + align + barriers
+  static constexpr size_t STAGING = (size_t)EPI_WARPS * STG_BYTES;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING + 1024 + 256;
 };
 
 __host__ __device__ constexpr uint32_t tc_idesc(int N, bool a_mn, bool b_mn) {
   return tc_idesc_bf16(TC_BM, N, a_mn, b_mn);
 }
-
-__device__ __forceinline__ void store8_bf16(bf16* p, const float* v) {
-  uint4 u;
-  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
-  u.x = *reinterpret_cast<uint32_t*>(&t0);
-  u.y = *reinterpret_cast<uint32_t*>(&t1);
-  u.z = *reinterpret_cast<uint32_t*>(&t2);
-  u.w = *reinterpret_cast<uint32_t*>(&t3);
-  *reinterpret_cast<uint4*>(p) = u;
-}
-__device__ __forceinline__ void load8_bf16(const bf16* p, float* v) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; i++) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-    v[2 * i] = f.x;
-    v[2 * i + 1] = f.y;
-  }
-}
-
-// Epilogue for 8 consecutive columns n..n+7 of row m (all in range when
-// full8, else element-wise bounds).
-__device__ __forceinline__ void epi8(const GemmArgs& g, float* v, int m, int n, bool full8,
-                                     float* partial) {
-  const int64_t o = (int64_t)m * g.ldo + n;
-  if (partial) {  // split-K: raw partial sums, fp32, leading dimension N
-    float* p = partial + (int64_t)m * g.N + n;
-    if (full8) {
-      *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
-    } else {
-      for (int j = 0; j < 8; j++) if (n + j < g.N) p[j] = v[j];
-    }
-    return;
-  }
-  if (g.bias && g.epi != EPI_GELU_BWD && g.epi != EPI_ACCUM) {
-#pragma unroll
-    for (int j = 0; j < 8; j++) v[j] += (full8 || n + j < g.N) ? g.bias[n + j] : 0.f;
-  }
-  switch (g.epi) {
-    case EPI_STORE:
-      if (g.out_f32) {
-        float* p = static_cast<float*>(g.out) + o;
-        if (full8) {
-          *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
-          *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
-        } else {
-          for (int j = 0; j < 8; j++) if (n + j < g.N) p[j] = v[j];
-        }
-      } else {
-        bf16* p = static_cast<bf16*>(g.out) + o;
-        if (full8) store8_bf16(p, v);
-        else for (int j = 0; j < 8; j++) if (n + j < g.N) p[j] = __float2bfloat16_rn(v[j]);
-      }
-      break;
-    case EPI_BIAS_GELU: {
-      bf16* p = static_cast<bf16*>(g.out) + o;
-      bf16* q = static_cast<bf16*>(g.out2) + o;
-      float gv[8];
-#pragma unroll
-      for (int j = 0; j < 8; j++) gv[j] = gelu_f(v[j]);
-      if (full8) { store8_bf16(p, v); store8_bf16(q, gv); }
-      else for (int j = 0; j < 8; j++) if (n + j < g.N) { p[j] = __float2bfloat16_rn(v[j]); q[j] = __float2bfloat16_rn(gv[j]); }
-    } break;
-    case EPI_RESIDUAL: {
-      float* p = static_cast<float*>(g.out) + o;
-      const float* r = static_cast<const float*>(g.aux) + o;
-      if (full8) {
-        const float4 a = *reinterpret_cast<const float4*>(r);
-        const float4 b = *reinterpret_cast<const float4*>(r + 4);
-        *reinterpret_cast<float4*>(p) = make_float4(a.x + v[0], a.y + v[1], a.z + v[2], a.w + v[3]);
-        *reinterpret_cast<float4*>(p + 4) = make_float4(b.x + v[4], b.y + v[5], b.z + v[6], b.w + v[7]);
-      } else {
-        for (int j = 0; j < 8; j++) if (n + j < g.N) p[j] = r[j] + v[j];
-      }
-    } break;
-    case EPI_GELU_BWD: {
-      bf16* p = static_cast<bf16*>(g.out) + o;
-      const bf16* h = static_cast<const bf16*>(g.aux) + o;
-      if (full8) {
-        float hv[8];
-        load8_bf16(h, hv);
-#pragma unroll
-        for (int j = 0; j < 8; j++) v[j] *= gelu_grad_f(hv[j]);
-        store8_bf16(p, v);
-      } else {
-        for (int j = 0; j < 8; j++)
-          if (n + j < g.N) p[j] = __float2bfloat16_rn(v[j] * gelu_grad_f(__bfloat162float(h[j])));
-      }
-    } break;
-    case EPI_ACCUM: {
-      float* p = static_cast<float*>(g.out) + o;
-      if (full8) {
-        float4 a = *reinterpret_cast<float4*>(p);
-        float4 b = *reinterpret_cast<float4*>(p + 4);
-        a.x += v[0]; a.y += v[1]; a.z += v[2]; a.w += v[3];
-        b.x += v[4]; b.y += v[5]; b.z += v[6]; b.w += v[7];
-        *reinterpret_cast<float4*>(p) = a;
-        *reinterpret_cast<float4*>(p + 4) = b;
-      } else {
-        for (int j = 0; j < 8; j++) if (n + j < g.N) p[j] += v[j];
-      }
-    } break;
-  }
-}
-
-// Persistent kernel: one CTA per SM walks the output tiles (split, m-tile,
-// n-tile) in a grouped raster (GROUP_M m-tiles per column sweep, so the
-// concurrently resident tiles share A and B tiles in L2).  Two TMEM
-// accumulators let the epilogue of one tile run while the MMAs of the next
-// one are issued.
-//   warp 0      TMA producer (one thread)
-//   warp 1      TMEM allocation + MMA issuer (one thread)
-//   warps 2..9  epilogue: warp w reads TMEM lane quarter w % 4, column half
-//               (w - 2) / 4 of the tile
-#define GROUP_M 8
-#define EPI_WARPS 8
-#define TC_THREADS (64 + 32 * EPI_WARPS)
 
 struct TileCoord {
   int split, mt, nt;
@@ -211,19 +109,50 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int mtiles, int ntiles) {
   return c;
 }
 
+// Byte offset of 16-byte chunk c of row r in a 128B-swizzled staging buffer.
+__device__ __forceinline__ uint32_t stg_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void put8_bf16(uint8_t* p, const float* v) {
+  uint4 u;
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&t0);
+  u.y = *reinterpret_cast<uint32_t*>(&t1);
+  u.z = *reinterpret_cast<uint32_t*>(&t2);
+  u.w = *reinterpret_cast<uint32_t*>(&t3);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+__device__ __forceinline__ void get8_bf16(const uint8_t* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+struct EpiMaps {
+  CUtensorMap out, out2, aux;
+};
+
 template <int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   GemmArgs g, int k_tiles, int k_per_split, int splits, float* partial, int* err) {
+                   const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
+                   int splits, int* err) {
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * Cfg::STAGE_BYTES);
+  uint8_t* staging = smem + (size_t)S * Cfg::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + Cfg::STAGING);
   uint64_t* empty = full + S;
-  uint64_t* acc_full = empty + S;   // [2]
+  uint64_t* acc_full = empty + S;      // [2]
   uint64_t* acc_empty = acc_full + 2;  // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  uint64_t* aux_bar = acc_empty + 2;   // [EPI_WARPS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + EPI_WARPS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int mtiles = (g.M + TC_BM - 1) / TC_BM, ntiles = (g.N + BN - 1) / BN;
@@ -232,6 +161,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], EPI_WARPS); }
+    for (int w = 0; w < EPI_WARPS; w++) mbar_init(&aux_bar[w], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -307,30 +237,123 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
     }
   } else {
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
+    uint8_t* stg = staging + (size_t)ew * STG_BYTES;
+    uint64_t* abar = &aux_bar[ew];
+    const bool split = splits > 1;
+    const int epi = g.epi;
+    const bool f32 = split || epi == EPI_RESIDUAL || epi == EPI_ACCUM || (epi == EPI_STORE && g.out_f32);
+    const bool has_aux = !split && (epi == EPI_RESIDUAL || epi == EPI_GELU_BWD);
+    const bool use_bias = !split && g.bias && (epi == EPI_STORE || epi == EPI_BIAS_GELU || epi == EPI_RESIDUAL);
+    const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
+    uint32_t aux_phase = 0;
     int ti = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
       const TileCoord tc = tile_coord(t, mtiles, ntiles);
       const int m0 = tc.mt * TC_BM, n0 = tc.nt * BN;
       const int a = ti & 1;
+      const int mrow = m0 + quarter * 32;
       mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
       tc_fence_after();
-      const int m = m0 + quarter * 32 + lane;
-      float* part = partial ? partial + (size_t)tc.split * (size_t)g.M * (size_t)g.N : nullptr;
 #pragma unroll 1
-      for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cc, r);
-        tmem_ld_wait();
-        if (m < g.M && n0 + cc < g.N) {
+      for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += CW) {
+        const int ncol = n0 + cc;
+        if (ncol >= g.N) break;
+        if (lane == 0) bulk_wait_read0();  // staging no longer read by earlier stores
+        __syncwarp();
+        if (has_aux && lane == 0) {
+          mbar_arrive_expect_tx(abar, STG_BYTES);
+          tma_load_2d(stg, &em.aux, abar, ncol, mrow);
+        }
+        float v[64];
+        const uint32_t taddr = tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cc;
+        {
+          uint32_t r[32];
+          tmem_ld32(taddr, r);
+          tmem_ld_wait();
 #pragma unroll
-          for (int j0 = 0; j0 < 32; j0 += 8) {
-            const int n = n0 + cc + j0;
-            if (n >= g.N) break;
-            float v[8];
+          for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+          if (!f32) {
+            tmem_ld32(taddr + 32, r);
+            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 8; j++) v[j] = __uint_as_float(r[j0 + j]);
-            epi8(g, v, m, n, n + 8 <= g.N, part);
+            for (int j = 0; j < 32; j++) v[32 + j] = __uint_as_float(r[j]);
+          } else {
+#pragma unroll
+            for (int j = 32; j < 64; j++) v[j] = 0.f;
+          }
+        }
+        if (use_bias) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            if (j < CW) {
+              const int n = ncol + j;
+              if (n + 4 <= g.N) {
+                const float4 bb = *reinterpret_cast<const float4*>(g.bias + n);
+                v[j] += bb.x; v[j + 1] += bb.y; v[j + 2] += bb.z; v[j + 3] += bb.w;
+              } else {
+                for (int q = 0; q < 4; q++) if (n + q < g.N) v[j + q] += g.bias[n + q];
+              }
+            }
+          }
+        }
+        if (has_aux) {
+          mbar_wait(abar, aux_phase, err);
+          aux_phase ^= 1u;
+        }
+        // results (and the auxiliary input) in the thread's staging row
+        if (f32) {
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            float4* p = reinterpret_cast<float4*>(stg + stg_off(lane, c));
+            float4 o = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            if (has_aux) {  // EPI_RESIDUAL: out = residual + (acc + bias)
+              const float4 r = *p;
+              o.x = r.x + o.x; o.y = r.y + o.y; o.z = r.z + o.z; o.w = r.w + o.w;
+            }
+            *p = o;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            uint8_t* p = stg + stg_off(lane, c);
+            float o[8];
+            if (has_aux) {  // EPI_GELU_BWD: out = acc * gelu'(pre-activation)
+              float hv[8];
+              get8_bf16(p, hv);
+#pragma unroll
+              for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * gelu_grad_hw(hv[q]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
+            }
+            put8_bf16(p, o);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (split) tma_store_3d(&em.out, stg, ncol, mrow, tc.split);
+          else if (epi == EPI_ACCUM) tma_reduce_add_2d(&em.out, stg, ncol, mrow);
+          else tma_store_2d(&em.out, stg, ncol, mrow);
+          bulk_commit();
+        }
+        if (epi == EPI_BIAS_GELU && !split) {  // second output: gelu(pre-activation)
+          if (lane == 0) bulk_wait_read0();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; c++) {
+            float o[8];
+#pragma unroll
+            for (int q = 0; q < 8; q++) o[q] = gelu_hw(v[8 * c + q]);
+            put8_bf16(stg + stg_off(lane, c), o);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&em.out2, stg, ncol, mrow);
+            bulk_commit();
           }
         }
       }
@@ -338,6 +361,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
     }
+    if (lane == 0) bulk_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -371,24 +395,35 @@ __global__ void splitk_reduce_kernel(float* out, int64_t ldo, const float* parti
 template <int BN, bool A_K, bool B_K>
 static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partial) {
   CUtensorMap ta, tb;
+  EpiMaps em;
+  memset(&em, 0, sizeof(em));
   bool ok;
-  if (A_K) ok = make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, TC_BM);
-  else ok = make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64);
-  if (B_K) ok = ok && make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN);
-  else ok = ok && make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64);
+  if (A_K) ok = make_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, TC_BM);
+  else ok = make_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
+  if (B_K) ok = ok && make_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, BN);
+  else ok = ok && make_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64);
+  const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
+  const int kps = (k_tiles + splits - 1) / splits;
+  const int zs = (k_tiles + kps - 1) / kps;
+  if (zs > 1) {
+    ok = ok && make_tmap(&em.out, partial, true, g.N, g.M, g.N, 32, 32, zs);
+  } else {
+    const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
+    ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
+    if (g.epi == EPI_BIAS_GELU) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
+    if (g.epi == EPI_GELU_BWD) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+  }
   if (!ok) {
     fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
     c.host_fail = 1;
     return;
   }
-  const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
-  const int kps = (k_tiles + splits - 1) / splits;
-  const int zs = (k_tiles + kps - 1) / kps;
   const int tiles = zs * ((g.N + BN - 1) / BN) * ((g.M + TC_BM - 1) / TC_BM);
   const int grid = std::min(tiles, c.num_sms);
   auto kern = gemm_tc_kernel<BN, A_K, B_K>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM);
-  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, c.stream>>>(ta, tb, g, k_tiles, kps, zs, zs > 1 ? partial : nullptr, c.err);
+  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, c.stream>>>(ta, tb, em, g, k_tiles, kps, zs, c.err);
   (*c.launches)++;
   if (zs > 1) {
     const int64_t n4 = (int64_t)g.M * g.N / 4;
