@@ -51,13 +51,13 @@ static EncodeTiledFnA encoder_fn() {
   return fn;
 }
 
-// [B][T][W] bf16 tensor, box {64, 128, 1}, 128-byte swizzle, rows past T zero.
-static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W) {
+// [B][T][W] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, rows past T zero.
+static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows = 128) {
   EncodeTiledFnA f = encoder_fn();
   if (!f) return false;
   cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)B};
   cuuint64_t strides[2] = {(cuuint64_t)W * 2, (cuuint64_t)T * W * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -328,72 +328,80 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 }
 
 // ============================================================ backward: dK, dV
-// smem: K | V | Q0 Q1 | dO0 dO1 | P^T (2 atoms) | dS^T (2 atoms) | lse[128] D[128] | bars
-#define AKV_SMEM (1024 + 10 * AT_TILE + 1024 + 256)
+// One CTA per (128-key block, b*h); the queries are walked in 64-row
+// sub-blocks so that a CTA needs 256 TMEM columns and ~97 KB of shared
+// memory and two CTAs share an SM (one's MMAs overlap the other's
+// elementwise work).
+// smem: K | V | Q0 Q1 | dO0 dO1 (64-row tiles) | P^T | dS^T ([128 x 64]) |
+//       lse[64] D[64] | barriers
+#define AB_SUB 64
+#define AT_SUBTILE 8192u  // bytes of one [64 x 64] bf16 tile
+#define AKV_SMEM (1024 + 2 * AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 512 + 256)
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(AT_THREADS, 2)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                           const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
+                           const __grid_constant__ CUtensorMap tm_qkv64,
+                           const __grid_constant__ CUtensorMap tm_dy64, bf16* dqkv, const float* lse,
                            const float* dsum, int T, int C, int NH, float scale, int* err) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sK = sm;
   uint8_t* sV = sm + AT_TILE;
-  uint8_t* sQ = sm + 2 * AT_TILE;   // 2 stages
-  uint8_t* sD = sm + 4 * AT_TILE;   // dO, 2 stages
-  uint8_t* sP = sm + 6 * AT_TILE;   // P^T, 2 atoms
-  uint8_t* sS = sm + 8 * AT_TILE;   // dS^T, 2 atoms
-  float* sl = reinterpret_cast<float*>(sm + 10 * AT_TILE);  // lse[128] (log2 units)
-  float* sdd = sl + 128;                                   // D[128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 10 * AT_TILE + 1024);
+  uint8_t* sQ = sm + 2 * AT_TILE;                   // 2 stages of [64 x 64]
+  uint8_t* sD = sQ + 2 * AT_SUBTILE;                // dO, 2 stages
+  uint8_t* sP = sD + 2 * AT_SUBTILE;                // P^T  [128 keys x 64 queries]
+  uint8_t* sS = sP + AT_TILE;                       // dS^T [128 keys x 64 queries]
+  float* sl = reinterpret_cast<float*>(sS + AT_TILE);  // lse[64] (log2 units)
+  float* sdd = sl + 64;                                 // D[64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + AT_TILE + 512);
   uint64_t* kv_full = bars;
   uint64_t* q_full = bars + 1;  // [2]
   uint64_t* s_done = bars + 3;
   uint64_t* o_done = bars + 4;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
 
-  const int nb = gridDim.x;
-  const int kb = blockIdx.x;  // key block
+  const int kb = (int)gridDim.x - 1 - (int)blockIdx.x;  // key block; longest first
   const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
   const int k0 = kb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int row = quarter * 32 + lane, key = k0 + row;
-  const int nq = nb - kb;  // query blocks kb .. nb-1
+  const int nsub = (T - k0 + AB_SUB - 1) / AB_SUB;  // 64-query sub-blocks from k0 to T
 
   if (tid == 0) {
     for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
-    tma_prefetch_desc(&tm_dy);
+    tma_prefetch_desc(&tm_qkv64);
+    tma_prefetch_desc(&tm_dy64);
   }
-  if (warp == 0) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  const uint32_t tS = tm, tdP = tm + 128, tdV = tm + 256, tdK = tm + 320;
+  const uint32_t tS = tm, tdP = tm + 64, tdV = tm + 128, tdK = tm + 192;
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
   if (tid == 0) {
     mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
     tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, k0, b);
     tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, k0, b);
-    for (int s = 0; s < 2 && s < nq; s++) {
-      mbar_arrive_expect_tx(&q_full[s], 2 * AT_TILE);
-      tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &q_full[s], h * AT_HS, (kb + s) * AT_BLK, b);
-      tma_load_3d(sD + s * AT_TILE, &tm_dy, &q_full[s], h * AT_HS, (kb + s) * AT_BLK, b);
+    for (int s = 0; s < 2 && s < nsub; s++) {
+      mbar_arrive_expect_tx(&q_full[s], 2 * AT_SUBTILE);
+      tma_load_3d(sQ + s * AT_SUBTILE, &tm_qkv64, &q_full[s], h * AT_HS, k0 + s * AB_SUB, b);
+      tma_load_3d(sD + s * AT_SUBTILE, &tm_dy64, &q_full[s], h * AT_HS, k0 + s * AB_SUB, b);
     }
   }
   const float sl2 = scale * 1.4426950408889634f;
-  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
   const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
-  for (int it = 0; it < nq; it++) {
-    const int qb = kb + it, q0 = qb * AT_BLK;
+  for (int it = 0; it < nsub; it++) {
+    const int q0 = k0 + it * AB_SUB;
     const int st = it & 1;
     const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-    if (tid < 128) {  // this query block's lse (log2 units) and D
+    if (tid < AB_SUB) {  // this sub-block's lse (log2 units) and D
       const int qq = q0 + tid;
       sl[tid] = qq < T ? lse[(int64_t)bh * T + qq] * 1.4426950408889634f : INFINITY;
       sdd[tid] = qq < T ? dsum[(int64_t)bh * T + qq] : 0.f;
@@ -403,37 +411,35 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       mbar_wait(&q_full[st], ph, err);
       tc_fence_after();
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      const uint32_t bQ = smem_u32(sQ + st * AT_TILE), bD = smem_u32(sD + st * AT_TILE);
+      const uint32_t bQ = smem_u32(sQ + st * AT_SUBTILE), bD = smem_u32(sD + st * AT_SUBTILE);
 #pragma unroll
       for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
       tc_commit(s_done);
     }
-    __syncthreads();  // lse / D of this block visible
+    __syncthreads();  // lse / D of this sub-block visible
     mbar_wait(s_done, (uint32_t)it & 1u, err);
     tc_fence_after();
-    const bool diag = it == 0;
-#pragma unroll 1
-    for (int cc = 0; cc < 2; cc++) {
-      const int c = half * 2 + cc;
+    const bool diag = q0 < k0 + AT_BLK;
+    {
       uint32_t rs[32], rd[32];
-      tmem_ld32(tS + lanebase + c * 32, rs);
-      tmem_ld32(tdP + lanebase + c * 32, rd);
+      tmem_ld32(tS + lanebase + half * 32, rs);
+      tmem_ld32(tdP + lanebase + half * 32, rd);
       tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; g++) {
         float p[8], ds[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-          const int qc = c * 32 + g * 8 + j;
+          const int qc = half * 32 + g * 8 + j;
           const bool ok = !diag || q0 + qc >= key;
           const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - sl[qc]) : 0.f;
           p[j] = pv;
           ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - sdd[qc]);
         }
-        st_swz8(sP, row, c * 4 + g, p);
-        st_swz8(sS, row, c * 4 + g, ds);
+        st_swz8(sP, row, half * 4 + g, p);
+        st_swz8(sS, row, half * 4 + g, ds);
       }
     }
     fence_proxy_async_smem();
@@ -442,19 +448,19 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     if (tid == 0) {
       tc_fence_after();
       const uint32_t aP = smem_u32(sP), aS = smem_u32(sS);
-      const uint32_t bQ = smem_u32(sQ + st * AT_TILE), bD = smem_u32(sD + st * AT_TILE);
+      const uint32_t bQ = smem_u32(sQ + st * AT_SUBTILE), bD = smem_u32(sD + st * AT_SUBTILE);
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdV, kmaj2(aP, kk), mnmaj(bD, kk), idO, (it > 0 || kk > 0));
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdV, kmaj(aP, kk), mnmaj(bD, kk), idO, (it > 0 || kk > 0));
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdK, kmaj2(aS, kk), mnmaj(bQ, kk), idO, (it > 0 || kk > 0));
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdK, kmaj(aS, kk), mnmaj(bQ, kk), idO, (it > 0 || kk > 0));
       tc_commit(o_done);
     }
     mbar_wait(o_done, (uint32_t)it & 1u, err);
     tc_fence_after();
-    if (tid == 0 && it + 2 < nq) {
-      mbar_arrive_expect_tx(&q_full[st], 2 * AT_TILE);
-      tma_load_3d(sQ + st * AT_TILE, &tm_qkv, &q_full[st], h * AT_HS, (qb + 2) * AT_BLK, b);
-      tma_load_3d(sD + st * AT_TILE, &tm_dy, &q_full[st], h * AT_HS, (qb + 2) * AT_BLK, b);
+    if (tid == 0 && it + 2 < nsub) {
+      mbar_arrive_expect_tx(&q_full[st], 2 * AT_SUBTILE);
+      tma_load_3d(sQ + st * AT_SUBTILE, &tm_qkv64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
+      tma_load_3d(sD + st * AT_SUBTILE, &tm_dy64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
     }
     tc_fence_before();
     __syncthreads();
@@ -480,25 +486,28 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
 }
 
 // ============================================================ backward: dQ
-// smem: Q | dO | K0 K1 | V0 V1 | dS (2 atoms) | bars
-#define AQ_SMEM (1024 + 8 * AT_TILE + 256)
+// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks
+// (256 TMEM columns, ~81 KB shared memory: two CTAs per SM).
+// smem: Q | dO | K0 K1 | V0 V1 (64-row tiles) | dS ([128 x 64]) | barriers
+#define AQ_SMEM (1024 + 2 * AT_TILE + 4 * AT_SUBTILE + AT_TILE + 256)
 
-__global__ void __launch_bounds__(AT_THREADS, 1)
+__global__ void __launch_bounds__(AT_THREADS, 2)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                          const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
+                          const __grid_constant__ CUtensorMap tm_dy,
+                          const __grid_constant__ CUtensorMap tm_qkv64, bf16* dqkv, const float* lse,
                           const float* dsum, int T, int C, int NH, float scale, int* err) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
   uint8_t* sD = sm + AT_TILE;
-  uint8_t* sK = sm + 2 * AT_TILE;  // 2 stages
-  uint8_t* sV = sm + 4 * AT_TILE;  // 2 stages
-  uint8_t* sS = sm + 6 * AT_TILE;  // dS, 2 atoms
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 8 * AT_TILE);
+  uint8_t* sK = sm + 2 * AT_TILE;    // 2 stages of [64 x 64]
+  uint8_t* sV = sK + 2 * AT_SUBTILE; // 2 stages
+  uint8_t* sS = sV + 2 * AT_SUBTILE; // dS [128 queries x 64 keys]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + AT_TILE);
   uint64_t* q_full = bars;
   uint64_t* kv_full = bars + 1;  // [2]
   uint64_t* s_done = bars + 3;
@@ -512,47 +521,49 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int row = quarter * 32 + lane, q = q0 + row;
-  const int nkb = qb + 1;
+  const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
 
   if (tid == 0) {
     for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_dy);
+    tma_prefetch_desc(&tm_qkv64);
   }
-  if (warp == 0) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  const uint32_t tS = tm, tdP = tm + 128, tdQ = tm + 256;
+  const uint32_t tS = tm, tdP = tm + 64, tdQ = tm + 128;
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
   if (tid == 0) {
     mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
     tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
     tma_load_3d(sD, &tm_dy, q_full, h * AT_HS, q0, b);
-    for (int s = 0; s < 2 && s < nkb; s++) {
-      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_TILE);
-      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &kv_full[s], C + h * AT_HS, s * AT_BLK, b);
-      tma_load_3d(sV + s * AT_TILE, &tm_qkv, &kv_full[s], 2 * C + h * AT_HS, s * AT_BLK, b);
+    for (int s = 0; s < 2 && s < nsub; s++) {
+      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_SUBTILE);
+      tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &kv_full[s], C + h * AT_HS, s * AB_SUB, b);
+      tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &kv_full[s], 2 * C + h * AT_HS, s * AB_SUB, b);
     }
   }
   const float sl2 = scale * 1.4426950408889634f;
   const float my_lse = q < T ? lse[(int64_t)bh * T + q] * 1.4426950408889634f : INFINITY;
   const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
-  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
   const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
-  for (int kb = 0; kb < nkb; kb++) {
+  for (int kb = 0; kb < nsub; kb++) {
     const int st = kb & 1;
     const uint32_t ph = (uint32_t)(kb >> 1) & 1u;
+    const int k0 = kb * AB_SUB;
     if (tid == 0) {
       if (kb == 0) mbar_wait(q_full, 0, err);
       mbar_wait(&kv_full[st], ph, err);
       tc_fence_after();
       const uint32_t aQ = smem_u32(sQ), aD = smem_u32(sD);
-      const uint32_t bK = smem_u32(sK + st * AT_TILE), bV = smem_u32(sV + st * AT_TILE);
+      const uint32_t bK = smem_u32(sK + st * AT_SUBTILE), bV = smem_u32(sV + st * AT_SUBTILE);
 #pragma unroll
       for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
 #pragma unroll
@@ -561,26 +572,23 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     }
     mbar_wait(s_done, (uint32_t)kb & 1u, err);
     tc_fence_after();
-    const bool diag = kb == qb;
-    const int k0 = kb * AT_BLK;
-#pragma unroll 1
-    for (int cc = 0; cc < 2; cc++) {
-      const int c = half * 2 + cc;
+    const bool diag = k0 + AB_SUB > q0;
+    {
       uint32_t rs[32], rd[32];
-      tmem_ld32(tS + lanebase + c * 32, rs);
-      tmem_ld32(tdP + lanebase + c * 32, rd);
+      tmem_ld32(tS + lanebase + half * 32, rs);
+      tmem_ld32(tdP + lanebase + half * 32, rd);
       tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; g++) {
         float ds[8];
 #pragma unroll
         for (int j = 0; j < 8; j++) {
-          const int kc = c * 32 + g * 8 + j;
+          const int kc = half * 32 + g * 8 + j;
           const bool ok = !diag || k0 + kc <= q;
           const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - my_lse) : 0.f;
           ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - my_d);
         }
-        st_swz8(sS, row, c * 4 + g, ds);
+        st_swz8(sS, row, half * 4 + g, ds);
       }
     }
     fence_proxy_async_smem();
@@ -588,17 +596,17 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t aS = smem_u32(sS), bK = smem_u32(sK + st * AT_TILE);
+      const uint32_t aS = smem_u32(sS), bK = smem_u32(sK + st * AT_SUBTILE);
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tdQ, kmaj2(aS, kk), mnmaj(bK, kk), idO, (kb > 0 || kk > 0));
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdQ, kmaj(aS, kk), mnmaj(bK, kk), idO, (kb > 0 || kk > 0));
       tc_commit(o_done);
     }
     mbar_wait(o_done, (uint32_t)kb & 1u, err);
     tc_fence_after();
-    if (tid == 0 && kb + 2 < nkb) {
-      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_TILE);
-      tma_load_3d(sK + st * AT_TILE, &tm_qkv, &kv_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
-      tma_load_3d(sV + st * AT_TILE, &tm_qkv, &kv_full[st], 2 * C + h * AT_HS, (kb + 2) * AT_BLK, b);
+    if (tid == 0 && kb + 2 < nsub) {
+      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_SUBTILE);
+      tma_load_3d(sK + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], C + h * AT_HS, k0 + 2 * AB_SUB, b);
+      tma_load_3d(sV + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], 2 * C + h * AT_HS, k0 + 2 * AB_SUB, b);
     }
     tc_fence_before();
     __syncthreads();
@@ -615,7 +623,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 512); }
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
 }
 
 // ============================================================ launchers
@@ -640,8 +648,9 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
     launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
     return;
   }
-  CUtensorMap tq, td;
-  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C)) {
+  CUtensorMap tq, td, tq64, td64;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C) ||
+      !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB) || !make_tmap_btw(&td64, dy, B, T, C, AB_SUB)) {
     c.host_fail = 1;
     return;
   }
@@ -652,9 +661,9 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
   const float scale = 1.f / sqrtf((float)AT_HS);
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AKV_SMEM);
-  attn_bwd_dkv_tc_kernel<<<grid, AT_THREADS, AKV_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  attn_bwd_dkv_tc_kernel<<<grid, AT_THREADS, AKV_SMEM, c.stream>>>(tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
   (*c.launches)++;
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  attn_bwd_dq_tc_kernel<<<grid, AT_THREADS, AQ_SMEM, c.stream>>>(tq, td, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  attn_bwd_dq_tc_kernel<<<grid, AT_THREADS, AQ_SMEM, c.stream>>>(tq, td, tq64, dqkv, lse, dsum, T, C, NH, scale, c.err);
   (*c.launches)++;
 }

@@ -308,24 +308,32 @@ template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, cons
                                          const float*, const float*, int, int);
 
 #define LNB_WARPS 8
-#define LNB_ROWS 64  // rows per block (8 per warp)
+#define LNB_ROWS 32  // rows per block (4 per warp)
 
 int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS) * 3 * C; }
 
-// One warp per row; gamma/beta gradient partials (and, when asked, the column
-// sums of the updated residual gradient) per warp in shared memory, combined
-// over the block's warps in warp order into one partial per block.
-template <typename ActT>
-__global__ void layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
-                                     const float* inp, const float* w, const float* mean,
-                                     const float* rstd, int N, int C, int accumulate) {
-  extern __shared__ float sm[];  // [LNB_WARPS][3][C]
+// One warp per row.  Each lane owns the float4 column chunks lane, lane+32,
+// ... (NCH = C/128 of them) and keeps its gamma / beta / residual-gradient
+// column partials in registers across the warp's rows; at the end the warps'
+// partials are summed in warp order through shared memory into one partial
+// per block (a single [3][C] buffer that the warps add into one after the
+// other, so little shared memory is taken from L1).  Pass 1 reads x and dy
+// for the two row sums (and prefetches the old residual gradient), pass 2
+// re-reads x and dy (L1 hits) to form dx.
+template <typename ActT, int NCH>
+__global__ void __launch_bounds__(LNB_WARPS * 32)
+    layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
+                         const float* inp, const float* w, const float* mean, const float* rstd,
+                         int N, int C, int accumulate) {
+  extern __shared__ float sm[];  // [3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sdw = sm + (int64_t)warp * 3 * C;
-  float* sdb = sdw + C;
-  float* sdr = sdb + C;
-  for (int c = lane; c < C; c += 32) { sdw[c] = 0.f; sdb[c] = 0.f; sdr[c] = 0.f; }
-  __syncwarp();
+  float4 pw[NCH], pb[NCH], pr[NCH], old[NCH];
+#pragma unroll
+  for (int k = 0; k < NCH; k++) {
+    pw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pb[k] = pw[k];
+    pr[k] = pw[k];
+  }
   const int row0 = blockIdx.x * LNB_ROWS + warp * (LNB_ROWS / LNB_WARPS);
   for (int rr = 0; rr < LNB_ROWS / LNB_WARPS; rr++) {
     const int row = row0 + rr;
@@ -333,59 +341,104 @@ __global__ void layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial
     const float* x = inp + (int64_t)row * C;
     const float* g = dy + (int64_t)row * C;
     const float m = mean[row], r = rstd[row];
+    float* dr = dres + (int64_t)row * C;
     float s1 = 0.f, s2 = 0.f;
-    for (int c = lane * 4; c < C; c += 128) {
-      const float4 xv = *reinterpret_cast<const float4*>(x + c);
-      const float4 gv = *reinterpret_cast<const float4*>(g + c);
-      const float4 wv = *reinterpret_cast<const float4*>(w + c);
-      const float h0 = gv.x * wv.x, h1 = gv.y * wv.y, h2 = gv.z * wv.z, h3 = gv.w * wv.w;
-      s1 += (h0 + h1) + (h2 + h3);
-      s2 += (h0 * (xv.x - m) * r + h1 * (xv.y - m) * r) + (h2 * (xv.z - m) * r + h3 * (xv.w - m) * r);
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+      const int c = (lane + 32 * k) * 4;
+      old[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (c < C) {
+        if (accumulate) old[k] = *reinterpret_cast<const float4*>(dr + c);
+        const float4 xv = *reinterpret_cast<const float4*>(x + c);
+        const float4 gv = *reinterpret_cast<const float4*>(g + c);
+        const float4 wv = *reinterpret_cast<const float4*>(w + c);
+        const float h0 = gv.x * wv.x, h1 = gv.y * wv.y, h2 = gv.z * wv.z, h3 = gv.w * wv.w;
+        s1 += (h0 + h1) + (h2 + h3);
+        s2 += (h0 * (xv.x - m) * r + h1 * (xv.y - m) * r) + (h2 * (xv.z - m) * r + h3 * (xv.w - m) * r);
+      }
     }
     const float mg = warp_sum(s1) / (float)C;
     const float mgx = warp_sum(s2) / (float)C;
-    float* dr = dres + (int64_t)row * C;
-    for (int c = lane * 4; c < C; c += 128) {
-      const float4 xv = *reinterpret_cast<const float4*>(x + c);
-      const float4 gv = *reinterpret_cast<const float4*>(g + c);
-      const float4 wv = *reinterpret_cast<const float4*>(w + c);
-      const float x0 = (xv.x - m) * r, x1 = (xv.y - m) * r, x2 = (xv.z - m) * r, x3 = (xv.w - m) * r;
-      float4 d;
-      d.x = r * (gv.x * wv.x - mg - x0 * mgx);
-      d.y = r * (gv.y * wv.y - mg - x1 * mgx);
-      d.z = r * (gv.z * wv.z - mg - x2 * mgx);
-      d.w = r * (gv.w * wv.w - mg - x3 * mgx);
-      if (accumulate) {
-        const float4 o = *reinterpret_cast<const float4*>(dr + c);
-        d.x += o.x; d.y += o.y; d.z += o.z; d.w += o.w;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C) {
+        const float4 xv = *reinterpret_cast<const float4*>(x + c);
+        const float4 gv = *reinterpret_cast<const float4*>(g + c);
+        const float4 wv = *reinterpret_cast<const float4*>(w + c);
+        const float x0 = (xv.x - m) * r, x1 = (xv.y - m) * r, x2 = (xv.z - m) * r, x3 = (xv.w - m) * r;
+        float4 d;
+        d.x = r * (gv.x * wv.x - mg - x0 * mgx);
+        d.y = r * (gv.y * wv.y - mg - x1 * mgx);
+        d.z = r * (gv.z * wv.z - mg - x2 * mgx);
+        d.w = r * (gv.w * wv.w - mg - x3 * mgx);
+        d.x += old[k].x; d.y += old[k].y; d.z += old[k].z; d.w += old[k].w;
+        *reinterpret_cast<float4*>(dr + c) = d;
+        if (dres_act) store4<ActT>(dres_act + (int64_t)row * C + c, d.x, d.y, d.z, d.w);
+        pw[k].x += gv.x * x0; pw[k].y += gv.y * x1; pw[k].z += gv.z * x2; pw[k].w += gv.w * x3;
+        pb[k].x += gv.x; pb[k].y += gv.y; pb[k].z += gv.z; pb[k].w += gv.w;
+        pr[k].x += d.x; pr[k].y += d.y; pr[k].z += d.z; pr[k].w += d.w;
       }
-      *reinterpret_cast<float4*>(dr + c) = d;
-      if (dres_act) store4<ActT>(dres_act + (int64_t)row * C + c, d.x, d.y, d.z, d.w);
-      sdw[c] += gv.x * x0; sdw[c + 1] += gv.y * x1; sdw[c + 2] += gv.z * x2; sdw[c + 3] += gv.w * x3;
-      sdb[c] += gv.x; sdb[c + 1] += gv.y; sdb[c + 2] += gv.z; sdb[c + 3] += gv.w;
-      sdr[c] += d.x; sdr[c + 1] += d.y; sdr[c + 2] += d.z; sdr[c + 3] += d.w;
     }
   }
-  __syncthreads();
+  for (int wv = 0; wv < LNB_WARPS; wv++) {  // warp order
+    if (warp == wv) {
+#pragma unroll
+      for (int k = 0; k < NCH; k++) {
+        const int c = (lane + 32 * k) * 4;
+        if (c < C) {
+          float4* a = reinterpret_cast<float4*>(sm + c);
+          float4* bq = reinterpret_cast<float4*>(sm + C + c);
+          float4* rq = reinterpret_cast<float4*>(sm + 2 * C + c);
+          if (wv == 0) { *a = pw[k]; *bq = pb[k]; *rq = pr[k]; }
+          else {
+            float4 t = *a; t.x += pw[k].x; t.y += pw[k].y; t.z += pw[k].z; t.w += pw[k].w; *a = t;
+            t = *bq; t.x += pb[k].x; t.y += pb[k].y; t.z += pb[k].z; t.w += pb[k].w; *bq = t;
+            t = *rq; t.x += pr[k].x; t.y += pr[k].y; t.z += pr[k].z; t.w += pr[k].w; *rq = t;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
   float* out = partial + (int64_t)blockIdx.x * 3 * C;
-  for (int c = threadIdx.x; c < 3 * C; c += blockDim.x) {
-    float s = 0.f;
-    for (int wv = 0; wv < LNB_WARPS; wv++) s += sm[(int64_t)wv * 3 * C + c];
-    out[c] = s;
+  for (int c = threadIdx.x; c < 3 * C; c += blockDim.x) out[c] = sm[c];
+}
+
+// Sum nb partial rows of width W = parts * seg and add segment i into
+// d[i][0:seg] (a null d[i] is skipped).  Block: 32 columns x 32 row groups;
+// group g sums rows g, g+32, ... in order, then the 32 group sums are added
+// in group order (a fixed order: the result repeats bit for bit).
+#define RP_COLS 32
+#define RP_GROUPS 32
+__global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
+    reduce_partials_kernel(float* d0, float* d1, float* d2, const float* partial, int nb, int W, int seg) {
+  __shared__ float sm[RP_GROUPS][RP_COLS + 1];
+  const int lane = threadIdx.x % RP_COLS, grp = threadIdx.x / RP_COLS;
+  const int c = blockIdx.x * RP_COLS + lane;
+  float s = 0.f;
+  if (c < W)
+    for (int b = grp; b < nb; b += RP_GROUPS) s += partial[(int64_t)b * W + c];
+  sm[grp][lane] = s;
+  __syncthreads();
+  if (grp == 0 && c < W) {
+    float* d = c < seg ? d0 : (c < 2 * seg ? d1 : d2);
+    if (!d) return;
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < RP_GROUPS; q++) t += sm[q][lane];
+    d[c % seg] += t;
   }
 }
 
-// Sum nb partial rows of width W = parts * seg in row order and add segment
-// i into d[i][0:seg] (a null d[i] is skipped).
-__global__ void reduce_partials_kernel(float* d0, float* d1, float* d2, const float* partial, int nb,
-                                       int W, int seg) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= W) return;
-  float* d = c < seg ? d0 : (c < 2 * seg ? d1 : d2);
-  if (!d) return;
-  float s = 0.f;
-  for (int b = 0; b < nb; b++) s += partial[(int64_t)b * W + c];
-  d[c % seg] += s;
+template <typename ActT, int NCH>
+static void ln_bwd_launch(LaunchCtx& c, int nb, size_t smem, float* dres, ActT* dres_act, float* partial,
+                          const float* dy, const float* inp, const float* w, const float* mean,
+                          const float* rstd, int N, int C, bool accumulate) {
+  cudaFuncSetAttribute(layernorm_bwd_kernel<ActT, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  layernorm_bwd_kernel<ActT, NCH><<<nb, LNB_WARPS * 32, smem, c.stream>>>(
+      dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
 }
 
 template <typename ActT>
@@ -394,14 +447,21 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial) {
   const int nb = cdiv(N, LNB_ROWS);
-  const size_t smem = (size_t)LNB_WARPS * 3 * C * sizeof(float);
-  cudaFuncSetAttribute(layernorm_bwd_kernel<ActT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem);
-  layernorm_bwd_kernel<ActT><<<nb, LNB_WARPS * 32, smem, c.stream>>>(
-      dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
+  const size_t smem = (size_t)3 * C * sizeof(float);
+  const int nch = (C + 127) / 128;  // C <= 1024 keeps the partials in registers
+  switch (nch) {
+    case 1: ln_bwd_launch<ActT, 1>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 2: ln_bwd_launch<ActT, 2>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 3: ln_bwd_launch<ActT, 3>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 4: ln_bwd_launch<ActT, 4>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 5: ln_bwd_launch<ActT, 5>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 6: ln_bwd_launch<ActT, 6>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 7: ln_bwd_launch<ActT, 7>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    default: ln_bwd_launch<ActT, 8>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+  }
   LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(3 * C, 256), 256, 0, c.stream>>>(dw, db, dres_colsum, partial, nb,
-                                                                   3 * C, C);
+  reduce_partials_kernel<<<cdiv(3 * C, RP_COLS), RP_COLS * RP_GROUPS, 0, c.stream>>>(
+      dw, db, dres_colsum, partial, nb, 3 * C, C);
   LAUNCH_CHECK(c);
 }
 template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
@@ -415,31 +475,54 @@ template void launch_layernorm_bwd<bf16>(LaunchCtx&, float*, bf16*, float*, floa
 #define CS_CHUNKS 128
 int64_t colsum_partial_floats(int M, int N) { return (int64_t)CS_CHUNKS * N; }
 
-// grid (ceil(N/256), CS_CHUNKS), 256 threads: 4 row groups x 64 threads x 4
-// columns.  Group g sums rows r0+g, r0+g+4, ... of the chunk in order; the 4
-// group sums are added in group order.
 template <typename T>
-__global__ void colsum_partial_kernel(float* partial, const T* x, int M, int N, int64_t ld) {
-  __shared__ float4 sg[4][64];
-  const int grp = threadIdx.x >> 6, t = threadIdx.x & 63;
-  const int col = (blockIdx.x * 64 + t) * 4;
+__device__ __forceinline__ void load8(const T* p, float* v);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8<bf16>(const bf16* p, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[i]));
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// grid (ceil(N/256), CS_CHUNKS), 256 threads: 8 row groups x 32 threads x 8
+// columns (16-byte loads for bf16).  Group g sums rows r0+g, r0+g+8, ... of
+// the chunk in order; the 8 group sums are added in group order.
+template <typename T>
+__global__ void __launch_bounds__(256) colsum_partial_kernel(float* partial, const T* x, int M, int N, int64_t ld) {
+  __shared__ float sg[8][256];
+  const int grp = threadIdx.x >> 5, t = threadIdx.x & 31;
+  const int col = blockIdx.x * 256 + t * 8;
   const int rows = (M + CS_CHUNKS - 1) / CS_CHUNKS;
   const int r0 = blockIdx.y * rows, r1 = min(M, r0 + rows);
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   if (col < N) {
 #pragma unroll 4
-    for (int r = r0 + grp; r < r1; r += 4) {
-      const float4 v = load4<T>(x + (int64_t)r * ld + col);
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    for (int r = r0 + grp; r < r1; r += 8) {
+      float v[8];
+      load8<T>(x + (int64_t)r * ld + col, v);
+#pragma unroll
+      for (int j = 0; j < 8; j++) s[j] += v[j];
     }
   }
-  sg[grp][t] = s;
-  __syncthreads();
-  if (grp == 0 && col < N) {
-    float4 o = sg[0][t];
 #pragma unroll
-    for (int q = 1; q < 4; q++) { o.x += sg[q][t].x; o.y += sg[q][t].y; o.z += sg[q][t].z; o.w += sg[q][t].w; }
-    *reinterpret_cast<float4*>(partial + (int64_t)blockIdx.y * N + col) = o;
+  for (int j = 0; j < 8; j++) sg[grp][t * 8 + j] = s[j];
+  __syncthreads();
+  const int cc = threadIdx.x;  // one column of the block each
+  if (blockIdx.x * 256 + cc < N) {
+    float o = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; q++) o += sg[q][cc];
+    partial[(int64_t)blockIdx.y * N + blockIdx.x * 256 + cc] = o;
   }
 }
 
@@ -448,7 +531,8 @@ void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld
   dim3 grid(cdiv(N, 256), CS_CHUNKS);
   colsum_partial_kernel<T><<<grid, 256, 0, c.stream>>>(partial, x, M, N, ld);
   LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(N, 256), 256, 0, c.stream>>>(db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
+  reduce_partials_kernel<<<cdiv(N, RP_COLS), RP_COLS * RP_GROUPS, 0, c.stream>>>(
+      db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
   LAUNCH_CHECK(c);
 }
 template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);
@@ -458,33 +542,52 @@ template void launch_colsum<bf16>(LaunchCtx&, float*, const bf16*, int, int, int
 __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) return;
-  s = s * expf(m - mm) + s2 * expf(m2 - mm);
+  s = s * exp2f(m - mm) + s2 * exp2f(m2 - mm);
   m = mm;
 }
 
-// One block per row.  Pass 1: per-thread online (max, sum exp) over the V
-// real columns, then a block reduction.  Pass 2 (the row is now in L2):
-// dlogits = (exp(l - lse) - onehot) * dscale, pad columns 0, written in place.
+#define LOG2E 1.4426950408889634f
+
+// One block per row; logits in log2 units (x * log2 e).  Pass 1 reads 8
+// logits at a time and folds each group into a running (max, sum of 2^(x -
+// max)) -- one max and one rescale per group of 8 -- then a block reduction.
+// Pass 2 (the row is now in L2) writes
+//   dlogits = (2^(x - lse2) - onehot(target)) * dscale,  pad columns 0,
+// in place.  loss = ln 2 * lse2 - logit[target].
 template <typename T>
-__global__ void crossentropy_kernel(T* logits, float* losses, const int32_t* targets, int V,
+__global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* losses, const int32_t* targets, int V,
                                     int Vp, float dscale, int write_dlogits, int* err) {
   __shared__ float sm_m[32], sm_s[32];
   const int64_t row = blockIdx.x;
   T* l = logits + row * Vp;
-  float m = -INFINITY, s = 0.f;
-  for (int j = threadIdx.x * 4; j < V; j += blockDim.x * 4) {
-    const float4 v = load4<T>(l + j);
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; q++) {
-      if (j + q < V) {
-        const float x = vv[q];
-        if (x > m) { s = s * expf(m - x) + 1.f; m = x; }
-        else s += expf(x - m);
-      }
-    }
+  int tg = targets ? targets[row] : -1;
+  if (targets && (tg < 0 || tg >= V)) {
+    if (threadIdx.x == 0) record_error(err, DEVERR_TOKEN);
+    tg = 0;
   }
-  // warp then block reduction of (m, s)
+  const float lt = targets ? to_f(l[tg]) : 0.f;  // read before any thread overwrites the row
+  float m = -INFINITY, s = 0.f;
+  const int nch = Vp / 8;
+  for (int q = threadIdx.x; q < nch; q += blockDim.x) {
+    float v[8];
+    load8<T>(l + q * 8, v);
+    const int base = q * 8;
+    float cm = -INFINITY;
+    if (base + 8 <= V) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) { v[j] *= LOG2E; cm = fmaxf(cm, v[j]); }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; j++) { v[j] = base + j < V ? v[j] * LOG2E : -INFINITY; cm = fmaxf(cm, v[j]); }
+    }
+    if (cm == -INFINITY) continue;
+    const float nm = fmaxf(m, cm);
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) a += exp2f(v[j] - nm);
+    s = s * exp2f(m - nm) + a;
+    m = nm;
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -506,28 +609,21 @@ __global__ void crossentropy_kernel(T* logits, float* losses, const int32_t* tar
     if (lane == 0) { sm_m[0] = m; sm_s[0] = s; }
   }
   __syncthreads();
-  const float lse = sm_m[0] + logf(sm_s[0]);
-  int tg = targets ? targets[row] : -1;
-  if (targets && (tg < 0 || tg >= V)) {
-    if (threadIdx.x == 0) record_error(err, DEVERR_TOKEN);
-    tg = 0;
-  }
-  __syncthreads();  // every thread has read its target logit source before overwriting
-  float lt = 0.f;
-  if (targets) lt = to_f(l[tg]);
-  __syncthreads();
-  if (threadIdx.x == 0 && targets) losses[row] = lse - lt;
+  const float lse2 = sm_m[0] + log2f(sm_s[0]);
+  if (threadIdx.x == 0 && targets) losses[row] = lse2 * 0.6931471805599453f - lt;
   if (!write_dlogits) return;
-  for (int j = threadIdx.x * 4; j < Vp; j += blockDim.x * 4) {
-    const float4 v = load4<T>(l + j);
-    const float vv[4] = {v.x, v.y, v.z, v.w};
-    float o[4];
+  for (int q = threadIdx.x; q < nch; q += blockDim.x) {
+    float v[8];
+    load8<T>(l + q * 8, v);
+    const int base = q * 8;
+    float o[8];
 #pragma unroll
-    for (int q = 0; q < 4; q++) {
-      const int jj = j + q;
-      o[q] = jj < V ? (expf(vv[q] - lse) - (jj == tg ? 1.f : 0.f)) * dscale : 0.f;
+    for (int j = 0; j < 8; j++) {
+      const int jj = base + j;
+      o[j] = jj < V ? (exp2f(v[j] * LOG2E - lse2) - (jj == tg ? 1.f : 0.f)) * dscale : 0.f;
     }
-    store4<T>(l + j, o[0], o[1], o[2], o[3]);
+    store4<T>(l + base, o[0], o[1], o[2], o[3]);
+    store4<T>(l + base + 4, o[4], o[5], o[6], o[7]);
   }
 }
 
