@@ -219,8 +219,46 @@ GPT2_API int gpt2_profile_read(gpt2_model* m, int32_t cls, const char** name,
 GPT2_API int gpt2_launch_count(const gpt2_model* m, int64_t* n);
 
 /* Text of the last error on this model (or of the last failed gpt2_build
- * when m is NULL).  Static or model-owned storage; never NULL. */
+ * or model-less call when m is NULL).  Static or model-owned storage;
+ * never NULL. */
 GPT2_API const char* gpt2_last_error(const gpt2_model* m);
+
+/* LayerNorm backward that allocates no device memory.  The pages have no
+ * counterpart: this entry point exists for callers of this library that
+ * cannot call cudaMalloc -- code whose device memory is owned by another
+ * allocator (a framework's caching allocator, a fixed pool) that must not be
+ * bypassed, and latency-critical loops where a cudaMalloc/cudaFree would
+ * synchronise the device.  It needs no gpt2_model.
+ *
+ * Computes, for N rows of width C (row-major fp32, device pointers):
+ *   xhat = (inp - mean) * rstd,  g = dout * weight,
+ *   dinp[i]     += rstd[i] * (g - mean_row(g) - xhat * mean_row(g * xhat))
+ *   dweight     += sum over rows of dout * xhat
+ *   dbias       += sum over rows of dout
+ *   dinp_colsum += sum over rows of the updated dinp   (skipped if NULL)
+ * (the same arithmetic as the LayerNorm backward inside gpt2_backward).
+ *   dinp [N, C], dweight [C], dbias [C], dinp_colsum [C] or NULL: outputs,
+ *       accumulated into (the caller zeroes them for plain values);
+ *   dout, inp [N, C], weight [C], mean, rstd [N]: inputs, read only;
+ *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
+ * Scratch: the per-block partial sums, ceil(N/32) * 3 * C floats, live in
+ * one file-scope __device__ array of 2^21 floats (8 MiB) that every GPU
+ * which loads the library holds until the process exits.  Larger sizes are
+ * rejected with GPT2_ERR_ARG (N * C must stay below about 22.4 million);
+ * also GPT2_ERR_ARG for a NULL input/output or C outside [4, 1024] or
+ * C % 4 != 0, GPT2_ERR_CUDA if a launch fails; gpt2_last_error(NULL) has
+ * the text.  Every call on a device shares the array and leaves the last
+ * call's partials in it; each call writes every partial it reads, so nothing
+ * needs clearing, but calls that overlap on the GPU (different streams, or
+ * other threads) race on the array.  The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Asynchronous;
+ * calls no cudaMalloc, cudaFree or other allocating routine. */
+GPT2_API int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias,
+                                             float* dinp_colsum, const float* dout,
+                                             const float* inp, const float* weight,
+                                             const float* mean, const float* rstd, int32_t N,
+                                             int32_t C, void* cuda_stream);
 
 #ifdef __cplusplus
 }

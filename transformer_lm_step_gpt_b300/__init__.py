@@ -18,7 +18,8 @@ import os
 
 import numpy as np
 
-__all__ = ["Model", "GPT2Error", "library_path", "load_library", "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
+__all__ = ["Model", "GPT2Error", "library_path", "load_library", "layernorm_backward_noalloc",
+           "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgpt2.so")
@@ -88,6 +89,7 @@ def load_library():
                                ctypes.POINTER(ctypes.c_double)], ctypes.c_int),
         "gpt2_launch_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_last_error": ([vp], ctypes.c_char_p),
+        "gpt2_layernorm_backward_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -260,3 +262,16 @@ class Model:
         n = ctypes.c_int64()
         self._check(self._lib.gpt2_launch_count(self._h, ctypes.byref(n)))
         return n.value
+
+
+def layernorm_backward_noalloc(dinp, dweight, dbias, dinp_colsum, dout, inp, weight, mean, rstd,
+                               N, C, stream=None):
+    """gpt2_layernorm_backward_noalloc on device buffers (torch tensors or
+    raw pointers); outputs are accumulated into.  Allocates nothing."""
+    L = load_library()
+    s = getattr(stream, "cuda_stream", stream)
+    rc = L.gpt2_layernorm_backward_noalloc(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dinp_colsum),
+                                           _ptr(dout), _ptr(inp), _ptr(weight), _ptr(mean), _ptr(rstd),
+                                           int(N), int(C), s)
+    if rc != 0:
+        raise GPT2Error(rc, L.gpt2_last_error(None).decode())

@@ -480,6 +480,8 @@ int forward_common(gpt2_model* m, bool with_targets, float* mean_loss) {
 
 }  // namespace
 
+void set_global_error(const char* msg) { g_build_error = msg; }
+
 // ====================================================================== ABI
 extern "C" {
 

@@ -13,6 +13,7 @@
 // reduction runs in a fixed order, so results repeat bit for bit.
 #include <cstdio>
 
+#include "../../include/gpt2.h"
 #include "common.cuh"
 #include "kernels.h"
 
@@ -694,4 +695,72 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
   int grid = (int)std::min<int64_t>(cdiv(n4, 256), (int64_t)c.num_sms * 16);
   adamw_kernel<<<grid, 256, 0, c.stream>>>(p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
   LAUNCH_CHECK(c);
+}
+
+// ============================================================ allocation-free LayerNorm backward
+// gpt2_layernorm_backward_noalloc: the LayerNorm backward above for callers
+// that cannot allocate device memory.  Its block partials (ceil(N/32) rows of
+// 3*C floats) live in this file-scope array instead of caller- or
+// model-owned scratch; every GPU that loads the library holds it until the
+// process exits.
+#define NOALLOC_SCRATCH_FLOATS (1 << 21)  // 8 MiB
+static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_SCRATCH_FLOATS];
+
+// Device address of the array on the current device, looked up once per
+// device (in host code the array's name is only a host-side stand-in).
+static float* noalloc_scratch(int dev) {
+  static float* addr[128] = {};
+  if (dev < 0 || dev >= 128) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
+extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias,
+                                               float* dinp_colsum, const float* dout,
+                                               const float* inp, const float* weight,
+                                               const float* mean, const float* rstd, int32_t N,
+                                               int32_t C, void* cuda_stream) {
+  if (!dinp || !dweight || !dbias || !dout || !inp || !weight || !mean || !rstd) {
+    set_global_error("gpt2_layernorm_backward_noalloc: NULL pointer");
+    return GPT2_ERR_ARG;
+  }
+  if (N < 1 || C < 4 || C > 1024 || C % 4 != 0) {
+    set_global_error("gpt2_layernorm_backward_noalloc: need N >= 1, 4 <= C <= 1024, C % 4 == 0");
+    return GPT2_ERR_ARG;
+  }
+  const int64_t need = (int64_t)cdiv(N, LNB_ROWS) * 3 * C;
+  if (need > NOALLOC_SCRATCH_FLOATS) {
+    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/32)*3*C exceeds the 2^21-float "
+                     "static scratch (N*C must stay below about 22.4 million)");
+    return GPT2_ERR_ARG;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  float* scratch = e == cudaSuccess ? noalloc_scratch(dev) : nullptr;
+  if (!scratch) {
+    set_global_error("gpt2_layernorm_backward_noalloc: no device address for the static scratch");
+    return GPT2_ERR_CUDA;
+  }
+  int64_t launches = 0;
+  LaunchCtx c;
+  c.stream = static_cast<cudaStream_t>(cuda_stream);
+  c.err = nullptr;
+  c.launches = &launches;
+  c.num_sms = 0;
+  c.host_fail = 0;
+  launch_layernorm_bwd<float>(c, dinp, nullptr, dweight, dbias, dinp_colsum, dout, inp, weight,
+                              mean, rstd, N, C, true, scratch);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_global_error(cudaGetErrorString(e));
+    return GPT2_ERR_CUDA;
+  }
+  return GPT2_OK;
 }

@@ -119,3 +119,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
                                int C, int NH);
+
+// Record the message gpt2_last_error(NULL) returns (entry points without a
+// model handle).
+void set_global_error(const char* msg);
