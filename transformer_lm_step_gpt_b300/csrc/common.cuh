@@ -78,6 +78,15 @@ __device__ __forceinline__ float gelu_grad_hw(float x) {
   return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * GELU_S * (1.f + 3.f * GELU_A * x * x);
 }
 
+// 2^x with the PTX ex2.approx.ftz.f32 instruction (relative error about
+// 2^-22; inputs below -126 flush to 0), for probabilities that are rounded
+// to bf16 or summed in fp32.
+__device__ __forceinline__ float ex2_hw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------ shared memory
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -67,6 +67,8 @@ static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W,
 #define AT_BLK 128
 #define AT_HS 64
 #define AT_TILE 16384u  // bytes of one [128 x 64] bf16 tile
+#define AB_SUB 64
+#define AT_SUBTILE 8192u  // bytes of one [64 x 64] bf16 tile
 
 // descriptors of a [128 rows x 64] tile read as a K-major operand (rows = M
 // or N, K = 64 head dims) at K-step kk (16 dims), or as an MN-major operand
@@ -135,26 +137,33 @@ __device__ __forceinline__ void store_row32_bf16(bf16* dst, const float* v, floa
 #define AT_THREADS 256
 
 // ============================================================ forward
-// smem: Q | K0 K1 | V | P (2 atoms) | row-max exchange [2][128] | barriers
-#define AF_SMEM (1024 + 6 * AT_TILE + 1024 + 256)
+// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks with
+// a two-deep software pipeline: the MMA S(j+1) = q k(j+1)^T runs while the
+// warps do the softmax of S(j), and O_blk(j) = P(j) v(j) runs while they
+// start on j+1 (its result is folded into the register accumulator one
+// iteration later).  TMEM: S[0], S[1], O[0], O[1] (64 columns each), so two
+// CTAs share an SM.
+// smem: Q | K0 K1 | V0 V1 (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][128] | barriers
+#define AF_SMEM (1024 + AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 1024 + 256)
 
 __global__ void __launch_bounds__(AT_THREADS, 2)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* y, float* lse, int T,
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+                       const __grid_constant__ CUtensorMap tm_qkv64, bf16* y, float* lse, int T,
                        int C, int NH, float scale, int* err) {
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
-  uint8_t* sK = sm + AT_TILE;      // 2 stages
-  uint8_t* sV = sm + 3 * AT_TILE;  // 1 stage
-  uint8_t* sP = sm + 4 * AT_TILE;  // 2 atoms
-  float* red = reinterpret_cast<float*>(sm + 6 * AT_TILE);  // [2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 6 * AT_TILE + 1024);
+  uint8_t* sK = sm + AT_TILE;            // 2 stages of [64 x 64]
+  uint8_t* sV = sK + 2 * AT_SUBTILE;     // 2 stages
+  uint8_t* sP = sV + 2 * AT_SUBTILE;     // 2 x [128 x 64]
+  float* red = reinterpret_cast<float*>(sP + 2 * AT_TILE);  // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * AT_TILE + 1024);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;  // [2]
-  uint64_t* v_full = bars + 3;
-  uint64_t* s_done = bars + 4;
-  uint64_t* o_done = bars + 5;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint64_t* v_full = bars + 3;  // [2]
+  uint64_t* s_done = bars + 5;  // [2]
+  uint64_t* o_done = bars + 7;  // [2]
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
 
   const int nqb = gridDim.x;
   const int qb = nqb - 1 - blockIdx.x;  // longest rows first
@@ -163,94 +172,103 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
   const int row = quarter * 32 + lane, q = q0 + row;
-  const int nkb = qb + 1;
+  const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
 
   if (tid == 0) {
-    for (int i = 0; i < 6; i++) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 9; i++) mbar_init(&bars[i], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_qkv64);
   }
   if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  const uint32_t tS = tm, tO = tm + 128;
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
+  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
+  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
   if (tid == 0) {
     mbar_arrive_expect_tx(q_full, AT_TILE);
     tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-    mbar_arrive_expect_tx(v_full, AT_TILE);
-    tma_load_3d(sV, &tm_qkv, v_full, 2 * C + h * AT_HS, 0, b);
-    for (int s = 0; s < 2 && s < nkb; s++) {
-      mbar_arrive_expect_tx(&k_full[s], AT_TILE);
-      tma_load_3d(sK + s * AT_TILE, &tm_qkv, &k_full[s], C + h * AT_HS, s * AT_BLK, b);
+    for (int s = 0; s < 2 && s < nsub; s++) {
+      mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
+      tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, s * AB_SUB, b);
+      mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
+      tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, s * AB_SUB, b);
     }
+    // S(0)
+    mbar_wait(q_full, 0, err);
+    mbar_wait(&k_full[0], 0, err);
+    tc_fence_after();
+    const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK);
+#pragma unroll
+    for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+    tc_commit(&s_done[0]);
   }
   const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
-  float m = -INFINITY, lpart = 0.f;
+  float m = -INFINITY, lpart = 0.f, alpha_prev = 1.f;
   float o[32];
 #pragma unroll
   for (int i = 0; i < 32; i++) o[i] = 0.f;
-  const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
-  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
-  for (int kb = 0; kb < nkb; kb++) {
-    const int st = kb & 1;
-    if (tid == 0) {
-      if (kb == 0) mbar_wait(q_full, 0, err);
-      mbar_wait(&k_full[st], (uint32_t)(kb >> 1) & 1u, err);
-      tc_fence_after();
-      const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + st * AT_TILE);
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-      tc_commit(s_done);
-    }
-    mbar_wait(s_done, (uint32_t)kb & 1u, err);
+  for (int j = 0; j < nsub; j++) {
+    const int sb = j & 1;
+    const uint32_t tS = tm + (uint32_t)(sb * 64), tO = tm + 128 + (uint32_t)(sb * 64);
+    mbar_wait(&s_done[sb], (uint32_t)(j >> 1) & 1u, err);
     tc_fence_after();
-    const bool diag = kb == qb;
-    const int k0 = kb * AT_BLK;
-    // pass 1: max over this half's 64 columns, exchanged with the partner warp
-    float mx = -INFINITY;
-#pragma unroll 1
-    for (int cc = 0; cc < 2; cc++) {
-      const int c = half * 2 + cc;
-      uint32_t r[32];
-      tmem_ld32(tS + lanebase + c * 32, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; j++) {
-        const float s = __uint_as_float(r[j]);
-        if (!diag || k0 + c * 32 + j <= q) mx = fmaxf(mx, s);
+    if (tid == 0) {
+      // S(j) is done with K stage sb: refill it with K(j+2)
+      if (j + 2 < nsub) {
+        mbar_arrive_expect_tx(&k_full[sb], AT_SUBTILE);
+        tma_load_3d(sK + sb * AT_SUBTILE, &tm_qkv64, &k_full[sb], C + h * AT_HS, (j + 2) * AB_SUB, b);
       }
+      // issue S(j+1) into the other S buffer (its last reader was softmax(j-1))
+      if (j + 1 < nsub) {
+        const int nb = sb ^ 1;
+        mbar_wait(&k_full[nb], (uint32_t)((j + 1) >> 1) & 1u, err);
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + nb * AT_SUBTILE);
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + (uint32_t)(nb * 64), kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+        tc_commit(&s_done[nb]);
+      }
+    }
+    const int k0 = j * AB_SUB;
+    const bool diag = k0 + AB_SUB - 1 > q0;
+    uint32_t r[32];
+    tmem_ld32(tS + lanebase + half * 32, r);
+    tmem_ld_wait();
+    // pass 1: max over this half's 32 columns, exchanged with the partner warp
+    float mx = -INFINITY;
+    if (diag) {
+#pragma unroll
+      for (int jj = 0; jj < 32; jj++)
+        if (k0 + half * 32 + jj <= q) mx = fmaxf(mx, __uint_as_float(r[jj]));
+    } else {
+#pragma unroll
+      for (int jj = 0; jj < 32; jj++) mx = fmaxf(mx, __uint_as_float(r[jj]));
     }
     red[half * 128 + row] = mx;
-    tc_fence_before();
     __syncthreads();
     const float mnew = fmaxf(m, fmaxf(red[row], red[128 + row]));
-    const float alpha = exp2f((m - mnew) * sl2);
+    const float alpha = ex2_hw((m - mnew) * sl2);
     const float mo = mnew * sl2;
-    // pass 2: P = exp(scale (s - mnew)) -> smem (bf16), partial row sum
+    // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
     float sum = 0.f;
-#pragma unroll 1
-    for (int cc = 0; cc < 2; cc++) {
-      const int c = half * 2 + cc;
-      uint32_t r[32];
-      tmem_ld32(tS + lanebase + c * 32, r);
-      tmem_ld_wait();
+    uint8_t* P = sP + sb * AT_TILE;
 #pragma unroll
-      for (int g = 0; g < 4; g++) {
-        float p[8];
+    for (int g = 0; g < 4; g++) {
+      float p[8];
 #pragma unroll
-        for (int j = 0; j < 8; j++) {
-          const int kc = c * 32 + g * 8 + j;
-          const float s = __uint_as_float(r[g * 8 + j]);
-          p[j] = (!diag || k0 + kc <= q) ? exp2f(s * sl2 - mo) : 0.f;
-          sum += p[j];
-        }
-        st_swz8(sP, row, c * 4 + g, p);
+      for (int jj = 0; jj < 8; jj++) {
+        const float s = __uint_as_float(r[g * 8 + jj]);
+        const bool ok = !diag || k0 + half * 32 + g * 8 + jj <= q;
+        p[jj] = ok ? ex2_hw(s * sl2 - mo) : 0.f;
+        sum += p[jj];
       }
+      st_swz8(P, row, half * 4 + g, p);
     }
     lpart = lpart * alpha + sum;
     m = mnew;
@@ -259,32 +277,39 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     __syncthreads();
     if (tid == 0) {
       tc_fence_after();
-      mbar_wait(v_full, (uint32_t)kb & 1u, err);
-      const uint32_t aP = smem_u32(sP), bV = smem_u32(sV);
+      mbar_wait(&v_full[sb], (uint32_t)(j >> 1) & 1u, err);
+      const uint32_t aP = smem_u32(P), bV = smem_u32(sV + sb * AT_SUBTILE);
 #pragma unroll
-      for (int kk = 0; kk < 8; kk++) tc_mma_bf16(tO, kmaj2(aP, kk), mnmaj(bV, kk), idO, kk > 0);
-      tc_commit(o_done);
+      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tO, kmaj(aP, kk), mnmaj(bV, kk), idO, kk > 0);
+      tc_commit(&o_done[sb]);
     }
-    mbar_wait(o_done, (uint32_t)kb & 1u, err);
-    tc_fence_after();
-    {
-      uint32_t r[32];
-      tmem_ld32(tO + lanebase + half * 32, r);
+    // fold in O_blk(j-1) (its MMA ran during this iteration's softmax)
+    if (j > 0) {
+      const int pb = sb ^ 1;
+      mbar_wait(&o_done[pb], (uint32_t)((j - 1) >> 1) & 1u, err);
+      tc_fence_after();
+      uint32_t ro[32];
+      tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; j++) o[j] = o[j] * alpha + __uint_as_float(r[j]);
-    }
-    if (tid == 0) {  // both MMAs of block kb are done: V and K stage st are free
-      if (kb + 1 < nkb) {
-        mbar_arrive_expect_tx(v_full, AT_TILE);
-        tma_load_3d(sV, &tm_qkv, v_full, 2 * C + h * AT_HS, (kb + 1) * AT_BLK, b);
-      }
-      if (kb + 2 < nkb) {
-        mbar_arrive_expect_tx(&k_full[st], AT_TILE);
-        tma_load_3d(sK + st * AT_TILE, &tm_qkv, &k_full[st], C + h * AT_HS, (kb + 2) * AT_BLK, b);
+      for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
+      if (tid == 0 && j + 1 < nsub) {  // PV(j-1) is done with V stage pb: load V(j+1)
+        mbar_arrive_expect_tx(&v_full[pb], AT_SUBTILE);
+        tma_load_3d(sV + pb * AT_SUBTILE, &tm_qkv64, &v_full[pb], 2 * C + h * AT_HS, (j + 1) * AB_SUB, b);
       }
     }
+    alpha_prev = alpha;
     tc_fence_before();
+  }
+  {  // the last O_blk
+    const int pb = (nsub - 1) & 1;
+    mbar_wait(&o_done[pb], (uint32_t)((nsub - 1) >> 1) & 1u, err);
+    tc_fence_after();
+    uint32_t ro[32];
+    tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
   }
   __syncthreads();
   red[half * 128 + row] = lpart;
@@ -334,8 +359,6 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 // elementwise work).
 // smem: K | V | Q0 Q1 | dO0 dO1 (64-row tiles) | P^T | dS^T ([128 x 64]) |
 //       lse[64] D[64] | barriers
-#define AB_SUB 64
-#define AT_SUBTILE 8192u  // bytes of one [64 x 64] bf16 tile
 #define AKV_SMEM (1024 + 2 * AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 512 + 256)
 
 __global__ void __launch_bounds__(AT_THREADS, 2)
@@ -434,7 +457,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
         for (int j = 0; j < 8; j++) {
           const int qc = half * 32 + g * 8 + j;
           const bool ok = !diag || q0 + qc >= key;
-          const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - sl[qc]) : 0.f;
+          const float pv = ok ? ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - sl[qc]) : 0.f;
           p[j] = pv;
           ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - sdd[qc]);
         }
@@ -585,7 +608,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
         for (int j = 0; j < 8; j++) {
           const int kc = half * 32 + g * 8 + j;
           const bool ok = !diag || k0 + kc <= q;
-          const float pv = ok ? exp2f(__uint_as_float(rs[g * 8 + j]) * sl2 - my_lse) : 0.f;
+          const float pv = ok ? ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - my_lse) : 0.f;
           ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - my_d);
         }
         st_swz8(sS, row, half * 4 + g, ds);
@@ -633,11 +656,14 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
     launch_attention_fwd_simt<bf16>(c, y, lse, qkv, B, T, C, NH);
     return;
   }
-  CUtensorMap tq;
-  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C)) { c.host_fail = 1; return; }
+  CUtensorMap tq, tq64;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB)) {
+    c.host_fail = 1;
+    return;
+  }
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
-  attn_fwd_tc_kernel<<<grid, AT_THREADS, AF_SMEM, c.stream>>>(tq, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
+  attn_fwd_tc_kernel<<<grid, AT_THREADS, AF_SMEM, c.stream>>>(tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
   (*c.launches)++;
 }
 
