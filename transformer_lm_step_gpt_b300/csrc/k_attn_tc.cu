@@ -143,8 +143,11 @@ __device__ __forceinline__ void store_row32_bf16(bf16* dst, const float* v, floa
 // start on j+1 (its result is folded into the register accumulator one
 // iteration later).  TMEM: S[0], S[1], O[0], O[1] (64 columns each), so two
 // CTAs share an SM.
-// smem: Q | K0 K1 | V0 V1 (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][128] | barriers
-#define AF_SMEM (1024 + AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 1024 + 256)
+// Warps w and w+4 exchange their half-row maxima through a double-buffered
+// array and a 64-thread named barrier; the softmax warps hand P to the
+// MMA-issuing thread through an mbarrier, so no step waits for the whole CTA.
+// smem: Q | K0 K1 | V0 V1 (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
+#define AF_SMEM (1024 + AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 2048 + 256)
 
 __global__ void __launch_bounds__(AT_THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
@@ -156,14 +159,15 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint8_t* sK = sm + AT_TILE;            // 2 stages of [64 x 64]
   uint8_t* sV = sK + 2 * AT_SUBTILE;     // 2 stages
   uint8_t* sP = sV + 2 * AT_SUBTILE;     // 2 x [128 x 64]
-  float* red = reinterpret_cast<float*>(sP + 2 * AT_TILE);  // [2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * AT_TILE + 1024);
+  float* red = reinterpret_cast<float*>(sP + 2 * AT_TILE);  // [2 iterations][2 halves][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * AT_TILE + 2048);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;  // [2]
   uint64_t* v_full = bars + 3;  // [2]
   uint64_t* s_done = bars + 5;  // [2]
   uint64_t* o_done = bars + 7;  // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* p_ready = bars + 9;  // 8 warp arrivals per sub-block
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
 
   const int nqb = gridDim.x;
   const int qb = nqb - 1 - blockIdx.x;  // longest rows first
@@ -176,6 +180,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 
   if (tid == 0) {
     for (int i = 0; i < 9; i++) mbar_init(&bars[i], 1);
+    mbar_init(p_ready, AT_THREADS / 32);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_qkv64);
@@ -250,9 +255,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 #pragma unroll
       for (int jj = 0; jj < 32; jj++) mx = fmaxf(mx, __uint_as_float(r[jj]));
     }
-    red[half * 128 + row] = mx;
-    __syncthreads();
-    const float mnew = fmaxf(m, fmaxf(red[row], red[128 + row]));
+    float* rd = red + sb * 256;
+    rd[half * 128 + row] = mx;
+    named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
+    const float mnew = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
     const float alpha = ex2_hw((m - mnew) * sl2);
     const float mo = mnew * sl2;
     // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
@@ -274,8 +280,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     m = mnew;
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_ready);
     if (tid == 0) {
+      mbar_wait(p_ready, (uint32_t)j & 1u, err);
       tc_fence_after();
       mbar_wait(&v_full[sb], (uint32_t)(j >> 1) & 1u, err);
       const uint32_t aP = smem_u32(P), bV = smem_u32(sV + sb * AT_SUBTILE);
@@ -381,7 +389,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint64_t* q_full = bars + 1;  // [2]
   uint64_t* s_done = bars + 3;
   uint64_t* o_done = bars + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  uint64_t* p_ready = bars + 5;  // 8 warp arrivals per sub-block
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
 
   const int kb = (int)gridDim.x - 1 - (int)blockIdx.x;  // key block; longest first
   const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
@@ -393,6 +402,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 
   if (tid == 0) {
     for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    mbar_init(p_ready, AT_THREADS / 32);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_qkv64);
@@ -467,8 +477,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_ready);
     if (tid == 0) {
+      mbar_wait(p_ready, (uint32_t)it & 1u, err);
       tc_fence_after();
       const uint32_t aP = smem_u32(sP), aS = smem_u32(sS);
       const uint32_t bQ = smem_u32(sQ + st * AT_SUBTILE), bD = smem_u32(sD + st * AT_SUBTILE);
@@ -485,10 +497,11 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
       tma_load_3d(sQ + st * AT_SUBTILE, &tm_qkv64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
       tma_load_3d(sD + st * AT_SUBTILE, &tm_dy64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
     }
+    // every thread has waited o_done: the P^T / dS^T / lse buffers are free
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
+  __syncthreads();
+  tc_fence_after();
   const int64_t C3 = 3 * (int64_t)C;
   float v[32];
   {
@@ -535,7 +548,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint64_t* kv_full = bars + 1;  // [2]
   uint64_t* s_done = bars + 3;
   uint64_t* o_done = bars + 4;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
+  uint64_t* p_ready = bars + 5;  // 8 warp arrivals per sub-block
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
 
   const int nqb = gridDim.x;
   const int qb = nqb - 1 - blockIdx.x;
@@ -548,6 +562,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 
   if (tid == 0) {
     for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
+    mbar_init(p_ready, AT_THREADS / 32);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_dy);
@@ -616,8 +631,10 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_ready);
     if (tid == 0) {
+      mbar_wait(p_ready, (uint32_t)kb & 1u, err);
       tc_fence_after();
       const uint32_t aS = smem_u32(sS), bK = smem_u32(sK + st * AT_SUBTILE);
 #pragma unroll
@@ -631,10 +648,11 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
       tma_load_3d(sK + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], C + h * AT_HS, k0 + 2 * AB_SUB, b);
       tma_load_3d(sV + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], 2 * C + h * AT_HS, k0 + 2 * AB_SUB, b);
     }
+    // every thread has waited o_done: the dS buffer is free
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
   }
+  __syncthreads();
+  tc_fence_after();
   float v[32];
   {
     uint32_t r[32];
