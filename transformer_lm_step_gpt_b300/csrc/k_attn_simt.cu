@@ -15,6 +15,8 @@
 
 template <typename T>
 __global__ void attn_fwd_simt_kernel(T* y, float* lse, const T* qkv, int Tn, int C, int NH) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sc[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * AS_WARPS + warp, h = blockIdx.y, b = blockIdx.z;
@@ -56,6 +58,8 @@ __global__ void attn_fwd_simt_kernel(T* y, float* lse, const T* qkv, int Tn, int
 template <typename T>
 __global__ void attn_bwd_dq_simt_kernel(T* dqkv, float* dsum, const T* dy, const T* y,
                                         const T* qkv, const float* lse, int Tn, int C, int NH) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sc[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * AS_WARPS + warp, h = blockIdx.y, b = blockIdx.z;
@@ -94,6 +98,8 @@ __global__ void attn_bwd_dq_simt_kernel(T* dqkv, float* dsum, const T* dy, const
 template <typename T>
 __global__ void attn_bwd_dkv_simt_kernel(T* dqkv, const float* dsum, const T* dy, const T* qkv,
                                          const float* lse, int Tn, int C, int NH) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sc[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = blockIdx.x * AS_WARPS + warp, h = blockIdx.y, b = blockIdx.z;
@@ -133,8 +139,7 @@ void launch_attention_fwd_simt(LaunchCtx& c, T* y, float* lse, const T* qkv, int
   dim3 grid((Tn + AS_WARPS - 1) / AS_WARPS, NH, B);
   const size_t smem = (size_t)AS_WARPS * Tn * sizeof(float);
   cudaFuncSetAttribute(attn_fwd_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_fwd_simt_kernel<T><<<grid, AS_WARPS * 32, smem, c.stream>>>(y, lse, qkv, Tn, C, NH);
-  (*c.launches)++;
+  launch_pdl(c, attn_fwd_simt_kernel<T>, dim3(grid), dim3(AS_WARPS * 32), smem, y, lse, qkv, Tn, C, NH);
 }
 
 int64_t attention_simt_scratch_floats(int B, int Tn, int NH) { return (int64_t)B * NH * Tn; }
@@ -147,12 +152,10 @@ void launch_attention_bwd_simt(LaunchCtx& c, T* dqkv, const T* dy, const T* y, c
   dim3 grid((Tn + AS_WARPS - 1) / AS_WARPS, NH, B);
   size_t smem = (size_t)AS_WARPS * Tn * sizeof(float);
   cudaFuncSetAttribute(attn_bwd_dq_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_bwd_dq_simt_kernel<T><<<grid, AS_WARPS * 32, smem, c.stream>>>(dqkv, dsum, dy, y, qkv, lse, Tn, C, NH);
-  (*c.launches)++;
+  launch_pdl(c, attn_bwd_dq_simt_kernel<T>, dim3(grid), dim3(AS_WARPS * 32), smem, dqkv, dsum, dy, y, qkv, lse, Tn, C, NH);
   smem = (size_t)AS_WARPS * 2 * Tn * sizeof(float);
   cudaFuncSetAttribute(attn_bwd_dkv_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_bwd_dkv_simt_kernel<T><<<grid, AS_WARPS * 32, smem, c.stream>>>(dqkv, dsum, dy, qkv, lse, Tn, C, NH);
-  (*c.launches)++;
+  launch_pdl(c, attn_bwd_dkv_simt_kernel<T>, dim3(grid), dim3(AS_WARPS * 32), smem, dqkv, dsum, dy, qkv, lse, Tn, C, NH);
 }
 
 template void launch_attention_fwd_simt<float>(LaunchCtx&, float*, float*, const float*, int, int, int, int);

@@ -153,6 +153,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                        const __grid_constant__ CUtensorMap tm_qkv64, bf16* y, float* lse, int T,
                        int C, int NH, float scale, int* err) {
+  pdl_trigger();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
   const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
   const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
@@ -336,6 +338,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
 // D[b,h,t] = sum_i dy[b,t,h*64+i] * y[b,t,h*64+i]
 __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y, int B, int T,
                                      int C, int NH) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n = (int64_t)B * T * NH;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -374,6 +378,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                            const __grid_constant__ CUtensorMap tm_qkv64,
                            const __grid_constant__ CUtensorMap tm_dy64, bf16* dqkv, const float* lse,
                            const float* dsum, int T, int C, int NH, float scale, int* err) {
+  pdl_trigger();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sK = sm;
@@ -413,6 +418,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
   const uint32_t tS = tm, tdP = tm + 64, tdV = tm + 128, tdK = tm + 192;
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
@@ -536,6 +542,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
                           const __grid_constant__ CUtensorMap tm_dy,
                           const __grid_constant__ CUtensorMap tm_qkv64, bf16* dqkv, const float* lse,
                           const float* dsum, int T, int C, int NH, float scale, int* err) {
+  pdl_trigger();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
@@ -573,6 +580,7 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
   const uint32_t tS = tm, tdP = tm + 64, tdQ = tm + 128;
   const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
@@ -681,8 +689,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
   }
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
-  attn_fwd_tc_kernel<<<grid, AT_THREADS, AF_SMEM, c.stream>>>(tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
-  (*c.launches)++;
+  launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AT_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
 }
 
 void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
@@ -699,15 +706,11 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
     return;
   }
   const int64_t n = (int64_t)B * T * NH;
-  attn_bwd_dsum_kernel<<<(int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16), 256, 0,
-                         c.stream>>>(dsum, dy, y, B, T, C, NH);
-  (*c.launches)++;
+  launch_pdl(c, attn_bwd_dsum_kernel, dim3((int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16)), dim3(256), 0, dsum, dy, y, B, T, C, NH);
   const float scale = 1.f / sqrtf((float)AT_HS);
   dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AKV_SMEM);
-  attn_bwd_dkv_tc_kernel<<<grid, AT_THREADS, AKV_SMEM, c.stream>>>(tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
-  (*c.launches)++;
+  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(AT_THREADS), AKV_SMEM, tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  attn_bwd_dq_tc_kernel<<<grid, AT_THREADS, AQ_SMEM, c.stream>>>(tq, td, tq64, dqkv, lse, dsum, T, C, NH, scale, c.err);
-  (*c.launches)++;
+  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AT_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, T, C, NH, scale, c.err);
 }

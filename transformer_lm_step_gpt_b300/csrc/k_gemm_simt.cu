@@ -20,6 +20,8 @@ __device__ __forceinline__ float epi_apply(const GemmArgs& g, int m, int n, floa
 }
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float As[SG_BK][SG_BM + 4];
   __shared__ float Bs[SG_BK][SG_BN + 4];
   const float* A = static_cast<const float*>(g.A);
@@ -91,6 +93,5 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
 
 void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g) {
   dim3 grid((g.N + SG_BN - 1) / SG_BN, (g.M + SG_BM - 1) / SG_BM);
-  gemm_f32_kernel<<<grid, 256, 0, c.stream>>>(g);
-  (*c.launches)++;
+  launch_pdl(c, gemm_f32_kernel, dim3(grid), dim3(256), 0, g);
 }

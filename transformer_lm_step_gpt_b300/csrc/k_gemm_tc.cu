@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
                    int splits, int* err) {
+  pdl_trigger();
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
 
   if (warp == 0) {
     if (lane == 0) {
@@ -374,6 +376,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // out[m, n] += sum over splits of partial[s][m][n], splits in order.
 __global__ void splitk_reduce_kernel(float* out, int64_t ldo, const float* partial, int splits,
                                      int M, int N) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t total = (int64_t)M * N;
   const int64_t MN = total;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total / 4;
@@ -423,13 +427,11 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   const int grid = std::min(tiles, c.num_sms);
   auto kern = gemm_tc_kernel<BN, A_K, B_K>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM);
-  kern<<<grid, TC_THREADS, TcCfg<BN>::SMEM, c.stream>>>(ta, tb, em, g, k_tiles, kps, zs, c.err);
-  (*c.launches)++;
+  launch_pdl(c, kern, dim3(grid), dim3(TC_THREADS), TcCfg<BN>::SMEM, ta, tb, em, g, k_tiles, kps, zs, c.err);
   if (zs > 1) {
     const int64_t n4 = (int64_t)g.M * g.N / 4;
     int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)c.num_sms * 8);
-    splitk_reduce_kernel<<<blocks, 256, 0, c.stream>>>(static_cast<float*>(g.out), g.ldo, partial, zs, g.M, g.N);
-    (*c.launches)++;
+    launch_pdl(c, splitk_reduce_kernel, dim3(blocks), dim3(256), 0, static_cast<float*>(g.out), g.ldo, partial, zs, g.M, g.N);
   }
 }
 

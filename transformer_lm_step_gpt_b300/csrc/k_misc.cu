@@ -35,6 +35,8 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
 }
 
 __global__ void init_params_kernel(float* p, InitSpec s) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t total = s.off[16];
   const double sd = 0.02, sdr = 0.02 / sqrt(2.0 * (double)(s.L > 0 ? s.L : 1));
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < total;
@@ -64,23 +66,25 @@ __global__ void init_params_kernel(float* p, InitSpec s) {
 }
 
 void launch_init_params(LaunchCtx& c, float* params, const InitSpec& s) {
-  init_params_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(params, s);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, init_params_kernel, dim3(c.num_sms * 8), dim3(256), 0, params, s);
 }
 
 __global__ void f32_to_bf16_kernel(bf16* out, const float* in, int64_t n) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     out[i] = __float2bfloat16_rn(in[i]);
 }
 void launch_f32_to_bf16(LaunchCtx& c, bf16* out, const float* in, int64_t n) {
-  f32_to_bf16_kernel<<<c.num_sms * 8, 256, 0, c.stream>>>(out, in, n);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, f32_to_bf16_kernel, dim3(c.num_sms * 8), dim3(256), 0, out, in, n);
 }
 
 // ============================================================ encoder
 __global__ void encoder_fwd_kernel(float* out, const int32_t* tok, const float* wte,
                                    const float* wpe, int B, int T, int C, int V, int* err) {
+  pdl_trigger();
+  pdl_wait();
   const int C4 = C / 4;
   const int64_t n = (int64_t)B * T * C4;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
@@ -103,12 +107,13 @@ void launch_encoder_fwd(LaunchCtx& c, float* out, const int32_t* tok, const floa
                         const float* wpe, int B, int T, int C, int V) {
   const int64_t n = (int64_t)B * T * (C / 4);
   int grid = (int)std::min<int64_t>(cdiv(n, 256), (int64_t)c.num_sms * 16);
-  encoder_fwd_kernel<<<grid, 256, 0, c.stream>>>(out, tok, wte, wpe, B, T, C, V, c.err);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, encoder_fwd_kernel, dim3(grid), dim3(256), 0, out, tok, wte, wpe, B, T, C, V, c.err);
 }
 
 // dwpe[t, c] += sum_b dout[b, t, c], b in order.
 __global__ void encoder_bwd_wpe_kernel(float* dwpe, const float* dout, int B, int T, int C) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t n = (int64_t)T * C;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -122,6 +127,8 @@ __global__ void encoder_bwd_wpe_kernel(float* dwpe, const float* dout, int B, in
 // Sort the keys tok*M + position (one block, bitonic sort in shared memory);
 // equal tokens end up adjacent, in position order.
 __global__ void encoder_sort_kernel(uint32_t* sorted, const int32_t* tok, int M, int Vp, int P) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint32_t keys[];
   for (int i = threadIdx.x; i < P; i += blockDim.x) {
     uint32_t k = 0xFFFFFFFFu;
@@ -163,6 +170,8 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_
 // segments add straight into dwte; longer ones leave a partial per piece.
 __global__ void encoder_bwd_piece_kernel(float* dwte, float* partial, const float* dout,
                                          const uint32_t* sorted, int M, int C) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x;
   const uint32_t key = sorted[i];
   const uint32_t id = key / (uint32_t)M;
@@ -191,6 +200,8 @@ __global__ void encoder_bwd_piece_kernel(float* dwte, float* partial, const floa
 
 __global__ void encoder_bwd_combine_kernel(float* dwte, const float* partial,
                                            const uint32_t* sorted, int M, int C) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x;
   const uint32_t id = sorted[i] / (uint32_t)M;
   if (i > 0 && sorted[i - 1] / (uint32_t)M == id) return;  // not a segment start
@@ -217,20 +228,16 @@ void launch_encoder_bwd(LaunchCtx& c, float* dwte, float* dwpe, const float* dou
   {
     const int64_t n = (int64_t)T * C;
     int grid = (int)std::min<int64_t>(cdiv(n, 256), (int64_t)c.num_sms * 8);
-    encoder_bwd_wpe_kernel<<<grid, 256, 0, c.stream>>>(dwpe, dout, B, T, C);
-    LAUNCH_CHECK(c);
+    launch_pdl(c, encoder_bwd_wpe_kernel, dim3(grid), dim3(256), 0, dwpe, dout, B, T, C);
   }
   int P = 1;
   while (P < M) P <<= 1;
   const size_t smem = (size_t)P * sizeof(uint32_t);
   cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  encoder_sort_kernel<<<1, 1024, smem, c.stream>>>(sorted, tok, M, Vp, P);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, encoder_sort_kernel, dim3(1), dim3(1024), smem, sorted, tok, M, Vp, P);
   const int threads = std::min(1024, std::max(32, ((C / 4) + 31) / 32 * 32));
-  encoder_bwd_piece_kernel<<<M, threads, 0, c.stream>>>(dwte, partial, dout, sorted, M, C);
-  LAUNCH_CHECK(c);
-  encoder_bwd_combine_kernel<<<M, threads, 0, c.stream>>>(dwte, partial, sorted, M, C);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, encoder_bwd_piece_kernel, dim3(M), dim3(threads), 0, dwte, partial, dout, sorted, M, C);
+  launch_pdl(c, encoder_bwd_combine_kernel, dim3(M), dim3(threads), 0, dwte, partial, sorted, M, C);
 }
 
 // ============================================================ LayerNorm
@@ -268,6 +275,8 @@ __device__ __forceinline__ float4 load4<bf16>(const bf16* p) {
 template <typename OutT>
 __global__ void layernorm_fwd_kernel(OutT* out, float* mean, float* rstd, const float* inp,
                                      const float* w, const float* b, int N, int C) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * (blockDim.x >> 5) + warp;
   if (row >= N) return;
@@ -300,8 +309,7 @@ __global__ void layernorm_fwd_kernel(OutT* out, float* mean, float* rstd, const 
 template <typename OutT>
 void launch_layernorm_fwd(LaunchCtx& c, OutT* out, float* mean, float* rstd, const float* inp,
                           const float* w, const float* b, int N, int C) {
-  layernorm_fwd_kernel<OutT><<<cdiv(N, 8), 256, 0, c.stream>>>(out, mean, rstd, inp, w, b, N, C);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, layernorm_fwd_kernel<OutT>, dim3(cdiv(N, 8)), dim3(256), 0, out, mean, rstd, inp, w, b, N, C);
 }
 template void launch_layernorm_fwd<float>(LaunchCtx&, float*, float*, float*, const float*,
                                           const float*, const float*, int, int);
@@ -326,6 +334,8 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
     layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
                          const float* inp, const float* w, const float* mean, const float* rstd,
                          int N, int C, int accumulate) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float sm[];  // [3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float4 pw[NCH], pb[NCH], pr[NCH], old[NCH];
@@ -414,6 +424,8 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
 #define RP_GROUPS 32
 __global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
     reduce_partials_kernel(float* d0, float* d1, float* d2, const float* partial, int nb, int W, int seg) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sm[RP_GROUPS][RP_COLS + 1];
   const int lane = threadIdx.x % RP_COLS, grp = threadIdx.x / RP_COLS;
   const int c = blockIdx.x * RP_COLS + lane;
@@ -438,8 +450,7 @@ static void ln_bwd_launch(LaunchCtx& c, int nb, size_t smem, float* dres, ActT* 
                           const float* rstd, int N, int C, bool accumulate) {
   cudaFuncSetAttribute(layernorm_bwd_kernel<ActT, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  layernorm_bwd_kernel<ActT, NCH><<<nb, LNB_WARPS * 32, smem, c.stream>>>(
-      dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
+  launch_pdl(c, layernorm_bwd_kernel<ActT, NCH>, dim3(nb), dim3(LNB_WARPS * 32), smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
 }
 
 template <typename ActT>
@@ -461,9 +472,7 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
     default: ln_bwd_launch<ActT, 8>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
   }
   LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(3 * C, RP_COLS), RP_COLS * RP_GROUPS, 0, c.stream>>>(
-      dw, db, dres_colsum, partial, nb, 3 * C, C);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nb, 3 * C, C);
 }
 template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
                                           const float*, const float*, const float*, const float*,
@@ -500,6 +509,8 @@ __device__ __forceinline__ void load8<bf16>(const bf16* p, float* v) {
 // the chunk in order; the 8 group sums are added in group order.
 template <typename T>
 __global__ void __launch_bounds__(256) colsum_partial_kernel(float* partial, const T* x, int M, int N, int64_t ld) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sg[8][256];
   const int grp = threadIdx.x >> 5, t = threadIdx.x & 31;
   const int col = blockIdx.x * 256 + t * 8;
@@ -530,11 +541,8 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* partial, con
 template <typename T>
 void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
   dim3 grid(cdiv(N, 256), CS_CHUNKS);
-  colsum_partial_kernel<T><<<grid, 256, 0, c.stream>>>(partial, x, M, N, ld);
-  LAUNCH_CHECK(c);
-  reduce_partials_kernel<<<cdiv(N, RP_COLS), RP_COLS * RP_GROUPS, 0, c.stream>>>(
-      db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, colsum_partial_kernel<T>, dim3(grid), dim3(256), 0, partial, x, M, N, ld);
+  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(N, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
 }
 template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);
 template void launch_colsum<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t, float*);
@@ -558,6 +566,8 @@ __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float 
 template <typename T>
 __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* losses, const int32_t* targets, int V,
                                     int Vp, float dscale, int write_dlogits, int* err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sm_m[32], sm_s[32];
   const int64_t row = blockIdx.x;
   T* l = logits + row * Vp;
@@ -631,9 +641,8 @@ __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* los
 template <typename T>
 void launch_crossentropy(LaunchCtx& c, T* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dscale, bool dlogits) {
-  crossentropy_kernel<T><<<M, 512, 0, c.stream>>>(logits, losses, targets, V, Vp, dscale,
+  launch_pdl(c, crossentropy_kernel<T>, dim3(M), dim3(512), 0, logits, losses, targets, V, Vp, dscale,
                                                   dlogits ? 1 : 0, c.err);
-  LAUNCH_CHECK(c);
 }
 template void launch_crossentropy<float>(LaunchCtx&, float*, float*, const int32_t*, int, int, int,
                                          float, bool);
@@ -641,6 +650,8 @@ template void launch_crossentropy<bf16>(LaunchCtx&, bf16*, float*, const int32_t
                                         float, bool);
 
 __global__ void mean_kernel(float* out, const float* x, int M) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float sm[32];
   float s = 0.f;
   for (int i = threadIdx.x; i < M; i += blockDim.x) s += x[i];
@@ -654,14 +665,15 @@ __global__ void mean_kernel(float* out, const float* x, int M) {
   }
 }
 void launch_mean(LaunchCtx& c, float* out, const float* losses, int M) {
-  mean_kernel<<<1, 1024, 0, c.stream>>>(out, losses, M);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, mean_kernel, dim3(1), dim3(1024), 0, out, losses, M);
 }
 
 // ============================================================ AdamW
 __global__ void adamw_kernel(float* p, const float* g, float* m, float* v, bf16* shadow, int64_t n4,
                              float lr, float b1, float b2, float eps, float wd, float c1,
                              float c2) {
+  pdl_trigger();
+  pdl_wait();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     float4 pp = reinterpret_cast<float4*>(p)[i];
@@ -693,8 +705,7 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
                   float c2) {
   const int64_t n4 = n / 4;  // the parameter count is a multiple of 4 (C % 8 == 0)
   int grid = (int)std::min<int64_t>(cdiv(n4, 256), (int64_t)c.num_sms * 16);
-  adamw_kernel<<<grid, 256, 0, c.stream>>>(p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
-  LAUNCH_CHECK(c);
+  launch_pdl(c, adamw_kernel, dim3(grid), dim3(256), 0, p, g, m, v, shadow, n4, lr, b1, b2, eps, wd, c1, c2);
 }
 
 // ============================================================ allocation-free LayerNorm backward

@@ -20,6 +20,25 @@ struct LaunchCtx {
   int host_fail;      // set by a launcher that could not enqueue its kernel
 };
 
+// Launch kernel `k` on c.stream with programmatic stream serialisation
+// (the kernel calls pdl_trigger / pdl_wait, common.cuh) and count it.
+template <typename... KArgs, typename... Args>
+inline void launch_pdl(LaunchCtx& c, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...) != cudaSuccess) c.host_fail = 1;
+  (*c.launches)++;
+}
+
 // ---------------------------------------------------------------- init
 struct InitSpec {
   int64_t off[17];  // start of each of the 16 parameter tensors, off[16] = total
