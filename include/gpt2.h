@@ -241,10 +241,10 @@ GPT2_API const char* gpt2_last_error(const gpt2_model* m);
  *       accumulated into (the caller zeroes them for plain values);
  *   dout, inp [N, C], weight [C], mean, rstd [N]: inputs, read only;
  *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
- * Scratch: the per-block partial sums, ceil(N/32) * 3 * C floats, live in
- * one file-scope __device__ array of 2^21 floats (8 MiB) that every GPU
- * which loads the library holds until the process exits.  Larger sizes are
- * rejected with GPT2_ERR_ARG (N * C must stay below about 22.4 million);
+ * Scratch: the partial sums, ceil(N/8) * 3 * C floats, live in one
+ * file-scope __device__ array of 2^21 floats (8 MiB) that every GPU which
+ * loads the library holds until the process exits.  Larger sizes are
+ * rejected with GPT2_ERR_ARG (N * C must stay below about 5.59 million);
  * also GPT2_ERR_ARG for a NULL input/output or C outside [4, 1024] or
  * C % 4 != 0, GPT2_ERR_CUDA if a launch fails; gpt2_last_error(NULL) has
  * the text.  Every call on a device shares the array and leaves the last

@@ -85,7 +85,7 @@ def test_noalloc_layernorm_backward_matches_gpt2_backward():
 
 def test_noalloc_rejects_sizes_beyond_the_static_scratch():
     lib = tl.load_library()
-    big_n, C = 1 << 20, 1024  # ceil(N/32) * 3 * C = 3 * 2^25 floats > 2^21
+    big_n, C = 1 << 20, 1024  # ceil(N/8) * 3 * C = 3 * 2^27 floats > 2^21
     rc = lib.gpt2_layernorm_backward_noalloc(*([ctypes.c_void_p(16)] * 9), big_n, C, None)
     assert rc == -1
     assert b"static scratch" in lib.gpt2_last_error(None)

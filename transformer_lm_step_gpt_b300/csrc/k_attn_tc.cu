@@ -94,6 +94,60 @@ __device__ __forceinline__ void st_swz8(uint8_t* buf, int r, int c8, const float
   *reinterpret_cast<uint4*>(buf + atom * AT_TILE + r * 128 + chunk * 16) = u;
 }
 
+// Same as st_swz8 for a [128 x 64] buffer (one atom), given the row's base
+// pointer (buf + r*128) and its swizzle (r & 7).
+__device__ __forceinline__ void st_row8(uint8_t* rowp, int rx, int c8, const float* v) {
+  uint4 u;
+  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
+  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
+  u.x = *reinterpret_cast<uint32_t*>(&t0);
+  u.y = *reinterpret_cast<uint32_t*>(&t1);
+  u.z = *reinterpret_cast<uint32_t*>(&t2);
+  u.w = *reinterpret_cast<uint32_t*>(&t3);
+  *reinterpret_cast<uint4*>(rowp + ((c8 ^ rx) << 4)) = u;
+}
+
+// Backward elementwise step for 32 score columns of one row, from the TMEM
+// words of S (rs) and dP (rd):  p = 2^(s*sl2 - lse2),  ds = p (dp - D).
+// KEYROW: the row is a key and the columns are queries (dK/dV kernel; lse2
+// and D per column), else the row is a query (dQ kernel; per row).  MASK
+// applies the causal mask (only on sub-blocks that cross the diagonal).
+template <bool KEYROW, bool MASK>
+__device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32_t* rd, const float* lse2c,
+                                                const float* dc, float lse2r, float dr, float sl2,
+                                                int col0, int rowpos, uint8_t* prow, uint8_t* srow,
+                                                int rx, int c8base) {
+#pragma unroll
+  for (int g = 0; g < 4; g++) {
+    float lv[8], dv[8];
+    if (KEYROW) {
+      const float4 a = *reinterpret_cast<const float4*>(lse2c + g * 8);
+      const float4 b = *reinterpret_cast<const float4*>(lse2c + g * 8 + 4);
+      const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
+      const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
+      lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w; lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
+      dv[0] = c.x; dv[1] = c.y; dv[2] = c.z; dv[3] = c.w; dv[4] = d.x; dv[5] = d.y; dv[6] = d.z; dv[7] = d.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; j++) { lv[j] = lse2r; dv[j] = dr; }
+    }
+    float p[8], ds[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
+      if (MASK) {
+        const int col = col0 + g * 8 + j;
+        const bool ok = KEYROW ? col >= rowpos : col <= rowpos;
+        pv = ok ? pv : 0.f;
+      }
+      p[j] = pv;
+      ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
+    }
+    if (KEYROW) st_row8(prow, rx, c8base + g, p);
+    st_row8(srow, rx, c8base + g, ds);
+  }
+}
+
 __device__ __forceinline__ void store_row64_bf16(bf16* dst, const float* v, float mul) {
 #pragma unroll
   for (int i = 0; i < 64; i += 8) {
@@ -266,17 +320,30 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
     float sum = 0.f;
     uint8_t* P = sP + sb * AT_TILE;
+    uint8_t* prow = P + row * 128;
+    if (diag) {
 #pragma unroll
-    for (int g = 0; g < 4; g++) {
-      float p[8];
+      for (int g = 0; g < 4; g++) {
+        float p[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; jj++) {
-        const float s = __uint_as_float(r[g * 8 + jj]);
-        const bool ok = !diag || k0 + half * 32 + g * 8 + jj <= q;
-        p[jj] = ok ? ex2_hw(s * sl2 - mo) : 0.f;
-        sum += p[jj];
+        for (int jj = 0; jj < 8; jj++) {
+          const float e = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
+          p[jj] = k0 + half * 32 + g * 8 + jj <= q ? e : 0.f;
+          sum += p[jj];
+        }
+        st_row8(prow, row & 7, half * 4 + g, p);
       }
-      st_swz8(P, row, half * 4 + g, p);
+    } else {
+#pragma unroll
+      for (int g = 0; g < 4; g++) {
+        float p[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; jj++) {
+          p[jj] = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
+          sum += p[jj];
+        }
+        st_row8(prow, row & 7, half * 4 + g, p);
+      }
     }
     lpart = lpart * alpha + sum;
     m = mnew;
@@ -466,20 +533,12 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
       tmem_ld32(tS + lanebase + half * 32, rs);
       tmem_ld32(tdP + lanebase + half * 32, rd);
       tmem_ld_wait();
-#pragma unroll
-      for (int g = 0; g < 4; g++) {
-        float p[8], ds[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-          const int qc = half * 32 + g * 8 + j;
-          const bool ok = !diag || q0 + qc >= key;
-          const float pv = ok ? ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - sl[qc]) : 0.f;
-          p[j] = pv;
-          ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - sdd[qc]);
-        }
-        st_swz8(sP, row, half * 4 + g, p);
-        st_swz8(sS, row, half * 4 + g, ds);
-      }
+      if (diag)
+        bwd_elementwise<true, true>(rs, rd, sl + half * 32, sdd + half * 32, 0.f, 0.f, sl2, q0 + half * 32,
+                                    key, sP + row * 128, sS + row * 128, row & 7, half * 4);
+      else
+        bwd_elementwise<true, false>(rs, rd, sl + half * 32, sdd + half * 32, 0.f, 0.f, sl2, q0 + half * 32,
+                                     key, sP + row * 128, sS + row * 128, row & 7, half * 4);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -624,18 +683,12 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
       tmem_ld32(tS + lanebase + half * 32, rs);
       tmem_ld32(tdP + lanebase + half * 32, rd);
       tmem_ld_wait();
-#pragma unroll
-      for (int g = 0; g < 4; g++) {
-        float ds[8];
-#pragma unroll
-        for (int j = 0; j < 8; j++) {
-          const int kc = half * 32 + g * 8 + j;
-          const bool ok = !diag || k0 + kc <= q;
-          const float pv = ok ? ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - my_lse) : 0.f;
-          ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - my_d);
-        }
-        st_swz8(sS, row, half * 4 + g, ds);
-      }
+      if (diag)
+        bwd_elementwise<false, true>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
+                                     nullptr, sS + row * 128, row & 7, half * 4);
+      else
+        bwd_elementwise<false, false>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
+                                      nullptr, sS + row * 128, row & 7, half * 4);
     }
     fence_proxy_async_smem();
     tc_fence_before();

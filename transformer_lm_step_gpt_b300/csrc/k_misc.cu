@@ -316,17 +316,18 @@ template void launch_layernorm_fwd<float>(LaunchCtx&, float*, float*, float*, co
 template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, const float*,
                                          const float*, const float*, int, int);
 
-#define LNB_WARPS 8
-#define LNB_ROWS 32  // rows per block (4 per warp)
+#define LNB_WARPS 4
+#define LNB_ROWS_PER_WARP 8
+#define LNB_ROWS (LNB_WARPS * LNB_ROWS_PER_WARP)  // rows per block
 
-int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS) * 3 * C; }
+// one partial row (3*C floats) per warp
+int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS_PER_WARP) * 3 * C; }
 
 // One warp per row.  Each lane owns the float4 column chunks lane, lane+32,
 // ... (NCH = C/128 of them) and keeps its gamma / beta / residual-gradient
-// column partials in registers across the warp's rows; at the end the warps'
-// partials are summed in warp order through shared memory into one partial
-// per block (a single [3][C] buffer that the warps add into one after the
-// other, so little shared memory is taken from L1).  Pass 1 reads x and dy
+// column partials in registers across the warp's LNB_ROWS_PER_WARP rows,
+// then writes them as the warp's own partial row (no shared memory, no
+// block-wide barrier); reduce_partials_kernel adds the partial rows in order.  Pass 1 reads x and dy
 // for the two row sums (and prefetches the old residual gradient), pass 2
 // re-reads x and dy (L1 hits) to form dx.
 template <typename ActT, int NCH>
@@ -336,7 +337,6 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
                          int N, int C, int accumulate) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ float sm[];  // [3][C]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float4 pw[NCH], pb[NCH], pr[NCH], old[NCH];
 #pragma unroll
@@ -345,8 +345,9 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
     pb[k] = pw[k];
     pr[k] = pw[k];
   }
-  const int row0 = blockIdx.x * LNB_ROWS + warp * (LNB_ROWS / LNB_WARPS);
-  for (int rr = 0; rr < LNB_ROWS / LNB_WARPS; rr++) {
+  const int gwarp = blockIdx.x * LNB_WARPS + warp;
+  const int row0 = gwarp * LNB_ROWS_PER_WARP;
+  for (int rr = 0; rr < LNB_ROWS_PER_WARP; rr++) {
     const int row = row0 + rr;
     if (row >= N) break;
     const float* x = inp + (int64_t)row * C;
@@ -392,28 +393,17 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
       }
     }
   }
-  for (int wv = 0; wv < LNB_WARPS; wv++) {  // warp order
-    if (warp == wv) {
+  if (row0 >= N) return;
+  float* out = partial + (int64_t)gwarp * 3 * C;
 #pragma unroll
-      for (int k = 0; k < NCH; k++) {
-        const int c = (lane + 32 * k) * 4;
-        if (c < C) {
-          float4* a = reinterpret_cast<float4*>(sm + c);
-          float4* bq = reinterpret_cast<float4*>(sm + C + c);
-          float4* rq = reinterpret_cast<float4*>(sm + 2 * C + c);
-          if (wv == 0) { *a = pw[k]; *bq = pb[k]; *rq = pr[k]; }
-          else {
-            float4 t = *a; t.x += pw[k].x; t.y += pw[k].y; t.z += pw[k].z; t.w += pw[k].w; *a = t;
-            t = *bq; t.x += pb[k].x; t.y += pb[k].y; t.z += pb[k].z; t.w += pb[k].w; *bq = t;
-            t = *rq; t.x += pr[k].x; t.y += pr[k].y; t.z += pr[k].z; t.w += pr[k].w; *rq = t;
-          }
-        }
-      }
+  for (int k = 0; k < NCH; k++) {
+    const int c = (lane + 32 * k) * 4;
+    if (c < C) {
+      *reinterpret_cast<float4*>(out + c) = pw[k];
+      *reinterpret_cast<float4*>(out + C + c) = pb[k];
+      *reinterpret_cast<float4*>(out + 2 * C + c) = pr[k];
     }
-    __syncthreads();
   }
-  float* out = partial + (int64_t)blockIdx.x * 3 * C;
-  for (int c = threadIdx.x; c < 3 * C; c += blockDim.x) out[c] = sm[c];
 }
 
 // Sum nb partial rows of width W = parts * seg and add segment i into
@@ -459,7 +449,8 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial) {
   const int nb = cdiv(N, LNB_ROWS);
-  const size_t smem = (size_t)3 * C * sizeof(float);
+  const int nparts = cdiv(N, LNB_ROWS_PER_WARP);
+  const size_t smem = 0;
   const int nch = (C + 127) / 128;  // C <= 1024 keeps the partials in registers
   switch (nch) {
     case 1: ln_bwd_launch<ActT, 1>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
@@ -471,8 +462,7 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
     case 7: ln_bwd_launch<ActT, 7>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
     default: ln_bwd_launch<ActT, 8>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
   }
-  LAUNCH_CHECK(c);
-  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nb, 3 * C, C);
+  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nparts, 3 * C, C);
 }
 template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
                                           const float*, const float*, const float*, const float*,
@@ -710,7 +700,7 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
 
 // ============================================================ allocation-free LayerNorm backward
 // gpt2_layernorm_backward_noalloc: the LayerNorm backward above for callers
-// that cannot allocate device memory.  Its block partials (ceil(N/32) rows of
+// that cannot allocate device memory.  Its partial sums (ceil(N/8) rows of
 // 3*C floats) live in this file-scope array instead of caller- or
 // model-owned scratch; every GPU that loads the library holds it until the
 // process exits.
@@ -746,10 +736,10 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
     set_global_error("gpt2_layernorm_backward_noalloc: need N >= 1, 4 <= C <= 1024, C % 4 == 0");
     return GPT2_ERR_ARG;
   }
-  const int64_t need = (int64_t)cdiv(N, LNB_ROWS) * 3 * C;
+  const int64_t need = ln_partial_floats(N, C);
   if (need > NOALLOC_SCRATCH_FLOATS) {
-    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/32)*3*C exceeds the 2^21-float "
-                     "static scratch (N*C must stay below about 22.4 million)");
+    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/8)*3*C exceeds the 2^21-float "
+                     "static scratch (N*C must stay below about 5.59 million)");
     return GPT2_ERR_ARG;
   }
   int dev = 0;
