@@ -63,7 +63,9 @@ typedef enum { GPT2_FP32 = 0, GPT2_BF16 = 1 } gpt2_precision;
  * named after the run log's header block (max_seq_len, vocab_size,
  * num_layers, num_heads, channels) mean what they mean there.
  * Constraints (checked by gpt2_build, GPT2_ERR_ARG otherwise):
- *   num_layers >= 1; channels % num_heads == 0; channels % 8 == 0;
+ *   num_layers >= 1; 8 <= channels <= 1024 (the LayerNorm kernels keep a
+ *   row's per-column partial sums in registers); channels % num_heads == 0;
+ *   channels % 8 == 0;
  *   head size channels/num_heads in {16, 32, 64, 128};
  *   vocab_size <= padded_vocab_size and padded_vocab_size % 8 == 0;
  *   1 <= seq_len <= max_seq_len <= 4096; batch_size >= 1;

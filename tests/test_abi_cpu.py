@@ -43,6 +43,7 @@ def test_binding_covers_every_symbol():
     dict(Vp=260, V=256),         # Vp % 8 != 0
     dict(L=0),                   # no layers
     dict(B=64, T=1024, maxT=1024),  # B*T > 32768
+    dict(C=1280, NH=20),         # C > 1024
 ])
 def test_build_rejects_bad_config_without_gpu(bad):
     cfg = dict(L=2, C=64, NH=4, V=256, Vp=256, maxT=32, B=4, T=32)

@@ -491,9 +491,11 @@ int gpt2_build(const gpt2_config* cfg, uint64_t seed, gpt2_model** out) {
   if (!cfg) return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: cfg is NULL");
   const gpt2_config& k = *cfg;
   const int hs = k.num_heads > 0 ? k.channels / k.num_heads : 0;
-  if (k.num_layers < 1 || k.num_heads < 1 || k.channels < 8 || k.channels % k.num_heads != 0 ||
-      k.channels % 8 != 0 || !(hs == 16 || hs == 32 || hs == 64 || hs == 128))
-    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need L>=1, C%NH==0, C%8==0, head size in {16,32,64,128}");
+  if (k.num_layers < 1 || k.num_heads < 1 || k.channels < 8 || k.channels > 1024 ||
+      k.channels % k.num_heads != 0 || k.channels % 8 != 0 ||
+      !(hs == 16 || hs == 32 || hs == 64 || hs == 128))
+    return fail(nullptr, GPT2_ERR_ARG,
+                "gpt2_build: need L>=1, 8<=C<=1024, C%NH==0, C%8==0, head size in {16,32,64,128}");
   if (k.vocab_size < 1 || k.padded_vocab_size < k.vocab_size || k.padded_vocab_size % 8 != 0)
     return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need 1 <= V <= Vp and Vp % 8 == 0");
   if (k.seq_len < 1 || k.seq_len > k.max_seq_len || k.max_seq_len > 4096 || k.batch_size < 1 ||

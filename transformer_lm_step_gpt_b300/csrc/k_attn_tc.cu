@@ -108,24 +108,28 @@ __device__ __forceinline__ void st_row8(uint8_t* rowp, int rx, int c8, const flo
 }
 
 // Backward elementwise step for 32 score columns of one row, from the TMEM
-// words of S (rs) and dP (rd):  p = 2^(s*sl2 - lse2),  ds = p (dp - D).
-// KEYROW: the row is a key and the columns are queries (dK/dV kernel; lse2
-// and D per column), else the row is a query (dQ kernel; per row).  MASK
-// applies the causal mask (only on sub-blocks that cross the diagonal).
+// words of S (rs) and dP (rd):  p = 2^(s*sl2 - lse*log2e),  ds = p (dp - D).
+// KEYROW: the row is a key and the columns are queries (dK/dV kernel; lse
+// in natural-log units and D per column, from shared memory), else the row
+// is a query (dQ kernel; lse2r = lse*log2e and dr per row).  MASK applies
+// the causal mask and, for KEYROW, drops columns at or past colmax (only on
+// sub-blocks that cross the diagonal or the end of the sequence).
 template <bool KEYROW, bool MASK>
-__device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32_t* rd, const float* lse2c,
+__device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32_t* rd, const float* lsec,
                                                 const float* dc, float lse2r, float dr, float sl2,
                                                 int col0, int rowpos, uint8_t* prow, uint8_t* srow,
-                                                int rx, int c8base) {
+                                                int rx, int c8base, int colmax = 0) {
 #pragma unroll
   for (int g = 0; g < 4; g++) {
     float lv[8], dv[8];
     if (KEYROW) {
-      const float4 a = *reinterpret_cast<const float4*>(lse2c + g * 8);
-      const float4 b = *reinterpret_cast<const float4*>(lse2c + g * 8 + 4);
+      const float4 a = *reinterpret_cast<const float4*>(lsec + g * 8);
+      const float4 b = *reinterpret_cast<const float4*>(lsec + g * 8 + 4);
       const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
       const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
-      lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w; lv[4] = b.x; lv[5] = b.y; lv[6] = b.z; lv[7] = b.w;
+      const float L2E = 1.4426950408889634f;
+      lv[0] = a.x * L2E; lv[1] = a.y * L2E; lv[2] = a.z * L2E; lv[3] = a.w * L2E;
+      lv[4] = b.x * L2E; lv[5] = b.y * L2E; lv[6] = b.z * L2E; lv[7] = b.w * L2E;
       dv[0] = c.x; dv[1] = c.y; dv[2] = c.z; dv[3] = c.w; dv[4] = d.x; dv[5] = d.y; dv[6] = d.z; dv[7] = d.w;
     } else {
 #pragma unroll
@@ -134,14 +138,17 @@ __device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32
     float p[8], ds[8];
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-      float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
-      if (MASK) {
+      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
+      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
+      float pk = pv;
+      if (MASK) {  // a masked column may hold stale lse / D: select, do not scale
         const int col = col0 + g * 8 + j;
-        const bool ok = KEYROW ? col >= rowpos : col <= rowpos;
-        pv = ok ? pv : 0.f;
+        const bool ok = KEYROW ? (col >= rowpos && col < colmax) : col <= rowpos;
+        pk = ok ? pk : 0.f;
+        dsv = ok ? dsv : 0.f;
       }
-      p[j] = pv;
-      ds[j] = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
+      p[j] = pk;
+      ds[j] = dsv;
     }
     if (KEYROW) st_row8(prow, rx, c8base + g, p);
     st_row8(srow, rx, c8base + g, ds);
@@ -224,9 +231,9 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint64_t* p_ready = bars + 9;  // 8 warp arrivals per sub-block
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
 
-  const int nqb = gridDim.x;
-  const int qb = nqb - 1 - blockIdx.x;  // longest rows first
-  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  const int nqb = gridDim.y;
+  const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the longest rows
+  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
@@ -432,15 +439,36 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 }
 
 // ============================================================ backward: dK, dV
-// One CTA per (128-key block, b*h); the queries are walked in 64-row
-// sub-blocks so that a CTA needs 256 TMEM columns and ~97 KB of shared
-// memory and two CTAs share an SM (one's MMAs overlap the other's
-// elementwise work).
-// smem: K | V | Q0 Q1 | dO0 dO1 (64-row tiles) | P^T | dS^T ([128 x 64]) |
-//       lse[64] D[64] | barriers
-#define AKV_SMEM (1024 + 2 * AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 512 + 256)
+// One CTA per (128-key block, b*h), queries walked in 64-row sub-blocks,
+// warp-specialised so the tensor core never waits for the elementwise work:
+//   warp 9      loader: TMA of q and dy sub-blocks into a DKV_STAGES-deep
+//               ring, with each sub-block's lse and D (bulk copies on the
+//               same barrier when T is a multiple of 4; otherwise all of the
+//               block's lse / D are read once, before the first sub-block)
+//   warp 8      MMA issuer: S^T(j) = K q(j)^T and dP^T(j) = V dy(j)^T into
+//               TMEM buffer j%2, then dV += P^T(j-1) dy(j-1), dK += dS^T(j-1)
+//               q(j-1) -- so sub-block j's scores are computed while the
+//               compute warps work on j-1
+//   warps 0..7  compute: P^T = 2^(S^T*scale*log2e - lse*log2e), dS^T = P^T
+//               (dP^T - D) into shared-memory buffer j%2 (two per TMEM lane
+//               quarter, splitting the 64 query columns)
+// A q / dy stage is refilled only once dV, dK of its sub-block are done, so
+// the ring is deep enough to cover that round trip plus the TMA latency.
+// TMEM: [S^T | dP^T] x 2 buffers, dV, dK (384 of 512 columns).
+// smem: K | V | DKV_STAGES x (q, dy) | 2 x (P^T, dS^T) | barriers | lse / D
+// (per stage: [DKV_STAGES][lse 64, D 64]; whole block: lse[Tq], D[Tq] with
+// Tq = T - k0 rounded up to 64).  The grid's y index is the key block, so
+// the hardware starts the longest blocks (most queries) first.
+#define DKV_STAGES 6
+#define DKV_THREADS (AT_THREADS + 64)
+#define AKV_FIXED (1024 + 2 * AT_TILE + DKV_STAGES * 2 * AT_SUBTILE + 4 * AT_TILE + 256)
+static inline bool akv_staged_ld(int T) { return T % 4 == 0; }
+static inline size_t akv_smem(int T) {
+  const size_t whole = 8 * (size_t)((T + 63) / 64 * 64);
+  return AKV_FIXED + (akv_staged_ld(T) ? (size_t)DKV_STAGES * 512 : whole);
+}
 
-__global__ void __launch_bounds__(AT_THREADS, 2)
+__global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                            const __grid_constant__ CUtensorMap tm_qkv64,
                            const __grid_constant__ CUtensorMap tm_dy64, bf16* dqkv, const float* lse,
@@ -450,144 +478,193 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint8_t* sm = align1024(smraw);
   uint8_t* sK = sm;
   uint8_t* sV = sm + AT_TILE;
-  uint8_t* sQ = sm + 2 * AT_TILE;                   // 2 stages of [64 x 64]
-  uint8_t* sD = sQ + 2 * AT_SUBTILE;                // dO, 2 stages
-  uint8_t* sP = sD + 2 * AT_SUBTILE;                // P^T  [128 keys x 64 queries]
-  uint8_t* sS = sP + AT_TILE;                       // dS^T [128 keys x 64 queries]
-  float* sl = reinterpret_cast<float*>(sS + AT_TILE);  // lse[64] (log2 units)
-  float* sdd = sl + 64;                                 // D[64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + AT_TILE + 512);
+  uint8_t* sQ = sm + 2 * AT_TILE;                     // [DKV_STAGES] x [64 x 64]
+  uint8_t* sD = sQ + DKV_STAGES * AT_SUBTILE;         // dy, [DKV_STAGES]
+  uint8_t* sP = sD + DKV_STAGES * AT_SUBTILE;         // P^T  [2] x [128 keys x 64 queries]
+  uint8_t* sS = sP + 2 * AT_TILE;                     // dS^T [2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * AT_TILE);
   uint64_t* kv_full = bars;
-  uint64_t* q_full = bars + 1;  // [2]
-  uint64_t* s_done = bars + 3;
-  uint64_t* o_done = bars + 4;
-  uint64_t* p_ready = bars + 5;  // 8 warp arrivals per sub-block
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
-
-  const int kb = (int)gridDim.x - 1 - (int)blockIdx.x;  // key block; longest first
-  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  uint64_t* ld_full = bars + 1;                  // whole-block lse / D written
+  uint64_t* q_full = bars + 2;                   // [DKV_STAGES]: TMA bytes
+  uint64_t* q_empty = q_full + DKV_STAGES;       // [DKV_STAGES]: MMA commit
+  uint64_t* s_full = q_empty + DKV_STAGES;       // [2]: S^T, dP^T ready
+  uint64_t* s_empty = s_full + 2;                // [2]: compute warps have read them
+  uint64_t* p_full = s_empty + 2;                // [2]: P^T, dS^T written
+  uint64_t* p_empty = p_full + 2;                // [2]: dV/dK MMAs have read them
+  uint64_t* done = p_empty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  float* sLD = reinterpret_cast<float*>(sS + 2 * AT_TILE + 256);
+  const int kb = blockIdx.y;  // key block
+  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int k0 = kb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row = quarter * 32 + lane, key = k0 + row;
   const int nsub = (T - k0 + AB_SUB - 1) / AB_SUB;  // 64-query sub-blocks from k0 to T
+  const bool staged = (T & 3) == 0;                 // per-stage lse / D bulk copies
 
   if (tid == 0) {
-    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
-    mbar_init(p_ready, AT_THREADS / 32);
+    mbar_init(kv_full, 1);
+    mbar_init(ld_full, 1);
+    for (int s = 0; s < DKV_STAGES; s++) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 8); mbar_init(&p_empty[i], 1);
+    }
+    mbar_init(done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_qkv64);
     tma_prefetch_desc(&tm_dy64);
   }
-  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
+  if (warp == 8) { tmem_alloc(tslot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
   pdl_wait();  // from here on global memory written by the previous kernel is read
-  const uint32_t tS = tm, tdP = tm + 64, tdV = tm + 128, tdK = tm + 192;
-  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
-
-  if (tid == 0) {
-    mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
-    tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, k0, b);
-    tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, k0, b);
-    for (int s = 0; s < 2 && s < nsub; s++) {
-      mbar_arrive_expect_tx(&q_full[s], 2 * AT_SUBTILE);
-      tma_load_3d(sQ + s * AT_SUBTILE, &tm_qkv64, &q_full[s], h * AT_HS, k0 + s * AB_SUB, b);
-      tma_load_3d(sD + s * AT_SUBTILE, &tm_dy64, &q_full[s], h * AT_HS, k0 + s * AB_SUB, b);
-    }
-  }
+  const uint32_t tdV = tm + 256, tdK = tm + 320;
   const float sl2 = scale * 1.4426950408889634f;
-  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
-  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+  const float* lrow = lse + (int64_t)bh * T + k0;
+  const float* drow = dsum + (int64_t)bh * T + k0;
 
-  for (int it = 0; it < nsub; it++) {
-    const int q0 = k0 + it * AB_SUB;
-    const int st = it & 1;
-    const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-    if (tid < AB_SUB) {  // this sub-block's lse (log2 units) and D
-      const int qq = q0 + tid;
-      sl[tid] = qq < T ? lse[(int64_t)bh * T + qq] * 1.4426950408889634f : INFINITY;
-      sdd[tid] = qq < T ? dsum[(int64_t)bh * T + qq] : 0.f;
+  if (warp == 9) {
+    // ---------------------------------------------------------------- loader
+    auto issue = [&](int j) {
+      const int s = j % DKV_STAGES, q0 = k0 + j * AB_SUB;
+      const uint32_t ldb = staged ? 4u * (uint32_t)min(AB_SUB, T - q0) : 0u;  // a multiple of 16
+      mbar_arrive_expect_tx(&q_full[s], 2 * AT_SUBTILE + 2 * ldb);
+      tma_load_3d(sQ + s * AT_SUBTILE, &tm_qkv64, &q_full[s], h * AT_HS, q0, b);
+      tma_load_3d(sD + s * AT_SUBTILE, &tm_dy64, &q_full[s], h * AT_HS, q0, b);
+      if (staged) {
+        bulk_load(sLD + s * 128, lrow + j * AB_SUB, ldb, &q_full[s]);
+        bulk_load(sLD + s * 128 + 64, drow + j * AB_SUB, ldb, &q_full[s]);
+      }
+    };
+    int j = 0;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
+      tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, k0, b);
+      tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, k0, b);
+      for (; j < nsub && j < DKV_STAGES; j++) issue(j);
     }
-    if (tid == 0) {
-      if (it == 0) mbar_wait(kv_full, 0, err);
-      mbar_wait(&q_full[st], ph, err);
-      tc_fence_after();
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      const uint32_t bQ = smem_u32(sQ + st * AT_SUBTILE), bD = smem_u32(sD + st * AT_SUBTILE);
+    if (!staged) {
+      float* sL = sLD;
+      float* sDd = sLD + nsub * AB_SUB;
+      const int nq = nsub * AB_SUB;
+      for (int i0 = 0; i0 < nq; i0 += 32 * 16) {  // 32 loads in flight per lane
+        float lv[16], dv[16];
 #pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
+        for (int u = 0; u < 16; u++) {
+          const int i = i0 + u * 32 + lane;
+          const bool in = i < nq && k0 + i < T;
+          lv[u] = in ? __ldg(lrow + i) : 0.f;
+          dv[u] = in ? __ldg(drow + i) : 0.f;
+        }
 #pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
-      tc_commit(s_done);
+        for (int u = 0; u < 16; u++) {
+          const int i = i0 + u * 32 + lane;
+          if (i < nq) { sL[i] = lv[u]; sDd[i] = dv[u]; }
+        }
+      }
     }
-    __syncthreads();  // lse / D of this sub-block visible
-    mbar_wait(s_done, (uint32_t)it & 1u, err);
-    tc_fence_after();
-    const bool diag = q0 < k0 + AT_BLK;
-    {
-      uint32_t rs[32], rd[32];
-      tmem_ld32(tS + lanebase + half * 32, rs);
-      tmem_ld32(tdP + lanebase + half * 32, rd);
-      tmem_ld_wait();
-      if (diag)
-        bwd_elementwise<true, true>(rs, rd, sl + half * 32, sdd + half * 32, 0.f, 0.f, sl2, q0 + half * 32,
-                                    key, sP + row * 128, sS + row * 128, row & 7, half * 4);
-      else
-        bwd_elementwise<true, false>(rs, rd, sl + half * 32, sdd + half * 32, 0.f, 0.f, sl2, q0 + half * 32,
-                                     key, sP + row * 128, sS + row * 128, row & 7, half * 4);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(p_ready);
-    if (tid == 0) {
-      mbar_wait(p_ready, (uint32_t)it & 1u, err);
+    if (lane == 0) {
+      mbar_arrive(ld_full);
+      for (j = DKV_STAGES; j < nsub; j++) {
+        mbar_wait(&q_empty[j % DKV_STAGES], ((uint32_t)(j / DKV_STAGES) & 1u) ^ 1u, err);
+        issue(j);
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
+      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+      mbar_wait(kv_full, 0, err);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      for (int j = 0; j <= nsub; j++) {
+        if (j < nsub) {
+          const int s = j % DKV_STAGES, bf = j & 1;
+          mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);
+          mbar_wait(&s_empty[bf], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);
+          tc_fence_after();
+          const uint32_t bQ = smem_u32(sQ + s * AT_SUBTILE), bD = smem_u32(sD + s * AT_SUBTILE);
+          const uint32_t tS = tm + (uint32_t)(bf * 128), tP = tS + 64;
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tP, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
+          tc_commit(&s_full[bf]);
+        }
+        if (j >= 1) {
+          const int jj = j - 1, s = jj % DKV_STAGES, bf = jj & 1;
+          mbar_wait(&p_full[bf], (uint32_t)(jj >> 1) & 1u, err);
+          tc_fence_after();
+          const uint32_t aP = smem_u32(sP + bf * AT_TILE), aS = smem_u32(sS + bf * AT_TILE);
+          const uint32_t bQ = smem_u32(sQ + s * AT_SUBTILE), bD = smem_u32(sD + s * AT_SUBTILE);
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdV, kmaj(aP, kk), mnmaj(bD, kk), idO, (jj > 0 || kk > 0));
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdK, kmaj(aS, kk), mnmaj(bQ, kk), idO, (jj > 0 || kk > 0));
+          tc_commit(&p_empty[bf]);
+          tc_commit(&q_empty[s]);
+        }
+      }
+      tc_commit(done);
+    }
+  } else {
+    // ---------------------------------------------------------------- compute warps
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane, key = k0 + row;
+    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
+    mbar_wait(ld_full, 0, err);
+    for (int j = 0; j < nsub; j++) {
+      const int bf = j & 1, s = j % DKV_STAGES;
+      const int q0 = k0 + j * AB_SUB;
+      mbar_wait(&s_full[bf], (uint32_t)(j >> 1) & 1u, err);
       tc_fence_after();
-      const uint32_t aP = smem_u32(sP), aS = smem_u32(sS);
-      const uint32_t bQ = smem_u32(sQ + st * AT_SUBTILE), bD = smem_u32(sD + st * AT_SUBTILE);
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdV, kmaj(aP, kk), mnmaj(bD, kk), idO, (it > 0 || kk > 0));
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdK, kmaj(aS, kk), mnmaj(bQ, kk), idO, (it > 0 || kk > 0));
-      tc_commit(o_done);
+      uint32_t rs[32], rd[32];
+      const uint32_t tS = tm + (uint32_t)(bf * 128);
+      tmem_ld32(tS + lanebase + half * 32, rs);
+      tmem_ld32(tS + 64 + lanebase + half * 32, rd);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[bf]);
+      mbar_wait(&p_empty[bf], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);  // P^T / dS^T buffer free
+      if (staged) mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);  // the stage's lse / D
+      const float* lc = staged ? sLD + s * 128 + half * 32 : sLD + j * AB_SUB + half * 32;
+      const float* dc = staged ? sLD + s * 128 + 64 + half * 32 : sLD + (nsub + j) * AB_SUB + half * 32;
+      uint8_t* prow = sP + bf * AT_TILE + row * 128;
+      uint8_t* srow = sS + bf * AT_TILE + row * 128;
+      if (q0 < k0 + AT_BLK || q0 + AB_SUB > T)
+        bwd_elementwise<true, true>(rs, rd, lc, dc, 0.f, 0.f, sl2, q0 + half * 32, key, prow, srow,
+                                    row & 7, half * 4, T);
+      else
+        bwd_elementwise<true, false>(rs, rd, lc, dc, 0.f, 0.f, sl2, q0 + half * 32, key, prow, srow,
+                                     row & 7, half * 4);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[bf]);
     }
-    mbar_wait(o_done, (uint32_t)it & 1u, err);
+    mbar_wait(done, 0, err);
     tc_fence_after();
-    if (tid == 0 && it + 2 < nsub) {
-      mbar_arrive_expect_tx(&q_full[st], 2 * AT_SUBTILE);
-      tma_load_3d(sQ + st * AT_SUBTILE, &tm_qkv64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
-      tma_load_3d(sD + st * AT_SUBTILE, &tm_dy64, &q_full[st], h * AT_HS, q0 + 2 * AB_SUB, b);
-    }
-    // every thread has waited o_done: the P^T / dS^T / lse buffers are free
-    tc_fence_before();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const int64_t C3 = 3 * (int64_t)C;
-  float v[32];
-  {
+    const int64_t C3 = 3 * (int64_t)C;
+    float v[32];
     uint32_t r[32];
     tmem_ld32(tdV + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
-  }
-  if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS + half * 32, v, 1.f);
-  {
-    uint32_t r[32];
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS + half * 32, v, 1.f);
     tmem_ld32(tdK + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
   }
-  if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
+  if (warp == 8) { tc_fence_after(); tmem_dealloc(tm, 512); }
 }
 
 // ============================================================ backward: dQ
@@ -617,9 +694,9 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint64_t* p_ready = bars + 5;  // 8 warp arrivals per sub-block
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
 
-  const int nqb = gridDim.x;
-  const int qb = nqb - 1 - blockIdx.x;
-  const int bh = blockIdx.y, b = bh / NH, h = bh % NH;
+  const int nqb = gridDim.y;
+  const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the blocks that meet the most keys
+  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, half = warp >> 2;
@@ -740,7 +817,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
     c.host_fail = 1;
     return;
   }
-  dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
+  dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
   cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
   launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AT_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
 }
@@ -761,9 +838,10 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
   const int64_t n = (int64_t)B * T * NH;
   launch_pdl(c, attn_bwd_dsum_kernel, dim3((int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16)), dim3(256), 0, dsum, dy, y, B, T, C, NH);
   const float scale = 1.f / sqrtf((float)AT_HS);
-  dim3 grid((T + AT_BLK - 1) / AT_BLK, B * NH);
-  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AKV_SMEM);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(AT_THREADS), AKV_SMEM, tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
+  const size_t kv_smem = akv_smem(T);
+  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_smem);
+  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
   launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AT_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, T, C, NH, scale, c.err);
 }

@@ -29,6 +29,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 
@@ -95,15 +96,15 @@ __host__ __device__ constexpr uint32_t tc_idesc(int N, bool a_mn, bool b_mn) {
 struct TileCoord {
   int split, mt, nt;
 };
-__device__ __forceinline__ TileCoord tile_coord(int t, int mtiles, int ntiles) {
+__device__ __forceinline__ TileCoord tile_coord(int t, int mtiles, int ntiles, int gm) {
   TileCoord c;
   const int per = mtiles * ntiles;
   c.split = t / per;
   const int r = t - c.split * per;
-  const int group = r / (GROUP_M * ntiles);
-  const int first_m = group * GROUP_M;
-  const int gsize = min(mtiles - first_m, GROUP_M);
-  const int idx = r - group * GROUP_M * ntiles;
+  const int group = r / (gm * ntiles);
+  const int first_m = group * gm;
+  const int gsize = min(mtiles - first_m, gm);
+  const int idx = r - group * gm * ntiles;
   c.mt = first_m + idx % gsize;
   c.nt = idx / gsize;
   return c;
@@ -136,6 +137,148 @@ __device__ __forceinline__ void get8_bf16(const uint8_t* p, float* v) {
 struct EpiMaps {
   CUtensorMap out, out2, aux;
 };
+
+// The bias of the warp's BN/2 columns of a tile, 4 per lane (lane l holds
+// columns 4l..4l+3 of the half), loaded before the accumulator is waited
+// for so that the global-load latency is hidden; read back by shuffles.
+template <int BN>
+__device__ __forceinline__ float4 load_bias4(const GemmArgs& g, bool use_bias, int n0, int half, int lane) {
+  float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int n = n0 + half * (BN / 2) + 4 * lane;
+  if (!use_bias || 4 * lane >= BN / 2) return b;
+  if (n + 4 <= g.N) return *reinterpret_cast<const float4*>(g.bias + n);
+  if (n < g.N) b.x = g.bias[n];
+  if (n + 1 < g.N) b.y = g.bias[n + 1];
+  if (n + 2 < g.N) b.z = g.bias[n + 2];
+  return b;
+}
+
+// Epilogue of one accumulator tile for one epilogue warp: 32 rows (this
+// warp's TMEM lane quarter, global rows mrow..mrow+31) by the warp's column
+// half of the BN columns starting at n0.  taddr: TMEM address of the
+// accumulator at (lane quarter, column 0); bq: load_bias4 of the tile.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& em, uint8_t* stg,
+                                              uint64_t* abar, uint32_t& aux_phase, uint32_t taddr0,
+                                              int half, int lane, int mrow, int n0, int split_idx,
+                                              bool split, bool f32, bool has_aux, bool use_bias,
+                                              float4 bq, int* err) {
+  const int epi = g.epi;
+  const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
+#pragma unroll 1
+  for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += CW) {
+    const int ncol = n0 + cc;
+    if (ncol >= g.N) break;
+    if (lane == 0) bulk_wait_read0();  // staging no longer read by earlier stores
+    __syncwarp();
+    if (has_aux && lane == 0) {
+      mbar_arrive_expect_tx(abar, STG_BYTES);
+      tma_load_2d(stg, &em.aux, abar, ncol, mrow);
+    }
+    float v[64];
+    const uint32_t taddr = taddr0 + (uint32_t)cc;
+    {
+      uint32_t r[32];
+      tmem_ld32(taddr, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+      if (!f32) {
+        tmem_ld32(taddr + 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j++) v[32 + j] = __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int j = 32; j < 64; j++) v[j] = 0.f;
+      }
+    }
+    if (use_bias) {
+      const int lb = (cc - half * (BN / 2)) >> 2;  // lane holding this chunk's first 4 columns
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        if (j < CW) {
+          const int src = lb + (j >> 2);
+          v[j] += __shfl_sync(0xffffffffu, bq.x, src);
+          v[j + 1] += __shfl_sync(0xffffffffu, bq.y, src);
+          v[j + 2] += __shfl_sync(0xffffffffu, bq.z, src);
+          v[j + 3] += __shfl_sync(0xffffffffu, bq.w, src);
+        }
+      }
+    }
+    if (has_aux) {
+      mbar_wait(abar, aux_phase, err);
+      aux_phase ^= 1u;
+    }
+    // results (and the auxiliary input) in the thread's staging row
+    if (f32) {
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        float4* p = reinterpret_cast<float4*>(stg + stg_off(lane, c));
+        float4 o = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        if (has_aux) {  // EPI_RESIDUAL: out = residual + (acc + bias)
+          const float4 r = *p;
+          o.x = r.x + o.x; o.y = r.y + o.y; o.z = r.z + o.z; o.w = r.w + o.w;
+        }
+        *p = o;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        uint8_t* p = stg + stg_off(lane, c);
+        float o[8];
+        if (has_aux) {  // EPI_GELU_BWD: out = acc * gelu'(pre-activation)
+          float hv[8];
+          get8_bf16(p, hv);
+#pragma unroll
+          for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * gelu_grad_hw(hv[q]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
+        }
+        put8_bf16(p, o);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (split) tma_store_3d(&em.out, stg, ncol, mrow, split_idx);
+      else if (epi == EPI_ACCUM) tma_reduce_add_2d(&em.out, stg, ncol, mrow);
+      else tma_store_2d(&em.out, stg, ncol, mrow);
+      bulk_commit();
+    }
+    if (epi == EPI_BIAS_GELU && !split) {  // second output: gelu(pre-activation)
+      if (lane == 0) bulk_wait_read0();
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 8; c++) {
+        float o[8];
+#pragma unroll
+        for (int q = 0; q < 8; q++) o[q] = gelu_hw(v[8 * c + q]);
+        put8_bf16(stg + stg_off(lane, c), o);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&em.out2, stg, ncol, mrow);
+        bulk_commit();
+      }
+    }
+  }
+}
+
+struct EpiFlags {
+  bool split, f32, has_aux, use_bias;
+};
+__device__ __forceinline__ EpiFlags epi_flags(const GemmArgs& g, int splits) {
+  EpiFlags f;
+  const int epi = g.epi;
+  f.split = splits > 1;
+  f.f32 = f.split || epi == EPI_RESIDUAL || epi == EPI_ACCUM || (epi == EPI_STORE && g.out_f32);
+  f.has_aux = !f.split && (epi == EPI_RESIDUAL || epi == EPI_GELU_BWD);
+  f.use_bias = !f.split && g.bias && (epi == EPI_STORE || epi == EPI_BIAS_GELU || epi == EPI_RESIDUAL);
+  return f;
+}
 
 template <int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -181,7 +324,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if (lane == 0) {
       int it = 0;  // running k-tile counter over all tiles of this CTA
       for (int t = blockIdx.x; t < total; t += gridDim.x) {
-        const TileCoord tc = tile_coord(t, mtiles, ntiles);
+        const TileCoord tc = tile_coord(t, mtiles, ntiles, GROUP_M);
         const int m0 = tc.mt * TC_BM, n0 = tc.nt * BN;
         const int kt0 = tc.split * k_per_split;
         const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
@@ -213,7 +356,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       constexpr uint32_t idesc = tc_idesc(BN, !A_K, !B_K);
       int it = 0, ti = 0;
       for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
-        const TileCoord tc = tile_coord(t, mtiles, ntiles);
+        const TileCoord tc = tile_coord(t, mtiles, ntiles, GROUP_M);
         const int kt0 = tc.split * k_per_split;
         const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
         const int a = ti & 1;
@@ -241,124 +384,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
-    uint8_t* stg = staging + (size_t)ew * STG_BYTES;
-    uint64_t* abar = &aux_bar[ew];
-    const bool split = splits > 1;
-    const int epi = g.epi;
-    const bool f32 = split || epi == EPI_RESIDUAL || epi == EPI_ACCUM || (epi == EPI_STORE && g.out_f32);
-    const bool has_aux = !split && (epi == EPI_RESIDUAL || epi == EPI_GELU_BWD);
-    const bool use_bias = !split && g.bias && (epi == EPI_STORE || epi == EPI_BIAS_GELU || epi == EPI_RESIDUAL);
-    const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
+    const EpiFlags f = epi_flags(g, splits);
     uint32_t aux_phase = 0;
     int ti = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
-      const TileCoord tc = tile_coord(t, mtiles, ntiles);
-      const int m0 = tc.mt * TC_BM, n0 = tc.nt * BN;
+      const TileCoord tc = tile_coord(t, mtiles, ntiles, GROUP_M);
       const int a = ti & 1;
-      const int mrow = m0 + quarter * 32;
+      const float4 bq = load_bias4<BN>(g, f.use_bias, tc.nt * BN, half, lane);
       mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
       tc_fence_after();
-#pragma unroll 1
-      for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += CW) {
-        const int ncol = n0 + cc;
-        if (ncol >= g.N) break;
-        if (lane == 0) bulk_wait_read0();  // staging no longer read by earlier stores
-        __syncwarp();
-        if (has_aux && lane == 0) {
-          mbar_arrive_expect_tx(abar, STG_BYTES);
-          tma_load_2d(stg, &em.aux, abar, ncol, mrow);
-        }
-        float v[64];
-        const uint32_t taddr = tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16) + (uint32_t)cc;
-        {
-          uint32_t r[32];
-          tmem_ld32(taddr, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
-          if (!f32) {
-            tmem_ld32(taddr + 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j++) v[32 + j] = __uint_as_float(r[j]);
-          } else {
-#pragma unroll
-            for (int j = 32; j < 64; j++) v[j] = 0.f;
-          }
-        }
-        if (use_bias) {
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            if (j < CW) {
-              const int n = ncol + j;
-              if (n + 4 <= g.N) {
-                const float4 bb = *reinterpret_cast<const float4*>(g.bias + n);
-                v[j] += bb.x; v[j + 1] += bb.y; v[j + 2] += bb.z; v[j + 3] += bb.w;
-              } else {
-                for (int q = 0; q < 4; q++) if (n + q < g.N) v[j + q] += g.bias[n + q];
-              }
-            }
-          }
-        }
-        if (has_aux) {
-          mbar_wait(abar, aux_phase, err);
-          aux_phase ^= 1u;
-        }
-        // results (and the auxiliary input) in the thread's staging row
-        if (f32) {
-#pragma unroll
-          for (int c = 0; c < 8; c++) {
-            float4* p = reinterpret_cast<float4*>(stg + stg_off(lane, c));
-            float4 o = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-            if (has_aux) {  // EPI_RESIDUAL: out = residual + (acc + bias)
-              const float4 r = *p;
-              o.x = r.x + o.x; o.y = r.y + o.y; o.z = r.z + o.z; o.w = r.w + o.w;
-            }
-            *p = o;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; c++) {
-            uint8_t* p = stg + stg_off(lane, c);
-            float o[8];
-            if (has_aux) {  // EPI_GELU_BWD: out = acc * gelu'(pre-activation)
-              float hv[8];
-              get8_bf16(p, hv);
-#pragma unroll
-              for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * gelu_grad_hw(hv[q]);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
-            }
-            put8_bf16(p, o);
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (split) tma_store_3d(&em.out, stg, ncol, mrow, tc.split);
-          else if (epi == EPI_ACCUM) tma_reduce_add_2d(&em.out, stg, ncol, mrow);
-          else tma_store_2d(&em.out, stg, ncol, mrow);
-          bulk_commit();
-        }
-        if (epi == EPI_BIAS_GELU && !split) {  // second output: gelu(pre-activation)
-          if (lane == 0) bulk_wait_read0();
-          __syncwarp();
-#pragma unroll
-          for (int c = 0; c < 8; c++) {
-            float o[8];
-#pragma unroll
-            for (int q = 0; q < 8; q++) o[q] = gelu_hw(v[8 * c + q]);
-            put8_bf16(stg + stg_off(lane, c), o);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&em.out2, stg, ncol, mrow);
-            bulk_commit();
-          }
-        }
-      }
+      epilogue_tile<BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[ew], aux_phase,
+                        tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16), half, lane,
+                        tc.mt * TC_BM + quarter * 32, tc.nt * BN, tc.split, f.split, f.f32, f.has_aux,
+                        f.use_bias, bq, err);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
@@ -370,6 +408,166 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * BN);
+  }
+}
+
+// ------------------------------------------------------------ CTA-pair kernel
+// Output tiles of 256 x 256 per cluster of two CTAs on one TPC (M = 256
+// tcgen05 MMA, cta_group::2).  CTA r of the pair loads rows 128r..128r+127
+// of the tile's A rows and of its B rows (output columns), so a stage is
+// 32 KB per CTA instead of 48 KB for a 128 x 256 tile on one SM: the ring
+// is six stages deep, and each SM pulls a third fewer operand bytes through
+// L2 per flop.  Both CTAs' TMA loads complete on the leader's (rank 0) full
+// barrier; the leader's single MMA thread multicasts each stage's release
+// and each finished accumulator to both CTAs; both CTAs' epilogue warps
+// release an accumulator on the leader's barrier.  Each CTA drains its own
+// 128 accumulator lanes with the epilogue above.
+#define PAIR_BN 256
+#define GROUP_PAIRS 4
+struct PairCfg {
+  static constexpr int STAGES = 6;
+  static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;            // 128 rows of A
+  static constexpr uint32_t B_BYTES = (PAIR_BN / 2) * TC_BK * 2;     // 128 rows of B
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr size_t STAGING = (size_t)EPI_WARPS * STG_BYTES;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING + 1024 + 256;
+};
+
+template <bool A_K, bool B_K>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
+                        int splits, int* err) {
+  pdl_trigger();
+  constexpr int S = PairCfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* staging = smem + (size_t)S * PairCfg::STAGE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + PairCfg::STAGING);  // used in the leader
+  uint64_t* empty = full + S;
+  uint64_t* acc_full = empty + S;      // [2]
+  uint64_t* acc_empty = acc_full + 2;  // [2], used in the leader
+  uint64_t* aux_bar = acc_empty + 2;   // [EPI_WARPS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + EPI_WARPS);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int mpairs = (g.M + 2 * TC_BM - 1) / (2 * TC_BM), ntiles = (g.N + PAIR_BN - 1) / PAIR_BN;
+  const int total = splits * mpairs * ntiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int a = 0; a < 2; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 2 * EPI_WARPS); }
+    for (int w = 0; w < EPI_WARPS; w++) mbar_init(&aux_bar[w], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 2 * PAIR_BN);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int it = 0;  // running k-tile counter over all tiles of this pair
+      for (int t = pair; t < total; t += npairs) {
+        const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
+        const int m0 = (2 * tc.mt + (int)rank) * TC_BM;
+        const int nb0 = tc.nt * PAIR_BN + (int)rank * (PAIR_BN / 2);
+        const int kt0 = tc.split * k_per_split;
+        const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
+        for (int i = 0; i < nkt; i++, it++) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          mbar_wait(&empty[s], ph ^ 1u, err);
+          uint8_t* sa = smem + (size_t)s * PairCfg::STAGE_BYTES;
+          uint8_t* sb = sa + PairCfg::A_BYTES;
+          const uint32_t bar = cluster_addr(&full[s], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * PairCfg::STAGE_BYTES);
+          const int k = (kt0 + i) * TC_BK;
+          if (A_K) {
+            tma_load_2d_pair(sa, &tmA, bar, k, m0);
+          } else {
+            tma_load_2d_pair(sa, &tmA, bar, m0, k);
+            tma_load_2d_pair(sa + 8192, &tmA, bar, m0 + 64, k);
+          }
+          if (B_K) {
+            tma_load_2d_pair(sb, &tmB, bar, k, nb0);
+          } else {
+            tma_load_2d_pair(sb, &tmB, bar, nb0, k);
+            tma_load_2d_pair(sb + 8192, &tmB, bar, nb0 + 64, k);
+          }
+        }
+      }
+      // every release the leader will still multicast here has landed
+      for (int d = max(0, it - S); d < it; d++) mbar_wait(&empty[d % S], (uint32_t)(d / S) & 1u, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = tc_idesc_bf16(2 * TC_BM, PAIR_BN, !A_K, !B_K);
+      int it = 0, ti = 0;
+      for (int t = pair; t < total; t += npairs, ti++) {
+        const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
+        const int kt0 = tc.split * k_per_split;
+        const int nkt = min(k_tiles, kt0 + k_per_split) - kt0;
+        const int a = ti & 1;
+        mbar_wait(&acc_empty[a], ((uint32_t)(ti >> 1) & 1u) ^ 1u, err);
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)(a * PAIR_BN);
+        for (int i = 0; i < nkt; i++, it++) {
+          const int s = it % S;
+          const uint32_t ph = (uint32_t)(it / S) & 1u;
+          mbar_wait(&full[s], ph, err);
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + (size_t)s * PairCfg::STAGE_BYTES);
+          const uint32_t b0 = a0 + PairCfg::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; kk++) {
+            const uint64_t ad = A_K ? sw128_desc(a0 + kk * 32, 16, 1024) : sw128_desc(a0 + kk * 2048, 8192, 1024);
+            const uint64_t bd = B_K ? sw128_desc(b0 + kk * 32, 16, 1024) : sw128_desc(b0 + kk * 2048, 8192, 1024);
+            tc_mma_bf16_pair(acc, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit_pair_both(&empty[s]);
+        }
+        tc_commit_pair_both(&acc_full[a]);
+      }
+      // both CTAs' epilogues have released every accumulator
+      for (int d = max(0, ti - 2); d < ti; d++) mbar_wait(&acc_empty[d & 1], (uint32_t)(d >> 1) & 1u, err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
+    const EpiFlags f = epi_flags(g, splits);
+    uint32_t aux_phase = 0;
+    int ti = 0;
+    for (int t = pair; t < total; t += npairs, ti++) {
+      const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
+      const int a = ti & 1;
+      const float4 bq = load_bias4<PAIR_BN>(g, f.use_bias, tc.nt * PAIR_BN, half, lane);
+      mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
+      tc_fence_after();
+      epilogue_tile<PAIR_BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[ew], aux_phase,
+                             tmem + (uint32_t)(a * PAIR_BN) + ((uint32_t)(quarter * 32) << 16), half,
+                             lane, (2 * tc.mt + (int)rank) * TC_BM + quarter * 32, tc.nt * PAIR_BN,
+                             tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[a], 0));
+    }
+    if (lane == 0) bulk_wait0();
+  }
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 2 * PAIR_BN);
   }
 }
 
@@ -435,6 +633,68 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   }
 }
 
+template <bool A_K, bool B_K>
+static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* partial) {
+  CUtensorMap ta, tb;
+  EpiMaps em;
+  memset(&em, 0, sizeof(em));
+  bool ok;
+  if (A_K) ok = make_tmap(&ta, g.A, false, g.K, g.M, g.lda, 64, TC_BM);
+  else ok = make_tmap(&ta, g.A, false, g.M, g.K, g.lda, 64, 64);
+  if (B_K) ok = ok && make_tmap(&tb, g.B, false, g.K, g.N, g.ldb, 64, PAIR_BN / 2);
+  else ok = ok && make_tmap(&tb, g.B, false, g.N, g.K, g.ldb, 64, 64);
+  const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
+  const int kps = (k_tiles + splits - 1) / splits;
+  const int zs = (k_tiles + kps - 1) / kps;
+  if (zs > 1) {
+    ok = ok && make_tmap(&em.out, partial, true, g.N, g.M, g.N, 32, 32, zs);
+  } else {
+    const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
+    ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
+    if (g.epi == EPI_BIAS_GELU) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
+    if (g.epi == EPI_GELU_BWD) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+  }
+  if (!ok) {
+    fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
+    c.host_fail = 1;
+    return;
+  }
+  using Cfg = PairCfg;
+  auto kern = gemm_tc_pair_kernel<A_K, B_K>;
+  static int max_pairs = 0;  // co-resident clusters of two, per instantiation
+  if (max_pairs == 0) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * c.num_sms);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = c.num_sms / 2;
+    }
+    max_pairs = n;
+  }
+  const int pair_tiles = zs * ((g.N + PAIR_BN - 1) / PAIR_BN) * ((g.M + 2 * TC_BM - 1) / (2 * TC_BM));
+  const int pairs = std::min(pair_tiles, max_pairs);
+  launch_pdl_cluster(c, kern, dim3(2 * pairs), dim3(TC_THREADS), Cfg::SMEM, 2, ta, tb, em, g, k_tiles, kps, zs, c.err);
+  if (zs > 1) {
+    const int64_t n4 = (int64_t)g.M * g.N / 4;
+    int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)c.num_sms * 8);
+    launch_pdl(c, splitk_reduce_kernel, dim3(blocks), dim3(256), 0, static_cast<float*>(g.out), g.ldo, partial, zs, g.M, g.N);
+  }
+}
+
+static int g_pair_mode = -1;  // GPT2_GEMM_PAIR=0 selects the one-SM kernel for every shape
+
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   const int BN = g.N >= 256 ? 256 : 128;
   const int tiles = ((g.N + BN - 1) / BN) * ((g.M + TC_BM - 1) / TC_BM);
@@ -450,6 +710,15 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   else if (g.a_kmajor && !g.b_kmajor) launch_tc<BNV, true, false>(c, g, splits, partial); \
   else if (!g.a_kmajor && g.b_kmajor) launch_tc<BNV, false, true>(c, g, splits, partial); \
   else launch_tc<BNV, false, false>(c, g, splits, partial);
-  if (BN == 256) { TC_DISPATCH(256) } else { TC_DISPATCH(128) }
+  if (g_pair_mode < 0) {
+    const char* e = getenv("GPT2_GEMM_PAIR");
+    g_pair_mode = (e && e[0] == '0') ? 0 : 1;
+  }
+  if (BN == 256 && g_pair_mode) {
+    if (g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true>(c, g, splits, partial);
+    else if (g.a_kmajor && !g.b_kmajor) launch_tc_pair<true, false>(c, g, splits, partial);
+    else if (!g.a_kmajor && g.b_kmajor) launch_tc_pair<false, true>(c, g, splits, partial);
+    else launch_tc_pair<false, false>(c, g, splits, partial);
+  } else if (BN == 256) { TC_DISPATCH(256) } else { TC_DISPATCH(128) }
 #undef TC_DISPATCH
 }

@@ -272,44 +272,93 @@ __device__ __forceinline__ float4 load4<bf16>(const bf16* p) {
 
 // One warp per row: mean, then variance about the mean (two passes; the row
 // stays in L1), then y = (x - mean) * rstd * w + b.
-template <typename OutT>
-__global__ void layernorm_fwd_kernel(OutT* out, float* mean, float* rstd, const float* inp,
-                                     const float* w, const float* b, int N, int C) {
+// One warp per row, rows strided over a grid of ~2 blocks per SM.  Lane l
+// holds the float4 column chunks l, l+32, ... (NCH = ceil(C/128)) of the
+// row in registers, so the row is read from HBM once; the next row's loads
+// are issued before this row is reduced.  mean = sum/C, var = sum((x -
+// mean)^2)/C (two passes over the registers), rstd = 1/sqrt(var + 1e-5).
+template <typename OutT, int NCH>
+__global__ void __launch_bounds__(256) layernorm_fwd_kernel(OutT* out, float* mean, float* rstd,
+                                                            const float* inp, const float* w,
+                                                            const float* b, int N, int C) {
   pdl_trigger();
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (row >= N) return;
-  const float* x = inp + (int64_t)row * C;
-  float s = 0.f;
-  for (int c = lane * 4; c < C; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(x + c);
-    s += (v.x + v.y) + (v.z + v.w);
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  float4 wv[NCH], bv[NCH], xv[NCH];
+#pragma unroll
+  for (int k = 0; k < NCH; k++) {
+    const int c = (lane + 32 * k) * 4;
+    wv[k] = bv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < C) {
+      wv[k] = *reinterpret_cast<const float4*>(w + c);
+      bv[k] = *reinterpret_cast<const float4*>(b + c);
+    }
   }
-  const float m = warp_sum(s) / (float)C;
-  float q = 0.f;
-  for (int c = lane * 4; c < C; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(x + c);
-    const float a = v.x - m, bb = v.y - m, cc = v.z - m, d = v.w - m;
-    q += (a * a + bb * bb) + (cc * cc + d * d);
+  pdl_wait();
+  int row = blockIdx.x * (blockDim.x >> 5) + warp;
+#pragma unroll
+  for (int k = 0; k < NCH; k++) {
+    const int c = (lane + 32 * k) * 4;
+    xv[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < N && c < C) xv[k] = *reinterpret_cast<const float4*>(inp + (int64_t)row * C + c);
   }
-  const float var = warp_sum(q) / (float)C;
-  const float r = 1.f / sqrtf(var + 1e-5f);
-  OutT* y = out + (int64_t)row * C;
-  for (int c = lane * 4; c < C; c += 128) {
-    const float4 v = *reinterpret_cast<const float4*>(x + c);
-    const float4 ww = *reinterpret_cast<const float4*>(w + c);
-    const float4 bb = *reinterpret_cast<const float4*>(b + c);
-    store4<OutT>(y + c, (v.x - m) * r * ww.x + bb.x, (v.y - m) * r * ww.y + bb.y,
-                 (v.z - m) * r * ww.z + bb.z, (v.w - m) * r * ww.w + bb.w);
+  for (; row < N; row += nwarps) {
+    float4 nx[NCH];
+    const int nrow = row + nwarps;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+      const int c = (lane + 32 * k) * 4;
+      nx[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (nrow < N && c < C) nx[k] = *reinterpret_cast<const float4*>(inp + (int64_t)nrow * C + c);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) s += (xv[k].x + xv[k].y) + (xv[k].z + xv[k].w);
+    const float m = warp_sum(s) / (float)C;
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+      if ((lane + 32 * k) * 4 < C) {
+        const float a = xv[k].x - m, bb = xv[k].y - m, cc = xv[k].z - m, d = xv[k].w - m;
+        q += (a * a + bb * bb) + (cc * cc + d * d);
+      }
+    }
+    const float var = warp_sum(q) / (float)C;
+    const float r = 1.f / sqrtf(var + 1e-5f);
+    OutT* y = out + (int64_t)row * C;
+#pragma unroll
+    for (int k = 0; k < NCH; k++) {
+      const int c = (lane + 32 * k) * 4;
+      if (c < C)
+        store4<OutT>(y + c, (xv[k].x - m) * r * wv[k].x + bv[k].x, (xv[k].y - m) * r * wv[k].y + bv[k].y,
+                     (xv[k].z - m) * r * wv[k].z + bv[k].z, (xv[k].w - m) * r * wv[k].w + bv[k].w);
+    }
+    if (lane == 0) { mean[row] = m; rstd[row] = r; }
+#pragma unroll
+    for (int k = 0; k < NCH; k++) xv[k] = nx[k];
   }
-  if (lane == 0) { mean[row] = m; rstd[row] = r; }
+}
+
+template <typename OutT, int NCH>
+static void ln_fwd_launch(LaunchCtx& c, OutT* out, float* mean, float* rstd, const float* inp,
+                          const float* w, const float* b, int N, int C) {
+  const int blocks = std::min(cdiv(N, 8), 2 * c.num_sms);
+  launch_pdl(c, layernorm_fwd_kernel<OutT, NCH>, dim3(blocks), dim3(256), 0, out, mean, rstd, inp, w, b, N, C);
 }
 
 template <typename OutT>
 void launch_layernorm_fwd(LaunchCtx& c, OutT* out, float* mean, float* rstd, const float* inp,
                           const float* w, const float* b, int N, int C) {
-  launch_pdl(c, layernorm_fwd_kernel<OutT>, dim3(cdiv(N, 8)), dim3(256), 0, out, mean, rstd, inp, w, b, N, C);
+  switch ((C + 127) / 128) {  // C <= 1024
+    case 1: ln_fwd_launch<OutT, 1>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 2: ln_fwd_launch<OutT, 2>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 3: ln_fwd_launch<OutT, 3>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 4: ln_fwd_launch<OutT, 4>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 5: ln_fwd_launch<OutT, 5>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 6: ln_fwd_launch<OutT, 6>(c, out, mean, rstd, inp, w, b, N, C); break;
+    case 7: ln_fwd_launch<OutT, 7>(c, out, mean, rstd, inp, w, b, N, C); break;
+    default: ln_fwd_launch<OutT, 8>(c, out, mean, rstd, inp, w, b, N, C); break;
+  }
 }
 template void launch_layernorm_fwd<float>(LaunchCtx&, float*, float*, float*, const float*,
                                           const float*, const float*, int, int);
@@ -451,7 +500,7 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
   const int nb = cdiv(N, LNB_ROWS);
   const int nparts = cdiv(N, LNB_ROWS_PER_WARP);
   const size_t smem = 0;
-  const int nch = (C + 127) / 128;  // C <= 1024 keeps the partials in registers
+  const int nch = (C + 127) / 128;  // C <= 1024 (checked by the callers): partials in registers
   switch (nch) {
     case 1: ln_bwd_launch<ActT, 1>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
     case 2: ln_bwd_launch<ActT, 2>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;

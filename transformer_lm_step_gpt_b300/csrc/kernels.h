@@ -39,6 +39,28 @@ inline void launch_pdl(LaunchCtx& c, void (*k)(KArgs...), dim3 grid, dim3 block,
   (*c.launches)++;
 }
 
+// Same, with thread-block clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+inline void launch_pdl_cluster(LaunchCtx& c, void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               int cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = cluster_x;
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...) != cudaSuccess) c.host_fail = 1;
+  (*c.launches)++;
+}
+
 // ---------------------------------------------------------------- init
 struct InitSpec {
   int64_t off[17];  // start of each of the 16 parameter tensors, off[16] = total
