@@ -243,7 +243,7 @@ GPT2_API const char* gpt2_last_error(const gpt2_model* m);
  *       accumulated into (the caller zeroes them for plain values);
  *   dout, inp [N, C], weight [C], mean, rstd [N]: inputs, read only;
  *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
- * Scratch: the partial sums, ceil(N/8) * 3 * C floats, live in one
+ * Scratch: the partial sums, at most ceil(N/64) * 8 * 3 * C floats, live in one
  * file-scope __device__ array of 2^21 floats (8 MiB) that every GPU which
  * loads the library holds until the process exits.  Larger sizes are
  * rejected with GPT2_ERR_ARG (N * C must stay below about 5.59 million);

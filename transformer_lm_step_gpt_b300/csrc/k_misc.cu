@@ -365,75 +365,109 @@ template void launch_layernorm_fwd<float>(LaunchCtx&, float*, float*, float*, co
 template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, const float*,
                                          const float*, const float*, int, int);
 
-#define LNB_WARPS 4
-#define LNB_ROWS_PER_WARP 8
-#define LNB_ROWS (LNB_WARPS * LNB_ROWS_PER_WARP)  // rows per block
+#define LNB_WARPS 8
+#define LNB_STAGES 2        // rows in flight per warp
+#define LNB_ROWS_PER_BLOCK 64  // rows per block at least (grid sizing)
 
-// one partial row (3*C floats) per warp
-int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS_PER_WARP) * 3 * C; }
+// partial rows: at most one per warp of a grid of cdiv(N, 64) blocks
+int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS_PER_BLOCK) * LNB_WARPS * 3 * C; }
 
-// One warp per row.  Each lane owns the float4 column chunks lane, lane+32,
-// ... (NCH = C/128 of them) and keeps its gamma / beta / residual-gradient
-// column partials in registers across the warp's LNB_ROWS_PER_WARP rows,
-// then writes them as the warp's own partial row (no shared memory, no
-// block-wide barrier); reduce_partials_kernel adds the partial rows in order.  Pass 1 reads x and dy
-// for the two row sums (and prefetches the old residual gradient), pass 2
-// re-reads x and dy (L1 hits) to form dx.
+static size_t lnb_smem(int C) {
+  return (size_t)LNB_WARPS * LNB_STAGES * 3 * C * sizeof(float) + LNB_WARPS * LNB_STAGES * sizeof(uint64_t);
+}
+
+// One warp per row, rows strided over a persistent grid.  Each warp streams
+// its rows (dy, x and, when accumulating, the old residual gradient) into
+// its own LNB_STAGES-deep shared-memory ring with bulk copies, so the next
+// rows' loads are in flight while this one is processed from shared memory.
+// Lane l owns the float4 column chunks l, l+32, ... (NCH = C/128 of them)
+// and keeps its gamma / beta / residual-gradient column partials in
+// registers across all of the warp's rows, then writes them as the warp's
+// own partial row; reduce_partials_kernel adds the partial rows in order.
+//   xhat = (x - mean) rstd, g = dy * gamma,
+//   dx = rstd (g - mean(g) - xhat mean(g xhat)),  dres (+)= dx.
 template <typename ActT, int NCH>
-__global__ void __launch_bounds__(LNB_WARPS * 32)
+__global__ void __launch_bounds__(LNB_WARPS * 32, 1)
     layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
                          const float* inp, const float* w, const float* mean, const float* rstd,
-                         int N, int C, int accumulate) {
+                         int N, int C, int accumulate, int* err) {
   pdl_trigger();
-  pdl_wait();
+  extern __shared__ __align__(16) uint8_t lnb_sm[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float4 pw[NCH], pb[NCH], pr[NCH], old[NCH];
+  float* ring = reinterpret_cast<float*>(lnb_sm) + (size_t)warp * LNB_STAGES * 3 * C;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lnb_sm + (size_t)LNB_WARPS * LNB_STAGES * 3 * C * sizeof(float)) +
+                   warp * LNB_STAGES;
+  if (lane == 0) {
+    for (int s = 0; s < LNB_STAGES; s++) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  float4 wv[NCH], pw[NCH], pb[NCH], pr[NCH];
 #pragma unroll
   for (int k = 0; k < NCH; k++) {
+    const int c = (lane + 32 * k) * 4;
     pw[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     pb[k] = pw[k];
     pr[k] = pw[k];
+    wv[k] = pw[k];
+    if (c < C) wv[k] = *reinterpret_cast<const float4*>(w + c);
   }
-  const int gwarp = blockIdx.x * LNB_WARPS + warp;
-  const int row0 = gwarp * LNB_ROWS_PER_WARP;
-  for (int rr = 0; rr < LNB_ROWS_PER_WARP; rr++) {
-    const int row = row0 + rr;
-    if (row >= N) break;
-    const float* x = inp + (int64_t)row * C;
-    const float* g = dy + (int64_t)row * C;
-    const float m = mean[row], r = rstd[row];
-    float* dr = dres + (int64_t)row * C;
+  pdl_wait();  // from here on global memory written by the previous kernel is read
+  const int gw = blockIdx.x * LNB_WARPS + warp, nw = gridDim.x * LNB_WARPS;
+  const uint32_t rowbytes = (uint32_t)C * sizeof(float);
+  auto issue = [&](int row, int s) {
+    float* st = ring + (size_t)s * 3 * C;
+    mbar_arrive_expect_tx(&bars[s], (accumulate ? 3u : 2u) * rowbytes);
+    bulk_load(st, dy + (int64_t)row * C, rowbytes, &bars[s]);
+    bulk_load(st + C, inp + (int64_t)row * C, rowbytes, &bars[s]);
+    if (accumulate) bulk_load(st + 2 * C, dres + (int64_t)row * C, rowbytes, &bars[s]);
+  };
+  if (lane == 0)
+    for (int s = 0; s < LNB_STAGES; s++)
+      if (gw + s * nw < N) issue(gw + s * nw, s);
+  float m = 0.f, r = 0.f;
+  if (gw < N) { m = mean[gw]; r = rstd[gw]; }
+  int it = 0;
+  for (int row = gw; row < N; row += nw, it++) {
+    const int s = it % LNB_STAGES;
+    const int nrow = row + nw;
+    float mn = 0.f, rn = 0.f;  // next row's statistics, loaded ahead
+    if (nrow < N) { mn = mean[nrow]; rn = rstd[nrow]; }
+    mbar_wait(&bars[s], (uint32_t)(it / LNB_STAGES) & 1u, err);
+    const float* g = ring + (size_t)s * 3 * C;
+    const float* x = g + C;
+    const float* o = x + C;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int k = 0; k < NCH; k++) {
       const int c = (lane + 32 * k) * 4;
-      old[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       if (c < C) {
-        if (accumulate) old[k] = *reinterpret_cast<const float4*>(dr + c);
         const float4 xv = *reinterpret_cast<const float4*>(x + c);
         const float4 gv = *reinterpret_cast<const float4*>(g + c);
-        const float4 wv = *reinterpret_cast<const float4*>(w + c);
-        const float h0 = gv.x * wv.x, h1 = gv.y * wv.y, h2 = gv.z * wv.z, h3 = gv.w * wv.w;
+        const float h0 = gv.x * wv[k].x, h1 = gv.y * wv[k].y, h2 = gv.z * wv[k].z, h3 = gv.w * wv[k].w;
         s1 += (h0 + h1) + (h2 + h3);
         s2 += (h0 * (xv.x - m) * r + h1 * (xv.y - m) * r) + (h2 * (xv.z - m) * r + h3 * (xv.w - m) * r);
       }
     }
     const float mg = warp_sum(s1) / (float)C;
     const float mgx = warp_sum(s2) / (float)C;
+    float* dr = dres + (int64_t)row * C;
 #pragma unroll
     for (int k = 0; k < NCH; k++) {
       const int c = (lane + 32 * k) * 4;
       if (c < C) {
         const float4 xv = *reinterpret_cast<const float4*>(x + c);
         const float4 gv = *reinterpret_cast<const float4*>(g + c);
-        const float4 wv = *reinterpret_cast<const float4*>(w + c);
         const float x0 = (xv.x - m) * r, x1 = (xv.y - m) * r, x2 = (xv.z - m) * r, x3 = (xv.w - m) * r;
         float4 d;
-        d.x = r * (gv.x * wv.x - mg - x0 * mgx);
-        d.y = r * (gv.y * wv.y - mg - x1 * mgx);
-        d.z = r * (gv.z * wv.z - mg - x2 * mgx);
-        d.w = r * (gv.w * wv.w - mg - x3 * mgx);
-        d.x += old[k].x; d.y += old[k].y; d.z += old[k].z; d.w += old[k].w;
+        d.x = r * (gv.x * wv[k].x - mg - x0 * mgx);
+        d.y = r * (gv.y * wv[k].y - mg - x1 * mgx);
+        d.z = r * (gv.z * wv[k].z - mg - x2 * mgx);
+        d.w = r * (gv.w * wv[k].w - mg - x3 * mgx);
+        if (accumulate) {
+          const float4 ov = *reinterpret_cast<const float4*>(o + c);
+          d.x += ov.x; d.y += ov.y; d.z += ov.z; d.w += ov.w;
+        }
         *reinterpret_cast<float4*>(dr + c) = d;
         if (dres_act) store4<ActT>(dres_act + (int64_t)row * C + c, d.x, d.y, d.z, d.w);
         pw[k].x += gv.x * x0; pw[k].y += gv.y * x1; pw[k].z += gv.z * x2; pw[k].w += gv.w * x3;
@@ -441,9 +475,12 @@ __global__ void __launch_bounds__(LNB_WARPS * 32)
         pr[k].x += d.x; pr[k].y += d.y; pr[k].z += d.z; pr[k].w += d.w;
       }
     }
+    __syncwarp();  // every lane is done with stage s
+    if (lane == 0 && row + LNB_STAGES * nw < N) issue(row + LNB_STAGES * nw, s);
+    m = mn;
+    r = rn;
   }
-  if (row0 >= N) return;
-  float* out = partial + (int64_t)gwarp * 3 * C;
+  float* out = partial + (int64_t)gw * 3 * C;
 #pragma unroll
   for (int k = 0; k < NCH; k++) {
     const int c = (lane + 32 * k) * 4;
@@ -484,12 +521,13 @@ __global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
 }
 
 template <typename ActT, int NCH>
-static void ln_bwd_launch(LaunchCtx& c, int nb, size_t smem, float* dres, ActT* dres_act, float* partial,
+static void ln_bwd_launch(LaunchCtx& c, int nb, float* dres, ActT* dres_act, float* partial,
                           const float* dy, const float* inp, const float* w, const float* mean,
                           const float* rstd, int N, int C, bool accumulate) {
+  const size_t smem = lnb_smem(C);
   cudaFuncSetAttribute(layernorm_bwd_kernel<ActT, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  launch_pdl(c, layernorm_bwd_kernel<ActT, NCH>, dim3(nb), dim3(LNB_WARPS * 32), smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0);
+  launch_pdl(c, layernorm_bwd_kernel<ActT, NCH>, dim3(nb), dim3(LNB_WARPS * 32), smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate ? 1 : 0, c.err);
 }
 
 template <typename ActT>
@@ -497,19 +535,18 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
                           float* dres_colsum, const float* dy, const float* inp, const float* w,
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial) {
-  const int nb = cdiv(N, LNB_ROWS);
-  const int nparts = cdiv(N, LNB_ROWS_PER_WARP);
-  const size_t smem = 0;
-  const int nch = (C + 127) / 128;  // C <= 1024 (checked by the callers): partials in registers
-  switch (nch) {
-    case 1: ln_bwd_launch<ActT, 1>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 2: ln_bwd_launch<ActT, 2>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 3: ln_bwd_launch<ActT, 3>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 4: ln_bwd_launch<ActT, 4>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 5: ln_bwd_launch<ActT, 5>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 6: ln_bwd_launch<ActT, 6>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    case 7: ln_bwd_launch<ActT, 7>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
-    default: ln_bwd_launch<ActT, 8>(c, nb, smem, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+  int nb = cdiv(N, LNB_ROWS_PER_BLOCK);  // partial rows nb * LNB_WARPS <= ln_partial_floats / (3C)
+  if (c.num_sms > 0) nb = std::min(nb, c.num_sms);
+  const int nparts = nb * LNB_WARPS;
+  switch ((C + 127) / 128) {  // C <= 1024 (checked by the callers): partials in registers
+    case 1: ln_bwd_launch<ActT, 1>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 2: ln_bwd_launch<ActT, 2>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 3: ln_bwd_launch<ActT, 3>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 4: ln_bwd_launch<ActT, 4>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 5: ln_bwd_launch<ActT, 5>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 6: ln_bwd_launch<ActT, 6>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    case 7: ln_bwd_launch<ActT, 7>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
+    default: ln_bwd_launch<ActT, 8>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
   }
   launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nparts, 3 * C, C);
 }
@@ -749,8 +786,8 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
 
 // ============================================================ allocation-free LayerNorm backward
 // gpt2_layernorm_backward_noalloc: the LayerNorm backward above for callers
-// that cannot allocate device memory.  Its partial sums (ceil(N/8) rows of
-// 3*C floats) live in this file-scope array instead of caller- or
+// that cannot allocate device memory.  Its partial sums (at most
+// ceil(N/64)*8 rows of 3*C floats) live in this file-scope array instead of caller- or
 // model-owned scratch; every GPU that loads the library holds it until the
 // process exits.
 #define NOALLOC_SCRATCH_FLOATS (1 << 21)  // 8 MiB
@@ -787,7 +824,7 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
   }
   const int64_t need = ln_partial_floats(N, C);
   if (need > NOALLOC_SCRATCH_FLOATS) {
-    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/8)*3*C exceeds the 2^21-float "
+    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/64)*8*3*C exceeds the 2^21-float "
                      "static scratch (N*C must stay below about 5.59 million)");
     return GPT2_ERR_ARG;
   }
