@@ -256,7 +256,8 @@ size_t layout(gpt2_model* m, char* base) {
   m->datty = b.take<char>(M * C * a);
   m->dsum = b.take<float>((int64_t)m->B * m->NH * m->T);
   m->ln_partial = b.take<float>(ln_partial_floats(m->M, m->C));
-  m->cs_partial = b.take<float>(colsum_partial_floats(m->M, 4 * m->C));
+  m->cs_partial = b.take<float>(std::max<int64_t>(colsum_partial_floats(m->M, 4 * m->C),
+                                                  (int64_t)((m->M + 31) / 32) * 4 * m->C));
   m->splitk_floats = m->bf ? 16 * C * C : 0;
   m->splitk = b.take<float>(m->splitk_floats);
   m->enc_sorted = b.take<uint32_t>(M);
@@ -399,6 +400,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     GemmArgs g = gemm(M, 4 * C, C, dres_act, C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C,
                       false, EPI_GELU_BWD, dbig, 4 * C, f32);
     g.aux = fch;
+    if (!f32) g.colsum_out = m->cs_partial;  // fc bias gradient partials, 32 rows each
     run_gemm(m, c, g, GS_FCPROJ);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
                         m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true), GS_FCPROJ);
@@ -411,7 +413,8 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         m->G(FCW) + (int64_t)l * 4 * C * C, C, true), GS_FC);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 4.0 * C);
-      launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
+      if (f32) launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
+      else launch_colsum_reduce(c, m->G(FCB) + (int64_t)l * 4 * C, m->cs_partial, (M + 31) / 32, 4 * C);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
@@ -425,13 +428,15 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
-    // attention
+    // attention (the tensor-core path also leaves the qkv bias gradient's
+    // partial rows in cs_partial)
+    bool qkvb_partials = false;
     {
       ProfScope ps(m, PC_ATTN_BWD, attn_flop);
       if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
-      else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
-                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                     lse, m->dsum, B, T, C, NH);
+      else qkvb_partials = launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
+                                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
+                                                     lse, m->dsum, B, T, C, NH, m->cs_partial);
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
@@ -440,7 +445,10 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
-      launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+      if (qkvb_partials)
+        launch_colsum_reduce(c, m->G(QKVB) + (int64_t)l * 3 * C, m->cs_partial, B * ((T + 127) / 128), 3 * C);
+      else
+        launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);

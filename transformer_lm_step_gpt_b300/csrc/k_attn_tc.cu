@@ -191,6 +191,24 @@ __device__ __forceinline__ void store_row32_bf16(bf16* dst, const float* v, floa
   }
 }
 
+// Column sums of a warp's 32 rows x 32 columns (lane = row, v[j] = column
+// j): a reduce-scatter over the lanes (16 + 8 + 4 + 2 + 1 shuffles); lane l
+// returns the sum of column l.
+__device__ __forceinline__ float warp_colsum32(float* v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; i++) {
+      const float send = up ? v[i] : v[i + off];
+      const float keep = up ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
 // 8 warps: warps w and w+4 read the same TMEM lane quarter (w % 4, i.e. the
 // same 32 query or key rows) and split the 128 score columns (half = w / 4
 // takes columns 64*half .. 64*half+63) and the 64 output head dims
@@ -472,7 +490,8 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                            const __grid_constant__ CUtensorMap tm_qkv64,
                            const __grid_constant__ CUtensorMap tm_dy64, bf16* dqkv, const float* lse,
-                           const float* dsum, int T, int C, int NH, float scale, int* err) {
+                           const float* dsum, float* bias_partial, int T, int C, int NH, float scale,
+                           int* err) {
   pdl_trigger();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -649,18 +668,30 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     mbar_wait(done, 0, err);
     tc_fence_after();
     const int64_t C3 = 3 * (int64_t)C;
+    float* red = reinterpret_cast<float*>(sP);  // [2][4][64]: free once every MMA is done
     float v[32];
     uint32_t r[32];
     tmem_ld32(tdV + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; i++) v[i] = key < T ? __uint_as_float(r[i]) : 0.f;
     if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS + half * 32, v, 1.f);
+    red[quarter * 64 + half * 32 + lane] = warp_colsum32(v);
     tmem_ld32(tdK + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; i++) v[i] = key < T ? __uint_as_float(r[i]) : 0.f;
     if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
+    red[256 + quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
+    // the block's column sums of dV and dK: one partial row of the qkv bias
+    // gradient per (batch row, key block)
+    named_bar_sync(1, AT_THREADS);
+    if (tid < 128) {
+      const int which = tid >> 6, col = tid & 63;  // 0: dV, 1: dK
+      const float* rr = red + which * 256 + col;
+      const float sum = (rr[0] + rr[64]) + (rr[128] + rr[192]);
+      bias_partial[((int64_t)b * gridDim.y + kb) * C3 + (which ? C : 2 * C) + h * AT_HS + col] = sum;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -677,7 +708,8 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_dy,
                           const __grid_constant__ CUtensorMap tm_qkv64, bf16* dqkv, const float* lse,
-                          const float* dsum, int T, int C, int NH, float scale, int* err) {
+                          const float* dsum, float* bias_partial, int T, int C, int NH, float scale,
+                          int* err) {
   pdl_trigger();
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -797,9 +829,18 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
     tmem_ld32(tdQ + lanebase + half * 32, r);
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+    for (int j = 0; j < 32; j++) v[j] = q < T ? __uint_as_float(r[j]) : 0.f;
   }
   if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
+  // the block's column sums of dQ: one partial row of the qkv bias gradient
+  // per (batch row, query block); the dS buffer is free after the loop
+  float* red = reinterpret_cast<float*>(sS);  // [4][64]
+  red[quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
+  __syncthreads();
+  if (tid < 64) {
+    const float* rr = red + tid;
+    bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * AT_HS + tid] = (rr[0] + rr[64]) + (rr[128] + rr[192]);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
@@ -822,18 +863,18 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
   launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AT_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
 }
 
-void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T,
-                               int C, int NH) {
+                               int C, int NH, float* bias_partial) {
   if (C / NH != AT_HS) {
     launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
-    return;
+    return false;
   }
   CUtensorMap tq, td, tq64, td64;
   if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C) ||
       !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB) || !make_tmap_btw(&td64, dy, B, T, C, AB_SUB)) {
     c.host_fail = 1;
-    return;
+    return false;
   }
   const int64_t n = (int64_t)B * T * NH;
   launch_pdl(c, attn_bwd_dsum_kernel, dim3((int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16)), dim3(256), 0, dsum, dy, y, B, T, C, NH);
@@ -841,7 +882,8 @@ void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
   dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
   const size_t kv_smem = akv_smem(T);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_smem);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, tq64, td64, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, tq64, td64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AT_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, T, C, NH, scale, c.err);
+  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AT_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
+  return true;
 }

@@ -247,6 +247,22 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       else tma_store_2d(&em.out, stg, ncol, mrow);
       bulk_commit();
     }
+    if (g.colsum_out && !f32 && !split) {
+      // column sums of the stored values over the warp's 32 rows, read back
+      // from the staging rows (lane l: columns 2l, 2l+1 of the chunk)
+      float s0 = 0.f, s1 = 0.f;
+      const int ch = lane >> 2, wo = (lane & 3) * 4;
+#pragma unroll 8
+      for (int r = 0; r < 32; r++) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(stg + r * 128 + ((ch ^ (r & 7)) << 4) + wo);
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+        s0 += f.x;
+        s1 += f.y;
+      }
+      const int n = ncol + 2 * lane;
+      if (mrow < g.M && n < g.N)
+        *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);
+    }
     if (epi == EPI_BIAS_GELU && !split) {  // second output: gelu(pre-activation)
       if (lane == 0) bulk_wait_read0();
       __syncwarp();

@@ -97,6 +97,8 @@ int64_t ln_partial_floats(int N, int C);
 
 // ---------------------------------------------------------------- column sums
 // db[j] += sum_i x[i*ld + j], i < M, j < N.  partial: float [colsum_partial_floats]
+// db[n] += sum over r < rows of partial[r * N + n], rows in order
+void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N);
 template <typename T>
 void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial);
 int64_t colsum_partial_floats(int M, int N);
@@ -137,6 +139,10 @@ struct GemmArgs {
   const void* aux;    // EPI_RESIDUAL (f32, ldo) / EPI_GELU_BWD (act, ldo)
   float* splitk_scratch;  // EPI_ACCUM with split-K (tensor-core path)
   int64_t splitk_scratch_floats;
+  // EPI_GELU_BWD on the tensor-core path: if set, also the column sums of
+  // the stored (bf16) output over each 32-row block, [ceil(M/32)][N] floats
+  // (launch_colsum_reduce adds them up)
+  float* colsum_out;
 };
 // fp32 operands, SIMT FFMA (no TF32)
 void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
@@ -157,9 +163,12 @@ void launch_attention_bwd_simt(LaunchCtx& c, T* dqkv, const T* dy, const T* y, c
 int64_t attention_simt_scratch_floats(int B, int T_, int NH);
 void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T_,
                                int C, int NH);
-void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+// Returns true when it also wrote the qkv bias gradient's partial rows
+// (head size 64, tensor-core path): bias_partial [B * ceil(T/128)][3C],
+// row b * ceil(T/128) + block (launch_colsum_reduce adds them up).
+bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
-                               int C, int NH);
+                               int C, int NH, float* bias_partial);
 
 // Record the message gpt2_last_error(NULL) returns (entry points without a
 // model handle).
