@@ -216,19 +216,24 @@ __device__ __forceinline__ float warp_colsum32(float* v) {
 #define AT_THREADS 256
 
 // ============================================================ forward
-// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks with
-// a two-deep software pipeline: the MMA S(j+1) = q k(j+1)^T runs while the
-// warps do the softmax of S(j), and O_blk(j) = P(j) v(j) runs while they
-// start on j+1 (its result is folded into the register accumulator one
-// iteration later).  TMEM: S[0], S[1], O[0], O[1] (64 columns each), so two
-// CTAs share an SM.
+// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks;
+// two CTAs share an SM.  Warps 0..7 do the online softmax; warp 8 (one
+// thread) issues every TMA load and MMA, so no softmax warp stalls on them:
+//   S(j) = q k(j)^T into TMEM S[j%2], issued two sub-blocks ahead (as soon
+//          as softmax(j-2) has read that buffer);
+//   O_blk(j) = P(j) v(j) into TMEM O[j%2] once P(j) is in shared memory;
+//          the softmax warps fold it into their register accumulator
+//          (online-softmax rescale) during sub-block j+1;
+//   k and v stream through three-stage rings, each stage refilled as soon
+//          as the MMA that read it has completed.
 // Warps w and w+4 exchange their half-row maxima through a double-buffered
-// array and a 64-thread named barrier; the softmax warps hand P to the
-// MMA-issuing thread through an mbarrier, so no step waits for the whole CTA.
-// smem: Q | K0 K1 | V0 V1 (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
-#define AF_SMEM (1024 + AT_TILE + 4 * AT_SUBTILE + 2 * AT_TILE + 2048 + 256)
+// array and a 64-thread named barrier.
+// smem: Q | K ring | V ring (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
+#define AF_KV_STAGES 3
+#define AF_THREADS (AT_THREADS + 32)
+#define AF_SMEM (1024 + AT_TILE + 2 * AF_KV_STAGES * AT_SUBTILE + 2 * AT_TILE + 2048 + 256)
 
-__global__ void __launch_bounds__(AT_THREADS, 2)
+__global__ void __launch_bounds__(AF_THREADS, 2)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                        const __grid_constant__ CUtensorMap tm_qkv64, bf16* y, float* lse, int T,
                        int C, int NH, float scale, int* err) {
@@ -236,31 +241,37 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
-  uint8_t* sK = sm + AT_TILE;            // 2 stages of [64 x 64]
-  uint8_t* sV = sK + 2 * AT_SUBTILE;     // 2 stages
-  uint8_t* sP = sV + 2 * AT_SUBTILE;     // 2 x [128 x 64]
+  uint8_t* sK = sm + AT_TILE;                    // [AF_KV_STAGES] x [64 x 64]
+  uint8_t* sV = sK + AF_KV_STAGES * AT_SUBTILE;  // [AF_KV_STAGES]
+  uint8_t* sP = sV + AF_KV_STAGES * AT_SUBTILE;  // 2 x [128 x 64]
   float* red = reinterpret_cast<float*>(sP + 2 * AT_TILE);  // [2 iterations][2 halves][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * AT_TILE + 2048);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;  // [2]
-  uint64_t* v_full = bars + 3;  // [2]
-  uint64_t* s_done = bars + 5;  // [2]
-  uint64_t* o_done = bars + 7;  // [2]
-  uint64_t* p_ready = bars + 9;  // 8 warp arrivals per sub-block
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* k_full = bars + 1;                  // [AF_KV_STAGES]
+  uint64_t* v_full = k_full + AF_KV_STAGES;     // [AF_KV_STAGES]
+  uint64_t* s_done = v_full + AF_KV_STAGES;     // [2]
+  uint64_t* o_done = s_done + 2;                // [2]
+  // [2]: 8 warp arrivals for sub-block j on p_ready[j % 2] (two barriers, so
+  // the softmax warps, which may run a sub-block ahead of the issuer, never
+  // complete a barrier's phase twice before the issuer has waited for it)
+  uint64_t* p_ready = o_done + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(p_ready + 2);
 
   const int nqb = gridDim.y;
   const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the longest rows
   const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row = quarter * 32 + lane, q = q0 + row;
   const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
 
   if (tid == 0) {
-    for (int i = 0; i < 9; i++) mbar_init(&bars[i], 1);
-    mbar_init(p_ready, AT_THREADS / 32);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < AF_KV_STAGES; s++) { mbar_init(&k_full[s], 1); mbar_init(&v_full[s], 1); }
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&s_done[i], 1);
+      mbar_init(&o_done[i], 1);
+      mbar_init(&p_ready[i], AT_THREADS / 32);
+    }
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_qkv64);
@@ -271,155 +282,164 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   tc_fence_after();
   const uint32_t tm = *tslot;
   pdl_wait();  // from here on global memory written by the previous kernel is read
-  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
-  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
-  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(q_full, AT_TILE);
-    tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-    for (int s = 0; s < 2 && s < nsub; s++) {
-      mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
-      tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, s * AB_SUB, b);
-      mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
-      tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, s * AB_SUB, b);
-    }
-    // S(0)
-    mbar_wait(q_full, 0, err);
-    mbar_wait(&k_full[0], 0, err);
-    tc_fence_after();
-    const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK);
-#pragma unroll
-    for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-    tc_commit(&s_done[0]);
-  }
-  const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
-  float m = -INFINITY, lpart = 0.f, alpha_prev = 1.f;
-  float o[32];
-#pragma unroll
-  for (int i = 0; i < 32; i++) o[i] = 0.f;
-
-  for (int j = 0; j < nsub; j++) {
-    const int sb = j & 1;
-    const uint32_t tS = tm + (uint32_t)(sb * 64), tO = tm + 128 + (uint32_t)(sb * 64);
-    mbar_wait(&s_done[sb], (uint32_t)(j >> 1) & 1u, err);
-    tc_fence_after();
-    if (tid == 0) {
-      // S(j) is done with K stage sb: refill it with K(j+2)
-      if (j + 2 < nsub) {
-        mbar_arrive_expect_tx(&k_full[sb], AT_SUBTILE);
-        tma_load_3d(sK + sb * AT_SUBTILE, &tm_qkv64, &k_full[sb], C + h * AT_HS, (j + 2) * AB_SUB, b);
-      }
-      // issue S(j+1) into the other S buffer (its last reader was softmax(j-1))
-      if (j + 1 < nsub) {
-        const int nb = sb ^ 1;
-        mbar_wait(&k_full[nb], (uint32_t)((j + 1) >> 1) & 1u, err);
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA + MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
+      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+      auto load_k = [&](int j) {
+        const int s = j % AF_KV_STAGES;
+        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
+        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
+      };
+      auto load_v = [&](int j) {
+        const int s = j % AF_KV_STAGES;
+        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
+        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
+      };
+      auto issue_s = [&](int j) {  // S(j) into S[j%2]
+        const int s = j % AF_KV_STAGES;
+        mbar_wait(&k_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
         tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + nb * AT_SUBTILE);
+        const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + s * AT_SUBTILE);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + (uint32_t)(nb * 64), kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-        tc_commit(&s_done[nb]);
-      }
-    }
-    const int k0 = j * AB_SUB;
-    const bool diag = k0 + AB_SUB - 1 > q0;
-    uint32_t r[32];
-    tmem_ld32(tS + lanebase + half * 32, r);
-    tmem_ld_wait();
-    // pass 1: max over this half's 32 columns, exchanged with the partner warp
-    float mx = -INFINITY;
-    if (diag) {
-#pragma unroll
-      for (int jj = 0; jj < 32; jj++)
-        if (k0 + half * 32 + jj <= q) mx = fmaxf(mx, __uint_as_float(r[jj]));
-    } else {
-#pragma unroll
-      for (int jj = 0; jj < 32; jj++) mx = fmaxf(mx, __uint_as_float(r[jj]));
-    }
-    float* rd = red + sb * 256;
-    rd[half * 128 + row] = mx;
-    named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
-    const float mnew = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
-    const float alpha = ex2_hw((m - mnew) * sl2);
-    const float mo = mnew * sl2;
-    // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
-    float sum = 0.f;
-    uint8_t* P = sP + sb * AT_TILE;
-    uint8_t* prow = P + row * 128;
-    if (diag) {
-#pragma unroll
-      for (int g = 0; g < 4; g++) {
-        float p[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; jj++) {
-          const float e = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
-          p[jj] = k0 + half * 32 + g * 8 + jj <= q ? e : 0.f;
-          sum += p[jj];
+        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + (uint32_t)((j & 1) * 64), kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+        tc_commit(&s_done[j & 1]);
+      };
+      mbar_arrive_expect_tx(q_full, AT_TILE);
+      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+      for (int j = 0; j < AF_KV_STAGES && j < nsub; j++) { load_k(j); load_v(j); }
+      mbar_wait(q_full, 0, err);
+      issue_s(0);
+      if (nsub > 1) issue_s(1);
+      for (int j = 0; j < nsub; j++) {
+        if (j + AF_KV_STAGES < nsub) {  // S(j) has completed: its k stage takes k(j+3)
+          mbar_wait(&s_done[j & 1], (uint32_t)(j >> 1) & 1u, err);
+          load_k(j + AF_KV_STAGES);
         }
-        st_row8(prow, row & 7, half * 4 + g, p);
-      }
-    } else {
+        mbar_wait(&p_ready[j & 1], (uint32_t)(j >> 1) & 1u, err);  // P(j) written, S[j%2] read
+        tc_fence_after();
+        {
+          const int s = j % AF_KV_STAGES;
+          mbar_wait(&v_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
+          tc_fence_after();
+          const uint32_t aP = smem_u32(sP + (j & 1) * AT_TILE), bV = smem_u32(sV + s * AT_SUBTILE);
 #pragma unroll
-      for (int g = 0; g < 4; g++) {
-        float p[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; jj++) {
-          p[jj] = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
-          sum += p[jj];
+          for (int kk = 0; kk < 4; kk++)
+            tc_mma_bf16(tm + 128 + (uint32_t)((j & 1) * 64), kmaj(aP, kk), mnmaj(bV, kk), idO, kk > 0);
+          tc_commit(&o_done[j & 1]);
         }
-        st_row8(prow, row & 7, half * 4 + g, p);
+        if (j + 2 < nsub) issue_s(j + 2);
+        if (j >= 1 && j + 2 < nsub && j + 2 >= AF_KV_STAGES) {  // PV(j-1) has completed: v(j+2)
+          mbar_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, err);
+          load_v(j + 2);
+        }
       }
     }
-    lpart = lpart * alpha + sum;
-    m = mnew;
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(p_ready);
-    if (tid == 0) {
-      mbar_wait(p_ready, (uint32_t)j & 1u, err);
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane, q = q0 + row;
+    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
+    float m = -INFINITY, lpart = 0.f, alpha_prev = 1.f;
+    float o[32];
+#pragma unroll
+    for (int i = 0; i < 32; i++) o[i] = 0.f;
+
+    for (int j = 0; j < nsub; j++) {
+      const int sb = j & 1;
+      const uint32_t tS = tm + (uint32_t)(sb * 64);
+      mbar_wait(&s_done[sb], (uint32_t)(j >> 1) & 1u, err);
       tc_fence_after();
-      mbar_wait(&v_full[sb], (uint32_t)(j >> 1) & 1u, err);
-      const uint32_t aP = smem_u32(P), bV = smem_u32(sV + sb * AT_SUBTILE);
+      const int k0 = j * AB_SUB;
+      const bool diag = k0 + AB_SUB - 1 > q0;
+      uint32_t r[32];
+      tmem_ld32(tS + lanebase + half * 32, r);
+      tmem_ld_wait();
+      // pass 1: max over this half's 32 columns, exchanged with the partner warp
+      float mx = -INFINITY;
+      if (diag) {
 #pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tO, kmaj(aP, kk), mnmaj(bV, kk), idO, kk > 0);
-      tc_commit(&o_done[sb]);
+        for (int jj = 0; jj < 32; jj++)
+          if (k0 + half * 32 + jj <= q) mx = fmaxf(mx, __uint_as_float(r[jj]));
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj++) mx = fmaxf(mx, __uint_as_float(r[jj]));
+      }
+      float* rd = red + sb * 256;
+      rd[half * 128 + row] = mx;
+      named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
+      const float mnew = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
+      const float alpha = ex2_hw((m - mnew) * sl2);
+      const float mo = mnew * sl2;
+      // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
+      float sum = 0.f;
+      uint8_t* prow = sP + sb * AT_TILE + row * 128;
+      if (diag) {
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+          float p[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; jj++) {
+            const float e = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
+            p[jj] = k0 + half * 32 + g * 8 + jj <= q ? e : 0.f;
+            sum += p[jj];
+          }
+          st_row8(prow, row & 7, half * 4 + g, p);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < 4; g++) {
+          float p[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; jj++) {
+            p[jj] = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
+            sum += p[jj];
+          }
+          st_row8(prow, row & 7, half * 4 + g, p);
+        }
+      }
+      lpart = lpart * alpha + sum;
+      m = mnew;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[sb]);
+      // fold in O_blk(j-1) (its MMA ran during this sub-block's softmax); once
+      // read, O[(j-1)%2] and P[(j-1)%2] may be reused by PV(j+1) and P(j+1)
+      if (j > 0) {
+        const int pb = sb ^ 1;
+        mbar_wait(&o_done[pb], (uint32_t)((j - 1) >> 1) & 1u, err);
+        tc_fence_after();
+        uint32_t ro[32];
+        tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
+      }
+      alpha_prev = alpha;
+      tc_fence_before();
     }
-    // fold in O_blk(j-1) (its MMA ran during this iteration's softmax)
-    if (j > 0) {
-      const int pb = sb ^ 1;
-      mbar_wait(&o_done[pb], (uint32_t)((j - 1) >> 1) & 1u, err);
+    {  // the last O_blk
+      const int pb = (nsub - 1) & 1;
+      mbar_wait(&o_done[pb], (uint32_t)((nsub - 1) >> 1) & 1u, err);
       tc_fence_after();
       uint32_t ro[32];
       tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
       tmem_ld_wait();
 #pragma unroll
       for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
-      if (tid == 0 && j + 1 < nsub) {  // PV(j-1) is done with V stage pb: load V(j+1)
-        mbar_arrive_expect_tx(&v_full[pb], AT_SUBTILE);
-        tma_load_3d(sV + pb * AT_SUBTILE, &tm_qkv64, &v_full[pb], 2 * C + h * AT_HS, (j + 1) * AB_SUB, b);
-      }
     }
-    alpha_prev = alpha;
-    tc_fence_before();
-  }
-  {  // the last O_blk
-    const int pb = (nsub - 1) & 1;
-    mbar_wait(&o_done[pb], (uint32_t)((nsub - 1) >> 1) & 1u, err);
-    tc_fence_after();
-    uint32_t ro[32];
-    tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
-  }
-  __syncthreads();
-  red[half * 128 + row] = lpart;
-  __syncthreads();
-  const float l = red[row] + red[128 + row];
-  if (q < T) {
-    store_row32_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS + half * 32, o, 1.f / l);
-    if (half == 0) lse[(int64_t)bh * T + q] = m * scale + logf(l);
+    named_bar_sync(5, AT_THREADS);  // every softmax warp is past its last exchange
+    red[half * 128 + row] = lpart;
+    named_bar_sync(5, AT_THREADS);
+    const float l = red[row] + red[128 + row];
+    if (q < T) {
+      store_row32_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS + half * 32, o, 1.f / l);
+      if (half == 0) lse[(int64_t)bh * T + q] = m * scale + logf(l);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -860,7 +880,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
   }
   dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
   cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
-  launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AT_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
+  launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AF_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
 }
 
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
