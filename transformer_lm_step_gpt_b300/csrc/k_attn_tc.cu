@@ -155,6 +155,56 @@ __device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32
   }
 }
 
+// The dK/dV kernel's elementwise step for 32 query columns of one key row,
+// kept in registers: P^T and dS^T as packed bf16 pairs (pk, dk: 16 words
+// each, column pairs in order), so they can be computed before the shared-
+// memory buffer they go to is free.  Same arithmetic as bwd_elementwise
+// with KEYROW (lse in natural-log units, D per column from shared memory).
+template <bool MASK>
+__device__ __forceinline__ void keyrow_pack(const uint32_t* rs, const uint32_t* rd, const float* lsec,
+                                            const float* dc, float sl2, int col0, int key, int colmax,
+                                            uint32_t* pk, uint32_t* dk) {
+  const float L2E = 1.4426950408889634f;
+#pragma unroll
+  for (int g = 0; g < 4; g++) {
+    const float4 a = *reinterpret_cast<const float4*>(lsec + g * 8);
+    const float4 bq = *reinterpret_cast<const float4*>(lsec + g * 8 + 4);
+    const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
+    const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
+    const float lv[8] = {a.x * L2E, a.y * L2E, a.z * L2E, a.w * L2E, bq.x * L2E, bq.y * L2E, bq.z * L2E, bq.w * L2E};
+    const float dv[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
+    float p[8], ds[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
+      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
+      float pkv = pv;
+      if (MASK) {  // a masked column may hold stale lse / D: select, do not scale
+        const int col = col0 + g * 8 + j;
+        const bool ok = col >= key && col < colmax;
+        pkv = ok ? pkv : 0.f;
+        dsv = ok ? dsv : 0.f;
+      }
+      p[j] = pkv;
+      ds[j] = dsv;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      __nv_bfloat162 tp = __floats2bfloat162_rn(p[j], p[j + 1]);
+      __nv_bfloat162 td = __floats2bfloat162_rn(ds[j], ds[j + 1]);
+      pk[g * 4 + j / 2] = *reinterpret_cast<uint32_t*>(&tp);
+      dk[g * 4 + j / 2] = *reinterpret_cast<uint32_t*>(&td);
+    }
+  }
+}
+// Write 16 packed words (32 bf16 columns, 16-byte chunks c8base..c8base+3)
+// into a row of a [rows x 64] 128B-swizzled atom (rowp = atom + r*128).
+__device__ __forceinline__ void store_packed32(uint8_t* rowp, int rx, int c8base, const uint32_t* w) {
+#pragma unroll
+  for (int g = 0; g < 4; g++)
+    *reinterpret_cast<uint4*>(rowp + (((c8base + g) ^ rx) << 4)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
+}
+
 __device__ __forceinline__ void store_row64_bf16(bf16* dst, const float* v, float mul) {
 #pragma unroll
   for (int i = 0; i < 64; i += 8) {
@@ -477,39 +527,46 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 }
 
 // ============================================================ backward: dK, dV
-// One CTA per (128-key block, b*h), queries walked in 64-row sub-blocks,
-// warp-specialised so the tensor core never waits for the elementwise work:
-//   warp 9      loader: TMA of q and dy sub-blocks into a DKV_STAGES-deep
+// One CTA per (128-key block, b*h), queries walked in 128-row sub-blocks,
+// warp-specialised:
+//   warp 9      loader: TMA of the q and dy tiles into a DKV_STAGES-deep
 //               ring, with each sub-block's lse and D (bulk copies on the
 //               same barrier when T is a multiple of 4; otherwise all of the
 //               block's lse / D are read once, before the first sub-block)
-//   warp 8      MMA issuer: S^T(j) = K q(j)^T and dP^T(j) = V dy(j)^T into
-//               TMEM buffer j%2, then dV += P^T(j-1) dy(j-1), dK += dS^T(j-1)
-//               q(j-1) -- so sub-block j's scores are computed while the
-//               compute warps work on j-1
-//   warps 0..7  compute: P^T = 2^(S^T*scale*log2e - lse*log2e), dS^T = P^T
-//               (dP^T - D) into shared-memory buffer j%2 (two per TMEM lane
-//               quarter, splitting the 64 query columns)
-// A q / dy stage is refilled only once dV, dK of its sub-block are done, so
-// the ring is deep enough to cover that round trip plus the TMA latency.
-// TMEM: [S^T | dP^T] x 2 buffers, dV, dK (384 of 512 columns).
-// smem: K | V | DKV_STAGES x (q, dy) | 2 x (P^T, dS^T) | barriers | lse / D
-// (per stage: [DKV_STAGES][lse 64, D 64]; whole block: lse[Tq], D[Tq] with
-// Tq = T - k0 rounded up to 64).  The grid's y index is the key block, so
+//   warp 16     MMA issuer: S^T(j) = K q(j)^T and dP^T(j) = V dy(j)^T
+//               (N = 128) into TMEM, then dV += P^T(j-1) dy(j-1) and dK +=
+//               dS^T(j-1) q(j-1) (N = 64, K = 128 queries) with P^T and dS^T
+//               read from TMEM (the A operand), dy and q from shared memory
+//   warps 0..15 compute: copy S^T(j), dP^T(j) to registers at once (so
+//               S^T(j+1) runs during their elementwise work), then P^T =
+//               2^(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D) as
+//               packed bf16 into TMEM (warps w, w+4, w+8, w+12 share TMEM
+//               lane quarter w%4 and take 32 of the 128 query columns each;
+//               the math runs before the buffer wait, so it overlaps
+//               dV/dK(j-1))
+// Keeping P^T and dS^T out of shared memory saves their stores and the
+// MMAs' operand reads: shared-memory bandwidth, not the tensor core, bounds
+// these N = 64 products when both operands come from shared memory.
+// A q / dy stage is refilled once dV, dK of its sub-block are done.
+// TMEM: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383, P^T 384..447,
+// dS^T 448..511 (bf16 pairs).
+// smem: K | V | DKV_STAGES x (q, dy) | barriers | lse / D
+// (per stage: [DKV_STAGES][lse 128, D 128]; whole block: lse[Tq], D[Tq] with
+// Tq = T - k0 rounded up to 128).  The grid's y index is the key block, so
 // the hardware starts the longest blocks (most queries) first.
-#define DKV_STAGES 6
-#define DKV_THREADS (AT_THREADS + 64)
-#define AKV_FIXED (1024 + 2 * AT_TILE + DKV_STAGES * 2 * AT_SUBTILE + 4 * AT_TILE + 256)
-static inline bool akv_staged_ld(int T) { return T % 4 == 0; }
+#define DKV_SUB 128
+#define DKV_STAGES 4
+#define DKV_CWARPS 16
+#define DKV_THREADS (DKV_CWARPS * 32 + 64)
+#define AKV_FIXED (1024 + 2 * AT_TILE + DKV_STAGES * 2 * AT_TILE + 256)
 static inline size_t akv_smem(int T) {
-  const size_t whole = 8 * (size_t)((T + 63) / 64 * 64);
-  return AKV_FIXED + (akv_staged_ld(T) ? (size_t)DKV_STAGES * 512 : whole);
+  const size_t whole = 8 * (size_t)((T + DKV_SUB - 1) / DKV_SUB * DKV_SUB);
+  return AKV_FIXED + ((T % 4 == 0) ? (size_t)DKV_STAGES * 8 * DKV_SUB : whole);
 }
 
 __global__ void __launch_bounds__(DKV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                           const __grid_constant__ CUtensorMap tm_qkv64,
-                           const __grid_constant__ CUtensorMap tm_dy64, bf16* dqkv, const float* lse,
+                           const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
                            const float* dsum, float* bias_partial, int T, int C, int NH, float scale,
                            int* err) {
   pdl_trigger();
@@ -517,65 +574,62 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
   uint8_t* sm = align1024(smraw);
   uint8_t* sK = sm;
   uint8_t* sV = sm + AT_TILE;
-  uint8_t* sQ = sm + 2 * AT_TILE;                     // [DKV_STAGES] x [64 x 64]
-  uint8_t* sD = sQ + DKV_STAGES * AT_SUBTILE;         // dy, [DKV_STAGES]
-  uint8_t* sP = sD + DKV_STAGES * AT_SUBTILE;         // P^T  [2] x [128 keys x 64 queries]
-  uint8_t* sS = sP + 2 * AT_TILE;                     // dS^T [2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * AT_TILE);
+  uint8_t* sQ = sm + 2 * AT_TILE;                // [DKV_STAGES] x [128 x 64]
+  uint8_t* sD = sQ + DKV_STAGES * AT_TILE;       // dy, [DKV_STAGES]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + DKV_STAGES * AT_TILE);
   uint64_t* kv_full = bars;
   uint64_t* ld_full = bars + 1;                  // whole-block lse / D written
   uint64_t* q_full = bars + 2;                   // [DKV_STAGES]: TMA bytes
-  uint64_t* q_empty = q_full + DKV_STAGES;       // [DKV_STAGES]: MMA commit
-  uint64_t* s_full = q_empty + DKV_STAGES;       // [2]: S^T, dP^T ready
-  uint64_t* s_empty = s_full + 2;                // [2]: compute warps have read them
-  uint64_t* p_full = s_empty + 2;                // [2]: P^T, dS^T written
-  uint64_t* p_empty = p_full + 2;                // [2]: dV/dK MMAs have read them
-  uint64_t* done = p_empty + 2;
+  uint64_t* q_empty = q_full + DKV_STAGES;       // [DKV_STAGES]: dV, dK of the stage done
+  uint64_t* s_full = q_empty + DKV_STAGES;       // S^T, dP^T in TMEM
+  uint64_t* s_empty = s_full + 1;                // 8 warps have copied them out
+  uint64_t* p_full = s_empty + 1;                // 8 warps have written P^T, dS^T
+  uint64_t* p_empty = p_full + 1;                // dV, dK MMAs have read them
+  uint64_t* done = p_empty + 1;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
-  float* sLD = reinterpret_cast<float*>(sS + 2 * AT_TILE + 256);
+  float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
   const int kb = blockIdx.y;  // key block
   const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int k0 = kb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nsub = (T - k0 + AB_SUB - 1) / AB_SUB;  // 64-query sub-blocks from k0 to T
-  const bool staged = (T & 3) == 0;                 // per-stage lse / D bulk copies
+  const int nsub = (T - k0 + DKV_SUB - 1) / DKV_SUB;  // 128-query sub-blocks from k0 to T
+  const bool staged = (T & 3) == 0;                   // per-stage lse / D bulk copies
 
   if (tid == 0) {
     mbar_init(kv_full, 1);
     mbar_init(ld_full, 1);
     for (int s = 0; s < DKV_STAGES; s++) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
-    for (int i = 0; i < 2; i++) {
-      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 8);
-      mbar_init(&p_full[i], 8); mbar_init(&p_empty[i], 1);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, DKV_CWARPS);
+    mbar_init(p_full, DKV_CWARPS);
+    mbar_init(p_empty, 1);
     mbar_init(done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
-    tma_prefetch_desc(&tm_qkv64);
-    tma_prefetch_desc(&tm_dy64);
+    tma_prefetch_desc(&tm_dy);
   }
-  if (warp == 8) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  if (warp == DKV_CWARPS) { tmem_alloc(tslot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
   pdl_wait();  // from here on global memory written by the previous kernel is read
-  const uint32_t tdV = tm + 256, tdK = tm + 320;
+  const uint32_t tSt = tm, tdPt = tm + 128, tdV = tm + 256, tdK = tm + 320, tPt = tm + 384, tdSt = tm + 448;
   const float sl2 = scale * 1.4426950408889634f;
   const float* lrow = lse + (int64_t)bh * T + k0;
   const float* drow = dsum + (int64_t)bh * T + k0;
 
-  if (warp == 9) {
+  if (warp == DKV_CWARPS + 1) {
     // ---------------------------------------------------------------- loader
     auto issue = [&](int j) {
-      const int s = j % DKV_STAGES, q0 = k0 + j * AB_SUB;
-      const uint32_t ldb = staged ? 4u * (uint32_t)min(AB_SUB, T - q0) : 0u;  // a multiple of 16
-      mbar_arrive_expect_tx(&q_full[s], 2 * AT_SUBTILE + 2 * ldb);
-      tma_load_3d(sQ + s * AT_SUBTILE, &tm_qkv64, &q_full[s], h * AT_HS, q0, b);
-      tma_load_3d(sD + s * AT_SUBTILE, &tm_dy64, &q_full[s], h * AT_HS, q0, b);
+      const int s = j % DKV_STAGES, q0 = k0 + j * DKV_SUB;
+      const uint32_t ldb = staged ? 4u * (uint32_t)min(DKV_SUB, T - q0) : 0u;  // a multiple of 16
+      mbar_arrive_expect_tx(&q_full[s], 2 * AT_TILE + 2 * ldb);
+      tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &q_full[s], h * AT_HS, q0, b);
+      tma_load_3d(sD + s * AT_TILE, &tm_dy, &q_full[s], h * AT_HS, q0, b);
       if (staged) {
-        bulk_load(sLD + s * 128, lrow + j * AB_SUB, ldb, &q_full[s]);
-        bulk_load(sLD + s * 128 + 64, drow + j * AB_SUB, ldb, &q_full[s]);
+        bulk_load(sLD + s * 2 * DKV_SUB, lrow + j * DKV_SUB, ldb, &q_full[s]);
+        bulk_load(sLD + s * 2 * DKV_SUB + DKV_SUB, drow + j * DKV_SUB, ldb, &q_full[s]);
       }
     };
     int j = 0;
@@ -587,8 +641,8 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     }
     if (!staged) {
       float* sL = sLD;
-      float* sDd = sLD + nsub * AB_SUB;
-      const int nq = nsub * AB_SUB;
+      float* sDd = sLD + nsub * DKV_SUB;
+      const int nq = nsub * DKV_SUB;
       for (int i0 = 0; i0 < nq; i0 += 32 * 16) {  // 32 loads in flight per lane
         float lv[16], dv[16];
 #pragma unroll
@@ -613,38 +667,36 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
         issue(j);
       }
     }
-  } else if (warp == 8) {
+  } else if (warp == DKV_CWARPS) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
+      const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
       const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
       mbar_wait(kv_full, 0, err);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
       for (int j = 0; j <= nsub; j++) {
         if (j < nsub) {
-          const int s = j % DKV_STAGES, bf = j & 1;
+          const int s = j % DKV_STAGES;
           mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);
-          mbar_wait(&s_empty[bf], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);
+          if (j > 0) mbar_wait(s_empty, (uint32_t)(j - 1) & 1u, err);  // S^T(j-1), dP^T(j-1) copied out
           tc_fence_after();
-          const uint32_t bQ = smem_u32(sQ + s * AT_SUBTILE), bD = smem_u32(sD + s * AT_SUBTILE);
-          const uint32_t tS = tm + (uint32_t)(bf * 128), tP = tS + 64;
+          const uint32_t bQ = smem_u32(sQ + s * AT_TILE), bD = smem_u32(sD + s * AT_TILE);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tSt, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tP, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
-          tc_commit(&s_full[bf]);
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdPt, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
+          tc_commit(s_full);
         }
         if (j >= 1) {
-          const int jj = j - 1, s = jj % DKV_STAGES, bf = jj & 1;
-          mbar_wait(&p_full[bf], (uint32_t)(jj >> 1) & 1u, err);
+          const int jj = j - 1, s = jj % DKV_STAGES;
+          mbar_wait(p_full, (uint32_t)jj & 1u, err);
           tc_fence_after();
-          const uint32_t aP = smem_u32(sP + bf * AT_TILE), aS = smem_u32(sS + bf * AT_TILE);
-          const uint32_t bQ = smem_u32(sQ + s * AT_SUBTILE), bD = smem_u32(sD + s * AT_SUBTILE);
+          const uint32_t bQ = smem_u32(sQ + s * AT_TILE), bD = smem_u32(sD + s * AT_TILE);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdV, kmaj(aP, kk), mnmaj(bD, kk), idO, (jj > 0 || kk > 0));
+          for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdV, tPt + kk * 8, mnmaj(bD, kk), idO, (jj > 0 || kk > 0));
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdK, kmaj(aS, kk), mnmaj(bQ, kk), idO, (jj > 0 || kk > 0));
-          tc_commit(&p_empty[bf]);
+          for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdK, tdSt + kk * 8, mnmaj(bQ, kk), idO, (jj > 0 || kk > 0));
+          tc_commit(p_empty);
           tc_commit(&q_empty[s]);
         }
       }
@@ -652,79 +704,88 @@ __global__ void __launch_bounds__(DKV_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- compute warps
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, colq = warp >> 2;  // lane quarter, 32-column group
     const int row = quarter * 32 + lane, key = k0 + row;
     const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
     mbar_wait(ld_full, 0, err);
     for (int j = 0; j < nsub; j++) {
-      const int bf = j & 1, s = j % DKV_STAGES;
-      const int q0 = k0 + j * AB_SUB;
-      mbar_wait(&s_full[bf], (uint32_t)(j >> 1) & 1u, err);
+      const int s = j % DKV_STAGES;
+      const int q0 = k0 + j * DKV_SUB;
+      mbar_wait(s_full, (uint32_t)j & 1u, err);
       tc_fence_after();
       uint32_t rs[32], rd[32];
-      const uint32_t tS = tm + (uint32_t)(bf * 128);
-      tmem_ld32(tS + lanebase + half * 32, rs);
-      tmem_ld32(tS + 64 + lanebase + half * 32, rd);
+      tmem_ld32(tSt + lanebase + colq * 32, rs);
+      tmem_ld32(tdPt + lanebase + colq * 32, rd);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[bf]);
-      mbar_wait(&p_empty[bf], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);  // P^T / dS^T buffer free
+      if (lane == 0) mbar_arrive(s_empty);
       if (staged) mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);  // the stage's lse / D
-      const float* lc = staged ? sLD + s * 128 + half * 32 : sLD + j * AB_SUB + half * 32;
-      const float* dc = staged ? sLD + s * 128 + 64 + half * 32 : sLD + (nsub + j) * AB_SUB + half * 32;
-      uint8_t* prow = sP + bf * AT_TILE + row * 128;
-      uint8_t* srow = sS + bf * AT_TILE + row * 128;
-      if (q0 < k0 + AT_BLK || q0 + AB_SUB > T)
-        bwd_elementwise<true, true>(rs, rd, lc, dc, 0.f, 0.f, sl2, q0 + half * 32, key, prow, srow,
-                                    row & 7, half * 4, T);
-      else
-        bwd_elementwise<true, false>(rs, rd, lc, dc, 0.f, 0.f, sl2, q0 + half * 32, key, prow, srow,
-                                     row & 7, half * 4);
-      fence_proxy_async_smem();
+      const float* lc = (staged ? sLD + s * 2 * DKV_SUB : sLD + j * DKV_SUB) + colq * 32;
+      const float* dc = (staged ? sLD + s * 2 * DKV_SUB + DKV_SUB : sLD + (nsub + j) * DKV_SUB) + colq * 32;
+      const int c0 = q0 + colq * 32;
+      // the math runs while dV, dK(j-1) still read the shared-memory buffers
+      uint32_t pk[16], dk[16];
+      if (q0 < k0 + AT_BLK || q0 + DKV_SUB > T) keyrow_pack<true>(rs, rd, lc, dc, sl2, c0, key, T, pk, dk);
+      else keyrow_pack<false>(rs, rd, lc, dc, sl2, c0, key, T, pk, dk);
+      if (j > 0) mbar_wait(p_empty, (uint32_t)(j - 1) & 1u, err);  // dV, dK(j-1) have read P^T, dS^T
+      tc_fence_after();
+      tmem_st16(tPt + lanebase + colq * 16, pk);
+      tmem_st16(tdSt + lanebase + colq * 16, dk);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[bf]);
+      if (lane == 0) mbar_arrive(p_full);
     }
     mbar_wait(done, 0, err);
     tc_fence_after();
+    // epilogue: column groups 0, 1 take dV columns 0..31, 32..63; 2, 3 take dK
     const int64_t C3 = 3 * (int64_t)C;
-    float* red = reinterpret_cast<float*>(sP);  // [2][4][64]: free once every MMA is done
+    const int which = colq >> 1, cc = (colq & 1) * 32;  // which: 0 dV, 1 dK
+    const float mul = which ? scale : 1.f;
+    float* red = reinterpret_cast<float*>(sQ);  // [2][4][64]: the q ring is free once every MMA is done
     float v[32];
     uint32_t r[32];
-    tmem_ld32(tdV + lanebase + half * 32, r);
+    tmem_ld32((which ? tdK : tdV) + lanebase + cc, r);
     tmem_ld_wait();
 #pragma unroll
     for (int i = 0; i < 32; i++) v[i] = key < T ? __uint_as_float(r[i]) : 0.f;
-    if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + 2 * C + h * AT_HS + half * 32, v, 1.f);
-    red[quarter * 64 + half * 32 + lane] = warp_colsum32(v);
-    tmem_ld32(tdK + lanebase + half * 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = key < T ? __uint_as_float(r[i]) : 0.f;
-    if (key < T) store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + C + h * AT_HS + half * 32, v, scale);
-    red[256 + quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
+    if (key < T)
+      store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * AT_HS + cc, v, mul);
+    red[which * 256 + quarter * 64 + cc + lane] = warp_colsum32(v) * mul;
     // the block's column sums of dV and dK: one partial row of the qkv bias
     // gradient per (batch row, key block)
-    named_bar_sync(1, AT_THREADS);
+    named_bar_sync(1, DKV_CWARPS * 32);
     if (tid < 128) {
-      const int which = tid >> 6, col = tid & 63;  // 0: dV, 1: dK
-      const float* rr = red + which * 256 + col;
+      const int wh = tid >> 6, col = tid & 63;  // 0: dV, 1: dK
+      const float* rr = red + wh * 256 + col;
       const float sum = (rr[0] + rr[64]) + (rr[128] + rr[192]);
-      bias_partial[((int64_t)b * gridDim.y + kb) * C3 + (which ? C : 2 * C) + h * AT_HS + col] = sum;
+      bias_partial[((int64_t)b * gridDim.y + kb) * C3 + (wh ? C : 2 * C) + h * AT_HS + col] = sum;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) { tc_fence_after(); tmem_dealloc(tm, 512); }
+  if (warp == DKV_CWARPS) { tc_fence_after(); tmem_dealloc(tm, 512); }
 }
 
 // ============================================================ backward: dQ
-// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks
-// (256 TMEM columns, ~81 KB shared memory: two CTAs per SM).
-// smem: Q | dO | K0 K1 | V0 V1 (64-row tiles) | dS ([128 x 64]) | barriers
-#define AQ_SMEM (1024 + 2 * AT_TILE + 4 * AT_SUBTILE + AT_TILE + 256)
+// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks; two
+// CTAs share an SM.  Warps 0..7 compute, warp 8 (one thread) issues every
+// TMA load and MMA:
+//   S(j) = q k(j)^T and dP(j) = dO v(j)^T into TMEM (one buffer: the
+//          compute warps copy it to registers first thing, so S(j+1) runs
+//          during the elementwise work of sub-block j);
+//   dQ += dS(j) k(j) once dS(j) is in shared memory (two dS buffers).
+// k streams through a three-stage ring (a stage is read by S(j) and by
+// dQ(j)), v through a two-stage one.
+// TMEM: S 0..63, dP 64..127, dQ 128..191 (256 columns).
+// smem: Q | dO | K ring | V ring (64-row tiles) | dS [2] ([128 x 64]) | barriers
+#define AQ_K_STAGES 3
+#define AQ_V_STAGES 2
+#define AQ_THREADS (AT_THREADS + 32)
+#define AQ_SMEM (1024 + 2 * AT_TILE + (AQ_K_STAGES + AQ_V_STAGES) * AT_SUBTILE + 2 * AT_TILE + 256)
 
-__global__ void __launch_bounds__(AT_THREADS, 2)
+__global__ void __launch_bounds__(AQ_THREADS, 2)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
                           const __grid_constant__ CUtensorMap tm_dy,
                           const __grid_constant__ CUtensorMap tm_qkv64, bf16* dqkv, const float* lse,
@@ -735,29 +796,36 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
   uint8_t* sD = sm + AT_TILE;
-  uint8_t* sK = sm + 2 * AT_TILE;    // 2 stages of [64 x 64]
-  uint8_t* sV = sK + 2 * AT_SUBTILE; // 2 stages
-  uint8_t* sS = sV + 2 * AT_SUBTILE; // dS [128 queries x 64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + AT_TILE);
+  uint8_t* sK = sm + 2 * AT_TILE;              // [AQ_K_STAGES] x [64 x 64]
+  uint8_t* sV = sK + AQ_K_STAGES * AT_SUBTILE; // [AQ_V_STAGES]
+  uint8_t* sS = sV + AQ_V_STAGES * AT_SUBTILE; // dS [2] x [128 queries x 64 keys]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * AT_TILE);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;  // [2]
-  uint64_t* s_done = bars + 3;
-  uint64_t* o_done = bars + 4;
-  uint64_t* p_ready = bars + 5;  // 8 warp arrivals per sub-block
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
+  uint64_t* k_full = bars + 1;                 // [AQ_K_STAGES]
+  uint64_t* k_empty = k_full + AQ_K_STAGES;    // [AQ_K_STAGES]: dQ(j) has read k(j)
+  uint64_t* v_full = k_empty + AQ_K_STAGES;    // [AQ_V_STAGES]
+  uint64_t* s_full = v_full + AQ_V_STAGES;     // S(j), dP(j) in TMEM
+  uint64_t* s_empty = s_full + 1;              // 8 warps have copied them out
+  uint64_t* p_full = s_empty + 1;              // [2]: 8 warps have written dS(j)
+  uint64_t* p_empty = p_full + 2;              // [2]: dQ(j) has read dS(j)
+  uint64_t* dq_done = p_empty + 2;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(dq_done + 1);
 
   const int nqb = gridDim.y;
   const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the blocks that meet the most keys
   const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
   const int q0 = qb * AT_BLK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, half = warp >> 2;
-  const int row = quarter * 32 + lane, q = q0 + row;
   const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
 
   if (tid == 0) {
-    for (int i = 0; i < 5; i++) mbar_init(&bars[i], 1);
-    mbar_init(p_ready, AT_THREADS / 32);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < AQ_K_STAGES; s++) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
+    for (int s = 0; s < AQ_V_STAGES; s++) mbar_init(&v_full[s], 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, AT_THREADS / 32);
+    for (int i = 0; i < 2; i++) { mbar_init(&p_full[i], AT_THREADS / 32); mbar_init(&p_empty[i], 1); }
+    mbar_init(dq_done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_dy);
@@ -770,96 +838,116 @@ __global__ void __launch_bounds__(AT_THREADS, 2)
   const uint32_t tm = *tslot;
   pdl_wait();  // from here on global memory written by the previous kernel is read
   const uint32_t tS = tm, tdP = tm + 64, tdQ = tm + 128;
-  const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
 
-  if (tid == 0) {
-    mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
-    tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-    tma_load_3d(sD, &tm_dy, q_full, h * AT_HS, q0, b);
-    for (int s = 0; s < 2 && s < nsub; s++) {
-      mbar_arrive_expect_tx(&kv_full[s], 2 * AT_SUBTILE);
-      tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &kv_full[s], C + h * AT_HS, s * AB_SUB, b);
-      tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &kv_full[s], 2 * C + h * AT_HS, s * AB_SUB, b);
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA + MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
+      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
+      auto load_k = [&](int j) {
+        const int s = j % AQ_K_STAGES;
+        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
+        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
+      };
+      auto load_v = [&](int j) {
+        const int s = j % AQ_V_STAGES;
+        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
+        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
+      };
+      auto issue_sdp = [&](int j) {  // S(j), dP(j)
+        const int ks = j % AQ_K_STAGES, vs = j % AQ_V_STAGES;
+        mbar_wait(&k_full[ks], (uint32_t)(j / AQ_K_STAGES) & 1u, err);
+        mbar_wait(&v_full[vs], (uint32_t)(j / AQ_V_STAGES) & 1u, err);
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ), aD = smem_u32(sD);
+        const uint32_t bK = smem_u32(sK + ks * AT_SUBTILE), bV = smem_u32(sV + vs * AT_SUBTILE);
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aD, kk), kmaj(bV, kk), idS, kk > 0);
+        tc_commit(s_full);
+      };
+      mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
+      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+      tma_load_3d(sD, &tm_dy, q_full, h * AT_HS, q0, b);
+      for (int j = 0; j < AQ_K_STAGES && j < nsub; j++) load_k(j);
+      for (int j = 0; j < AQ_V_STAGES && j < nsub; j++) load_v(j);
+      mbar_wait(q_full, 0, err);
+      issue_sdp(0);
+      for (int j = 0; j < nsub; j++) {
+        if (j + 1 < nsub) {
+          mbar_wait(s_empty, (uint32_t)j & 1u, err);  // S(j), dP(j) copied out (so dP(j) is done)
+          if (j + AQ_V_STAGES < nsub) load_v(j + AQ_V_STAGES);
+          issue_sdp(j + 1);
+        }
+        mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, err);  // dS(j) written
+        tc_fence_after();
+        {
+          const int ks = j % AQ_K_STAGES;
+          const uint32_t aS = smem_u32(sS + (j & 1) * AT_TILE), bK = smem_u32(sK + ks * AT_SUBTILE);
+#pragma unroll
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdQ, kmaj(aS, kk), mnmaj(bK, kk), idO, (j > 0 || kk > 0));
+          tc_commit(&p_empty[j & 1]);
+          tc_commit(&k_empty[ks]);
+        }
+        if (j >= 1 && j + 2 < nsub) {  // dQ(j-1) has read k(j-1): its stage takes k(j+2)
+          mbar_wait(&k_empty[(j - 1) % AQ_K_STAGES], (uint32_t)((j - 1) / AQ_K_STAGES) & 1u, err);
+          load_k(j + 2);
+        }
+      }
+      tc_commit(dq_done);
     }
-  }
-  const float sl2 = scale * 1.4426950408889634f;
-  const float my_lse = q < T ? lse[(int64_t)bh * T + q] * 1.4426950408889634f : INFINITY;
-  const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
-  const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
-  const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
-
-  for (int kb = 0; kb < nsub; kb++) {
-    const int st = kb & 1;
-    const uint32_t ph = (uint32_t)(kb >> 1) & 1u;
-    const int k0 = kb * AB_SUB;
-    if (tid == 0) {
-      if (kb == 0) mbar_wait(q_full, 0, err);
-      mbar_wait(&kv_full[st], ph, err);
+  } else {
+    // ------------------------------------------------------------ compute warps
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane, q = q0 + row;
+    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = scale * 1.4426950408889634f;
+    const float my_lse = q < T ? lse[(int64_t)bh * T + q] * 1.4426950408889634f : INFINITY;
+    const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+    for (int j = 0; j < nsub; j++) {
+      const int k0 = j * AB_SUB;
+      mbar_wait(s_full, (uint32_t)j & 1u, err);
       tc_fence_after();
-      const uint32_t aQ = smem_u32(sQ), aD = smem_u32(sD);
-      const uint32_t bK = smem_u32(sK + st * AT_SUBTILE), bV = smem_u32(sV + st * AT_SUBTILE);
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aD, kk), kmaj(bV, kk), idS, kk > 0);
-      tc_commit(s_done);
-    }
-    mbar_wait(s_done, (uint32_t)kb & 1u, err);
-    tc_fence_after();
-    const bool diag = k0 + AB_SUB > q0;
-    {
       uint32_t rs[32], rd[32];
       tmem_ld32(tS + lanebase + half * 32, rs);
       tmem_ld32(tdP + lanebase + half * 32, rd);
       tmem_ld_wait();
-      if (diag)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      mbar_wait(&p_empty[j & 1], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);  // dQ(j-2) has read the buffer
+      uint8_t* srow = sS + (j & 1) * AT_TILE + row * 128;
+      if (k0 + AB_SUB > q0)
         bwd_elementwise<false, true>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
-                                     nullptr, sS + row * 128, row & 7, half * 4);
+                                     nullptr, srow, row & 7, half * 4);
       else
         bwd_elementwise<false, false>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
-                                      nullptr, sS + row * 128, row & 7, half * 4);
+                                      nullptr, srow, row & 7, half * 4);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[j & 1]);
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(p_ready);
-    if (tid == 0) {
-      mbar_wait(p_ready, (uint32_t)kb & 1u, err);
-      tc_fence_after();
-      const uint32_t aS = smem_u32(sS), bK = smem_u32(sK + st * AT_SUBTILE);
-#pragma unroll
-      for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdQ, kmaj(aS, kk), mnmaj(bK, kk), idO, (kb > 0 || kk > 0));
-      tc_commit(o_done);
-    }
-    mbar_wait(o_done, (uint32_t)kb & 1u, err);
+    mbar_wait(dq_done, 0, err);
     tc_fence_after();
-    if (tid == 0 && kb + 2 < nsub) {
-      mbar_arrive_expect_tx(&kv_full[st], 2 * AT_SUBTILE);
-      tma_load_3d(sK + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], C + h * AT_HS, k0 + 2 * AB_SUB, b);
-      tma_load_3d(sV + st * AT_SUBTILE, &tm_qkv64, &kv_full[st], 2 * C + h * AT_HS, k0 + 2 * AB_SUB, b);
-    }
-    // every thread has waited o_done: the dS buffer is free
-    tc_fence_before();
-  }
-  __syncthreads();
-  tc_fence_after();
-  float v[32];
-  {
-    uint32_t r[32];
-    tmem_ld32(tdQ + lanebase + half * 32, r);
-    tmem_ld_wait();
+    float v[32];
+    {
+      uint32_t r[32];
+      tmem_ld32(tdQ + lanebase + half * 32, r);
+      tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; j++) v[j] = q < T ? __uint_as_float(r[j]) : 0.f;
-  }
-  if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
-  // the block's column sums of dQ: one partial row of the qkv bias gradient
-  // per (batch row, query block); the dS buffer is free after the loop
-  float* red = reinterpret_cast<float*>(sS);  // [4][64]
-  red[quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
-  __syncthreads();
-  if (tid < 64) {
-    const float* rr = red + tid;
-    bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * AT_HS + tid] = (rr[0] + rr[64]) + (rr[128] + rr[192]);
+      for (int i = 0; i < 32; i++) v[i] = q < T ? __uint_as_float(r[i]) : 0.f;
+    }
+    if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
+    // the block's column sums of dQ: one partial row of the qkv bias gradient
+    // per (batch row, query block); the dS buffers are free once dQ is done
+    float* red = reinterpret_cast<float*>(sS);  // [4][64]
+    red[quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
+    named_bar_sync(1, AT_THREADS);
+    if (tid < 64) {
+      const float* rr = red + tid;
+      bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * AT_HS + tid] = (rr[0] + rr[64]) + (rr[128] + rr[192]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -890,9 +978,9 @@ bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
     launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
     return false;
   }
-  CUtensorMap tq, td, tq64, td64;
+  CUtensorMap tq, td, tq64;
   if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C) ||
-      !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB) || !make_tmap_btw(&td64, dy, B, T, C, AB_SUB)) {
+      !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB)) {
     c.host_fail = 1;
     return false;
   }
@@ -902,8 +990,8 @@ bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
   dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
   const size_t kv_smem = akv_smem(T);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_smem);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, tq64, td64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
+  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, td, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AT_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
+  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AQ_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
   return true;
 }
