@@ -7,21 +7,25 @@
 // time in TMEM and folded into an online softmax (forward) or recomputed from
 // the saved row logsumexp (backward).
 //
-// Head size 64.  Every tile of q, k, v, dy is one TMA box [128 rows x 64]
-// of a 3-D tensor map over [B, T, width] (rows past T read as zero), landing
-// 128-byte-swizzled in shared memory, where a tcgen05 descriptor can read it
-// either as a K-major operand (rows = M or N) or as an MN-major one (rows =
-// K) -- so S = q k^T, P v, dV = P^T dy, dK = dS^T q and dQ = dS k all read the
-// same tiles.  P and dS are written to shared memory in the same swizzled
-// K-major layout by the softmax threads.
+// Head size 64.  Every tile of q, k, v, dy is one TMA box [128 or 64 rows x
+// 64] of a 3-D tensor map over [B, T, width] (rows past T read as zero),
+// landing 128-byte-swizzled in shared memory, where a tcgen05 descriptor can
+// read it either as a K-major operand (rows = M or N) or as an MN-major one
+// (rows = K) -- so S = q k^T, P v, dV = P^T dy, dK = dS^T q and dQ = dS k all
+// read the same tiles.  Each kernel is warp-specialised: one thread issues
+// the TMA loads and MMAs, the other warps do the elementwise work, and every
+// hand-off is an mbarrier.
 //
-//   forward   one CTA per (128-query block, batch*head), 8 warps: S -> TMEM,
-//             row max / exp / row sum from TMEM (thread = query row), P -> smem,
-//             O_blk = P v -> TMEM, O accumulated in registers with the
-//             online-softmax rescale.  Saves lse = max + log(sum).
+//   forward   one CTA per (128-query block, b*h), 64-key sub-blocks: S -> TMEM
+//             (two buffers, issued two sub-blocks ahead), online softmax by 8
+//             warps (thread = query row), P -> smem, O_blk = P v -> TMEM, O in
+//             registers with the online-softmax rescale.  Saves lse in base 2:
+//             max*scale*log2e + log2(sum).
 //   backward  D = rowsum(dy * y); one CTA per (128-key block, b*h) for dK, dV
-//             (S^T, dP^T recomputed, dV += P^T dy, dK += dS^T q accumulated in
-//             TMEM); one CTA per (128-query block, b*h) for dQ (dQ += dS k).
+//             over 128-query sub-blocks (S^T, dP^T recomputed into TMEM; P^T
+//             and dS^T written back to TMEM and read there as the A operand
+//             of dV += P^T dy, dK += dS^T q); one CTA per (128-query block,
+//             b*h) for dQ over 64-key sub-blocks (dQ += dS k, dS in smem).
 //             No atomics: every output element is written by one CTA, so the
 //             result is deterministic.
 // All mbarrier waits are bounded (common.cuh); a wait that gives up records
@@ -75,27 +79,9 @@ static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W,
 // (rows = K, 64 columns = N) at K-step kk (16 rows)
 __device__ __forceinline__ uint64_t kmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 32, 16, 1024); }
 __device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, 8192, 1024); }
-// descriptor of a [128 rows x 128] K-major operand stored as two 64-wide atoms
-__device__ __forceinline__ uint64_t kmaj2(uint32_t buf, int kk) {
-  return sw128_desc(buf + (kk >> 2) * AT_TILE + (kk & 3) * 32, 16, 1024);
-}
-
-// Write 8 consecutive bf16 values (columns c8*8 .. c8*8+7) of row r into a
-// [128 x 128] K-major swizzled buffer (two 64-column atoms).
-__device__ __forceinline__ void st_swz8(uint8_t* buf, int r, int c8, const float* v) {
-  const int atom = c8 >> 3, chunk = (c8 & 7) ^ (r & 7);
-  uint4 u;
-  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
-  u.x = *reinterpret_cast<uint32_t*>(&t0);
-  u.y = *reinterpret_cast<uint32_t*>(&t1);
-  u.z = *reinterpret_cast<uint32_t*>(&t2);
-  u.w = *reinterpret_cast<uint32_t*>(&t3);
-  *reinterpret_cast<uint4*>(buf + atom * AT_TILE + r * 128 + chunk * 16) = u;
-}
-
-// Same as st_swz8 for a [128 x 64] buffer (one atom), given the row's base
-// pointer (buf + r*128) and its swizzle (r & 7).
+// Write 8 consecutive bf16 values (16-byte chunk c8 of a row) into a
+// 128B-swizzled [rows x 64] buffer (one atom), given the row's base pointer
+// (buf + r*128) and its swizzle (r & 7).
 __device__ __forceinline__ void st_row8(uint8_t* rowp, int rx, int c8, const float* v) {
   uint4 u;
   __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
@@ -107,50 +93,26 @@ __device__ __forceinline__ void st_row8(uint8_t* rowp, int rx, int c8, const flo
   *reinterpret_cast<uint4*>(rowp + ((c8 ^ rx) << 4)) = u;
 }
 
-// Backward elementwise step for 32 score columns of one row, from the TMEM
-// words of S (rs) and dP (rd):  p = 2^(s*sl2 - lse*log2e),  ds = p (dp - D).
-// KEYROW: the row is a key and the columns are queries (dK/dV kernel; lse
-// in natural-log units and D per column, from shared memory), else the row
-// is a query (dQ kernel; lse2r = lse*log2e and dr per row).  MASK applies
-// the causal mask and, for KEYROW, drops columns at or past colmax (only on
-// sub-blocks that cross the diagonal or the end of the sequence).
-template <bool KEYROW, bool MASK>
-__device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32_t* rd, const float* lsec,
-                                                const float* dc, float lse2r, float dr, float sl2,
-                                                int col0, int rowpos, uint8_t* prow, uint8_t* srow,
-                                                int rx, int c8base, int colmax = 0) {
+// The dQ kernel's elementwise step for 32 key columns of one query row,
+// from the TMEM words of S (rs) and dP (rd): p = 2^(s*sl2 - lse2), ds =
+// p (dp - D), with the row's lse2 (base-2 units, as the forward saves it)
+// and D; dS (bf16) goes to the row's 16-byte chunks c8base.. of a
+// 128B-swizzled [rows x 64] atom (srow = atom + r*128, rx = r & 7).  MASK
+// applies the causal mask (only on sub-blocks that cross the diagonal).
+template <bool MASK>
+__device__ __forceinline__ void qrow_elementwise(const uint32_t* rs, const uint32_t* rd, float lse2r, float dr,
+                                                 float sl2, int col0, int rowpos, uint8_t* srow, int rx,
+                                                 int c8base) {
 #pragma unroll
   for (int g = 0; g < 4; g++) {
-    float lv[8], dv[8];
-    if (KEYROW) {
-      const float4 a = *reinterpret_cast<const float4*>(lsec + g * 8);
-      const float4 b = *reinterpret_cast<const float4*>(lsec + g * 8 + 4);
-      const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
-      const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
-      const float L2E = 1.4426950408889634f;
-      lv[0] = a.x * L2E; lv[1] = a.y * L2E; lv[2] = a.z * L2E; lv[3] = a.w * L2E;
-      lv[4] = b.x * L2E; lv[5] = b.y * L2E; lv[6] = b.z * L2E; lv[7] = b.w * L2E;
-      dv[0] = c.x; dv[1] = c.y; dv[2] = c.z; dv[3] = c.w; dv[4] = d.x; dv[5] = d.y; dv[6] = d.z; dv[7] = d.w;
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; j++) { lv[j] = lse2r; dv[j] = dr; }
-    }
-    float p[8], ds[8];
+    float ds[8];
 #pragma unroll
     for (int j = 0; j < 8; j++) {
-      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
-      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
-      float pk = pv;
-      if (MASK) {  // a masked column may hold stale lse / D: select, do not scale
-        const int col = col0 + g * 8 + j;
-        const bool ok = KEYROW ? (col >= rowpos && col < colmax) : col <= rowpos;
-        pk = ok ? pk : 0.f;
-        dsv = ok ? dsv : 0.f;
-      }
-      p[j] = pk;
+      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lse2r);
+      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dr);
+      if (MASK) dsv = col0 + g * 8 + j <= rowpos ? dsv : 0.f;
       ds[j] = dsv;
     }
-    if (KEYROW) st_row8(prow, rx, c8base + g, p);
     st_row8(srow, rx, c8base + g, ds);
   }
 }
@@ -158,20 +120,19 @@ __device__ __forceinline__ void bwd_elementwise(const uint32_t* rs, const uint32
 // The dK/dV kernel's elementwise step for 32 query columns of one key row,
 // kept in registers: P^T and dS^T as packed bf16 pairs (pk, dk: 16 words
 // each, column pairs in order), so they can be computed before the shared-
-// memory buffer they go to is free.  Same arithmetic as bwd_elementwise
-// with KEYROW (lse in natural-log units, D per column from shared memory).
+// memory buffer they go to is free.  lse2c: the columns' lse in base-2
+// units (as the forward saves it), dc: their D, both from shared memory.
 template <bool MASK>
-__device__ __forceinline__ void keyrow_pack(const uint32_t* rs, const uint32_t* rd, const float* lsec,
+__device__ __forceinline__ void keyrow_pack(const uint32_t* rs, const uint32_t* rd, const float* lse2c,
                                             const float* dc, float sl2, int col0, int key, int colmax,
                                             uint32_t* pk, uint32_t* dk) {
-  const float L2E = 1.4426950408889634f;
 #pragma unroll
   for (int g = 0; g < 4; g++) {
-    const float4 a = *reinterpret_cast<const float4*>(lsec + g * 8);
-    const float4 bq = *reinterpret_cast<const float4*>(lsec + g * 8 + 4);
+    const float4 a = *reinterpret_cast<const float4*>(lse2c + g * 8);
+    const float4 bq = *reinterpret_cast<const float4*>(lse2c + g * 8 + 4);
     const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
     const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
-    const float lv[8] = {a.x * L2E, a.y * L2E, a.z * L2E, a.w * L2E, bq.x * L2E, bq.y * L2E, bq.z * L2E, bq.w * L2E};
+    const float lv[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
     const float dv[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
     float p[8], ds[8];
 #pragma unroll
@@ -197,30 +158,6 @@ __device__ __forceinline__ void keyrow_pack(const uint32_t* rs, const uint32_t* 
     }
   }
 }
-// Write 16 packed words (32 bf16 columns, 16-byte chunks c8base..c8base+3)
-// into a row of a [rows x 64] 128B-swizzled atom (rowp = atom + r*128).
-__device__ __forceinline__ void store_packed32(uint8_t* rowp, int rx, int c8base, const uint32_t* w) {
-#pragma unroll
-  for (int g = 0; g < 4; g++)
-    *reinterpret_cast<uint4*>(rowp + (((c8base + g) ^ rx) << 4)) = make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]);
-}
-
-__device__ __forceinline__ void store_row64_bf16(bf16* dst, const float* v, float mul) {
-#pragma unroll
-  for (int i = 0; i < 64; i += 8) {
-    uint4 u;
-    __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i] * mul, v[i + 1] * mul);
-    __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2] * mul, v[i + 3] * mul);
-    __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4] * mul, v[i + 5] * mul);
-    __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6] * mul, v[i + 7] * mul);
-    u.x = *reinterpret_cast<uint32_t*>(&t0);
-    u.y = *reinterpret_cast<uint32_t*>(&t1);
-    u.z = *reinterpret_cast<uint32_t*>(&t2);
-    u.w = *reinterpret_cast<uint32_t*>(&t3);
-    *reinterpret_cast<uint4*>(dst + i) = u;
-  }
-}
-
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
 }
@@ -488,7 +425,7 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
     const float l = red[row] + red[128 + row];
     if (q < T) {
       store_row32_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS + half * 32, o, 1.f / l);
-      if (half == 0) lse[(int64_t)bh * T + q] = m * scale + logf(l);
+      if (half == 0) lse[(int64_t)bh * T + q] = m * sl2 + log2f(l);  // base-2 units
     }
   }
   tc_fence_before();
@@ -539,7 +476,7 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 //               read from TMEM (the A operand), dy and q from shared memory
 //   warps 0..15 compute: copy S^T(j), dP^T(j) to registers at once (so
 //               S^T(j+1) runs during their elementwise work), then P^T =
-//               2^(S^T*scale*log2e - lse*log2e), dS^T = P^T (dP^T - D) as
+//               2^(S^T*scale*log2e - lse2), dS^T = P^T (dP^T - D) as
 //               packed bf16 into TMEM (warps w, w+4, w+8, w+12 share TMEM
 //               lane quarter w%4 and take 32 of the 128 query columns each;
 //               the math runs before the buffer wait, so it overlaps
@@ -903,7 +840,7 @@ __global__ void __launch_bounds__(AQ_THREADS, 2)
     const int row = quarter * 32 + lane, q = q0 + row;
     const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
     const float sl2 = scale * 1.4426950408889634f;
-    const float my_lse = q < T ? lse[(int64_t)bh * T + q] * 1.4426950408889634f : INFINITY;
+    const float my_lse = q < T ? lse[(int64_t)bh * T + q] : INFINITY;  // base 2
     const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
     for (int j = 0; j < nsub; j++) {
       const int k0 = j * AB_SUB;
@@ -919,11 +856,9 @@ __global__ void __launch_bounds__(AQ_THREADS, 2)
       mbar_wait(&p_empty[j & 1], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);  // dQ(j-2) has read the buffer
       uint8_t* srow = sS + (j & 1) * AT_TILE + row * 128;
       if (k0 + AB_SUB > q0)
-        bwd_elementwise<false, true>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
-                                     nullptr, srow, row & 7, half * 4);
+        qrow_elementwise<true>(rs, rd, my_lse, my_d, sl2, k0 + half * 32, q, srow, row & 7, half * 4);
       else
-        bwd_elementwise<false, false>(rs, rd, nullptr, nullptr, my_lse, my_d, sl2, k0 + half * 32, q,
-                                      nullptr, srow, row & 7, half * 4);
+        qrow_elementwise<false>(rs, rd, my_lse, my_d, sl2, k0 + half * 32, q, srow, row & 7, half * 4);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j & 1]);

@@ -97,11 +97,11 @@ int64_t ln_partial_floats(int N, int C);
 
 // ---------------------------------------------------------------- column sums
 // db[j] += sum_i x[i*ld + j], i < M, j < N.  partial: float [colsum_partial_floats]
-// db[n] += sum over r < rows of partial[r * N + n], rows in order
-void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N);
 template <typename T>
 void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial);
 int64_t colsum_partial_floats(int M, int N);
+// db[n] += sum over r < rows of partial[r * N + n], rows in order
+void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N);
 
 // ---------------------------------------------------------------- softmax + CE
 // Per row i < M of logits [M, Vp]: loss_i = logsumexp(l[0:V]) - l[target];
@@ -151,8 +151,11 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g);
 bool gemm_bf16_init();  // resolves the driver's tensor-map encoder; false on failure
 
 // ---------------------------------------------------------------- attention
-// qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T] (natural-log logsumexp of the
-// scaled, masked scores of each query row).
+// qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T]: the logsumexp of the scaled,
+// masked scores of each query row, in natural-log units on the CUDA-core
+// path (launch_attention_*_simt) and in base-2 units (log2 of the row's sum
+// of 2^(score*scale*log2 e)) on the tensor-core path (*_bf16 with head size
+// 64); each backward reads what its own forward wrote.
 template <typename T>
 void launch_attention_fwd_simt(LaunchCtx& c, T* y, float* lse, const T* qkv, int B, int T_,
                                int C, int NH);
