@@ -73,6 +73,12 @@ __device__ __forceinline__ float tanh_hw(float x) {
 __device__ __forceinline__ float gelu_hw(float x) {
   return 0.5f * x * (1.f + tanh_hw(GELU_S * (x + GELU_A * x * x * x)));
 }
+// gelu(x) and gelu'(x) from one tanh.approx
+__device__ __forceinline__ void gelu_and_grad_hw(float x, float& g, float& gd) {
+  const float th = tanh_hw(GELU_S * (x + GELU_A * x * x * x));
+  g = 0.5f * x * (1.f + th);
+  gd = 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * GELU_S * (1.f + 3.f * GELU_A * x * x);
+}
 __device__ __forceinline__ float gelu_grad_hw(float x) {
   const float th = tanh_hw(GELU_S * (x + GELU_A * x * x * x));
   return 0.5f * (1.f + th) + 0.5f * x * (1.f - th * th) * GELU_S * (1.f + 3.f * GELU_A * x * x);

@@ -100,7 +100,7 @@ struct gpt2_model {
   // activations (act = bf16 or fp32 per mode; residual stream fp32)
   std::vector<float*> res;  // L+1 residual streams [M,C]; res[0] = encoder output
   std::vector<float*> mid;  // L after-attention residuals [M,C]
-  char *ln1, *qkv, *atty, *ln2, *fch, *fcg, *lnf, *logits;
+  char *ln1, *qkv, *atty, *ln2, *fcd, *fcg, *lnf, *logits;
   float *ln1_mean, *ln1_rstd, *ln2_mean, *ln2_rstd, *lse, *lnf_mean, *lnf_rstd;
   float *losses, *loss;
   // backward scratch
@@ -236,7 +236,7 @@ size_t layout(gpt2_model* m, char* base) {
   m->qkv = b.take<char>(L * M * 3 * C * a);
   m->atty = b.take<char>(L * M * C * a);
   m->ln2 = b.take<char>(L * M * C * a);
-  m->fch = b.take<char>(L * M * 4 * C * a);
+  m->fcd = b.take<char>(L * M * 4 * C * a);
   m->fcg = b.take<char>(L * M * 4 * C * a);
   m->lnf = b.take<char>(M * C * a);
   m->logits = b.take<char>(M * (int64_t)m->Vp * a);
@@ -308,7 +308,7 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
     ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
     ActT* atty = m->A<ActT>(m->atty, l, (int64_t)M * C);
     ActT* ln2 = m->A<ActT>(m->ln2, l, (int64_t)M * C);
-    ActT* fch = m->A<ActT>(m->fch, l, (int64_t)M * 4 * C);
+    ActT* fcd = m->A<ActT>(m->fcd, l, (int64_t)M * 4 * C);
     ActT* fcg = m->A<ActT>(m->fcg, l, (int64_t)M * 4 * C);
     float* lse = m->lse + (int64_t)l * B * NH * T;
     {
@@ -335,8 +335,9 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
       launch_layernorm_fwd<ActT>(c, ln2, m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
                                  m->mid[l], m->P(LN2W) + l * C, m->P(LN2B) + l * C, M, C);
     }
-    g = gemm(M, 4 * C, C, ln2, C, true, w(FCW, (int64_t)l * 4 * C * C), C, true, EPI_BIAS_GELU,
-             fch, 4 * C, f32);
+    // fc: x = ln2 Wfc^T + b; fcg = gelu(x), and fcd = gelu'(x) for the backward
+    g = gemm(M, 4 * C, C, ln2, C, true, w(FCW, (int64_t)l * 4 * C * C), C, true, EPI_GELU_FWD,
+             fcd, 4 * C, f32);
     g.bias = m->P(FCB) + (int64_t)l * 4 * C;
     g.out2 = fcg;
     run_gemm(m, c, g, GS_FC);
@@ -393,20 +394,20 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
     ActT* atty = m->A<ActT>(m->atty, l, (int64_t)M * C);
     ActT* ln2 = m->A<ActT>(m->ln2, l, (int64_t)M * C);
-    ActT* fch = m->A<ActT>(m->fch, l, (int64_t)M * 4 * C);
+    ActT* fcd = m->A<ActT>(m->fcd, l, (int64_t)M * 4 * C);
     ActT* fcg = m->A<ActT>(m->fcg, l, (int64_t)M * 4 * C);
     float* lse = m->lse + (int64_t)l * B * NH * T;
     // fcproj: res[l+1] = mid + fcg Wfcproj^T + b
     GemmArgs g = gemm(M, 4 * C, C, dres_act, C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C,
-                      false, EPI_GELU_BWD, dbig, 4 * C, f32);
-    g.aux = fch;
+                      false, EPI_MUL_AUX, dbig, 4 * C, f32);
+    g.aux = fcd;  // d(fc pre-activation) = d(fcg) * gelu'(x)
     if (!f32) g.colsum_out = m->cs_partial;  // fc bias gradient partials, 32 rows each
     run_gemm(m, c, g, GS_FCPROJ);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
                         m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true), GS_FCPROJ);
     // fcproj bias gradient: column sums of dres, taken by the LayerNorm
     // backward that produced dres (LN_f or the next block's LN1)
-    // fc: fch = ln2 Wfc^T + b
+    // fc: x = ln2 Wfc^T + b
     run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
                         EPI_STORE, m->dln, C, true), GS_FC);
     run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,

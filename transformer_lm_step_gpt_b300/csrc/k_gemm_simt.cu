@@ -78,13 +78,13 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
       float v = acc[i][j];
       switch (g.epi) {
         case EPI_STORE: out[o] = epi_apply(g, m, n, v); break;
-        case EPI_BIAS_GELU: {
+        case EPI_GELU_FWD: {
           v = epi_apply(g, m, n, v);
-          out[o] = v;
+          out[o] = gelu_grad_f(v);
           static_cast<float*>(g.out2)[o] = gelu_f(v);
         } break;
         case EPI_RESIDUAL: out[o] = static_cast<const float*>(g.aux)[o] + epi_apply(g, m, n, v); break;
-        case EPI_GELU_BWD: out[o] = v * gelu_grad_f(static_cast<const float*>(g.aux)[o]); break;
+        case EPI_MUL_AUX: out[o] = v * static_cast<const float*>(g.aux)[o]; break;
         case EPI_ACCUM: out[o] += v; break;
       }
     }

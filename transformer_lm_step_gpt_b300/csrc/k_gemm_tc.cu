@@ -20,7 +20,7 @@
 //               TMEM lane quarter (w % 4: 32 rows) and column half
 //               ((w-2)/4), 32-row x 128-byte chunks at a time.  Every global
 //               byte of the epilogue moves by TMA: the chunk's auxiliary
-//               input (residual stream, pre-GELU activation) is TMA-loaded
+//               input (residual stream, GELU derivative) is TMA-loaded
 //               into a 128B-swizzled staging buffer, each thread (one row)
 //               applies the fused epilogue from registers, writes the result
 //               back into the staging buffer and one lane TMA-stores it (or
@@ -227,11 +227,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       for (int c = 0; c < 8; c++) {
         uint8_t* p = stg + stg_off(lane, c);
         float o[8];
-        if (has_aux) {  // EPI_GELU_BWD: out = acc * gelu'(pre-activation)
+        if (has_aux) {  // EPI_MUL_AUX: out = acc * aux
           float hv[8];
           get8_bf16(p, hv);
 #pragma unroll
-          for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * gelu_grad_hw(hv[q]);
+          for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * hv[q];
+        } else if (epi == EPI_GELU_FWD && !split) {  // out = gelu'(x); v keeps gelu(x) for out2
+#pragma unroll
+          for (int q = 0; q < 8; q++) gelu_and_grad_hw(v[8 * c + q], v[8 * c + q], o[q]);
         } else {
 #pragma unroll
           for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
@@ -263,14 +266,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       if (mrow < g.M && n < g.N)
         *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);
     }
-    if (epi == EPI_BIAS_GELU && !split) {  // second output: gelu(pre-activation)
+    if (epi == EPI_GELU_FWD && !split) {  // second output: gelu(x), already in v
       if (lane == 0) bulk_wait_read0();
       __syncwarp();
 #pragma unroll
       for (int c = 0; c < 8; c++) {
         float o[8];
 #pragma unroll
-        for (int q = 0; q < 8; q++) o[q] = gelu_hw(v[8 * c + q]);
+        for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
         put8_bf16(stg + stg_off(lane, c), o);
       }
       fence_proxy_async_smem();
@@ -291,9 +294,112 @@ __device__ __forceinline__ EpiFlags epi_flags(const GemmArgs& g, int splits) {
   const int epi = g.epi;
   f.split = splits > 1;
   f.f32 = f.split || epi == EPI_RESIDUAL || epi == EPI_ACCUM || (epi == EPI_STORE && g.out_f32);
-  f.has_aux = !f.split && (epi == EPI_RESIDUAL || epi == EPI_GELU_BWD);
-  f.use_bias = !f.split && g.bias && (epi == EPI_STORE || epi == EPI_BIAS_GELU || epi == EPI_RESIDUAL);
+  f.has_aux = !f.split && (epi == EPI_RESIDUAL || epi == EPI_MUL_AUX);
+  f.use_bias = !f.split && g.bias && (epi == EPI_STORE || epi == EPI_GELU_FWD || epi == EPI_RESIDUAL);
   return f;
+}
+
+// Epilogue of a tile whose result combines the accumulator with an
+// auxiliary input tile of the same shape (EPI_RESIDUAL: fp32 residual
+// stream; EPI_MUL_AUX: bf16 gelu'), with the aux tiles fetched
+// ahead: the warp owns two staging buffers used by alternate chunks; the
+// caller issues chunk 0's aux load into buffer 0 before it waits for the
+// accumulator, and chunk c+1's load goes into the other buffer while chunk
+// c is processed.  The result overwrites the aux tile in place and is
+// TMA-stored from there.  aph: phase bits of the two aux barriers.
+template <int BN>
+__device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMaps& em, uint8_t* stg2,
+                                                  uint64_t* abar2, uint32_t& aph, uint32_t taddr0,
+                                                  int half, int lane, int mrow, int n0, bool f32,
+                                                  bool use_bias, float4 bq, int* err) {
+  const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
+  const int nch = (BN / 2) / CW;
+#pragma unroll 1
+  for (int c = 0; c < nch; c++) {
+    const int cc = half * (BN / 2) + c * CW;
+    const int ncol = n0 + cc;
+    if (ncol >= g.N) break;
+    uint8_t* stg = stg2 + (c & 1) * STG_BYTES;
+    if (c + 1 < nch && ncol + CW < g.N) {
+      if (lane == 0) bulk_wait_read0();  // the other buffer's last store has read it
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&abar2[(c + 1) & 1], STG_BYTES);
+        tma_load_2d(stg2 + ((c + 1) & 1) * STG_BYTES, &em.aux, &abar2[(c + 1) & 1], ncol + CW, mrow);
+      }
+    }
+    float v[64];
+    const uint32_t taddr = taddr0 + (uint32_t)cc;
+    {
+      uint32_t r[32];
+      tmem_ld32(taddr, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; j++) v[j] = __uint_as_float(r[j]);
+      if (!f32) {
+        tmem_ld32(taddr + 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; j++) v[32 + j] = __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int j = 32; j < 64; j++) v[j] = 0.f;
+      }
+    }
+    if (use_bias) {
+      const int lb = (cc - half * (BN / 2)) >> 2;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        if (j < CW) {
+          const int src = lb + (j >> 2);
+          v[j] += __shfl_sync(0xffffffffu, bq.x, src);
+          v[j + 1] += __shfl_sync(0xffffffffu, bq.y, src);
+          v[j + 2] += __shfl_sync(0xffffffffu, bq.z, src);
+          v[j + 3] += __shfl_sync(0xffffffffu, bq.w, src);
+        }
+      }
+    }
+    mbar_wait(&abar2[c & 1], (aph >> (c & 1)) & 1u, err);
+    aph ^= 1u << (c & 1);
+    if (f32) {  // EPI_RESIDUAL: out = residual + (acc + bias)
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        float4* pp = reinterpret_cast<float4*>(stg + stg_off(lane, q));
+        const float4 r = *pp;
+        *pp = make_float4(r.x + v[4 * q], r.y + v[4 * q + 1], r.z + v[4 * q + 2], r.w + v[4 * q + 3]);
+      }
+    } else {  // EPI_MUL_AUX: out = acc * aux
+#pragma unroll
+      for (int q = 0; q < 8; q++) {
+        uint8_t* pp = stg + stg_off(lane, q);
+        float hv[8], o[8];
+        get8_bf16(pp, hv);
+#pragma unroll
+        for (int k = 0; k < 8; k++) o[k] = v[8 * q + k] * hv[k];
+        put8_bf16(pp, o);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&em.out, stg, ncol, mrow);
+      bulk_commit();
+    }
+    if (g.colsum_out && !f32) {
+      float s0 = 0.f, s1 = 0.f;
+      const int ch = lane >> 2, wo = (lane & 3) * 4;
+#pragma unroll 8
+      for (int r = 0; r < 32; r++) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(stg + r * 128 + ((ch ^ (r & 7)) << 4) + wo);
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+        s0 += f.x;
+        s1 += f.y;
+      }
+      const int n = ncol + 2 * lane;
+      if (mrow < g.M && n < g.N)
+        *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);
+    }
+  }
 }
 
 template <int BN, bool A_K, bool B_K>
@@ -440,21 +546,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // 128 accumulator lanes with the epilogue above.
 #define PAIR_BN 256
 #define GROUP_PAIRS 4
-struct PairCfg {
-  static constexpr int STAGES = 6;
+// AUX: the epilogue reads an aux tile (EPI_RESIDUAL, EPI_MUL_AUX) and gets
+// two staging buffers per warp to fetch it ahead, for one operand stage.
+template <bool AUX>
+struct PairCfgT {
+  static constexpr int STAGES = AUX ? 5 : 6;
   static constexpr uint32_t A_BYTES = TC_BM * TC_BK * 2;            // 128 rows of A
   static constexpr uint32_t B_BYTES = (PAIR_BN / 2) * TC_BK * 2;     // 128 rows of B
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr size_t STAGING = (size_t)EPI_WARPS * STG_BYTES;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING + 1024 + 256;
+  static constexpr size_t STAGING = (size_t)EPI_WARPS * STG_BYTES * (AUX ? 2 : 1);
+  // + 1024 alignment slack + 512 for the barriers (up to 32) and the TMEM slot
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING + 1024 + 512;
 };
 
-template <bool A_K, bool B_K>
+template <bool A_K, bool B_K, bool AUX>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
                         int splits, int* err) {
   pdl_trigger();
+  using PairCfg = PairCfgT<AUX>;
   constexpr int S = PairCfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -463,8 +574,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;      // [2]
   uint64_t* acc_empty = acc_full + 2;  // [2], used in the leader
-  uint64_t* aux_bar = acc_empty + 2;   // [EPI_WARPS]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + EPI_WARPS);
+  uint64_t* aux_bar = acc_empty + 2;   // [EPI_WARPS][2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(aux_bar + 2 * EPI_WARPS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -475,7 +586,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int a = 0; a < 2; a++) { mbar_init(&acc_full[a], 1); mbar_init(&acc_empty[a], 2 * EPI_WARPS); }
-    for (int w = 0; w < EPI_WARPS; w++) mbar_init(&aux_bar[w], 1);
+    for (int w = 0; w < 2 * EPI_WARPS; w++) mbar_init(&aux_bar[w], 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -566,13 +677,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int t = pair; t < total; t += npairs, ti++) {
       const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
       const int a = ti & 1;
-      const float4 bq = load_bias4<PAIR_BN>(g, f.use_bias, tc.nt * PAIR_BN, half, lane);
-      mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
-      tc_fence_after();
-      epilogue_tile<PAIR_BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[ew], aux_phase,
-                             tmem + (uint32_t)(a * PAIR_BN) + ((uint32_t)(quarter * 32) << 16), half,
-                             lane, (2 * tc.mt + (int)rank) * TC_BM + quarter * 32, tc.nt * PAIR_BN,
-                             tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err);
+      const int mrow = (2 * tc.mt + (int)rank) * TC_BM + quarter * 32, n0 = tc.nt * PAIR_BN;
+      const uint32_t taddr = tmem + (uint32_t)(a * PAIR_BN) + ((uint32_t)(quarter * 32) << 16);
+      if (AUX) {
+        // chunk 0's aux tile, fetched while this tile's MMAs still run
+        uint8_t* stg2 = staging + (size_t)ew * 2 * STG_BYTES;
+        const int ncol0 = n0 + half * (PAIR_BN / 2);
+        if (lane == 0) bulk_wait_read0();
+        __syncwarp();
+        if (lane == 0 && ncol0 < g.N) {
+          mbar_arrive_expect_tx(&aux_bar[2 * ew], STG_BYTES);
+          tma_load_2d(stg2, &em.aux, &aux_bar[2 * ew], ncol0, mrow);
+        }
+        const float4 bq = load_bias4<PAIR_BN>(g, f.use_bias, n0, half, lane);
+        mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
+        tc_fence_after();
+        epilogue_tile_aux<PAIR_BN>(g, em, stg2, &aux_bar[2 * ew], aux_phase, taddr, half, lane, mrow, n0,
+                                   f.f32, f.use_bias, bq, err);
+      } else {
+        const float4 bq = load_bias4<PAIR_BN>(g, f.use_bias, n0, half, lane);
+        mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
+        tc_fence_after();
+        epilogue_tile<PAIR_BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[2 * ew], aux_phase, taddr,
+                               half, lane, mrow, n0, tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(cluster_addr(&acc_empty[a], 0));
@@ -628,9 +756,9 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   } else {
     const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
     ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
-    if (g.epi == EPI_BIAS_GELU) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_GELU_FWD) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
     if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
-    if (g.epi == EPI_GELU_BWD) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_MUL_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
   }
   if (!ok) {
     fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
@@ -649,7 +777,7 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   }
 }
 
-template <bool A_K, bool B_K>
+template <bool A_K, bool B_K, bool AUX>
 static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* partial) {
   CUtensorMap ta, tb;
   EpiMaps em;
@@ -667,17 +795,17 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
   } else {
     const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
     ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
-    if (g.epi == EPI_BIAS_GELU) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_GELU_FWD) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
     if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
-    if (g.epi == EPI_GELU_BWD) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_MUL_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
   }
   if (!ok) {
     fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
     c.host_fail = 1;
     return;
   }
-  using Cfg = PairCfg;
-  auto kern = gemm_tc_pair_kernel<A_K, B_K>;
+  using Cfg = PairCfgT<AUX>;
+  auto kern = gemm_tc_pair_kernel<A_K, B_K, AUX>;
   static int max_pairs = 0;  // co-resident clusters of two, per instantiation
   if (max_pairs == 0) {
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
@@ -731,10 +859,15 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
     g_pair_mode = (e && e[0] == '0') ? 0 : 1;
   }
   if (BN == 256 && g_pair_mode) {
-    if (g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true>(c, g, splits, partial);
-    else if (g.a_kmajor && !g.b_kmajor) launch_tc_pair<true, false>(c, g, splits, partial);
-    else if (!g.a_kmajor && g.b_kmajor) launch_tc_pair<false, true>(c, g, splits, partial);
-    else launch_tc_pair<false, false>(c, g, splits, partial);
+    // epilogues that read an aux tile use the prefetching variant; the model's
+    // aux GEMMs (attproj / fcproj forward, fcproj dgrad) are A K-major
+    const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX);
+    if (aux && g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, true>(c, g, splits, partial);
+    else if (aux && g.a_kmajor) launch_tc_pair<true, false, true>(c, g, splits, partial);
+    else if (g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, false>(c, g, splits, partial);
+    else if (g.a_kmajor && !g.b_kmajor) launch_tc_pair<true, false, false>(c, g, splits, partial);
+    else if (!g.a_kmajor && g.b_kmajor) launch_tc_pair<false, true, false>(c, g, splits, partial);
+    else launch_tc_pair<false, false, false>(c, g, splits, partial);
   } else if (BN == 256) { TC_DISPATCH(256) } else { TC_DISPATCH(128) }
 #undef TC_DISPATCH
 }

@@ -123,9 +123,9 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
 //   B(n,k) = B[n*ldb + k] (b_kmajor) or B[k*ldb + n] (N-major)
 enum GemmEpi {
   EPI_STORE = 0,     // out = acc (+ bias)                          out: act or f32
-  EPI_BIAS_GELU,     // out = acc + bias (pre-activation), out2 = gelu(out)  both act
+  EPI_GELU_FWD,      // x = acc + bias: out = gelu'(x), out2 = gelu(x)       both act
   EPI_RESIDUAL,      // out(f32) = aux(f32) + acc + bias
-  EPI_GELU_BWD,      // out(act) = acc * gelu'(aux(act))
+  EPI_MUL_AUX,       // out(act) = acc * aux(act)  (the GELU backward with aux = gelu')
   EPI_ACCUM,         // out(f32) += acc
 };
 struct GemmArgs {
@@ -135,11 +135,11 @@ struct GemmArgs {
   int epi;
   void* out; int64_t ldo; bool out_f32;
   const float* bias;  // [N] or null
-  void* out2;         // EPI_BIAS_GELU
-  const void* aux;    // EPI_RESIDUAL (f32, ldo) / EPI_GELU_BWD (act, ldo)
+  void* out2;         // EPI_GELU_FWD
+  const void* aux;    // EPI_RESIDUAL (f32, ldo) / EPI_MUL_AUX (act, ldo)
   float* splitk_scratch;  // EPI_ACCUM with split-K (tensor-core path)
   int64_t splitk_scratch_floats;
-  // EPI_GELU_BWD on the tensor-core path: if set, also the column sums of
+  // EPI_MUL_AUX on the tensor-core path: if set, also the column sums of
   // the stored (bf16) output over each 32-row block, [ceil(M/32)][N] floats
   // (launch_colsum_reduce adds them up)
   float* colsum_out;
