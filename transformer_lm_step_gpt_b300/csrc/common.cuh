@@ -321,6 +321,37 @@ __host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, bool a_mn, bo
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------ cross-CTA flags
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// order this thread's generic-proxy accesses against its async-proxy (TMA)
+// accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *p == want (another CTA's release); records a timeout
+// and gives up like mbar_wait.
+__device__ __forceinline__ bool flag_wait(const int* p, int want, int* err) {
+  if (ld_acquire_gpu(p) == want) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0;; i++) {
+    if (ld_acquire_gpu(p) == want) return true;
+    if ((i & 63u) == 63u) {
+      if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
+      if (global_ns() - t0 > GPT2_WAIT_LIMIT_NS) {
+        record_error(err, DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------ CTA pairs
 // A cluster of two CTAs on the two SMs of a TPC drives one M=256 MMA
 // (tcgen05 cta_group::2): each CTA holds half of A (its 128 rows), half of

@@ -110,6 +110,8 @@ struct gpt2_model {
   char *dbig, *datty;
   float *dsum, *ln_partial, *cs_partial, *splitk;
   int64_t splitk_floats;
+  int* splitk_flags;  // turnstiles of the in-kernel split-K reduction
+  int64_t splitk_flag_count;
   uint32_t* enc_sorted;
   float* enc_partial;
   int* err;
@@ -201,6 +203,8 @@ int check_device(gpt2_model* m, const char* where) {
   if (e != cudaSuccess) return cuda_fail(m, e, where);
   if (w) {
     cudaMemset(m->err, 0, sizeof(int));
+    // a launch that gave up may have left split-K turnstiles set
+    if (m->splitk_flag_count) cudaMemset(m->splitk_flags, 0, sizeof(int) * m->splitk_flag_count);
     if (w & DEVERR_TIMEOUT) return fail(m, GPT2_ERR_TIMEOUT, std::string(where) + ": a bounded device wait expired");
     if (w & DEVERR_TOKEN) return fail(m, GPT2_ERR_TOKEN, std::string(where) + ": token or target id outside [0, V)");
   }
@@ -260,6 +264,8 @@ size_t layout(gpt2_model* m, char* base) {
                                                   (int64_t)((m->M + 31) / 32) * 4 * m->C));
   m->splitk_floats = m->bf ? 16 * C * C : 0;
   m->splitk = b.take<float>(m->splitk_floats);
+  m->splitk_flag_count = m->bf ? 8192 : 0;
+  m->splitk_flags = b.take<int>(m->splitk_flag_count);
   m->enc_sorted = b.take<uint32_t>(M);
   m->enc_partial = b.take<float>(M * C);
   m->err = b.take<int>(1);
@@ -283,6 +289,8 @@ void run_gemm(gpt2_model* m, LaunchCtx& c, GemmArgs g, int site) {
   if (m->bf) {
     g.splitk_scratch = m->splitk;
     g.splitk_scratch_floats = m->splitk_floats;
+    g.splitk_flags = m->splitk_flags;
+    g.splitk_flag_count = m->splitk_flag_count;
     launch_gemm_bf16(c, g);
   } else {
     launch_gemm_f32(c, g);
@@ -551,6 +559,7 @@ int gpt2_build(const gpt2_config* cfg, uint64_t seed, gpt2_model** out) {
   cudaMemset(m->adam_m, 0, sizeof(float) * m->n_params);
   cudaMemset(m->adam_v, 0, sizeof(float) * m->n_params);
   cudaMemset(m->err, 0, sizeof(int));
+  if (m->splitk_flag_count) cudaMemset(m->splitk_flags, 0, sizeof(int) * m->splitk_flag_count);
   LaunchCtx c = ctx(m);
   InitSpec s;
   for (int t = 0; t <= NT; t++) s.off[t] = m->off[t];

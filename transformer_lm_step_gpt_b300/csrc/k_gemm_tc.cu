@@ -75,6 +75,7 @@ static bool make_tmap(CUtensorMap* m, const void* base, bool f32, uint64_t inner
 #define TC_BM 128
 #define TC_BK 64
 #define GROUP_M 8
+#define SPLITK_SERIAL_MAX 4
 #define EPI_WARPS 8
 #define TC_THREADS (64 + 32 * EPI_WARPS)
 #define STG_BYTES 4096  // one epilogue chunk: 32 rows x 128 bytes, swizzled
@@ -162,9 +163,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
                                               uint64_t* abar, uint32_t& aux_phase, uint32_t taddr0,
                                               int half, int lane, int mrow, int n0, int split_idx,
                                               bool split, bool f32, bool has_aux, bool use_bias,
-                                              float4 bq, int* err) {
+                                              float4 bq, int* err, int* tflag = nullptr, int nsplits = 1) {
   const int epi = g.epi;
   const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
+  if (tflag) {
+    // split-K reduced in the kernel: split s of this warp's region adds its
+    // part into the output only after split s-1 has (ld.acquire of the
+    // region's flag), so the sum is formed in split order -- deterministic
+    if (lane == 0) {
+      flag_wait(tflag, split_idx, err);
+      fence_proxy_async_global();
+    }
+    __syncwarp();
+  }
 #pragma unroll 1
   for (int cc = half * (BN / 2); cc < (half + 1) * (BN / 2); cc += CW) {
     const int ncol = n0 + cc;
@@ -283,6 +294,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
         bulk_commit();
       }
     }
+  }
+  if (tflag) {  // this split's additions are complete: hand the region on
+    if (lane == 0) {
+      bulk_wait0();
+      fence_proxy_async_global();
+      st_release_gpu(tflag, split_idx + 1 == nsplits ? 0 : split_idx + 1);
+    }
+    __syncwarp();
   }
 }
 
@@ -406,7 +425,7 @@ template <int BN, bool A_K, bool B_K>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
-                   int splits, int* err) {
+                   int splits, int* flags, int* err) {
   pdl_trigger();
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
@@ -506,19 +525,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
-    const EpiFlags f = epi_flags(g, splits);
+    // flags: split-K reduced in the kernel (the epilogue then accumulates like a
+    // single split, in split order); else split s writes partial plane s
+    const EpiFlags f = epi_flags(g, flags ? 1 : splits);
     uint32_t aux_phase = 0;
     int ti = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ti++) {
       const TileCoord tc = tile_coord(t, mtiles, ntiles, GROUP_M);
       const int a = ti & 1;
+      int* tflag = flags ? flags + (int64_t)(tc.mt * ntiles + tc.nt) * EPI_WARPS + ew : nullptr;
       const float4 bq = load_bias4<BN>(g, f.use_bias, tc.nt * BN, half, lane);
       mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
       tc_fence_after();
       epilogue_tile<BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[ew], aux_phase,
                         tmem + (uint32_t)(a * BN) + ((uint32_t)(quarter * 32) << 16), half, lane,
                         tc.mt * TC_BM + quarter * 32, tc.nt * BN, tc.split, f.split, f.f32, f.has_aux,
-                        f.use_bias, bq, err);
+                        f.use_bias, bq, err, tflag, splits);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[a]);
@@ -563,7 +585,7 @@ template <bool A_K, bool B_K, bool AUX>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
-                        int splits, int* err) {
+                        int splits, int* flags, int* err) {
   pdl_trigger();
   using PairCfg = PairCfgT<AUX>;
   constexpr int S = PairCfg::STAGES;
@@ -671,12 +693,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2, quarter = warp & 3, half = ew >> 2;
-    const EpiFlags f = epi_flags(g, splits);
+    const EpiFlags f = epi_flags(g, flags ? 1 : splits);  // flags: split-K reduced in the kernel
     uint32_t aux_phase = 0;
     int ti = 0;
     for (int t = pair; t < total; t += npairs, ti++) {
       const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
       const int a = ti & 1;
+      int* tflag = flags ? flags + ((int64_t)(tc.mt * ntiles + tc.nt) * 2 + rank) * EPI_WARPS + ew : nullptr;
       const int mrow = (2 * tc.mt + (int)rank) * TC_BM + quarter * 32, n0 = tc.nt * PAIR_BN;
       const uint32_t taddr = tmem + (uint32_t)(a * PAIR_BN) + ((uint32_t)(quarter * 32) << 16);
       if (AUX) {
@@ -699,7 +722,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
         tc_fence_after();
         epilogue_tile<PAIR_BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[2 * ew], aux_phase, taddr,
-                               half, lane, mrow, n0, tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err);
+                               half, lane, mrow, n0, tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err,
+                               tflag, splits);
       }
       tc_fence_before();
       __syncwarp();
@@ -751,7 +775,12 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
   const int kps = (k_tiles + splits - 1) / splits;
   const int zs = (k_tiles + kps - 1) / kps;
-  if (zs > 1) {
+  const int64_t nflags = (int64_t)((g.M + TC_BM - 1) / TC_BM) * ((g.N + BN - 1) / BN) * EPI_WARPS;
+  // in-kernel reduction for up to SPLITK_SERIAL_MAX splits (each split waits
+  // for the previous one, ~3 us per hand-off); more splits use partial planes
+  int* flags = zs > 1 && zs <= SPLITK_SERIAL_MAX && g.splitk_flags && nflags <= g.splitk_flag_count ? g.splitk_flags
+                                                                                                       : nullptr;
+  if (zs > 1 && !flags) {
     ok = ok && make_tmap(&em.out, partial, true, g.N, g.M, g.N, 32, 32, zs);
   } else {
     const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
@@ -769,8 +798,8 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
   const int grid = std::min(tiles, c.num_sms);
   auto kern = gemm_tc_kernel<BN, A_K, B_K>;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::SMEM);
-  launch_pdl(c, kern, dim3(grid), dim3(TC_THREADS), TcCfg<BN>::SMEM, ta, tb, em, g, k_tiles, kps, zs, c.err);
-  if (zs > 1) {
+  launch_pdl(c, kern, dim3(grid), dim3(TC_THREADS), TcCfg<BN>::SMEM, ta, tb, em, g, k_tiles, kps, zs, flags, c.err);
+  if (zs > 1 && !flags) {
     const int64_t n4 = (int64_t)g.M * g.N / 4;
     int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)c.num_sms * 8);
     launch_pdl(c, splitk_reduce_kernel, dim3(blocks), dim3(256), 0, static_cast<float*>(g.out), g.ldo, partial, zs, g.M, g.N);
@@ -790,7 +819,12 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
   const int kps = (k_tiles + splits - 1) / splits;
   const int zs = (k_tiles + kps - 1) / kps;
-  if (zs > 1) {
+  const int64_t nflags = (int64_t)((g.M + 2 * TC_BM - 1) / (2 * TC_BM)) * ((g.N + PAIR_BN - 1) / PAIR_BN) * 2 * EPI_WARPS;
+  // in-kernel reduction for up to SPLITK_SERIAL_MAX splits (each split waits
+  // for the previous one, ~3 us per hand-off); more splits use partial planes
+  int* flags = zs > 1 && zs <= SPLITK_SERIAL_MAX && g.splitk_flags && nflags <= g.splitk_flag_count ? g.splitk_flags
+                                                                                                       : nullptr;
+  if (zs > 1 && !flags) {
     ok = ok && make_tmap(&em.out, partial, true, g.N, g.M, g.N, 32, 32, zs);
   } else {
     const bool f32 = g.epi == EPI_RESIDUAL || g.epi == EPI_ACCUM || (g.epi == EPI_STORE && g.out_f32);
@@ -829,8 +863,8 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
   }
   const int pair_tiles = zs * ((g.N + PAIR_BN - 1) / PAIR_BN) * ((g.M + 2 * TC_BM - 1) / (2 * TC_BM));
   const int pairs = std::min(pair_tiles, max_pairs);
-  launch_pdl_cluster(c, kern, dim3(2 * pairs), dim3(TC_THREADS), Cfg::SMEM, 2, ta, tb, em, g, k_tiles, kps, zs, c.err);
-  if (zs > 1) {
+  launch_pdl_cluster(c, kern, dim3(2 * pairs), dim3(TC_THREADS), Cfg::SMEM, 2, ta, tb, em, g, k_tiles, kps, zs, flags, c.err);
+  if (zs > 1 && !flags) {
     const int64_t n4 = (int64_t)g.M * g.N / 4;
     int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)c.num_sms * 8);
     launch_pdl(c, splitk_reduce_kernel, dim3(blocks), dim3(256), 0, static_cast<float*>(g.out), g.ldo, partial, zs, g.M, g.N);

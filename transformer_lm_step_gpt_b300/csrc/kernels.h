@@ -139,6 +139,11 @@ struct GemmArgs {
   const void* aux;    // EPI_RESIDUAL (f32, ldo) / EPI_MUL_AUX (act, ldo)
   float* splitk_scratch;  // EPI_ACCUM with split-K (tensor-core path)
   int64_t splitk_scratch_floats;
+  // split-K reduced inside the GEMM kernel, in split order, when the tile
+  // count needs no more flags than this (zero on entry, left zero on exit;
+  // else the partial planes in splitk_scratch and a reduction kernel)
+  int* splitk_flags;
+  int64_t splitk_flag_count;
   // EPI_MUL_AUX on the tensor-core path: if set, also the column sums of
   // the stored (bf16) output over each 32-row block, [ceil(M/32)][N] floats
   // (launch_colsum_reduce adds them up)
