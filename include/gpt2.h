@@ -49,6 +49,8 @@ extern "C" {
 #define GPT2_ERR_TOKEN (-5)     /* a token or target id outside [0, V)            */
 #define GPT2_ERR_TIMEOUT (-6)   /* a bounded device-side wait expired             */
 #define GPT2_ERR_NONFINITE (-7) /* the loss is NaN or infinite                    */
+#define GPT2_ERR_IO (-8)        /* a checkpoint or token file could not be read,
+                                   written, or is truncated                      */
 
 /* Arithmetic of the step.
  *   GPT2_FP32: every product and sum in fp32 (SIMT FFMA; no TF32, no bf16).
@@ -198,6 +200,52 @@ GPT2_API int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* host_ds
  * Synchronises; reports device-side errors like gpt2_synchronize and
  * GPT2_ERR_NONFINITE for a NaN/Inf loss. */
 GPT2_API int gpt2_read_loss(gpt2_model* m, float* host_loss);
+
+/* ---------------------------------------------------------------- checkpoints
+ * Training state saved and resumed as one flat file: InfoQ's account of
+ * llm.c loads its model as a checkpoint file of fp32 weights in one block;
+ * femtoGPT resumes training from its saved state.  The page gives no
+ * layout; this one is:
+ *   64 little-endian int32 header words: [0] magic 0x43545047 ("GPTC"),
+ *   [1] version 1, [2] header words (64), [3..11] max_seq_len, vocab_size,
+ *   padded_vocab_size, num_layers, num_heads, channels, batch_size, seq_len,
+ *   precision of the saving model, [12] the step t, [13], [14] the number of
+ *   fp32 parameters (low, high 32 bits), [15] the arenas that follow (3:
+ *   params, AdamW m, AdamW v); the rest 0;
+ *   then each arena as n_params fp32 values, in gpt2_tensor_info's order.
+ * gpt2_save_checkpoint synchronises the model's stream and writes the file
+ * (step >= 0 is stored as given).  gpt2_load_checkpoint needs a file whose
+ * max_seq_len, vocab_size, padded_vocab_size, num_layers, num_heads,
+ * channels and parameter count match the model (batch shape and precision
+ * may differ); it replaces params, m and v, refreshes the bf16 weight copy,
+ * zeroes the gradients, requires a new forward before the next backward, and
+ * returns the saved step in *step (may be NULL).  Errors: GPT2_ERR_ARG (NULL
+ * model or path, step < 0, a header that does not match), GPT2_ERR_IO
+ * (open / read / write failure, short file), GPT2_ERR_CUDA; a header or
+ * length check that fails leaves the model unchanged. */
+GPT2_API int gpt2_save_checkpoint(gpt2_model* m, const char* path, int32_t step);
+GPT2_API int gpt2_load_checkpoint(gpt2_model* m, const char* path, int32_t* step);
+
+/* ---------------------------------------------------------------- token files
+ * InfoQ's account of llm.c: the data-preparation scripts write each split
+ * as a .bin file holding the raw bytes of int32 GPT-2 token ids.  A
+ * gpt2_tokens reads such a file into host memory once and serves
+ * next-token batches from a cursor: gpt2_tokens_next_batch copies
+ * tokens[i] = s[p + i] and targets[i] = s[p + i + 1] for i < B*T (row-major
+ * [B, T] host buffers owned by the caller) and advances p by B*T; a batch
+ * that would read past the end starts over at p = 0.  The ids are not
+ * range-checked here (gpt2_forward reports ids outside [0, V) as
+ * GPT2_ERR_TOKEN).  Errors (message in gpt2_last_error(NULL)):
+ * GPT2_ERR_ARG (NULL arguments, B or T < 1, a file whose size is not a
+ * multiple of 4, or fewer than B*T+1 tokens), GPT2_ERR_IO (cannot read the
+ * file), GPT2_ERR_OOM. */
+typedef struct gpt2_tokens gpt2_tokens;
+GPT2_API int gpt2_tokens_open(const char* path, gpt2_tokens** out);
+GPT2_API int gpt2_tokens_count(const gpt2_tokens* d, int64_t* n);
+GPT2_API int gpt2_tokens_next_batch(gpt2_tokens* d, int32_t B, int32_t T, int32_t* tokens,
+                                    int32_t* targets);
+GPT2_API int gpt2_tokens_reset(gpt2_tokens* d);
+GPT2_API void gpt2_tokens_close(gpt2_tokens* d); /* NULL-safe */
 
 /* Kernel timing with CUDA events recorded on the model's stream around
  * every launch of the selected kernel classes (bit i of class_mask selects

@@ -18,7 +18,7 @@ import os
 
 import numpy as np
 
-__all__ = ["Model", "GPT2Error", "library_path", "load_library", "layernorm_backward_noalloc",
+__all__ = ["Model", "GPT2Error", "TokenFile", "library_path", "load_library", "layernorm_backward_noalloc",
            "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +29,7 @@ PARAMS, GRADS, ADAM_M, ADAM_V = 0, 1, 2, 3
 FP32, BF16 = 0, 1
 
 ERRORS = {0: "OK", -1: "GPT2_ERR_ARG", -2: "GPT2_ERR_OOM", -3: "GPT2_ERR_CUDA", -4: "GPT2_ERR_STATE",
-          -5: "GPT2_ERR_TOKEN", -6: "GPT2_ERR_TIMEOUT", -7: "GPT2_ERR_NONFINITE"}
+          -5: "GPT2_ERR_TOKEN", -6: "GPT2_ERR_TIMEOUT", -7: "GPT2_ERR_NONFINITE", -8: "GPT2_ERR_IO"}
 
 
 class GPT2Error(RuntimeError):
@@ -90,6 +90,13 @@ def load_library():
         "gpt2_launch_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_last_error": ([vp], ctypes.c_char_p),
         "gpt2_layernorm_backward_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp], ctypes.c_int),
+        "gpt2_save_checkpoint": ([vp, ctypes.c_char_p, i32], ctypes.c_int),
+        "gpt2_load_checkpoint": ([vp, ctypes.c_char_p, ctypes.POINTER(i32)], ctypes.c_int),
+        "gpt2_tokens_open": ([ctypes.c_char_p, ctypes.POINTER(vp)], ctypes.c_int),
+        "gpt2_tokens_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
+        "gpt2_tokens_next_batch": ([vp, i32, i32, vp, vp], ctypes.c_int),
+        "gpt2_tokens_reset": ([vp], ctypes.c_int),
+        "gpt2_tokens_close": ([vp], None),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -262,6 +269,72 @@ class Model:
         n = ctypes.c_int64()
         self._check(self._lib.gpt2_launch_count(self._h, ctypes.byref(n)))
         return n.value
+
+    # -- checkpoints ---------------------------------------------------------
+    def save_checkpoint(self, path, step=0):
+        """Write params, AdamW m and v and `step` to one flat file."""
+        self._check(self._lib.gpt2_save_checkpoint(self._h, os.fsencode(path), int(step)))
+
+    def load_checkpoint(self, path) -> int:
+        """Replace params, m and v from a checkpoint of this model's shape;
+        returns the saved step."""
+        t = ctypes.c_int32()
+        self._check(self._lib.gpt2_load_checkpoint(self._h, os.fsencode(path), ctypes.byref(t)))
+        return t.value
+
+
+class TokenFile:
+    """A raw int32 token file (.bin) served as next-token batches:
+    next_batch(B, T) -> (tokens, targets), int32 arrays [B, T] with
+    targets[i] = tokens[i + 1] along the file, the cursor advancing by B*T
+    and starting over when a batch would run past the end."""
+
+    def __init__(self, path):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        rc = self._lib.gpt2_tokens_open(os.fsencode(path), ctypes.byref(h))
+        if rc != 0:
+            raise GPT2Error(rc, self._lib.gpt2_last_error(None).decode())
+        self._h = h
+
+    def __len__(self):
+        n = ctypes.c_int64()
+        self._check(self._lib.gpt2_tokens_count(self._h, ctypes.byref(n)))
+        return n.value
+
+    def _check(self, rc):
+        if rc != 0:
+            raise GPT2Error(rc, self._lib.gpt2_last_error(None).decode())
+
+    def next_batch(self, B, T, tokens=None, targets=None):
+        """Fill (and return) host int32 buffers of B*T elements; pinned
+        torch tensors or numpy arrays may be passed in."""
+        if tokens is None:
+            tokens = np.empty((B, T), np.int32)
+        if targets is None:
+            targets = np.empty((B, T), np.int32)
+        self._check(self._lib.gpt2_tokens_next_batch(self._h, int(B), int(T), _ptr(tokens), _ptr(targets)))
+        return tokens, targets
+
+    def reset(self):
+        self._check(self._lib.gpt2_tokens_reset(self._h))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.gpt2_tokens_close(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def layernorm_backward_noalloc(dinp, dweight, dbias, dinp_colsum, dout, inp, weight, mean, rstd,

@@ -728,6 +728,112 @@ int gpt2_copy_in(gpt2_model* m, int32_t arena, const float* srch) {
   return check_device(m, "gpt2_copy_in");
 }
 
+// ---------------------------------------------------------------- checkpoints
+// Header and arena layout: see gpt2_save_checkpoint in gpt2.h.
+#define CKPT_MAGIC 0x43545047  // "GPTC"
+#define CKPT_VERSION 1
+#define CKPT_HEADER 64
+#define CKPT_CHUNK (1 << 24)  // floats per host staging chunk (64 MB)
+
+static void ckpt_header(const gpt2_model* m, int32_t step, int32_t* h) {
+  std::memset(h, 0, sizeof(int32_t) * CKPT_HEADER);
+  const gpt2_config& k = m->cfg;
+  h[0] = CKPT_MAGIC; h[1] = CKPT_VERSION; h[2] = CKPT_HEADER;
+  h[3] = k.max_seq_len; h[4] = k.vocab_size; h[5] = k.padded_vocab_size; h[6] = k.num_layers;
+  h[7] = k.num_heads; h[8] = k.channels; h[9] = k.batch_size; h[10] = k.seq_len; h[11] = k.precision;
+  h[12] = step;
+  h[13] = (int32_t)(uint32_t)((uint64_t)m->n_params & 0xffffffffu);
+  h[14] = (int32_t)(uint32_t)((uint64_t)m->n_params >> 32);
+  h[15] = 3;
+}
+
+int gpt2_save_checkpoint(gpt2_model* m, const char* path, int32_t step) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!path || step < 0) return fail(m, GPT2_ERR_ARG, "gpt2_save_checkpoint: NULL path or step < 0");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_save_checkpoint");
+  if (rc) return rc;
+  FILE* f = std::fopen(path, "wb");
+  if (!f) return fail(m, GPT2_ERR_IO, std::string("gpt2_save_checkpoint: cannot open ") + path);
+  int32_t h[CKPT_HEADER];
+  ckpt_header(m, step, h);
+  bool ok = std::fwrite(h, sizeof(int32_t), CKPT_HEADER, f) == CKPT_HEADER;
+  std::vector<float> buf((size_t)std::min<int64_t>(m->n_params, CKPT_CHUNK));
+  const float* arenas[3] = {m->params, m->adam_m, m->adam_v};
+  cudaError_t e = cudaSuccess;
+  for (int a = 0; a < 3 && ok && e == cudaSuccess; a++) {
+    for (int64_t i = 0; i < m->n_params && ok; i += CKPT_CHUNK) {
+      const size_t n = (size_t)std::min<int64_t>(CKPT_CHUNK, m->n_params - i);
+      e = cudaMemcpy(buf.data(), arenas[a] + i, n * sizeof(float), cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) break;
+      ok = std::fwrite(buf.data(), sizeof(float), n, f) == n;
+    }
+  }
+  ok = (std::fclose(f) == 0) && ok;
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_save_checkpoint");
+  if (!ok) return fail(m, GPT2_ERR_IO, std::string("gpt2_save_checkpoint: write failed: ") + path);
+  return GPT2_OK;
+}
+
+int gpt2_load_checkpoint(gpt2_model* m, const char* path, int32_t* step) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!path) return fail(m, GPT2_ERR_ARG, "gpt2_load_checkpoint: NULL path");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_load_checkpoint");
+  if (rc) return rc;
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return fail(m, GPT2_ERR_IO, std::string("gpt2_load_checkpoint: cannot open ") + path);
+  int32_t h[CKPT_HEADER], want[CKPT_HEADER];
+  if (std::fread(h, sizeof(int32_t), CKPT_HEADER, f) != CKPT_HEADER) {
+    std::fclose(f);
+    return fail(m, GPT2_ERR_IO, "gpt2_load_checkpoint: short header");
+  }
+  ckpt_header(m, h[12], want);
+  bool match = h[0] == want[0] && h[1] == want[1] && h[2] == want[2] && h[15] == want[15] && h[12] >= 0;
+  for (int i = 3; i <= 8; i++) match = match && h[i] == want[i];  // model shape
+  match = match && h[13] == want[13] && h[14] == want[14];        // parameter count
+  if (!match) {
+    std::fclose(f);
+    return fail(m, GPT2_ERR_ARG, "gpt2_load_checkpoint: not a checkpoint of this model's shape");
+  }
+  // the whole file is there before anything of the model is replaced
+  std::fseek(f, 0, SEEK_END);
+  const long long bytes = (long long)std::ftell(f);
+  std::fseek(f, (long)(sizeof(int32_t) * CKPT_HEADER), SEEK_SET);
+  if (bytes < (long long)(sizeof(int32_t) * CKPT_HEADER) + 3LL * (long long)sizeof(float) * m->n_params) {
+    std::fclose(f);
+    return fail(m, GPT2_ERR_IO, "gpt2_load_checkpoint: file ends before the arenas do");
+  }
+  std::vector<float> buf((size_t)std::min<int64_t>(m->n_params, CKPT_CHUNK));
+  float* arenas[3] = {m->params, m->adam_m, m->adam_v};
+  bool ok = true;
+  cudaError_t e = cudaSuccess;
+  for (int a = 0; a < 3 && ok && e == cudaSuccess; a++) {
+    for (int64_t i = 0; i < m->n_params && ok; i += CKPT_CHUNK) {
+      const size_t n = (size_t)std::min<int64_t>(CKPT_CHUNK, m->n_params - i);
+      ok = std::fread(buf.data(), sizeof(float), n, f) == n;
+      if (ok) e = cudaMemcpy(arenas[a] + i, buf.data(), n * sizeof(float), cudaMemcpyHostToDevice);
+      if (e != cudaSuccess) break;
+    }
+  }
+  std::fclose(f);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_load_checkpoint");
+  if (!ok) return fail(m, GPT2_ERR_IO, "gpt2_load_checkpoint: file ends before the arenas do");
+  e = cudaMemsetAsync(m->grads, 0, sizeof(float) * m->n_params, m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_load_checkpoint");
+  if (m->bf) {
+    LaunchCtx c = ctx(m);
+    launch_f32_to_bf16(c, m->wb, m->params, m->n_params);
+    rc = after_launches(m, c, "gpt2_load_checkpoint");
+    if (rc) return rc;
+  }
+  m->have_fwd = false;
+  rc = check_device(m, "gpt2_load_checkpoint");
+  if (rc) return rc;
+  if (step) *step = h[12];
+  return GPT2_OK;
+}
+
 int gpt2_copy_losses_out(gpt2_model* m, float* dst) {
   if (!m || !dst) return GPT2_ERR_ARG;
   cudaSetDevice(m->device);
