@@ -65,6 +65,12 @@ def lib():
         L.oracle_gelu_backward_f64.argtypes = [_f64p, _f64p, _f64p, _i64]
         L.oracle_crossentropy_forward_f64.argtypes = [_f64p, _f64p, _f64p, vp, _i64, _i64]
         L.oracle_crossentropy_backward_f64.argtypes = [_f64p, _f64p, _i32p, _i64, _i64, ctypes.c_double]
+        L.oracle_decode_logits_f64.argtypes = [_i32p, _f64p, _i32p, _f64p]
+        L.oracle_decode_logits_f64.restype = ctypes.c_int
+        L.oracle_generate_f64.argtypes = [_i32p, _f64p, _i32p, _i64, _i64, ctypes.c_double, _f64p, _i32p, vp]
+        L.oracle_generate_f64.restype = ctypes.c_int
+        L.oracle_sample_f64.argtypes = [_f64p, _i64, ctypes.c_double, ctypes.c_double]
+        L.oracle_sample_f64.restype = _i64
         _lib = L
     return _lib
 
@@ -164,6 +170,40 @@ def step(cfg, params, m, v, tokens, targets, lr, b1, b2, eps, wd, t):
     r = fwdbwd(cfg, params, tokens, targets, want_grads=True)
     adamw(params, r["grads"], m, v, lr, b1, b2, eps, wd, t)
     return r["loss"], r["grads"], r["losses"]
+
+
+# ---- generation with a key/value cache (double) ----------------------------
+
+def decode_logits(cfg, params, tokens):
+    """Logits [B, T, V] of every position, computed one position at a time
+    with the key/value cache (the incremental form of the forward)."""
+    B, T, V = int(cfg[6]), int(cfg[7]), int(cfg[3])
+    out = np.zeros(B * T * V)
+    assert lib().oracle_decode_logits_f64(cfg, np.ascontiguousarray(params, np.float64),
+                                          np.ascontiguousarray(tokens, np.int32).reshape(-1), out) == 0
+    return out.reshape(B, T, V)
+
+
+def generate(cfg, params, prompt, n_new, temperature, uniforms):
+    """Prompt [B, T0] -> (tokens [B, T0 + n_new], logits [n_new, B, V]); new
+    token i of sequence b is drawn with uniforms[i, b]."""
+    B, V = int(cfg[6]), int(cfg[3])
+    prompt = np.ascontiguousarray(prompt, np.int32).reshape(B, -1)
+    T0 = prompt.shape[1]
+    u = np.ascontiguousarray(uniforms, np.float64).reshape(-1)
+    assert u.size == n_new * B
+    toks = np.zeros((B, T0 + n_new), np.int32)
+    logits = np.zeros(max(n_new, 1) * B * V)
+    assert lib().oracle_generate_f64(cfg, np.ascontiguousarray(params, np.float64), prompt.reshape(-1),
+                                     T0, n_new, float(temperature), u, toks, _ptr(logits)) == 0
+    return toks, logits[:n_new * B * V].reshape(n_new, B, V)
+
+
+def sample(logits, temperature, u):
+    """Index drawn from one row of scores (inverse CDF of the softmax at the
+    temperature; greedy for temperature <= 0)."""
+    lg = np.ascontiguousarray(logits, np.float64).reshape(-1)
+    return int(lib().oracle_sample_f64(lg, lg.size, float(temperature), float(u)))
 
 
 # ---- layer primitives (double) -------------------------------------------

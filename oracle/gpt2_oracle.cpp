@@ -594,6 +594,108 @@ double fwdbwd(const int32_t* cfg8, const R* params, const int32_t* tok,
   return loss;
 }
 
+// ---------------------------------------------------------------- generation
+
+// One new position `pos` of one sequence, computed with a key/value cache
+// ([GeekNews], "How KV caching works": after a token is generated the next
+// one needs only the new row; the keys and values of the earlier rows are
+// kept from the earlier iterations and reused).  kc, vc: this sequence's
+// cache, [L][maxT][C]; rows 0..pos-1 hold the earlier positions and row pos
+// is written here.  The arithmetic of every step is the one of the full
+// forward above, applied to the single new row; the attention of the new
+// query over cache rows 0..pos is the row t = pos of attention_forward.
+// logits: the V scores of the new row ([GeekNews], "The Transformer core":
+// the final LayerNorm output at the last position times the embedding
+// matrix).
+template <typename R>
+void decode_position(const Shape& s, const R* params, R* kc, R* vc, int32_t token, int64_t pos,
+                     R* logits) {
+  const int64_t C = s.C, L = s.L, NH = s.NH, hs = C / NH, maxT = s.maxT;
+  int64_t psz[NUM_PARAMS];
+  param_sizes(s, psz);
+  Tensors<R> P(const_cast<R*>(params), psz, NUM_PARAMS);
+  std::vector<R> x(C), ln(C), qkv(3 * C), y(C), ap(C), x2(C), fch(4 * C), fcg(4 * C), fp(C);
+  std::vector<R> sc(pos + 1);
+  R mean = 0, rstd = 0;
+  // token embedding plus the embedding of position pos
+  encoder_forward(x.data(), &token, P[WTE], P[WPE] + pos * C, 1, 1, C);
+  const R scale = (R)1 / std::sqrt((R)hs);
+  for (int64_t l = 0; l < L; l++) {
+    R* kl = kc + l * maxT * C;
+    R* vl = vc + l * maxT * C;
+    layernorm_forward(ln.data(), &mean, &rstd, x.data(), P[LN1W] + l * C, P[LN1B] + l * C, 1, C);
+    matmul_forward(qkv.data(), ln.data(), P[QKVW] + l * 3 * C * C, P[QKVB] + l * 3 * C, 1, C, 3 * C);
+    for (int64_t i = 0; i < C; i++) {
+      kl[pos * C + i] = qkv[C + i];
+      vl[pos * C + i] = qkv[2 * C + i];
+    }
+    for (int64_t h = 0; h < NH; h++) {
+      const R* q = qkv.data() + h * hs;
+      R mx = -std::numeric_limits<R>::infinity();
+      for (int64_t j = 0; j <= pos; j++) {
+        const R* k = kl + j * C + h * hs;
+        R d = 0;
+        for (int64_t i = 0; i < hs; i++) d += q[i] * k[i];
+        d = d * scale;
+        sc[j] = d;
+        if (d > mx) mx = d;
+      }
+      R sum = 0;
+      for (int64_t j = 0; j <= pos; j++) {
+        sc[j] = std::exp(sc[j] - mx);
+        sum += sc[j];
+      }
+      for (int64_t j = 0; j <= pos; j++) sc[j] = sc[j] / sum;
+      R* yh = y.data() + h * hs;
+      for (int64_t i = 0; i < hs; i++) yh[i] = 0;
+      for (int64_t j = 0; j <= pos; j++) {
+        const R* v = vl + j * C + h * hs;
+        for (int64_t i = 0; i < hs; i++) yh[i] += sc[j] * v[i];
+      }
+    }
+    matmul_forward(ap.data(), y.data(), P[ATTPROJW] + l * C * C, P[ATTPROJB] + l * C, 1, C, C);
+    residual_forward(x2.data(), x.data(), ap.data(), C);
+    layernorm_forward(ln.data(), &mean, &rstd, x2.data(), P[LN2W] + l * C, P[LN2B] + l * C, 1, C);
+    matmul_forward(fch.data(), ln.data(), P[FCW] + l * 4 * C * C, P[FCB] + l * 4 * C, 1, C, 4 * C);
+    gelu_forward(fcg.data(), fch.data(), 4 * C);
+    matmul_forward(fp.data(), fcg.data(), P[FCPROJW] + l * 4 * C * C, P[FCPROJB] + l * C, 1, 4 * C, C);
+    residual_forward(x.data(), x2.data(), fp.data(), C);
+  }
+  layernorm_forward(ln.data(), &mean, &rstd, x.data(), P[LNFW], P[LNFB], 1, C);
+  matmul_forward(logits, ln.data(), P[WTE], (const R*)nullptr, 1, C, s.V);
+}
+
+// The next token drawn from the V scores of one row.  The pages print the
+// generated ids ([InfoQ] run log, "generated: ...") but not the rule; the
+// plainest reading taken here is inverse-CDF sampling of the softmax at a
+// temperature: p_i proportional to exp((l_i - max l) / temperature), and
+// the token is the smallest i whose running sum p_0 + ... + p_i exceeds
+// u * (p_0 + ... + p_{V-1}), u a uniform draw in [0, 1) supplied by the
+// caller.  temperature <= 0 is greedy decoding: the first index of the
+// largest score.  Should rounding leave no running sum above the threshold,
+// the last index with p_i > 0 is taken.
+int64_t sample_row(const double* l, int64_t V, double temperature, double u) {
+  int64_t best = 0;
+  for (int64_t i = 1; i < V; i++) if (l[i] > l[best]) best = i;
+  if (!(temperature > 0)) return best;
+  const double mx = l[best];
+  std::vector<double> p(V);
+  double sum = 0;
+  for (int64_t i = 0; i < V; i++) {
+    p[i] = std::exp((l[i] - mx) / temperature);
+    sum += p[i];
+  }
+  const double target = u * sum;
+  double run = 0;
+  int64_t last = best;
+  for (int64_t i = 0; i < V; i++) {
+    run += p[i];
+    if (p[i] > 0) last = i;
+    if (run > target) return i;
+  }
+  return last;
+}
+
 // ---------------------------------------------------------------- init RNG
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
@@ -737,6 +839,62 @@ int oracle_residuals_f32(const int32_t* cfg8, const float* params, const int32_t
 double oracle_fwdbwd_f64(const int32_t* cfg8, const double* params, const int32_t* tok,
                          const int32_t* tgt, double* grads, double* losses, double* logits) {
   return fwdbwd<double>(cfg8, params, tok, tgt, grads, losses, logits);
+}
+
+// Logits of every position of tok [B, T], computed position by position with
+// the key/value cache of decode_position (row t of sequence b uses cache rows
+// 0..t).  out: [B, T, V].  Returns 0, or -1 for a bad shape or id.
+int oracle_decode_logits_f64(const int32_t* cfg8, const double* params, const int32_t* tok,
+                             double* out) {
+  Shape s = shape_from(cfg8);
+  if (!shape_ok(s) || s.T > s.maxT) return -1;
+  for (int64_t i = 0; i < s.B * s.T; i++)
+    if (tok[i] < 0 || tok[i] >= s.V) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < s.B; b++) {
+    std::vector<double> kc(s.L * s.maxT * s.C), vc(s.L * s.maxT * s.C);
+    for (int64_t t = 0; t < s.T; t++)
+      decode_position(s, params, kc.data(), vc.data(), tok[b * s.T + t], t, out + (b * s.T + t) * s.V);
+  }
+  return 0;
+}
+
+// Generation: for each of the B sequences, the prompt prompt[b, 0..T0-1] is
+// run through decode_position (filling the cache), then n_new tokens are
+// drawn one at a time with sample_row from the scores of the last row, the
+// drawn token being the input of the next position.  uniforms: [n_new, B],
+// the draw of new token i of sequence b at uniforms[i * B + b].
+// out_tokens: [B, T0 + n_new] (prompt, then the drawn tokens); out_logits
+// (may be null): [n_new, B, V], the scores each new token was drawn from.
+// Needs 1 <= T0 and T0 + n_new <= maxT + 1 (the last drawn token is not fed
+// back).  Returns 0, or -1 for a bad shape or id.
+int oracle_generate_f64(const int32_t* cfg8, const double* params, const int32_t* prompt, int64_t T0,
+                        int64_t n_new, double temperature, const double* uniforms, int32_t* out_tokens,
+                        double* out_logits) {
+  Shape s = shape_from(cfg8);
+  if (!shape_ok(s) || T0 < 1 || n_new < 0 || T0 + n_new > s.maxT + 1 || T0 > s.maxT) return -1;
+  for (int64_t i = 0; i < s.B * T0; i++)
+    if (prompt[i] < 0 || prompt[i] >= s.V) return -1;
+  const int64_t TT = T0 + n_new;
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < s.B; b++) {
+    std::vector<double> kc(s.L * s.maxT * s.C), vc(s.L * s.maxT * s.C), lg(s.V);
+    for (int64_t t = 0; t < T0; t++) out_tokens[b * TT + t] = prompt[b * T0 + t];
+    for (int64_t t = 0; t < T0 - 1; t++)
+      decode_position(s, params, kc.data(), vc.data(), prompt[b * T0 + t], t, lg.data());
+    int32_t cur = prompt[b * T0 + T0 - 1];
+    for (int64_t i = 0; i < n_new; i++) {
+      decode_position(s, params, kc.data(), vc.data(), cur, T0 - 1 + i, lg.data());
+      if (out_logits) std::memcpy(out_logits + (i * s.B + b) * s.V, lg.data(), sizeof(double) * s.V);
+      cur = (int32_t)sample_row(lg.data(), s.V, temperature, uniforms[i * s.B + b]);
+      out_tokens[b * TT + T0 + i] = cur;
+    }
+  }
+  return 0;
+}
+
+int64_t oracle_sample_f64(const double* logits, int64_t V, double temperature, double u) {
+  return sample_row(logits, V, temperature, u);
 }
 
 void oracle_adamw_f32(int64_t n, float* p, const float* g, float* m, float* v, float lr,
