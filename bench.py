@@ -24,6 +24,14 @@ Prints ONE JSON line (rank 0).  Keys:
 
 --impl reference times the CPU oracle itself (the only other implementation
 of this step) on bounded samples of the same workload.
+
+--mode decode measures generation with the key/value cache instead: GPT-2
+124M, B=16 sequences, a 512-token prompt per sequence run through one
+forward (the prefill), then one gpt2_decode_step per new token (temperature
+1.0, uniforms from a fixed seed).  value = generated tokens/s over the timed
+decode steps; the roofline is the whole decode step against the HBM copy
+peak (its algorithmic bytes: the bf16 weights read once, the cached keys and
+values of rows 0..pos read once, the new cache row and the scores written).
 """
 import argparse
 import hashlib
@@ -54,6 +62,8 @@ WORKLOADS = {
                                dist="zipf", lr=6e-4, wd=0.1),
 }
 DEFAULT_WORKLOAD = "gpt2-124M-B16-T1024"
+DECODE_METRIC = "GPT-2 124M generated tokens/sec with a key/value cache (B=16 sequences) on 1 B300"
+DECODE = dict(L=12, C=768, NH=12, V=50257, Vp=50304, maxT=1024, B=16, T=1024, prompt=512, temperature=1.0)
 BETAS, EPS = (0.9, 0.999), 1e-8
 L2_BYTES = 126 * 2 ** 20
 
@@ -383,6 +393,130 @@ def step_bytes(w):
     return 30 * n + 3 * acts
 
 
+# ---------------------------------------------------------------- decode mode
+def decode_step_bytes(d, pos):
+    """Algorithmic bytes of one decode step at position pos: every input read
+    once (bf16 weight matrices, fp32 biases and LayerNorm parameters, the
+    token and position embedding rows, the cached keys and values of rows
+    0..pos), every output written once (the new cache row of q, k, v); the
+    scores and the per-row activations are intermediates."""
+    L, C, Vp, B = d["L"], d["C"], d["Vp"], d["B"]
+    matrices = 2 * (Vp * C + L * 12 * C * C)
+    small = 4 * (L * 13 * C + 2 * C) + 4 * (B + 1) * C
+    kv_read = 2 * L * B * pos * 2 * C
+    new_row = 2 * L * B * 3 * C
+    return matrices + small + kv_read + new_row
+
+
+def run_decode(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import transformer_lm_step_gpt_b300 as tl
+
+    d = DECODE
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, T, P = d["B"], d["T"], d["prompt"]
+    stream = torch.cuda.Stream(device=dev)
+    m = tl.Model(d["L"], d["C"], d["NH"], d["V"], d["Vp"], d["maxT"], B, T, precision="bf16",
+                 seed=1337 + rank, stream=stream)
+    W, K = args.warmup, args.steps
+    if P - 1 + W + K > T:
+        raise SystemExit("decode mode: prompt + warm-up + steps must fit in %d positions" % T)
+    rng = np.random.default_rng(77 + rank)
+    prompt = np.zeros((B, T), np.int32)
+    prompt[:, :P] = rng.integers(0, d["V"], (B, P))
+    u = rng.random((W + K, B)).astype(np.float32)
+    with torch.cuda.stream(stream):
+        tok_d = torch.from_numpy(prompt).to(dev)
+        seq = torch.empty((W + K + 1, B), dtype=torch.int32, device=dev)
+        seq[0] = tok_d[:, P - 1]
+        u_d = torch.from_numpy(u).to(dev)
+    stream.synchronize()
+    m.forward(tok_d, None, sync=False)
+    for i in range(W):
+        m.decode_step(seq[i], P - 1 + i, d["temperature"], u_d[i], out=seq[i + 1])
+    m.profile_enable("all")
+    m.profile_reset()
+    clocks = ClockSampler(gpu_uuid(local))
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    n0 = m.launch_count
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(W, W + K):
+        m.decode_step(seq[i], P - 1 + i, d["temperature"], u_d[i], out=seq[i + 1])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    local_ms = e0.elapsed_time(e1)
+    launches = m.launch_count - n0
+    prof = m.profile_read()
+    m.profile_enable(None)
+    total_ms, _, value = aggregate(local_ms, K * B, world, dev)
+    ms_per_step = total_ms / K
+    # profiling events around every launch stretch the step a little: time
+    # the same steps again without them for the reported value
+    m.forward(tok_d, None, sync=False)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0.record(stream)
+    for i in range(W, W + K):
+        m.decode_step(seq[i], P - 1 + i, d["temperature"], u_d[i], out=seq[i + 1])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms, _, value = aggregate(e0.elapsed_time(e1), K * B, world, dev)
+    ms_per_step = total_ms / K
+    by = sum(decode_step_bytes(d, P - 1 + i) for i in range(W, W + K)) / K
+    peaks = load_peaks()
+    achieved = by / (ms_per_step / 1e3) / 1e9
+    breakdown = {r["name"]: round(r["ms"] / K, 4) for r in prof if r["launches"]}
+    # end to end through Model.generate: prompt copied in, prefill forward,
+    # K new tokens, all tokens read back
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    m.generate(prompt[:, :P], K, temperature=d["temperature"], uniforms=u[:K])
+    e2e = K * B / (time.perf_counter() - t0) * world
+    out = dict(metric=DECODE_METRIC, value=round(value, 1), unit="tokens/s", n_gpus=world, steps=K, warmup=W,
+               ms_per_step=round(ms_per_step, 4), higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="bf16", data="synthetic: uniform prompt ids, random GPT-2 init weights, uniforms from a fixed seed",
+               config=dict(workload="gpt2-124M-decode-B16-P512", batch=B, prompt=P, cache_rows=T,
+                           temperature=d["temperature"], mode="decode",
+                           l2="no flush: each step reads the 0.25 GB of bf16 weights and the cache (> 126 MB L2)"),
+               roofline=dict(bound="hbm", achieved=round(achieved, 1), peak=peaks["hbm_gbs"], unit="GB/s",
+                             frac=round(achieved / peaks["hbm_gbs"], 4), traffic=None, kernel="decode step (all kernels)",
+                             bytes_per_step=by, peak_source="%s hbm_gbs" % peaks["source"]),
+               e2e=dict(value=round(e2e, 1), unit="tokens/s", h2d_bytes_per_step=round(B * P * 4 / K + B * 4, 1),
+                        d2h_bytes_per_step=B * 4,
+                        note="Model.generate: prefill forward + %d decode steps, prompt in and tokens out" % K),
+               gpu_launches=launches, clocks=clk, kernels_ms_per_step=breakdown)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = decode_cpu_baseline(d)
+    m.close()
+    return out if rank == 0 else None
+
+
+def decode_cpu_baseline(d):
+    import numpy as np
+
+    import oracle
+    cfg = oracle.cfg8(d["L"], d["C"], d["NH"], d["V"], d["Vp"], d["maxT"], 1, 8)
+    p = oracle.init_params(cfg, 1337)
+    prompt = np.arange(1, 9, dtype=np.int32).reshape(1, 8)
+    n_new = 4
+    t0 = time.perf_counter()
+    oracle.generate(cfg, p, prompt, n_new, 1.0, np.full((n_new, 1), 0.5))
+    dt = time.perf_counter() - t0
+    return dict(value=n_new / dt, unit="tokens/s", cores=1, kind="oracle",
+                sample="one sequence: an 8-token prompt and %d new tokens through the oracle's incremental "
+                       "forward (fp64, one thread per sequence), %.1f s" % (n_new, dt))
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, w, world, rank):
     if rank != 0:
@@ -413,6 +547,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["train", "decode"], default="train")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -420,7 +555,10 @@ def main(argv=None):
     if world != args.gpus and world > 1:
         print("warning: WORLD_SIZE=%d but --gpus %d" % (world, args.gpus), file=sys.stderr)
     w = WORKLOADS[args.workload]
-    out = run_reference(args, w, world, rank) if args.impl == "reference" else run_ours(args, w, world, rank, local)
+    if args.mode == "decode" and args.impl == "ours":
+        out = run_decode(args, world, rank, local)
+    else:
+        out = run_reference(args, w, world, rank) if args.impl == "reference" else run_ours(args, w, world, rank, local)
     if out is not None and rank == 0:
         print(json.dumps(out), flush=True)
 

@@ -201,6 +201,43 @@ GPT2_API int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* host_ds
  * GPT2_ERR_NONFINITE for a NaN/Inf loss. */
 GPT2_API int gpt2_read_loss(gpt2_model* m, float* host_loss);
 
+/* ---------------------------------------------------------------- generation
+ * Decoding with a key/value cache.  GeekNews, "A GPT-2-based ChatGPT clone in
+ * 3000 bytes of C", section "How KV caching works": after a token is
+ * generated, the results of the earlier rows are reused and only the new row
+ * is computed; section "The Transformer core": the final LayerNorm output at
+ * the last position times the embedding matrix scores the next token.  The
+ * cache is the per-layer qkv activation of gpt2_forward ([B, T, 3C] per
+ * layer, in the model's activation precision): a gpt2_forward over a batch
+ * whose first P positions are the prompts fills rows 0..P-1 (later rows do
+ * not influence them: attention is causal), then one gpt2_decode_step per
+ * new position pos = P-1+i ... appends.
+ *
+ * gpt2_decode_step computes position pos of every sequence b: the input id
+ * tokens[b] (device, [B] int32) at position pos; keys and values of that
+ * row are written into row pos of the cache, its query attends to rows
+ * 0..pos (the caller guarantees rows 0..pos-1 hold this sequence's earlier
+ * positions); the scores l of the row (its V real columns) give
+ * next_tokens[b] (device, [B] int32): the smallest i whose running sum of
+ * p_j = exp((l_j - max l) / temperature) passes uniforms[b] * sum_j p_j
+ * (inverse-CDF sampling; uniforms: device [B] floats in [0, 1) that the
+ * caller draws), or, for temperature <= 0, the first index of the largest
+ * score.  All three pointers are read / written on the model's stream
+ * after the call returns (stream order); the caller owns them.  A row pos
+ * and its input can be fed back as tokens = next_tokens for pos + 1.
+ * Asynchronous: errors of the device side (an id outside [0, V)) surface at
+ * the next synchronising call.  After a decode step the training state of
+ * the last forward is gone (gpt2_backward needs a new gpt2_forward);
+ * gpt2_adamw_step, gpt2_copy_in(GPT2_PARAMS) and gpt2_load_checkpoint
+ * invalidate the cache.  Errors: GPT2_ERR_ARG (NULL pointer, pos outside
+ * [0, T), non-finite temperature), GPT2_ERR_STATE (no cache of the current
+ * weights), GPT2_ERR_CUDA. */
+GPT2_API int gpt2_decode_step(gpt2_model* m, const int32_t* tokens, int32_t pos, float temperature,
+                              const float* uniforms, int32_t* next_tokens);
+/* The scores [B, Vp] (as fp32; pad columns 0) of the last decode step.
+ * Synchronises.  GPT2_ERR_STATE before the first decode step. */
+GPT2_API int gpt2_copy_decode_logits_out(gpt2_model* m, float* host_dst);
+
 /* ---------------------------------------------------------------- checkpoints
  * Training state saved and resumed as one flat file: InfoQ's account of
  * llm.c loads its model as a checkpoint file of fp32 weights in one block;

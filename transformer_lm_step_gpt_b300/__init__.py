@@ -97,6 +97,8 @@ def load_library():
         "gpt2_tokens_next_batch": ([vp, i32, i32, vp, vp], ctypes.c_int),
         "gpt2_tokens_reset": ([vp], ctypes.c_int),
         "gpt2_tokens_close": ([vp], None),
+        "gpt2_decode_step": ([vp, vp, i32, f32, vp, vp], ctypes.c_int),
+        "gpt2_copy_decode_logits_out": ([vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -269,6 +271,54 @@ class Model:
         n = ctypes.c_int64()
         self._check(self._lib.gpt2_launch_count(self._h, ctypes.byref(n)))
         return n.value
+
+    # -- generation ----------------------------------------------------------
+    def decode_step(self, tokens, pos, temperature, uniforms, out=None):
+        """One position of every sequence with the key/value cache (see
+        gpt2_decode_step): tokens (int32 [B]) at position pos in, the drawn
+        next tokens (int32 [B]) out; uniforms: float32 [B] in [0, 1).  All
+        three are CUDA tensors used in the model's stream order."""
+        if out is None:
+            import torch
+            out = torch.empty(self.B, dtype=torch.int32, device=tokens.device)
+        self._check(self._lib.gpt2_decode_step(self._h, _ptr(tokens), int(pos), float(temperature),
+                                               _ptr(uniforms), _ptr(out)))
+        return out
+
+    def decode_logits(self) -> np.ndarray:
+        """Scores [B, Vp] of the last decode step (synchronises)."""
+        a = np.empty((self.B, self.Vp), np.float32)
+        self._check(self._lib.gpt2_copy_decode_logits_out(self._h, a.ctypes.data))
+        return a
+
+    def generate(self, prompt, n_new, temperature=1.0, seed=0, uniforms=None):
+        """prompt: int32 [B, T0] host ids (1 <= T0 <= T).  A forward over the
+        prompts (padded to T) fills the cache; then n_new decode steps at
+        positions T0-1 .. T0-2+n_new each draw one token, new token i of
+        sequence b with uniforms[i, b] (default: numpy's generator seeded with
+        `seed`).  Returns int32 [B, T0 + n_new]: prompt, then the new tokens."""
+        import torch
+        prompt = np.ascontiguousarray(prompt, np.int32).reshape(self.B, -1)
+        T0 = prompt.shape[1]
+        if not (1 <= T0 <= self.T) or n_new < 0 or T0 - 1 + n_new > self.T:
+            raise ValueError("need 1 <= T0 <= T and T0 - 1 + n_new <= T")
+        if uniforms is None:
+            uniforms = np.random.default_rng(seed).random((n_new, self.B))
+        u = np.ascontiguousarray(uniforms, np.float32).reshape(n_new, self.B)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        padded = np.zeros((self.B, self.T), np.int32)
+        padded[:, :T0] = prompt
+        tok_d = torch.from_numpy(padded).to(dev)
+        seq_d = torch.empty((n_new + 1, self.B), dtype=torch.int32, device=dev)
+        seq_d[0] = torch.from_numpy(np.ascontiguousarray(prompt[:, T0 - 1])).to(dev)
+        u_d = torch.from_numpy(u).to(dev)
+        torch.cuda.synchronize(dev)  # inputs in place before the model's stream reads them
+        self.forward(tok_d, None, sync=False)
+        for i in range(n_new):
+            self.decode_step(seq_d[i], T0 - 1 + i, temperature, u_d[i], out=seq_d[i + 1])
+        self.synchronize()
+        new = seq_d[1:].cpu().numpy().T
+        return np.concatenate([prompt, new], axis=1).astype(np.int32)
 
     # -- checkpoints ---------------------------------------------------------
     def save_checkpoint(self, path, step=0):

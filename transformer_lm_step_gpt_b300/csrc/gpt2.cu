@@ -44,7 +44,8 @@ thread_local std::string g_build_error = "no error";
 enum GemmSite { GS_QKV = 0, GS_ATTPROJ, GS_FC, GS_FCPROJ, GS_HEAD, GS_N };
 enum GemmPass { GP_FWD = 0, GP_DGRAD, GP_WGRAD };
 enum ProfClass { PC_GEMM0 = 0, PC_ATTN_FWD = 3 * GS_N, PC_ATTN_BWD, PC_LN_FWD, PC_LN_BWD, PC_CE,
-                 PC_BIAS_GRAD, PC_ENC_FWD, PC_ENC_BWD, PC_ADAMW, PC_ZERO_GRAD, PC_N };
+                 PC_BIAS_GRAD, PC_ENC_FWD, PC_ENC_BWD, PC_ADAMW, PC_ZERO_GRAD, PC_DEC_ATTN, PC_SAMPLE,
+                 PC_N };
 const char* kProfNames[PC_N] = {
     "gemm_qkv_fwd", "gemm_qkv_dgrad", "gemm_qkv_wgrad",
     "gemm_attproj_fwd", "gemm_attproj_dgrad", "gemm_attproj_wgrad",
@@ -52,11 +53,11 @@ const char* kProfNames[PC_N] = {
     "gemm_fcproj_fwd", "gemm_fcproj_dgrad", "gemm_fcproj_wgrad",
     "gemm_head_fwd", "gemm_head_dgrad", "gemm_head_wgrad",
     "attention_fwd", "attention_bwd", "layernorm_fwd", "layernorm_bwd", "crossentropy",
-    "bias_grad", "encoder_fwd", "encoder_bwd", "adamw", "zero_grad"};
+    "bias_grad", "encoder_fwd", "encoder_bwd", "adamw", "zero_grad", "decode_attention", "sample"};
 const char* kProfUnits[PC_N] = {
     "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop", "flop",
     "flop", "flop", "flop", "flop", "flop", "flop", "byte", "byte", "byte", "byte", "byte",
-    "byte", "byte", "byte"};
+    "byte", "byte", "byte", "byte", "byte"};
 
 struct ProfState {
   uint32_t mask = 0;
@@ -117,7 +118,12 @@ struct gpt2_model {
   int* err;
   int64_t launches = 0;
   ProfState prof;
+  // generation: one row per sequence (the key/value cache is qkv above)
+  float *dec_x, *dec_mid, *dec_mean, *dec_rstd;
+  char *dec_ln, *dec_y, *dec_fcd, *dec_fcg, *dec_logits;
   bool have_fwd = false, fwd_targets = false;
+  bool have_cache = false;  // qkv holds keys / values of the current weights
+  bool have_dec = false;    // dec_logits holds a decode step's scores
   std::string last_error = "no error";
 
   int64_t tensor(int t) const { return off[t]; }
@@ -268,6 +274,15 @@ size_t layout(gpt2_model* m, char* base) {
   m->splitk_flags = b.take<int>(m->splitk_flag_count);
   m->enc_sorted = b.take<uint32_t>(M);
   m->enc_partial = b.take<float>(M * C);
+  m->dec_x = b.take<float>((int64_t)m->B * C);
+  m->dec_mid = b.take<float>((int64_t)m->B * C);
+  m->dec_mean = b.take<float>(m->B);
+  m->dec_rstd = b.take<float>(m->B);
+  m->dec_ln = b.take<char>((int64_t)m->B * C * a);
+  m->dec_y = b.take<char>((int64_t)m->B * C * a);
+  m->dec_fcd = b.take<char>((int64_t)m->B * 4 * C * a);
+  m->dec_fcg = b.take<char>((int64_t)m->B * 4 * C * a);
+  m->dec_logits = b.take<char>((int64_t)m->B * m->Vp * a);
   m->err = b.take<int>(1);
   return b.off + 256;
 }
@@ -368,6 +383,78 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
                               1.f / (float)M, with_targets);
   }
   if (with_targets) launch_mean(c, m->loss, m->losses, M);
+}
+
+// One new position `pos` of every sequence with the key/value cache: the
+// forward of forward_layers applied to row pos only (GeekNews, "A GPT-2-based
+// ChatGPT clone in 3000 bytes of C", section "How KV caching works": the rows
+// before it are reused, only the new one is computed).  Its k, v go into row
+// pos of each layer's qkv; its attention reads rows 0..pos; the final
+// LayerNorm output times wte^T gives the row's scores, from which the next
+// token is drawn.
+template <typename ActT>
+void decode_layers(gpt2_model* m, LaunchCtx& c, const int32_t* tok, int pos, float temperature,
+                   const float* u, int32_t* next) {
+  const int M = m->M, C = m->C, L = m->L, B = m->B, T = m->T, NH = m->NH;
+  const bool f32 = !m->bf;
+  const int64_t WS = sizeof(ActT) == 2 ? 2 : 4;
+  auto w = [&](int t, int64_t o) {
+    return static_cast<const void*>(static_cast<const char*>(m->W(t)) + o * WS);
+  };
+  ActT* ln = reinterpret_cast<ActT*>(m->dec_ln);
+  ActT* y = reinterpret_cast<ActT*>(m->dec_y);
+  float *x = m->dec_x, *mid = m->dec_mid;
+  const double a = (double)sizeof(ActT);
+  const double ln_bytes = (double)B * C * (4 + a) + 8.0 * B;
+  {
+    ProfScope ps(m, PC_ENC_FWD, 12.0 * B * C);
+    launch_encoder_fwd(c, x, tok, m->P(WTE), m->P(WPE) + (int64_t)pos * C, B, 1, C, m->V);
+  }
+  for (int l = 0; l < L; l++) {
+    ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
+    {
+      ProfScope ps(m, PC_LN_FWD, ln_bytes);
+      launch_layernorm_fwd<ActT>(c, ln, m->dec_mean, m->dec_rstd, x, m->P(LN1W) + l * C, m->P(LN1B) + l * C, B, C);
+    }
+    // row pos of sequence b sits at qkv + (b*T + pos)*3C: rows of stride T*3C
+    GemmArgs g = gemm(B, 3 * C, C, ln, C, true, w(QKVW, (int64_t)l * 3 * C * C), C, true, EPI_STORE,
+                      qkv + (int64_t)pos * 3 * C, (int64_t)T * 3 * C, f32);
+    g.bias = m->P(QKVB) + (int64_t)l * 3 * C;
+    run_gemm(m, c, g, GS_QKV);
+    {
+      // the cached keys and values of rows 0..pos read once, the output row written
+      ProfScope ps(m, PC_DEC_ATTN, a * ((double)B * (pos + 1) * 2 * C + 2.0 * B * C));
+      launch_attention_decode<ActT>(c, y, C, qkv, B, T, C, NH, pos);
+    }
+    g = gemm(B, C, C, y, C, true, w(ATTPROJW, (int64_t)l * C * C), C, true, EPI_RESIDUAL, mid, C, true);
+    g.bias = m->P(ATTPROJB) + (int64_t)l * C;
+    g.aux = x;
+    run_gemm(m, c, g, GS_ATTPROJ);
+    {
+      ProfScope ps(m, PC_LN_FWD, ln_bytes);
+      launch_layernorm_fwd<ActT>(c, ln, m->dec_mean, m->dec_rstd, mid, m->P(LN2W) + l * C, m->P(LN2B) + l * C, B, C);
+    }
+    g = gemm(B, 4 * C, C, ln, C, true, w(FCW, (int64_t)l * 4 * C * C), C, true, EPI_GELU_FWD, m->dec_fcd,
+             4 * C, f32);
+    g.bias = m->P(FCB) + (int64_t)l * 4 * C;
+    g.out2 = m->dec_fcg;
+    run_gemm(m, c, g, GS_FC);
+    g = gemm(B, C, 4 * C, m->dec_fcg, 4 * C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C, true,
+             EPI_RESIDUAL, x, C, true);
+    g.bias = m->P(FCPROJB) + (int64_t)l * C;
+    g.aux = mid;
+    run_gemm(m, c, g, GS_FCPROJ);
+  }
+  {
+    ProfScope ps(m, PC_LN_FWD, ln_bytes);
+    launch_layernorm_fwd<ActT>(c, ln, m->dec_mean, m->dec_rstd, x, m->P(LNFW), m->P(LNFB), B, C);
+  }
+  ActT* logits = reinterpret_cast<ActT*>(m->dec_logits);
+  run_gemm(m, c, gemm(B, m->Vp, C, ln, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32), GS_HEAD);
+  {
+    ProfScope ps(m, PC_SAMPLE, a * (double)B * m->V);
+    launch_sample<ActT>(c, next, logits, m->Vp, B, m->V, temperature, u);
+  }
 }
 
 template <typename ActT>
@@ -480,6 +567,7 @@ int forward_common(gpt2_model* m, bool with_targets, float* mean_loss) {
   int rc = after_launches(m, c, "gpt2_forward");
   if (rc) return rc;
   m->have_fwd = true;
+  m->have_cache = true;
   m->fwd_targets = with_targets;
   if (mean_loss) {
     rc = check_device(m, "gpt2_forward");
@@ -654,6 +742,7 @@ int gpt2_adamw_step(gpt2_model* m, float lr, float b1, float b2, float eps, floa
     launch_adamw(c, m->params, m->grads, m->adam_m, m->adam_v, m->bf ? m->wb : nullptr, m->n_params,
                  lr, b1, b2, eps, wd, c1, c2);
   }
+  m->have_cache = false;  // keys / values of the old weights
   return after_launches(m, c, "gpt2_adamw_step");
 }
 
@@ -719,6 +808,7 @@ int gpt2_copy_in(gpt2_model* m, int32_t arena, const float* srch) {
   cudaError_t e = cudaStreamSynchronize(m->stream);
   if (e == cudaSuccess) e = cudaMemcpy(dst, srch, sizeof(float) * m->n_params, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_copy_in");
+  if (arena == GPT2_PARAMS) m->have_cache = false;
   if (arena == GPT2_PARAMS && m->bf) {
     LaunchCtx c = ctx(m);
     launch_f32_to_bf16(c, m->wb, m->params, m->n_params);
@@ -828,9 +918,51 @@ int gpt2_load_checkpoint(gpt2_model* m, const char* path, int32_t* step) {
     if (rc) return rc;
   }
   m->have_fwd = false;
+  m->have_cache = false;
   rc = check_device(m, "gpt2_load_checkpoint");
   if (rc) return rc;
   if (step) *step = h[12];
+  return GPT2_OK;
+}
+
+int gpt2_decode_step(gpt2_model* m, const int32_t* tokens, int32_t pos, float temperature,
+                     const float* uniforms, int32_t* next_tokens) {
+  if (!m) return GPT2_ERR_ARG;
+  if (!tokens || !uniforms || !next_tokens) return fail(m, GPT2_ERR_ARG, "gpt2_decode_step: NULL pointer");
+  if (pos < 0 || pos >= m->T) return fail(m, GPT2_ERR_ARG, "gpt2_decode_step: pos outside [0, T)");
+  if (!std::isfinite(temperature)) return fail(m, GPT2_ERR_ARG, "gpt2_decode_step: temperature is not finite");
+  if (!m->have_cache)
+    return fail(m, GPT2_ERR_STATE, "gpt2_decode_step: no key/value cache of the current weights (run gpt2_forward first)");
+  cudaSetDevice(m->device);
+  LaunchCtx c = ctx(m);
+  if (m->bf) decode_layers<bf16>(m, c, tokens, pos, temperature, uniforms, next_tokens);
+  else decode_layers<float>(m, c, tokens, pos, temperature, uniforms, next_tokens);
+  // row pos of the cache now holds the new position: the activations of the
+  // last forward no longer match each other
+  m->have_fwd = false;
+  m->fwd_targets = false;
+  m->have_dec = true;
+  return after_launches(m, c, "gpt2_decode_step");
+}
+
+int gpt2_copy_decode_logits_out(gpt2_model* m, float* dst) {
+  if (!m || !dst) return GPT2_ERR_ARG;
+  if (!m->have_dec) return fail(m, GPT2_ERR_STATE, "gpt2_copy_decode_logits_out: no decode step to read");
+  cudaSetDevice(m->device);
+  int rc = check_device(m, "gpt2_copy_decode_logits_out");
+  if (rc) return rc;
+  const size_t n = (size_t)m->B * m->Vp;
+  if (!m->bf) {
+    cudaError_t e = cudaMemcpy(dst, m->dec_logits, sizeof(float) * n, cudaMemcpyDeviceToHost);
+    return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_decode_logits_out");
+  }
+  std::vector<uint16_t> tmp(n);
+  cudaError_t e = cudaMemcpy(tmp.data(), m->dec_logits, 2 * n, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_copy_decode_logits_out");
+  for (size_t i = 0; i < n; i++) {
+    uint32_t u = (uint32_t)tmp[i] << 16;
+    std::memcpy(&dst[i], &u, 4);
+  }
   return GPT2_OK;
 }
 

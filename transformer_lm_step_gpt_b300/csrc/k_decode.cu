@@ -1,0 +1,295 @@
+// k_decode.cu -- generation with a key/value cache: the attention of one new
+// query row per sequence over the cached keys and values, and the draw of the
+// next token from the scores of that row.
+//
+// GeekNews, "A GPT-2-based ChatGPT clone in 3000 bytes of C", section "How KV
+// caching works": once a token has been generated, the keys and values of the
+// earlier rows are kept and only the new row is computed; section "The
+// Transformer core": the final LayerNorm output at the last position times the
+// embedding matrix scores the candidates for the next token.  The cache is the
+// per-layer qkv activation [B, T, 3C] of the forward pass: row t of sequence b
+// holds [q | k | v] of position t.
+#include <algorithm>
+#include <climits>
+
+#include "common.cuh"
+#include "kernels.h"
+
+#define DEC_THREADS 256
+#define SMP_THREADS 1024
+
+template <typename T>
+__device__ __forceinline__ void load8f(const T* p, float* f);
+template <>
+__device__ __forceinline__ void load8f<float>(const float* p, float* f) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+template <>
+__device__ __forceinline__ void load8f<bf16>(const bf16* p, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Block-wide reductions over DEC_THREADS / SMP_THREADS threads through
+// shared scratch red[32]; every thread gets the result.  The order of the
+// additions is fixed (lanes by shuffle tree, then warps in index order).
+template <int NT>
+__device__ __forceinline__ float block_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < NT / 32; i++) r = fmaxf(r, red[i]);
+  return r;
+}
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5;
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int i = 1; i < NT / 32; i++) r += red[i];
+  return r;
+}
+
+// y[b, h*hs + d] = sum_{j <= pos} p_j v_j[d],  p = softmax_j(q . k_j * scale),
+// q = row pos of qkv[b] (part q), k_j / v_j = row j (parts k / v), head h.
+// One CTA per (b, h).  Scores: thread per key, kept in shared memory
+// (pos + 1 floats); the weighted sum: whole value rows per warp load, the
+// warps' partial sums added in warp order.
+template <typename T>
+__global__ void __launch_bounds__(DEC_THREADS)
+    attn_decode_kernel(T* y, int64_t ldy, const T* qkv, int T_, int C, int NH, int pos, float scale) {
+  pdl_trigger();
+  extern __shared__ float dsm[];
+  const int hs = C / NH;
+  float* qs = dsm;              // [hs]
+  float* red = qs + hs;         // [32]
+  float* sc = red + 32;         // [pos + 1]
+  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
+  const int tid = threadIdx.x;
+  const int64_t C3 = 3 * (int64_t)C;
+  const T* base = qkv + (int64_t)b * T_ * C3;
+  pdl_wait();
+  for (int d = tid; d < hs; d += DEC_THREADS) qs[d] = to_f(base[(int64_t)pos * C3 + h * hs + d]);
+  __syncthreads();
+  float mx = -INFINITY;
+  for (int j = tid; j <= pos; j += DEC_THREADS) {
+    const T* k = base + (int64_t)j * C3 + C + h * hs;
+    float s = 0.f;
+    for (int d = 0; d < hs; d += 8) {
+      float f[8];
+      load8f<T>(k + d, f);
+#pragma unroll
+      for (int i = 0; i < 8; i++) s = fmaf(qs[d + i], f[i], s);
+    }
+    s *= scale;
+    sc[j] = s;
+    mx = fmaxf(mx, s);
+  }
+  mx = block_max<DEC_THREADS>(mx, red);
+  float sum = 0.f;
+  for (int j = tid; j <= pos; j += DEC_THREADS) {
+    const float e = expf(sc[j] - mx);
+    sc[j] = e;
+    sum += e;
+  }
+  sum = block_sum<DEC_THREADS>(sum, red);  // its barriers also publish sc[]
+  const float inv = 1.f / sum;
+  // weighted sum of the values: a key's row of hs values is read by LPK =
+  // hs/8 lanes (16 bytes each), so a warp reads KPW = 32/LPK whole rows per
+  // load; warp w takes keys w*KPW + r*8*KPW + (lane / LPK), four rows per
+  // lane in flight, and keeps 8 partial sums (its lane's 8 dimensions)
+  const int LPK = hs / 8, KPW = 32 / LPK;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int kl = lane / LPK, d0 = (lane % LPK) * 8;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) acc[i] = 0.f;
+  const T* vbase = base + 2 * C + h * hs + d0;
+  const int step = (DEC_THREADS / 32) * KPW;
+  int j = warp * KPW + kl;
+  for (; j + 3 * step <= pos; j += 4 * step) {
+    float f[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; u++) load8f<T>(vbase + (int64_t)(j + u * step) * C3, f[u]);
+#pragma unroll
+    for (int u = 0; u < 4; u++) {
+      const float p = sc[j + u * step];
+#pragma unroll
+      for (int i = 0; i < 8; i++) acc[i] = fmaf(p, f[u][i], acc[i]);
+    }
+  }
+  for (; j <= pos; j += step) {
+    float f[8];
+    load8f<T>(vbase + (int64_t)j * C3, f);
+    const float p = sc[j];
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] = fmaf(p, f[i], acc[i]);
+  }
+  // add the KPW key slots of the warp (lanes with the same lane % LPK)
+  for (int o = LPK; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  __syncthreads();  // every thread is done reading sc[]: reuse it for the warps' sums
+  if (kl == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) sc[warp * hs + d0 + i] = acc[i];
+  }
+  __syncthreads();
+  if (tid < hs) {
+    float r = 0.f;
+    for (int w = 0; w < DEC_THREADS / 32; w++) r += sc[w * hs + tid];
+    y[(int64_t)b * ldy + h * hs + tid] = from_f<T>(r * inv);
+  }
+}
+
+template <typename T>
+void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int B, int T_, int C, int NH,
+                             int pos) {
+  const int hs = C / NH;
+  // scores (pos + 1) and, later, the warps' partial sums (8 x hs) share one array
+  const size_t smem = sizeof(float) * (hs + 32 + std::max(pos + 1, (DEC_THREADS / 32) * hs));
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(attn_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+    attr = true;
+  }
+  launch_pdl(c, attn_decode_kernel<T>, dim3(B * NH), dim3(DEC_THREADS), smem, y, ldy, qkv, T_, C, NH, pos,
+             1.f / sqrtf((float)hs));
+}
+template void launch_attention_decode<float>(LaunchCtx&, float*, int64_t, const float*, int, int, int, int, int);
+template void launch_attention_decode<bf16>(LaunchCtx&, bf16*, int64_t, const bf16*, int, int, int, int, int);
+
+// One CTA per row b of logits [B, ld]: the next token from the first V
+// scores (inverse-CDF sampling of the softmax at `temperature` with the
+// uniform draw u[b]; temperature <= 0: the first index of the largest score).
+// Thread t owns the contiguous chunk [t*cs, (t+1)*cs) of the row; the chunk
+// sums of e_i = exp((l_i - max) / temperature) are scanned in thread order,
+// and the thread whose chunk holds the threshold u * sum walks it again.
+template <typename T>
+__global__ void __launch_bounds__(SMP_THREADS)
+    sample_kernel(int32_t* next, const T* logits, int64_t ld, int V, float temperature, const float* u) {
+  pdl_trigger();
+  __shared__ float red[32];
+  __shared__ float wsum[SMP_THREADS / 32];
+  __shared__ int pick;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const T* l = logits + (int64_t)b * ld;
+  pdl_wait();
+  const int cs = (V + SMP_THREADS - 1) / SMP_THREADS;
+  const int i0 = min(tid * cs, V), i1 = min(i0 + cs, V);
+  // largest score; its first index
+  float mx = -INFINITY;
+  int arg = INT_MAX;
+  for (int i = i0; i < i1; i++) {
+    const float x = to_f(l[i]);
+    if (x > mx) { mx = x; arg = i; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, mx, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+    if (om > mx || (om == mx && oa < arg)) { mx = om; arg = oa; }
+  }
+  __shared__ int rarg[32];
+  if (lane == 0) { red[w] = mx; rarg[w] = arg; }
+  __syncthreads();
+  if (tid == 0) {
+    float bm = red[0];
+    int ba = rarg[0];
+    for (int i = 1; i < SMP_THREADS / 32; i++)
+      if (red[i] > bm || (red[i] == bm && rarg[i] < ba)) { bm = red[i]; ba = rarg[i]; }
+    red[0] = bm;
+    pick = ba;
+  }
+  __syncthreads();
+  if (!(temperature > 0.f)) {
+    if (tid == 0) next[b] = pick;
+    return;
+  }
+  const float m = red[0], it = 1.f / temperature;
+  float s = 0.f;
+  int lastnz = -1;
+  for (int i = i0; i < i1; i++) {
+    const float e = expf((to_f(l[i]) - m) * it);
+    s += e;
+    if (e > 0.f) lastnz = i;
+  }
+  // inclusive scan of the chunk sums in thread order
+  float incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) wsum[w] = incl;
+  int lnz = lastnz;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lnz = max(lnz, __shfl_xor_sync(0xffffffffu, lnz, o));
+  __syncthreads();
+  if (tid == 0) {
+    float run = 0.f;
+    for (int i = 0; i < SMP_THREADS / 32; i++) {
+      const float t = wsum[i];
+      wsum[i] = run;  // exclusive prefix of warp i
+      run += t;
+    }
+    red[1] = run;  // total
+  }
+  if (lane == 0) rarg[w] = lnz;
+  __syncthreads();
+  if (tid == 0) {
+    int g = -1;
+    for (int i = 0; i < SMP_THREADS / 32; i++) g = max(g, rarg[i]);
+    pick = g;  // fallback: the last index with a nonzero weight
+  }
+  __syncthreads();
+  const float total = red[1];
+  const float target = u[b] * total;
+  __shared__ float excl_s[SMP_THREADS];
+  excl_s[tid] = wsum[w] + (incl - s);  // sum of the chunks before this thread's
+  __syncthreads();
+  // thread t claims the threshold when excl[t] <= target < excl[t+1]
+  // (excl[SMP_THREADS] = +inf): at least one thread does, since excl[0] = 0;
+  // if rounding lets two claim, the smaller index wins; a claimed chunk
+  // whose running sum never passes the threshold (rounding again) yields
+  // its last index with a nonzero weight.  Otherwise (the threshold at the
+  // very top) the last index with a nonzero weight overall is kept.
+  const float ex = excl_s[tid];
+  const float ex_next = tid + 1 < SMP_THREADS ? excl_s[tid + 1] : INFINITY;
+  if (s > 0.f && ex <= target && target < ex_next) {
+    float run = ex;
+    int found = lastnz;
+    for (int i = i0; i < i1; i++) {
+      run += expf((to_f(l[i]) - m) * it);
+      if (run > target) { found = i; break; }
+    }
+    atomicMin(&pick, found);
+  }
+  __syncthreads();
+  if (tid == 0) next[b] = pick;
+}
+
+template <typename T>
+void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, float temperature,
+                   const float* u) {
+  launch_pdl(c, sample_kernel<T>, dim3(B), dim3(SMP_THREADS), 0, next, logits, ld, V, temperature, u);
+}
+template void launch_sample<float>(LaunchCtx&, int32_t*, const float*, int64_t, int, int, float, const float*);
+template void launch_sample<bf16>(LaunchCtx&, int32_t*, const bf16*, int64_t, int, int, float, const float*);

@@ -874,6 +874,10 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
 static int g_pair_mode = -1;  // GPT2_GEMM_PAIR=0 selects the one-SM kernel for every shape
 
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
+  if (gemm_skinny_applies(g)) {  // a few rows: the weights stream once through the CUDA cores
+    launch_gemm_skinny(c, g);
+    return;
+  }
   const int BN = g.N >= 256 ? 256 : 128;
   const int tiles = ((g.N + BN - 1) / BN) * ((g.M + TC_BM - 1) / TC_BM);
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;

@@ -154,6 +154,11 @@ void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
 // bf16 operands on tcgen05 tensor cores, fp32 accumulation in TMEM
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g);
 bool gemm_bf16_init();  // resolves the driver's tensor-map encoder; false on failure
+// M <= 16 rows, both operands K-major, EPI_STORE / EPI_RESIDUAL / EPI_GELU_FWD:
+// the CUDA-core kernel for generation-sized products (launch_gemm_bf16 uses
+// it by itself for such arguments)
+bool gemm_skinny_applies(const GemmArgs& g);
+void launch_gemm_skinny(LaunchCtx& c, const GemmArgs& g);
 
 // ---------------------------------------------------------------- attention
 // qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T]: the logsumexp of the scaled,
@@ -177,6 +182,20 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
                                int C, int NH, float* bias_partial);
+
+// ---------------------------------------------------------------- decode
+// Generation with the key/value cache qkv [B, T_, 3C] (row t of sequence b:
+// [q | k | v] of position t): y[b*ldy + h*hs + d] = the attention of the
+// query of row pos over rows 0..pos (head h, natural-log softmax, fp32).
+template <typename T>
+void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int B, int T_, int C, int NH,
+                             int pos);
+// next[b] = the token drawn from logits[b*ld + 0..V-1]: inverse-CDF sampling
+// of softmax(l / temperature) at the uniform u[b] (temperature <= 0: the
+// first index of the largest score).
+template <typename T>
+void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, float temperature,
+                   const float* u);
 
 // Record the message gpt2_last_error(NULL) returns (entry points without a
 // model handle).
