@@ -465,8 +465,10 @@ def run_decode(args, world, rank, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     e0.record(stream)
+    h0 = time.perf_counter()
     for i in range(W, W + K):
         m.decode_step(seq[i], P - 1 + i, d["temperature"], u_d[i], out=seq[i + 1])
+    host_ms = (time.perf_counter() - h0) * 1e3 / K  # time to enqueue one step
     e1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -494,7 +496,8 @@ def run_decode(args, world, rank, local):
                e2e=dict(value=round(e2e, 1), unit="tokens/s", h2d_bytes_per_step=round(B * P * 4 / K + B * 4, 1),
                         d2h_bytes_per_step=B * 4,
                         note="Model.generate: prefill forward + %d decode steps, prompt in and tokens out" % K),
-               gpu_launches=launches, clocks=clk, kernels_ms_per_step=breakdown)
+               gpu_launches=launches, clocks=clk, kernels_ms_per_step=breakdown,
+               host_enqueue_ms_per_step=round(host_ms, 4))
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = decode_cpu_baseline(d)
     m.close()

@@ -121,6 +121,14 @@ struct gpt2_model {
   // generation: one row per sequence (the key/value cache is qkv above)
   float *dec_x, *dec_mid, *dec_mean, *dec_rstd;
   char *dec_ln, *dec_y, *dec_fcd, *dec_fcg, *dec_logits;
+  int32_t *dec_tok, *dec_next;  // the step's input ids and drawn ids [B]
+  float *dec_u, *dec_temp;      // the step's uniforms [B] and temperature
+  int* dec_pos;                 // the step's position
+  // the decode step as a CUDA graph (its launches do not depend on the step)
+  cudaStream_t dec_cap = nullptr;
+  cudaGraph_t dec_graph = nullptr;
+  cudaGraphExec_t dec_exec = nullptr;
+  int64_t dec_graph_launches = 0;
   bool have_fwd = false, fwd_targets = false;
   bool have_cache = false;  // qkv holds keys / values of the current weights
   bool have_dec = false;    // dec_logits holds a decode step's scores
@@ -283,6 +291,11 @@ size_t layout(gpt2_model* m, char* base) {
   m->dec_fcd = b.take<char>((int64_t)m->B * 4 * C * a);
   m->dec_fcg = b.take<char>((int64_t)m->B * 4 * C * a);
   m->dec_logits = b.take<char>((int64_t)m->B * m->Vp * a);
+  m->dec_tok = b.take<int32_t>(m->B);
+  m->dec_next = b.take<int32_t>(m->B);
+  m->dec_u = b.take<float>(m->B);
+  m->dec_temp = b.take<float>(1);
+  m->dec_pos = b.take<int>(1);
   m->err = b.take<int>(1);
   return b.off + 256;
 }
@@ -392,9 +405,12 @@ void forward_layers(gpt2_model* m, LaunchCtx& c, bool with_targets) {
 // pos of each layer's qkv; its attention reads rows 0..pos; the final
 // LayerNorm output times wte^T gives the row's scores, from which the next
 // token is drawn.
+// Inputs in dec_tok, dec_pos, dec_temp, dec_u; the drawn ids go to
+// dec_next.  dev_rows: the new cache row is located on the device (from
+// dec_pos), so that the launches do not depend on the step (graph capture);
+// otherwise at row `pos`.
 template <typename ActT>
-void decode_layers(gpt2_model* m, LaunchCtx& c, const int32_t* tok, int pos, float temperature,
-                   const float* u, int32_t* next) {
+void decode_layers(gpt2_model* m, LaunchCtx& c, bool dev_rows, int pos) {
   const int M = m->M, C = m->C, L = m->L, B = m->B, T = m->T, NH = m->NH;
   const bool f32 = !m->bf;
   const int64_t WS = sizeof(ActT) == 2 ? 2 : 4;
@@ -408,7 +424,7 @@ void decode_layers(gpt2_model* m, LaunchCtx& c, const int32_t* tok, int pos, flo
   const double ln_bytes = (double)B * C * (4 + a) + 8.0 * B;
   {
     ProfScope ps(m, PC_ENC_FWD, 12.0 * B * C);
-    launch_encoder_fwd(c, x, tok, m->P(WTE), m->P(WPE) + (int64_t)pos * C, B, 1, C, m->V);
+    launch_decode_embed(c, x, m->dec_tok, m->P(WTE), m->P(WPE), m->dec_pos, B, C, m->V);
   }
   for (int l = 0; l < L; l++) {
     ActT* qkv = m->A<ActT>(m->qkv, l, (int64_t)M * 3 * C);
@@ -418,13 +434,17 @@ void decode_layers(gpt2_model* m, LaunchCtx& c, const int32_t* tok, int pos, flo
     }
     // row pos of sequence b sits at qkv + (b*T + pos)*3C: rows of stride T*3C
     GemmArgs g = gemm(B, 3 * C, C, ln, C, true, w(QKVW, (int64_t)l * 3 * C * C), C, true, EPI_STORE,
-                      qkv + (int64_t)pos * 3 * C, (int64_t)T * 3 * C, f32);
+                      dev_rows ? qkv : qkv + (int64_t)pos * 3 * C, (int64_t)T * 3 * C, f32);
     g.bias = m->P(QKVB) + (int64_t)l * 3 * C;
+    if (dev_rows) {
+      g.out_row = m->dec_pos;
+      g.out_row_stride = 3 * (int64_t)C;
+    }
     run_gemm(m, c, g, GS_QKV);
     {
       // the cached keys and values of rows 0..pos read once, the output row written
       ProfScope ps(m, PC_DEC_ATTN, a * ((double)B * (pos + 1) * 2 * C + 2.0 * B * C));
-      launch_attention_decode<ActT>(c, y, C, qkv, B, T, C, NH, pos);
+      launch_attention_decode<ActT>(c, y, C, qkv, B, T, C, NH, m->dec_pos);
     }
     g = gemm(B, C, C, y, C, true, w(ATTPROJW, (int64_t)l * C * C), C, true, EPI_RESIDUAL, mid, C, true);
     g.bias = m->P(ATTPROJB) + (int64_t)l * C;
@@ -453,7 +473,7 @@ void decode_layers(gpt2_model* m, LaunchCtx& c, const int32_t* tok, int pos, flo
   run_gemm(m, c, gemm(B, m->Vp, C, ln, C, true, m->W(WTE), C, true, EPI_STORE, logits, m->Vp, f32), GS_HEAD);
   {
     ProfScope ps(m, PC_SAMPLE, a * (double)B * m->V);
-    launch_sample<ActT>(c, next, logits, m->Vp, B, m->V, temperature, u);
+    launch_sample<ActT>(c, m->dec_next, logits, m->Vp, B, m->V, m->dec_temp, m->dec_u);
   }
 }
 
@@ -672,6 +692,9 @@ void gpt2_free(gpt2_model* m) {
   cudaStreamSynchronize(m->stream);
   for (auto& p : m->prof.pending) { cudaEventDestroy(p.second.first); cudaEventDestroy(p.second.second); }
   for (cudaEvent_t e : m->prof.pool) cudaEventDestroy(e);
+  if (m->dec_exec) cudaGraphExecDestroy(m->dec_exec);
+  if (m->dec_graph) cudaGraphDestroy(m->dec_graph);
+  if (m->dec_cap) cudaStreamDestroy(m->dec_cap);
   cudaFree(m->block);
   delete m;
 }
@@ -925,6 +948,40 @@ int gpt2_load_checkpoint(gpt2_model* m, const char* path, int32_t* step) {
   return GPT2_OK;
 }
 
+// Record the decode step's launches once into a CUDA graph (on a private
+// stream); they read the step's inputs from the model's buffers.
+static int capture_decode(gpt2_model* m) {
+  cudaError_t e = cudaSuccess;
+  if (!m->dec_cap) e = cudaStreamCreateWithFlags(&m->dec_cap, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_decode_step: stream");
+  LaunchCtx c = ctx(m);
+  c.stream = m->dec_cap;
+  const int64_t l0 = m->launches;
+  e = cudaStreamBeginCapture(m->dec_cap, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_decode_step: begin capture");
+  if (m->bf) decode_layers<bf16>(m, c, true, 0);
+  else decode_layers<float>(m, c, true, 0);
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(m->dec_cap, &graph);
+  const int64_t n = m->launches - l0;
+  m->launches = l0;  // counted when the graph is launched
+  if (e != cudaSuccess || c.host_fail || !graph) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return fail(m, GPT2_ERR_CUDA, "gpt2_decode_step: capturing the step failed");
+  }
+  cudaGraphExec_t exec = nullptr;
+  e = cudaGraphInstantiate(&exec, graph, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return cuda_fail(m, e, "gpt2_decode_step: graph instantiation");
+  }
+  m->dec_graph = graph;
+  m->dec_exec = exec;
+  m->dec_graph_launches = n;
+  return GPT2_OK;
+}
+
 int gpt2_decode_step(gpt2_model* m, const int32_t* tokens, int32_t pos, float temperature,
                      const float* uniforms, int32_t* next_tokens) {
   if (!m) return GPT2_ERR_ARG;
@@ -935,14 +992,34 @@ int gpt2_decode_step(gpt2_model* m, const int32_t* tokens, int32_t pos, float te
     return fail(m, GPT2_ERR_STATE, "gpt2_decode_step: no key/value cache of the current weights (run gpt2_forward first)");
   cudaSetDevice(m->device);
   LaunchCtx c = ctx(m);
-  if (m->bf) decode_layers<bf16>(m, c, tokens, pos, temperature, uniforms, next_tokens);
-  else decode_layers<float>(m, c, tokens, pos, temperature, uniforms, next_tokens);
+  launch_decode_inputs(c, m->dec_tok, tokens, m->dec_u, uniforms, m->dec_pos, pos, m->dec_temp, temperature, m->B);
+  int rc = after_launches(m, c, "gpt2_decode_step");
+  if (rc) return rc;
+  // replayed as one graph unless kernel classes are being timed (events per
+  // launch) or the few-row matmul does not apply (more than 16 sequences)
+  const bool graph = m->prof.mask == 0 && (!m->bf || m->B <= 16);
+  if (graph) {
+    if (!m->dec_exec) {
+      rc = capture_decode(m);
+      if (rc) return rc;
+    }
+    cudaError_t e = cudaGraphLaunch(m->dec_exec, m->stream);
+    if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_decode_step: graph launch");
+    m->launches += m->dec_graph_launches;
+  } else {
+    if (m->bf) decode_layers<bf16>(m, c, false, pos);
+    else decode_layers<float>(m, c, false, pos);
+    rc = after_launches(m, c, "gpt2_decode_step");
+    if (rc) return rc;
+  }
+  cudaError_t e = cudaMemcpyAsync(next_tokens, m->dec_next, sizeof(int32_t) * m->B, cudaMemcpyDeviceToDevice, m->stream);
+  if (e != cudaSuccess) return cuda_fail(m, e, "gpt2_decode_step: copying the drawn ids");
   // row pos of the cache now holds the new position: the activations of the
   // last forward no longer match each other
   m->have_fwd = false;
   m->fwd_targets = false;
   m->have_dec = true;
-  return after_launches(m, c, "gpt2_decode_step");
+  return GPT2_OK;
 }
 
 int gpt2_copy_decode_logits_out(gpt2_model* m, float* dst) {

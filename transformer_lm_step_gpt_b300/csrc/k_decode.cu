@@ -66,55 +66,80 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t dec_cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void dec_cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
+}
+__device__ __forceinline__ float dec_ld_cluster(const float* p, uint32_t rank) {
+  uint32_t a;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+
 // y[b, h*hs + d] = sum_{j <= pos} p_j v_j[d],  p = softmax_j(q . k_j * scale),
 // q = row pos of qkv[b] (part q), k_j / v_j = row j (parts k / v), head h.
-// One CTA per (b, h).  Scores: thread per key, kept in shared memory
-// (pos + 1 floats); the weighted sum: whole value rows per warp load, the
-// warps' partial sums added in warp order.
-template <typename T>
+// A cluster of KS CTAs per (b, h), CTA r taking the contiguous key range
+// [r*kr, (r+1)*kr) of 0..pos: its scores (thread per key, kept in shared
+// memory), their maximum m_r, sum s_r of exp(score - m_r) and the weighted
+// sum o_r of the value rows (whole rows per warp load, warps added in
+// order).  The first CTA of the cluster then combines the ranks in order
+// through distributed shared memory: m = max m_r, y = sum_r e^(m_r - m) o_r
+// / sum_r e^(m_r - m) s_r -- the softmax over all keys, split (the
+// split-softmax identity), with a result that does not depend on scheduling.
+template <typename T, int HS>
 __global__ void __launch_bounds__(DEC_THREADS)
-    attn_decode_kernel(T* y, int64_t ldy, const T* qkv, int T_, int C, int NH, int pos, float scale) {
+    attn_decode_kernel(T* y, int64_t ldy, const T* qkv, int T_, int C, int NH, const int* pos_dev, float scale,
+                       int KS) {
   pdl_trigger();
   extern __shared__ float dsm[];
-  const int hs = C / NH;
+  constexpr int hs = HS;
   float* qs = dsm;              // [hs]
   float* red = qs + hs;         // [32]
-  float* sc = red + 32;         // [pos + 1]
-  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
+  float* part = red + 32;       // [hs + 2]: this rank's o (hs), m, s
+  float* sc = part + hs + 2;    // [kr], later the warps' partial sums (8 x hs)
+  const uint32_t rank = KS > 1 ? dec_cluster_rank() : 0u;
+  const int bh = blockIdx.x / KS, b = bh / NH, h = bh % NH;
   const int tid = threadIdx.x;
   const int64_t C3 = 3 * (int64_t)C;
   const T* base = qkv + (int64_t)b * T_ * C3;
   pdl_wait();
+  const int pos = *pos_dev;
+  const int kr = (pos + 1 + KS - 1) / KS;
+  const int j0 = (int)rank * kr, j1 = min(pos + 1, j0 + kr);  // this rank's keys [j0, j1); may be empty
   for (int d = tid; d < hs; d += DEC_THREADS) qs[d] = to_f(base[(int64_t)pos * C3 + h * hs + d]);
   __syncthreads();
   float mx = -INFINITY;
-  for (int j = tid; j <= pos; j += DEC_THREADS) {
+  for (int j = j0 + tid; j < j1; j += DEC_THREADS) {
     const T* k = base + (int64_t)j * C3 + C + h * hs;
-    float s = 0.f;
-    for (int d = 0; d < hs; d += 8) {
-      float f[8];
-      load8f<T>(k + d, f);
+    float f[HS];  // the whole key row in flight at once
 #pragma unroll
-      for (int i = 0; i < 8; i++) s = fmaf(qs[d + i], f[i], s);
-    }
+    for (int d = 0; d < HS; d += 8) load8f<T>(k + d, f + d);
+    float s = 0.f;
+#pragma unroll
+    for (int d = 0; d < HS; d++) s = fmaf(qs[d], f[d], s);
     s *= scale;
-    sc[j] = s;
+    sc[j - j0] = s;
     mx = fmaxf(mx, s);
   }
   mx = block_max<DEC_THREADS>(mx, red);
   float sum = 0.f;
-  for (int j = tid; j <= pos; j += DEC_THREADS) {
-    const float e = expf(sc[j] - mx);
-    sc[j] = e;
+  for (int j = j0 + tid; j < j1; j += DEC_THREADS) {
+    const float e = j1 > j0 ? expf(sc[j - j0] - mx) : 0.f;
+    sc[j - j0] = e;
     sum += e;
   }
   sum = block_sum<DEC_THREADS>(sum, red);  // its barriers also publish sc[]
-  const float inv = 1.f / sum;
   // weighted sum of the values: a key's row of hs values is read by LPK =
   // hs/8 lanes (16 bytes each), so a warp reads KPW = 32/LPK whole rows per
-  // load; warp w takes keys w*KPW + r*8*KPW + (lane / LPK), four rows per
-  // lane in flight, and keeps 8 partial sums (its lane's 8 dimensions)
-  const int LPK = hs / 8, KPW = 32 / LPK;
+  // load; warp w takes keys j0 + w*KPW + r*8*KPW + (lane / LPK), four rows
+  // per lane in flight, and keeps 8 partial sums (its lane's 8 dimensions)
+  constexpr int LPK = HS / 8, KPW = 32 / LPK;
   const int warp = tid >> 5, lane = tid & 31;
   const int kl = lane / LPK, d0 = (lane % LPK) * 8;
   float acc[8];
@@ -122,22 +147,22 @@ __global__ void __launch_bounds__(DEC_THREADS)
   for (int i = 0; i < 8; i++) acc[i] = 0.f;
   const T* vbase = base + 2 * C + h * hs + d0;
   const int step = (DEC_THREADS / 32) * KPW;
-  int j = warp * KPW + kl;
-  for (; j + 3 * step <= pos; j += 4 * step) {
+  int j = j0 + warp * KPW + kl;
+  for (; j + 3 * step < j1; j += 4 * step) {
     float f[4][8];
 #pragma unroll
     for (int u = 0; u < 4; u++) load8f<T>(vbase + (int64_t)(j + u * step) * C3, f[u]);
 #pragma unroll
     for (int u = 0; u < 4; u++) {
-      const float p = sc[j + u * step];
+      const float p = sc[j + u * step - j0];
 #pragma unroll
       for (int i = 0; i < 8; i++) acc[i] = fmaf(p, f[u][i], acc[i]);
     }
   }
-  for (; j <= pos; j += step) {
+  for (; j < j1; j += step) {
     float f[8];
     load8f<T>(vbase + (int64_t)j * C3, f);
-    const float p = sc[j];
+    const float p = sc[j - j0];
 #pragma unroll
     for (int i = 0; i < 8; i++) acc[i] = fmaf(p, f[i], acc[i]);
   }
@@ -155,26 +180,52 @@ __global__ void __launch_bounds__(DEC_THREADS)
   if (tid < hs) {
     float r = 0.f;
     for (int w = 0; w < DEC_THREADS / 32; w++) r += sc[w * hs + tid];
-    y[(int64_t)b * ldy + h * hs + tid] = from_f<T>(r * inv);
+    part[tid] = r;
   }
+  if (tid == 0) { part[hs] = mx; part[hs + 1] = sum; }
+  if (KS == 1) {
+    __syncthreads();
+    if (tid < hs) y[(int64_t)b * ldy + h * hs + tid] = from_f<T>(part[tid] / part[hs + 1]);
+    return;
+  }
+  dec_cluster_sync();  // every rank's (o, m, s) in its shared memory
+  if (rank == 0 && tid < hs) {
+    float m = -INFINITY;
+    for (int q = 0; q < KS; q++) m = fmaxf(m, dec_ld_cluster(part + hs, (uint32_t)q));
+    float o = 0.f, l = 0.f;
+    for (int q = 0; q < KS; q++) {
+      const float mq = dec_ld_cluster(part + hs, (uint32_t)q);
+      const float f = mq == -INFINITY ? 0.f : expf(mq - m);  // a rank without keys adds nothing
+      o += f * dec_ld_cluster(part + tid, (uint32_t)q);
+      l += f * dec_ld_cluster(part + hs + 1, (uint32_t)q);
+    }
+    y[(int64_t)b * ldy + h * hs + tid] = from_f<T>(o / l);
+  }
+  dec_cluster_sync();  // the first rank has read the others: they may exit
 }
 
 template <typename T>
 void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int B, int T_, int C, int NH,
-                             int pos) {
+                             const int* pos) {
   const int hs = C / NH;
-  // scores (pos + 1) and, later, the warps' partial sums (8 x hs) share one array
-  const size_t smem = sizeof(float) * (hs + 32 + std::max(pos + 1, (DEC_THREADS / 32) * hs));
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(attn_decode_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
-    attr = true;
-  }
-  launch_pdl(c, attn_decode_kernel<T>, dim3(B * NH), dim3(DEC_THREADS), smem, y, ldy, qkv, T_, C, NH, pos,
-             1.f / sqrtf((float)hs));
+  // split the keys over a cluster of up to 8 CTAs (fixed by the cache size,
+  // so that the launch does not depend on the position)
+  const int KS = std::max(1, std::min(8, (T_ + 63) / 64));
+  const int kr = (T_ + KS - 1) / KS;  // the most keys a rank can get
+  const size_t smem = sizeof(float) * (hs + 32 + hs + 2 + std::max(kr, (DEC_THREADS / 32) * hs));
+  auto kern = hs == 16 ? attn_decode_kernel<T, 16>
+              : hs == 32 ? attn_decode_kernel<T, 32>
+              : hs == 64 ? attn_decode_kernel<T, 64>
+                         : attn_decode_kernel<T, 128>;
+  const float scale = 1.f / sqrtf((float)hs);
+  if (KS > 1)
+    launch_pdl_cluster(c, kern, dim3(B * NH * KS), dim3(DEC_THREADS), smem, KS, y, ldy, qkv, T_, C, NH, pos, scale,
+                       KS);
+  else
+    launch_pdl(c, kern, dim3(B * NH), dim3(DEC_THREADS), smem, y, ldy, qkv, T_, C, NH, pos, scale, KS);
 }
-template void launch_attention_decode<float>(LaunchCtx&, float*, int64_t, const float*, int, int, int, int, int);
-template void launch_attention_decode<bf16>(LaunchCtx&, bf16*, int64_t, const bf16*, int, int, int, int, int);
+template void launch_attention_decode<float>(LaunchCtx&, float*, int64_t, const float*, int, int, int, int, const int*);
+template void launch_attention_decode<bf16>(LaunchCtx&, bf16*, int64_t, const bf16*, int, int, int, int, const int*);
 
 // One CTA per row b of logits [B, ld]: the next token from the first V
 // scores (inverse-CDF sampling of the softmax at `temperature` with the
@@ -184,7 +235,7 @@ template void launch_attention_decode<bf16>(LaunchCtx&, bf16*, int64_t, const bf
 // and the thread whose chunk holds the threshold u * sum walks it again.
 template <typename T>
 __global__ void __launch_bounds__(SMP_THREADS)
-    sample_kernel(int32_t* next, const T* logits, int64_t ld, int V, float temperature, const float* u) {
+    sample_kernel(int32_t* next, const T* logits, int64_t ld, int V, const float* temp_dev, const float* u) {
   pdl_trigger();
   __shared__ float red[32];
   __shared__ float wsum[SMP_THREADS / 32];
@@ -192,6 +243,7 @@ __global__ void __launch_bounds__(SMP_THREADS)
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const T* l = logits + (int64_t)b * ld;
   pdl_wait();
+  const float temperature = *temp_dev;
   const int cs = (V + SMP_THREADS - 1) / SMP_THREADS;
   const int i0 = min(tid * cs, V), i1 = min(i0 + cs, V);
   // largest score; its first index
@@ -287,9 +339,53 @@ __global__ void __launch_bounds__(SMP_THREADS)
 }
 
 template <typename T>
-void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, float temperature,
+void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, const float* temperature,
                    const float* u) {
   launch_pdl(c, sample_kernel<T>, dim3(B), dim3(SMP_THREADS), 0, next, logits, ld, V, temperature, u);
 }
-template void launch_sample<float>(LaunchCtx&, int32_t*, const float*, int64_t, int, int, float, const float*);
-template void launch_sample<bf16>(LaunchCtx&, int32_t*, const bf16*, int64_t, int, int, float, const float*);
+template void launch_sample<float>(LaunchCtx&, int32_t*, const float*, int64_t, int, int, const float*, const float*);
+template void launch_sample<bf16>(LaunchCtx&, int32_t*, const bf16*, int64_t, int, int, const float*, const float*);
+
+// x[b, :] = wte[tok[b], :] + wpe[pos, :]: one CTA per row, C/4 threads.
+__global__ void decode_embed_kernel(float* x, const int32_t* tok, const float* wte, const float* wpe,
+                                    const int* pos_dev, int C, int V, int* err) {
+  pdl_trigger();
+  pdl_wait();
+  const int b = blockIdx.x;
+  int id = tok[b];
+  if (id < 0 || id >= V) {
+    if (threadIdx.x == 0) record_error(err, DEVERR_TOKEN);
+    id = 0;
+  }
+  const int pos = *pos_dev;
+  for (int c4 = threadIdx.x; c4 < C / 4; c4 += blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(wte + (int64_t)id * C)[c4];
+    const float4 e = reinterpret_cast<const float4*>(wpe + (int64_t)pos * C)[c4];
+    reinterpret_cast<float4*>(x + (int64_t)b * C)[c4] = make_float4(a.x + e.x, a.y + e.y, a.z + e.z, a.w + e.w);
+  }
+}
+
+void launch_decode_embed(LaunchCtx& c, float* x, const int32_t* tok, const float* wte, const float* wpe,
+                         const int* pos, int B, int C, int V) {
+  launch_pdl(c, decode_embed_kernel, dim3(B), dim3(std::min(256, C / 4)), 0, x, tok, wte, wpe, pos, C, V, c.err);
+}
+
+__global__ void decode_inputs_kernel(int32_t* tok_dst, const int32_t* tok_src, float* u_dst, const float* u_src,
+                                     int* pos_dst, int pos, float* temp_dst, float temperature, int B) {
+  pdl_trigger();
+  pdl_wait();
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    tok_dst[i] = tok_src[i];
+    u_dst[i] = u_src[i];
+  }
+  if (threadIdx.x == 0) {
+    *pos_dst = pos;
+    *temp_dst = temperature;
+  }
+}
+
+void launch_decode_inputs(LaunchCtx& c, int32_t* tok_dst, const int32_t* tok_src, float* u_dst, const float* u_src,
+                          int* pos_dst, int pos, float* temp_dst, float temperature, int B) {
+  launch_pdl(c, decode_inputs_kernel, dim3(1), dim3(128), 0, tok_dst, tok_src, u_dst, u_src, pos_dst, pos, temp_dst,
+             temperature, B);
+}

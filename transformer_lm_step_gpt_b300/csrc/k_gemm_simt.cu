@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
     }
     __syncthreads();
   }
-  float* out = static_cast<float*>(g.out);
+  const int64_t orow = g.out_row ? (int64_t)(*g.out_row) * g.out_row_stride : 0;
+  float* out = static_cast<float*>(g.out) + orow;
 #pragma unroll
   for (int i = 0; i < 4; i++) {
     const int m = m0 + ty * 4 + i;
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(GemmArgs g) {
         case EPI_GELU_FWD: {
           v = epi_apply(g, m, n, v);
           out[o] = gelu_grad_f(v);
-          static_cast<float*>(g.out2)[o] = gelu_f(v);
+          static_cast<float*>(g.out2)[orow + o] = gelu_f(v);
         } break;
         case EPI_RESIDUAL: out[o] = static_cast<const float*>(g.aux)[o] + epi_apply(g, m, n, v); break;
         case EPI_MUL_AUX: out[o] = v * static_cast<const float*>(g.aux)[o]; break;

@@ -871,11 +871,187 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
   }
 }
 
+// ====================================================================== few-row products
+// out[m, n] = sum_k A[m, k] W[n, k] (+ epilogue) for M <= 16 rows of A (one
+// row per sequence while generating).  The operands swap roles: a CTA owns
+// 128 weight rows n as the tcgen05 M dimension and the (up to 16) rows of A
+// form the N = 16 dimension, so the MMA is M = 128, N = 16 and no tensor-core
+// work is spent on padding rows; the weights stream once through TMA (the
+// product is bound by HBM).  When there are few 128-row tiles, K is split
+// over a cluster of up to 8 CTAs; their fp32 partials are added by the first
+// CTA of the cluster through distributed shared memory, in rank order, so the
+// sum does not depend on scheduling.  Thread n of the epilogue owns weight row
+// n and writes out[m, n] for every m: consecutive lanes, consecutive columns.
+#define RT_STAGES 6
+#define RT_XROWS 16
+#define RT_WBYTES (TC_BM * 128)     // 128 weight rows x 64 bf16
+#define RT_XBYTES (RT_XROWS * 128)  // 16 rows of A x 64 bf16
+#define RT_THREADS 128
+#define RT_SMEM (1024 + RT_STAGES * (RT_WBYTES + RT_XBYTES) + TC_BM * RT_XROWS * 4 + 256)
+#define RT_MAX_CLUSTER 8
+
+__device__ __forceinline__ uint32_t cluster_size() {
+  uint32_t n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(RT_THREADS, 1)
+    gemm_rows_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
+                        const GemmArgs g, int ktiles, int kps, int* err) {
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sW = sm;                                                   // [STAGES][128 x 64]
+  uint8_t* sX = sW + RT_STAGES * RT_WBYTES;                           // [STAGES][16 x 64]
+  float* red = reinterpret_cast<float*>(sX + RT_STAGES * RT_XBYTES);  // [16][128] partial sums
+  uint64_t* full = reinterpret_cast<uint64_t*>(red + TC_BM * RT_XROWS);
+  uint64_t* empty = full + RT_STAGES;
+  uint64_t* done = empty + RT_STAGES;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  const uint32_t S = cluster_size(), rank = cluster_rank();
+  const int n0 = (int)(blockIdx.x / S) * TC_BM;
+  const int kt0 = (int)rank * kps;
+  const int nk = max(0, min(ktiles, kt0 + kps) - kt0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RT_STAGES; s++) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    mbar_init(done, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tw);
+    tma_prefetch_desc(&tx);
+  }
+  if (warp == 1) { tmem_alloc(tslot, 32); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tslot;
+  pdl_wait();
+  if (warp == 0 && lane == 0) {  // TMA producer
+    for (int i = 0; i < nk; i++) {
+      const int s = i % RT_STAGES;
+      if (i >= RT_STAGES) mbar_wait(&empty[s], (uint32_t)((i / RT_STAGES) - 1) & 1u, err);
+      mbar_arrive_expect_tx(&full[s], RT_WBYTES + RT_XBYTES);
+      tma_load_2d(sW + s * RT_WBYTES, &tw, &full[s], (kt0 + i) * TC_BK, n0);
+      tma_load_2d(sX + s * RT_XBYTES, &tx, &full[s], (kt0 + i) * TC_BK, 0);
+    }
+  } else if (warp == 1 && lane == 0) {  // MMA issuer
+    const uint32_t idesc = tc_idesc_bf16(TC_BM, RT_XROWS, false, false);
+    for (int i = 0; i < nk; i++) {
+      const int s = i % RT_STAGES;
+      mbar_wait(&full[s], (uint32_t)(i / RT_STAGES) & 1u, err);
+      tc_fence_after();
+      const uint32_t a = smem_u32(sW + s * RT_WBYTES), b = smem_u32(sX + s * RT_XBYTES);
+#pragma unroll
+      for (int kk = 0; kk < TC_BK / 16; kk++)
+        tc_mma_bf16(tm, sw128_desc(a + kk * 32, 16, 1024), sw128_desc(b + kk * 32, 16, 1024), idesc,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&empty[s]);
+    }
+    tc_commit(done);  // with no MMA issued it arrives at once
+  }
+  __syncwarp();
+  mbar_wait(done, 0, err);
+  tc_fence_after();
+  float acc[RT_XROWS];
+  const int nl = warp * 32 + lane;  // this thread's weight row within the tile
+  if (nk > 0) {
+    uint32_t r[32];
+    tmem_ld32(tm + ((uint32_t)(warp * 32) << 16), r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int m = 0; m < RT_XROWS; m++) acc[m] = __uint_as_float(r[m]);
+  } else {
+#pragma unroll
+    for (int m = 0; m < RT_XROWS; m++) acc[m] = 0.f;
+  }
+  if (S > 1) {
+#pragma unroll
+    for (int m = 0; m < RT_XROWS; m++) red[m * TC_BM + nl] = acc[m];
+    cluster_sync();  // every rank's partial sums are in its shared memory
+    if (rank == 0) {
+      for (uint32_t q = 1; q < S; q++) {
+        const uint32_t base = cluster_addr(red, q);
+#pragma unroll
+        for (int m = 0; m < RT_XROWS; m++) acc[m] += ld_cluster_f32(base + (uint32_t)(m * TC_BM + nl) * 4u);
+      }
+    }
+    cluster_sync();  // the first CTA has read them: the others may exit
+  }
+  const int n = n0 + nl;
+  if (rank == 0 && n < g.N) {
+    const float bias = g.bias ? g.bias[n] : 0.f;
+    const int64_t orow = g.out_row ? (int64_t)(*g.out_row) * g.out_row_stride : 0;
+#pragma unroll
+    for (int m = 0; m < RT_XROWS; m++) {
+      if (m >= g.M) break;
+      const float x = acc[m] + bias;
+      const int64_t o = (int64_t)m * g.ldo + n;
+      if (g.epi == EPI_RESIDUAL) {
+        static_cast<float*>(g.out)[orow + o] = static_cast<const float*>(g.aux)[o] + x;
+      } else if (g.epi == EPI_GELU_FWD) {
+        float gl, gd;
+        gelu_and_grad_hw(x, gl, gd);
+        static_cast<bf16*>(g.out)[orow + o] = __float2bfloat16_rn(gd);
+        static_cast<bf16*>(g.out2)[orow + o] = __float2bfloat16_rn(gl);
+      } else if (g.out_f32) {
+        static_cast<float*>(g.out)[orow + o] = x;
+      } else {
+        static_cast<bf16*>(g.out)[orow + o] = __float2bfloat16_rn(x);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) { tc_fence_after(); tmem_dealloc(tm, 32); }
+}
+
+bool gemm_rows_applies(const GemmArgs& g) {
+  return g.M >= 1 && g.M <= RT_XROWS && g.a_kmajor && g.b_kmajor && !g.colsum_out &&
+         (g.epi == EPI_STORE || g.epi == EPI_RESIDUAL || g.epi == EPI_GELU_FWD);
+}
+
+void launch_gemm_rows(LaunchCtx& c, const GemmArgs& g) {
+  CUtensorMap tw, tx;
+  bool ok = make_tmap(&tw, g.B, false, g.K, g.N, g.ldb, 64, TC_BM);
+  ok = ok && make_tmap(&tx, g.A, false, g.K, g.M, g.lda, 64, RT_XROWS);
+  if (!ok) {
+    fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
+    c.host_fail = 1;
+    return;
+  }
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(gemm_rows_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, RT_SMEM);
+    attr = true;
+  }
+  const int ntiles = (g.N + TC_BM - 1) / TC_BM;
+  const int ktiles = (g.K + TC_BK - 1) / TC_BK;
+  // split K so that the clusters cover the SMs; no rank without K tiles
+  int S = std::min({RT_MAX_CLUSTER, ktiles, std::max(1, (c.num_sms + ntiles - 1) / ntiles)});
+  const int kps = (ktiles + S - 1) / S;
+  S = (ktiles + kps - 1) / kps;
+  if (S > 1)
+    launch_pdl_cluster(c, gemm_rows_tc_kernel, dim3(ntiles * S), dim3(RT_THREADS), RT_SMEM, S, tw, tx, g, ktiles,
+                       kps, c.err);
+  else
+    launch_pdl(c, gemm_rows_tc_kernel, dim3(ntiles), dim3(RT_THREADS), RT_SMEM, tw, tx, g, ktiles, kps, c.err);
+}
+
 static int g_pair_mode = -1;  // GPT2_GEMM_PAIR=0 selects the one-SM kernel for every shape
 
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
-  if (gemm_skinny_applies(g)) {  // a few rows: the weights stream once through the CUDA cores
-    launch_gemm_skinny(c, g);
+  if (gemm_rows_applies(g)) {  // a few rows of A: the weights stream once, M and N swapped
+    launch_gemm_rows(c, g);
+    return;
+  }
+  if (g.out_row) {  // a device-side output row is a feature of the few-row kernel only
+    c.host_fail = 1;
     return;
   }
   const int BN = g.N >= 256 ? 256 : 128;

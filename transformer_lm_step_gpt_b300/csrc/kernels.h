@@ -148,6 +148,11 @@ struct GemmArgs {
   // the stored (bf16) output over each 32-row block, [ceil(M/32)][N] floats
   // (launch_colsum_reduce adds them up)
   float* colsum_out;
+  // if set (few-row and CUDA-core kernels only): out and out2 start
+  // (*out_row) * out_row_stride elements further, read on the device (the
+  // cache row of a generation step, fixed launch arguments for CUDA graphs)
+  const int* out_row;
+  int64_t out_row_stride;
 };
 // fp32 operands, SIMT FFMA (no TF32)
 void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
@@ -155,10 +160,10 @@ void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g);
 bool gemm_bf16_init();  // resolves the driver's tensor-map encoder; false on failure
 // M <= 16 rows, both operands K-major, EPI_STORE / EPI_RESIDUAL / EPI_GELU_FWD:
-// the CUDA-core kernel for generation-sized products (launch_gemm_bf16 uses
-// it by itself for such arguments)
-bool gemm_skinny_applies(const GemmArgs& g);
-void launch_gemm_skinny(LaunchCtx& c, const GemmArgs& g);
+// the generation-sized products (weights as the 128-row MMA operand, the few
+// rows of A as N = 16; launch_gemm_bf16 uses it by itself for such arguments)
+bool gemm_rows_applies(const GemmArgs& g);
+void launch_gemm_rows(LaunchCtx& c, const GemmArgs& g);
 
 // ---------------------------------------------------------------- attention
 // qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T]: the logsumexp of the scaled,
@@ -187,15 +192,24 @@ bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
 // Generation with the key/value cache qkv [B, T_, 3C] (row t of sequence b:
 // [q | k | v] of position t): y[b*ldy + h*hs + d] = the attention of the
 // query of row pos over rows 0..pos (head h, natural-log softmax, fp32).
+// pos: device int (the position, read by the kernel).
 template <typename T>
 void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int B, int T_, int C, int NH,
-                             int pos);
+                             const int* pos);
 // next[b] = the token drawn from logits[b*ld + 0..V-1]: inverse-CDF sampling
-// of softmax(l / temperature) at the uniform u[b] (temperature <= 0: the
-// first index of the largest score).
+// of softmax(l / *temperature) at the uniform u[b] (*temperature <= 0: the
+// first index of the largest score); temperature: device float.
 template <typename T>
-void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, float temperature,
+void launch_sample(LaunchCtx& c, int32_t* next, const T* logits, int64_t ld, int B, int V, const float* temperature,
                    const float* u);
+// x[b, :] = wte[tok[b], :] + wpe[*pos, :] (ids outside [0, V) set
+// DEVERR_TOKEN and read row 0)
+void launch_decode_embed(LaunchCtx& c, float* x, const int32_t* tok, const float* wte, const float* wpe,
+                         const int* pos, int B, int C, int V);
+// the step's inputs into the model's buffers: tok_dst = tok_src, u_dst =
+// u_src ([B] each), *pos_dst = pos, *temp_dst = temperature
+void launch_decode_inputs(LaunchCtx& c, int32_t* tok_dst, const int32_t* tok_src, float* u_dst, const float* u_src,
+                          int* pos_dst, int pos, float* temp_dst, float temperature, int B);
 
 // Record the message gpt2_last_error(NULL) returns (entry points without a
 // model handle).
