@@ -71,6 +71,14 @@ def lib():
         L.oracle_generate_f64.restype = ctypes.c_int
         L.oracle_sample_f64.argtypes = [_f64p, _i64, ctypes.c_double, ctypes.c_double]
         L.oracle_sample_f64.restype = _i64
+        _u8p = np.ctypeslib.ndpointer(np.uint8, flags="C_CONTIGUOUS")
+        L.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.oracle_e4m3_decode.restype = ctypes.c_double
+        L.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        L.oracle_e4m3_encode.restype = ctypes.c_uint8
+        L.oracle_fp8_quantize.argtypes = [_f32p, _i64, _u8p]
+        L.oracle_fp8_quantize.restype = ctypes.c_float
+        L.oracle_fp8_matmul.argtypes = [_f64p, _u8p, ctypes.c_double, _u8p, ctypes.c_double, vp, _i64, _i64, _i64]
         _lib = L
     return _lib
 
@@ -204,6 +212,36 @@ def sample(logits, temperature, u):
     temperature; greedy for temperature <= 0)."""
     lg = np.ascontiguousarray(logits, np.float64).reshape(-1)
     return int(lib().oracle_sample_f64(lg, lg.size, float(temperature), float(u)))
+
+
+# ---- FP8 (E4M3) with per-tensor scaling -------------------------------------
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().oracle_e4m3_decode(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(x)))
+
+
+def fp8_quantize(x):
+    """(codes uint8 like x, scale s = 448 / max|x|) for a float32 array."""
+    x = np.ascontiguousarray(x, np.float32)
+    q = np.zeros(x.shape, np.uint8)
+    s = lib().oracle_fp8_quantize(x.reshape(-1), x.size, q.reshape(-1))
+    return q, float(np.float32(s))
+
+
+def fp8_matmul(qa, sa, qb, sb, bias=None):
+    """qa [M, K], qb [N, K] uint8 codes -> (dec(qa) dec(qb)^T) / (sa sb) + bias, float64 [M, N]."""
+    qa = np.ascontiguousarray(qa, np.uint8)
+    qb = np.ascontiguousarray(qb, np.uint8)
+    M, K = qa.shape
+    N = qb.shape[0]
+    out = np.zeros((M, N))
+    b = None if bias is None else np.ascontiguousarray(bias, np.float64)
+    lib().oracle_fp8_matmul(out, qa, float(sa), qb, float(sb), _ptr(b), M, N, K)
+    return out
 
 
 # ---- layer primitives (double) -------------------------------------------

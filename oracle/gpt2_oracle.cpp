@@ -696,6 +696,64 @@ int64_t sample_row(const double* l, int64_t V, double temperature, double u) {
   return last;
 }
 
+// ---------------------------------------------------------------- FP8 (E4M3)
+// Lower precision for the matmuls ([QbitAI]: precision can go from fp32 to
+// fp16 or lower).  The 8-bit format is E4M3 as the OCP FP8 specification
+// defines it: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits; a
+// code with exponent field e > 0 is (-1)^s 2^(e-7) (1 + m/8), with e = 0 it
+// is (-1)^s 2^-6 (m/8) (subnormal); S.1111.111 is NaN; there is no infinity,
+// so the largest finite magnitude is 2^8 * 1.75 = 448.
+double e4m3_decode(uint8_t c) {
+  const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return std::numeric_limits<double>::quiet_NaN();
+  const double mag = e == 0 ? std::ldexp((double)m / 8.0, -6) : std::ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sgn ? -mag : mag;
+}
+
+// The code nearest to x (ties to the code with an even mantissa field, i.e.
+// round-half-to-even on the 3-bit mantissa grid); magnitudes above 448
+// saturate to 448 (the "satfinite" conversion); NaN gives NaN.  Written as a
+// search over the 127 non-negative finite codes, which are in increasing
+// order of value.
+uint8_t e4m3_encode(double x) {
+  if (std::isnan(x)) return 0x7F;
+  const uint8_t sgn = std::signbit(x) ? 0x80 : 0x00;
+  const double a = std::fabs(x);
+  if (a >= 448.0) return sgn | 0x7E;
+  uint8_t lo = 0;  // largest code with value <= a
+  for (int c = 1; c <= 0x7E; c++)
+    if (e4m3_decode((uint8_t)c) <= a) lo = (uint8_t)c;
+  const uint8_t hi = (uint8_t)(lo + 1);
+  const double dl = a - e4m3_decode(lo), dh = e4m3_decode(hi) - a;
+  uint8_t c = lo;
+  if (dh < dl || (dh == dl && (hi & 1) == 0)) c = hi;
+  return sgn | c;
+}
+
+// Per-tensor scaling: s = 448 / max|x| (1 when x is all zeros) maps the
+// largest magnitude onto the largest code; q_i = encode(x_i * s) with the
+// product taken in float, as a float32 pipeline computes it.
+float fp8_quantize(const float* x, int64_t n, uint8_t* q) {
+  float amax = 0.f;
+  for (int64_t i = 0; i < n; i++) amax = std::fmax(amax, std::fabs(x[i]));
+  const float s = amax > 0.f ? 448.f / amax : 1.f;
+  for (int64_t i = 0; i < n; i++) q[i] = e4m3_encode((double)(x[i] * s));
+  return s;
+}
+
+// out[m, n] = (sum_k dec(qa[m, k]) dec(qb[n, k])) / (sa sb) (+ bias[n]):
+// the matmul of the two dequantised operands, in double.
+void fp8_matmul(double* out, const uint8_t* qa, double sa, const uint8_t* qb, double sb,
+                const double* bias, int64_t M, int64_t N, int64_t K) {
+#pragma omp parallel for schedule(static)
+  for (int64_t m = 0; m < M; m++)
+    for (int64_t n = 0; n < N; n++) {
+      double acc = 0;
+      for (int64_t k = 0; k < K; k++) acc += e4m3_decode(qa[m * K + k]) * e4m3_decode(qb[n * K + k]);
+      out[m * N + n] = acc / (sa * sb) + (bias ? bias[n] : 0.0);
+    }
+}
+
 // ---------------------------------------------------------------- init RNG
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
@@ -895,6 +953,14 @@ int oracle_generate_f64(const int32_t* cfg8, const double* params, const int32_t
 
 int64_t oracle_sample_f64(const double* logits, int64_t V, double temperature, double u) {
   return sample_row(logits, V, temperature, u);
+}
+
+double oracle_e4m3_decode(uint8_t c) { return e4m3_decode(c); }
+uint8_t oracle_e4m3_encode(double x) { return e4m3_encode(x); }
+float oracle_fp8_quantize(const float* x, int64_t n, uint8_t* q) { return fp8_quantize(x, n, q); }
+void oracle_fp8_matmul(double* out, const uint8_t* qa, double sa, const uint8_t* qb, double sb,
+                       const double* bias, int64_t M, int64_t N, int64_t K) {
+  fp8_matmul(out, qa, sa, qb, sb, bias, M, N, K);
 }
 
 void oracle_adamw_f32(int64_t n, float* p, const float* g, float* m, float* v, float lr,
