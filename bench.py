@@ -25,6 +25,13 @@ Prints ONE JSON line (rank 0).  Keys:
 --impl reference times the CPU oracle itself (the only other implementation
 of this step) on bounded samples of the same workload.
 
+--mode fp8 measures the E4M3 matmuls (gpt2_fp8_matmul) on the five forward
+products of GPT-2 124M at M = B*T = 16384 rows (qkv, attproj, fc, fcproj,
+tied head) with bf16 outputs: value = their total FLOPs / total time
+(each product timed alone with CUDA events, L2 flushed before each), the
+roofline against twice the measured bf16 peak (the nominal fp8 : bf16
+tensor ratio).
+
 --mode decode measures generation with the key/value cache instead: GPT-2
 124M, B=16 sequences, a 512-token prompt per sequence run through one
 forward (the prefill), then one gpt2_decode_step per new token (temperature
@@ -520,6 +527,96 @@ def decode_cpu_baseline(d):
                        "forward (fp64, one thread per sequence), %.1f s" % (n_new, dt))
 
 
+# ---------------------------------------------------------------- fp8 mode
+FP8_METRIC = "GPT-2 124M forward matmuls in FP8 (E4M3, per-tensor scales) TFLOP/s on 1 B300"
+FP8_SHAPES = [("qkv", 2304, 768), ("attproj", 768, 768), ("fc", 3072, 768), ("fcproj", 768, 3072),
+              ("head", 50304, 768)]
+
+
+def run_fp8(args):
+    import numpy as np
+    import torch
+
+    import transformer_lm_step_gpt_b300 as tl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    M = 16384
+    g = torch.Generator(device=dev).manual_seed(5)
+    flush = torch.empty(256 * 2 ** 20, dtype=torch.uint8, device=dev)
+    ops = []
+    for name, N, K in FP8_SHAPES:
+        a = torch.randn((M, K), generator=g, device=dev)
+        w = torch.randn((N, K), generator=g, device=dev) * 0.02
+        qa, sa = tl.fp8_quantize(a)
+        qw, sw = tl.fp8_quantize(w)
+        ops.append((name, N, K, qa, sa, qw, sw))
+    torch.cuda.synchronize()
+    W, Kst = args.warmup, args.steps
+    per = {}
+    clocks = ClockSampler(gpu_uuid(0))
+    clocks.start()
+    for name, N, K, qa, sa, qw, sw in ops:
+        for _ in range(W):
+            tl.fp8_matmul(qa, sa, qw, sw, out_dtype=torch.bfloat16)
+        ms = 0.0
+        for _ in range(Kst):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            tl.fp8_matmul(qa, sa, qw, sw, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms += e0.elapsed_time(e1)
+        per[name] = dict(N=N, K=K, ms=ms / Kst, tflops=2.0 * M * N * K / (ms / Kst / 1e3) / 1e12)
+    clk = clocks.stop()
+    tl.fp8_check()
+    flops = sum(2.0 * M * v["N"] * v["K"] for v in per.values())
+    tot_ms = sum(v["ms"] for v in per.values())
+    value = flops / (tot_ms / 1e3) / 1e12
+    peaks = load_peaks()
+    peak = 2.0 * peaks["bf16"]
+    top = max(per, key=lambda k: per[k]["ms"])
+    # end to end: fp32 activations from pinned host memory, quantised and
+    # multiplied on the device, the bf16 result read back (weights resident)
+    name, N, K, _, _, qw, sw = [o for o in ops if o[0] == "fc"][0]
+    a_h = torch.randn((M, K)).pin_memory()
+    o_h = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(Kst):
+        a_d = a_h.to(dev, non_blocking=True)
+        qa, sa = tl.fp8_quantize(a_d)
+        o_h.copy_(tl.fp8_matmul(qa, sa, qw, sw, out_dtype=torch.bfloat16), non_blocking=True)
+    torch.cuda.synchronize()
+    e2e = 2.0 * M * N * K * Kst / (time.perf_counter() - t0) / 1e12
+    out = dict(metric=FP8_METRIC, value=round(value, 1), unit="TFLOP/s", n_gpus=1, steps=Kst, warmup=W,
+               ms_per_step=round(tot_ms, 4), higher_is_better=True, scaling="weak", vs_baseline=None,
+               dtype="e4m3", data="synthetic: normal activations, N(0, 0.02) weights, quantised with per-tensor scales",
+               config=dict(workload="gpt2-124M-forward-matmuls-M16384-fp8", rows=M, mode="fp8",
+                           products={k: [v["N"], v["K"]] for k, v in per.items()},
+                           l2="flushed (256 MB write) before every timed product"),
+               roofline=dict(bound="tensor", achieved=round(per[top]["tflops"], 1), peak=peak, unit="TFLOP/s",
+                             frac=round(per[top]["tflops"] / peak, 4), traffic=None, kernel="gemm_tc_pair_kernel<F8> (%s)" % top,
+                             peak_source="%s bf16_tflops x 2 (nominal fp8 : bf16 ratio)" % peaks["source"]),
+               e2e=dict(value=round(e2e, 1), unit="TFLOP/s", h2d_bytes_per_step=M * K * 4, d2h_bytes_per_step=M * N * 2,
+                        note="fc shape: fp32 activations in from pinned memory, quantise, matmul, bf16 out"),
+               gpu_launches=len(per) * Kst, clocks=clk,
+               products={k: dict(ms=round(v["ms"], 4), tflops=round(v["tflops"], 1)) for k, v in per.items()})
+    if not args.no_cpu_baseline:
+        import oracle
+        rng = np.random.default_rng(0)
+        qa = rng.integers(0, 0x7E, (8, 768)).astype(np.uint8)
+        qb = rng.integers(0, 0x7E, (768, 768)).astype(np.uint8)
+        t0 = time.perf_counter()
+        oracle.fp8_matmul(qa, 1.0, qb, 1.0)
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = dict(value=2.0 * 8 * 768 * 768 / dt / 1e12, unit="TFLOP/s", cores=oracle.set_threads(0),
+                                   kind="oracle", sample="8 x 768 x 768 product of the oracle's fp8_matmul, %.2f s" % dt)
+    return out
+
+
 # ---------------------------------------------------------------- reference arm
 def run_reference(args, w, world, rank):
     if rank != 0:
@@ -550,7 +647,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["train", "decode"], default="train")
+    ap.add_argument("--mode", choices=["train", "decode", "fp8"], default="train")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -560,6 +657,8 @@ def main(argv=None):
     w = WORKLOADS[args.workload]
     if args.mode == "decode" and args.impl == "ours":
         out = run_decode(args, world, rank, local)
+    elif args.mode == "fp8" and args.impl == "ours":
+        out = run_fp8(args) if rank == 0 else None
     else:
         out = run_reference(args, w, world, rank) if args.impl == "reference" else run_ours(args, w, world, rank, local)
     if out is not None and rank == 0:

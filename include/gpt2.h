@@ -238,6 +238,39 @@ GPT2_API int gpt2_decode_step(gpt2_model* m, const int32_t* tokens, int32_t pos,
  * Synchronises.  GPT2_ERR_STATE before the first decode step. */
 GPT2_API int gpt2_copy_decode_logits_out(gpt2_model* m, float* host_dst);
 
+/* ---------------------------------------------------------------- FP8 matmuls
+ * Lower precision for the matmuls (QbitAI's account of llm.c: precision can
+ * go from fp32 to fp16 or lower).  E4M3 codes (OCP 8-bit float: 1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits, largest finite 448, no
+ * infinity) with one scale per tensor.  These entry points need no
+ * gpt2_model; all pointers are device pointers owned by the caller, all work
+ * is enqueued on cuda_stream (NULL = legacy stream) and nothing is
+ * allocated.
+ *
+ * gpt2_fp8_quantize: x [n] (fp32, or bf16 if x_is_bf16) -> q [n] codes and
+ *   scale[0] = s = 448 / max|x| (1 if x is all zeros; NaN entries are left
+ *   out of the maximum), q[i] = E4M3(x[i] * s) with the product in fp32,
+ *   rounded to nearest (ties to even), saturating at +-448 (NaN -> 0x7F).
+ *   scale points to 2 floats; scale[1] is scratch.  x and q 16-byte aligned.
+ * gpt2_fp8_matmul: out[m, n] = (sum_k E(a[m, k]) E(b[n, k])) /
+ *   (scale_a[0] * scale_b[0]) + bias[n] (bias may be NULL), with E the code's
+ *   value; a [M, K] and b [N, K] row-major codes with row strides lda, ldb
+ *   bytes (multiples of 16, >= K); out [M, N] fp32 (or bf16 if out_is_bf16)
+ *   with row stride ldo elements (16-byte rows); the products accumulate in
+ *   fp32 on the tensor cores (tcgen05 kind::f8f6f4).  scale_a / scale_b are
+ *   the scale[0] words of the two quantisations (device).
+ * gpt2_fp8_check: synchronises cuda_stream and reports a bounded device
+ *   wait of these entry points that expired (GPT2_ERR_TIMEOUT), then clears it.
+ * Errors: GPT2_ERR_ARG (NULL pointer, size below 1, misaligned pointer or
+ * stride), GPT2_ERR_CUDA (a launch failed); gpt2_last_error(NULL) has the text. */
+GPT2_API int gpt2_fp8_quantize(const void* x, int32_t x_is_bf16, int64_t n, uint8_t* q, float* scale,
+                               void* cuda_stream);
+GPT2_API int gpt2_fp8_matmul(const uint8_t* a, int64_t lda, const float* scale_a, const uint8_t* b,
+                             int64_t ldb, const float* scale_b, int32_t M, int32_t N, int32_t K,
+                             const float* bias, void* out, int64_t ldo, int32_t out_is_bf16,
+                             void* cuda_stream);
+GPT2_API int gpt2_fp8_check(void* cuda_stream);
+
 /* ---------------------------------------------------------------- checkpoints
  * Training state saved and resumed as one flat file: InfoQ's account of
  * llm.c loads its model as a checkpoint file of fp32 weights in one block;

@@ -19,6 +19,7 @@ import os
 import numpy as np
 
 __all__ = ["Model", "GPT2Error", "TokenFile", "library_path", "load_library", "layernorm_backward_noalloc",
+           "fp8_quantize", "fp8_matmul", "fp8_check",
            "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -98,6 +99,9 @@ def load_library():
         "gpt2_tokens_reset": ([vp], ctypes.c_int),
         "gpt2_tokens_close": ([vp], None),
         "gpt2_decode_step": ([vp, vp, i32, f32, vp, vp], ctypes.c_int),
+        "gpt2_fp8_quantize": ([vp, i32, i64, vp, vp, vp], ctypes.c_int),
+        "gpt2_fp8_matmul": ([vp, i64, vp, vp, i64, vp, i32, i32, i32, vp, vp, i64, i32, vp], ctypes.c_int),
+        "gpt2_fp8_check": ([vp], ctypes.c_int),
         "gpt2_copy_decode_logits_out": ([vp, vp], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -398,3 +402,49 @@ def layernorm_backward_noalloc(dinp, dweight, dbias, dinp_colsum, dout, inp, wei
                                            int(N), int(C), s)
     if rc != 0:
         raise GPT2Error(rc, L.gpt2_last_error(None).decode())
+
+
+# ---- FP8 (E4M3) matmuls with per-tensor scaling ------------------------------
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _check_global(rc):
+    if rc != 0:
+        raise GPT2Error(rc, load_library().gpt2_last_error(None).decode())
+
+
+def fp8_quantize(x, stream=None):
+    """x: contiguous fp32 or bf16 CUDA tensor -> (q: uint8 codes like x,
+    scale: float32 [2] with scale[0] = 448 / max|x|), see gpt2_fp8_quantize."""
+    import torch
+    assert x.is_cuda and x.is_contiguous() and x.dtype in (torch.float32, torch.bfloat16)
+    q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scale = torch.empty(2, dtype=torch.float32, device=x.device)
+    _check_global(load_library().gpt2_fp8_quantize(x.data_ptr(), int(x.dtype == torch.bfloat16), x.numel(),
+                                                   q.data_ptr(), scale.data_ptr(), _stream_ptr(stream)))
+    return q, scale
+
+
+def fp8_matmul(qa, scale_a, qb, scale_b, bias=None, out_dtype=None, stream=None):
+    """(E(qa) E(qb)^T) / (scale_a[0] scale_b[0]) + bias: qa [M, K], qb [N, K]
+    uint8 codes (row strides multiples of 16 bytes); out [M, N] fp32 or bf16."""
+    import torch
+    out_dtype = torch.float32 if out_dtype is None else out_dtype
+    M, K = qa.shape
+    N = qb.shape[0]
+    out = torch.empty((M, N), dtype=out_dtype, device=qa.device)
+    _check_global(load_library().gpt2_fp8_matmul(
+        qa.data_ptr(), qa.stride(0), scale_a.data_ptr(), qb.data_ptr(), qb.stride(0), scale_b.data_ptr(),
+        M, N, K, None if bias is None else bias.data_ptr(), out.data_ptr(), out.stride(0),
+        int(out_dtype == torch.bfloat16), _stream_ptr(stream)))
+    return out
+
+
+def fp8_check(stream=None):
+    """Synchronise and report an expired device wait of the FP8 entry points."""
+    _check_global(load_library().gpt2_fp8_check(_stream_ptr(stream)))

@@ -204,6 +204,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
         for (int j = 32; j < 64; j++) v[j] = 0.f;
       }
     }
+    if (g.dequant_a) {  // E4M3 products: undo the operands' per-tensor scales
+      const float sc = 1.f / (*g.dequant_a * *g.dequant_b);
+#pragma unroll
+      for (int j = 0; j < 64; j++) v[j] *= sc;
+    }
     if (use_bias) {
       const int lb = (cc - half * (BN / 2)) >> 2;  // lane holding this chunk's first 4 columns
 #pragma unroll
@@ -581,7 +586,10 @@ struct PairCfgT {
   static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + STAGING + 1024 + 512;
 };
 
-template <bool A_K, bool B_K, bool AUX>
+// F8: A and B are E4M3 codes (one byte each, K-major), the MMA kind is
+// f8f6f4 and a 128-byte smem row holds 128 K-elements, so a stage covers
+// K = 128 with the same byte layout and descriptors as 64 bf16.
+template <bool A_K, bool B_K, bool AUX, bool F8 = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
@@ -640,7 +648,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           uint8_t* sb = sa + PairCfg::A_BYTES;
           const uint32_t bar = cluster_addr(&full[s], 0);
           if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * PairCfg::STAGE_BYTES);
-          const int k = (kt0 + i) * TC_BK;
+          const int k = (kt0 + i) * (F8 ? 2 * TC_BK : TC_BK);
           if (A_K) {
             tma_load_2d_pair(sa, &tmA, bar, k, m0);
           } else {
@@ -660,7 +668,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = tc_idesc_bf16(2 * TC_BM, PAIR_BN, !A_K, !B_K);
+      constexpr uint32_t idesc = F8 ? tc_idesc_e4m3(2 * TC_BM, PAIR_BN) : tc_idesc_bf16(2 * TC_BM, PAIR_BN, !A_K, !B_K);
       int it = 0, ti = 0;
       for (int t = pair; t < total; t += npairs, ti++) {
         const TileCoord tc = tile_coord(t, mpairs, ntiles, GROUP_PAIRS);
@@ -681,7 +689,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int kk = 0; kk < TC_BK / 16; kk++) {
             const uint64_t ad = A_K ? sw128_desc(a0 + kk * 32, 16, 1024) : sw128_desc(a0 + kk * 2048, 8192, 1024);
             const uint64_t bd = B_K ? sw128_desc(b0 + kk * 32, 16, 1024) : sw128_desc(b0 + kk * 2048, 8192, 1024);
-            tc_mma_bf16_pair(acc, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            if (F8) tc_mma_e4m3_pair(acc, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            else tc_mma_bf16_pair(acc, ad, bd, idesc, (i > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit_pair_both(&empty[s]);
         }
@@ -1041,6 +1050,61 @@ void launch_gemm_rows(LaunchCtx& c, const GemmArgs& g) {
                        kps, c.err);
   else
     launch_pdl(c, gemm_rows_tc_kernel, dim3(ntiles), dim3(RT_THREADS), RT_SMEM, tw, tx, g, ktiles, kps, c.err);
+}
+
+// [outer][inner] bytes (E4M3 codes), row stride ld bytes, box {128, box_outer}.
+static bool make_tmap_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                         uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld};
+  cuuint32_t box[2] = {128, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void launch_gemm_fp8(LaunchCtx& c, const GemmArgs& g) {
+  CUtensorMap ta, tb;
+  EpiMaps em;
+  memset(&em, 0, sizeof(em));
+  bool ok = g.epi == EPI_STORE && g.a_kmajor && g.b_kmajor && g.dequant_a && g.dequant_b;
+  ok = ok && make_tmap_u8(&ta, g.A, g.K, g.M, g.lda, TC_BM);
+  ok = ok && make_tmap_u8(&tb, g.B, g.K, g.N, g.ldb, PAIR_BN / 2);
+  ok = ok && make_tmap(&em.out, g.out, g.out_f32, g.N, g.M, g.ldo, g.out_f32 ? 32 : 64, 32);
+  if (!ok) {
+    fprintf(stderr, "gpt2: fp8 matmul setup failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
+    c.host_fail = 1;
+    return;
+  }
+  using Cfg = PairCfgT<false>;
+  auto kern = gemm_tc_pair_kernel<true, true, false, true>;
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * c.num_sms);
+    cfg.blockDim = dim3(TC_THREADS);
+    cfg.dynamicSmemBytes = Cfg::SMEM;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = c.num_sms / 2;
+    }
+    max_pairs = n;
+  }
+  const int k_tiles = (g.K + 2 * TC_BK - 1) / (2 * TC_BK);  // 128 codes per stage
+  const int pair_tiles = ((g.N + PAIR_BN - 1) / PAIR_BN) * ((g.M + 2 * TC_BM - 1) / (2 * TC_BM));
+  const int pairs = std::min(pair_tiles, max_pairs);
+  launch_pdl_cluster(c, kern, dim3(2 * pairs), dim3(TC_THREADS), Cfg::SMEM, 2, ta, tb, em, g, k_tiles, k_tiles, 1,
+                     (int*)nullptr, c.err);
 }
 
 static int g_pair_mode = -1;  // GPT2_GEMM_PAIR=0 selects the one-SM kernel for every shape

@@ -153,7 +153,19 @@ struct GemmArgs {
   // cache row of a generation step, fixed launch arguments for CUDA graphs)
   const int* out_row;
   int64_t out_row_stride;
+  // E4M3 operands (launch_gemm_fp8): the accumulator is divided by
+  // (*dequant_a) * (*dequant_b), the operands' per-tensor scales (device)
+  const float* dequant_a;
+  const float* dequant_b;
 };
+// E4M3 operands A [M, K], B [N, K] (uint8 codes, K-major, lda / ldb in
+// bytes, multiples of 16), EPI_STORE only (bias allowed), dequant_a / _b set:
+// the CTA-pair kernel with kind::f8f6f4 MMAs.
+void launch_gemm_fp8(LaunchCtx& c, const GemmArgs& g);
+// E4M3 per-tensor quantisation of n values (fp32 or bf16): scale[1] (scratch,
+// zeroed here) collects max|x|, scale[0] = s = 448 / max|x| (1 for all zeros),
+// q[i] = E4M3(x[i] * s) rounded to nearest even, saturating.
+void launch_fp8_quantize(LaunchCtx& c, const void* x, bool x_bf16, int64_t n, uint8_t* q, float* scale);
 // fp32 operands, SIMT FFMA (no TF32)
 void launch_gemm_f32(LaunchCtx& c, const GemmArgs& g);
 // bf16 operands on tcgen05 tensor cores, fp32 accumulation in TMEM
