@@ -627,21 +627,23 @@ void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int row
 template void launch_colsum<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t, float*);
 
 // ============================================================ softmax + cross-entropy
+#define LOG2E 1.4426950408889634f
+
+// (m, s) pairs: a running maximum m (natural units) and s = sum of e^(x - m).
 __device__ __forceinline__ void lse_combine(float& m, float& s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) return;
-  s = s * exp2f(m - mm) + s2 * exp2f(m2 - mm);
+  s = s * ex2_hw((m - mm) * LOG2E) + s2 * ex2_hw((m2 - mm) * LOG2E);
   m = mm;
 }
 
-#define LOG2E 1.4426950408889634f
-
-// One block per row; logits in log2 units (x * log2 e).  Pass 1 reads 8
-// logits at a time and folds each group into a running (max, sum of 2^(x -
-// max)) -- one max and one rescale per group of 8 -- then a block reduction.
-// Pass 2 (the row is now in L2) writes
-//   dlogits = (2^(x - lse2) - onehot(target)) * dscale,  pad columns 0,
-// in place.  loss = ln 2 * lse2 - logit[target].
+// One block per row.  Pass 1 reads 8 logits at a time and folds each group
+// into the running (max, sum of e^(x - max)) -- one max and one rescale per
+// group of 8, each e^(x - m) one FFMA and one ex2 -- then a block reduction
+// gives lse.  Pass 2 (the row is now in L2) writes
+//   dlogits = (e^(x - lse) - onehot(target)) * dscale,  pad columns 0,
+// in place; only the group holding the target and the groups past V take
+// the slow path.  loss = lse - logit[target].
 template <typename T>
 __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* losses, const int32_t* targets, int V,
                                     int Vp, float dscale, int write_dlogits, int* err) {
@@ -662,20 +664,19 @@ __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* los
     float v[8];
     load8<T>(l + q * 8, v);
     const int base = q * 8;
-    float cm = -INFINITY;
-    if (base + 8 <= V) {
+    if (base + 8 > V) {
 #pragma unroll
-      for (int j = 0; j < 8; j++) { v[j] *= LOG2E; cm = fmaxf(cm, v[j]); }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; j++) { v[j] = base + j < V ? v[j] * LOG2E : -INFINITY; cm = fmaxf(cm, v[j]); }
+      for (int j = 0; j < 8; j++) v[j] = base + j < V ? v[j] : -INFINITY;
     }
+    float cm = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; j++) cm = fmaxf(cm, v[j]);
     if (cm == -INFINITY) continue;
-    const float nm = fmaxf(m, cm);
+    const float nm = fmaxf(m, cm), nl = -nm * LOG2E;
     float a = 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; j++) a += exp2f(v[j] - nm);
-    s = s * exp2f(m - nm) + a;
+    for (int j = 0; j < 8; j++) a += ex2_hw(fmaf(v[j], LOG2E, nl));
+    s = s * ex2_hw((m - nm) * LOG2E) + a;
     m = nm;
   }
 #pragma unroll
@@ -699,18 +700,23 @@ __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* los
     if (lane == 0) { sm_m[0] = m; sm_s[0] = s; }
   }
   __syncthreads();
-  const float lse2 = sm_m[0] + log2f(sm_s[0]);
-  if (threadIdx.x == 0 && targets) losses[row] = lse2 * 0.6931471805599453f - lt;
+  const float lse = sm_m[0] + logf(sm_s[0]);
+  if (threadIdx.x == 0 && targets) losses[row] = lse - lt;
   if (!write_dlogits) return;
+  const float nl = -lse * LOG2E;
   for (int q = threadIdx.x; q < nch; q += blockDim.x) {
     float v[8];
     load8<T>(l + q * 8, v);
     const int base = q * 8;
     float o[8];
 #pragma unroll
-    for (int j = 0; j < 8; j++) {
-      const int jj = base + j;
-      o[j] = jj < V ? (exp2f(v[j] * LOG2E - lse2) - (jj == tg ? 1.f : 0.f)) * dscale : 0.f;
+    for (int j = 0; j < 8; j++) o[j] = ex2_hw(fmaf(v[j], LOG2E, nl)) * dscale;
+    if (base + 8 > V || (base <= tg && tg < base + 8)) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        if (base + j >= V) o[j] = 0.f;
+        else if (base + j == tg) o[j] -= dscale;
+      }
     }
     store4<T>(l + base, o[0], o[1], o[2], o[3]);
     store4<T>(l + base + 4, o[4], o[5], o[6], o[7]);
