@@ -18,9 +18,10 @@
 //
 //   forward   one CTA per (128-query block, b*h), 64-key sub-blocks: S -> TMEM
 //             (two buffers, issued two sub-blocks ahead), online softmax by 8
-//             warps (thread = query row), P -> smem, O_blk = P v -> TMEM, O in
-//             registers with the online-softmax rescale.  Saves lse in base 2:
-//             max*scale*log2e + log2(sum).
+//             warps (thread = query row), P -> smem, O += P v accumulated in
+//             TMEM; the softmax reference maximum moves only when a row's
+//             maximum grows by more than 2^8, and only then is O rescaled in
+//             place.  Saves lse in base 2: max*scale*log2e + log2(sum).
 //   backward  D = rowsum(dy * y); one CTA per (128-key block, b*h) for dK, dV
 //             over 128-query sub-blocks (S^T, dP^T recomputed into TMEM; P^T
 //             and dS^T written back to TMEM and read there as the A operand
@@ -208,13 +209,16 @@ __device__ __forceinline__ float warp_colsum32(float* v) {
 // thread) issues every TMA load and MMA, so no softmax warp stalls on them:
 //   S(j) = q k(j)^T into TMEM S[j%2], issued two sub-blocks ahead (as soon
 //          as softmax(j-2) has read that buffer);
-//   O_blk(j) = P(j) v(j) into TMEM O[j%2] once P(j) is in shared memory;
-//          the softmax warps fold it into their register accumulator
-//          (online-softmax rescale) during sub-block j+1;
+//   O += P(j) v(j) into one TMEM accumulator once P(j) is in shared
+//          memory; the softmax warps take P relative to a reference maximum
+//          that moves only when a row's maximum exceeds it by more than 8 in
+//          log2 units (P <= 2^8), and then rescale O in TMEM after PV(j-1)
+//          has completed and before they release P(j) (lazy rescaling);
 //   k and v stream through three-stage rings, each stage refilled as soon
 //          as the MMA that read it has completed.
 // Warps w and w+4 exchange their half-row maxima through a double-buffered
 // array and a 64-thread named barrier.
+// TMEM: S0 S1 (columns 0..127), O (128..191).
 // smem: Q | K ring | V ring (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
 #define AF_KV_STAGES 3
 #define AF_THREADS (AT_THREADS + 32)
@@ -313,8 +317,7 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
           tc_fence_after();
           const uint32_t aP = smem_u32(sP + (j & 1) * AT_TILE), bV = smem_u32(sV + s * AT_SUBTILE);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++)
-            tc_mma_bf16(tm + 128 + (uint32_t)((j & 1) * 64), kmaj(aP, kk), mnmaj(bV, kk), idO, kk > 0);
+          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + 128, kmaj(aP, kk), mnmaj(bV, kk), idO, (j > 0 || kk > 0));
           tc_commit(&o_done[j & 1]);
         }
         if (j + 2 < nsub) issue_s(j + 2);
@@ -330,10 +333,11 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
     const int row = quarter * 32 + lane, q = q0 + row;
     const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
     const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
-    float m = -INFINITY, lpart = 0.f, alpha_prev = 1.f;
-    float o[32];
-#pragma unroll
-    for (int i = 0; i < 32; i++) o[i] = 0.f;
+    // m: the row's reference maximum (raw score units).  P and the row sum
+    // are taken relative to it; it moves only when a new maximum exceeds it
+    // by more than 8 in log2 units (so P <= 2^8), and then the accumulator O
+    // in TMEM and the row sum are rescaled by 2^((m_old - m_new) * sl2).
+    float m = -INFINITY, lpart = 0.f;
 
     for (int j = 0; j < nsub; j++) {
       const int sb = j & 1;
@@ -358,10 +362,33 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
       float* rd = red + sb * 256;
       rd[half * 128 + row] = mx;
       named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
-      const float mnew = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
-      const float alpha = ex2_hw((m - mnew) * sl2);
-      const float mo = mnew * sl2;
-      // pass 2: P = exp(scale (s - mnew)) -> smem P[sb] (bf16), partial row sum
+      const float mcand = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
+      const bool resc = (mcand - m) * sl2 > 8.f;  // always at j = 0 (m = -inf)
+      float alpha = 1.f;
+      if (resc) {
+        alpha = ex2_hw((m - mcand) * sl2);
+        lpart *= alpha;
+        m = mcand;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // O holds PV(0 .. j-1) once PV(j-1) completes; PV(j) waits for this
+        // sub-block's p_ready, so the rescale cannot race an MMA
+        mbar_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, err);
+        tc_fence_after();
+        const uint32_t tO = tm + 128 + lanebase + half * 32;
+        uint32_t ro[32];
+        tmem_ld32(tO, ro);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; i++) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
+        tmem_st16(tO, ro);
+        tmem_st16(tO + 16, ro + 16);
+        tmem_st_wait();
+      }
+      // P[sb] was read by PV(j-2)
+      if (j >= 2) mbar_wait(&o_done[sb], (uint32_t)((j - 2) >> 1) & 1u, err);
+      const float mo = m * sl2;
+      // pass 2: P = 2^(scale (s - m) log2 e) -> smem P[sb] (bf16), partial row sum
       float sum = 0.f;
       uint8_t* prow = sP + sb * AT_TILE + row * 128;
       if (diag) {
@@ -388,36 +415,22 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
           st_row8(prow, row & 7, half * 4 + g, p);
         }
       }
-      lpart = lpart * alpha + sum;
-      m = mnew;
+      lpart += sum;
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_ready[sb]);
-      // fold in O_blk(j-1) (its MMA ran during this sub-block's softmax); once
-      // read, O[(j-1)%2] and P[(j-1)%2] may be reused by PV(j+1) and P(j+1)
-      if (j > 0) {
-        const int pb = sb ^ 1;
-        mbar_wait(&o_done[pb], (uint32_t)((j - 1) >> 1) & 1u, err);
-        tc_fence_after();
-        uint32_t ro[32];
-        tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
-      }
-      alpha_prev = alpha;
-      tc_fence_before();
     }
-    {  // the last O_blk
+    float o[32];
+    {  // O = PV(0 .. nsub-1), relative to the final reference maximum
       const int pb = (nsub - 1) & 1;
       mbar_wait(&o_done[pb], (uint32_t)((nsub - 1) >> 1) & 1u, err);
       tc_fence_after();
       uint32_t ro[32];
-      tmem_ld32(tm + 128 + (uint32_t)(pb * 64) + lanebase + half * 32, ro);
+      tmem_ld32(tm + 128 + lanebase + half * 32, ro);
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 32; i++) o[i] = o[i] * alpha_prev + __uint_as_float(ro[i]);
+      for (int i = 0; i < 32; i++) o[i] = __uint_as_float(ro[i]);
     }
     named_bar_sync(5, AT_THREADS);  // every softmax warp is past its last exchange
     red[half * 128 + row] = lpart;
