@@ -206,7 +206,8 @@ __device__ __forceinline__ float warp_colsum32(float* v) {
 // ============================================================ forward
 // One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks;
 // two CTAs share an SM.  Warps 0..7 do the online softmax; warp 8 (one
-// thread) issues every TMA load and MMA, so no softmax warp stalls on them:
+// thread) issues every MMA and warp 9 (one thread) every TMA load, so no
+// softmax warp stalls on them and no load waits behind an MMA hand-off:
 //   S(j) = q k(j)^T into TMEM S[j%2], issued two sub-blocks ahead (as soon
 //          as softmax(j-2) has read that buffer);
 //   O += P(j) v(j) into one TMEM accumulator once P(j) is in shared
@@ -214,14 +215,15 @@ __device__ __forceinline__ float warp_colsum32(float* v) {
 //          that moves only when a row's maximum exceeds it by more than 8 in
 //          log2 units (P <= 2^8), and then rescale O in TMEM after PV(j-1)
 //          has completed and before they release P(j) (lazy rescaling);
-//   k and v stream through three-stage rings, each stage refilled as soon
-//          as the MMA that read it has completed.
+//   k and v stream through three-stage rings, each stage refilled by the
+//          loader as soon as the MMA that read it has completed (k_empty /
+//          v_empty, committed with the MMAs).
 // Warps w and w+4 exchange their half-row maxima through a double-buffered
 // array and a 64-thread named barrier.
 // TMEM: S0 S1 (columns 0..127), O (128..191).
 // smem: Q | K ring | V ring (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
 #define AF_KV_STAGES 3
-#define AF_THREADS (AT_THREADS + 32)
+#define AF_THREADS (AT_THREADS + 64)
 #define AF_SMEM (1024 + AT_TILE + 2 * AF_KV_STAGES * AT_SUBTILE + 2 * AT_TILE + 2048 + 256)
 
 __global__ void __launch_bounds__(AF_THREADS, 2)
@@ -246,7 +248,9 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
   // the softmax warps, which may run a sub-block ahead of the issuer, never
   // complete a barrier's phase twice before the issuer has waited for it)
   uint64_t* p_ready = o_done + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(p_ready + 2);
+  uint64_t* k_empty = p_ready + 2;               // [AF_KV_STAGES]: S of the stage done
+  uint64_t* v_empty = k_empty + AF_KV_STAGES;    // [AF_KV_STAGES]: PV of the stage done
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(v_empty + AF_KV_STAGES);
 
   const int nqb = gridDim.y;
   const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the longest rows
@@ -257,7 +261,12 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
 
   if (tid == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < AF_KV_STAGES; s++) { mbar_init(&k_full[s], 1); mbar_init(&v_full[s], 1); }
+    for (int s = 0; s < AF_KV_STAGES; s++) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
     for (int i = 0; i < 2; i++) {
       mbar_init(&s_done[i], 1);
       mbar_init(&o_done[i], 1);
@@ -275,21 +284,11 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
   pdl_wait();  // from here on global memory written by the previous kernel is read
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA + MMA issuer
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
       const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
-      auto load_k = [&](int j) {
-        const int s = j % AF_KV_STAGES;
-        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
-        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
-      };
-      auto load_v = [&](int j) {
-        const int s = j % AF_KV_STAGES;
-        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
-        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
-      };
-      auto issue_s = [&](int j) {  // S(j) into S[j%2]
+      auto issue_s = [&](int j) {  // S(j) into S[j%2]; its k stage is then free
         const int s = j % AF_KV_STAGES;
         mbar_wait(&k_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
         tc_fence_after();
@@ -297,34 +296,41 @@ __global__ void __launch_bounds__(AF_THREADS, 2)
 #pragma unroll
         for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + (uint32_t)((j & 1) * 64), kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
         tc_commit(&s_done[j & 1]);
+        tc_commit(&k_empty[s]);
       };
-      mbar_arrive_expect_tx(q_full, AT_TILE);
-      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-      for (int j = 0; j < AF_KV_STAGES && j < nsub; j++) { load_k(j); load_v(j); }
       mbar_wait(q_full, 0, err);
       issue_s(0);
       if (nsub > 1) issue_s(1);
       for (int j = 0; j < nsub; j++) {
-        if (j + AF_KV_STAGES < nsub) {  // S(j) has completed: its k stage takes k(j+3)
-          mbar_wait(&s_done[j & 1], (uint32_t)(j >> 1) & 1u, err);
-          load_k(j + AF_KV_STAGES);
-        }
         mbar_wait(&p_ready[j & 1], (uint32_t)(j >> 1) & 1u, err);  // P(j) written, S[j%2] read
         tc_fence_after();
-        {
-          const int s = j % AF_KV_STAGES;
-          mbar_wait(&v_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
-          tc_fence_after();
-          const uint32_t aP = smem_u32(sP + (j & 1) * AT_TILE), bV = smem_u32(sV + s * AT_SUBTILE);
+        const int s = j % AF_KV_STAGES;
+        mbar_wait(&v_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
+        tc_fence_after();
+        const uint32_t aP = smem_u32(sP + (j & 1) * AT_TILE), bV = smem_u32(sV + s * AT_SUBTILE);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + 128, kmaj(aP, kk), mnmaj(bV, kk), idO, (j > 0 || kk > 0));
-          tc_commit(&o_done[j & 1]);
-        }
+        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + 128, kmaj(aP, kk), mnmaj(bV, kk), idO, (j > 0 || kk > 0));
+        tc_commit(&o_done[j & 1]);
+        tc_commit(&v_empty[s]);
         if (j + 2 < nsub) issue_s(j + 2);
-        if (j >= 1 && j + 2 < nsub && j + 2 >= AF_KV_STAGES) {  // PV(j-1) has completed: v(j+2)
-          mbar_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, err);
-          load_v(j + 2);
-        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ TMA loader
+    // q once; k(j) and v(j) into their ring stages as soon as the MMA that
+    // read the stage's previous tile (S(j-3), PV(j-3)) has completed
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, AT_TILE);
+      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
+      for (int j = 0; j < nsub; j++) {
+        const int s = j % AF_KV_STAGES;
+        const uint32_t ph = (uint32_t)(j / AF_KV_STAGES - 1) & 1u;
+        if (j >= AF_KV_STAGES) mbar_wait(&k_empty[s], ph, err);
+        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
+        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
+        if (j >= AF_KV_STAGES) mbar_wait(&v_empty[s], ph, err);
+        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
+        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
       }
     }
   } else {
