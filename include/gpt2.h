@@ -253,7 +253,7 @@ GPT2_API int gpt2_copy_decode_logits_out(gpt2_model* m, float* host_dst);
  *   rounded to nearest (ties to even), saturating at +-448 (NaN -> 0x7F).
  *   scale points to 2 floats; scale[1] is scratch.  x and q 16-byte aligned.
  * gpt2_fp8_matmul: out[m, n] = (sum_k E(a[m, k]) E(b[n, k])) /
- *   (scale_a[0] * scale_b[0]) + bias[n] (bias may be NULL), with E the code's
+ *   (scale_a[0] * scale_b[0]) + bias[n] (bias may be NULL; 16-byte aligned), with E the code's
  *   value; a [M, K] and b [N, K] row-major codes with row strides lda, ldb
  *   bytes (multiples of 16, >= K); out [M, N] fp32 (or bf16 if out_is_bf16)
  *   with row stride ldo elements (16-byte rows); the products accumulate in

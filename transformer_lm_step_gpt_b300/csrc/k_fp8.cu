@@ -139,9 +139,9 @@ extern "C" int gpt2_fp8_matmul(const uint8_t* a, int64_t lda, const float* scale
   }
   const int64_t esz = out_is_bf16 ? 2 : 4;
   if (lda < K || ldb < K || lda % 16 || ldb % 16 || ldo < N || (ldo * esz) % 16 || !aligned16(a) || !aligned16(b) ||
-      !aligned16(out)) {
+      !aligned16(out) || (bias && !aligned16(bias))) {
     set_global_error("gpt2_fp8_matmul: need lda, ldb >= K and multiples of 16, ldo >= N with 16-byte rows, "
-                     "16-byte aligned a, b, out");
+                     "16-byte aligned a, b, out and bias");
     return GPT2_ERR_ARG;
   }
   if (!gemm_bf16_init()) {

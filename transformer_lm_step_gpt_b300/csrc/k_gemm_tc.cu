@@ -163,7 +163,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
                                               uint64_t* abar, uint32_t& aux_phase, uint32_t taddr0,
                                               int half, int lane, int mrow, int n0, int split_idx,
                                               bool split, bool f32, bool has_aux, bool use_bias,
-                                              float4 bq, int* err, int* tflag = nullptr, int nsplits = 1) {
+                                              float4 bq, int* err, int* tflag = nullptr, int nsplits = 1,
+                                              uint8_t* stg2 = nullptr) {
   const int epi = g.epi;
   const int CW = f32 ? 32 : 64;  // columns per 128-byte staging row
   if (tflag) {
@@ -251,6 +252,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
         } else if (epi == EPI_GELU_FWD && !split) {  // out = gelu'(x); v keeps gelu(x) for out2
 #pragma unroll
           for (int q = 0; q < 8; q++) gelu_and_grad_hw(v[8 * c + q], v[8 * c + q], o[q]);
+          if (stg2) put8_bf16(stg2 + stg_off(lane, c), &v[8 * c]);  // gelu(x) into the second buffer
         } else {
 #pragma unroll
           for (int q = 0; q < 8; q++) o[q] = v[8 * c + q];
@@ -264,6 +266,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       if (split) tma_store_3d(&em.out, stg, ncol, mrow, split_idx);
       else if (epi == EPI_ACCUM) tma_reduce_add_2d(&em.out, stg, ncol, mrow);
       else tma_store_2d(&em.out, stg, ncol, mrow);
+      if (epi == EPI_GELU_FWD && !split && stg2) tma_store_2d(&em.out2, stg2, ncol, mrow);
       bulk_commit();
     }
     if (g.colsum_out && !f32 && !split) {
@@ -282,7 +285,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       if (mrow < g.M && n < g.N)
         *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);
     }
-    if (epi == EPI_GELU_FWD && !split) {  // second output: gelu(x), already in v
+    if (epi == EPI_GELU_FWD && !split && !stg2) {  // second output: gelu(x), already in v
       if (lane == 0) bulk_wait_read0();
       __syncwarp();
 #pragma unroll
@@ -573,8 +576,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 // 128 accumulator lanes with the epilogue above.
 #define PAIR_BN 256
 #define GROUP_PAIRS 4
-// AUX: the epilogue reads an aux tile (EPI_RESIDUAL, EPI_MUL_AUX) and gets
-// two staging buffers per warp to fetch it ahead, for one operand stage.
+// AUX: two staging buffers per warp, for one operand stage: an epilogue that
+// reads an aux tile (EPI_RESIDUAL, EPI_MUL_AUX) fetches it ahead into one,
+// and the GELU forward writes its two outputs into both at once.
 template <bool AUX>
 struct PairCfgT {
   static constexpr int STAGES = AUX ? 5 : 6;
@@ -711,7 +715,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int* tflag = flags ? flags + ((int64_t)(tc.mt * ntiles + tc.nt) * 2 + rank) * EPI_WARPS + ew : nullptr;
       const int mrow = (2 * tc.mt + (int)rank) * TC_BM + quarter * 32, n0 = tc.nt * PAIR_BN;
       const uint32_t taddr = tmem + (uint32_t)(a * PAIR_BN) + ((uint32_t)(quarter * 32) << 16);
-      if (AUX) {
+      if (AUX && f.has_aux) {
         // chunk 0's aux tile, fetched while this tile's MMAs still run
         uint8_t* stg2 = staging + (size_t)ew * 2 * STG_BYTES;
         const int ncol0 = n0 + half * (PAIR_BN / 2);
@@ -730,9 +734,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const float4 bq = load_bias4<PAIR_BN>(g, f.use_bias, n0, half, lane);
         mbar_wait(&acc_full[a], (uint32_t)(ti >> 1) & 1u, err);
         tc_fence_after();
-        epilogue_tile<PAIR_BN>(g, em, staging + (size_t)ew * STG_BYTES, &aux_bar[2 * ew], aux_phase, taddr,
-                               half, lane, mrow, n0, tc.split, f.split, f.f32, f.has_aux, f.use_bias, bq, err,
-                               tflag, splits);
+        // with the doubled staging of the AUX configuration, the GELU
+        // forward writes its two outputs into two buffers (no wait between)
+        uint8_t* st = AUX ? staging + (size_t)ew * 2 * STG_BYTES : staging + (size_t)ew * STG_BYTES;
+        epilogue_tile<PAIR_BN>(g, em, st, &aux_bar[2 * ew], aux_phase, taddr, half, lane, mrow, n0, tc.split,
+                               f.split, f.f32, f.has_aux, f.use_bias, bq, err, tflag, splits,
+                               AUX ? st + STG_BYTES : nullptr);
       }
       tc_fence_before();
       __syncwarp();
@@ -1139,7 +1146,7 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   if (BN == 256 && g_pair_mode) {
     // epilogues that read an aux tile use the prefetching variant; the model's
     // aux GEMMs (attproj / fcproj forward, fcproj dgrad) are A K-major
-    const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX);
+    const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX || g.epi == EPI_GELU_FWD);
     if (aux && g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, true>(c, g, splits, partial);
     else if (aux && g.a_kmajor) launch_tc_pair<true, false, true>(c, g, splits, partial);
     else if (g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, false>(c, g, splits, partial);
