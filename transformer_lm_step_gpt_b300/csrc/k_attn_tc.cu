@@ -57,7 +57,11 @@ static EncodeTiledFnA encoder_fn() {
 }
 
 // [B][T][W] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, rows past T zero.
-static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows = 128) {
+static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows = 128);
+bool attn_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows) {
+  return make_tmap_btw(m, base, B, T, W, rows);
+}
+static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows) {
   EncodeTiledFnA f = encoder_fn();
   if (!f) return false;
   cuuint64_t dims[3] = {(cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)B};

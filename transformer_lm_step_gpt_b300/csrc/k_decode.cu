@@ -9,6 +9,8 @@
 // embedding matrix scores the candidates for the next token.  The cache is the
 // per-layer qkv activation [B, T, 3C] of the forward pass: row t of sequence b
 // holds [q | k | v] of position t.
+#include <cuda.h>
+
 #include <algorithm>
 #include <climits>
 
@@ -204,6 +206,127 @@ __global__ void __launch_bounds__(DEC_THREADS)
   dec_cluster_sync();  // the first rank has read the others: they may exit
 }
 
+// The same for bf16 and head size 64, with the rank's key and value rows
+// staged by TMA: one bulk tensor copy per 128 rows brings the rows [j0,
+// j0 + 128 nbox) of k and of v (128-byte swizzled: logical 16-byte chunk c of
+// row r sits at chunk c ^ (r & 7)) into shared memory at once, so the
+// scores (thread per key) and the weighted sum (whole rows per warp) read
+// shared memory instead of waiting on one global load after another.
+#define DEC_ROWS 128
+__global__ void __launch_bounds__(DEC_THREADS)
+    attn_decode_tma_kernel(const __grid_constant__ CUtensorMap tm, bf16* y, int64_t ldy, const bf16* qkv, int T_,
+                           int C, int NH, const int* pos_dev, float scale, int KS, int nbox, int* err) {
+  pdl_trigger();
+  extern __shared__ __align__(1024) uint8_t dtm[];
+  constexpr int HS = 64;
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dtm) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sK = sm;                                   // [nbox * 128 rows][128 B]
+  uint8_t* sV = sK + (size_t)nbox * DEC_ROWS * 128;   // same
+  float* qs = reinterpret_cast<float*>(sV + (size_t)nbox * DEC_ROWS * 128);  // [64]
+  float* red = qs + HS;                               // [32]
+  float* part = red + 32;                             // [66]: o, m, s
+  float* sc = part + HS + 2;                          // [nbox * 128], later the warps' sums [8][64]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sc + max(nbox * DEC_ROWS, (DEC_THREADS / 32) * HS));
+  const uint32_t rank = KS > 1 ? dec_cluster_rank() : 0u;
+  const int bh = blockIdx.x / KS, b = bh / NH, h = bh % NH;
+  const int tid = threadIdx.x;
+  const int64_t C3 = 3 * (int64_t)C;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm);
+  }
+  __syncthreads();
+  pdl_wait();
+  const int pos = *pos_dev;
+  const int kr = (pos + 1 + KS - 1) / KS;
+  const int j0 = (int)rank * kr, j1 = min(pos + 1, j0 + kr);  // this rank's keys [j0, j1); may be empty
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * nbox * DEC_ROWS * 128));
+    for (int i = 0; i < nbox; i++) {
+      tma_load_3d(sK + (size_t)i * DEC_ROWS * 128, &tm, bar, C + h * HS, j0 + i * DEC_ROWS, b);
+      tma_load_3d(sV + (size_t)i * DEC_ROWS * 128, &tm, bar, 2 * C + h * HS, j0 + i * DEC_ROWS, b);
+    }
+  }
+  if (tid < HS) qs[tid] = __bfloat162float(qkv[((int64_t)b * T_ + pos) * C3 + h * HS + tid]);
+  __syncthreads();
+  mbar_wait(bar, 0, err);
+  float mx = -INFINITY;
+  for (int j = j0 + tid; j < j1; j += DEC_THREADS) {
+    const int r = j - j0;
+    const uint8_t* row = sK + (size_t)r * 128;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; c++) {
+      float f[8];
+      load8f<bf16>(reinterpret_cast<const bf16*>(row + ((c ^ (r & 7)) << 4)), f);
+#pragma unroll
+      for (int i = 0; i < 8; i++) s = fmaf(qs[c * 8 + i], f[i], s);
+    }
+    s *= scale;
+    sc[r] = s;
+    mx = fmaxf(mx, s);
+  }
+  mx = block_max<DEC_THREADS>(mx, red);
+  float sum = 0.f;
+  for (int j = j0 + tid; j < j1; j += DEC_THREADS) {
+    const float e = expf(sc[j - j0] - mx);
+    sc[j - j0] = e;
+    sum += e;
+  }
+  sum = block_sum<DEC_THREADS>(sum, red);  // its barriers also publish sc[]
+  // weighted sum of the value rows: 8 lanes per row (16 bytes each), 4 rows
+  // per warp step; warp w takes rows w*4 + (lane / 8) + 32 i
+  const int warp = tid >> 5, lane = tid & 31;
+  const int kl = lane >> 3, cl = lane & 7;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) acc[i] = 0.f;
+  for (int r = warp * 4 + kl; r < j1 - j0; r += 32) {
+    float f[8];
+    load8f<bf16>(reinterpret_cast<const bf16*>(sV + (size_t)r * 128 + ((cl ^ (r & 7)) << 4)), f);
+    const float p = sc[r];
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] = fmaf(p, f[i], acc[i]);
+  }
+#pragma unroll
+  for (int o = 8; o < 32; o <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+  }
+  __syncthreads();  // every thread is done reading sc[]: reuse it for the warps' sums
+  if (kl == 0) {
+#pragma unroll
+    for (int i = 0; i < 8; i++) sc[warp * HS + cl * 8 + i] = acc[i];
+  }
+  __syncthreads();
+  if (tid < HS) {
+    float r = 0.f;
+    for (int w = 0; w < DEC_THREADS / 32; w++) r += sc[w * HS + tid];
+    part[tid] = r;
+  }
+  if (tid == 0) { part[HS] = mx; part[HS + 1] = sum; }
+  if (KS == 1) {
+    __syncthreads();
+    if (tid < HS) y[(int64_t)b * ldy + h * HS + tid] = __float2bfloat16_rn(part[tid] / part[HS + 1]);
+    return;
+  }
+  dec_cluster_sync();  // every rank's (o, m, s) in its shared memory
+  if (rank == 0 && tid < HS) {
+    float m = -INFINITY;
+    for (int q = 0; q < KS; q++) m = fmaxf(m, dec_ld_cluster(part + HS, (uint32_t)q));
+    float o = 0.f, l = 0.f;
+    for (int q = 0; q < KS; q++) {
+      const float mq = dec_ld_cluster(part + HS, (uint32_t)q);
+      const float f = mq == -INFINITY ? 0.f : expf(mq - m);  // a rank without keys adds nothing
+      o += f * dec_ld_cluster(part + tid, (uint32_t)q);
+      l += f * dec_ld_cluster(part + HS + 1, (uint32_t)q);
+    }
+    y[(int64_t)b * ldy + h * HS + tid] = __float2bfloat16_rn(o / l);
+  }
+  dec_cluster_sync();  // the first rank has read the others: they may exit
+}
+
 template <typename T>
 void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int B, int T_, int C, int NH,
                              const int* pos) {
@@ -212,12 +335,36 @@ void launch_attention_decode(LaunchCtx& c, T* y, int64_t ldy, const T* qkv, int 
   // so that the launch does not depend on the position)
   const int KS = std::max(1, std::min(8, (T_ + 63) / 64));
   const int kr = (T_ + KS - 1) / KS;  // the most keys a rank can get
+  const float scale = 1.f / sqrtf((float)hs);
+  if constexpr (sizeof(T) == 2) {
+    if (hs == 64) {  // key / value rows staged by TMA
+      CUtensorMap tmap;
+      if (!attn_tmap_btw(&tmap, qkv, B, T_, 3 * C, DEC_ROWS)) {
+        c.host_fail = 1;
+        return;
+      }
+      const int nbox = (kr + DEC_ROWS - 1) / DEC_ROWS;
+      const size_t smem = 1024 + (size_t)2 * nbox * DEC_ROWS * 128 +
+                          sizeof(float) * (64 + 32 + 66 + std::max(nbox * DEC_ROWS, (DEC_THREADS / 32) * 64)) + 8;
+      static bool attr = false;
+      if (!attr) {
+        cudaFuncSetAttribute(attn_decode_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        attr = true;
+      }
+      if (KS > 1)
+        launch_pdl_cluster(c, attn_decode_tma_kernel, dim3(B * NH * KS), dim3(DEC_THREADS), smem, KS, tmap, y, ldy,
+                           qkv, T_, C, NH, pos, scale, KS, nbox, c.err);
+      else
+        launch_pdl(c, attn_decode_tma_kernel, dim3(B * NH), dim3(DEC_THREADS), smem, tmap, y, ldy, qkv, T_, C, NH,
+                   pos, scale, KS, nbox, c.err);
+      return;
+    }
+  }
   const size_t smem = sizeof(float) * (hs + 32 + hs + 2 + std::max(kr, (DEC_THREADS / 32) * hs));
   auto kern = hs == 16 ? attn_decode_kernel<T, 16>
               : hs == 32 ? attn_decode_kernel<T, 32>
               : hs == 64 ? attn_decode_kernel<T, 64>
                          : attn_decode_kernel<T, 128>;
-  const float scale = 1.f / sqrtf((float)hs);
   if (KS > 1)
     launch_pdl_cluster(c, kern, dim3(B * NH * KS), dim3(DEC_THREADS), smem, KS, y, ldy, qkv, T_, C, NH, pos, scale,
                        KS);

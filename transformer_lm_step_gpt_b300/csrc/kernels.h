@@ -200,6 +200,12 @@ bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const b
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
                                int C, int NH, float* bias_partial);
 
+// A tensor map over a [B][T][W] bf16 tensor with box {64, rows, 1},
+// 128-byte swizzle, rows past T read as 0 (false if the driver's encoder is
+// unavailable).  CUtensorMap is opaque here: a 128-byte aligned 128-byte blob.
+struct CUtensorMap_st;
+bool attn_tmap_btw(CUtensorMap_st* m, const void* base, int B, int T, int W, int rows);
+
 // ---------------------------------------------------------------- decode
 // Generation with the key/value cache qkv [B, T_, 3C] (row t of sequence b:
 // [q | k | v] of position t): y[b*ldy + h*hs + d] = the attention of the
