@@ -64,3 +64,30 @@ def test_null_model_calls_return_arg_error():
     assert lib.gpt2_forward(None, None, None, None) == -1
     lib.gpt2_free(None)  # NULL is allowed
     assert lib.gpt2_last_error(None)  # never NULL
+
+
+def test_generation_and_fp8_entry_points_check_arguments_without_gpu():
+    lib = tl.load_library()
+    # generation: a NULL model
+    assert lib.gpt2_decode_step(None, None, 0, 1.0, None, None) == -1
+    assert lib.gpt2_copy_decode_logits_out(None, None) == -1
+    # FP8: NULL pointers, sizes below 1, misaligned pointers and strides are
+    # refused before any device work
+    assert lib.gpt2_fp8_quantize(None, 0, 16, None, None, None) == -1
+    assert b"NULL" in lib.gpt2_last_error(None)
+    buf = ctypes.create_string_buffer(4096)
+    p = (ctypes.addressof(buf) + 255) & ~255   # an aligned host address, never dereferenced here
+    assert lib.gpt2_fp8_quantize(p, 0, 0, p, p, None) == -1          # n < 1
+    assert lib.gpt2_fp8_quantize(p + 4, 0, 16, p, p, None) == -1     # x not 16-byte aligned
+    args = dict(lda=64, ldb=64, M=8, N=8, K=64, ldo=8)
+
+    def mm(**kw):
+        a = dict(args, **kw)
+        return lib.gpt2_fp8_matmul(p, a["lda"], p, p, a["ldb"], p, a["M"], a["N"], a["K"], None, p, a["ldo"], 0,
+                                   None)
+    assert mm(lda=40) == -1      # not a multiple of 16
+    assert mm(ldb=32) == -1      # smaller than K
+    assert mm(ldo=6) == -1       # ldo < N
+    assert mm(M=0) == -1
+    assert lib.gpt2_fp8_matmul(p, 64, p, p, 64, p, 8, 8, 64, p + 4, p, 8, 0, None) == -1   # bias misaligned
+    assert b"aligned" in lib.gpt2_last_error(None)
