@@ -35,7 +35,7 @@
  *             Rust", section "Gradient checking" (the test method used to
  *             pin the backward passes, see tests/test_oracle_grad.py).
  *
- * Readings where the pages are silent (each one also listed in the design doc):
+ * Readings where the pages are silent:
  *  - pre-LN block: x += proj(attn(LN1(x))); x += fcproj(GELU(fc(LN2(x))));
  *    then LN_f and the tied head logits = LN_f(x) * wte^T (no head bias);
  *  - LayerNorm: biased variance (divide by C), eps = 1e-5 inside the sqrt;
