@@ -182,6 +182,20 @@ GPT2_API int gpt2_tensor_info(const gpt2_model* m, int32_t idx, const char** nam
  * refreshes the bf16 weight copy. */
 GPT2_API int gpt2_copy_out(gpt2_model* m, int32_t arena, float* host_dst);
 GPT2_API int gpt2_copy_in(gpt2_model* m, int32_t arena, const float* host_src);
+/* The same for one named array each: gpt2_copy_params_out(m, dst) is
+ * gpt2_copy_out(m, GPT2_PARAMS, dst), and so on for the gradients and the
+ * AdamW moments; gpt2_copy_params_in(m, src) is gpt2_copy_in(m,
+ * GPT2_PARAMS, src). */
+GPT2_API int gpt2_copy_params_out(gpt2_model* m, float* host_dst);
+GPT2_API int gpt2_copy_grads_out(gpt2_model* m, float* host_dst);
+GPT2_API int gpt2_copy_m_out(gpt2_model* m, float* host_dst);
+GPT2_API int gpt2_copy_v_out(gpt2_model* m, float* host_dst);
+GPT2_API int gpt2_copy_params_in(gpt2_model* m, const float* host_src);
+/* *out = the device address of the fp32 mean loss that a gpt2_forward with
+ * targets writes (valid for the model's lifetime; read it in the model's
+ * stream order, e.g. after gpt2_forward(..., NULL) without a host sync).
+ * Errors: GPT2_ERR_ARG for a NULL model or out. */
+GPT2_API int gpt2_loss_device_ptr(const gpt2_model* m, const float** out);
 
 /* Per-position losses [B*T] of the last forward with targets.  Synchronises. */
 GPT2_API int gpt2_copy_losses_out(gpt2_model* m, float* host_dst);

@@ -91,3 +91,12 @@ def test_generation_and_fp8_entry_points_check_arguments_without_gpu():
     assert mm(M=0) == -1
     assert lib.gpt2_fp8_matmul(p, 64, p, p, 64, p, 8, 8, 64, p + 4, p, 8, 0, None) == -1   # bias misaligned
     assert b"aligned" in lib.gpt2_last_error(None)
+
+
+def test_named_copies_reject_a_null_model():
+    lib = tl.load_library()
+    for fn in (lib.gpt2_copy_params_out, lib.gpt2_copy_grads_out, lib.gpt2_copy_m_out, lib.gpt2_copy_v_out,
+               lib.gpt2_copy_params_in):
+        assert fn(None, None) == -1
+    out = ctypes.c_void_p()
+    assert lib.gpt2_loss_device_ptr(None, ctypes.byref(out)) == -1

@@ -197,3 +197,40 @@ def test_stream_is_honoured():
         t1, t2 = cuda_ids(tok), cuda_ids(tgt)
     loss = m.forward(t1, t2)
     assert math.isfinite(loss)
+
+
+def test_named_array_copies_and_device_loss_pointer():
+    # gpt2_copy_{params,grads,m,v}_out / gpt2_copy_params_in against the
+    # arena-indexed copies, and the device mean-loss address against
+    # gpt2_read_loss, after one full step
+    import ctypes
+    from cuda.bindings import runtime as rt
+    from transformer_lm_step_gpt_b300 import ADAM_M, ADAM_V, load_library
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=31)
+    lib = load_library()
+    tok, tgt = synthetic.batch(32, B, T, V)
+    m.forward(cuda_ids(tok), cuda_ids(tgt))
+    m.zero_grad()
+    m.backward()
+    m.adamw_step(1e-3, 0.9, 0.999, 1e-8, 0.1, 1)
+    m.forward(cuda_ids(tok), cuda_ids(tgt), sync=False)
+    m.synchronize()
+    n = m.num_params
+    for fn, arena in [(lib.gpt2_copy_params_out, PARAMS), (lib.gpt2_copy_grads_out, GRADS),
+                      (lib.gpt2_copy_m_out, ADAM_M), (lib.gpt2_copy_v_out, ADAM_V)]:
+        a = np.empty(n, np.float32)
+        assert fn(m._h, a.ctypes.data) == 0
+        assert np.array_equal(a, m.copy_out(arena))
+    p = np.random.default_rng(3).normal(0, 0.02, n).astype(np.float32)
+    assert lib.gpt2_copy_params_in(m._h, p.ctypes.data) == 0
+    assert np.array_equal(m.copy_out(PARAMS), p)
+    m.forward(cuda_ids(tok), cuda_ids(tgt), sync=False)
+    m.synchronize()
+    ptr = m.loss_device_ptr()
+    assert ptr
+    host = np.zeros(1, np.float32)
+    (err,) = rt.cudaMemcpy(host.ctypes.data, ptr, 4, rt.cudaMemcpyKind.cudaMemcpyDefault)
+    assert err == rt.cudaError_t.cudaSuccess
+    assert host[0] == np.float32(m.read_loss())
+    assert lib.gpt2_loss_device_ptr(None, None) == -1

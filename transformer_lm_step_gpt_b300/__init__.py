@@ -78,6 +78,12 @@ def load_library():
                               ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_copy_out": ([vp, i32, vp], ctypes.c_int),
         "gpt2_copy_in": ([vp, i32, vp], ctypes.c_int),
+        "gpt2_copy_params_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_grads_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_m_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_v_out": ([vp, vp], ctypes.c_int),
+        "gpt2_copy_params_in": ([vp, vp], ctypes.c_int),
+        "gpt2_loss_device_ptr": ([vp, ctypes.POINTER(vp)], ctypes.c_int),
         "gpt2_copy_losses_out": ([vp, vp], ctypes.c_int),
         "gpt2_copy_logits_out": ([vp, vp], ctypes.c_int),
         "gpt2_copy_residual_out": ([vp, i32, vp], ctypes.c_int),
@@ -233,6 +239,12 @@ class Model:
         a = np.empty((self.B * self.T, self.C), np.float32)
         self._check(self._lib.gpt2_copy_residual_out(self._h, int(layer), a.ctypes.data))
         return a
+
+    def loss_device_ptr(self) -> int:
+        """Device address of the fp32 mean loss of the last forward with targets."""
+        p = ctypes.c_void_p()
+        self._check(self._lib.gpt2_loss_device_ptr(self._h, ctypes.byref(p)))
+        return p.value
 
     def read_loss(self) -> float:
         """Mean loss of the last forward with targets (synchronises)."""

@@ -1085,6 +1085,18 @@ int gpt2_copy_residual_out(gpt2_model* m, int32_t layer, float* dst) {
   return e == cudaSuccess ? GPT2_OK : cuda_fail(m, e, "gpt2_copy_residual_out");
 }
 
+int gpt2_copy_params_out(gpt2_model* m, float* dst) { return gpt2_copy_out(m, GPT2_PARAMS, dst); }
+int gpt2_copy_grads_out(gpt2_model* m, float* dst) { return gpt2_copy_out(m, GPT2_GRADS, dst); }
+int gpt2_copy_m_out(gpt2_model* m, float* dst) { return gpt2_copy_out(m, GPT2_ADAM_M, dst); }
+int gpt2_copy_v_out(gpt2_model* m, float* dst) { return gpt2_copy_out(m, GPT2_ADAM_V, dst); }
+int gpt2_copy_params_in(gpt2_model* m, const float* src) { return gpt2_copy_in(m, GPT2_PARAMS, src); }
+
+int gpt2_loss_device_ptr(const gpt2_model* m, const float** out) {
+  if (!m || !out) return GPT2_ERR_ARG;
+  *out = m->loss;
+  return GPT2_OK;
+}
+
 int gpt2_read_loss(gpt2_model* m, float* host_loss) {
   if (!m || !host_loss) return GPT2_ERR_ARG;
   if (!m->fwd_targets) return fail(m, GPT2_ERR_STATE, "gpt2_read_loss: no forward with targets");
