@@ -160,6 +160,15 @@ GPT2_API int gpt2_adamw_step(gpt2_model* m, float lr, float beta1, float beta2,
  * last synchronising call (GPT2_ERR_TOKEN, GPT2_ERR_TIMEOUT). */
 GPT2_API int gpt2_synchronize(gpt2_model* m);
 
+/* Failure-path check of the bounded device waits: enqueues, on the model's
+ * stream, one kernel that waits on an mbarrier that nothing ever completes,
+ * with the same time limit as every wait of the library's kernels (2 s).
+ * The wait gives up, the kernel ends normally, and the next synchronising
+ * call reports GPT2_ERR_TIMEOUT and clears the condition; the model stays
+ * usable.  For tests of the error path: no fault, trap or hang is involved.
+ * Errors: GPT2_ERR_ARG (NULL model), GPT2_ERR_CUDA (launch failed). */
+GPT2_API int gpt2_expire_a_wait(gpt2_model* m);
+
 /* The configuration the model was built with. */
 GPT2_API int gpt2_get_config(const gpt2_model* m, gpt2_config* out);
 

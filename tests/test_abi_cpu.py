@@ -100,3 +100,7 @@ def test_named_copies_reject_a_null_model():
         assert fn(None, None) == -1
     out = ctypes.c_void_p()
     assert lib.gpt2_loss_device_ptr(None, ctypes.byref(out)) == -1
+
+
+def test_expire_a_wait_rejects_a_null_model():
+    assert tl.load_library().gpt2_expire_a_wait(None) == -1

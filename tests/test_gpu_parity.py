@@ -234,3 +234,22 @@ def test_named_array_copies_and_device_loss_pointer():
     assert err == rt.cudaError_t.cudaSuccess
     assert host[0] == np.float32(m.read_loss())
     assert lib.gpt2_loss_device_ptr(None, None) == -1
+
+
+def test_expired_wait_is_reported_and_the_model_recovers():
+    # a kernel whose bounded mbarrier wait nothing completes: it gives up
+    # after the limit, the next synchronising call reports GPT2_ERR_TIMEOUT,
+    # and the model keeps working (the same step repeats bit for bit)
+    import time
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=41)
+    tok, tgt = synthetic.batch(42, B, T, V)
+    l0 = m.forward(cuda_ids(tok), cuda_ids(tgt))
+    t0 = time.time()
+    m.expire_a_wait()
+    with pytest.raises(GPT2Error) as e:
+        m.synchronize()
+    assert e.value.code == -6
+    assert time.time() - t0 >= 1.5
+    m.synchronize()   # the condition was cleared
+    assert m.forward(cuda_ids(tok), cuda_ids(tgt)) == l0

@@ -71,6 +71,7 @@ def load_library():
         "gpt2_backward": ([vp], ctypes.c_int),
         "gpt2_adamw_step": ([vp, f32, f32, f32, f32, f32, i32], ctypes.c_int),
         "gpt2_synchronize": ([vp], ctypes.c_int),
+        "gpt2_expire_a_wait": ([vp], ctypes.c_int),
         "gpt2_get_config": ([vp, ctypes.POINTER(Config)], ctypes.c_int),
         "gpt2_num_params": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_num_tensors": ([vp, ctypes.POINTER(i32)], ctypes.c_int),
@@ -192,6 +193,11 @@ class Model:
 
     def adamw_step(self, lr, beta1, beta2, eps, weight_decay, t):
         self._check(self._lib.gpt2_adamw_step(self._h, lr, beta1, beta2, eps, weight_decay, int(t)))
+
+    def expire_a_wait(self):
+        """Enqueue a kernel whose bounded wait runs out (see gpt2_expire_a_wait):
+        the next synchronising call raises GPT2_ERR_TIMEOUT."""
+        self._check(self._lib.gpt2_expire_a_wait(self._h))
 
     def synchronize(self):
         self._check(self._lib.gpt2_synchronize(self._h))

@@ -775,6 +775,14 @@ int gpt2_synchronize(gpt2_model* m) {
   return check_device(m, "gpt2_synchronize");
 }
 
+int gpt2_expire_a_wait(gpt2_model* m) {
+  if (!m) return GPT2_ERR_ARG;
+  cudaSetDevice(m->device);
+  LaunchCtx c = ctx(m);
+  launch_expire_wait(c);
+  return after_launches(m, c, "gpt2_expire_a_wait");
+}
+
 int gpt2_get_config(const gpt2_model* m, gpt2_config* out) {
   if (!m || !out) return GPT2_ERR_ARG;
   *out = m->cfg;

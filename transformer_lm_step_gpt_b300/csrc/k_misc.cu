@@ -860,3 +860,22 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
   }
   return GPT2_OK;
 }
+
+// ============================================================ error path
+// One warp waits on a freshly initialised mbarrier that nothing arrives
+// on; the bounded wait (common.cuh) gives up after its time limit, records
+// DEVERR_TIMEOUT and the kernel returns.
+__global__ void expire_wait_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  mbar_wait(&bar, 0, err);
+}
+
+void launch_expire_wait(LaunchCtx& c) {
+  expire_wait_kernel<<<1, 32, 0, c.stream>>>(c.err);
+  (*c.launches)++;
+}

@@ -229,6 +229,10 @@ void launch_decode_embed(LaunchCtx& c, float* x, const int32_t* tok, const float
 void launch_decode_inputs(LaunchCtx& c, int32_t* tok_dst, const int32_t* tok_src, float* u_dst, const float* u_src,
                           int* pos_dst, int pos, float* temp_dst, float temperature, int B);
 
+// One kernel whose mbarrier wait nothing completes: it gives up after the
+// bounded-wait limit and sets DEVERR_TIMEOUT (tests of the error path).
+void launch_expire_wait(LaunchCtx& c);
+
 // Record the message gpt2_last_error(NULL) returns (entry points without a
 // model handle).
 void set_global_error(const char* msg);
