@@ -1,0 +1,412 @@
+"""Randomised interleaving checks of the mbarrier protocols of the three
+tensor-core attention kernels (CPU only; no GPU code runs).
+
+Each kernel's roles are modelled as actors that wait for barrier phases,
+arrive on barriers and touch buffers in the order the kernel's source does.
+Asynchronous work completes after random delays: a TMA copy writes its
+buffer until it arrives on its barrier, and the MMA groups issued by one
+thread run one after another, in issue order, reading their operands and
+writing their accumulators until they complete; a commit arrives once
+every group issued before it has completed (tcgen05.commit).  Warps that
+run the same code are separate actors (they touch disjoint rows), so one
+may run a sub-block ahead of another.
+
+For every interleaving tried:
+  * every actor finishes (no deadlock);
+  * no wait begins after its barrier has already completed the phase after
+    the one it waits for (a wait on the phase's parity bit would misread
+    the barrier: phase aliasing);
+  * no two agents (TMA, the MMA pipe, the warps) overlap on a buffer where
+    one of them writes it (a race).
+Planted mistakes in the models show that each check fires.  The models
+follow attn_fwd_tc_kernel, attn_bwd_dkv_tc_kernel and attn_bwd_dq_tc_kernel
+in csrc/k_attn_tc.cu; a change to a kernel's hand-offs changes its model.
+"""
+import random
+
+import pytest
+
+# warps and ring stages as the kernels are compiled: 8 softmax warps and 3
+# key/value stages (forward); 16 compute warps and 4 query stages (dK/dV);
+# 8 compute warps, 3 key and 2 value stages (dQ)
+FWD_WARPS, FWD_STAGES = 8, 3
+DKV_WARPS, DKV_STAGES = 16, 4
+DQ_WARPS, DQ_K_STAGES, DQ_V_STAGES = 8, 3, 2
+
+
+class Sim:
+    def __init__(self, seed, plant=None):
+        self.rnd = random.Random(seed)
+        self.plant = plant  # the name of a planted mistake, or None
+        self.t = 0
+        self.done = {}      # barrier -> completed phases
+        self.count = {}     # barrier -> arrivals in the current phase
+        self.need = {}      # barrier -> arrivals that complete a phase
+        self.pending = []   # (time, callback)
+        self.pipe_t = 0     # completion time of the last MMA group issued
+        self.acc = []       # (buffer, "r" | "w", agent, t0, t1)
+        self.errors = []
+
+    # ---------------------------------------------------------- barriers
+    def bar(self, name, need=1):
+        self.done[name] = 0
+        self.count[name] = 0
+        self.need[name] = need
+
+    def arrive(self, name):
+        self.count[name] += 1
+        if self.count[name] == self.need[name]:
+            self.count[name] = 0
+            self.done[name] += 1
+
+    def wait(self, name, k):  # for the completion of phase k (k = -1: none yet)
+        if self.done[name] >= k + 2:
+            self.errors.append("aliased wait: %s phase %d (completed %d)" % (name, k, self.done[name]))
+        while self.done[name] < k + 1:
+            yield
+
+    # ---------------------------------------------------------- agents
+    def tma(self, name, *bufs):  # a copy into bufs whose bytes complete the barrier
+        t1 = self.t + self.rnd.randint(1, 40)
+        for b in bufs:
+            self.acc.append((b, "w", "tma", self.t, t1))
+        self.pending.append((t1, lambda: self.arrive(name)))
+
+    def mma(self, reads=(), writes=()):  # one group of MMAs, run in issue order
+        t0 = max(self.pipe_t, self.t)
+        self.pipe_t = t0 + self.rnd.randint(1, 30)
+        for b in reads:
+            self.acc.append((b, "r", "mma", t0, self.pipe_t))
+        for b in writes:
+            self.acc.append((b, "w", "mma", t0, self.pipe_t))
+
+    def commit(self, name):
+        self.pending.append((max(self.pipe_t, self.t + 1), lambda: self.arrive(name)))
+
+    def touch(self, agent, mode, t0, *bufs):  # a warp's access from t0 until now
+        for b in bufs:
+            self.acc.append((b, mode, agent, t0, self.t))
+
+    def work(self, lo=0, hi=4):
+        for _ in range(self.rnd.randint(lo, hi)):
+            yield
+
+    # ---------------------------------------------------------- run
+    def run(self, actors, limit=400000):
+        alive = [True] * len(actors)
+        for _ in range(limit):
+            self.t += 1
+            due = [p for p in self.pending if p[0] <= self.t]
+            self.pending = [p for p in self.pending if p[0] > self.t]
+            for _, fn in due:
+                fn()
+            order = list(range(len(actors)))
+            self.rnd.shuffle(order)
+            for i in order:
+                if alive[i] and self.rnd.random() < 0.7:
+                    try:
+                        next(actors[i])
+                    except StopIteration:
+                        alive[i] = False
+            if not any(alive) and not self.pending:
+                self.check_races()
+                return
+        self.errors.append("no progress (deadlock)")
+
+    def check_races(self):
+        by_buf = {}
+        for a in self.acc:
+            by_buf.setdefault(a[0], []).append(a)
+        for buf, accs in by_buf.items():
+            for i, (_, m1, g1, s1, e1) in enumerate(accs):
+                for (_, m2, g2, s2, e2) in accs[i + 1:]:
+                    if g1 == g2 and g1 != "tma":
+                        continue  # one pipe in order, or warps on disjoint rows
+                    if "w" in (m1, m2) and s1 < e2 and s2 < e1:
+                        self.errors.append("race on %s: %s %s [%d,%d) / %s %s [%d,%d)"
+                                           % (buf, g1, m1, s1, e1, g2, m2, s2, e2))
+                        return
+
+
+# -------------------------------------------------------------- forward
+def forward(nsub, seed, plant=None, nsoft=FWD_WARPS, stages=FWD_STAGES):
+    """Loader warp: q once, then k(j), v(j) into ring stage j % stages once
+    S(j - stages), PV(j - stages) have read it.  MMA warp: S(0), S(1), then
+    per sub-block PV(j) once P(j) is written and S(j + 2) after it.  Softmax
+    warps: S(j) -> P(j) in shared memory (after PV(j - 2) has read that
+    buffer), with an occasional rescale of O in tensor memory once PV(j - 1)
+    is done; O read at the end."""
+    sim = Sim(seed, plant)
+    sim.bar("q")
+    for s in range(stages):
+        for n in ("kf%d", "vf%d", "ke%d", "ve%d"):
+            sim.bar(n % s)
+    for i in range(2):
+        sim.bar("s%d" % i)
+        sim.bar("o%d" % i)
+        sim.bar("p%d" % i, nsoft)
+    if plant == "one_p_barrier":   # P(j) written: one barrier for both buffers
+        P, Pk = (lambda j: "p0"), (lambda j: j)
+    else:
+        P, Pk = (lambda j: "p%d" % (j & 1)), (lambda j: j >> 1)
+
+    def loader():
+        sim.tma("q", "sQ")
+        for j in range(nsub):
+            s = j % stages
+            if j >= stages and plant != "k_refill_unguarded":
+                yield from sim.wait("ke%d" % s, j // stages - 1)
+            sim.tma("kf%d" % s, "sK%d" % s)
+            if j >= stages:
+                yield from sim.wait("ve%d" % s, j // stages - 1)
+            sim.tma("vf%d" % s, "sV%d" % s)
+
+    def issuer():
+        def issue_s(j):
+            s = j % stages
+            yield from sim.wait("kf%d" % s, j // stages)
+            sim.mma(reads=("sQ", "sK%d" % s), writes=("S%d" % (j & 1),))
+            sim.commit("s%d" % (j & 1))
+            sim.commit("ke%d" % s)
+        yield from sim.wait("q", 0)
+        yield from issue_s(0)
+        if nsub > 1:
+            yield from issue_s(1)
+        for j in range(nsub):
+            if plant == "one_p_barrier":
+                yield from sim.work(0, 60)      # a slow issuer
+            yield from sim.wait(P(j), Pk(j))
+            s = j % stages
+            yield from sim.wait("vf%d" % s, j // stages)
+            sim.mma(reads=("sP%d" % (j & 1), "sV%d" % s), writes=("O",))
+            sim.commit("o%d" % (j & 1))
+            sim.commit("ve%d" % s)
+            if j + 2 < nsub:
+                yield from issue_s(j + 2)
+
+    def softmax():
+        for j in range(nsub):
+            yield from sim.wait("s%d" % (j & 1), j >> 1)
+            t0 = sim.t
+            yield from sim.work()
+            if j > 0 and sim.rnd.random() < 0.3:   # a lazy rescale of O
+                if plant != "rescale_unguarded":
+                    yield from sim.wait("o%d" % ((j - 1) & 1), (j - 1) >> 1)
+                t1 = sim.t
+                yield from sim.work(1, 4)
+                sim.touch("warp", "w", t1, "O")
+            if j >= 2:
+                yield from sim.wait("o%d" % (j & 1), (j - 2) >> 1)
+            t2 = sim.t
+            yield from sim.work(1, 4)
+            sim.touch("warp", "w", t2, "sP%d" % (j & 1))
+            sim.touch("warp", "r", t0, "S%d" % (j & 1))
+            sim.arrive(P(j))
+        yield from sim.wait("o%d" % ((nsub - 1) & 1), (nsub - 1) >> 1)
+        t3 = sim.t
+        yield from sim.work(1, 4)
+        sim.touch("warp", "r", t3, "O")
+
+    sim.run([loader(), issuer()] + [softmax() for _ in range(nsoft)])
+    return sim.errors
+
+
+# -------------------------------------------------------------- dK / dV
+def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES):
+    """Loader warp: k, v once; q(j), dy(j) (and, staged, that sub-block's
+    lse / D) into ring stage j % stages once dV, dK(j - stages) have read it;
+    not staged, the whole block's lse / D by plain stores first.  MMA warp:
+    S^T(j), dP^T(j) into tensor memory once the warps have copied out
+    S^T(j - 1), dP^T(j - 1); then dV, dK(j - 1) from P^T, dS^T(j - 1).
+    Compute warps: S^T, dP^T -> P^T, dS^T in tensor memory (after dV,
+    dK(j - 1) have read them); dV, dK read at the end."""
+    sim = Sim(seed, plant)
+    for n in ("kv", "ld", "sf", "pe", "done"):
+        sim.bar(n)
+    for s in range(stages):
+        sim.bar("qf%d" % s)
+        sim.bar("qe%d" % s)
+    sim.bar("se", ncomp)
+    sim.bar("pf", ncomp)
+
+    def stage_bufs(s):
+        return ("sQ%d" % s, "sD%d" % s) + (("sLD%d" % s,) if staged else ())
+
+    def loader():
+        sim.tma("kv", "sK", "sV")
+        for j in range(min(nsub, stages)):
+            sim.tma("qf%d" % (j % stages), *stage_bufs(j % stages))
+        if not staged:
+            t0 = sim.t
+            yield from sim.work(1, 6)
+            sim.touch("loader", "w", t0, "sLD")
+        sim.arrive("ld")
+        for j in range(stages, nsub):
+            s = j % stages
+            yield from sim.wait("qe%d" % s, j // stages - 1)
+            sim.tma("qf%d" % s, *stage_bufs(s))
+
+    def mma():
+        yield from sim.wait("kv", 0)
+        for j in range(nsub + 1):
+            if j < nsub:
+                s = j % stages
+                yield from sim.wait("qf%d" % s, j // stages)
+                if j > 0:
+                    yield from sim.wait("se", j - 1)
+                sim.mma(reads=("sK", "sV", "sQ%d" % s, "sD%d" % s), writes=("St", "dPt"))
+                sim.commit("sf")
+            if j >= 1:
+                jj = j - 1
+                s = jj % stages
+                yield from sim.wait("pf", jj)
+                sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s), writes=("dV", "dK"))
+                sim.commit("pe")
+                sim.commit("qe%d" % s)
+        sim.commit("done")
+
+    def compute():
+        yield from sim.wait("ld", 0)
+        for j in range(nsub):
+            s = j % stages
+            yield from sim.wait("sf", j)
+            t0 = sim.t
+            yield from sim.work(1, 3)
+            sim.touch("warp", "r", t0, "St", "dPt")
+            sim.arrive("se")
+            if staged:  # the stage's lse / D arrive with its q / dy tiles
+                yield from sim.wait("qf%d" % s, j // stages)
+            t1 = sim.t
+            yield from sim.work()
+            if j > 0 and plant != "p_overwrite_unguarded":
+                yield from sim.wait("pe", j - 1)
+            t2 = sim.t
+            yield from sim.work(1, 3)
+            sim.touch("warp", "w", t2, "Pt", "dSt")
+            sim.touch("warp", "r", t1, "sLD%d" % s if staged else "sLD")
+            sim.arrive("pf")
+        yield from sim.wait("done", 0)
+        t3 = sim.t
+        yield from sim.work(1, 3)
+        sim.touch("warp", "r", t3, "dV", "dK")
+
+    sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
+    return sim.errors
+
+
+# -------------------------------------------------------------- dQ
+def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES):
+    """One warp loads and issues: q, dy once, k(0..kst-1), v(0..vst-1); S(0),
+    dP(0).  Per sub-block j: once the warps have copied out S(j), dP(j),
+    v(j + vst) into v's stage and S(j + 1), dP(j + 1); once dS(j) is in
+    shared memory buffer j % 2, dQ(j); once dQ(j - 1) has read k's stage,
+    k(j + 2) into it.  Compute warps: S(j), dP(j) -> dS(j) (after dQ(j - 2)
+    has read the buffer); dQ read at the end."""
+    sim = Sim(seed, plant)
+    for n in ("q", "sf", "done"):
+        sim.bar(n)
+    for s in range(kst):
+        sim.bar("kf%d" % s)
+        sim.bar("ke%d" % s)
+    for s in range(vst):
+        sim.bar("vf%d" % s)
+    sim.bar("se", ncomp)
+    for i in range(2):
+        sim.bar("pf%d" % i, ncomp)
+        sim.bar("pe%d" % i)
+
+    def issuer():
+        def load_k(j):
+            sim.tma("kf%d" % (j % kst), "sK%d" % (j % kst))
+
+        def load_v(j):
+            sim.tma("vf%d" % (j % vst), "sV%d" % (j % vst))
+
+        def issue_sdp(j):
+            ks, vs = j % kst, j % vst
+            yield from sim.wait("kf%d" % ks, j // kst)
+            yield from sim.wait("vf%d" % vs, j // vst)
+            sim.mma(reads=("sQ", "sD", "sK%d" % ks, "sV%d" % vs), writes=("S", "dP"))
+            sim.commit("sf")
+        sim.tma("q", "sQ", "sD")
+        for j in range(min(kst, nsub)):
+            load_k(j)
+        for j in range(min(vst, nsub)):
+            load_v(j)
+        yield from sim.wait("q", 0)
+        yield from issue_sdp(0)
+        for j in range(nsub):
+            if j + 1 < nsub:
+                yield from sim.wait("se", j)
+                if j + vst < nsub:
+                    load_v(j + vst)
+                yield from issue_sdp(j + 1)
+            yield from sim.wait("pf%d" % (j & 1), j >> 1)
+            ks = j % kst
+            sim.mma(reads=("sS%d" % (j & 1), "sK%d" % ks), writes=("dQ",))
+            sim.commit("pe%d" % (j & 1))
+            sim.commit("ke%d" % ks)
+            if j >= 1 and j + 2 < nsub:
+                if plant != "k_refill_unguarded":
+                    yield from sim.wait("ke%d" % ((j - 1) % kst), (j - 1) // kst)
+                load_k(j + 2)
+        sim.commit("done")
+
+    def compute():
+        for j in range(nsub):
+            yield from sim.wait("sf", j)
+            t0 = sim.t
+            yield from sim.work(1, 3)
+            sim.touch("warp", "r", t0, "S", "dP")
+            sim.arrive("se")
+            # dQ(j - 2) has read dS buffer j % 2; for j < 2 the wait is on
+            # phase -1 (the barrier must still be in phase 0)
+            k = (j - 2) >> 1 if plant != "p_wrong_phase" else j >> 1
+            yield from sim.wait("pe%d" % (j & 1), k)
+            t1 = sim.t
+            yield from sim.work(1, 4)
+            sim.touch("warp", "w", t1, "sS%d" % (j & 1))
+            sim.arrive("pf%d" % (j & 1))
+        yield from sim.wait("done", 0)
+        t2 = sim.t
+        yield from sim.work(1, 3)
+        sim.touch("warp", "r", t2, "dQ")
+
+    sim.run([issuer()] + [compute() for _ in range(ncomp)])
+    return sim.errors
+
+
+NSUB = list(range(1, 10)) + [16, 17]
+
+
+@pytest.mark.parametrize("model", [forward, dkv, dq])
+def test_protocol_has_no_deadlock_aliased_wait_or_race(model):
+    for nsub in NSUB:
+        for seed in range(8):
+            errs = model(nsub, seed)
+            assert not errs, (model.__name__, nsub, seed, errs[:3])
+
+
+def test_dkv_protocol_with_whole_block_lse_preload():
+    for nsub in (1, 3, 5, 8):
+        for seed in range(8):
+            errs = dkv(nsub, seed, staged=False)
+            assert not errs, (nsub, seed, errs[:3])
+
+
+@pytest.mark.parametrize("model,plant,kind", [
+    (forward, "one_p_barrier", "aliased wait"),
+    (forward, "k_refill_unguarded", "race on sK"),
+    (forward, "rescale_unguarded", "race on O"),
+    (dkv, "p_overwrite_unguarded", "race on Pt"),
+    (dq, "k_refill_unguarded", "race on sK"),
+    (dq, "p_wrong_phase", "no progress"),
+])
+def test_the_checker_finds_a_planted_mistake(model, plant, kind):
+    found = []
+    for nsub in range(4, 12):
+        for seed in range(10):
+            found += model(nsub, seed, plant=plant)
+        if any(kind in e for e in found):
+            return
+    pytest.fail("%s with %s: %s" % (model.__name__, plant, found[:3]))
