@@ -1,30 +1,18 @@
 """Randomised interleaving checks of the mbarrier protocols of the three
 tensor-core attention kernels (CPU only; no GPU code runs).
 
-Each kernel's roles are modelled as actors that wait for barrier phases,
-arrive on barriers and touch buffers in the order the kernel's source does.
-Asynchronous work completes after random delays: a TMA copy writes its
-buffer until it arrives on its barrier, and the MMA groups issued by one
-thread run one after another, in issue order, reading their operands and
-writing their accumulators until they complete; a commit arrives once
-every group issued before it has completed (tcgen05.commit).  Warps that
-run the same code are separate actors (they touch disjoint rows), so one
-may run a sub-block ahead of another.
-
-For every interleaving tried:
-  * every actor finishes (no deadlock);
-  * no wait begins after its barrier has already completed the phase after
-    the one it waits for (a wait on the phase's parity bit would misread
-    the barrier: phase aliasing);
-  * no two agents (TMA, the MMA pipe, the warps) overlap on a buffer where
-    one of them writes it (a race).
-Planted mistakes in the models show that each check fires.  The models
+Each kernel's roles are actors of the simulator in protocol_sim.py, which
+checks every interleaving tried for deadlock, aliased phase waits,
+arrivals that land in another phase, races on shared-memory and TMEM
+buffers, and work still in flight at exit.  Warps that run the same code
+are separate actors, so one may run a sub-block ahead of another.
+Planted mistakes in the models show that the checks fire.  The models
 follow attn_fwd_tc_kernel, attn_bwd_dkv_tc_kernel and attn_bwd_dq_tc_kernel
 in csrc/k_attn_tc.cu; a change to a kernel's hand-offs changes its model.
 """
-import random
-
 import pytest
+
+from protocol_sim import Sim, find
 
 # warps and ring stages as the kernels are compiled: 8 softmax warps and 3
 # key/value stages (forward); 16 compute warps and 4 query stages (dK/dV);
@@ -32,100 +20,6 @@ import pytest
 FWD_WARPS, FWD_STAGES = 8, 3
 DKV_WARPS, DKV_STAGES = 16, 4
 DQ_WARPS, DQ_K_STAGES, DQ_V_STAGES = 8, 3, 2
-
-
-class Sim:
-    def __init__(self, seed, plant=None):
-        self.rnd = random.Random(seed)
-        self.plant = plant  # the name of a planted mistake, or None
-        self.t = 0
-        self.done = {}      # barrier -> completed phases
-        self.count = {}     # barrier -> arrivals in the current phase
-        self.need = {}      # barrier -> arrivals that complete a phase
-        self.pending = []   # (time, callback)
-        self.pipe_t = 0     # completion time of the last MMA group issued
-        self.acc = []       # (buffer, "r" | "w", agent, t0, t1)
-        self.errors = []
-
-    # ---------------------------------------------------------- barriers
-    def bar(self, name, need=1):
-        self.done[name] = 0
-        self.count[name] = 0
-        self.need[name] = need
-
-    def arrive(self, name):
-        self.count[name] += 1
-        if self.count[name] == self.need[name]:
-            self.count[name] = 0
-            self.done[name] += 1
-
-    def wait(self, name, k):  # for the completion of phase k (k = -1: none yet)
-        if self.done[name] >= k + 2:
-            self.errors.append("aliased wait: %s phase %d (completed %d)" % (name, k, self.done[name]))
-        while self.done[name] < k + 1:
-            yield
-
-    # ---------------------------------------------------------- agents
-    def tma(self, name, *bufs):  # a copy into bufs whose bytes complete the barrier
-        t1 = self.t + self.rnd.randint(1, 40)
-        for b in bufs:
-            self.acc.append((b, "w", "tma", self.t, t1))
-        self.pending.append((t1, lambda: self.arrive(name)))
-
-    def mma(self, reads=(), writes=()):  # one group of MMAs, run in issue order
-        t0 = max(self.pipe_t, self.t)
-        self.pipe_t = t0 + self.rnd.randint(1, 30)
-        for b in reads:
-            self.acc.append((b, "r", "mma", t0, self.pipe_t))
-        for b in writes:
-            self.acc.append((b, "w", "mma", t0, self.pipe_t))
-
-    def commit(self, name):
-        self.pending.append((max(self.pipe_t, self.t + 1), lambda: self.arrive(name)))
-
-    def touch(self, agent, mode, t0, *bufs):  # a warp's access from t0 until now
-        for b in bufs:
-            self.acc.append((b, mode, agent, t0, self.t))
-
-    def work(self, lo=0, hi=4):
-        for _ in range(self.rnd.randint(lo, hi)):
-            yield
-
-    # ---------------------------------------------------------- run
-    def run(self, actors, limit=400000):
-        alive = [True] * len(actors)
-        for _ in range(limit):
-            self.t += 1
-            due = [p for p in self.pending if p[0] <= self.t]
-            self.pending = [p for p in self.pending if p[0] > self.t]
-            for _, fn in due:
-                fn()
-            order = list(range(len(actors)))
-            self.rnd.shuffle(order)
-            for i in order:
-                if alive[i] and self.rnd.random() < 0.7:
-                    try:
-                        next(actors[i])
-                    except StopIteration:
-                        alive[i] = False
-            if not any(alive) and not self.pending:
-                self.check_races()
-                return
-        self.errors.append("no progress (deadlock)")
-
-    def check_races(self):
-        by_buf = {}
-        for a in self.acc:
-            by_buf.setdefault(a[0], []).append(a)
-        for buf, accs in by_buf.items():
-            for i, (_, m1, g1, s1, e1) in enumerate(accs):
-                for (_, m2, g2, s2, e2) in accs[i + 1:]:
-                    if g1 == g2 and g1 != "tma":
-                        continue  # one pipe in order, or warps on disjoint rows
-                    if "w" in (m1, m2) and s1 < e2 and s2 < e1:
-                        self.errors.append("race on %s: %s %s [%d,%d) / %s %s [%d,%d)"
-                                           % (buf, g1, m1, s1, e1, g2, m2, s2, e2))
-                        return
 
 
 # -------------------------------------------------------------- forward
@@ -151,23 +45,23 @@ def forward(nsub, seed, plant=None, nsoft=FWD_WARPS, stages=FWD_STAGES):
         P, Pk = (lambda j: "p%d" % (j & 1)), (lambda j: j >> 1)
 
     def loader():
-        sim.tma("q", "sQ")
+        sim.tma("q", "sQ", phase=0)
         for j in range(nsub):
             s = j % stages
             if j >= stages and plant != "k_refill_unguarded":
                 yield from sim.wait("ke%d" % s, j // stages - 1)
-            sim.tma("kf%d" % s, "sK%d" % s)
+            sim.tma("kf%d" % s, "sK%d" % s, phase=j // stages)
             if j >= stages:
                 yield from sim.wait("ve%d" % s, j // stages - 1)
-            sim.tma("vf%d" % s, "sV%d" % s)
+            sim.tma("vf%d" % s, "sV%d" % s, phase=j // stages)
 
     def issuer():
         def issue_s(j):
             s = j % stages
             yield from sim.wait("kf%d" % s, j // stages)
             sim.mma(reads=("sQ", "sK%d" % s), writes=("S%d" % (j & 1),))
-            sim.commit("s%d" % (j & 1))
-            sim.commit("ke%d" % s)
+            sim.commit("s%d" % (j & 1), phase=j >> 1)
+            sim.commit("ke%d" % s, phase=j // stages)
         yield from sim.wait("q", 0)
         yield from issue_s(0)
         if nsub > 1:
@@ -179,8 +73,8 @@ def forward(nsub, seed, plant=None, nsoft=FWD_WARPS, stages=FWD_STAGES):
             s = j % stages
             yield from sim.wait("vf%d" % s, j // stages)
             sim.mma(reads=("sP%d" % (j & 1), "sV%d" % s), writes=("O",))
-            sim.commit("o%d" % (j & 1))
-            sim.commit("ve%d" % s)
+            sim.commit("o%d" % (j & 1), phase=j >> 1)
+            sim.commit("ve%d" % s, phase=j // stages)
             if j + 2 < nsub:
                 yield from issue_s(j + 2)
 
@@ -201,7 +95,7 @@ def forward(nsub, seed, plant=None, nsoft=FWD_WARPS, stages=FWD_STAGES):
             yield from sim.work(1, 4)
             sim.touch("warp", "w", t2, "sP%d" % (j & 1))
             sim.touch("warp", "r", t0, "S%d" % (j & 1))
-            sim.arrive(P(j))
+            sim.arrive(P(j), phase=Pk(j))
         yield from sim.wait("o%d" % ((nsub - 1) & 1), (nsub - 1) >> 1)
         t3 = sim.t
         yield from sim.work(1, 4)
@@ -233,18 +127,18 @@ def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES)
         return ("sQ%d" % s, "sD%d" % s) + (("sLD%d" % s,) if staged else ())
 
     def loader():
-        sim.tma("kv", "sK", "sV")
+        sim.tma("kv", "sK", "sV", phase=0)
         for j in range(min(nsub, stages)):
-            sim.tma("qf%d" % (j % stages), *stage_bufs(j % stages))
+            sim.tma("qf%d" % (j % stages), *stage_bufs(j % stages), phase=0)
         if not staged:
             t0 = sim.t
             yield from sim.work(1, 6)
             sim.touch("loader", "w", t0, "sLD")
-        sim.arrive("ld")
+        sim.arrive("ld", phase=0)
         for j in range(stages, nsub):
             s = j % stages
             yield from sim.wait("qe%d" % s, j // stages - 1)
-            sim.tma("qf%d" % s, *stage_bufs(s))
+            sim.tma("qf%d" % s, *stage_bufs(s), phase=j // stages)
 
     def mma():
         yield from sim.wait("kv", 0)
@@ -255,15 +149,15 @@ def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES)
                 if j > 0:
                     yield from sim.wait("se", j - 1)
                 sim.mma(reads=("sK", "sV", "sQ%d" % s, "sD%d" % s), writes=("St", "dPt"))
-                sim.commit("sf")
+                sim.commit("sf", phase=j)
             if j >= 1:
                 jj = j - 1
                 s = jj % stages
                 yield from sim.wait("pf", jj)
                 sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s), writes=("dV", "dK"))
-                sim.commit("pe")
-                sim.commit("qe%d" % s)
-        sim.commit("done")
+                sim.commit("pe", phase=jj)
+                sim.commit("qe%d" % s, phase=jj // stages)
+        sim.commit("done", phase=0)
 
     def compute():
         yield from sim.wait("ld", 0)
@@ -273,7 +167,7 @@ def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES)
             t0 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t0, "St", "dPt")
-            sim.arrive("se")
+            sim.arrive("se", phase=j)
             if staged:  # the stage's lse / D arrive with its q / dy tiles
                 yield from sim.wait("qf%d" % s, j // stages)
             t1 = sim.t
@@ -284,7 +178,7 @@ def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES)
             yield from sim.work(1, 3)
             sim.touch("warp", "w", t2, "Pt", "dSt")
             sim.touch("warp", "r", t1, "sLD%d" % s if staged else "sLD")
-            sim.arrive("pf")
+            sim.arrive("pf", phase=j)
         yield from sim.wait("done", 0)
         t3 = sim.t
         yield from sim.work(1, 3)
@@ -317,18 +211,18 @@ def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES)
 
     def issuer():
         def load_k(j):
-            sim.tma("kf%d" % (j % kst), "sK%d" % (j % kst))
+            sim.tma("kf%d" % (j % kst), "sK%d" % (j % kst), phase=j // kst)
 
         def load_v(j):
-            sim.tma("vf%d" % (j % vst), "sV%d" % (j % vst))
+            sim.tma("vf%d" % (j % vst), "sV%d" % (j % vst), phase=j // vst)
 
         def issue_sdp(j):
             ks, vs = j % kst, j % vst
             yield from sim.wait("kf%d" % ks, j // kst)
             yield from sim.wait("vf%d" % vs, j // vst)
             sim.mma(reads=("sQ", "sD", "sK%d" % ks, "sV%d" % vs), writes=("S", "dP"))
-            sim.commit("sf")
-        sim.tma("q", "sQ", "sD")
+            sim.commit("sf", phase=j)
+        sim.tma("q", "sQ", "sD", phase=0)
         for j in range(min(kst, nsub)):
             load_k(j)
         for j in range(min(vst, nsub)):
@@ -344,13 +238,13 @@ def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES)
             yield from sim.wait("pf%d" % (j & 1), j >> 1)
             ks = j % kst
             sim.mma(reads=("sS%d" % (j & 1), "sK%d" % ks), writes=("dQ",))
-            sim.commit("pe%d" % (j & 1))
-            sim.commit("ke%d" % ks)
+            sim.commit("pe%d" % (j & 1), phase=j >> 1)
+            sim.commit("ke%d" % ks, phase=j // kst)
             if j >= 1 and j + 2 < nsub:
                 if plant != "k_refill_unguarded":
                     yield from sim.wait("ke%d" % ((j - 1) % kst), (j - 1) // kst)
                 load_k(j + 2)
-        sim.commit("done")
+        sim.commit("done", phase=0)
 
     def compute():
         for j in range(nsub):
@@ -358,7 +252,7 @@ def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES)
             t0 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t0, "S", "dP")
-            sim.arrive("se")
+            sim.arrive("se", phase=j)
             # dQ(j - 2) has read dS buffer j % 2; for j < 2 the wait is on
             # phase -1 (the barrier must still be in phase 0)
             k = (j - 2) >> 1 if plant != "p_wrong_phase" else j >> 1
@@ -366,7 +260,7 @@ def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES)
             t1 = sim.t
             yield from sim.work(1, 4)
             sim.touch("warp", "w", t1, "sS%d" % (j & 1))
-            sim.arrive("pf%d" % (j & 1))
+            sim.arrive("pf%d" % (j & 1), phase=j >> 1)
         yield from sim.wait("done", 0)
         t2 = sim.t
         yield from sim.work(1, 3)
@@ -403,10 +297,5 @@ def test_dkv_protocol_with_whole_block_lse_preload():
     (dq, "p_wrong_phase", "no progress"),
 ])
 def test_the_checker_finds_a_planted_mistake(model, plant, kind):
-    found = []
-    for nsub in range(4, 12):
-        for seed in range(10):
-            found += model(nsub, seed, plant=plant)
-        if any(kind in e for e in found):
-            return
-    pytest.fail("%s with %s: %s" % (model.__name__, plant, found[:3]))
+    errs = find(model, plant, kind, range(4, 12))
+    assert errs, "%s with %s: not found" % (model.__name__, plant)
