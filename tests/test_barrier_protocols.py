@@ -1,5 +1,6 @@
 """Randomised interleaving checks of the mbarrier protocols of the three
-tensor-core attention kernels (CPU only; no GPU code runs).
+tensor-core attention kernels and of the LayerNorm backward's row ring
+(CPU only; no GPU code runs).
 
 Each kernel's roles are actors of the simulator in protocol_sim.py, which
 checks every interleaving tried for deadlock, aliased phase waits,
@@ -7,8 +8,9 @@ arrivals that land in another phase, races on shared-memory and TMEM
 buffers, and work still in flight at exit.  Warps that run the same code
 are separate actors, so one may run a sub-block ahead of another.
 Planted mistakes in the models show that the checks fire.  The models
-follow attn_fwd_tc_kernel, attn_bwd_dkv_tc_kernel and attn_bwd_dq_tc_kernel
-in csrc/k_attn_tc.cu; a change to a kernel's hand-offs changes its model.
+follow attn_fwd_tc_kernel, attn_bwd_dkv_tc_kernel, attn_bwd_dq_tc_kernel
+(csrc/k_attn_tc.cu) and layernorm_bwd_kernel (csrc/k_misc.cu); a change
+to a kernel's hand-offs changes its model.
 """
 import pytest
 
@@ -299,3 +301,45 @@ def test_dkv_protocol_with_whole_block_lse_preload():
 def test_the_checker_finds_a_planted_mistake(model, plant, kind):
     errs = find(model, plant, kind, range(4, 12))
     assert errs, "%s with %s: not found" % (model.__name__, plant)
+
+
+# -------------------------------------------------------------- LayerNorm backward
+LNB_STAGES = 2      # rows in flight per warp
+
+
+def ln_bwd_ring(nrows, seed, plant=None, nwarps=3, stages=LNB_STAGES):
+    """layernorm_bwd_kernel: warp w of nwarps takes rows w, w + nwarps, ...;
+    its lane 0 bulk-copies the first `stages` of them (dy, x and the old
+    residual gradient) into its own ring and, once the whole warp is done
+    with a stage (__syncwarp), the row `stages` rows further on into it."""
+    sim = Sim(seed, plant)
+
+    def warp(w):
+        for s in range(stages):
+            sim.bar("b%d_%d" % (w, s))
+        rows = list(range(w, nrows, nwarps))
+        for i in range(min(stages, len(rows))):
+            sim.tma("b%d_%d" % (w, i), "ring%d_%d" % (w, i), phase=0)
+        for it, _ in enumerate(rows):
+            s = it % stages
+            yield from sim.wait("b%d_%d" % (w, s), it // stages)
+            t0 = sim.t
+            yield from sim.work(1, 4)
+            if plant != "early_refill":
+                sim.touch("lanes%d" % w, "r", t0, "ring%d_%d" % (w, s))
+                yield                                   # __syncwarp: every lane is done with the stage
+            else:                                       # no __syncwarp: a lane may still be reading
+                sim.touch("lanes%d" % w, "r", t0, "ring%d_%d" % (w, s), until=sim.t + 3)
+            if it + stages < len(rows):
+                sim.tma("b%d_%d" % (w, s), "ring%d_%d" % (w, s), phase=(it + stages) // stages)
+
+    sim.run([warp(w) for w in range(nwarps)])
+    return sim.errors
+
+
+def test_layernorm_backward_row_ring():
+    for nrows in (1, 2, 5, 9, 20):
+        for seed in range(6):
+            errs = ln_bwd_ring(nrows, seed)
+            assert not errs, (nrows, seed, errs[:3])
+    assert find(ln_bwd_ring, "early_refill", "race on ring", [9, 20])
