@@ -1,6 +1,8 @@
-"""bench.py's N > 1 path (independent replicas, one per GPU) on CPU with
-two gloo ranks: the slowest rank's time and the sum of all ranks' tokens
-make the whole-job throughput."""
+"""bench.py on CPU: the N > 1 path (independent replicas, one per GPU) with
+two gloo ranks (the slowest rank's time and the sum of all ranks' tokens
+make the whole-job throughput); the reference arm's JSON line (the CPU
+oracle on bounded samples); the warm-up floor; and the library's arm
+failing loudly, with no result line, where there is no GPU."""
 import os
 import socket
 
@@ -48,3 +50,43 @@ def test_replica_aggregation_two_gloo_ranks():
         assert ms == 150.0                    # max over ranks
         assert tokens == 2 * 16 * 1024 * 50   # sum over ranks
         assert abs(value - tokens / 0.150) < 1e-6 * value
+
+
+def _run_bench(*args, timeout=300):
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    return subprocess.run([sys.executable, os.path.join(root, "bench.py"), *args], cwd=root,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_prints_one_json_line_with_the_contract_keys():
+    import json
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "3")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in out, k
+    assert out["impl"] == "reference"
+    assert out["steps"] == 1 and out["warmup"] == 3 and out["n_gpus"] == 1
+    assert out["value"] > 0 and out["higher_is_better"] is True
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["cores"] >= 1
+    assert out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"] == dict(value=out["value"], unit=out["unit"], h2d_bytes_per_step=0, d2h_bytes_per_step=0)
+    assert out["config"]["workload"]
+
+
+def test_bench_rejects_fewer_than_three_warmup_steps():
+    r = _run_bench("--impl", "reference", "--steps", "1", "--warmup", "2", timeout=120)
+    assert r.returncode != 0 and "warmup" in r.stderr
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_our_arm_fails_loudly_without_a_gpu():
+    # no CPU fallback: without a device the library's arm exits non-zero and prints no result line
+    r = _run_bench("--steps", "1", "--warmup", "3", "--no-cpu-baseline", timeout=120)
+    assert r.returncode != 0
+    assert not any(l.startswith("{") for l in r.stdout.splitlines())
