@@ -166,7 +166,9 @@ def _sdpa(qkv, B, T, C, NH):
     return y.transpose(1, 2).reshape(B, T, C)
 
 
-@pytest.mark.parametrize("B,T,C,NH", [(2, 8, 16, 2), (1, 5, 12, 3), (3, 1, 8, 2)])
+@pytest.mark.parametrize("B,T,C,NH", [(2, 8, 16, 2), (1, 5, 12, 3), (3, 1, 8, 2),
+                                      # every head size the library accepts: 16, 32, 64, 128
+                                      (1, 7, 64, 4), (2, 6, 64, 2), (1, 9, 128, 2), (1, 5, 128, 1)])
 def test_attention_vs_torch_sdpa(B, T, C, NH):
     rng = np.random.default_rng(3)
     qkv = rng.normal(size=(B, T, 3 * C))
