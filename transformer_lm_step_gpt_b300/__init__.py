@@ -119,17 +119,32 @@ def load_library():
     return L
 
 
-def _ptr(x):
-    """Address of a torch tensor, numpy array or raw int (None -> NULL)."""
-    if x is None:
-        return None
-    if isinstance(x, int):
+def _buf(x, n, dtype, where, name):
+    """Address of a buffer in which the library reads or writes n elements of
+    dtype ("int32", "float32", ...); where is "cuda" (device memory) or
+    "host".  A torch tensor or numpy array is checked first (its device, its
+    dtype, contiguity, at least n elements), so that a wrong buffer raises
+    here instead of being read or written past its end; a raw int address is
+    passed on unchecked; None is NULL."""
+    if x is None or isinstance(x, int):
         return x
-    if hasattr(x, "data_ptr"):
-        return x.data_ptr()
-    if isinstance(x, np.ndarray):
-        return x.ctypes.data
-    raise TypeError(type(x))
+    if hasattr(x, "data_ptr"):  # a torch tensor
+        if bool(x.is_cuda) != (where == "cuda"):
+            raise ValueError("%s: need a %s tensor" % (name, "CUDA" if where == "cuda" else "host (CPU)"))
+        dt, contiguous, numel, addr = str(x.dtype).replace("torch.", ""), x.is_contiguous(), x.numel(), x.data_ptr()
+    elif isinstance(x, np.ndarray):
+        if where == "cuda":
+            raise ValueError("%s: need a CUDA tensor, not a numpy array" % name)
+        dt, contiguous, numel, addr = str(x.dtype), bool(x.flags["C_CONTIGUOUS"]), x.size, x.ctypes.data
+    else:
+        raise TypeError("%s: unsupported buffer type %s" % (name, type(x).__name__))
+    if dt != dtype:
+        raise TypeError("%s: dtype %s, need %s" % (name, dt, dtype))
+    if not contiguous:
+        raise ValueError("%s: must be contiguous" % name)
+    if numel < n:
+        raise ValueError("%s: %d elements, need %d" % (name, numel, n))
+    return addr
 
 
 class Model:
@@ -173,16 +188,20 @@ class Model:
     def forward(self, tokens, targets=None, sync=True):
         """tokens/targets: int32 device tensors [B, T].  Returns the mean loss
         (a float) when sync and targets are given, else None."""
+        M = self.B * self.T
+        tok = _buf(tokens, M, "int32", "cuda", "tokens")
+        tgt = _buf(targets, M, "int32", "cuda", "targets")
         loss = ctypes.c_float(float("nan"))
-        self._check(self._lib.gpt2_forward(self._h, _ptr(tokens), _ptr(targets),
-                                           ctypes.byref(loss) if sync else None))
+        self._check(self._lib.gpt2_forward(self._h, tok, tgt, ctypes.byref(loss) if sync else None))
         return loss.value if (sync and targets is not None) else None
 
     def forward_host(self, tokens, targets=None, sync=True):
         """As forward, with host (ideally pinned) int32 buffers."""
+        M = self.B * self.T
+        tok = _buf(tokens, M, "int32", "host", "tokens")
+        tgt = _buf(targets, M, "int32", "host", "targets")
         loss = ctypes.c_float(float("nan"))
-        self._check(self._lib.gpt2_forward_host(self._h, _ptr(tokens), _ptr(targets),
-                                                ctypes.byref(loss) if sync else None))
+        self._check(self._lib.gpt2_forward_host(self._h, tok, tgt, ctypes.byref(loss) if sync else None))
         return loss.value if (sync and targets is not None) else None
 
     def zero_grad(self):
@@ -302,9 +321,12 @@ class Model:
         three are CUDA tensors used in the model's stream order."""
         if out is None:
             import torch
-            out = torch.empty(self.B, dtype=torch.int32, device=tokens.device)
-        self._check(self._lib.gpt2_decode_step(self._h, _ptr(tokens), int(pos), float(temperature),
-                                               _ptr(uniforms), _ptr(out)))
+            dev = tokens.device if hasattr(tokens, "device") else torch.device("cuda", torch.cuda.current_device())
+            out = torch.empty(self.B, dtype=torch.int32, device=dev)
+        tok = _buf(tokens, self.B, "int32", "cuda", "tokens")
+        u = _buf(uniforms, self.B, "float32", "cuda", "uniforms")
+        nxt = _buf(out, self.B, "int32", "cuda", "out")
+        self._check(self._lib.gpt2_decode_step(self._h, tok, int(pos), float(temperature), u, nxt))
         return out
 
     def decode_logits(self) -> np.ndarray:
@@ -385,7 +407,9 @@ class TokenFile:
             tokens = np.empty((B, T), np.int32)
         if targets is None:
             targets = np.empty((B, T), np.int32)
-        self._check(self._lib.gpt2_tokens_next_batch(self._h, int(B), int(T), _ptr(tokens), _ptr(targets)))
+        n = int(B) * int(T)
+        self._check(self._lib.gpt2_tokens_next_batch(self._h, int(B), int(T), _buf(tokens, n, "int32", "host", "tokens"),
+                                                     _buf(targets, n, "int32", "host", "targets")))
         return tokens, targets
 
     def reset(self):
@@ -415,9 +439,12 @@ def layernorm_backward_noalloc(dinp, dweight, dbias, dinp_colsum, dout, inp, wei
     raw pointers); outputs are accumulated into.  Allocates nothing."""
     L = load_library()
     s = getattr(stream, "cuda_stream", stream)
-    rc = L.gpt2_layernorm_backward_noalloc(_ptr(dinp), _ptr(dweight), _ptr(dbias), _ptr(dinp_colsum),
-                                           _ptr(dout), _ptr(inp), _ptr(weight), _ptr(mean), _ptr(rstd),
-                                           int(N), int(C), s)
+    N, C = int(N), int(C)
+    f = lambda x, n, name: _buf(x, n, "float32", "cuda", name)  # noqa: E731
+    rc = L.gpt2_layernorm_backward_noalloc(f(dinp, N * C, "dinp"), f(dweight, C, "dweight"), f(dbias, C, "dbias"),
+                                           f(dinp_colsum, C, "dinp_colsum"), f(dout, N * C, "dout"),
+                                           f(inp, N * C, "inp"), f(weight, C, "weight"), f(mean, N, "mean"),
+                                           f(rstd, N, "rstd"), N, C, s)
     if rc != 0:
         raise GPT2Error(rc, L.gpt2_last_error(None).decode())
 
@@ -440,7 +467,12 @@ def fp8_quantize(x, stream=None):
     """x: contiguous fp32 or bf16 CUDA tensor -> (q: uint8 codes like x,
     scale: float32 [2] with scale[0] = 448 / max|x|), see gpt2_fp8_quantize."""
     import torch
-    assert x.is_cuda and x.is_contiguous() and x.dtype in (torch.float32, torch.bfloat16)
+    if not (isinstance(x, torch.Tensor) and x.is_cuda):
+        raise ValueError("x: need a CUDA tensor")
+    if x.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("x: dtype %s, need float32 or bfloat16" % str(x.dtype).replace("torch.", ""))
+    if not x.is_contiguous():
+        raise ValueError("x: must be contiguous")
     q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
     scale = torch.empty(2, dtype=torch.float32, device=x.device)
     _check_global(load_library().gpt2_fp8_quantize(x.data_ptr(), int(x.dtype == torch.bfloat16), x.numel(),
@@ -453,13 +485,26 @@ def fp8_matmul(qa, scale_a, qb, scale_b, bias=None, out_dtype=None, stream=None)
     uint8 codes (row strides multiples of 16 bytes); out [M, N] fp32 or bf16."""
     import torch
     out_dtype = torch.float32 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("out_dtype: need float32 or bfloat16")
+    for t, name in ((qa, "qa"), (qb, "qb")):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda):
+            raise ValueError("%s: need a CUDA tensor" % name)
+        if t.dtype != torch.uint8:
+            raise TypeError("%s: dtype %s, need uint8 codes" % (name, str(t.dtype).replace("torch.", "")))
+        if t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("%s: need a 2-D tensor whose rows are contiguous" % name)
     M, K = qa.shape
     N = qb.shape[0]
+    if qb.shape[1] != K:
+        raise ValueError("qa and qb: K differs (%d, %d)" % (K, qb.shape[1]))
+    sa = _buf(scale_a, 1, "float32", "cuda", "scale_a")
+    sb = _buf(scale_b, 1, "float32", "cuda", "scale_b")
+    bp = _buf(bias, N, "float32", "cuda", "bias")
     out = torch.empty((M, N), dtype=out_dtype, device=qa.device)
     _check_global(load_library().gpt2_fp8_matmul(
-        qa.data_ptr(), qa.stride(0), scale_a.data_ptr(), qb.data_ptr(), qb.stride(0), scale_b.data_ptr(),
-        M, N, K, None if bias is None else bias.data_ptr(), out.data_ptr(), out.stride(0),
-        int(out_dtype == torch.bfloat16), _stream_ptr(stream)))
+        qa.data_ptr(), qa.stride(0), sa, qb.data_ptr(), qb.stride(0), sb, M, N, K, bp, out.data_ptr(),
+        out.stride(0), int(out_dtype == torch.bfloat16), _stream_ptr(stream)))
     return out
 
 
