@@ -18,6 +18,9 @@ Prints ONE JSON line (rank 0).  Keys:
                         timed live with CUDA events inside the timed region:
                         algorithmic work per launch / average launch duration
                         against the measured peak
+  mfu                   one GPU's tokens/s x algorithmic FLOPs per token over the
+                        measured bf16 burst and sustained peaks; six_n: the same with
+                        the 6 x parameters convention, for comparison only
   cpu_baseline          the CPU oracle timed on this host on a bounded sample
   clocks                nvidia-smi samples taken during the timed region
   gpu_launches          kernel launches of the library inside the timed region
@@ -80,6 +83,28 @@ def flops_per_token(w):
     = 2 L (3C^2 + C^2 + 4C^2 + 4C^2) + 2 C Vp + 2*2 L C (T/2)."""
     L, C, Vp, T = w["L"], w["C"], w["Vp"], w["T"]
     return 3.0 * (2 * L * 12 * C * C + 2 * C * Vp + 4 * L * C * (T / 2))
+
+
+def num_params(w):
+    """Parameters without the vocabulary padding: wte, wpe, L blocks of
+    12 C^2 + 13 C (four Linears with biases, two LayerNorms) and the final
+    LayerNorm."""
+    L, C = w["L"], w["C"]
+    return w["V"] * C + w["maxT"] * C + L * (12 * C * C + 13 * C) + 2 * C
+
+
+def mfu_report(tokens_per_s_per_gpu, w, peaks):
+    """MFU of one GPU's throughput against the bf16 burst and sustained
+    peaks with the algorithmic FLOPs per token; the common 6N convention
+    (6 x parameters per token, no attention scores) beside it, for
+    comparison only."""
+    ftok = flops_per_token(w)
+    f6n = 6.0 * num_params(w)
+    r = lambda f, peak: round(tokens_per_s_per_gpu * f / (peak * 1e12), 4)  # noqa: E731
+    return dict(vs_bf16_burst=r(ftok, peaks["bf16"]), vs_bf16_sustained=r(ftok, peaks["bf16_sustained"]),
+                flops_per_token=ftok, peak_source=peaks["source"],
+                six_n=dict(flops_per_token=f6n, vs_bf16_burst=r(f6n, peaks["bf16"]),
+                           vs_bf16_sustained=r(f6n, peaks["bf16_sustained"])))
 
 
 def load_peaks():
@@ -341,10 +366,6 @@ def run_ours(args, w, world, rank, local):
     _, _, e2e_value = aggregate((t1 - t0) * 1000.0, K * B * T, world, dev)
 
     peaks = load_peaks()
-    ftok = flops_per_token(w)
-    per_gpu = value / world
-    mfu = per_gpu * ftok / (peaks["bf16"] * 1e12)
-    mfu_s = per_gpu * ftok / (peaks["bf16_sustained"] * 1e12)
     tensor = top["unit"] == "flop"
     avg_ms = kprof["ms"] / max(kprof["launches"], 1)
     work_per_launch = kprof["work"] / max(kprof["launches"], 1)
@@ -370,10 +391,10 @@ def run_ours(args, w, world, rank, local):
                            parallelism="replicas only" if world > 1 else "single GPU",
                            layers=w["L"], channels=w["C"], heads=w["NH"], vocab=w["V"], padded_vocab=w["Vp"],
                            token_dist=w["dist"], lr=lr, weight_decay=wd, betas=list(BETAS), eps=EPS,
+                           seeds=dict(build=1337 + rank, token_batches="1338 + 100003 * rank + step index"),
                            l2="no flush: each step streams ~%.1f GB of weights, activations and optimizer "
                               "state (> 126 MB L2)" % (step_bytes(w) / 1e9)),
-               mfu=dict(vs_bf16_burst=round(mfu, 4), vs_bf16_sustained=round(mfu_s, 4),
-                        flops_per_token=ftok, peak_source=peaks["source"]),
+               mfu=mfu_report(value / world, w, peaks),
                roofline=roofline,
                e2e=dict(value=round(e2e_value, 1), unit="tokens/s", h2d_bytes_per_step=2 * B * T * 4,
                         d2h_bytes_per_step=4),

@@ -90,3 +90,15 @@ def test_our_arm_fails_loudly_without_a_gpu():
     r = _run_bench("--steps", "1", "--warmup", "3", "--no-cpu-baseline", timeout=120)
     assert r.returncode != 0
     assert not any(l.startswith("{") for l in r.stdout.splitlines())
+
+
+def test_mfu_report_of_the_124m_step():
+    import bench
+    w = bench.WORKLOADS["gpt2-124M-B16-T1024"]
+    assert bench.num_params(w) == 124_439_808          # the parameter count the 124M run log prints
+    assert bench.flops_per_token(w) == 798_031_872.0   # 3 x (matmuls + causal attention), Vp = 50304
+    peaks = dict(bf16=1772.9, bf16_sustained=1366.0, hbm_gbs=6338.5, source="measured")
+    r = bench.mfu_report(919_310.0, w, peaks)
+    assert abs(r["vs_bf16_burst"] - 0.4138) < 1e-4 and abs(r["vs_bf16_sustained"] - 0.5371) < 1e-4
+    assert r["six_n"]["flops_per_token"] == 6 * 124_439_808
+    assert abs(r["six_n"]["vs_bf16_burst"] - 919_310.0 * 6 * 124_439_808 / 1772.9e12) < 1e-4
