@@ -16,6 +16,7 @@
 //   backward  head dgrad/wgrad -> LN_f -> L x reversed block -> encoder
 //   update    one fused AdamW pass over the whole parameter array
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -159,13 +160,18 @@ cudaEvent_t take_event(gpt2_model* m) {
   return e;
 }
 
-// Records an event pair around the launches made in its scope when the
-// class is selected; accounts the launch and its algorithmic work.
+// Names the launches made in its scope with an NVTX range of the class (for
+// profilers; without one attached the calls do nothing), and records an
+// event pair around them when the class is selected, accounting the launch
+// and its algorithmic work.
 struct ProfScope {
   gpt2_model* m = nullptr;
   int cls;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
   ProfScope(gpt2_model* mm, int c, double work) : cls(c) {
+    nvtxRangePushA(kProfNames[c]);
     if (!(mm->prof.mask & (1u << c))) return;
     m = mm;
     e0 = take_event(m);
@@ -175,9 +181,11 @@ struct ProfScope {
     m->prof.work[c] += work;
   }
   ~ProfScope() {
-    if (!m) return;
-    cudaEventRecord(e1, m->stream);
-    m->prof.pending.push_back({cls, {e0, e1}});
+    if (m) {
+      cudaEventRecord(e1, m->stream);
+      m->prof.pending.push_back({cls, {e0, e1}});
+    }
+    nvtxRangePop();
   }
 };
 
