@@ -163,6 +163,18 @@ def test_errors_are_reported():
     assert e.value.code == -1
 
 
+def test_out_of_memory_is_reported_and_the_context_stays_usable():
+    # 2048 layers of C = 1024 need ~0.5 TB for the parameters and optimizer
+    # state alone: the build's one cudaMalloc fails, which is GPT2_ERR_OOM
+    with pytest.raises(GPT2Error) as e:
+        Model(2048, 1024, 16, 50257, 50304, 1024, 1, 1024, precision="bf16", seed=1)
+    assert e.value.code == -2  # GPT2_ERR_OOM
+    L, C, NH, V, Vp, maxT, B, T = TINY
+    m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=1)
+    tok, tgt = synthetic.batch(2, B, T, V)
+    assert math.isfinite(m.forward(cuda_ids(tok), cuda_ids(tgt)))
+
+
 def test_host_entry_point_matches_device_entry_point():
     L, C, NH, V, Vp, maxT, B, T = RAGGED
     m = Model(L, C, NH, V, Vp, maxT, B, T, precision="bf16", seed=5)
