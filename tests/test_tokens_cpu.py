@@ -68,3 +68,20 @@ def test_into_caller_buffers(tmp_path):
         f.next_batch(2, 7, x, y)
     np.testing.assert_array_equal(x.ravel(), s[:14])
     np.testing.assert_array_equal(y.ravel(), s[1:15])
+
+
+def test_caller_buffers_are_checked_before_the_read(tmp_path):
+    p = tmp_path / "toks.bin"
+    _write(p, np.arange(200))
+    with tl.TokenFile(str(p)) as f:
+        x, y = np.empty((2, 8), np.int32), np.empty((2, 8), np.int32)
+        f.next_batch(2, 8, x, y)                      # caller-owned buffers are filled in place
+        np.testing.assert_array_equal(x.ravel(), np.arange(16))
+        with pytest.raises(ValueError, match="15 elements, need 16"):
+            f.next_batch(2, 8, np.empty(15, np.int32), y)
+        with pytest.raises(TypeError, match="int64"):
+            f.next_batch(2, 8, x, np.empty(16, np.int64))
+        with pytest.raises(ValueError, match="contiguous"):
+            f.next_batch(2, 8, np.empty((2, 16), np.int32)[:, ::2], y)
+        x2, _ = f.next_batch(2, 8, x, y)              # the failed calls did not move the cursor
+        np.testing.assert_array_equal(x2.ravel(), np.arange(16, 32))
