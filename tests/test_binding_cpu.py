@@ -107,3 +107,10 @@ def test_fp8_entry_points_check_their_operands():
         tl.fp8_matmul(q, s, q, s)
     with pytest.raises(TypeError, match="out_dtype"):
         tl.fp8_matmul(q, s, q, s, out_dtype=torch.float16)
+
+
+def test_copy_in_checks_the_length():
+    m = stub_model()                                   # the stub reports an arena of 0 values
+    with pytest.raises(ValueError, match="5 values, the arena holds 0"):
+        m.copy_in(np.zeros(5, np.float32))
+    assert not any(c[0] == "gpt2_copy_in" for c in m._lib.calls)

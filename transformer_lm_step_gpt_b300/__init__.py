@@ -246,7 +246,8 @@ class Model:
 
     def copy_in(self, arr, arena=PARAMS):
         a = np.ascontiguousarray(arr, dtype=np.float32)
-        assert a.size == self.num_params
+        if a.size != self.num_params:
+            raise ValueError("copy_in: %d values, the arena holds %d" % (a.size, self.num_params))
         self._check(self._lib.gpt2_copy_in(self._h, arena, a.ctypes.data))
 
     def losses(self) -> np.ndarray:
