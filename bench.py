@@ -426,7 +426,7 @@ def decode_step_bytes(d, pos):
     """Algorithmic bytes of one decode step at position pos: every input read
     once (bf16 weight matrices, fp32 biases and LayerNorm parameters, the
     token and position embedding rows, the cached keys and values of rows
-    0..pos), every output written once (the new cache row of q, k, v); the
+    0..pos-1), every output written once (the new cache row of q, k, v); the
     scores and the per-row activations are intermediates."""
     L, C, Vp, B = d["L"], d["C"], d["Vp"], d["B"]
     matrices = 2 * (Vp * C + L * 12 * C * C)

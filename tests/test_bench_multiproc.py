@@ -102,3 +102,14 @@ def test_mfu_report_of_the_124m_step():
     assert abs(r["vs_bf16_burst"] - 0.4138) < 1e-4 and abs(r["vs_bf16_sustained"] - 0.5371) < 1e-4
     assert r["six_n"]["flops_per_token"] == 6 * 124_439_808
     assert abs(r["six_n"]["vs_bf16_burst"] - 919_310.0 * 6 * 124_439_808 / 1772.9e12) < 1e-4
+
+
+def test_decode_step_bytes_at_position_530():
+    import bench
+    d = bench.DECODE
+    matrices = 2 * (50304 * 768 + 12 * (2304 + 768 + 3072 + 3072) * 768)   # bf16 wte and the four Linears
+    kv = 2 * 12 * 16 * 530 * (768 + 768)                                   # bf16 keys and values of rows 0..529
+    new_row = 2 * 12 * 16 * 2304                                           # the new q, k, v row of every layer
+    small = 4 * (12 * (2304 + 768 + 3072 + 768 + 4 * 768) + 2 * 768) + 4 * (16 + 1) * 768
+    assert matrices == 247_136_256 and kv == 312_606_720
+    assert bench.decode_step_bytes(d, 530) == matrices + kv + new_row + small == 561_165_312
