@@ -20,6 +20,8 @@ CHAR = (8, 128, 8, 1000, 1000, 64, 32, 64)
 RAGGED = (2, 64, 4, 250, 256, 64, 3, 50)        # M=150, V<Vp, T=50, hs=16
 RAGGED64 = (1, 128, 2, 1000, 1000, 96, 2, 80)   # hs=64, M=160, T=80
 RAGGED64_ODD = (1, 128, 2, 1000, 1000, 200, 2, 199)  # hs=64, T=199: not a multiple of 4
+RAGGED32 = (1, 64, 2, 300, 304, 48, 2, 40)      # hs=32, V<Vp, T=40
+RAGGED128 = (1, 128, 1, 200, 200, 48, 2, 33)    # hs=128, one head, T=33
 GPT2_124M = (12, 768, 12, 50257, 50304, 1024)
 
 
@@ -76,7 +78,7 @@ def test_config_char_ten_steps(prec):
     assert res["loss_gpu"][-1] < res["loss_gpu"][0]
 
 
-@pytest.mark.parametrize("shape", [RAGGED, RAGGED64, RAGGED64_ODD])
+@pytest.mark.parametrize("shape", [RAGGED, RAGGED64, RAGGED64_ODD, RAGGED32, RAGGED128])
 @pytest.mark.parametrize("prec", ["fp32", "bf16"])
 def test_ragged_shapes(shape, prec):
     res = run_steps(shape, prec, 2, 1e-3, 0.9, 0.95, 1e-8, 0.1, "zipf", seed=13,
