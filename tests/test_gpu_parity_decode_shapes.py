@@ -1,13 +1,17 @@
-"""GPU parity of generation with the key/value cache at head sizes 32 and
-128, against the oracle's incremental forward, through the C ABI.
+"""GPU parity of generation with the key/value cache on shapes beyond
+test_gpu_decode.py's, against the oracle's incremental forward, through the
+C ABI.
 
-Both shapes run the generic decode attention (the TMA-staged one serves
-bf16 at head size 64 only) with the keys split over a cluster: T = 130
-gives a cluster of 3 CTAs, T = 70 one of 2, so the ranks' (max, sum,
-output) combine is exercised outside head size 64.  The checks are those of
-test_gpu_decode.py: every step's scores within the training tolerances and
-each drawn token valid against the oracle's CDF (equal to the oracle's
-wherever the draw is unique)."""
+- Head sizes 32 and 128 run the generic decode attention (the TMA-staged
+  one serves bf16 at head size 64 only) with the keys split over a cluster:
+  T = 130 gives a cluster of 3 CTAs, T = 70 one of 2, so the ranks' (max,
+  sum, output) combine is exercised outside head size 64.
+- 20 sequences in bf16: more rows than the few-row matmul takes (16), so
+  the step runs without its CUDA graph, with the host's position, through
+  the tiled matmuls writing the new cache row at a row stride of T rows.
+The checks are those of test_gpu_decode.py: every step's scores within the
+training tolerances and each drawn token valid against the oracle's CDF
+(equal to the oracle's wherever the draw is unique)."""
 import numpy as np
 import pytest
 import torch
@@ -21,11 +25,12 @@ pytestmark = pytest.mark.gpu
 #        L  C    NH  V    Vp   maxT B  T
 HS32 = (1, 64, 2, 97, 104, 130, 2, 130)    # head size 32, keys over 3 CTAs
 HS128 = (1, 128, 1, 120, 128, 70, 2, 70)   # head size 128, one head, keys over 2 CTAs
+B20 = (1, 128, 2, 97, 104, 100, 20, 100)   # 20 sequences, head size 64, keys over 2 CTAs
 
 
-@pytest.mark.parametrize("prec", ["fp32", "bf16"])
-@pytest.mark.parametrize("shape", [HS32, HS128])
-def test_teacher_forced_decode_at_head_sizes_32_and_128(shape, prec):
+@pytest.mark.parametrize("shape,prec", [(HS32, "fp32"), (HS32, "bf16"), (HS128, "fp32"), (HS128, "bf16"),
+                                        (B20, "bf16")])
+def test_teacher_forced_decode(shape, prec):
     L, C, NH, V, Vp, maxT, B, T = shape
     m, p = setup(shape, prec, seed=17)
     cfg = oracle.cfg8(*shape)
