@@ -118,6 +118,11 @@ def _prefix_losses(shape, prec, rows, tprefix, dist, seed):
     (GPT2_124M + (4, 1024), 4, 48, "uniform"),    # 124M, B=4 single step
     (GPT2_124M + (16, 1024), 2, 32, "zipf"),      # 124M throughput shape
     ((24, 1024, 16, 50257, 50304, 1024, 8, 1024), 2, 24, "uniform"),  # 350M
+    # the largest shapes the build accepts, one layer each: T = 4096 with
+    # B*T = 32768 and C = 1024; and Vp*B*T just below 2^32 (4.29e9 logits,
+    # past 2^31: every index into them must be 64-bit)
+    ((1, 1024, 16, 50257, 50304, 4096, 8, 4096), 1, 24, "uniform"),
+    ((1, 1024, 16, 131064, 131064, 1024, 32, 1024), 1, 16, "uniform"),
 ])
 def test_full_size_sampled(shape, rows, tp, dist):
     L, C, NH, V, Vp, maxT, B, T = shape
