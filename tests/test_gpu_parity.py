@@ -22,6 +22,7 @@ RAGGED64 = (1, 128, 2, 1000, 1000, 96, 2, 80)   # hs=64, M=160, T=80
 RAGGED64_ODD = (1, 128, 2, 1000, 1000, 200, 2, 199)  # hs=64, T=199: not a multiple of 4
 RAGGED32 = (1, 64, 2, 300, 304, 48, 2, 40)      # hs=32, V<Vp, T=40
 RAGGED128 = (1, 128, 1, 200, 200, 48, 2, 33)    # hs=128, one head, T=33
+SINGLE_TOKEN = (1, 128, 2, 100, 104, 8, 2, 1)   # T=1 (each position attends to itself), M=2
 GPT2_124M = (12, 768, 12, 50257, 50304, 1024)
 
 
@@ -84,6 +85,29 @@ def test_ragged_shapes(shape, prec):
     res = run_steps(shape, prec, 2, 1e-3, 0.9, 0.95, 1e-8, 0.1, "zipf", seed=13,
                     check_grads_every_step=True)
     assert_parity(res, shape, prec)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_single_token_sequences(prec):
+    # T = 1: each position attends only to itself, so the softmax has no
+    # gradient and the query and key rows of qkvw and qkvb get an exactly zero
+    # gradient in the oracle (rounding-level on the GPU).  The loss and every
+    # gradient tensor are compared with the oracle; the parameters that
+    # AdamW's first step moves by the sign of that rounding are not.
+    L, C, NH, V, Vp, maxT, B, T = SINGLE_TOKEN
+    res = run_steps(SINGLE_TOKEN, prec, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, "zipf", seed=13)
+    tol = TOL[prec]
+    assert abs(res["loss_gpu"][0] - res["loss_ref"][0]) <= tol["loss"]
+    bad = {k: v for k, v in res["grad_err"][0].items() if not v <= tol["rel"]}
+    assert not bad, bad
+    tab = dict((n, (o, k)) for n, o, k in res["tab"])
+    g = res["grads_gpu"]
+    o, _ = tab["qkvw"]
+    w = g[o:o + 3 * C * C].reshape(3 * C, C)       # rows q | k | v
+    assert np.linalg.norm(w[:2 * C]) <= 1e-3 * np.linalg.norm(w[2 * C:])
+    o, _ = tab["qkvb"]
+    b = g[o:o + 3 * C]
+    assert np.linalg.norm(b[:2 * C]) <= 1e-3 * np.linalg.norm(b[2 * C:])
 
 
 def test_gpt2_124m_shapes_short_sequence_bf16():
