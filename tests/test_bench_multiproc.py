@@ -113,3 +113,38 @@ def test_decode_step_bytes_at_position_530():
     small = 4 * (12 * (2304 + 768 + 3072 + 768 + 4 * 768) + 2 * 768) + 4 * (16 + 1) * 768
     assert matrices == 247_136_256 and kv == 312_606_720
     assert bench.decode_step_bytes(d, 530) == matrices + kv + new_row + small == 561_165_312
+
+
+def test_clock_sampler_summary_from_nvidia_smi_lines():
+    import threading
+
+    import bench
+
+    class FakeProc:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+        def kill(self):
+            pass
+
+    s = bench.ClockSampler(0)
+    s.proc = FakeProc()
+    s.t = threading.Thread(target=lambda: None)
+    s.t.start()
+    na = "Not Active"
+    s.lines = [
+        "0, 1942, 2032, 1010.5, 0x0000000000000004, %s, %s, %s, Active" % (na, na, na),
+        "0, 1965, 2032, 1050.1, 0x0000000000000000, %s, %s, %s, %s" % (na, na, na, na),
+        "0, 1905, 2032, 1094.2, 0x0000000000000004, %s, %s, %s, Active" % (na, na, na),
+        "0, [N/A], 2032, 990.0, 0x0, %s, %s, %s, %s" % (na, na, na, na),   # unreadable: skipped
+        "garbage",                                                         # short: skipped
+    ]
+    r = s.stop()
+    assert r == dict(sm_mhz=1942.0, sm_max_mhz=2032.0, reasons=["sw_power_cap"], samples=3)
+    s.lines.append("0, 1200, 2032, 700.0, 0x8, Active, %s, %s, %s" % (na, na, na))
+    assert s.stop()["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    s.lines = []
+    assert s.stop() is None
