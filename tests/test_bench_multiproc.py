@@ -148,3 +148,19 @@ def test_clock_sampler_summary_from_nvidia_smi_lines():
     assert s.stop()["reasons"] == ["hw_slowdown", "sw_power_cap"]
     s.lines = []
     assert s.stop() is None
+
+
+def test_traffic_is_reported_only_while_the_sources_are_unchanged(tmp_path, monkeypatch):
+    import json
+
+    import bench
+    (tmp_path / "profiles").mkdir()
+    src = tmp_path / "k.cu"
+    src.write_text("__global__ void k() {}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    rec = dict(sources=["k.cu"], digest=bench.source_digest(["k.cu"]), bytes_per_launch=12345)
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"attention_bwd": rec}))
+    assert bench.load_traffic("attention_bwd") == 12345.0
+    assert bench.load_traffic("layernorm_bwd") is None          # no record for this class
+    src.write_text("__global__ void k() { }\n")                  # the kernel changed since the capture
+    assert bench.load_traffic("attention_bwd") is None
