@@ -44,6 +44,13 @@ def test_binding_covers_every_symbol():
     dict(L=0),                   # no layers
     dict(B=64, T=1024, maxT=1024),  # B*T > 32768
     dict(C=1280, NH=20),         # C > 1024
+    dict(B=0),                   # no sequences
+    dict(T=0),                   # empty sequences
+    dict(maxT=8192, T=32),       # maxT > 4096
+    dict(C=96, NH=1),            # head size 96: not 16, 32, 64 or 128
+    dict(C=64, NH=8),            # head size 8
+    dict(V=0),                   # empty vocabulary
+    dict(V=131072, Vp=131072, B=32, T=1024, maxT=1024),  # Vp*B*T = 2^32: the encoder's sort key would not fit
 ])
 def test_build_rejects_bad_config_without_gpu(bad):
     cfg = dict(L=2, C=64, NH=4, V=256, Vp=256, maxT=32, B=4, T=32)
@@ -104,3 +111,13 @@ def test_named_copies_reject_a_null_model():
 
 def test_expire_a_wait_rejects_a_null_model():
     assert tl.load_library().gpt2_expire_a_wait(None) == -1
+
+
+def test_the_logits_limit_is_exact():
+    # Vp*B*T = 131064*32768 < 2^32 passes the argument checks (without a GPU
+    # the build then fails at the device, never with GPT2_ERR_ARG)
+    try:
+        m = tl.Model(1, 1024, 16, 131064, 131064, 1024, 32, 1024, precision="bf16")
+        m.close()
+    except tl.GPT2Error as e:
+        assert e.code != -1, str(e)
