@@ -329,3 +329,22 @@ def test_initial_loss_near_ln_v():
     tok, tgt = synthetic.batch(1338, B, T, V)
     r = oracle.fwdbwd(cfg, p, tok, tgt, want_grads=False)
     assert abs(r["loss"] - math.log(V)) < 0.05
+
+
+def test_oracle_results_do_not_depend_on_the_thread_count():
+    # OpenMP splits only independent outputs; every sum runs in formula order
+    from transformer_lm_step_gpt_b300 import synthetic
+    L, C, NH, V, Vp, maxT, B, T = 2, 32, 2, 50, 56, 16, 3, 12
+    cfg = oracle.cfg8(L, C, NH, V, Vp, maxT, B, T)
+    p = synthetic.params(oracle.param_table(cfg), L, C, V, 3, kind="perturbed")
+    tok, tgt = synthetic.batch(4, B, T, V, "zipf")
+    out = []
+    try:
+        for n in (1, max(2, min(8, os.cpu_count() or 2))):
+            oracle.set_threads(n)
+            r = oracle.fwdbwd(cfg, p, tok, tgt)
+            out.append((r["loss"], r["grads"].copy()))
+    finally:
+        oracle.set_threads(0)
+    assert out[0][0] == out[1][0]
+    assert np.array_equal(out[0][1], out[1][1])
