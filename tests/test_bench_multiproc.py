@@ -164,3 +164,15 @@ def test_traffic_is_reported_only_while_the_sources_are_unchanged(tmp_path, monk
     assert bench.load_traffic("layernorm_bwd") is None          # no record for this class
     src.write_text("__global__ void k() { }\n")                  # the kernel changed since the capture
     assert bench.load_traffic("attention_bwd") is None
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1", MASTER_ADDR="127.0.0.1", MASTER_PORT="29599")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
