@@ -384,6 +384,11 @@ GPT2_API const char* gpt2_last_error(const gpt2_model* m);
  *       accumulated into (the caller zeroes them for plain values);
  *   dout, inp [N, C], weight [C], mean, rstd [N]: inputs, read only;
  *   cuda_stream: the cudaStream_t to enqueue on (NULL = legacy stream).
+ * Alignment: dinp, dweight, dbias, dinp_colsum, dout, inp and weight must
+ * start on 16-byte boundaries (rows move by bulk copies, columns in 16-byte
+ * vectors), mean and rstd on 4-byte ones; otherwise GPT2_ERR_ARG.
+ * Ordering: the call's first kernel starts only after all work enqueued
+ * before it on cuda_stream has finished (no programmatic overlap).
  * Scratch: the partial sums, at most ceil(N/64) * 8 * 3 * C floats, live in one
  * file-scope __device__ array of 2^21 floats (8 MiB) that every GPU which
  * loads the library holds until the process exits.  Larger sizes are
@@ -396,12 +401,21 @@ GPT2_API const char* gpt2_last_error(const gpt2_model* m);
  * other threads) race on the array.  The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Asynchronous;
- * calls no cudaMalloc, cudaFree or other allocating routine. */
+ * calls no cudaMalloc, cudaFree or other allocating routine.  A bounded
+ * device wait that expires inside the call (its outputs are then incomplete)
+ * sets a per-device error word that gpt2_noalloc_check reports. */
 GPT2_API int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias,
                                              float* dinp_colsum, const float* dout,
                                              const float* inp, const float* weight,
                                              const float* mean, const float* rstd, int32_t N,
                                              int32_t C, void* cuda_stream);
+
+/* gpt2_noalloc_check: synchronises cuda_stream, then reads and clears the
+ * current device's error word of gpt2_layernorm_backward_noalloc.  Returns
+ * GPT2_ERR_TIMEOUT if a bounded wait of an earlier call expired (that call's
+ * outputs are incomplete), GPT2_ERR_CUDA if the stream reports a CUDA error,
+ * else GPT2_OK.  Allocates nothing. */
+GPT2_API int gpt2_noalloc_check(void* cuda_stream);
 
 #ifdef __cplusplus
 }

@@ -121,3 +121,30 @@ def test_the_logits_limit_is_exact():
         m.close()
     except tl.GPT2Error as e:
         assert e.code != -1, str(e)
+
+
+def test_noalloc_layernorm_backward_checks_arguments_without_gpu():
+    # gpt2_layernorm_backward_noalloc refuses NULL buffers, sizes beyond its
+    # static scratch and misaligned addresses before any device work (the
+    # addresses below are never dereferenced)
+    lib = tl.load_library()
+    buf = ctypes.create_string_buffer(4096)
+    p = (ctypes.addressof(buf) + 255) & ~255
+    ptrs = [p] * 9
+
+    def call(ptrs, N=150, C=64):
+        return lib.gpt2_layernorm_backward_noalloc(*[ctypes.c_void_p(x) for x in ptrs], N, C, None)
+    assert call([p, p, p, p, None, p, p, p, p]) == -1
+    assert b"NULL" in lib.gpt2_last_error(None)
+    assert call(ptrs, N=1 << 20, C=1024) == -1
+    assert b"static scratch" in lib.gpt2_last_error(None)
+    assert call(ptrs, C=62) == -1          # C % 4 != 0
+    for i in range(7):  # dinp, dweight, dbias, dinp_colsum, dout, inp, weight: 16-byte
+        bad = list(ptrs)
+        bad[i] = p + 4
+        assert call(bad) == -1, i
+        assert b"aligned" in lib.gpt2_last_error(None)
+    for i in (7, 8):    # mean, rstd: 4-byte
+        bad = list(ptrs)
+        bad[i] = p + 2
+        assert call(bad) == -1, i

@@ -116,7 +116,7 @@ def _prefix_losses(shape, prec, rows, tprefix, dist, seed):
 
 
 @pytest.mark.parametrize("shape,rows,tp,dist", [
-    (GPT2_124M + (4, 1024), 4, 48, "uniform"),    # 124M, B=4 single step
+    (GPT2_124M + (4, 1024), 1, 1024, "uniform"),  # 124M, B=4 single step: one whole row
     (GPT2_124M + (16, 1024), 2, 32, "zipf"),      # 124M throughput shape
     ((24, 1024, 16, 50257, 50304, 1024, 8, 1024), 2, 24, "uniform"),  # 350M
 ])
@@ -256,6 +256,45 @@ def test_expired_wait_is_reported_and_the_model_recovers():
     assert time.time() - t0 >= 1.5
     m.synchronize()   # the condition was cleared
     assert m.forward(cuda_ids(tok), cuda_ids(tgt)) == l0
+
+
+# ---- whole-step parity at the configurations' sequence length: every gradient
+# ---- tensor, updated parameter, m and v against the oracle on one-layer
+# ---- models small enough for the oracle, but on the launch paths the 124M and
+# ---- 350M steps take (causal mask: GeekNews, "A GPT-2-based ChatGPT clone in
+# ---- 3000 bytes of C", *The Transformer core*; per-layer backward: QbitAI,
+# ---- "OpenAI founder hand-writes...", *Manually implementing each layer's
+# ---- forward/backward pass*)
+
+# T = 1024, B = 4 (M = 4096): the attention kernels walk 16 key blocks of 64
+# and 8 of 128 for the last query rows; the qkv and attproj weight gradients
+# have fewer output tiles than SMs and K = 4096, so their split-K runs more
+# than 4 ways and is reduced by the separate split-order kernel
+LONG1024 = (1, 128, 2, 1000, 1000, 1024, 4, 1024)
+# T = 4096, one sequence, head size 64: 64 key blocks of 64 per query row
+LONG4096 = (1, 128, 2, 1000, 1000, 4096, 1, 4096)
+# C = 1024, 16 heads (the 350M layer): the LayerNorm kernels' widest rows and
+# every 350M matmul shape, with K = 4096 weight gradients split 6 ways
+WIDE1024 = (1, 1024, 16, 1000, 1000, 1024, 4, 1024)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_long_sequence_whole_step(prec):
+    res = run_steps(LONG1024, prec, 2, 1e-3, 0.9, 0.95, 1e-8, 0.1, "zipf", seed=15,
+                    check_grads_every_step=True)
+    assert_parity(res, LONG1024, prec)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_longest_sequence_whole_step(prec):
+    res = run_steps(LONG4096, prec, 1, 1e-3, 0.9, 0.95, 1e-8, 0.1, "uniform", seed=16)
+    assert_parity(res, LONG4096, prec)
+
+
+@pytest.mark.parametrize("prec", ["fp32", "bf16"])
+def test_widest_layer_whole_step(prec):
+    res = run_steps(WIDE1024, prec, 1, 6e-4, 0.9, 0.999, 1e-8, 0.1, "uniform", seed=17)
+    assert_parity(res, WIDE1024, prec)
 
 
 # ---- the edges of what the build accepts (head sizes 32 and 128, single-token

@@ -10,7 +10,10 @@ lnfb and, through its residual-gradient column sums, the fcproj bias
 gradient of the last block.  The LayerNorm's inputs are reconstructed from
 what the existing entry points expose (the residual stream entering LN_f,
 the logits, wte and lnfw).  Two calls in a row must both match: the second
-one reuses the partials the first left in the static array.
+one reuses the partials the first left in the static array.  The outputs are
+also compared element by element with the oracle's LayerNorm backward at the
+GPT-2 widths C = 768 and 1024, with output buffers that start nonzero (the
+call adds into them).
 """
 import ctypes
 
@@ -18,6 +21,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import transformer_lm_step_gpt_b300 as tl
 from transformer_lm_step_gpt_b300 import GRADS, PARAMS, Model, synthetic
 
@@ -78,6 +82,44 @@ def test_noalloc_layernorm_backward_matches_gpt2_backward():
         assert rel_l2(db, want_db) <= REL
         assert rel_l2(cs, want_cs) <= REL
         assert rel_l2(dx.sum(0), cs) <= 1e-5
+        results.append((dx, dw, db, cs))
+    for a, b in zip(results[0], results[1]):
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("N,C", [(1000, 768), (2000, 1024)])
+def test_noalloc_layernorm_backward_matches_the_oracle(N, C):
+    rng = np.random.default_rng(N + C)
+    x = rng.normal(0.3, 1.7, (N, C)).astype(np.float32)
+    dout = rng.normal(0, 1e-3, (N, C)).astype(np.float32)
+    w = (1.0 + rng.normal(0, 0.1, C)).astype(np.float32)
+    x64 = x.astype(np.float64)
+    mean = x64.mean(1).astype(np.float32)
+    rstd = (1.0 / np.sqrt(x64.var(1) + 1e-5)).astype(np.float32)
+    # the oracle on exactly the inputs the GPU reads
+    dx_ref, dw_ref, db_ref = oracle.layernorm_backward(dout.astype(np.float64), x64, w.astype(np.float64),
+                                                       mean.astype(np.float64), rstd.astype(np.float64))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()  # noqa: E731
+    ins = [dev(dout), dev(x), dev(w), dev(mean), dev(rstd)]
+    # outputs start nonzero: the call adds into them
+    init = [rng.normal(0, 1e-3, (N, C)), rng.normal(0, 1e-2, C), rng.normal(0, 1e-2, C), rng.normal(0, 1e-2, C)]
+    init = [a.astype(np.float32) for a in init]
+    results = []
+    for _ in range(2):
+        outs = [dev(a) for a in init]
+        tl.layernorm_backward_noalloc(*outs, *ins, N, C)
+        tl.noalloc_check()
+        dx, dw, db, cs = [t.cpu().numpy().astype(np.float64) for t in outs]
+        dx -= init[0]
+        dw -= init[1]
+        db -= init[2]
+        cs -= init[3]
+        assert rel_l2(dx, dx_ref) <= REL
+        assert np.max(np.abs(dx - dx_ref)) <= REL * np.max(np.abs(dx_ref))
+        assert rel_l2(dw, dw_ref) <= REL
+        assert rel_l2(db, db_ref) <= REL
+        # the column sums of the updated dinp: of the initial values plus dx
+        assert rel_l2(cs, (init[0].astype(np.float64) + dx_ref).sum(0)) <= REL
         results.append((dx, dw, db, cs))
     for a, b in zip(results[0], results[1]):
         assert np.array_equal(a, b)

@@ -18,7 +18,7 @@ import os
 
 import numpy as np
 
-__all__ = ["Model", "GPT2Error", "TokenFile", "library_path", "load_library", "layernorm_backward_noalloc",
+__all__ = ["Model", "GPT2Error", "TokenFile", "library_path", "load_library", "layernorm_backward_noalloc", "noalloc_check",
            "fp8_quantize", "fp8_matmul", "fp8_check",
            "PARAMS", "GRADS", "ADAM_M", "ADAM_V"]
 
@@ -98,6 +98,7 @@ def load_library():
         "gpt2_launch_count": ([vp, ctypes.POINTER(i64)], ctypes.c_int),
         "gpt2_last_error": ([vp], ctypes.c_char_p),
         "gpt2_layernorm_backward_noalloc": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp], ctypes.c_int),
+        "gpt2_noalloc_check": ([vp], ctypes.c_int),
         "gpt2_save_checkpoint": ([vp, ctypes.c_char_p, i32], ctypes.c_int),
         "gpt2_load_checkpoint": ([vp, ctypes.c_char_p, ctypes.POINTER(i32)], ctypes.c_int),
         "gpt2_tokens_open": ([ctypes.c_char_p, ctypes.POINTER(vp)], ctypes.c_int),
@@ -446,6 +447,15 @@ def layernorm_backward_noalloc(dinp, dweight, dbias, dinp_colsum, dout, inp, wei
                                            f(dinp_colsum, C, "dinp_colsum"), f(dout, N * C, "dout"),
                                            f(inp, N * C, "inp"), f(weight, C, "weight"), f(mean, N, "mean"),
                                            f(rstd, N, "rstd"), N, C, s)
+    if rc != 0:
+        raise GPT2Error(rc, L.gpt2_last_error(None).decode())
+
+
+def noalloc_check(stream=None):
+    """gpt2_noalloc_check: synchronise the stream and raise GPT2Error if a
+    bounded device wait of an earlier allocation-free call expired."""
+    L = load_library()
+    rc = L.gpt2_noalloc_check(getattr(stream, "cuda_stream", stream))
     if rc != 0:
         raise GPT2Error(rc, L.gpt2_last_error(None).decode())
 

@@ -1114,8 +1114,6 @@ void launch_gemm_fp8(LaunchCtx& c, const GemmArgs& g) {
                      (int*)nullptr, c.err);
 }
 
-static int g_pair_mode = -1;  // GPT2_GEMM_PAIR=0 selects the one-SM kernel for every shape
-
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   if (gemm_rows_applies(g)) {  // a few rows of A: the weights stream once, M and N swapped
     launch_gemm_rows(c, g);
@@ -1139,11 +1137,7 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   else if (g.a_kmajor && !g.b_kmajor) launch_tc<BNV, true, false>(c, g, splits, partial); \
   else if (!g.a_kmajor && g.b_kmajor) launch_tc<BNV, false, true>(c, g, splits, partial); \
   else launch_tc<BNV, false, false>(c, g, splits, partial);
-  if (g_pair_mode < 0) {
-    const char* e = getenv("GPT2_GEMM_PAIR");
-    g_pair_mode = (e && e[0] == '0') ? 0 : 1;
-  }
-  if (BN == 256 && g_pair_mode) {
+  if (BN == 256) {
     // epilogues that read an aux tile use the prefetching variant; the model's
     // aux GEMMs (attproj / fcproj forward, fcproj dgrad) are A K-major
     const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX || g.epi == EPI_GELU_FWD);
@@ -1153,6 +1147,8 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
     else if (g.a_kmajor && !g.b_kmajor) launch_tc_pair<true, false, false>(c, g, splits, partial);
     else if (!g.a_kmajor && g.b_kmajor) launch_tc_pair<false, true, false>(c, g, splits, partial);
     else launch_tc_pair<false, false, false>(c, g, splits, partial);
-  } else if (BN == 256) { TC_DISPATCH(256) } else { TC_DISPATCH(128) }
+  } else {
+    TC_DISPATCH(128)
+  }
 #undef TC_DISPATCH
 }

@@ -798,25 +798,37 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
 // that cannot allocate device memory.  Its partial sums (at most
 // ceil(N/64)*8 rows of 3*C floats) live in this file-scope array instead of caller- or
 // model-owned scratch; every GPU that loads the library holds it until the
-// process exits.
+// process exits.  Its bounded waits report into g_noalloc_err, which
+// gpt2_noalloc_check reads and clears.
 #define NOALLOC_SCRATCH_FLOATS (1 << 21)  // 8 MiB
 static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_SCRATCH_FLOATS];
+static __device__ int g_noalloc_err;
 
-// Device address of the array on the current device, looked up once per
-// device (in host code the array's name is only a host-side stand-in).
-static float* noalloc_scratch(int dev) {
-  static float* addr[128] = {};
-  if (dev < 0 || dev >= 128) return nullptr;
-  if (!addr[dev]) {
+// Device addresses of the two arrays on the current device, looked up once
+// per device (in host code their names are only host-side stand-ins).
+struct NoallocAddr {
+  float* scratch;
+  int* err;
+};
+static bool noalloc_addr(int dev, NoallocAddr* out) {
+  static NoallocAddr addr[128] = {};
+  if (dev < 0 || dev >= 128) return false;
+  if (!addr[dev].scratch) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&q, g_noalloc_err) != cudaSuccess) {
       cudaGetLastError();
-      return nullptr;
+      return false;
     }
-    addr[dev] = static_cast<float*>(p);
+    addr[dev].err = static_cast<int*>(q);
+    addr[dev].scratch = static_cast<float*>(p);
   }
-  return addr[dev];
+  *out = addr[dev];
+  return true;
 }
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, float* dbias,
                                                float* dinp_colsum, const float* dout,
@@ -831,6 +843,14 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
     set_global_error("gpt2_layernorm_backward_noalloc: need N >= 1, 4 <= C <= 1024, C % 4 == 0");
     return GPT2_ERR_ARG;
   }
+  // rows move by bulk copies and columns by 16-byte vectors
+  if (!aligned16(dinp) || !aligned16(dweight) || !aligned16(dbias) || !aligned16(dinp_colsum) ||
+      !aligned16(dout) || !aligned16(inp) || !aligned16(weight) ||
+      (reinterpret_cast<uintptr_t>(mean) & 3u) || (reinterpret_cast<uintptr_t>(rstd) & 3u)) {
+    set_global_error("gpt2_layernorm_backward_noalloc: dinp, dweight, dbias, dinp_colsum, dout, inp "
+                     "and weight need 16-byte aligned addresses, mean and rstd 4-byte");
+    return GPT2_ERR_ARG;
+  }
   const int64_t need = ln_partial_floats(N, C);
   if (need > NOALLOC_SCRATCH_FLOATS) {
     set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/64)*8*3*C exceeds the 2^21-float "
@@ -838,25 +858,53 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
     return GPT2_ERR_ARG;
   }
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  float* scratch = e == cudaSuccess ? noalloc_scratch(dev) : nullptr;
-  if (!scratch) {
-    set_global_error("gpt2_layernorm_backward_noalloc: no device address for the static scratch");
+  NoallocAddr a = {};
+  if (cudaGetDevice(&dev) != cudaSuccess || !noalloc_addr(dev, &a)) {
+    cudaGetLastError();
+    set_global_error("gpt2_layernorm_backward_noalloc: no device address for the static arrays");
     return GPT2_ERR_CUDA;
   }
   int64_t launches = 0;
   LaunchCtx c;
   c.stream = static_cast<cudaStream_t>(cuda_stream);
-  c.err = nullptr;
+  c.err = a.err;
   c.launches = &launches;
   c.num_sms = 0;
   c.host_fail = 0;
+  // No programmatic overlap with whatever the caller enqueued before (the
+  // kernel reads weight before its dependency wait, which is only safe
+  // behind the model's own kernels).
+  c.pdl = 0;
   launch_layernorm_bwd<float>(c, dinp, nullptr, dweight, dbias, dinp_colsum, dout, inp, weight,
-                              mean, rstd, N, C, true, scratch);
-  e = cudaGetLastError();
+                              mean, rstd, N, C, true, a.scratch);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || c.host_fail) {
+    set_global_error(e != cudaSuccess ? cudaGetErrorString(e) : "gpt2_layernorm_backward_noalloc: launch failed");
+    return GPT2_ERR_CUDA;
+  }
+  return GPT2_OK;
+}
+
+extern "C" int gpt2_noalloc_check(void* cuda_stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream));
+  int dev = 0;
+  NoallocAddr a = {};
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || !noalloc_addr(dev, &a)) {
+    cudaGetLastError();
+    set_global_error(e != cudaSuccess ? cudaGetErrorString(e) : "gpt2_noalloc_check: no error word");
+    return GPT2_ERR_CUDA;
+  }
+  int v = 0;
+  e = cudaMemcpy(&v, a.err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) {
     set_global_error(cudaGetErrorString(e));
     return GPT2_ERR_CUDA;
+  }
+  if (v) {
+    cudaMemset(a.err, 0, sizeof(int));
+    set_global_error("gpt2_noalloc_check: a bounded device wait expired");
+    return GPT2_ERR_TIMEOUT;
   }
   return GPT2_OK;
 }

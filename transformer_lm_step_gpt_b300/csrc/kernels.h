@@ -18,6 +18,8 @@ struct LaunchCtx {
   int64_t* launches;  // host-side count of kernel launches
   int num_sms;
   int host_fail;      // set by a launcher that could not enqueue its kernel
+  int pdl = 1;        // 0: launch_pdl launches without programmatic serialisation,
+                      // so the first kernel waits for all earlier work on the stream
 };
 
 // Launch kernel `k` on c.stream with programmatic stream serialisation
@@ -34,7 +36,7 @@ inline void launch_pdl(LaunchCtx& c, void (*k)(KArgs...), dim3 grid, dim3 block,
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = c.pdl ? 1 : 0;
   if (cudaLaunchKernelEx(&cfg, k, static_cast<KArgs>(args)...) != cudaSuccess) c.host_fail = 1;
   (*c.launches)++;
 }
