@@ -16,290 +16,381 @@ import pytest
 
 from protocol_sim import Sim, find
 
-# warps and ring stages as the kernels are compiled: 8 softmax warps and 3
-# key/value stages (forward); 16 compute warps and 4 query stages (dK/dV);
-# 8 compute warps, 3 key and 2 value stages (dQ)
-FWD_WARPS, FWD_STAGES = 8, 3
-DKV_WARPS, DKV_STAGES = 16, 4
-DQ_WARPS, DQ_K_STAGES, DQ_V_STAGES = 8, 3, 2
+# warps and ring stages as the kernels are compiled (head size 64): 8
+# softmax warps, 2 query buffers and 2-stage key / value rings (forward);
+# 16 elementwise warps, 2 key/value buffers and a 4-stage query ring
+# (dK/dV); 16 elementwise warps, 2 query buffers, 3 key and 2 value stages
+# (dQ).  A CTA walks a list of work items; ITEMS are the item lengths (key
+# or query blocks) of the lists tried, longest first as the kernels order
+# them.
+FWD_WARPS, FWD_QB, FWD_KV = 8, 2, 2
+DKV_WARPS, DKV_KVB, DKV_STAGES = 16, 2, 4
+DQ_WARPS, DQ_QB, DQ_KST, DQ_VST = 16, 2, 3, 2
+ITEMS = [[1], [3], [8, 5, 2], [4, 4, 1, 1], [2, 1, 1, 1, 1], [16, 9]]
 
 
 # -------------------------------------------------------------- forward
-def forward(nsub, seed, plant=None, nsoft=FWD_WARPS, stages=FWD_STAGES):
-    """Loader warp: q once, then k(j), v(j) into ring stage j % stages once
-    S(j - stages), PV(j - stages) have read it.  MMA warp: S(0), S(1), then
-    per sub-block PV(j) once P(j) is written and S(j + 2) after it.  Softmax
-    warps: S(j) -> P(j) in shared memory (after PV(j - 2) has read that
-    buffer), with an occasional rescale of O in tensor memory once PV(j - 1)
-    is done; O read at the end."""
+def forward(items, seed, plant=None, nsoft=FWD_WARPS, qb=FWD_QB, kv=FWD_KV):
+    """attn_fwd_tc_kernel.  Loader: per item q into buffer it % qb once the
+    item qb back has issued its last S; per block k, v into ring stage
+    g % kv once S(g - kv), PV(g - kv) have read it.  MMA issuer, over the
+    blocks g of all items in turn: S(g) once k(g) is in and the softmax
+    warps have copied S(g - 1) out; then PV(g - 1) once P(g - 1) is
+    written (so PV of an item's last block runs after the next item's
+    first S).  Softmax warps: copy S(g) out, then P(g) into tensor memory
+    once PV(g - 1) has read the P columns (at an item's first block the
+    previous item's epilogue has waited for that), with an occasional
+    rescale of O in tensor memory at the same point; O read at the end of
+    each item."""
     sim = Sim(seed, plant)
-    sim.bar("q")
-    for s in range(stages):
-        for n in ("kf%d", "vf%d", "ke%d", "ve%d"):
+    for i in range(qb):
+        sim.bar("qf%d" % i)
+        sim.bar("qe%d" % i)
+    for s in range(kv):
+        for n in ("kf%d", "ke%d", "vf%d", "ve%d"):
             sim.bar(n % s)
-    for i in range(2):
-        sim.bar("s%d" % i)
-        sim.bar("o%d" % i)
-        sim.bar("p%d" % i, nsoft)
-    if plant == "one_p_barrier":   # P(j) written: one barrier for both buffers
-        P, Pk = (lambda j: "p0"), (lambda j: j)
-    else:
-        P, Pk = (lambda j: "p%d" % (j & 1)), (lambda j: j >> 1)
+    sim.bar("sf")
+    sim.bar("sfree", nsoft)
+    sim.bar("pf", nsoft)
+    sim.bar("od")
 
     def loader():
-        sim.tma("q", "sQ", phase=0)
-        for j in range(nsub):
-            s = j % stages
-            if j >= stages and plant != "k_refill_unguarded":
-                yield from sim.wait("ke%d" % s, j // stages - 1)
-            sim.tma("kf%d" % s, "sK%d" % s, phase=j // stages)
-            if j >= stages:
-                yield from sim.wait("ve%d" % s, j // stages - 1)
-            sim.tma("vf%d" % s, "sV%d" % s, phase=j // stages)
+        g = 0
+        for it, nk in enumerate(items):
+            qs = it % qb
+            if it >= qb and plant != "q_refill_unguarded":
+                yield from sim.wait("qe%d" % qs, it // qb - 1)
+            sim.tma("qf%d" % qs, "sQ%d" % qs, phase=it // qb)
+            for _ in range(nk):
+                s = g % kv
+                if g >= kv:
+                    yield from sim.wait("ke%d" % s, g // kv - 1)
+                sim.tma("kf%d" % s, "sK%d" % s, phase=g // kv)
+                if g >= kv:
+                    yield from sim.wait("ve%d" % s, g // kv - 1)
+                sim.tma("vf%d" % s, "sV%d" % s, phase=g // kv)
+                g += 1
 
     def issuer():
-        def issue_s(j):
-            s = j % stages
-            yield from sim.wait("kf%d" % s, j // stages)
-            sim.mma(reads=("sQ", "sK%d" % s), writes=("S%d" % (j & 1),))
-            sim.commit("s%d" % (j & 1), phase=j >> 1)
-            sim.commit("ke%d" % s, phase=j // stages)
-        yield from sim.wait("q", 0)
-        yield from issue_s(0)
-        if nsub > 1:
-            yield from issue_s(1)
-        for j in range(nsub):
-            if plant == "one_p_barrier":
-                yield from sim.work(0, 60)      # a slow issuer
-            yield from sim.wait(P(j), Pk(j))
-            s = j % stages
-            yield from sim.wait("vf%d" % s, j // stages)
-            sim.mma(reads=("sP%d" % (j & 1), "sV%d" % s), writes=("O",))
-            sim.commit("o%d" % (j & 1), phase=j >> 1)
-            sim.commit("ve%d" % s, phase=j // stages)
-            if j + 2 < nsub:
-                yield from issue_s(j + 2)
+        def pv(gp, first):
+            yield from sim.wait("pf", gp)
+            yield from sim.wait("vf%d" % (gp % kv), gp // kv)
+            sim.mma(reads=("P", "sV%d" % (gp % kv)) + (() if first else ("O",)), writes=("O",))
+            sim.commit("ve%d" % (gp % kv), phase=gp // kv)
+            sim.commit("od", phase=gp)
+        g, prev = 0, None
+        for it, nk in enumerate(items):
+            qs = it % qb
+            yield from sim.wait("qf%d" % qs, it // qb)
+            for j in range(nk):
+                yield from sim.wait("kf%d" % (g % kv), g // kv)
+                if g > 0:
+                    yield from sim.wait("sfree", g - 1)
+                sim.mma(reads=("sQ%d" % qs, "sK%d" % (g % kv)), writes=("S",))
+                sim.commit("ke%d" % (g % kv), phase=g // kv)
+                if j == nk - 1:
+                    sim.commit("qe%d" % qs, phase=it // qb)
+                sim.commit("sf", phase=g)
+                if prev is not None:
+                    yield from pv(*prev)
+                prev = (g, j == 0)
+                g += 1
+        if prev is not None:
+            yield from pv(*prev)
 
     def softmax():
-        for j in range(nsub):
-            yield from sim.wait("s%d" % (j & 1), j >> 1)
-            t0 = sim.t
-            yield from sim.work()
-            if j > 0 and sim.rnd.random() < 0.3:   # a lazy rescale of O
-                if plant != "rescale_unguarded":
-                    yield from sim.wait("o%d" % ((j - 1) & 1), (j - 1) >> 1)
-                t1 = sim.t
-                yield from sim.work(1, 4)
-                sim.touch("warp", "w", t1, "O")
-            if j >= 2:
-                yield from sim.wait("o%d" % (j & 1), (j - 2) >> 1)
-            t2 = sim.t
-            yield from sim.work(1, 4)
-            sim.touch("warp", "w", t2, "sP%d" % (j & 1))
-            sim.touch("warp", "r", t0, "S%d" % (j & 1))
-            sim.arrive(P(j), phase=Pk(j))
-        yield from sim.wait("o%d" % ((nsub - 1) & 1), (nsub - 1) >> 1)
-        t3 = sim.t
-        yield from sim.work(1, 4)
-        sim.touch("warp", "r", t3, "O")
+        g = 0
+        for nk in items:
+            for j in range(nk):
+                yield from sim.wait("sf", g)
+                t0 = sim.t
+                yield from sim.work(1, 3)
+                if plant == "s_free_early":
+                    sim.arrive("sfree", phase=g)
+                    yield from sim.work(1, 3)
+                    sim.touch("warp", "r", t0, "S")
+                else:
+                    sim.touch("warp", "r", t0, "S")
+                    sim.arrive("sfree", phase=g)
+                yield from sim.work()
+                if j > 0:
+                    if plant != "p_unguarded":
+                        yield from sim.wait("od", g - 1)
+                    if sim.rnd.random() < 0.3:   # a lazy rescale of O
+                        t1 = sim.t
+                        yield from sim.work(1, 3)
+                        sim.touch("warp", "w", t1, "O")
+                t2 = sim.t
+                yield from sim.work(1, 3)
+                sim.touch("warp", "w", t2, "P")
+                sim.arrive("pf", phase=g)
+                g += 1
+            yield from sim.wait("od", g - 1)
+            t3 = sim.t
+            yield from sim.work(1, 3)
+            sim.touch("warp", "r", t3, "O")
 
     sim.run([loader(), issuer()] + [softmax() for _ in range(nsoft)])
     return sim.errors
 
 
 # -------------------------------------------------------------- dK / dV
-def dkv(nsub, seed, plant=None, staged=True, ncomp=DKV_WARPS, stages=DKV_STAGES):
-    """Loader warp: k, v once; q(j), dy(j) (and, staged, that sub-block's
-    lse / D) into ring stage j % stages once dV, dK(j - stages) have read it;
-    not staged, the whole block's lse / D by plain stores first.  MMA warp:
-    S^T(j), dP^T(j) into tensor memory once the warps have copied out
-    S^T(j - 1), dP^T(j - 1); then dV, dK(j - 1) from P^T, dS^T(j - 1).
-    Compute warps: S^T, dP^T -> P^T, dS^T in tensor memory (after dV,
-    dK(j - 1) have read them); dV, dK read at the end."""
+def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stages=DKV_STAGES):
+    """attn_bwd_dkv_tc_kernel.  Loader: per item k, v into buffer it % kvb
+    once the item kvb back has issued its last S^T, dP^T; per query
+    sub-block g q, dy (and, staged, their lse / D) into ring stage
+    g % stages once dV, dK(g - stages) have read it.  MMA issuer, over all
+    sub-blocks in turn: S^T(g), dP^T(g) once the warps have copied out
+    S^T(g - 1), dP^T(g - 1); then dV, dK(g - 1) from P^T, dS^T(g - 1);
+    the item's last one also commits the accumulators' completion.
+    Elementwise warps: copy S^T, dP^T out; (staged) wait for the stage's
+    lse / D; P^T, dS^T into tensor memory once dV, dK(g - 1) have read them;
+    dV, dK read at the end of each item."""
     sim = Sim(seed, plant)
-    for n in ("kv", "ld", "sf", "pe", "done"):
-        sim.bar(n)
+    for i in range(kvb):
+        sim.bar("kvf%d" % i)
+        sim.bar("kve%d" % i)
     for s in range(stages):
         sim.bar("qf%d" % s)
         sim.bar("qe%d" % s)
-    sim.bar("se", ncomp)
+    sim.bar("sf")
+    sim.bar("sfree", ncomp)
     sim.bar("pf", ncomp)
+    sim.bar("pe")
+    sim.bar("acc")
 
     def stage_bufs(s):
         return ("sQ%d" % s, "sD%d" % s) + (("sLD%d" % s,) if staged else ())
 
     def loader():
-        sim.tma("kv", "sK", "sV", phase=0)
-        for j in range(min(nsub, stages)):
-            sim.tma("qf%d" % (j % stages), *stage_bufs(j % stages), phase=0)
-        if not staged:
-            t0 = sim.t
-            yield from sim.work(1, 6)
-            sim.touch("loader", "w", t0, "sLD")
-        sim.arrive("ld", phase=0)
-        for j in range(stages, nsub):
-            s = j % stages
-            yield from sim.wait("qe%d" % s, j // stages - 1)
-            sim.tma("qf%d" % s, *stage_bufs(s), phase=j // stages)
+        g = 0
+        for it, nsub in enumerate(items):
+            b = it % kvb
+            if it >= kvb and plant != "kv_refill_unguarded":
+                yield from sim.wait("kve%d" % b, it // kvb - 1)
+            sim.tma("kvf%d" % b, "sK%d" % b, "sV%d" % b, phase=it // kvb)
+            for _ in range(nsub):
+                s = g % stages
+                if g >= stages:
+                    yield from sim.wait("qe%d" % s, g // stages - 1)
+                sim.tma("qf%d" % s, *stage_bufs(s), phase=g // stages)
+                g += 1
 
     def mma():
-        yield from sim.wait("kv", 0)
-        for j in range(nsub + 1):
-            if j < nsub:
-                s = j % stages
-                yield from sim.wait("qf%d" % s, j // stages)
-                if j > 0:
-                    yield from sim.wait("se", j - 1)
-                sim.mma(reads=("sK", "sV", "sQ%d" % s, "sD%d" % s), writes=("St", "dPt"))
-                sim.commit("sf", phase=j)
-            if j >= 1:
-                jj = j - 1
-                s = jj % stages
-                yield from sim.wait("pf", jj)
-                sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s), writes=("dV", "dK"))
-                sim.commit("pe", phase=jj)
-                sim.commit("qe%d" % s, phase=jj // stages)
-        sim.commit("done", phase=0)
+        def dvdk(gp, first, last):
+            s = gp % stages
+            yield from sim.wait("pf", gp)
+            acc = () if first else ("dV", "dK")
+            sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s) + acc, writes=("dV", "dK"))
+            sim.commit("qe%d" % s, phase=gp // stages)
+            sim.commit("pe", phase=gp)
+            if last:
+                sim.commit("acc", phase=it_of[gp])
+        g, prev = 0, None
+        it_of = {}
+        for it, nsub in enumerate(items):
+            b = it % kvb
+            yield from sim.wait("kvf%d" % b, it // kvb)
+            for j in range(nsub):
+                s = g % stages
+                it_of[g] = it
+                yield from sim.wait("qf%d" % s, g // stages)
+                if g > 0:
+                    yield from sim.wait("sfree", g - 1)
+                sim.mma(reads=("sK%d" % b, "sV%d" % b, "sQ%d" % s, "sD%d" % s), writes=("St", "dPt"))
+                if j == nsub - 1:
+                    sim.commit("kve%d" % b, phase=it // kvb)
+                sim.commit("sf", phase=g)
+                if prev is not None:
+                    yield from dvdk(*prev)
+                prev = (g, j == 0, j == nsub - 1)
+                g += 1
+        if prev is not None:
+            yield from dvdk(*prev)
 
     def compute():
-        yield from sim.wait("ld", 0)
-        for j in range(nsub):
-            s = j % stages
-            yield from sim.wait("sf", j)
-            t0 = sim.t
+        g = 0
+        for it, nsub in enumerate(items):
+            for _ in range(nsub):
+                s = g % stages
+                yield from sim.wait("sf", g)
+                t0 = sim.t
+                yield from sim.work(1, 3)
+                sim.touch("warp", "r", t0, "St", "dPt")
+                sim.arrive("sfree", phase=g)
+                if staged:  # the stage's lse / D arrive with its q / dy tiles
+                    yield from sim.wait("qf%d" % s, g // stages)
+                t1 = sim.t
+                yield from sim.work()
+                if staged:
+                    sim.touch("warp", "r", t1, "sLD%d" % s)
+                if g > 0 and plant != "p_overwrite_unguarded":
+                    yield from sim.wait("pe", g - 1)
+                t2 = sim.t
+                yield from sim.work(1, 3)
+                sim.touch("warp", "w", t2, "Pt", "dSt")
+                sim.arrive("pf", phase=g)
+                g += 1
+            yield from sim.wait("acc", it)
+            t3 = sim.t
             yield from sim.work(1, 3)
-            sim.touch("warp", "r", t0, "St", "dPt")
-            sim.arrive("se", phase=j)
-            if staged:  # the stage's lse / D arrive with its q / dy tiles
-                yield from sim.wait("qf%d" % s, j // stages)
-            t1 = sim.t
-            yield from sim.work()
-            if j > 0 and plant != "p_overwrite_unguarded":
-                yield from sim.wait("pe", j - 1)
-            t2 = sim.t
-            yield from sim.work(1, 3)
-            sim.touch("warp", "w", t2, "Pt", "dSt")
-            sim.touch("warp", "r", t1, "sLD%d" % s if staged else "sLD")
-            sim.arrive("pf", phase=j)
-        yield from sim.wait("done", 0)
-        t3 = sim.t
-        yield from sim.work(1, 3)
-        sim.touch("warp", "r", t3, "dV", "dK")
+            sim.touch("warp", "r", t3, "dV", "dK")
+            yield  # the named barrier around the column-sum exchange
 
     sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
 
 
 # -------------------------------------------------------------- dQ
-def dq(nsub, seed, plant=None, ncomp=DQ_WARPS, kst=DQ_K_STAGES, vst=DQ_V_STAGES):
-    """One warp loads and issues: q, dy once, k(0..kst-1), v(0..vst-1); S(0),
-    dP(0).  Per sub-block j: once the warps have copied out S(j), dP(j),
-    v(j + vst) into v's stage and S(j + 1), dP(j + 1); once dS(j) is in
-    shared memory buffer j % 2, dQ(j); once dQ(j - 1) has read k's stage,
-    k(j + 2) into it.  Compute warps: S(j), dP(j) -> dS(j) (after dQ(j - 2)
-    has read the buffer); dQ read at the end."""
+def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST):
+    """attn_bwd_dq_tc_kernel.  Loader: per item q, dy into buffer it % qb
+    once the item qb back has issued its last S, dP; per key block k into
+    stage g % kst once dQ(g - kst) has read it, v into stage g % vst once
+    dP(g - vst) has.  MMA issuer, over all blocks in turn: S(g), dP(g) once
+    the warps have copied out S(g - 1), dP(g - 1); then dQ(g - 1) from
+    dS(g - 1) (the item's last one also commits dQ's completion).
+    Elementwise warps: copy S, dP out; dS into tensor memory once dQ(g - 1)
+    has read it; dQ read at the end of each item."""
     sim = Sim(seed, plant)
-    for n in ("q", "sf", "done"):
-        sim.bar(n)
+    for i in range(qb):
+        sim.bar("qf%d" % i)
+        sim.bar("qe%d" % i)
     for s in range(kst):
         sim.bar("kf%d" % s)
         sim.bar("ke%d" % s)
     for s in range(vst):
         sim.bar("vf%d" % s)
-    sim.bar("se", ncomp)
-    for i in range(2):
-        sim.bar("pf%d" % i, ncomp)
-        sim.bar("pe%d" % i)
+        sim.bar("ve%d" % s)
+    sim.bar("sf")
+    sim.bar("sfree", ncomp)
+    sim.bar("pf", ncomp)
+    sim.bar("dsf")
+    sim.bar("dqf")
 
-    def issuer():
-        def load_k(j):
-            sim.tma("kf%d" % (j % kst), "sK%d" % (j % kst), phase=j // kst)
+    def loader():
+        g = 0
+        for it, nk in enumerate(items):
+            b = it % qb
+            if it >= qb:
+                yield from sim.wait("qe%d" % b, it // qb - 1)
+            sim.tma("qf%d" % b, "sQ%d" % b, "sD%d" % b, phase=it // qb)
+            for _ in range(nk):
+                ks, vs = g % kst, g % vst
+                if g >= kst and plant != "k_refill_unguarded":
+                    yield from sim.wait("ke%d" % ks, g // kst - 1)
+                sim.tma("kf%d" % ks, "sK%d" % ks, phase=g // kst)
+                if g >= vst:
+                    yield from sim.wait("ve%d" % vs, g // vst - 1)
+                sim.tma("vf%d" % vs, "sV%d" % vs, phase=g // vst)
+                g += 1
 
-        def load_v(j):
-            sim.tma("vf%d" % (j % vst), "sV%d" % (j % vst), phase=j // vst)
+    def mma():
+        it_of = {}
 
-        def issue_sdp(j):
-            ks, vs = j % kst, j % vst
-            yield from sim.wait("kf%d" % ks, j // kst)
-            yield from sim.wait("vf%d" % vs, j // vst)
-            sim.mma(reads=("sQ", "sD", "sK%d" % ks, "sV%d" % vs), writes=("S", "dP"))
-            sim.commit("sf", phase=j)
-        sim.tma("q", "sQ", "sD", phase=0)
-        for j in range(min(kst, nsub)):
-            load_k(j)
-        for j in range(min(vst, nsub)):
-            load_v(j)
-        yield from sim.wait("q", 0)
-        yield from issue_sdp(0)
-        for j in range(nsub):
-            if j + 1 < nsub:
-                yield from sim.wait("se", j)
-                if j + vst < nsub:
-                    load_v(j + vst)
-                yield from issue_sdp(j + 1)
-            yield from sim.wait("pf%d" % (j & 1), j >> 1)
-            ks = j % kst
-            sim.mma(reads=("sS%d" % (j & 1), "sK%d" % ks), writes=("dQ",))
-            sim.commit("pe%d" % (j & 1), phase=j >> 1)
-            sim.commit("ke%d" % ks, phase=j // kst)
-            if j >= 1 and j + 2 < nsub:
-                if plant != "k_refill_unguarded":
-                    yield from sim.wait("ke%d" % ((j - 1) % kst), (j - 1) // kst)
-                load_k(j + 2)
-        sim.commit("done", phase=0)
+        def dqm(gp, first, last):
+            ks = gp % kst
+            yield from sim.wait("pf", gp)
+            sim.mma(reads=("dS", "sK%d" % ks) + (() if first else ("dQ",)), writes=("dQ",))
+            sim.commit("ke%d" % ks, phase=gp // kst)
+            sim.commit("dsf", phase=gp)
+            if last:
+                sim.commit("dqf", phase=it_of[gp])
+        g, prev = 0, None
+        for it, nk in enumerate(items):
+            b = it % qb
+            yield from sim.wait("qf%d" % b, it // qb)
+            for j in range(nk):
+                ks, vs = g % kst, g % vst
+                it_of[g] = it
+                yield from sim.wait("kf%d" % ks, g // kst)
+                yield from sim.wait("vf%d" % vs, g // vst)
+                if g > 0:
+                    yield from sim.wait("sfree", g - 1)
+                sim.mma(reads=("sQ%d" % b, "sD%d" % b, "sK%d" % ks, "sV%d" % vs), writes=("S", "dP"))
+                sim.commit("ve%d" % vs, phase=g // vst)
+                if j == nk - 1:
+                    sim.commit("qe%d" % b, phase=it // qb)
+                sim.commit("sf", phase=g)
+                if prev is not None:
+                    yield from dqm(*prev)
+                prev = (g, j == 0, j == nk - 1)
+                g += 1
+        if prev is not None:
+            yield from dqm(*prev)
 
     def compute():
-        for j in range(nsub):
-            yield from sim.wait("sf", j)
-            t0 = sim.t
+        g = 0
+        for it, nk in enumerate(items):
+            for _ in range(nk):
+                yield from sim.wait("sf", g)
+                t0 = sim.t
+                yield from sim.work(1, 3)
+                sim.touch("warp", "r", t0, "S", "dP")
+                sim.arrive("sfree", phase=g)
+                yield from sim.work()
+                if g > 0:
+                    k = g - 1 if plant != "ds_wrong_phase" else g
+                    yield from sim.wait("dsf", k)
+                t1 = sim.t
+                yield from sim.work(1, 3)
+                sim.touch("warp", "w", t1, "dS")
+                sim.arrive("pf", phase=g)
+                g += 1
+            yield from sim.wait("dqf", it)
+            t2 = sim.t
             yield from sim.work(1, 3)
-            sim.touch("warp", "r", t0, "S", "dP")
-            sim.arrive("se", phase=j)
-            # dQ(j - 2) has read dS buffer j % 2; for j < 2 the wait is on
-            # phase -1 (the barrier must still be in phase 0)
-            k = (j - 2) >> 1 if plant != "p_wrong_phase" else j >> 1
-            yield from sim.wait("pe%d" % (j & 1), k)
-            t1 = sim.t
-            yield from sim.work(1, 4)
-            sim.touch("warp", "w", t1, "sS%d" % (j & 1))
-            sim.arrive("pf%d" % (j & 1), phase=j >> 1)
-        yield from sim.wait("done", 0)
-        t2 = sim.t
-        yield from sim.work(1, 3)
-        sim.touch("warp", "r", t2, "dQ")
+            sim.touch("warp", "r", t2, "dQ")
+            yield  # the named barrier around the column-sum exchange
 
-    sim.run([issuer()] + [compute() for _ in range(ncomp)])
+    sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
-
-
-NSUB = list(range(1, 10)) + [16, 17]
 
 
 @pytest.mark.parametrize("model", [forward, dkv, dq])
 def test_protocol_has_no_deadlock_aliased_wait_or_race(model):
-    for nsub in NSUB:
-        for seed in range(8):
-            errs = model(nsub, seed)
-            assert not errs, (model.__name__, nsub, seed, errs[:3])
+    for items in ITEMS:
+        for seed in range(6):
+            errs = model(items, seed)
+            assert not errs, (model.__name__, items, seed, errs[:3])
 
 
-def test_dkv_protocol_with_whole_block_lse_preload():
-    for nsub in (1, 3, 5, 8):
-        for seed in range(8):
-            errs = dkv(nsub, seed, staged=False)
-            assert not errs, (nsub, seed, errs[:3])
+def test_protocols_with_one_buffer_per_item_and_head_size_128_rings():
+    # head size 128: one q buffer (forward keeps two), one k/v buffer set
+    # (dK/dV), one q/dy buffer and 2 key stages (dQ)
+    for items in ITEMS:
+        for seed in range(4):
+            assert not dkv(items, seed, kvb=1), items
+            assert not dq(items, seed, qb=1, kst=2), items
+            assert not forward(items, seed, qb=1), items
 
 
-@pytest.mark.parametrize("model,plant,kind", [
-    (forward, "one_p_barrier", "aliased wait"),
-    (forward, "k_refill_unguarded", "race on sK"),
-    (forward, "rescale_unguarded", "race on O"),
-    (dkv, "p_overwrite_unguarded", "race on Pt"),
-    (dq, "k_refill_unguarded", "race on sK"),
-    (dq, "p_wrong_phase", "no progress"),
+def test_dkv_protocol_with_lse_and_d_from_global_memory():
+    for items in ITEMS:
+        for seed in range(4):
+            errs = dkv(items, seed, staged=False)
+            assert not errs, (items, seed, errs[:3])
+
+
+def _find(model, plant, kind, seeds=12, **kw):
+    for items in ITEMS[2:]:
+        for seed in range(seeds):
+            errs = model(items, seed, plant=plant, **kw)
+            if any(kind in e for e in errs):
+                return errs
+    return []
+
+
+@pytest.mark.parametrize("model,plant,kind,kw", [
+    (forward, "s_free_early", "race on S", {}),
+    (forward, "p_unguarded", "race on P", {}),
+    (forward, "q_refill_unguarded", "race on sQ", dict(qb=1)),
+    (dkv, "p_overwrite_unguarded", "race on Pt", {}),
+    (dkv, "kv_refill_unguarded", "race on sK", dict(kvb=1)),
+    (dq, "k_refill_unguarded", "race on sK", {}),
+    (dq, "ds_wrong_phase", "no progress", {}),
 ])
-def test_the_checker_finds_a_planted_mistake(model, plant, kind):
-    errs = find(model, plant, kind, range(4, 12))
+def test_the_checker_finds_a_planted_mistake(model, plant, kind, kw):
+    errs = _find(model, plant, kind, **kw)
     assert errs, "%s with %s: not found" % (model.__name__, plant)
 
 

@@ -3,34 +3,46 @@
 // GeekNews, "A GPT-2-based ChatGPT clone in 3000 bytes of C", section "The
 // Transformer core": per head, S = q k^T (scaled by 1/sqrt(hs)), the lower-
 // triangular causal mask, softmax over each query row, times v.  Here the
-// T x T score matrix is never stored: it is computed one 128 x 128 tile at a
-// time in TMEM and folded into an online softmax (forward) or recomputed from
-// the saved row logsumexp (backward).
+// T x T score matrix is never stored: it is computed one 128 x 128 block at
+// a time in tensor memory (TMEM), folded into an online softmax (forward) or
+// recomputed from the saved row logsumexp (backward).
 //
-// Head size 64.  Every tile of q, k, v, dy is one TMA box [128 or 64 rows x
-// 64] of a 3-D tensor map over [B, T, width] (rows past T read as zero),
-// landing 128-byte-swizzled in shared memory, where a tcgen05 descriptor can
-// read it either as a K-major operand (rows = M or N) or as an MN-major one
-// (rows = K) -- so S = q k^T, P v, dV = P^T dy, dK = dS^T q and dQ = dS k all
-// read the same tiles.  Each kernel is warp-specialised: one thread issues
-// the TMA loads and MMAs, the other warps do the elementwise work, and every
-// hand-off is an mbarrier.
+// Head sizes 16, 32, 64 and 128.  Every tile of q, k, v, dy is one or two
+// TMA boxes [rows x 64 columns] of a 3-D tensor map over [B, T, width] (rows
+// past T read as zero), 128-byte swizzled in shared memory, where a tcgen05
+// descriptor reads it either as a K-major operand (rows = M or N, K = head
+// dims) or as an MN-major one (rows = K).  Head sizes below 64 load the
+// full 64-column box (the extra columns are never multiplied).  The
+// probabilities P and the score gradients dS never go to shared memory:
+// the elementwise warps write them into TMEM as packed bf16 pairs, where
+// the next product reads them as its A operand.
 //
-//   forward   one CTA per (128-query block, b*h), 64-key sub-blocks: S -> TMEM
-//             (two buffers, issued two sub-blocks ahead), online softmax by 8
-//             warps (thread = query row), P -> smem, O += P v accumulated in
-//             TMEM; the softmax reference maximum moves only when a row's
-//             maximum grows by more than 2^8, and only then is O rescaled in
-//             place.  Saves lse in base 2: max*scale*log2e + log2(sum).
-//   backward  D = rowsum(dy * y); one CTA per (128-key block, b*h) for dK, dV
-//             over 128-query sub-blocks (S^T, dP^T recomputed into TMEM; P^T
-//             and dS^T written back to TMEM and read there as the A operand
-//             of dV += P^T dy, dK += dS^T q); one CTA per (128-query block,
-//             b*h) for dQ over 64-key sub-blocks (dQ += dS k, dS in smem).
-//             No atomics: every output element is written by one CTA, so the
-//             result is deterministic.
-// All mbarrier waits are bounded (common.cuh); a wait that gives up records
-// a timeout and the kernel runs to completion without trapping.
+// The tensor pipe takes about 71 cycles for one M = 128, K = 16 product at
+// N = 64 and at N = 128, and 128 cycles at N = 256 (measured on this B300),
+// so every score product here has N = 128 keys (or queries): 128-key blocks.
+//
+// All three kernels are persistent: a CTA walks a fixed list of work items
+// (a query block or key block of one (batch, head)), longest first and
+// assigned in a snake order over the grid, and the roles run ahead across
+// item boundaries (the next item's loads and score products start while
+// this item's last elementwise step and epilogue run).  Roles per CTA: one
+// TMA loader thread, one MMA issuer thread, 8 or 16 elementwise warps; every
+// hand-off is an mbarrier; every wait is bounded (common.cuh) and a wait that
+// gives up records a timeout and the kernel runs on to its end.
+//
+//   forward  item (128-query block, b*h), 128-key blocks: S(j) = q k(j)^T in
+//            TMEM; the softmax warps copy it to registers (so S(j+1) runs
+//            during their work), take P relative to a row reference maximum
+//            that moves only when the row maximum grows by more than 2^8
+//            (then O is rescaled in TMEM), write P into TMEM; O += P v(j)
+//            accumulates in TMEM.  Saves lse in base 2.
+//   dK, dV   item (128-key block, b*h), query sub-blocks of 128 (64 for head
+//            size 128): S^T = k q^T and dP^T = v dy^T; P^T and dS^T =
+//            P^T (dP^T - D) into TMEM; dV += P^T dy, dK += dS^T q.
+//   dQ       item (128-query block, b*h), 128-key blocks: S = q k^T, dP =
+//            dy v^T; dS into TMEM; dQ += dS k.
+// No atomics: every output element is written by one CTA, so the results
+// repeat bit for bit.
 #include <cuda.h>
 
 #include <cstdio>
@@ -57,10 +69,6 @@ static EncodeTiledFnA encoder_fn() {
 }
 
 // [B][T][W] bf16 tensor, box {64, rows, 1}, 128-byte swizzle, rows past T zero.
-static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows = 128);
-bool attn_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows) {
-  return make_tmap_btw(m, base, B, T, W, rows);
-}
 static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows) {
   EncodeTiledFnA f = encoder_fn();
   if (!f) return false;
@@ -72,408 +80,339 @@ static bool make_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W,
            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-#define AT_BLK 128
-#define AT_HS 64
-#define AT_TILE 16384u  // bytes of one [128 x 64] bf16 tile
-#define AB_SUB 64
-#define AT_SUBTILE 8192u  // bytes of one [64 x 64] bf16 tile
-
-// descriptors of a [128 rows x 64] tile read as a K-major operand (rows = M
-// or N, K = 64 head dims) at K-step kk (16 dims), or as an MN-major operand
-// (rows = K, 64 columns = N) at K-step kk (16 rows)
-__device__ __forceinline__ uint64_t kmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 32, 16, 1024); }
-__device__ __forceinline__ uint64_t mnmaj(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, 8192, 1024); }
-// Write 8 consecutive bf16 values (16-byte chunk c8 of a row) into a
-// 128B-swizzled [rows x 64] buffer (one atom), given the row's base pointer
-// (buf + r*128) and its swizzle (r & 7).
-__device__ __forceinline__ void st_row8(uint8_t* rowp, int rx, int c8, const float* v) {
-  uint4 u;
-  __nv_bfloat162 t0 = __floats2bfloat162_rn(v[0], v[1]), t1 = __floats2bfloat162_rn(v[2], v[3]);
-  __nv_bfloat162 t2 = __floats2bfloat162_rn(v[4], v[5]), t3 = __floats2bfloat162_rn(v[6], v[7]);
-  u.x = *reinterpret_cast<uint32_t*>(&t0);
-  u.y = *reinterpret_cast<uint32_t*>(&t1);
-  u.z = *reinterpret_cast<uint32_t*>(&t2);
-  u.w = *reinterpret_cast<uint32_t*>(&t3);
-  *reinterpret_cast<uint4*>(rowp + ((c8 ^ rx) << 4)) = u;
+bool attn_tmap_btw(CUtensorMap* m, const void* base, int B, int T, int W, int rows) {
+  return make_tmap_btw(m, base, B, T, W, rows);
 }
 
-// The dQ kernel's elementwise step for 32 key columns of one query row,
-// from the TMEM words of S (rs) and dP (rd): p = 2^(s*sl2 - lse2), ds =
-// p (dp - D), with the row's lse2 (base-2 units, as the forward saves it)
-// and D; dS (bf16) goes to the row's 16-byte chunks c8base.. of a
-// 128B-swizzled [rows x 64] atom (srow = atom + r*128, rx = r & 7).  MASK
-// applies the causal mask (only on sub-blocks that cross the diagonal).
-template <bool MASK>
-__device__ __forceinline__ void qrow_elementwise(const uint32_t* rs, const uint32_t* rd, float lse2r, float dr,
-                                                 float sl2, int col0, int rowpos, uint8_t* srow, int rx,
-                                                 int c8base) {
-#pragma unroll
-  for (int g = 0; g < 4; g++) {
-    float ds[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lse2r);
-      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dr);
-      if (MASK) dsv = col0 + g * 8 + j <= rowpos ? dsv : 0.f;
-      ds[j] = dsv;
-    }
-    st_row8(srow, rx, c8base + g, ds);
-  }
-}
+#define LOG2E_F 1.4426950408889634f
 
-// The dK/dV kernel's elementwise step for 32 query columns of one key row,
-// kept in registers: P^T and dS^T as packed bf16 pairs (pk, dk: 16 words
-// each, column pairs in order), so they can be computed before the shared-
-// memory buffer they go to is free.  lse2c: the columns' lse in base-2
-// units (as the forward saves it), dc: their D, both from shared memory.
-template <bool MASK>
-__device__ __forceinline__ void keyrow_pack(const uint32_t* rs, const uint32_t* rd, const float* lse2c,
-                                            const float* dc, float sl2, int col0, int key, int colmax,
-                                            uint32_t* pk, uint32_t* dk) {
-#pragma unroll
-  for (int g = 0; g < 4; g++) {
-    const float4 a = *reinterpret_cast<const float4*>(lse2c + g * 8);
-    const float4 bq = *reinterpret_cast<const float4*>(lse2c + g * 8 + 4);
-    const float4 c = *reinterpret_cast<const float4*>(dc + g * 8);
-    const float4 d = *reinterpret_cast<const float4*>(dc + g * 8 + 4);
-    const float lv[8] = {a.x, a.y, a.z, a.w, bq.x, bq.y, bq.z, bq.w};
-    const float dv[8] = {c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
-    float p[8], ds[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-      const float pv = ex2_hw(__uint_as_float(rs[g * 8 + j]) * sl2 - lv[j]);
-      float dsv = pv * (__uint_as_float(rd[g * 8 + j]) - dv[j]);
-      float pkv = pv;
-      if (MASK) {  // a masked column may hold stale lse / D: select, do not scale
-        const int col = col0 + g * 8 + j;
-        const bool ok = col >= key && col < colmax;
-        pkv = ok ? pkv : 0.f;
-        dsv = ok ? dsv : 0.f;
-      }
-      p[j] = pkv;
-      ds[j] = dsv;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; j += 2) {
-      __nv_bfloat162 tp = __floats2bfloat162_rn(p[j], p[j + 1]);
-      __nv_bfloat162 td = __floats2bfloat162_rn(ds[j], ds[j + 1]);
-      pk[g * 4 + j / 2] = *reinterpret_cast<uint32_t*>(&tp);
-      dk[g * 4 + j / 2] = *reinterpret_cast<uint32_t*>(&td);
-    }
-  }
-}
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
 }
 
-__device__ __forceinline__ void store_row32_bf16(bf16* dst, const float* v, float mul) {
+// Tiles: R rows x HS head dims, stored as NB = ceil(HS/64) boxes of
+// [R rows x 64 columns] (128 bytes per row, 128-byte swizzle), box i at
+// tile + i * R * 128.
+template <int HS>
+struct Hs {
+  static_assert(HS == 16 || HS == 32 || HS == 64 || HS == 128, "head size");
+  static constexpr int NB = HS > 64 ? 2 : 1;
+  static constexpr int KS = HS / 16;  // K steps of 16 over the head dims
+};
+// K-major operand (rows = M or N, K = head dims), K step kk
+__device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int kk) {
+  return sw128_desc(tile + (uint32_t)((kk >> 2) * rows * 128 + (kk & 3) * 32), 16, 1024);
+}
+// MN-major operand (rows = K, head dims = N), K step kk (16 rows); the
+// 64-column boxes are rows*128 bytes apart
+__device__ __forceinline__ uint64_t ndesc(uint32_t tile, int rows, int kk) {
+  return sw128_desc(tile + (uint32_t)(kk * 2048), (uint32_t)(rows * 128), 1024);
+}
+// TMA of one tile (NB boxes) onto one barrier
+template <int HS>
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int col,
+                                          int row, int b, int rows) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
+  for (int i = 0; i < Hs<HS>::NB; i++) tma_load_3d(dst + i * rows * 128, map, bar, col + 64 * i, row, b);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+// N floats (N a multiple of 8) times mul as bf16 to 16-byte aligned global memory
+template <int N>
+__device__ __forceinline__ void store_bf16_row(bf16* dst, const float* v, float mul) {
+#pragma unroll
+  for (int i = 0; i < N; i += 8) {
     uint4 u;
-    __nv_bfloat162 t0 = __floats2bfloat162_rn(v[i] * mul, v[i + 1] * mul);
-    __nv_bfloat162 t1 = __floats2bfloat162_rn(v[i + 2] * mul, v[i + 3] * mul);
-    __nv_bfloat162 t2 = __floats2bfloat162_rn(v[i + 4] * mul, v[i + 5] * mul);
-    __nv_bfloat162 t3 = __floats2bfloat162_rn(v[i + 6] * mul, v[i + 7] * mul);
-    u.x = *reinterpret_cast<uint32_t*>(&t0);
-    u.y = *reinterpret_cast<uint32_t*>(&t1);
-    u.z = *reinterpret_cast<uint32_t*>(&t2);
-    u.w = *reinterpret_cast<uint32_t*>(&t3);
+    u.x = pack_bf16(v[i] * mul, v[i + 1] * mul);
+    u.y = pack_bf16(v[i + 2] * mul, v[i + 3] * mul);
+    u.z = pack_bf16(v[i + 4] * mul, v[i + 5] * mul);
+    u.w = pack_bf16(v[i + 6] * mul, v[i + 7] * mul);
     *reinterpret_cast<uint4*>(dst + i) = u;
   }
 }
-
-// Column sums of a warp's 32 rows x 32 columns (lane = row, v[j] = column
-// j): a reduce-scatter over the lanes (16 + 8 + 4 + 2 + 1 shuffles); lane l
-// returns the sum of column l.
-__device__ __forceinline__ float warp_colsum32(float* v) {
-  const int lane = threadIdx.x & 31;
+// Sum over the 32 lanes of each of N values; every lane gets the sums.
+template <int N>
+__device__ __forceinline__ void warp_sum_cols(float* v) {
 #pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const bool up = (lane & off) != 0;
-#pragma unroll
-    for (int i = 0; i < off; i++) {
-      const float send = up ? v[i] : v[i + off];
-      const float keep = up ? v[i + off] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
-  return v[0];
+  for (int i = 0; i < N; i++) v[i] = warp_sum(v[i]);
 }
 
-// 8 warps: warps w and w+4 read the same TMEM lane quarter (w % 4, i.e. the
-// same 32 query or key rows) and split the 128 score columns (half = w / 4
-// takes columns 64*half .. 64*half+63) and the 64 output head dims
-// (32*half .. 32*half+31).
-#define AT_THREADS 256
+// The persistent schedule: round r of CTA c takes item r*G + c (r even) or
+// r*G + G-1-c (r odd), so the longest items (first in the list) spread over
+// the grid and each CTA's total stays close to the mean.
+__device__ __forceinline__ int snake_item(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
 
 // ============================================================ forward
-// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks;
-// two CTAs share an SM.  Warps 0..7 do the online softmax; warp 8 (one
-// thread) issues every MMA and warp 9 (one thread) every TMA load, so no
-// softmax warp stalls on them and no load waits behind an MMA hand-off:
-//   S(j) = q k(j)^T into TMEM S[j%2], issued two sub-blocks ahead (as soon
-//          as softmax(j-2) has read that buffer);
-//   O += P(j) v(j) into one TMEM accumulator once P(j) is in shared
-//          memory; the softmax warps take P relative to a reference maximum
-//          that moves only when a row's maximum exceeds it by more than 8 in
-//          log2 units (P <= 2^8), and then rescale O in TMEM after PV(j-1)
-//          has completed and before they release P(j) (lazy rescaling);
-//   k and v stream through three-stage rings, each stage refilled by the
-//          loader as soon as the MMA that read it has completed (k_empty /
-//          v_empty, committed with the MMAs).
-// Warps w and w+4 exchange their half-row maxima through a double-buffered
-// array and a 64-thread named barrier.
-// TMEM: S0 S1 (columns 0..127), O (128..191).
-// smem: Q | K ring | V ring (64-row tiles) | P0 P1 ([128 x 64]) | row-max exchange [2][2][128] | barriers
-#define AF_KV_STAGES 3
-#define AF_THREADS (AT_THREADS + 64)
-#define AF_SMEM (1024 + AT_TILE + 2 * AF_KV_STAGES * AT_SUBTILE + 2 * AT_TILE + 2048 + 256)
+// Warps 0..7 softmax (warps w and w+4 share TMEM lane quarter w % 4, i.e. 32
+// query rows, and take key columns 0..63 / 64..127 of a block and head dims
+// 0..HS/2-1 / HS/2..HS-1 of O), warp 8 the MMA issuer, warp 9 the loader.
+// TMEM: S 0..127, P 128..191 (bf16 pairs), O 192..192+HS-1.
+// smem: Q [2] | K ring [2] | V ring [2] | row-max exchange [2][2][128] |
+//       row-sum exchange [2][128] | barriers.
+#define FW_SOFT 8
+#define FW_THREADS (FW_SOFT * 32 + 64)
+template <int HS>
+struct FwdCfg {
+  static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;  // [128 x HS]
+  static constexpr int QB = 2, KV = 2;
+  static constexpr int TMEM = HS > 64 ? 512 : 256;
+  static constexpr int PER_SM = HS > 64 ? 1 : 2;
+  static constexpr uint32_t SMEM = 1024 + (QB + 2 * KV) * TILE + 2048 + 1024 + 256;
+};
 
-__global__ void __launch_bounds__(AF_THREADS, 2)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                       const __grid_constant__ CUtensorMap tm_qkv64, bf16* y, float* lse, int T,
+template <int HS>
+__global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* y, float* lse, int B, int T,
                        int C, int NH, float scale, int* err) {
-  pdl_trigger();
+  using Cf = FwdCfg<HS>;
+  constexpr int QB = Cf::QB, KV = Cf::KV;
+  constexpr uint32_t TILE = Cf::TILE;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
   uint8_t* sQ = sm;
-  uint8_t* sK = sm + AT_TILE;                    // [AF_KV_STAGES] x [64 x 64]
-  uint8_t* sV = sK + AF_KV_STAGES * AT_SUBTILE;  // [AF_KV_STAGES]
-  uint8_t* sP = sV + AF_KV_STAGES * AT_SUBTILE;  // 2 x [128 x 64]
-  float* red = reinterpret_cast<float*>(sP + 2 * AT_TILE);  // [2 iterations][2 halves][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * AT_TILE + 2048);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                  // [AF_KV_STAGES]
-  uint64_t* v_full = k_full + AF_KV_STAGES;     // [AF_KV_STAGES]
-  uint64_t* s_done = v_full + AF_KV_STAGES;     // [2]
-  uint64_t* o_done = s_done + 2;                // [2]
-  // [2]: 8 warp arrivals for sub-block j on p_ready[j % 2] (two barriers, so
-  // the softmax warps, which may run a sub-block ahead of the issuer, never
-  // complete a barrier's phase twice before the issuer has waited for it)
-  uint64_t* p_ready = o_done + 2;
-  uint64_t* k_empty = p_ready + 2;               // [AF_KV_STAGES]: S of the stage done
-  uint64_t* v_empty = k_empty + AF_KV_STAGES;    // [AF_KV_STAGES]: PV of the stage done
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(v_empty + AF_KV_STAGES);
+  uint8_t* sK = sQ + QB * TILE;
+  uint8_t* sV = sK + KV * TILE;
+  float* red = reinterpret_cast<float*>(sV + KV * TILE);  // [2][2][128]
+  float* lred = red + 512;                                 // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lred + 256);
+  uint64_t* q_full = bars;             // [QB]
+  uint64_t* q_empty = q_full + QB;     // [QB]: the item's last S has read Q
+  uint64_t* k_full = q_empty + QB;     // [KV]
+  uint64_t* k_empty = k_full + KV;     // [KV]
+  uint64_t* v_full = k_empty + KV;     // [KV]
+  uint64_t* v_empty = v_full + KV;     // [KV]
+  uint64_t* s_full = v_empty + KV;     // S(g) in TMEM
+  uint64_t* s_free = s_full + 1;       // the softmax warps have copied S(g) out
+  uint64_t* p_full = s_free + 1;       // the softmax warps have written P(g)
+  uint64_t* o_done = p_full + 1;       // P(g) V(g) complete
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(o_done + 1);
 
-  const int nqb = gridDim.y;
-  const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the longest rows
-  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
-  const int q0 = qb * AT_BLK;
+  const int nqb = (T + 127) / 128, BH = B * NH, nitems = nqb * BH;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
-
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < AF_KV_STAGES; s++) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_empty[s], 1);
+    for (int i = 0; i < QB; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
+    for (int i = 0; i < KV; i++) {
+      mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1);
     }
-    for (int i = 0; i < 2; i++) {
-      mbar_init(&s_done[i], 1);
-      mbar_init(&o_done[i], 1);
-      mbar_init(&p_ready[i], AT_THREADS / 32);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, FW_SOFT);
+    mbar_init(p_full, FW_SOFT);
+    mbar_init(o_done, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
-    tma_prefetch_desc(&tm_qkv64);
   }
-  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
+  if (warp == 0) { tmem_alloc(tslot, Cf::TMEM); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  pdl_wait();  // from here on global memory written by the previous kernel is read
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
+  pdl_wait();     // from here on global memory written by the previous kernel is read
+  const uint32_t tS = tm, tP = tm + 128, tO = tm + 192;
 
-  if (warp == 8) {
+  if (warp == FW_SOFT) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
-      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
-      auto issue_s = [&](int j) {  // S(j) into S[j%2]; its k stage is then free
-        const int s = j % AF_KV_STAGES;
-        mbar_wait(&k_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
+      const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+      const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
+      auto pv = [&](int gp, bool first) {  // O (+)= P(gp) v(gp), P from TMEM
+        mbar_wait(p_full, (uint32_t)gp & 1u, err);
+        mbar_wait(&v_full[gp % KV], (uint32_t)(gp / KV) & 1u, err);
         tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ), bK = smem_u32(sK + s * AT_SUBTILE);
+        const uint32_t bV = smem_u32(sV + (gp % KV) * TILE);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + (uint32_t)((j & 1) * 64), kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-        tc_commit(&s_done[j & 1]);
-        tc_commit(&k_empty[s]);
+        for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tO, tP + kk * 8, ndesc(bV, 128, kk), idO, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(&v_empty[gp % KV]);
+        tc_commit(o_done);
       };
-      mbar_wait(q_full, 0, err);
-      issue_s(0);
-      if (nsub > 1) issue_s(1);
-      for (int j = 0; j < nsub; j++) {
-        mbar_wait(&p_ready[j & 1], (uint32_t)(j >> 1) & 1u, err);  // P(j) written, S[j%2] read
-        tc_fence_after();
-        const int s = j % AF_KV_STAGES;
-        mbar_wait(&v_full[s], (uint32_t)(j / AF_KV_STAGES) & 1u, err);
-        tc_fence_after();
-        const uint32_t aP = smem_u32(sP + (j & 1) * AT_TILE), bV = smem_u32(sV + s * AT_SUBTILE);
+      int g = 0, it = 0;
+      bool prev = false, prev_first = false;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int nk = nqb - idx / BH;  // key blocks 0 .. qb
+        const int qs = it % QB;
+        mbar_wait(&q_full[qs], (uint32_t)(it / QB) & 1u, err);
+        const uint32_t aQ = smem_u32(sQ + qs * TILE);
+        for (int j = 0; j < nk; j++, g++) {
+          mbar_wait(&k_full[g % KV], (uint32_t)(g / KV) & 1u, err);
+          if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
+          tc_fence_after();
+          const uint32_t bK = smem_u32(sK + (g % KV) * TILE);
 #pragma unroll
-        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tm + 128, kmaj(aP, kk), mnmaj(bV, kk), idO, (j > 0 || kk > 0));
-        tc_commit(&o_done[j & 1]);
-        tc_commit(&v_empty[s]);
-        if (j + 2 < nsub) issue_s(j + 2);
+          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tS, kdesc(aQ, 128, kk), kdesc(bK, 128, kk), idS, kk > 0 ? 1u : 0u);
+          tc_commit(&k_empty[g % KV]);
+          if (j == nk - 1) tc_commit(&q_empty[qs]);
+          tc_commit(s_full);
+          if (prev) pv(g - 1, prev_first);  // the previous block's PV runs after this S
+          prev = true;
+          prev_first = j == 0;
+        }
       }
+      if (prev) pv(g - 1, prev_first);
     }
-  } else if (warp == 9) {
+  } else if (warp == FW_SOFT + 1) {
     // ------------------------------------------------------------ TMA loader
-    // q once; k(j) and v(j) into their ring stages as soon as the MMA that
-    // read the stage's previous tile (S(j-3), PV(j-3)) has completed
     if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, AT_TILE);
-      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-      for (int j = 0; j < nsub; j++) {
-        const int s = j % AF_KV_STAGES;
-        const uint32_t ph = (uint32_t)(j / AF_KV_STAGES - 1) & 1u;
-        if (j >= AF_KV_STAGES) mbar_wait(&k_empty[s], ph, err);
-        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
-        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
-        if (j >= AF_KV_STAGES) mbar_wait(&v_empty[s], ph, err);
-        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
-        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
+      int g = 0, it = 0;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
+        const int qs = it % QB;
+        if (it >= QB) mbar_wait(&q_empty[qs], (uint32_t)(it / QB - 1) & 1u, err);
+        mbar_arrive_expect_tx(&q_full[qs], TILE);
+        load_tile<HS>(sQ + qs * TILE, &tm_qkv, &q_full[qs], h * HS, qb * 128, b, 128);
+        for (int j = 0; j <= qb; j++, g++) {
+          const int s = g % KV;
+          if (g >= KV) mbar_wait(&k_empty[s], (uint32_t)(g / KV - 1) & 1u, err);
+          mbar_arrive_expect_tx(&k_full[s], TILE);
+          load_tile<HS>(sK + s * TILE, &tm_qkv, &k_full[s], C + h * HS, j * 128, b, 128);
+          if (g >= KV) mbar_wait(&v_empty[s], (uint32_t)(g / KV - 1) & 1u, err);
+          mbar_arrive_expect_tx(&v_full[s], TILE);
+          load_tile<HS>(sV + s * TILE, &tm_qkv, &v_full[s], 2 * C + h * HS, j * 128, b, 128);
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane, q = q0 + row;
-    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
-    const float sl2 = scale * 1.4426950408889634f;  // scores -> log2 units
-    // m: the row's reference maximum (raw score units).  P and the row sum
-    // are taken relative to it; it moves only when a new maximum exceeds it
-    // by more than 8 in log2 units (so P <= 2^8), and then the accumulator O
-    // in TMEM and the row sum are rescaled by 2^((m_old - m_new) * sl2).
-    float m = -INFINITY, lpart = 0.f;
-
-    for (int j = 0; j < nsub; j++) {
-      const int sb = j & 1;
-      const uint32_t tS = tm + (uint32_t)(sb * 64);
-      mbar_wait(&s_done[sb], (uint32_t)(j >> 1) & 1u, err);
-      tc_fence_after();
-      const int k0 = j * AB_SUB;
-      const bool diag = k0 + AB_SUB - 1 > q0;
-      uint32_t r[32];
-      tmem_ld32(tS + lanebase + half * 32, r);
-      tmem_ld_wait();
-      // pass 1: max over this half's 32 columns, exchanged with the partner warp
-      float mx = -INFINITY;
-      if (diag) {
-#pragma unroll
-        for (int jj = 0; jj < 32; jj++)
-          if (k0 + half * 32 + jj <= q) mx = fmaxf(mx, __uint_as_float(r[jj]));
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 32; jj++) mx = fmaxf(mx, __uint_as_float(r[jj]));
-      }
-      float* rd = red + sb * 256;
-      rd[half * 128 + row] = mx;
-      named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
-      const float mcand = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
-      const bool resc = (mcand - m) * sl2 > 8.f;  // always at j = 0 (m = -inf)
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2_hw((m - mcand) * sl2);
-        lpart *= alpha;
-        m = mcand;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // O holds PV(0 .. j-1) once PV(j-1) completes; PV(j) waits for this
-        // sub-block's p_ready, so the rescale cannot race an MMA
-        mbar_wait(&o_done[(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, err);
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = scale * LOG2E_F;  // scores -> log2 units
+    constexpr int OH = HS / 2;          // O columns of this warp
+    int g = 0;
+    for (int r = 0;; r++) {
+      const int idx = snake_item(r);
+      if (idx >= nitems) break;
+      const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
+      const int q = qb * 128 + row, nk = qb + 1;
+      // m: the row's reference maximum (raw score units); P and the row sum
+      // are relative to it; it moves only when a block's maximum exceeds it
+      // by more than 8 in log2 units, and then O and the sum are rescaled
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nk; j++, g++) {
+        mbar_wait(s_full, (uint32_t)g & 1u, err);
         tc_fence_after();
-        const uint32_t tO = tm + 128 + lanebase + half * 32;
-        uint32_t ro[32];
-        tmem_ld32(tO, ro);
+        uint32_t s[64];
+        tmem_ld32(tS + lb + half * 64, *reinterpret_cast<uint32_t(*)[32]>(s));
+        tmem_ld32(tS + lb + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
         tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        const int k0 = j * 128 + half * 64;  // key of column 0 of this warp
+        const bool diag = j == nk - 1;
+        float mx = -INFINITY;
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 32; i++) ro[i] = __float_as_uint(__uint_as_float(ro[i]) * alpha);
-        tmem_st16(tO, ro);
-        tmem_st16(tO + 16, ro + 16);
+          for (int c = 0; c < 64; c++)
+            if (k0 + c <= q) mx = fmaxf(mx, __uint_as_float(s[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c++) mx = fmaxf(mx, __uint_as_float(s[c]));
+        }
+        float* rd = red + (g & 1) * 256;
+        rd[half * 128 + row] = mx;
+        named_bar_sync(1 + quarter, 64);  // warps quarter and quarter + 4
+        const float mcand = fmaxf(m, fmaxf(rd[row], rd[128 + row]));
+        const bool resc = (mcand - m) * sl2 > 8.f;  // always at j = 0 (m = -inf)
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_hw((m - mcand) * sl2);
+          l *= alpha;
+          m = mcand;
+        }
+        const float mo = m * sl2;
+        float sum = 0.f;
+        uint32_t pk[32];
+        if (diag) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = k0 + c <= q ? ex2_hw(__uint_as_float(s[c]) * sl2 - mo) : 0.f;
+            const float p1 = k0 + c + 1 <= q ? ex2_hw(__uint_as_float(s[c + 1]) * sl2 - mo) : 0.f;
+            sum += p0 + p1;
+            pk[c >> 1] = pack_bf16(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; c += 2) {
+            const float p0 = ex2_hw(__uint_as_float(s[c]) * sl2 - mo);
+            const float p1 = ex2_hw(__uint_as_float(s[c + 1]) * sl2 - mo);
+            sum += p0 + p1;
+            pk[c >> 1] = pack_bf16(p0, p1);
+          }
+        }
+        if (j > 0) {
+          // P(g-1) V(g-1) done: the P columns are free and O is complete up
+          // to block g-1 (at j = 0 the previous item's epilogue waited)
+          mbar_wait(o_done, (uint32_t)(g - 1) & 1u, err);
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, resc)) {
+            uint32_t o[OH];
+            tmem_ld_cols<OH>(tO + lb + half * OH, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < OH; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_cols<OH>(tO + lb + half * OH, o);
+          }
+        }
+        l += sum;
+        tmem_st16(tP + lb + half * 32, pk);
+        tmem_st16(tP + lb + half * 32 + 16, pk + 16);
         tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      // P[sb] was read by PV(j-2)
-      if (j >= 2) mbar_wait(&o_done[sb], (uint32_t)((j - 2) >> 1) & 1u, err);
-      const float mo = m * sl2;
-      // pass 2: P = 2^(scale (s - m) log2 e) -> smem P[sb] (bf16), partial row sum
-      float sum = 0.f;
-      uint8_t* prow = sP + sb * AT_TILE + row * 128;
-      if (diag) {
-#pragma unroll
-        for (int g = 0; g < 4; g++) {
-          float p[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; jj++) {
-            const float e = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
-            p[jj] = k0 + half * 32 + g * 8 + jj <= q ? e : 0.f;
-            sum += p[jj];
-          }
-          st_row8(prow, row & 7, half * 4 + g, p);
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < 4; g++) {
-          float p[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; jj++) {
-            p[jj] = ex2_hw(__uint_as_float(r[g * 8 + jj]) * sl2 - mo);
-            sum += p[jj];
-          }
-          st_row8(prow, row & 7, half * 4 + g, p);
-        }
-      }
-      lpart += sum;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[sb]);
-    }
-    float o[32];
-    {  // O = PV(0 .. nsub-1), relative to the final reference maximum
-      const int pb = (nsub - 1) & 1;
-      mbar_wait(&o_done[pb], (uint32_t)((nsub - 1) >> 1) & 1u, err);
+      // epilogue: O = sum over blocks of P V, relative to the final maximum
+      mbar_wait(o_done, (uint32_t)(g - 1) & 1u, err);
       tc_fence_after();
-      uint32_t ro[32];
-      tmem_ld32(tm + 128 + lanebase + half * 32, ro);
+      uint32_t o[OH];
+      tmem_ld_cols<OH>(tO + lb + half * OH, o);
       tmem_ld_wait();
+      lred[half * 128 + row] = l;
+      named_bar_sync(1 + quarter, 64);
+      const float lt = lred[row] + lred[128 + row];
+      if (q < T) {
+        float v[OH];
 #pragma unroll
-      for (int i = 0; i < 32; i++) o[i] = __uint_as_float(ro[i]);
-    }
-    named_bar_sync(5, AT_THREADS);  // every softmax warp is past its last exchange
-    red[half * 128 + row] = lpart;
-    named_bar_sync(5, AT_THREADS);
-    const float l = red[row] + red[128 + row];
-    if (q < T) {
-      store_row32_bf16(y + ((int64_t)b * T + q) * C + h * AT_HS + half * 32, o, 1.f / l);
-      if (half == 0) lse[(int64_t)bh * T + q] = m * sl2 + log2f(l);  // base-2 units
+        for (int i = 0; i < OH; i++) v[i] = __uint_as_float(o[i]);
+        store_bf16_row<OH>(y + ((int64_t)b * T + q) * C + h * HS + half * OH, v, 1.f / lt);
+        if (half == 0) lse[(int64_t)bh * T + q] = m * sl2 + log2f(lt);  // base-2 units
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
+  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, Cf::TMEM); }
 }
 
 // ============================================================ backward: D
-// D[b,h,t] = sum_i dy[b,t,h*64+i] * y[b,t,h*64+i]
-__global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y, int B, int T,
-                                     int C, int NH) {
+// D[b,h,t] = sum_i dy[b,t,h*HS+i] * y[b,t,h*HS+i].  Thread i takes the
+// 16-byte chunk i of the [B*T, C] rows (coalesced), the HS/8 threads of one
+// head add their partial dots with shuffles, the first writes D.
+template <int HS>
+__global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y, int B, int T, int C,
+                                     int NH) {
   pdl_trigger();
   pdl_wait();
-  const int64_t n = (int64_t)B * T * NH;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int h = (int)(i % NH);
-    const int64_t bt = i / NH;
-    const int t = (int)(bt % T), b = (int)(bt / T);
-    const uint4* a = reinterpret_cast<const uint4*>(dy + bt * C + h * AT_HS);
-    const uint4* c = reinterpret_cast<const uint4*>(y + bt * C + h * AT_HS);
+  constexpr int G = HS / 8;  // threads per head
+  const int chunks = C / 8;
+  const int64_t n = (int64_t)B * T * chunks;
+  for (int64_t i0 = (int64_t)blockIdx.x * blockDim.x; i0 < n; i0 += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
     float s = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-      const uint4 ua = a[k], uc = c[k];
+    if (i < n) {
+      const uint4 ua = reinterpret_cast<const uint4*>(dy)[i];
+      const uint4 uc = reinterpret_cast<const uint4*>(y)[i];
       const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wc[4] = {uc.x, uc.y, uc.z, uc.w};
 #pragma unroll
       for (int j = 0; j < 4; j++) {
@@ -482,474 +421,582 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
         s += fa.x * fc.x + fa.y * fc.y;
       }
     }
-    dsum[((int64_t)b * NH + h) * T + t] = s;
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (i < n && (i % G) == 0) {
+      const int64_t bt = i / chunks;
+      const int h = (int)(i % chunks) / G;
+      const int t = (int)(bt % T), b = (int)(bt / T);
+      dsum[((int64_t)b * NH + h) * T + t] = s;
+    }
   }
 }
 
 // ============================================================ backward: dK, dV
-// One CTA per (128-key block, b*h), queries walked in 128-row sub-blocks,
-// warp-specialised:
-//   warp 9      loader: TMA of the q and dy tiles into a DKV_STAGES-deep
-//               ring, with each sub-block's lse and D (bulk copies on the
-//               same barrier when T is a multiple of 4; otherwise all of the
-//               block's lse / D are read once, before the first sub-block)
-//   warp 16     MMA issuer: S^T(j) = K q(j)^T and dP^T(j) = V dy(j)^T
-//               (N = 128) into TMEM, then dV += P^T(j-1) dy(j-1) and dK +=
-//               dS^T(j-1) q(j-1) (N = 64, K = 128 queries) with P^T and dS^T
-//               read from TMEM (the A operand), dy and q from shared memory
-//   warps 0..15 compute: copy S^T(j), dP^T(j) to registers at once (so
-//               S^T(j+1) runs during their elementwise work), then P^T =
-//               2^(S^T*scale*log2e - lse2), dS^T = P^T (dP^T - D) as
-//               packed bf16 into TMEM (warps w, w+4, w+8, w+12 share TMEM
-//               lane quarter w%4 and take 32 of the 128 query columns each;
-//               the math runs before the buffer wait, so it overlaps
-//               dV/dK(j-1))
-// Keeping P^T and dS^T out of shared memory saves their stores and the
-// MMAs' shared-memory operand reads (an M = 128, N = 64, K = 16 MMA takes
-// about 75 cycles whether A comes from tensor or shared memory).
-// A q / dy stage is refilled once dV, dK of its sub-block are done.
-// TMEM: S^T 0..127, dP^T 128..255, dV 256..319, dK 320..383, P^T 384..447,
-// dS^T 448..511 (bf16 pairs).
-// smem: K | V | DKV_STAGES x (q, dy) | barriers | lse / D
-// (per stage: [DKV_STAGES][lse 128, D 128]; whole block: lse[Tq], D[Tq] with
-// Tq = T - k0 rounded up to 128).  The grid's y index is the key block, so
-// the hardware starts the longest blocks (most queries) first.
-#define DKV_SUB 128
-#define DKV_STAGES 4
-#define DKV_CWARPS 16
-#define DKV_THREADS (DKV_CWARPS * 32 + 64)
-#define AKV_FIXED (1024 + 2 * AT_TILE + DKV_STAGES * 2 * AT_TILE + 256)
-static inline size_t akv_smem(int T) {
-  const size_t whole = 8 * (size_t)((T + DKV_SUB - 1) / DKV_SUB * DKV_SUB);
-  return AKV_FIXED + ((T % 4 == 0) ? (size_t)DKV_STAGES * 8 * DKV_SUB : whole);
-}
+// Item (128-key block kb, b*h): query sub-blocks of QS rows from k0 = 128 kb
+// to T.  Warps 0..15 elementwise (warps w, w+4, w+8, w+12 share TMEM lane
+// quarter w % 4 = 32 key rows and take QS/4 query columns each), warp 16
+// the MMA issuer, warp 17 the loader.
+//   S^T = k q^T, dP^T = v dy^T (M = 128 keys, N = QS queries, K = HS);
+//   P^T = 2^(S^T scale log2e - lse2), dS^T = P^T (dP^T - D), into TMEM;
+//   dV += P^T dy, dK += dS^T q (N = HS, K = QS queries; A from TMEM).
+// TMEM: S^T 0..QS-1, dP^T QS..2QS-1, P^T 2QS.., dS^T 2.5QS.., dV 3QS..,
+// dK 3QS+HS.. (at most 512 columns).
+// smem: K, V [KVB] | q, dy ring [ST] | lse / D per stage [ST][2][QS] |
+//       column-sum exchange | barriers.
+// lse and D of a sub-block arrive by bulk copy with its tiles when T is a
+// multiple of 4 (16-byte aligned rows); otherwise the elementwise warps read
+// them from global memory.
+#define KV_CW 16
+#define KV_THREADS (KV_CW * 32 + 64)
+template <int HS>
+struct KvCfg {
+  static constexpr int QS = HS > 64 ? 64 : 128;
+  static constexpr int CPT = QS / 4;  // query columns per elementwise thread
+  static constexpr uint32_t KTILE = Hs<HS>::NB * 16384u;                  // [128 x HS]
+  static constexpr uint32_t QTILE = Hs<HS>::NB * (uint32_t)QS * 128u;     // [QS x HS]
+  static constexpr int KVB = HS > 64 ? 1 : 2;
+  static constexpr int ST = 4;
+  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + 8 * HS * 4 + 256;
+};
 
-__global__ void __launch_bounds__(DKV_THREADS, 1)
-    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
+template <int HS>
+__global__ void __launch_bounds__(KV_THREADS, 1)
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                            const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
-                           const float* dsum, float* bias_partial, int T, int C, int NH, float scale,
+                           const float* dsum, float* bias_partial, int B, int T, int C, int NH, float scale,
                            int* err) {
-  pdl_trigger();
+  using Cf = KvCfg<HS>;
+  constexpr int QS = Cf::QS, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
+  constexpr uint32_t KTILE = Cf::KTILE, QTILE = Cf::QTILE;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  uint8_t* sK = sm;
-  uint8_t* sV = sm + AT_TILE;
-  uint8_t* sQ = sm + 2 * AT_TILE;                // [DKV_STAGES] x [128 x 64]
-  uint8_t* sD = sQ + DKV_STAGES * AT_TILE;       // dy, [DKV_STAGES]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sD + DKV_STAGES * AT_TILE);
-  uint64_t* kv_full = bars;
-  uint64_t* ld_full = bars + 1;                  // whole-block lse / D written
-  uint64_t* q_full = bars + 2;                   // [DKV_STAGES]: TMA bytes
-  uint64_t* q_empty = q_full + DKV_STAGES;       // [DKV_STAGES]: dV, dK of the stage done
-  uint64_t* s_full = q_empty + DKV_STAGES;       // S^T, dP^T in TMEM
-  uint64_t* s_empty = s_full + 1;                // 8 warps have copied them out
-  uint64_t* p_full = s_empty + 1;                // 8 warps have written P^T, dS^T
-  uint64_t* p_empty = p_full + 1;                // dV, dK MMAs have read them
-  uint64_t* done = p_empty + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
-  float* sLD = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 256);
-  const int kb = blockIdx.y;  // key block
-  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
-  const int k0 = kb * AT_BLK;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nsub = (T - k0 + DKV_SUB - 1) / DKV_SUB;  // 128-query sub-blocks from k0 to T
-  const bool staged = (T & 3) == 0;                   // per-stage lse / D bulk copies
+  uint8_t* sK = sm;                          // [KVB]
+  uint8_t* sV = sK + KVB * KTILE;            // [KVB]
+  uint8_t* sQ = sV + KVB * KTILE;            // [ST]
+  uint8_t* sD = sQ + ST * QTILE;             // dy [ST]
+  float* sLD = reinterpret_cast<float*>(sD + ST * QTILE);  // [ST][lse QS, D QS]
+  float* red = sLD + ST * 2 * QS;                          // [2][4][HS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 8 * HS);
+  uint64_t* kv_full = bars;              // [KVB]
+  uint64_t* kv_empty = kv_full + KVB;    // [KVB]: the item's last S^T, dP^T have read k, v
+  uint64_t* q_full = kv_empty + KVB;     // [ST]
+  uint64_t* q_empty = q_full + ST;       // [ST]: dV, dK of the sub-block done
+  uint64_t* s_full = q_empty + ST;       // S^T, dP^T in TMEM
+  uint64_t* s_free = s_full + 1;         // copied out by the 16 warps
+  uint64_t* p_full = s_free + 1;         // P^T, dS^T written by the 16 warps
+  uint64_t* p_empty = p_full + 1;        // dV, dK have read them
+  uint64_t* acc_full = p_empty + 1;      // the item's dV, dK complete
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
+  const int nkb = (T + 127) / 128, BH = B * NH, nitems = nkb * BH;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool staged = (T & 3) == 0;
   if (tid == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(ld_full, 1);
-    for (int s = 0; s < DKV_STAGES; s++) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
+    for (int i = 0; i < KVB; i++) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    for (int i = 0; i < ST; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, DKV_CWARPS);
-    mbar_init(p_full, DKV_CWARPS);
+    mbar_init(s_free, KV_CW);
+    mbar_init(p_full, KV_CW);
     mbar_init(p_empty, 1);
-    mbar_init(done, 1);
+    mbar_init(acc_full, 1);
     fence_mbar_init();
-    tma_prefetch_desc(&tm_qkv);
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kv);
     tma_prefetch_desc(&tm_dy);
   }
-  if (warp == DKV_CWARPS) { tmem_alloc(tslot, 512); tmem_relinquish(); }
+  if (warp == KV_CW) { tmem_alloc(tslot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  pdl_wait();  // from here on global memory written by the previous kernel is read
-  const uint32_t tSt = tm, tdPt = tm + 128, tdV = tm + 256, tdK = tm + 320, tPt = tm + 384, tdSt = tm + 448;
-  const float sl2 = scale * 1.4426950408889634f;
-  const float* lrow = lse + (int64_t)bh * T + k0;
-  const float* drow = dsum + (int64_t)bh * T + k0;
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
+  pdl_wait();
+  const uint32_t tSt = tm, tdPt = tm + QS, tPt = tm + 2 * QS, tdSt = tm + 2 * QS + QS / 2;
+  const uint32_t tdV = tm + 3 * QS, tdK = tm + 3 * QS + HS;
+  const float sl2 = scale * LOG2E_F;
 
-  if (warp == DKV_CWARPS + 1) {
+  if (warp == KV_CW + 1) {
     // ---------------------------------------------------------------- loader
-    auto issue = [&](int j) {
-      const int s = j % DKV_STAGES, q0 = k0 + j * DKV_SUB;
-      const uint32_t ldb = staged ? 4u * (uint32_t)min(DKV_SUB, T - q0) : 0u;  // a multiple of 16
-      mbar_arrive_expect_tx(&q_full[s], 2 * AT_TILE + 2 * ldb);
-      tma_load_3d(sQ + s * AT_TILE, &tm_qkv, &q_full[s], h * AT_HS, q0, b);
-      tma_load_3d(sD + s * AT_TILE, &tm_dy, &q_full[s], h * AT_HS, q0, b);
-      if (staged) {
-        bulk_load(sLD + s * 2 * DKV_SUB, lrow + j * DKV_SUB, ldb, &q_full[s]);
-        bulk_load(sLD + s * 2 * DKV_SUB + DKV_SUB, drow + j * DKV_SUB, ldb, &q_full[s]);
-      }
-    };
-    int j = 0;
     if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * AT_TILE);
-      tma_load_3d(sK, &tm_qkv, kv_full, C + h * AT_HS, k0, b);
-      tma_load_3d(sV, &tm_qkv, kv_full, 2 * C + h * AT_HS, k0, b);
-      for (; j < nsub && j < DKV_STAGES; j++) issue(j);
-    }
-    if (!staged) {
-      float* sL = sLD;
-      float* sDd = sLD + nsub * DKV_SUB;
-      const int nq = nsub * DKV_SUB;
-      for (int i0 = 0; i0 < nq; i0 += 32 * 16) {  // 32 loads in flight per lane
-        float lv[16], dv[16];
-#pragma unroll
-        for (int u = 0; u < 16; u++) {
-          const int i = i0 + u * 32 + lane;
-          const bool in = i < nq && k0 + i < T;
-          lv[u] = in ? __ldg(lrow + i) : 0.f;
-          dv[u] = in ? __ldg(drow + i) : 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < 16; u++) {
-          const int i = i0 + u * 32 + lane;
-          if (i < nq) { sL[i] = lv[u]; sDd[i] = dv[u]; }
+      int g = 0, it = 0;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int kb = idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH, k0 = kb * 128;
+        const int kvb = it % KVB;
+        if (it >= KVB) mbar_wait(&kv_empty[kvb], (uint32_t)(it / KVB - 1) & 1u, err);
+        mbar_arrive_expect_tx(&kv_full[kvb], 2 * KTILE);
+        load_tile<HS>(sK + kvb * KTILE, &tm_kv, &kv_full[kvb], C + h * HS, k0, b, 128);
+        load_tile<HS>(sV + kvb * KTILE, &tm_kv, &kv_full[kvb], 2 * C + h * HS, k0, b, 128);
+        const int nsub = (T - k0 + QS - 1) / QS;
+        for (int j = 0; j < nsub; j++, g++) {
+          const int s = g % ST, q0 = k0 + j * QS;
+          if (g >= ST) mbar_wait(&q_empty[s], (uint32_t)(g / ST - 1) & 1u, err);
+          const uint32_t ldb = staged ? 4u * (uint32_t)min(QS, T - q0) : 0u;  // a multiple of 16
+          mbar_arrive_expect_tx(&q_full[s], 2 * QTILE + 2 * ldb);
+          load_tile<HS>(sQ + s * QTILE, &tm_q, &q_full[s], h * HS, q0, b, QS);
+          load_tile<HS>(sD + s * QTILE, &tm_dy, &q_full[s], h * HS, q0, b, QS);
+          if (staged) {
+            bulk_load(sLD + s * 2 * QS, lse + (int64_t)bh * T + q0, ldb, &q_full[s]);
+            bulk_load(sLD + s * 2 * QS + QS, dsum + (int64_t)bh * T + q0, ldb, &q_full[s]);
+          }
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(ld_full);
-      for (j = DKV_STAGES; j < nsub; j++) {
-        mbar_wait(&q_empty[j % DKV_STAGES], ((uint32_t)(j / DKV_STAGES) & 1u) ^ 1u, err);
-        issue(j);
-      }
-    }
-  } else if (warp == DKV_CWARPS) {
+  } else if (warp == KV_CW) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
-      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
-      mbar_wait(kv_full, 0, err);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      for (int j = 0; j <= nsub; j++) {
-        if (j < nsub) {
-          const int s = j % DKV_STAGES;
-          mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);
-          if (j > 0) mbar_wait(s_empty, (uint32_t)(j - 1) & 1u, err);  // S^T(j-1), dP^T(j-1) copied out
+      const uint32_t idS = tc_idesc_bf16(128, QS, false, false);
+      const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
+      auto dvdk = [&](int gp, bool first, bool last) {
+        mbar_wait(p_full, (uint32_t)gp & 1u, err);
+        tc_fence_after();
+        const int s = gp % ST;
+        const uint32_t bQ = smem_u32(sQ + s * QTILE), bD = smem_u32(sD + s * QTILE);
+#pragma unroll
+        for (int kk = 0; kk < QS / 16; kk++)
+          tc_mma_bf16_ts(tdV, tPt + kk * 8, ndesc(bD, QS, kk), idO, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < QS / 16; kk++)
+          tc_mma_bf16_ts(tdK, tdSt + kk * 8, ndesc(bQ, QS, kk), idO, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(&q_empty[s]);
+        tc_commit(p_empty);
+        if (last) tc_commit(acc_full);
+      };
+      int g = 0, it = 0;
+      bool prev = false, prev_first = false, prev_last = false;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int k0 = (idx / BH) * 128;
+        const int nsub = (T - k0 + QS - 1) / QS;
+        const int kvb = it % KVB;
+        mbar_wait(&kv_full[kvb], (uint32_t)(it / KVB) & 1u, err);
+        const uint32_t aK = smem_u32(sK + kvb * KTILE), aV = smem_u32(sV + kvb * KTILE);
+        for (int j = 0; j < nsub; j++, g++) {
+          const int s = g % ST;
+          mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);
+          if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
           tc_fence_after();
-          const uint32_t bQ = smem_u32(sQ + s * AT_TILE), bD = smem_u32(sD + s * AT_TILE);
+          const uint32_t bQ = smem_u32(sQ + s * QTILE), bD = smem_u32(sD + s * QTILE);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tSt, kmaj(aK, kk), kmaj(bQ, kk), idS, kk > 0);
+          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tSt, kdesc(aK, 128, kk), kdesc(bQ, QS, kk), idS, kk > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdPt, kmaj(aV, kk), kmaj(bD, kk), idS, kk > 0);
+          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tdPt, kdesc(aV, 128, kk), kdesc(bD, QS, kk), idS, kk > 0 ? 1u : 0u);
+          if (j == nsub - 1) tc_commit(&kv_empty[kvb]);
           tc_commit(s_full);
-        }
-        if (j >= 1) {
-          const int jj = j - 1, s = jj % DKV_STAGES;
-          mbar_wait(p_full, (uint32_t)jj & 1u, err);
-          tc_fence_after();
-          const uint32_t bQ = smem_u32(sQ + s * AT_TILE), bD = smem_u32(sD + s * AT_TILE);
-#pragma unroll
-          for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdV, tPt + kk * 8, mnmaj(bD, kk), idO, (jj > 0 || kk > 0));
-#pragma unroll
-          for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdK, tdSt + kk * 8, mnmaj(bQ, kk), idO, (jj > 0 || kk > 0));
-          tc_commit(p_empty);
-          tc_commit(&q_empty[s]);
+          if (prev) dvdk(g - 1, prev_first, prev_last);
+          prev = true;
+          prev_first = j == 0;
+          prev_last = j == nsub - 1;
         }
       }
-      tc_commit(done);
+      if (prev) dvdk(g - 1, prev_first, prev_last);
     }
   } else {
-    // ---------------------------------------------------------------- compute warps
-    const int quarter = warp & 3, colq = warp >> 2;  // lane quarter, 32-column group
-    const int row = quarter * 32 + lane, key = k0 + row;
-    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
-    mbar_wait(ld_full, 0, err);
-    for (int j = 0; j < nsub; j++) {
-      const int s = j % DKV_STAGES;
-      const int q0 = k0 + j * DKV_SUB;
-      mbar_wait(s_full, (uint32_t)j & 1u, err);
-      tc_fence_after();
-      uint32_t rs[32], rd[32];
-      tmem_ld32(tSt + lanebase + colq * 32, rs);
-      tmem_ld32(tdPt + lanebase + colq * 32, rd);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      if (staged) mbar_wait(&q_full[s], (uint32_t)(j / DKV_STAGES) & 1u, err);  // the stage's lse / D
-      const float* lc = (staged ? sLD + s * 2 * DKV_SUB : sLD + j * DKV_SUB) + colq * 32;
-      const float* dc = (staged ? sLD + s * 2 * DKV_SUB + DKV_SUB : sLD + (nsub + j) * DKV_SUB) + colq * 32;
-      const int c0 = q0 + colq * 32;
-      // the math runs while dV, dK(j-1) still read the shared-memory buffers
-      uint32_t pk[16], dk[16];
-      if (q0 < k0 + AT_BLK || q0 + DKV_SUB > T) keyrow_pack<true>(rs, rd, lc, dc, sl2, c0, key, T, pk, dk);
-      else keyrow_pack<false>(rs, rd, lc, dc, sl2, c0, key, T, pk, dk);
-      if (j > 0) mbar_wait(p_empty, (uint32_t)(j - 1) & 1u, err);  // dV, dK(j-1) have read P^T, dS^T
-      tc_fence_after();
-      tmem_st16(tPt + lanebase + colq * 16, pk);
-      tmem_st16(tdSt + lanebase + colq * 16, dk);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    mbar_wait(done, 0, err);
-    tc_fence_after();
-    // epilogue: column groups 0, 1 take dV columns 0..31, 32..63; 2, 3 take dK
-    const int64_t C3 = 3 * (int64_t)C;
-    const int which = colq >> 1, cc = (colq & 1) * 32;  // which: 0 dV, 1 dK
-    const float mul = which ? scale : 1.f;
-    float* red = reinterpret_cast<float*>(sQ);  // [2][4][64]: the q ring is free once every MMA is done
-    float v[32];
-    uint32_t r[32];
-    tmem_ld32((which ? tdK : tdV) + lanebase + cc, r);
-    tmem_ld_wait();
+    // ---------------------------------------------------------------- elementwise warps
+    const int quarter = warp & 3, cg = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+    int g = 0, it = 0;
+    for (int r = 0;; r++, it++) {
+      const int idx = snake_item(r);
+      if (idx >= nitems) break;
+      const int kb = idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH, k0 = kb * 128;
+      const int key = k0 + row;
+      const int nsub = (T - k0 + QS - 1) / QS;
+      for (int j = 0; j < nsub; j++, g++) {
+        const int s = g % ST, q0 = k0 + j * QS;
+        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        tc_fence_after();
+        uint32_t rs[CPT], rd[CPT];
+        tmem_ld_cols<CPT>(tSt + lb + cg * CPT, rs);
+        tmem_ld_cols<CPT>(tdPt + lb + cg * CPT, rd);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        const int c0 = q0 + cg * CPT;  // query of column 0 of this warp
+        if (staged) mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
+        const float* lc = sLD + s * 2 * QS + cg * CPT;
+        uint32_t pk[CPT / 2], dk[CPT / 2];
+        const bool mask = q0 < k0 + 128 || q0 + QS > T;
 #pragma unroll
-    for (int i = 0; i < 32; i++) v[i] = key < T ? __uint_as_float(r[i]) : 0.f;
-    if (key < T)
-      store_row32_bf16(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * AT_HS + cc, v, mul);
-    red[which * 256 + quarter * 64 + cc + lane] = warp_colsum32(v) * mul;
-    // the block's column sums of dV and dK: one partial row of the qkv bias
-    // gradient per (batch row, key block)
-    named_bar_sync(1, DKV_CWARPS * 32);
-    if (tid < 128) {
-      const int wh = tid >> 6, col = tid & 63;  // 0: dV, 1: dK
-      const float* rr = red + wh * 256 + col;
-      const float sum = (rr[0] + rr[64]) + (rr[128] + rr[192]);
-      bias_partial[((int64_t)b * gridDim.y + kb) * C3 + (wh ? C : 2 * C) + h * AT_HS + col] = sum;
+        for (int i = 0; i < CPT; i += 4) {
+          float lv[4], dv[4];
+          if (staged) {
+            const float4 a = *reinterpret_cast<const float4*>(lc + i);
+            const float4 d = *reinterpret_cast<const float4*>(lc + QS + i);
+            lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
+            dv[0] = d.x; dv[1] = d.y; dv[2] = d.z; dv[3] = d.w;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; u++) {
+              const int qq = min(c0 + i + u, T - 1);
+              lv[u] = __ldg(lse + (int64_t)bh * T + qq);
+              dv[u] = __ldg(dsum + (int64_t)bh * T + qq);
+            }
+          }
+          float p[4], d[4];
+#pragma unroll
+          for (int u = 0; u < 4; u++) {
+            p[u] = ex2_hw(__uint_as_float(rs[i + u]) * sl2 - lv[u]);
+            d[u] = p[u] * (__uint_as_float(rd[i + u]) - dv[u]);
+            if (mask) {  // a masked column may hold a stale lse / D: select, do not scale
+              const bool ok = c0 + i + u >= key && c0 + i + u < T;
+              p[u] = ok ? p[u] : 0.f;
+              d[u] = ok ? d[u] : 0.f;
+            }
+          }
+          pk[i >> 1] = pack_bf16(p[0], p[1]);
+          pk[(i >> 1) + 1] = pack_bf16(p[2], p[3]);
+          dk[i >> 1] = pack_bf16(d[0], d[1]);
+          dk[(i >> 1) + 1] = pack_bf16(d[2], d[3]);
+        }
+        if (g > 0) {
+          mbar_wait(p_empty, (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read P^T, dS^T
+          tc_fence_after();
+        }
+        tmem_st_cols<CPT / 2>(tPt + lb + cg * (CPT / 2), pk);
+        tmem_st_cols<CPT / 2>(tdSt + lb + cg * (CPT / 2), dk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // epilogue: warps cg 0, 1 take dV columns 0..HS/2-1, HS/2..; 2, 3 take dK
+      mbar_wait(acc_full, (uint32_t)it & 1u, err);
+      tc_fence_after();
+      constexpr int EH = HS / 2;
+      const int which = cg >> 1, ch = cg & 1;  // which: 0 dV, 1 dK
+      const float mul = which ? scale : 1.f;
+      constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
+      const int64_t C3 = 3 * (int64_t)C;
+#pragma unroll
+      for (int e = 0; e < EH; e += EC) {
+        uint32_t ra[EC];
+        tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, ra);
+        tmem_ld_wait();
+        float v[EC];
+#pragma unroll
+        for (int i = 0; i < EC; i++) v[i] = key < T ? __uint_as_float(ra[i]) * mul : 0.f;
+        if (key < T)
+          store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, 1.f);
+        // the block's column sums of dV and dK: one partial row of the qkv
+        // bias gradient per (batch row, key block)
+        warp_sum_cols<EC>(v);
+        if (lane == 0) {
+#pragma unroll
+          for (int i = 0; i < EC; i++) red[(which * 4 + quarter) * HS + ch * EH + e + i] = v[i];
+        }
+      }
+      named_bar_sync(1, KV_CW * 32);
+      if (tid < 2 * HS) {
+        const int wh = tid / HS, col = tid % HS;
+        const float* rr = red + wh * 4 * HS + col;
+        const float sum = (rr[0] + rr[HS]) + (rr[2 * HS] + rr[3 * HS]);
+        bias_partial[((int64_t)b * nkb + kb) * C3 + (wh ? C : 2 * C) + h * HS + col] = sum;
+      }
+      named_bar_sync(1, KV_CW * 32);  // red is reused by the next item
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == DKV_CWARPS) { tc_fence_after(); tmem_dealloc(tm, 512); }
+  if (warp == KV_CW) { tc_fence_after(); tmem_dealloc(tm, 512); }
 }
 
 // ============================================================ backward: dQ
-// One CTA per (128-query block, b*h), keys walked in 64-row sub-blocks; two
-// CTAs share an SM.  Warps 0..7 compute, warp 8 (one thread) issues every
-// TMA load and MMA:
-//   S(j) = q k(j)^T and dP(j) = dO v(j)^T into TMEM (one buffer: the
-//          compute warps copy it to registers first thing, so S(j+1) runs
-//          during the elementwise work of sub-block j);
-//   dQ += dS(j) k(j) once dS(j) is in shared memory (two dS buffers).
-// k streams through a three-stage ring (a stage is read by S(j) and by
-// dQ(j)), v through a two-stage one.
-// TMEM: S 0..63, dP 64..127, dQ 128..191 (256 columns).
-// smem: Q | dO | K ring | V ring (64-row tiles) | dS [2] ([128 x 64]) | barriers
-#define AQ_K_STAGES 3
-#define AQ_V_STAGES 2
-#define AQ_THREADS (AT_THREADS + 32)
-#define AQ_SMEM (1024 + 2 * AT_TILE + (AQ_K_STAGES + AQ_V_STAGES) * AT_SUBTILE + 2 * AT_TILE + 256)
+// Item (128-query block, b*h), 128-key blocks.  Warps 0..15 elementwise
+// (warps w, w+4, w+8, w+12 share lane quarter w % 4 = 32 query rows and
+// take 32 key columns each), warp 16 the MMA issuer, warp 17 the loader.
+//   S = q k^T, dP = dy v^T (M = 128 queries, N = 128 keys, K = HS);
+//   dS = P (dP - D) into TMEM; dQ += dS k (N = HS, K = 128 keys).
+// TMEM: S 0..127, dP 128..255, dS 256..319, dQ 320..320+HS-1.
+// smem: q, dy [QB] | K ring [KST] | V ring [2] | column-sum exchange | barriers.
+#define DQ_CW 16
+#define DQ_THREADS (DQ_CW * 32 + 64)
+template <int HS>
+struct DqCfg {
+  static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;
+  static constexpr int QB = HS > 64 ? 1 : 2;
+  static constexpr int KST = HS > 64 ? 2 : 3;
+  static constexpr int VST = 2;
+  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + 4 * HS * 4 + 256;
+};
 
-__global__ void __launch_bounds__(AQ_THREADS, 2)
-    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv,
-                          const __grid_constant__ CUtensorMap tm_dy,
-                          const __grid_constant__ CUtensorMap tm_qkv64, bf16* dqkv, const float* lse,
-                          const float* dsum, float* bias_partial, int T, int C, int NH, float scale,
-                          int* err) {
-  pdl_trigger();
+template <int HS>
+__global__ void __launch_bounds__(DQ_THREADS, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
+                          bf16* dqkv, const float* lse, const float* dsum, float* bias_partial, int B, int T,
+                          int C, int NH, float scale, int* err) {
+  using Cf = DqCfg<HS>;
+  constexpr int QB = Cf::QB, KST = Cf::KST, VST = Cf::VST;
+  constexpr uint32_t TILE = Cf::TILE;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
-  uint8_t* sQ = sm;
-  uint8_t* sD = sm + AT_TILE;
-  uint8_t* sK = sm + 2 * AT_TILE;              // [AQ_K_STAGES] x [64 x 64]
-  uint8_t* sV = sK + AQ_K_STAGES * AT_SUBTILE; // [AQ_V_STAGES]
-  uint8_t* sS = sV + AQ_V_STAGES * AT_SUBTILE; // dS [2] x [128 queries x 64 keys]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sS + 2 * AT_TILE);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;                 // [AQ_K_STAGES]
-  uint64_t* k_empty = k_full + AQ_K_STAGES;    // [AQ_K_STAGES]: dQ(j) has read k(j)
-  uint64_t* v_full = k_empty + AQ_K_STAGES;    // [AQ_V_STAGES]
-  uint64_t* s_full = v_full + AQ_V_STAGES;     // S(j), dP(j) in TMEM
-  uint64_t* s_empty = s_full + 1;              // 8 warps have copied them out
-  uint64_t* p_full = s_empty + 1;              // [2]: 8 warps have written dS(j)
-  uint64_t* p_empty = p_full + 2;              // [2]: dQ(j) has read dS(j)
-  uint64_t* dq_done = p_empty + 2;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(dq_done + 1);
+  uint8_t* sQ = sm;                     // [QB] x (q, dy)
+  uint8_t* sK = sQ + QB * 2 * TILE;     // [KST]
+  uint8_t* sV = sK + KST * TILE;        // [VST]
+  float* red = reinterpret_cast<float*>(sV + VST * TILE);  // [4][HS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * HS);
+  uint64_t* qd_full = bars;             // [QB]
+  uint64_t* qd_empty = qd_full + QB;    // [QB]: the item's last S, dP have read q, dy
+  uint64_t* k_full = qd_empty + QB;     // [KST]
+  uint64_t* k_empty = k_full + KST;     // [KST]: dQ of the block has read k
+  uint64_t* v_full = k_empty + KST;     // [VST]
+  uint64_t* v_empty = v_full + VST;     // [VST]
+  uint64_t* s_full = v_empty + VST;
+  uint64_t* s_free = s_full + 1;
+  uint64_t* p_full = s_free + 1;
+  uint64_t* ds_free = p_full + 1;       // dQ of the block has read dS
+  uint64_t* dq_full = ds_free + 1;      // the item's dQ complete
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(dq_full + 1);
 
-  const int nqb = gridDim.y;
-  const int qb = nqb - 1 - blockIdx.y;  // the grid starts with the blocks that meet the most keys
-  const int bh = blockIdx.x, b = bh / NH, h = bh % NH;
-  const int q0 = qb * AT_BLK;
+  const int nqb = (T + 127) / 128, BH = B * NH, nitems = nqb * BH;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nsub = (min(q0 + AT_BLK, T) + AB_SUB - 1) / AB_SUB;  // key sub-blocks up to the last query
-
   if (tid == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < AQ_K_STAGES; s++) { mbar_init(&k_full[s], 1); mbar_init(&k_empty[s], 1); }
-    for (int s = 0; s < AQ_V_STAGES; s++) mbar_init(&v_full[s], 1);
+    for (int i = 0; i < QB; i++) { mbar_init(&qd_full[i], 1); mbar_init(&qd_empty[i], 1); }
+    for (int i = 0; i < KST; i++) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
+    for (int i = 0; i < VST; i++) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
     mbar_init(s_full, 1);
-    mbar_init(s_empty, AT_THREADS / 32);
-    for (int i = 0; i < 2; i++) { mbar_init(&p_full[i], AT_THREADS / 32); mbar_init(&p_empty[i], 1); }
-    mbar_init(dq_done, 1);
+    mbar_init(s_free, DQ_CW);
+    mbar_init(p_full, DQ_CW);
+    mbar_init(ds_free, 1);
+    mbar_init(dq_full, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
     tma_prefetch_desc(&tm_dy);
-    tma_prefetch_desc(&tm_qkv64);
   }
-  if (warp == 0) { tmem_alloc(tslot, 256); tmem_relinquish(); }
+  if (warp == DQ_CW) { tmem_alloc(tslot, 512); tmem_relinquish(); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
-  pdl_wait();  // from here on global memory written by the previous kernel is read
-  const uint32_t tS = tm, tdP = tm + 64, tdQ = tm + 128;
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
+  pdl_wait();
+  const uint32_t tS = tm, tdP = tm + 128, tdS = tm + 256, tdQ = tm + 320;
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ TMA + MMA issuer
+  if (warp == DQ_CW + 1) {
+    // ---------------------------------------------------------------- loader
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
-      const uint32_t idO = tc_idesc_bf16(128, 64, false, true);
-      auto load_k = [&](int j) {
-        const int s = j % AQ_K_STAGES;
-        mbar_arrive_expect_tx(&k_full[s], AT_SUBTILE);
-        tma_load_3d(sK + s * AT_SUBTILE, &tm_qkv64, &k_full[s], C + h * AT_HS, j * AB_SUB, b);
-      };
-      auto load_v = [&](int j) {
-        const int s = j % AQ_V_STAGES;
-        mbar_arrive_expect_tx(&v_full[s], AT_SUBTILE);
-        tma_load_3d(sV + s * AT_SUBTILE, &tm_qkv64, &v_full[s], 2 * C + h * AT_HS, j * AB_SUB, b);
-      };
-      auto issue_sdp = [&](int j) {  // S(j), dP(j)
-        const int ks = j % AQ_K_STAGES, vs = j % AQ_V_STAGES;
-        mbar_wait(&k_full[ks], (uint32_t)(j / AQ_K_STAGES) & 1u, err);
-        mbar_wait(&v_full[vs], (uint32_t)(j / AQ_V_STAGES) & 1u, err);
-        tc_fence_after();
-        const uint32_t aQ = smem_u32(sQ), aD = smem_u32(sD);
-        const uint32_t bK = smem_u32(sK + ks * AT_SUBTILE), bV = smem_u32(sV + vs * AT_SUBTILE);
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tS, kmaj(aQ, kk), kmaj(bK, kk), idS, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdP, kmaj(aD, kk), kmaj(bV, kk), idS, kk > 0);
-        tc_commit(s_full);
-      };
-      mbar_arrive_expect_tx(q_full, 2 * AT_TILE);
-      tma_load_3d(sQ, &tm_qkv, q_full, h * AT_HS, q0, b);
-      tma_load_3d(sD, &tm_dy, q_full, h * AT_HS, q0, b);
-      for (int j = 0; j < AQ_K_STAGES && j < nsub; j++) load_k(j);
-      for (int j = 0; j < AQ_V_STAGES && j < nsub; j++) load_v(j);
-      mbar_wait(q_full, 0, err);
-      issue_sdp(0);
-      for (int j = 0; j < nsub; j++) {
-        if (j + 1 < nsub) {
-          mbar_wait(s_empty, (uint32_t)j & 1u, err);  // S(j), dP(j) copied out (so dP(j) is done)
-          if (j + AQ_V_STAGES < nsub) load_v(j + AQ_V_STAGES);
-          issue_sdp(j + 1);
-        }
-        mbar_wait(&p_full[j & 1], (uint32_t)(j >> 1) & 1u, err);  // dS(j) written
-        tc_fence_after();
-        {
-          const int ks = j % AQ_K_STAGES;
-          const uint32_t aS = smem_u32(sS + (j & 1) * AT_TILE), bK = smem_u32(sK + ks * AT_SUBTILE);
-#pragma unroll
-          for (int kk = 0; kk < 4; kk++) tc_mma_bf16(tdQ, kmaj(aS, kk), mnmaj(bK, kk), idO, (j > 0 || kk > 0));
-          tc_commit(&p_empty[j & 1]);
-          tc_commit(&k_empty[ks]);
-        }
-        if (j >= 1 && j + 2 < nsub) {  // dQ(j-1) has read k(j-1): its stage takes k(j+2)
-          mbar_wait(&k_empty[(j - 1) % AQ_K_STAGES], (uint32_t)((j - 1) / AQ_K_STAGES) & 1u, err);
-          load_k(j + 2);
+      int g = 0, it = 0;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
+        const int ib = it % QB;
+        if (it >= QB) mbar_wait(&qd_empty[ib], (uint32_t)(it / QB - 1) & 1u, err);
+        mbar_arrive_expect_tx(&qd_full[ib], 2 * TILE);
+        load_tile<HS>(sQ + ib * 2 * TILE, &tm_qkv, &qd_full[ib], h * HS, qb * 128, b, 128);
+        load_tile<HS>(sQ + ib * 2 * TILE + TILE, &tm_dy, &qd_full[ib], h * HS, qb * 128, b, 128);
+        for (int j = 0; j <= qb; j++, g++) {
+          const int ks = g % KST, vs = g % VST;
+          if (g >= KST) mbar_wait(&k_empty[ks], (uint32_t)(g / KST - 1) & 1u, err);
+          mbar_arrive_expect_tx(&k_full[ks], TILE);
+          load_tile<HS>(sK + ks * TILE, &tm_qkv, &k_full[ks], C + h * HS, j * 128, b, 128);
+          if (g >= VST) mbar_wait(&v_empty[vs], (uint32_t)(g / VST - 1) & 1u, err);
+          mbar_arrive_expect_tx(&v_full[vs], TILE);
+          load_tile<HS>(sV + vs * TILE, &tm_qkv, &v_full[vs], 2 * C + h * HS, j * 128, b, 128);
         }
       }
-      tc_commit(dq_done);
+    }
+  } else if (warp == DQ_CW) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+      const uint32_t idQ = tc_idesc_bf16(128, HS, false, true);
+      auto dq = [&](int gp, bool first, bool last) {  // dQ (+)= dS(gp) k(gp)
+        mbar_wait(p_full, (uint32_t)gp & 1u, err);
+        tc_fence_after();
+        const uint32_t bK = smem_u32(sK + (gp % KST) * TILE);
+#pragma unroll
+        for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdQ, tdS + kk * 8, ndesc(bK, 128, kk), idQ, (!first || kk > 0) ? 1u : 0u);
+        tc_commit(&k_empty[gp % KST]);
+        tc_commit(ds_free);
+        if (last) tc_commit(dq_full);
+      };
+      int g = 0, it = 0;
+      bool prev = false, prev_first = false, prev_last = false;
+      for (int r = 0;; r++, it++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int nk = nqb - idx / BH;
+        const int ib = it % QB;
+        mbar_wait(&qd_full[ib], (uint32_t)(it / QB) & 1u, err);
+        const uint32_t aQ = smem_u32(sQ + ib * 2 * TILE), aD = aQ + TILE;
+        for (int j = 0; j < nk; j++, g++) {
+          const int ks = g % KST, vs = g % VST;
+          mbar_wait(&k_full[ks], (uint32_t)(g / KST) & 1u, err);
+          mbar_wait(&v_full[vs], (uint32_t)(g / VST) & 1u, err);
+          if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
+          tc_fence_after();
+          const uint32_t bK = smem_u32(sK + ks * TILE), bV = smem_u32(sV + vs * TILE);
+#pragma unroll
+          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tS, kdesc(aQ, 128, kk), kdesc(bK, 128, kk), idS, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tdP, kdesc(aD, 128, kk), kdesc(bV, 128, kk), idS, kk > 0 ? 1u : 0u);
+          tc_commit(&v_empty[vs]);
+          if (j == nk - 1) tc_commit(&qd_empty[ib]);
+          tc_commit(s_full);
+          if (prev) dq(g - 1, prev_first, prev_last);
+          prev = true;
+          prev_first = j == 0;
+          prev_last = j == nk - 1;
+        }
+      }
+      if (prev) dq(g - 1, prev_first, prev_last);
     }
   } else {
-    // ------------------------------------------------------------ compute warps
-    const int quarter = warp & 3, half = warp >> 2;
-    const int row = quarter * 32 + lane, q = q0 + row;
-    const uint32_t lanebase = (uint32_t)(quarter * 32) << 16;
-    const float sl2 = scale * 1.4426950408889634f;
-    const float my_lse = q < T ? lse[(int64_t)bh * T + q] : INFINITY;  // base 2
-    const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
-    for (int j = 0; j < nsub; j++) {
-      const int k0 = j * AB_SUB;
-      mbar_wait(s_full, (uint32_t)j & 1u, err);
-      tc_fence_after();
-      uint32_t rs[32], rd[32];
-      tmem_ld32(tS + lanebase + half * 32, rs);
-      tmem_ld32(tdP + lanebase + half * 32, rd);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      mbar_wait(&p_empty[j & 1], ((uint32_t)(j >> 1) & 1u) ^ 1u, err);  // dQ(j-2) has read the buffer
-      uint8_t* srow = sS + (j & 1) * AT_TILE + row * 128;
-      if (k0 + AB_SUB > q0)
-        qrow_elementwise<true>(rs, rd, my_lse, my_d, sl2, k0 + half * 32, q, srow, row & 7, half * 4);
-      else
-        qrow_elementwise<false>(rs, rd, my_lse, my_d, sl2, k0 + half * 32, q, srow, row & 7, half * 4);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
-    }
-    mbar_wait(dq_done, 0, err);
-    tc_fence_after();
-    float v[32];
-    {
-      uint32_t r[32];
-      tmem_ld32(tdQ + lanebase + half * 32, r);
-      tmem_ld_wait();
+    // ---------------------------------------------------------------- elementwise warps
+    const int quarter = warp & 3, cg = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+    const float sl2 = scale * LOG2E_F;
+    int g = 0, it = 0;
+    for (int r = 0;; r++, it++) {
+      const int idx = snake_item(r);
+      if (idx >= nitems) break;
+      const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
+      const int q = qb * 128 + row, nk = qb + 1;
+      const float my_lse = q < T ? lse[(int64_t)bh * T + q] : INFINITY;  // base 2
+      const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+      for (int j = 0; j < nk; j++, g++) {
+        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        tc_fence_after();
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tS + lb + cg * 32, rs);
+        tmem_ld32(tdP + lb + cg * 32, rd);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        const int c0 = j * 128 + cg * 32;  // key of column 0 of this warp
+        const bool diag = j == nk - 1;
+        uint32_t dk[16];
 #pragma unroll
-      for (int i = 0; i < 32; i++) v[i] = q < T ? __uint_as_float(r[i]) : 0.f;
-    }
-    if (q < T) store_row32_bf16(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * AT_HS + half * 32, v, scale);
-    // the block's column sums of dQ: one partial row of the qkv bias gradient
-    // per (batch row, query block); the dS buffers are free once dQ is done
-    float* red = reinterpret_cast<float*>(sS);  // [4][64]
-    red[quarter * 64 + half * 32 + lane] = warp_colsum32(v) * scale;
-    named_bar_sync(1, AT_THREADS);
-    if (tid < 64) {
-      const float* rr = red + tid;
-      bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * AT_HS + tid] = (rr[0] + rr[64]) + (rr[128] + rr[192]);
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2_hw(__uint_as_float(rs[i]) * sl2 - my_lse);
+          const float p1 = ex2_hw(__uint_as_float(rs[i + 1]) * sl2 - my_lse);
+          float d0 = p0 * (__uint_as_float(rd[i]) - my_d);
+          float d1 = p1 * (__uint_as_float(rd[i + 1]) - my_d);
+          if (diag) {
+            d0 = c0 + i <= q ? d0 : 0.f;
+            d1 = c0 + i + 1 <= q ? d1 : 0.f;
+          }
+          dk[i >> 1] = pack_bf16(d0, d1);
+        }
+        if (g > 0) {
+          mbar_wait(ds_free, (uint32_t)(g - 1) & 1u, err);  // dQ(g-1) has read dS
+          tc_fence_after();
+        }
+        tmem_st16(tdS + lb + cg * 16, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+      }
+      // epilogue: warp cg takes dQ columns cg*HS/4 .. cg*HS/4 + HS/4 - 1
+      mbar_wait(dq_full, (uint32_t)it & 1u, err);
+      tc_fence_after();
+      constexpr int EQ = HS / 4;
+      uint32_t ra[EQ];
+      tmem_ld_cols<EQ>(tdQ + lb + cg * EQ, ra);
+      tmem_ld_wait();
+      float v[EQ];
+#pragma unroll
+      for (int i = 0; i < EQ; i++) v[i] = q < T ? __uint_as_float(ra[i]) * scale : 0.f;
+      if constexpr (EQ >= 8) {
+        if (q < T) store_bf16_row<EQ>(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * HS + cg * EQ, v, 1.f);
+      } else {
+        if (q < T) {  // 4 columns: one 8-byte store
+          uint2 u;
+          u.x = pack_bf16(v[0], v[1]);
+          u.y = pack_bf16(v[2], v[3]);
+          *reinterpret_cast<uint2*>(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * HS + cg * EQ) = u;
+        }
+      }
+      // the block's column sums of dQ: one partial row of the qkv bias
+      // gradient per (batch row, query block)
+      warp_sum_cols<EQ>(v);
+      if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < EQ; i++) red[quarter * HS + cg * EQ + i] = v[i];
+      }
+      named_bar_sync(1, DQ_CW * 32);
+      if (tid < HS) {
+        const float* rr = red + tid;
+        bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * HS + tid] = (rr[0] + rr[HS]) + (rr[2 * HS] + rr[3 * HS]);
+      }
+      named_bar_sync(1, DQ_CW * 32);  // red is reused by the next item
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, 256); }
+  if (warp == DQ_CW) { tc_fence_after(); tmem_dealloc(tm, 512); }
 }
 
 // ============================================================ launchers
-void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T,
-                               int C, int NH) {
-  if (C / NH != AT_HS) {
-    launch_attention_fwd_simt<bf16>(c, y, lse, qkv, B, T, C, NH);
-    return;
-  }
-  CUtensorMap tq, tq64;
-  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB)) {
+template <int HS>
+static void fwd_hs(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T, int C, int NH) {
+  using Cf = FwdCfg<HS>;
+  CUtensorMap tq;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C, 128)) {
     c.host_fail = 1;
     return;
   }
-  dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
-  cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AF_SMEM);
-  launch_pdl(c, attn_fwd_tc_kernel, dim3(grid), dim3(AF_THREADS), AF_SMEM, tq, tq64, y, lse, T, C, NH, 1.f / sqrtf((float)AT_HS), c.err);
+  const int nitems = ((T + 127) / 128) * B * NH;
+  const int grid = std::min(nitems, Cf::PER_SM * c.num_sms);
+  cudaFuncSetAttribute(attn_fwd_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
+  launch_pdl(c, attn_fwd_tc_kernel<HS>, dim3(grid), dim3(FW_THREADS), Cf::SMEM, tq, y, lse, B, T, C, NH,
+             1.f / sqrtf((float)HS), c.err);
+}
+
+void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T,
+                               int C, int NH) {
+  switch (C / NH) {  // head sizes 16, 32, 64, 128 (checked at build)
+    case 16: fwd_hs<16>(c, y, lse, qkv, B, T, C, NH); break;
+    case 32: fwd_hs<32>(c, y, lse, qkv, B, T, C, NH); break;
+    case 64: fwd_hs<64>(c, y, lse, qkv, B, T, C, NH); break;
+    case 128: fwd_hs<128>(c, y, lse, qkv, B, T, C, NH); break;
+    default: c.host_fail = 1;
+  }
+}
+
+template <int HS>
+static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, const bf16* qkv, const float* lse,
+                   float* dsum, int B, int T, int C, int NH, float* bias_partial) {
+  using Kv = KvCfg<HS>;
+  using Dq = DqCfg<HS>;
+  CUtensorMap tq, tq_s, td, td_s;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C, 128) || !make_tmap_btw(&td, dy, B, T, C, 128) ||
+      !make_tmap_btw(&tq_s, qkv, B, T, 3 * C, Kv::QS) || !make_tmap_btw(&td_s, dy, B, T, C, Kv::QS)) {
+    c.host_fail = 1;
+    return;
+  }
+  const int64_t chunks = (int64_t)B * T * (C / 8);
+  launch_pdl(c, attn_bwd_dsum_kernel<HS>, dim3((int)std::min<int64_t>((chunks + 255) / 256, (int64_t)c.num_sms * 8)),
+             dim3(256), 0, dsum, dy, y, B, T, C, NH);
+  const float scale = 1.f / sqrtf((float)HS);
+  const int nitems = ((T + 127) / 128) * B * NH;
+  const int grid = std::min(nitems, c.num_sms);
+  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
+  launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, dqkv, lse,
+             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
+  cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Dq::SMEM);
+  launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, dqkv, lse,
+             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
 }
 
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T,
                                int C, int NH, float* bias_partial) {
-  if (C / NH != AT_HS) {
-    launch_attention_bwd_simt<bf16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, nullptr);
-    return false;
+  switch (C / NH) {
+    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
+    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
+    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
+    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
+    default: c.host_fail = 1; return false;
   }
-  CUtensorMap tq, td, tq64;
-  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C) || !make_tmap_btw(&td, dy, B, T, C) ||
-      !make_tmap_btw(&tq64, qkv, B, T, 3 * C, AB_SUB)) {
-    c.host_fail = 1;
-    return false;
-  }
-  const int64_t n = (int64_t)B * T * NH;
-  launch_pdl(c, attn_bwd_dsum_kernel, dim3((int)std::min<int64_t>((n + 255) / 256, (int64_t)c.num_sms * 16)), dim3(256), 0, dsum, dy, y, B, T, C, NH);
-  const float scale = 1.f / sqrtf((float)AT_HS);
-  dim3 grid(B * NH, (T + AT_BLK - 1) / AT_BLK);
-  const size_t kv_smem = akv_smem(T);
-  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kv_smem);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel, dim3(grid), dim3(DKV_THREADS), kv_smem, tq, td, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
-  cudaFuncSetAttribute(attn_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AQ_SMEM);
-  launch_pdl(c, attn_bwd_dq_tc_kernel, dim3(grid), dim3(AQ_THREADS), AQ_SMEM, tq, td, tq64, dqkv, lse, dsum, bias_partial, T, C, NH, scale, c.err);
   return true;
 }

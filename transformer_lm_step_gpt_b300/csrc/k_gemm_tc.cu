@@ -434,7 +434,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
                    int splits, int* flags, int* err) {
-  pdl_trigger();
   using Cfg = TcCfg<BN>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -467,6 +466,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
   pdl_wait();  // from here on global memory written by the previous kernel is read
 
   if (warp == 0) {
@@ -598,7 +598,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ EpiMaps em, GemmArgs g, int k_tiles, int k_per_split,
                         int splits, int* flags, int* err) {
-  pdl_trigger();
   using PairCfg = PairCfgT<AUX>;
   constexpr int S = PairCfg::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -633,6 +632,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
   pdl_wait();  // from here on global memory written by the previous kernel is read
 
   if (warp == 0) {
@@ -920,7 +920,6 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
 __global__ void __launch_bounds__(RT_THREADS, 1)
     gemm_rows_tc_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tx,
                         const GemmArgs g, int ktiles, int kps, int* err) {
-  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sW = sm;                                                   // [STAGES][128 x 64]
@@ -947,6 +946,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tslot;
+  pdl_trigger();  // dependents launch only once every CTA holds its tensor memory
   pdl_wait();
   if (warp == 0 && lane == 0) {  // TMA producer
     for (int i = 0; i < nk; i++) {
