@@ -70,6 +70,10 @@ WORKLOADS = {
     # the 124M model on a small batch: the size used for ncu captures
     "gpt2-124M-B2-T1024": dict(L=12, C=768, NH=12, V=50257, Vp=50304, maxT=1024, B=2, T=1024,
                                dist="zipf", lr=6e-4, wd=0.1),
+    # two 124M layers at the throughput batch: the attention and layer kernels
+    # see the throughput shapes, the device holds ~4 GB (ncu captures)
+    "gpt2-124M-L2-B16-T1024": dict(L=2, C=768, NH=12, V=50257, Vp=50304, maxT=1024, B=16, T=1024,
+                                   dist="zipf", lr=6e-4, wd=0.1),
 }
 DEFAULT_WORKLOAD = "gpt2-124M-B16-T1024"
 DECODE_METRIC = "GPT-2 124M generated tokens/sec with a key/value cache (B=16 sequences) on 1 B300"

@@ -235,7 +235,6 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
             t3 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t3, "dV", "dK")
-            yield  # the named barrier around the column-sum exchange
 
     sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
@@ -340,7 +339,6 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
             t2 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t2, "dQ")
-            yield  # the named barrier around the column-sum exchange
 
     sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
     return sim.errors

@@ -3,7 +3,7 @@
 // Types, warp reductions, the device error word, and thin inline-PTX
 // wrappers (mbarrier, TMA bulk tensor copies, tcgen05) written from the
 // public PTX ISA.  Every wait on an mbarrier is bounded by the global
-// nanosecond timer: on expiry the waiting thread records GPT2 timeout in the
+// SM cycle counter: on expiry the waiting thread records a timeout in the
 // error word and returns false, and the kernel winds down without trapping.
 #pragma once
 
@@ -20,8 +20,12 @@ enum : int {
   DEVERR_TIMEOUT = 2,  // a bounded wait expired
 };
 
-// A bounded wait gives up after this many nanoseconds of global time.
-#define GPT2_WAIT_LIMIT_NS 2000000000ull
+// A bounded wait gives up after this many SM clock cycles: 2 s at the
+// B300's top SM clock (2,032 MHz), under 4 s at 1 GHz.  The SM's own cycle
+// counter is read (a few cycles) rather than the global nanosecond timer,
+// whose reads are slow enough to delay every wait that is not already
+// complete on its first test.
+#define GPT2_WAIT_LIMIT_CYCLES 4000000000ll
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
@@ -40,11 +44,7 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+__device__ __forceinline__ long long sm_cycles() { return clock64(); }
 
 __device__ __forceinline__ void record_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
@@ -96,6 +96,40 @@ __device__ __forceinline__ float ex2_hw(float x) {
   return y;
 }
 
+// Pairs of fp32 values in one 64-bit register and the PTX .f32x2
+// arithmetic (sm_100 and later): one instruction for two elements, which
+// halves the issue slots that elementwise warps take from the single
+// thread that issues a kernel's tensor-core instructions.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// max of three (PTX three-input max.f32, sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -143,21 +177,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same test, but a thread whose phase has not completed is suspended
+// until it completes or about `ns` nanoseconds pass.  A waiting thread then
+// issues nothing: a polling loop without the hint takes issue slots from
+// the warps that share its scheduler (measured: it halved the rate of the
+// attention kernels' elementwise warps and MMA issue).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records a timeout) if the time limit passes first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 0;; i++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u) {
-      // once any wait of the launch has given up, the others stop early
-      // instead of each spending the full limit
-      if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
-      if (global_ns() - t0 > GPT2_WAIT_LIMIT_NS) {
-        record_error(err, DEVERR_TIMEOUT);
-        return false;
-      }
+  const long long t0 = sm_cycles();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    // once any wait of the launch has given up, the others stop early
+    // instead of each spending the full limit
+    if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
+    if (sm_cycles() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+      record_error(err, DEVERR_TIMEOUT);
+      return false;
     }
   }
 }
@@ -213,6 +261,41 @@ __device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Four consecutive K steps in one statement (one predicate set-up for all
+// four): D (+)= A_k B_k^T for k = 0..3 with shared-memory descriptors
+// a + k*AS and b + k*BS (AS, BS: the K step's byte offset / 16); the first
+// accumulates iff acc != 0, the others always.  The issuing thread then
+// spends about one instruction per MMA, which matters when it shares its
+// scheduler with busy elementwise warps.
+template <int AS, int BS>
+__device__ __forceinline__ void tc_mma4_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n"
+      " setp.ne.b32 p, %3, 0;\n setp.eq.b32 t, %3, %3;\n"
+      " add.s64 a1, %1, %5;\n add.s64 a2, %1, %6;\n add.s64 a3, %1, %7;\n"
+      " add.s64 b1, %2, %8;\n add.s64 b2, %2, %9;\n add.s64 b3, %2, %10;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %4, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %4, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %4, t;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(acc), "r"(idesc), "n"(AS), "n"(2 * AS), "n"(3 * AS), "n"(BS), "n"(2 * BS), "n"(3 * BS)
+      : "memory");
+}
+// The same with A in tensor memory: columns a, a+8, a+16, a+24 (K = 16
+// bf16 values packed in 8 columns per step).
+template <int BS>
+__device__ __forceinline__ void tc_mma4_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p, t;\n .reg .b64 b1, b2, b3;\n"
+      " setp.ne.b32 p, %3, 0;\n setp.eq.b32 t, %3, %3;\n"
+      " add.s64 b1, %2, %5;\n add.s64 b2, %2, %6;\n add.s64 b3, %2, %7;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+8], b1, %4, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+16], b2, %4, t;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1+24], b3, %4, t;\n}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(acc), "r"(idesc), "n"(BS), "n"(2 * BS), "n"(3 * BS)
       : "memory");
 }
 // Arrive on an mbarrier once all previously issued tcgen05.mma of this
@@ -399,12 +482,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // and gives up like mbar_wait.
 __device__ __forceinline__ bool flag_wait(const int* p, int want, int* err) {
   if (ld_acquire_gpu(p) == want) return true;
-  const uint64_t t0 = global_ns();
+  const long long t0 = sm_cycles();
   for (uint32_t i = 0;; i++) {
+    __nanosleep(64);  // leave the issue slots to the warps that share the scheduler
     if (ld_acquire_gpu(p) == want) return true;
     if ((i & 63u) == 63u) {
       if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
-      if (global_ns() - t0 > GPT2_WAIT_LIMIT_NS) {
+      if (sm_cycles() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
         record_error(err, DEVERR_TIMEOUT);
         return false;
       }

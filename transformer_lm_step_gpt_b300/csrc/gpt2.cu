@@ -552,15 +552,13 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
-    // attention (the tensor-core path also leaves the qkv bias gradient's
-    // partial rows in cs_partial)
-    bool qkvb_partials = false;
+    // attention
     {
       ProfScope ps(m, PC_ATTN_BWD, attn_flop);
       if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
-      else qkvb_partials = launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
-                                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                                     lse, m->dsum, B, T, C, NH, m->cs_partial);
+      else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
+                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
+                                     lse, m->dsum, B, T, C, NH);
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
@@ -569,10 +567,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
-      if (qkvb_partials)
-        launch_colsum_reduce(c, m->G(QKVB) + (int64_t)l * 3 * C, m->cs_partial, B * ((T + 127) / 128), 3 * C);
-      else
-        launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+      launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);

@@ -35,14 +35,18 @@
 //            during their work), take P relative to a row reference maximum
 //            that moves only when the row maximum grows by more than 2^8
 //            (then O is rescaled in TMEM), write P into TMEM; O += P v(j)
-//            accumulates in TMEM.  Saves lse in base 2.
+//            accumulates in TMEM.  Saves minus the row logsumexp in base 2
+//            (the backward adds it in one fused multiply-add).
 //   dK, dV   item (128-key block, b*h), query sub-blocks of 128 (64 for head
 //            size 128): S^T = k q^T and dP^T = v dy^T; P^T and dS^T =
-//            P^T (dP^T - D) into TMEM; dV += P^T dy, dK += dS^T q.
+//            P^T (dP^T - D) into TMEM; dV += P^T dy, dK += dS^T q.  D is
+//            stored negated (added, not subtracted).
 //   dQ       item (128-query block, b*h), 128-key blocks: S = q k^T, dP =
 //            dy v^T; dS into TMEM; dQ += dS k.
 // No atomics: every output element is written by one CTA, so the results
-// repeat bit for bit.
+// repeat bit for bit.  The qkv bias gradient (column sums of dqkv) is left
+// to a separate coalesced column-sum pass: summing columns across the 32
+// lanes of each warp in these epilogues cost more than re-reading dqkv.
 #include <cuda.h>
 
 #include <cstdio>
@@ -107,6 +111,34 @@ __device__ __forceinline__ uint64_t kdesc(uint32_t tile, int rows, int kk) {
 // 64-column boxes are rows*128 bytes apart
 __device__ __forceinline__ uint64_t ndesc(uint32_t tile, int rows, int kk) {
   return sw128_desc(tile + (uint32_t)(kk * 2048), (uint32_t)(rows * 128), 1024);
+}
+// The same descriptors as a base (K step 0) plus a constant: the start
+// address field holds address / 16 in the low bits, so a K step adds its
+// byte offset / 16 to the 64-bit descriptor
+__device__ __forceinline__ uint64_t kstep(int rows, int kk) {
+  return (uint64_t)(((kk >> 2) * rows * 128 + (kk & 3) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t nstep(int kk) { return (uint64_t)(kk * 128); }
+// A chain of K steps over the head dims (KS = HS/16) of two K-major
+// shared-memory operands with `arows` and `brows` rows: four steps per
+// statement while at least four remain in a 64-column box.
+template <int KS>
+__device__ __forceinline__ void mma_hs_ss(uint32_t d, uint64_t a, int arows, uint64_t b, int brows, uint32_t idesc) {
+  if constexpr (KS >= 4) {
+#pragma unroll
+    for (int c = 0; c < KS / 4; c++)
+      tc_mma4_ss<2, 2>(d, a + kstep(arows, 4 * c), b + kstep(brows, 4 * c), idesc, c > 0 ? 1u : 0u);
+  } else {
+#pragma unroll
+    for (int kk = 0; kk < KS; kk++) tc_mma_bf16(d, a + kstep(arows, kk), b + kstep(brows, kk), idesc, kk > 0 ? 1u : 0u);
+  }
+}
+// A chain of NK K steps (a multiple of 4) with A in TMEM from column a and
+// an MN-major B operand (K = rows): dst (+)= A B, accumulating iff acc.
+template <int NK>
+__device__ __forceinline__ void mma_ts_chain(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+#pragma unroll
+  for (int c = 0; c < NK / 4; c++) tc_mma4_ts<128>(d, a + 32 * c, b + nstep(4 * c), idesc, (acc || c > 0) ? 1u : 0u);
 }
 // TMA of one tile (NB boxes) onto one barrier
 template <int HS>
@@ -226,9 +258,8 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
         mbar_wait(p_full, (uint32_t)gp & 1u, err);
         mbar_wait(&v_full[gp % KV], (uint32_t)(gp / KV) & 1u, err);
         tc_fence_after();
-        const uint32_t bV = smem_u32(sV + (gp % KV) * TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tO, tP + kk * 8, ndesc(bV, 128, kk), idO, (!first || kk > 0) ? 1u : 0u);
+        const uint64_t dV = ndesc(smem_u32(sV + (gp % KV) * TILE), 128, 0);
+        mma_ts_chain<8>(tO, tP, dV, idO, !first);
         tc_commit(&v_empty[gp % KV]);
         tc_commit(o_done);
       };
@@ -240,14 +271,13 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
         const int nk = nqb - idx / BH;  // key blocks 0 .. qb
         const int qs = it % QB;
         mbar_wait(&q_full[qs], (uint32_t)(it / QB) & 1u, err);
-        const uint32_t aQ = smem_u32(sQ + qs * TILE);
+        const uint64_t dQ = kdesc(smem_u32(sQ + qs * TILE), 128, 0);
         for (int j = 0; j < nk; j++, g++) {
           mbar_wait(&k_full[g % KV], (uint32_t)(g / KV) & 1u, err);
           if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
           tc_fence_after();
-          const uint32_t bK = smem_u32(sK + (g % KV) * TILE);
-#pragma unroll
-          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tS, kdesc(aQ, 128, kk), kdesc(bK, 128, kk), idS, kk > 0 ? 1u : 0u);
+          const uint64_t dK = kdesc(smem_u32(sK + (g % KV) * TILE), 128, 0);
+          mma_hs_ss<Hs<HS>::KS>(tS, dQ, 128, dK, 128, idS);
           tc_commit(&k_empty[g % KV]);
           if (j == nk - 1) tc_commit(&q_empty[qs]);
           tc_commit(s_full);
@@ -309,15 +339,20 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);
         const int k0 = j * 128 + half * 64;  // key of column 0 of this warp
-        const bool diag = j == nk - 1;
-        float mx = -INFINITY;
-        if (diag) {
+        if (j == nk - 1) {  // the diagonal block: keys after the query read as -inf
 #pragma unroll
           for (int c = 0; c < 64; c++)
-            if (k0 + c <= q) mx = fmaxf(mx, __uint_as_float(s[c]));
-        } else {
+            if (k0 + c > q) s[c] = __float_as_uint(-INFINITY);
+        }
+        float mx;
+        {
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int c = 0; c < 64; c++) mx = fmaxf(mx, __uint_as_float(s[c]));
+          for (int c = 0; c < 64; c += 8)
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+              m4[u] = fmax3(m4[u], __uint_as_float(s[c + 2 * u]), __uint_as_float(s[c + 2 * u + 1]));
+          mx = fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
         }
         float* rd = red + (g & 1) * 256;
         rd[half * 128 + row] = mx;
@@ -330,26 +365,21 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
           l *= alpha;
           m = mcand;
         }
-        const float mo = m * sl2;
-        float sum = 0.f;
+        // p = 2^(s sl2 - m sl2), two columns per instruction
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nmo2 = f2_pack(-m * sl2, -m * sl2);
+        uint64_t sum2 = f2_pack(0.f, 0.f);
         uint32_t pk[32];
-        if (diag) {
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = k0 + c <= q ? ex2_hw(__uint_as_float(s[c]) * sl2 - mo) : 0.f;
-            const float p1 = k0 + c + 1 <= q ? ex2_hw(__uint_as_float(s[c + 1]) * sl2 - mo) : 0.f;
-            sum += p0 + p1;
-            pk[c >> 1] = pack_bf16(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float p0 = ex2_hw(__uint_as_float(s[c]) * sl2 - mo);
-            const float p1 = ex2_hw(__uint_as_float(s[c + 1]) * sl2 - mo);
-            sum += p0 + p1;
-            pk[c >> 1] = pack_bf16(p0, p1);
-          }
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nmo2), x0, x1);
+          const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
+          sum2 = f2_add(sum2, f2_pack(p0, p1));
+          pk[c >> 1] = pack_bf16(p0, p1);
         }
+        float sa, sb;
+        f2_unpack(sum2, sa, sb);
+        const float sum = sa + sb;
         if (j > 0) {
           // P(g-1) V(g-1) done: the P columns are free and O is complete up
           // to block g-1 (at j = 0 the previous item's epilogue waited)
@@ -386,7 +416,7 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
 #pragma unroll
         for (int i = 0; i < OH; i++) v[i] = __uint_as_float(o[i]);
         store_bf16_row<OH>(y + ((int64_t)b * T + q) * C + h * HS + half * OH, v, 1.f / lt);
-        if (half == 0) lse[(int64_t)bh * T + q] = m * sl2 + log2f(lt);  // base-2 units
+        if (half == 0) lse[(int64_t)bh * T + q] = -(m * sl2 + log2f(lt));  // minus lse, base-2 units
       }
     }
   }
@@ -427,12 +457,65 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
       const int64_t bt = i / chunks;
       const int h = (int)(i % chunks) / G;
       const int t = (int)(bt % T), b = (int)(bt / T);
-      dsum[((int64_t)b * NH + h) * T + t] = s;
+      dsum[((int64_t)b * NH + h) * T + t] = -s;
     }
   }
 }
 
 // ============================================================ backward: dK, dV
+// The elementwise step of one key row over N query columns (c0 .. c0+N-1):
+// P^T = 2^(S^T sl2 - lse2), dS^T = P^T (dP^T - D), packed to bf16 pairs.
+// nl, nd: minus lse2 and minus D of the columns, from shared memory
+// (staged) or global memory (gl, gd: the (b, h) rows, read at c0 + i).
+// MASK: columns before the key or past T give 0 (a masked column may hold
+// a stale lse / D: select, do not scale).
+template <int N, bool MASK>
+__device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_t* rd, const float* nl, const float* nd,
+                                               bool staged, const float* gl, const float* gd, int c0, int key, int T,
+                                               float sl2, uint32_t* pk, uint32_t* dk) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2);
+#pragma unroll
+  for (int i = 0; i < N; i += 4) {
+    float4 a, d;
+    if (staged) {
+      a = *reinterpret_cast<const float4*>(nl + i);
+      d = *reinterpret_cast<const float4*>(nd + i);
+    } else {
+      float t[8];
+#pragma unroll
+      for (int u = 0; u < 4; u++) {
+        const int qq = min(c0 + i + u, T - 1);
+        t[u] = __ldg(gl + qq);
+        t[4 + u] = __ldg(gd + qq);
+      }
+      a = make_float4(t[0], t[1], t[2], t[3]);
+      d = make_float4(t[4], t[5], t[6], t[7]);
+    }
+    float x0, x1, x2, x3;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, f2_pack(a.x, a.y)), x0, x1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i + 2]), __uint_as_float(rs[i + 3])), sl2x2, f2_pack(a.z, a.w)), x2, x3);
+    float p0 = ex2_hw(x0), p1 = ex2_hw(x1), p2 = ex2_hw(x2), p3 = ex2_hw(x3);
+    const uint64_t t01 = f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), f2_pack(d.x, d.y));
+    const uint64_t t23 = f2_add(f2_pack(__uint_as_float(rd[i + 2]), __uint_as_float(rd[i + 3])), f2_pack(d.z, d.w));
+    float d0, d1, d2, d3;
+    f2_unpack(f2_mul(f2_pack(p0, p1), t01), d0, d1);
+    f2_unpack(f2_mul(f2_pack(p2, p3), t23), d2, d3);
+    if (MASK) {
+      const int c = c0 + i;
+      const bool ok0 = c >= key && c < T, ok1 = c + 1 >= key && c + 1 < T;
+      const bool ok2 = c + 2 >= key && c + 2 < T, ok3 = c + 3 >= key && c + 3 < T;
+      p0 = ok0 ? p0 : 0.f; d0 = ok0 ? d0 : 0.f;
+      p1 = ok1 ? p1 : 0.f; d1 = ok1 ? d1 : 0.f;
+      p2 = ok2 ? p2 : 0.f; d2 = ok2 ? d2 : 0.f;
+      p3 = ok3 ? p3 : 0.f; d3 = ok3 ? d3 : 0.f;
+    }
+    pk[i >> 1] = pack_bf16(p0, p1);
+    pk[(i >> 1) + 1] = pack_bf16(p2, p3);
+    dk[i >> 1] = pack_bf16(d0, d1);
+    dk[(i >> 1) + 1] = pack_bf16(d2, d3);
+  }
+}
+
 // Item (128-key block kb, b*h): query sub-blocks of QS rows from k0 = 128 kb
 // to T.  Warps 0..15 elementwise (warps w, w+4, w+8, w+12 share TMEM lane
 // quarter w % 4 = 32 key rows and take QS/4 query columns each), warp 16
@@ -442,8 +525,7 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 //   dV += P^T dy, dK += dS^T q (N = HS, K = QS queries; A from TMEM).
 // TMEM: S^T 0..QS-1, dP^T QS..2QS-1, P^T 2QS.., dS^T 2.5QS.., dV 3QS..,
 // dK 3QS+HS.. (at most 512 columns).
-// smem: K, V [KVB] | q, dy ring [ST] | lse / D per stage [ST][2][QS] |
-//       column-sum exchange | barriers.
+// smem: K, V [KVB] | q, dy ring [ST] | lse / D per stage [ST][2][QS] | barriers.
 // lse and D of a sub-block arrive by bulk copy with its tiles when T is a
 // multiple of 4 (16-byte aligned rows); otherwise the elementwise warps read
 // them from global memory.
@@ -457,15 +539,14 @@ struct KvCfg {
   static constexpr uint32_t QTILE = Hs<HS>::NB * (uint32_t)QS * 128u;     // [QS x HS]
   static constexpr int KVB = HS > 64 ? 1 : 2;
   static constexpr int ST = 4;
-  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + 8 * HS * 4 + 256;
+  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                            const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
-                           const float* dsum, float* bias_partial, int B, int T, int C, int NH, float scale,
-                           int* err) {
+                           const float* dsum, int B, int T, int C, int NH, float scale, int* err) {
   using Cf = KvCfg<HS>;
   constexpr int QS = Cf::QS, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
   constexpr uint32_t KTILE = Cf::KTILE, QTILE = Cf::QTILE;
@@ -476,8 +557,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sQ = sV + KVB * KTILE;            // [ST]
   uint8_t* sD = sQ + ST * QTILE;             // dy [ST]
   float* sLD = reinterpret_cast<float*>(sD + ST * QTILE);  // [ST][lse QS, D QS]
-  float* red = sLD + ST * 2 * QS;                          // [2][4][HS]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 8 * HS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + ST * 2 * QS);
   uint64_t* kv_full = bars;              // [KVB]
   uint64_t* kv_empty = kv_full + KVB;    // [KVB]: the item's last S^T, dP^T have read k, v
   uint64_t* q_full = kv_empty + KVB;     // [ST]
@@ -553,13 +633,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         mbar_wait(p_full, (uint32_t)gp & 1u, err);
         tc_fence_after();
         const int s = gp % ST;
-        const uint32_t bQ = smem_u32(sQ + s * QTILE), bD = smem_u32(sD + s * QTILE);
-#pragma unroll
-        for (int kk = 0; kk < QS / 16; kk++)
-          tc_mma_bf16_ts(tdV, tPt + kk * 8, ndesc(bD, QS, kk), idO, (!first || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < QS / 16; kk++)
-          tc_mma_bf16_ts(tdK, tdSt + kk * 8, ndesc(bQ, QS, kk), idO, (!first || kk > 0) ? 1u : 0u);
+        const uint64_t dQn = ndesc(smem_u32(sQ + s * QTILE), QS, 0), dDn = ndesc(smem_u32(sD + s * QTILE), QS, 0);
+        mma_ts_chain<QS / 16>(tdV, tPt, dDn, idO, !first);
+        mma_ts_chain<QS / 16>(tdK, tdSt, dQn, idO, !first);
         tc_commit(&q_empty[s]);
         tc_commit(p_empty);
         if (last) tc_commit(acc_full);
@@ -573,17 +649,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         const int nsub = (T - k0 + QS - 1) / QS;
         const int kvb = it % KVB;
         mbar_wait(&kv_full[kvb], (uint32_t)(it / KVB) & 1u, err);
-        const uint32_t aK = smem_u32(sK + kvb * KTILE), aV = smem_u32(sV + kvb * KTILE);
+        const uint64_t dK = kdesc(smem_u32(sK + kvb * KTILE), 128, 0), dV = kdesc(smem_u32(sV + kvb * KTILE), 128, 0);
         for (int j = 0; j < nsub; j++, g++) {
           const int s = g % ST;
           mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);
           if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
           tc_fence_after();
-          const uint32_t bQ = smem_u32(sQ + s * QTILE), bD = smem_u32(sD + s * QTILE);
-#pragma unroll
-          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tSt, kdesc(aK, 128, kk), kdesc(bQ, QS, kk), idS, kk > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tdPt, kdesc(aV, 128, kk), kdesc(bD, QS, kk), idS, kk > 0 ? 1u : 0u);
+          const uint64_t dQ = kdesc(smem_u32(sQ + s * QTILE), QS, 0), dD = kdesc(smem_u32(sD + s * QTILE), QS, 0);
+          mma_hs_ss<Hs<HS>::KS>(tSt, dK, 128, dQ, QS, idS);
+          mma_hs_ss<Hs<HS>::KS>(tdPt, dV, 128, dD, QS, idS);
           if (j == nsub - 1) tc_commit(&kv_empty[kvb]);
           tc_commit(s_full);
           if (prev) dvdk(g - 1, prev_first, prev_last);
@@ -619,41 +693,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         if (lane == 0) mbar_arrive(s_free);
         const int c0 = q0 + cg * CPT;  // query of column 0 of this warp
         if (staged) mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
-        const float* lc = sLD + s * 2 * QS + cg * CPT;
+        const float* lc = sLD + s * 2 * QS + cg * CPT;  // minus lse, minus D of the columns
         uint32_t pk[CPT / 2], dk[CPT / 2];
-        const bool mask = q0 < k0 + 128 || q0 + QS > T;
-#pragma unroll
-        for (int i = 0; i < CPT; i += 4) {
-          float lv[4], dv[4];
-          if (staged) {
-            const float4 a = *reinterpret_cast<const float4*>(lc + i);
-            const float4 d = *reinterpret_cast<const float4*>(lc + QS + i);
-            lv[0] = a.x; lv[1] = a.y; lv[2] = a.z; lv[3] = a.w;
-            dv[0] = d.x; dv[1] = d.y; dv[2] = d.z; dv[3] = d.w;
-          } else {
-#pragma unroll
-            for (int u = 0; u < 4; u++) {
-              const int qq = min(c0 + i + u, T - 1);
-              lv[u] = __ldg(lse + (int64_t)bh * T + qq);
-              dv[u] = __ldg(dsum + (int64_t)bh * T + qq);
-            }
-          }
-          float p[4], d[4];
-#pragma unroll
-          for (int u = 0; u < 4; u++) {
-            p[u] = ex2_hw(__uint_as_float(rs[i + u]) * sl2 - lv[u]);
-            d[u] = p[u] * (__uint_as_float(rd[i + u]) - dv[u]);
-            if (mask) {  // a masked column may hold a stale lse / D: select, do not scale
-              const bool ok = c0 + i + u >= key && c0 + i + u < T;
-              p[u] = ok ? p[u] : 0.f;
-              d[u] = ok ? d[u] : 0.f;
-            }
-          }
-          pk[i >> 1] = pack_bf16(p[0], p[1]);
-          pk[(i >> 1) + 1] = pack_bf16(p[2], p[3]);
-          dk[i >> 1] = pack_bf16(d[0], d[1]);
-          dk[(i >> 1) + 1] = pack_bf16(d[2], d[3]);
-        }
+        if (q0 < k0 + 128 || q0 + QS > T)
+          kv_elementwise<CPT, true>(rs, rd, lc, lc + QS, staged, lse + (int64_t)bh * T, dsum + (int64_t)bh * T, c0, key,
+                                    T, sl2, pk, dk);
+        else
+          kv_elementwise<CPT, false>(rs, rd, lc, lc + QS, staged, lse + (int64_t)bh * T, dsum + (int64_t)bh * T, c0, key,
+                                     T, sl2, pk, dk);
         if (g > 0) {
           mbar_wait(p_empty, (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read P^T, dS^T
           tc_fence_after();
@@ -680,25 +727,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         tmem_ld_wait();
         float v[EC];
 #pragma unroll
-        for (int i = 0; i < EC; i++) v[i] = key < T ? __uint_as_float(ra[i]) * mul : 0.f;
+        for (int i = 0; i < EC; i++) v[i] = __uint_as_float(ra[i]);
         if (key < T)
-          store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, 1.f);
-        // the block's column sums of dV and dK: one partial row of the qkv
-        // bias gradient per (batch row, key block)
-        warp_sum_cols<EC>(v);
-        if (lane == 0) {
-#pragma unroll
-          for (int i = 0; i < EC; i++) red[(which * 4 + quarter) * HS + ch * EH + e + i] = v[i];
-        }
+          store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, mul);
       }
-      named_bar_sync(1, KV_CW * 32);
-      if (tid < 2 * HS) {
-        const int wh = tid / HS, col = tid % HS;
-        const float* rr = red + wh * 4 * HS + col;
-        const float sum = (rr[0] + rr[HS]) + (rr[2 * HS] + rr[3 * HS]);
-        bias_partial[((int64_t)b * nkb + kb) * C3 + (wh ? C : 2 * C) + h * HS + col] = sum;
-      }
-      named_bar_sync(1, KV_CW * 32);  // red is reused by the next item
     }
   }
   tc_fence_before();
@@ -713,7 +745,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 //   S = q k^T, dP = dy v^T (M = 128 queries, N = 128 keys, K = HS);
 //   dS = P (dP - D) into TMEM; dQ += dS k (N = HS, K = 128 keys).
 // TMEM: S 0..127, dP 128..255, dS 256..319, dQ 320..320+HS-1.
-// smem: q, dy [QB] | K ring [KST] | V ring [2] | column-sum exchange | barriers.
+// smem: q, dy [QB] | K ring [KST] | V ring [2] | barriers.
 #define DQ_CW 16
 #define DQ_THREADS (DQ_CW * 32 + 64)
 template <int HS>
@@ -722,14 +754,14 @@ struct DqCfg {
   static constexpr int QB = HS > 64 ? 1 : 2;
   static constexpr int KST = HS > 64 ? 2 : 3;
   static constexpr int VST = 2;
-  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + 4 * HS * 4 + 256;
+  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
-                          bf16* dqkv, const float* lse, const float* dsum, float* bias_partial, int B, int T,
-                          int C, int NH, float scale, int* err) {
+                          bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH,
+                          float scale, int* err) {
   using Cf = DqCfg<HS>;
   constexpr int QB = Cf::QB, KST = Cf::KST, VST = Cf::VST;
   constexpr uint32_t TILE = Cf::TILE;
@@ -738,8 +770,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint8_t* sQ = sm;                     // [QB] x (q, dy)
   uint8_t* sK = sQ + QB * 2 * TILE;     // [KST]
   uint8_t* sV = sK + KST * TILE;        // [VST]
-  float* red = reinterpret_cast<float*>(sV + VST * TILE);  // [4][HS]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red + 4 * HS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * TILE);
   uint64_t* qd_full = bars;             // [QB]
   uint64_t* qd_empty = qd_full + QB;    // [QB]: the item's last S, dP have read q, dy
   uint64_t* k_full = qd_empty + QB;     // [KST]
@@ -809,9 +840,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       auto dq = [&](int gp, bool first, bool last) {  // dQ (+)= dS(gp) k(gp)
         mbar_wait(p_full, (uint32_t)gp & 1u, err);
         tc_fence_after();
-        const uint32_t bK = smem_u32(sK + (gp % KST) * TILE);
-#pragma unroll
-        for (int kk = 0; kk < 8; kk++) tc_mma_bf16_ts(tdQ, tdS + kk * 8, ndesc(bK, 128, kk), idQ, (!first || kk > 0) ? 1u : 0u);
+        const uint64_t dKn = ndesc(smem_u32(sK + (gp % KST) * TILE), 128, 0);
+        mma_ts_chain<8>(tdQ, tdS, dKn, idQ, !first);
         tc_commit(&k_empty[gp % KST]);
         tc_commit(ds_free);
         if (last) tc_commit(dq_full);
@@ -824,18 +854,16 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         const int nk = nqb - idx / BH;
         const int ib = it % QB;
         mbar_wait(&qd_full[ib], (uint32_t)(it / QB) & 1u, err);
-        const uint32_t aQ = smem_u32(sQ + ib * 2 * TILE), aD = aQ + TILE;
+        const uint64_t dQ = kdesc(smem_u32(sQ + ib * 2 * TILE), 128, 0), dD = kdesc(smem_u32(sQ + ib * 2 * TILE + TILE), 128, 0);
         for (int j = 0; j < nk; j++, g++) {
           const int ks = g % KST, vs = g % VST;
           mbar_wait(&k_full[ks], (uint32_t)(g / KST) & 1u, err);
           mbar_wait(&v_full[vs], (uint32_t)(g / VST) & 1u, err);
           if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
           tc_fence_after();
-          const uint32_t bK = smem_u32(sK + ks * TILE), bV = smem_u32(sV + vs * TILE);
-#pragma unroll
-          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tS, kdesc(aQ, 128, kk), kdesc(bK, 128, kk), idS, kk > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < Hs<HS>::KS; kk++) tc_mma_bf16(tdP, kdesc(aD, 128, kk), kdesc(bV, 128, kk), idS, kk > 0 ? 1u : 0u);
+          const uint64_t dK = kdesc(smem_u32(sK + ks * TILE), 128, 0), dV = kdesc(smem_u32(sV + vs * TILE), 128, 0);
+          mma_hs_ss<Hs<HS>::KS>(tS, dQ, 128, dK, 128, idS);
+          mma_hs_ss<Hs<HS>::KS>(tdP, dD, 128, dV, 128, idS);
           tc_commit(&v_empty[vs]);
           if (j == nk - 1) tc_commit(&qd_empty[ib]);
           tc_commit(s_full);
@@ -859,8 +887,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       if (idx >= nitems) break;
       const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
       const int q = qb * 128 + row, nk = qb + 1;
-      const float my_lse = q < T ? lse[(int64_t)bh * T + q] : INFINITY;  // base 2
-      const float my_d = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+        // minus the row's lse (base 2) and minus its D; rows past T give P = 0
+      const float nl = q < T ? lse[(int64_t)bh * T + q] : -INFINITY;
+      const float nd = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
       for (int j = 0; j < nk; j++, g++) {
         mbar_wait(s_full, (uint32_t)g & 1u, err);
         tc_fence_after();
@@ -876,10 +906,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         uint32_t dk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2_hw(__uint_as_float(rs[i]) * sl2 - my_lse);
-          const float p1 = ex2_hw(__uint_as_float(rs[i + 1]) * sl2 - my_lse);
-          float d0 = p0 * (__uint_as_float(rd[i]) - my_d);
-          float d1 = p1 * (__uint_as_float(rd[i + 1]) - my_d);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, nl2), x0, x1);
+          const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
+          float d0, d1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), nd2)), d0, d1);
           if (diag) {
             d0 = c0 + i <= q ? d0 : 0.f;
             d1 = c0 + i + 1 <= q ? d1 : 0.f;
@@ -916,19 +947,6 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           *reinterpret_cast<uint2*>(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * HS + cg * EQ) = u;
         }
       }
-      // the block's column sums of dQ: one partial row of the qkv bias
-      // gradient per (batch row, query block)
-      warp_sum_cols<EQ>(v);
-      if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < EQ; i++) red[quarter * HS + cg * EQ + i] = v[i];
-      }
-      named_bar_sync(1, DQ_CW * 32);
-      if (tid < HS) {
-        const float* rr = red + tid;
-        bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * HS + tid] = (rr[0] + rr[HS]) + (rr[2 * HS] + rr[3 * HS]);
-      }
-      named_bar_sync(1, DQ_CW * 32);  // red is reused by the next item
     }
   }
   tc_fence_before();
@@ -965,7 +983,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 
 template <int HS>
 static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, const bf16* qkv, const float* lse,
-                   float* dsum, int B, int T, int C, int NH, float* bias_partial) {
+                   float* dsum, int B, int T, int C, int NH) {
   using Kv = KvCfg<HS>;
   using Dq = DqCfg<HS>;
   CUtensorMap tq, tq_s, td, td_s;
@@ -982,21 +1000,20 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
   const int grid = std::min(nitems, c.num_sms);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
   launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, dqkv, lse,
-             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
+             (const float*)dsum, B, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Dq::SMEM);
   launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, dqkv, lse,
-             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
+             (const float*)dsum, B, T, C, NH, scale, c.err);
 }
 
-bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T,
-                               int C, int NH, float* bias_partial) {
+                               int C, int NH) {
   switch (C / NH) {
-    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
-    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
-    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
-    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); break;
-    default: c.host_fail = 1; return false;
+    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
+    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
+    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
+    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
+    default: c.host_fail = 1;
   }
-  return true;
 }

@@ -182,9 +182,10 @@ void launch_gemm_rows(LaunchCtx& c, const GemmArgs& g);
 // ---------------------------------------------------------------- attention
 // qkv [B,T,3C] -> y [B,T,C], lse [B,NH,T]: the logsumexp of the scaled,
 // masked scores of each query row, in natural-log units on the CUDA-core
-// path (launch_attention_*_simt) and in base-2 units (log2 of the row's sum
-// of 2^(score*scale*log2 e)) on the tensor-core path (*_bf16 with head size
-// 64); each backward reads what its own forward wrote.
+// path (launch_attention_*_simt), and minus it in base-2 units (minus log2
+// of the row's sum of 2^(score*scale*log2 e)) on the tensor-core path
+// (*_bf16); each backward reads what its own forward wrote (the tensor-core
+// backward also keeps D = rowsum(dy * y) negated in dsum).
 template <typename T>
 void launch_attention_fwd_simt(LaunchCtx& c, T* y, float* lse, const T* qkv, int B, int T_,
                                int C, int NH);
@@ -195,12 +196,10 @@ void launch_attention_bwd_simt(LaunchCtx& c, T* dqkv, const T* dy, const T* y, c
 int64_t attention_simt_scratch_floats(int B, int T_, int NH);
 void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T_,
                                int C, int NH);
-// Returns true when it also wrote the qkv bias gradient's partial rows
-// (head size 64, tensor-core path): bias_partial [B * ceil(T/128)][3C],
-// row b * ceil(T/128) + block (launch_colsum_reduce adds them up).
-bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+// qkv, y, dy -> dqkv [B,T,3C] (dq | dk | dv); dsum [B,NH,T] is scratch.
+void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
-                               int C, int NH, float* bias_partial);
+                               int C, int NH);
 
 // A tensor map over a [B][T][W] bf16 tensor with box {64, rows, 1},
 // 128-byte swizzle, rows past T read as 0 (false if the driver's encoder is
