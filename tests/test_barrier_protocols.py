@@ -139,10 +139,12 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
     """attn_bwd_dkv_tc_kernel.  Loader: per item k, v into buffer it % kvb
     once the item kvb back has issued its last S^T, dP^T; per query
     sub-block g q, dy (and, staged, their lse / D) into ring stage
-    g % stages once dV, dK(g - stages) have read it.  MMA issuer, over all
-    sub-blocks in turn: S^T(g), dP^T(g) once the warps have copied out
-    S^T(g - 1), dP^T(g - 1); then dV, dK(g - 1) from P^T, dS^T(g - 1);
-    the item's last one also commits the accumulators' completion.
+    g % stages once dV, dK(g - stages) have read it.  Score issuer, over
+    all sub-blocks in turn: S^T(g), dP^T(g) once the warps have copied out
+    S^T(g - 1), dP^T(g - 1).  Gradient issuer (another thread, its MMAs
+    interleave with the score issuer's in any order): dV, dK(g) from
+    P^T, dS^T(g); an item's last one also commits the accumulators'
+    completion.
     Elementwise warps: copy S^T, dP^T out; (staged) wait for the stage's
     lse / D; P^T, dS^T into tensor memory once dV, dK(g - 1) have read them;
     dV, dK read at the end of each item."""
@@ -176,24 +178,13 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
                 sim.tma("qf%d" % s, *stage_bufs(s), phase=g // stages)
                 g += 1
 
-    def mma():
-        def dvdk(gp, first, last):
-            s = gp % stages
-            yield from sim.wait("pf", gp)
-            acc = () if first else ("dV", "dK")
-            sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s) + acc, writes=("dV", "dK"))
-            sim.commit("qe%d" % s, phase=gp // stages)
-            sim.commit("pe", phase=gp)
-            if last:
-                sim.commit("acc", phase=it_of[gp])
-        g, prev = 0, None
-        it_of = {}
+    def score_mma():
+        g = 0
         for it, nsub in enumerate(items):
             b = it % kvb
             yield from sim.wait("kvf%d" % b, it // kvb)
             for j in range(nsub):
                 s = g % stages
-                it_of[g] = it
                 yield from sim.wait("qf%d" % s, g // stages)
                 if g > 0:
                     yield from sim.wait("sfree", g - 1)
@@ -201,12 +192,21 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
                 if j == nsub - 1:
                     sim.commit("kve%d" % b, phase=it // kvb)
                 sim.commit("sf", phase=g)
-                if prev is not None:
-                    yield from dvdk(*prev)
-                prev = (g, j == 0, j == nsub - 1)
                 g += 1
-        if prev is not None:
-            yield from dvdk(*prev)
+
+    def grad_mma():
+        g = 0
+        for it, nsub in enumerate(items):
+            for j in range(nsub):
+                s = g % stages
+                yield from sim.wait("pf", g)
+                acc = () if j == 0 else ("dV", "dK")
+                sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s) + acc, writes=("dV", "dK"))
+                sim.commit("qe%d" % s, phase=g // stages)
+                sim.commit("pe", phase=g)
+                if j == nsub - 1:
+                    sim.commit("acc", phase=it)
+                g += 1
 
     def compute():
         g = 0
@@ -236,7 +236,7 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t3, "dV", "dK")
 
-    sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
+    sim.run([loader(), score_mma(), grad_mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
 
 
@@ -245,9 +245,10 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
     """attn_bwd_dq_tc_kernel.  Loader: per item q, dy into buffer it % qb
     once the item qb back has issued its last S, dP; per key block k into
     stage g % kst once dQ(g - kst) has read it, v into stage g % vst once
-    dP(g - vst) has.  MMA issuer, over all blocks in turn: S(g), dP(g) once
-    the warps have copied out S(g - 1), dP(g - 1); then dQ(g - 1) from
-    dS(g - 1) (the item's last one also commits dQ's completion).
+    dP(g - vst) has.  Score issuer, over all blocks in turn: S(g), dP(g)
+    once the warps have copied out S(g - 1), dP(g - 1).  dQ issuer
+    (another thread): dQ(g) from dS(g) (an item's last one also commits
+    dQ's completion).
     Elementwise warps: copy S, dP out; dS into tensor memory once dQ(g - 1)
     has read it; dQ read at the end of each item."""
     sim = Sim(seed, plant)
@@ -283,24 +284,13 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
                 sim.tma("vf%d" % vs, "sV%d" % vs, phase=g // vst)
                 g += 1
 
-    def mma():
-        it_of = {}
-
-        def dqm(gp, first, last):
-            ks = gp % kst
-            yield from sim.wait("pf", gp)
-            sim.mma(reads=("dS", "sK%d" % ks) + (() if first else ("dQ",)), writes=("dQ",))
-            sim.commit("ke%d" % ks, phase=gp // kst)
-            sim.commit("dsf", phase=gp)
-            if last:
-                sim.commit("dqf", phase=it_of[gp])
-        g, prev = 0, None
+    def score_mma():
+        g = 0
         for it, nk in enumerate(items):
             b = it % qb
             yield from sim.wait("qf%d" % b, it // qb)
             for j in range(nk):
                 ks, vs = g % kst, g % vst
-                it_of[g] = it
                 yield from sim.wait("kf%d" % ks, g // kst)
                 yield from sim.wait("vf%d" % vs, g // vst)
                 if g > 0:
@@ -310,12 +300,20 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
                 if j == nk - 1:
                     sim.commit("qe%d" % b, phase=it // qb)
                 sim.commit("sf", phase=g)
-                if prev is not None:
-                    yield from dqm(*prev)
-                prev = (g, j == 0, j == nk - 1)
                 g += 1
-        if prev is not None:
-            yield from dqm(*prev)
+
+    def dq_mma():
+        g = 0
+        for it, nk in enumerate(items):
+            for j in range(nk):
+                ks = g % kst
+                yield from sim.wait("pf", g)
+                sim.mma(reads=("dS", "sK%d" % ks) + (() if j == 0 else ("dQ",)), writes=("dQ",))
+                sim.commit("ke%d" % ks, phase=g // kst)
+                sim.commit("dsf", phase=g)
+                if j == nk - 1:
+                    sim.commit("dqf", phase=it)
+                g += 1
 
     def compute():
         g = 0
@@ -340,7 +338,7 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t2, "dQ")
 
-    sim.run([loader(), mma()] + [compute() for _ in range(ncomp)])
+    sim.run([loader(), score_mma(), dq_mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
 
 

@@ -251,6 +251,8 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
 
   if (warp == FW_SOFT) {
     // ------------------------------------------------------------ MMA issuer
+    // (one thread: a second issuer warp would cost the softmax warps the
+    // registers that two CTAs per SM leave them)
     if (lane == 0) {
       const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
       const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
@@ -519,7 +521,8 @@ __device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_
 // Item (128-key block kb, b*h): query sub-blocks of QS rows from k0 = 128 kb
 // to T.  Warps 0..15 elementwise (warps w, w+4, w+8, w+12 share TMEM lane
 // quarter w % 4 = 32 key rows and take QS/4 query columns each), warp 16
-// the MMA issuer, warp 17 the loader.
+// issues the score products, warp 17 loads, warp 18 issues the gradient
+// products.
 //   S^T = k q^T, dP^T = v dy^T (M = 128 keys, N = QS queries, K = HS);
 //   P^T = 2^(S^T scale log2e - lse2), dS^T = P^T (dP^T - D), into TMEM;
 //   dV += P^T dy, dK += dS^T q (N = HS, K = QS queries; A from TMEM).
@@ -530,7 +533,7 @@ __device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_
 // multiple of 4 (16-byte aligned rows); otherwise the elementwise warps read
 // them from global memory.
 #define KV_CW 16
-#define KV_THREADS (KV_CW * 32 + 64)
+#define KV_THREADS (KV_CW * 32 + 96)
 template <int HS>
 struct KvCfg {
   static constexpr int QS = HS > 64 ? 64 : 128;
@@ -625,23 +628,10 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       }
     }
   } else if (warp == KV_CW) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- score MMAs
     if (lane == 0) {
       const uint32_t idS = tc_idesc_bf16(128, QS, false, false);
-      const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
-      auto dvdk = [&](int gp, bool first, bool last) {
-        mbar_wait(p_full, (uint32_t)gp & 1u, err);
-        tc_fence_after();
-        const int s = gp % ST;
-        const uint64_t dQn = ndesc(smem_u32(sQ + s * QTILE), QS, 0), dDn = ndesc(smem_u32(sD + s * QTILE), QS, 0);
-        mma_ts_chain<QS / 16>(tdV, tPt, dDn, idO, !first);
-        mma_ts_chain<QS / 16>(tdK, tdSt, dQn, idO, !first);
-        tc_commit(&q_empty[s]);
-        tc_commit(p_empty);
-        if (last) tc_commit(acc_full);
-      };
       int g = 0, it = 0;
-      bool prev = false, prev_first = false, prev_last = false;
       for (int r = 0;; r++, it++) {
         const int idx = snake_item(r);
         if (idx >= nitems) break;
@@ -660,13 +650,34 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           mma_hs_ss<Hs<HS>::KS>(tdPt, dV, 128, dD, QS, idS);
           if (j == nsub - 1) tc_commit(&kv_empty[kvb]);
           tc_commit(s_full);
-          if (prev) dvdk(g - 1, prev_first, prev_last);
-          prev = true;
-          prev_first = j == 0;
-          prev_last = j == nsub - 1;
         }
       }
-      if (prev) dvdk(g - 1, prev_first, prev_last);
+    }
+  } else if (warp == KV_CW + 2) {
+    // ---------------------------------------------------------------- gradient MMAs
+    // dV, dK (g) once P^T, dS^T (g) are in TMEM; a thread on another
+    // scheduler than the score MMAs' issuer, so that the two instruction
+    // streams compete with different elementwise warps for issue slots
+    if (lane == 0) {
+      const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
+      int g = 0;
+      for (int r = 0;; r++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int k0 = (idx / BH) * 128;
+        const int nsub = (T - k0 + QS - 1) / QS;
+        for (int j = 0; j < nsub; j++, g++) {
+          mbar_wait(p_full, (uint32_t)g & 1u, err);
+          tc_fence_after();
+          const int s = g % ST;
+          const uint64_t dQn = ndesc(smem_u32(sQ + s * QTILE), QS, 0), dDn = ndesc(smem_u32(sD + s * QTILE), QS, 0);
+          mma_ts_chain<QS / 16>(tdV, tPt, dDn, idO, j > 0);
+          mma_ts_chain<QS / 16>(tdK, tdSt, dQn, idO, j > 0);
+          tc_commit(&q_empty[s]);
+          tc_commit(p_empty);
+          if (j == nsub - 1) tc_commit(acc_full);
+        }
+      }
     }
   } else {
     // ---------------------------------------------------------------- elementwise warps
@@ -741,13 +752,14 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 // ============================================================ backward: dQ
 // Item (128-query block, b*h), 128-key blocks.  Warps 0..15 elementwise
 // (warps w, w+4, w+8, w+12 share lane quarter w % 4 = 32 query rows and
-// take 32 key columns each), warp 16 the MMA issuer, warp 17 the loader.
+// take 32 key columns each), warp 16 issues the score products, warp 17
+// loads, warp 18 issues the dQ products.
 //   S = q k^T, dP = dy v^T (M = 128 queries, N = 128 keys, K = HS);
 //   dS = P (dP - D) into TMEM; dQ += dS k (N = HS, K = 128 keys).
 // TMEM: S 0..127, dP 128..255, dS 256..319, dQ 320..320+HS-1.
 // smem: q, dy [QB] | K ring [KST] | V ring [2] | barriers.
 #define DQ_CW 16
-#define DQ_THREADS (DQ_CW * 32 + 64)
+#define DQ_THREADS (DQ_CW * 32 + 96)
 template <int HS>
 struct DqCfg {
   static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;
@@ -833,21 +845,10 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
   } else if (warp == DQ_CW) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- score MMAs
     if (lane == 0) {
       const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
-      const uint32_t idQ = tc_idesc_bf16(128, HS, false, true);
-      auto dq = [&](int gp, bool first, bool last) {  // dQ (+)= dS(gp) k(gp)
-        mbar_wait(p_full, (uint32_t)gp & 1u, err);
-        tc_fence_after();
-        const uint64_t dKn = ndesc(smem_u32(sK + (gp % KST) * TILE), 128, 0);
-        mma_ts_chain<8>(tdQ, tdS, dKn, idQ, !first);
-        tc_commit(&k_empty[gp % KST]);
-        tc_commit(ds_free);
-        if (last) tc_commit(dq_full);
-      };
       int g = 0, it = 0;
-      bool prev = false, prev_first = false, prev_last = false;
       for (int r = 0;; r++, it++) {
         const int idx = snake_item(r);
         if (idx >= nitems) break;
@@ -867,13 +868,30 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           tc_commit(&v_empty[vs]);
           if (j == nk - 1) tc_commit(&qd_empty[ib]);
           tc_commit(s_full);
-          if (prev) dq(g - 1, prev_first, prev_last);
-          prev = true;
-          prev_first = j == 0;
-          prev_last = j == nk - 1;
         }
       }
-      if (prev) dq(g - 1, prev_first, prev_last);
+    }
+  } else if (warp == DQ_CW + 2) {
+    // ---------------------------------------------------------------- dQ MMAs
+    // dQ (+)= dS(g) k(g) once dS(g) is in TMEM, from a thread on another
+    // scheduler than the score MMAs' issuer
+    if (lane == 0) {
+      const uint32_t idQ = tc_idesc_bf16(128, HS, false, true);
+      int g = 0;
+      for (int r = 0;; r++) {
+        const int idx = snake_item(r);
+        if (idx >= nitems) break;
+        const int nk = nqb - idx / BH;
+        for (int j = 0; j < nk; j++, g++) {
+          mbar_wait(p_full, (uint32_t)g & 1u, err);
+          tc_fence_after();
+          const uint64_t dKn = ndesc(smem_u32(sK + (g % KST) * TILE), 128, 0);
+          mma_ts_chain<8>(tdQ, tdS, dKn, idQ, j > 0);
+          tc_commit(&k_empty[g % KST]);
+          tc_commit(ds_free);
+          if (j == nk - 1) tc_commit(dq_full);
+        }
+      }
     }
   } else {
     // ---------------------------------------------------------------- elementwise warps
