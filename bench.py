@@ -35,6 +35,10 @@ tied head) with bf16 outputs: value = their total FLOPs / total time
 roofline against twice the measured bf16 peak (the nominal fp8 : bf16
 tensor ratio).
 
+--mode oracle times one full step of the CPU oracle on the tiny and
+char-level configurations and on GPT-2 124M at B=4, T=1024 (tokens/s per
+configuration, the host's CPU model and thread count); it uses no GPU.
+
 --mode decode measures generation with the key/value cache instead: GPT-2
 124M, B=16 sequences, a 512-token prompt per sequence run through one
 forward (the prefill), then one gpt2_decode_step per new token (temperature
@@ -653,15 +657,52 @@ def run_reference(args, w, world, rank):
     rate, cores, dt = oracle_sample_rate(w, B, T, args.steps, warmup=args.warmup)
     sample = ("per step: one full oracle training step (fwd+bwd+AdamW over all parameters) on B=%d, "
               "T=%d of the %s workload" % (B, T, args.workload))
+    model = "gpt2-124M" if w["L"] == 12 else ("gpt2-350M" if w["L"] == 24 else "gpt2-L%d" % w["L"])
     return dict(impl="reference", metric=METRIC, value=round(rate, 3), unit="tokens/s", n_gpus=world,
                 steps=args.steps, warmup=args.warmup, ms_per_step=round(dt / args.steps * 1000, 2),
                 higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f32",
                 data="synthetic: same token stream recipe and GPT-2 init as our arm",
-                config=dict(workload=args.workload, global_batch=w["B"], seq_len=w["T"],
-                            parallelism="CPU oracle, rank 0 only"),
+                config=dict(workload="%s-B%d-T%d" % (model, B, T), sample_of=args.workload, global_batch=B,
+                            seq_len=T, parallelism="CPU oracle, rank 0 only", cpu_model=cpu_model()),
                 cpu_baseline=dict(value=round(rate, 3), unit="tokens/s", kind="oracle", cores=cores,
                                   sample=sample),
                 e2e=dict(value=round(rate, 3), unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+# the method's configurations whose full steps the oracle runs (one step each)
+ORACLE_CONFIGS = {
+    "tiny-fp32 (L2 C64 NH4 T32 B4 V256)": dict(L=2, C=64, NH=4, V=256, Vp=256, maxT=32, B=4, T=32,
+                                              dist="uniform", lr=1e-4, wd=0.0),
+    "char (L8 C128 NH8 T64 B32 V1000)": dict(L=8, C=128, NH=8, V=1000, Vp=1000, maxT=64, B=32, T=64,
+                                            dist="zipf", lr=3e-4, wd=0.1),
+    "gpt2-124M-B4-T1024": WORKLOADS["gpt2-124M-B4-T1024"],
+}
+
+
+def run_oracle_timing(args):
+    """One full training step (fwd + bwd + AdamW) of the CPU oracle on each
+    configuration the oracle can finish: the tiny and char-level models and
+    GPT-2 124M at B=4, T=1024, with the host's CPU model and thread count."""
+    out = dict(mode="oracle", metric="CPU oracle training tokens/sec, one full step per configuration",
+               unit="tokens/s", cpu_model=cpu_model(), configs={})
+    for name, w in ORACLE_CONFIGS.items():
+        rate, cores, dt = oracle_sample_rate(w, w["B"], w["T"], 1)
+        out["configs"][name] = dict(tokens=w["B"] * w["T"], seconds=round(dt, 3), tokens_per_s=round(rate, 2),
+                                    flops_per_token=flops_per_token(w),
+                                    gflops_per_s=round(rate * flops_per_token(w) / 1e9, 2))
+        out["cores"] = cores
+    return out
 
 
 def main(argv=None):
@@ -672,7 +713,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["train", "decode", "fp8"], default="train")
+    ap.add_argument("--mode", choices=["train", "decode", "fp8", "oracle"], default="train")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -680,7 +721,9 @@ def main(argv=None):
     if world != args.gpus and world > 1:
         print("warning: WORLD_SIZE=%d but --gpus %d" % (world, args.gpus), file=sys.stderr)
     w = WORKLOADS[args.workload]
-    if args.mode == "decode" and args.impl == "ours":
+    if args.mode == "oracle":
+        out = run_oracle_timing(args) if rank == 0 else None
+    elif args.mode == "decode" and args.impl == "ours":
         out = run_decode(args, world, rank, local)
     elif args.mode == "fp8" and args.impl == "ours":
         out = run_fp8(args) if rank == 0 else None
