@@ -541,15 +541,21 @@ struct KvCfg {
   static constexpr uint32_t KTILE = Hs<HS>::NB * 16384u;                  // [128 x HS]
   static constexpr uint32_t QTILE = Hs<HS>::NB * (uint32_t)QS * 128u;     // [QS x HS]
   static constexpr int KVB = HS > 64 ? 1 : 2;
-  static constexpr int ST = 4;
-  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + 256;
+  // head size 64: dV and dK tiles ([128 x 64] bf16 each) leave through a
+  // shared-memory staging area and one TMA store each (three ring stages
+  // leave room for it); other head sizes store rows directly
+  static constexpr bool STAGE_OUT = HS == 64;
+  static constexpr int ST = STAGE_OUT ? 3 : 4;
+  static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 2 * 16384u : 0u;
+  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + OUT_BYTES + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                           const __grid_constant__ CUtensorMap tm_dy, bf16* dqkv, const float* lse,
-                           const float* dsum, int B, int T, int C, int NH, float scale, int* err) {
+                           const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_out,
+                           bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH, float scale,
+                           int* err) {
   using Cf = KvCfg<HS>;
   constexpr int QS = Cf::QS, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
   constexpr uint32_t KTILE = Cf::KTILE, QTILE = Cf::QTILE;
@@ -560,7 +566,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sQ = sV + KVB * KTILE;            // [ST]
   uint8_t* sD = sQ + ST * QTILE;             // dy [ST]
   float* sLD = reinterpret_cast<float*>(sD + ST * QTILE);  // [ST][lse QS, D QS]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + ST * 2 * QS);
+  uint8_t* sOut = reinterpret_cast<uint8_t*>(sLD + ST * 2 * QS);  // dV | dK staging (head size 64)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cf::OUT_BYTES);
   uint64_t* kv_full = bars;              // [KVB]
   uint64_t* kv_empty = kv_full + KVB;    // [KVB]: the item's last S^T, dP^T have read k, v
   uint64_t* q_full = kv_empty + KVB;     // [ST]
@@ -729,21 +736,52 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       constexpr int EH = HS / 2;
       const int which = cg >> 1, ch = cg & 1;  // which: 0 dV, 1 dK
       const float mul = which ? scale : 1.f;
-      constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
-      const int64_t C3 = 3 * (int64_t)C;
-#pragma unroll
-      for (int e = 0; e < EH; e += EC) {
-        uint32_t ra[EC];
-        tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, ra);
+      if constexpr (Cf::STAGE_OUT) {
+        // the 128 key rows x 32 columns of this warp into the 128B-swizzled
+        // staging tile (row = key, 16-byte chunks ch*4 .. ch*4+3), then one
+        // thread stores the dV and dK tiles with TMA (rows past T are not
+        // written); the staging area was read by the previous item's stores
+        // before anyone writes it again
+        uint32_t ra[32];
+        tmem_ld32((which ? tdK : tdV) + lb + ch * 32, ra);
+        if (tid == 0) bulk_wait_read0();
+        named_bar_sync(1, KV_CW * 32);
         tmem_ld_wait();
-        float v[EC];
+        uint8_t* rowp = sOut + which * 16384 + row * 128;
 #pragma unroll
-        for (int i = 0; i < EC; i++) v[i] = __uint_as_float(ra[i]);
-        if (key < T)
-          store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, mul);
+        for (int q = 0; q < 4; q++) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(ra[8 * q]) * mul, __uint_as_float(ra[8 * q + 1]) * mul);
+          u.y = pack_bf16(__uint_as_float(ra[8 * q + 2]) * mul, __uint_as_float(ra[8 * q + 3]) * mul);
+          u.z = pack_bf16(__uint_as_float(ra[8 * q + 4]) * mul, __uint_as_float(ra[8 * q + 5]) * mul);
+          u.w = pack_bf16(__uint_as_float(ra[8 * q + 6]) * mul, __uint_as_float(ra[8 * q + 7]) * mul);
+          *reinterpret_cast<uint4*>(rowp + (((ch * 4 + q) ^ (row & 7)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, KV_CW * 32);
+        if (tid == 0) {
+          tma_store_3d(&tm_out, sOut, 2 * C + h * HS, k0, b);        // dV
+          tma_store_3d(&tm_out, sOut + 16384, C + h * HS, k0, b);    // dK
+          bulk_commit();
+        }
+      } else {
+        constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
+        const int64_t C3 = 3 * (int64_t)C;
+#pragma unroll
+        for (int e = 0; e < EH; e += EC) {
+          uint32_t ra[EC];
+          tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, ra);
+          tmem_ld_wait();
+          float v[EC];
+#pragma unroll
+          for (int i = 0; i < EC; i++) v[i] = __uint_as_float(ra[i]);
+          if (key < T)
+            store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, mul);
+        }
       }
     }
   }
+  if (Cf::STAGE_OUT && tid == 0) bulk_wait0();  // the last item's stores are complete
   tc_fence_before();
   __syncthreads();
   if (warp == KV_CW) { tc_fence_after(); tmem_dealloc(tm, 512); }
@@ -766,13 +804,16 @@ struct DqCfg {
   static constexpr int QB = HS > 64 ? 1 : 2;
   static constexpr int KST = HS > 64 ? 2 : 3;
   static constexpr int VST = 2;
-  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + 256;
+  // head size 64: the dQ tile leaves through shared memory and one TMA store
+  static constexpr bool STAGE_OUT = HS == 64;
+  static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 16384u : 0u;
+  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + OUT_BYTES + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
-                          bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH,
+                          const __grid_constant__ CUtensorMap tm_out, bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH,
                           float scale, int* err) {
   using Cf = DqCfg<HS>;
   constexpr int QB = Cf::QB, KST = Cf::KST, VST = Cf::VST;
@@ -782,7 +823,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint8_t* sQ = sm;                     // [QB] x (q, dy)
   uint8_t* sK = sQ + QB * 2 * TILE;     // [KST]
   uint8_t* sV = sK + KST * TILE;        // [VST]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * TILE);
+  uint8_t* sOut = sV + VST * TILE;  // dQ staging (head size 64)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cf::OUT_BYTES);
   uint64_t* qd_full = bars;             // [QB]
   uint64_t* qd_empty = qd_full + QB;    // [QB]: the item's last S, dP have read q, dy
   uint64_t* k_full = qd_empty + QB;     // [KST]
@@ -951,6 +993,31 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       constexpr int EQ = HS / 4;
       uint32_t ra[EQ];
       tmem_ld_cols<EQ>(tdQ + lb + cg * EQ, ra);
+      if constexpr (Cf::STAGE_OUT) {
+        // 16 columns of the warp's 32 query rows into the 128B-swizzled
+        // staging tile (row = query, 16-byte chunks 2cg, 2cg+1), then one
+        // TMA store of the [128 x 64] tile (rows past T are not written)
+        if (tid == 0) bulk_wait_read0();  // the previous item's store has read the staging tile
+        named_bar_sync(1, DQ_CW * 32);
+        tmem_ld_wait();
+        uint8_t* rowp = sOut + row * 128;
+#pragma unroll
+        for (int qq = 0; qq < 2; qq++) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(ra[8 * qq]) * scale, __uint_as_float(ra[8 * qq + 1]) * scale);
+          u.y = pack_bf16(__uint_as_float(ra[8 * qq + 2]) * scale, __uint_as_float(ra[8 * qq + 3]) * scale);
+          u.z = pack_bf16(__uint_as_float(ra[8 * qq + 4]) * scale, __uint_as_float(ra[8 * qq + 5]) * scale);
+          u.w = pack_bf16(__uint_as_float(ra[8 * qq + 6]) * scale, __uint_as_float(ra[8 * qq + 7]) * scale);
+          *reinterpret_cast<uint4*>(rowp + (((cg * 2 + qq) ^ (row & 7)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, DQ_CW * 32);
+        if (tid == 0) {
+          tma_store_3d(&tm_out, sOut, h * HS, qb * 128, b);
+          bulk_commit();
+        }
+        continue;
+      }
       tmem_ld_wait();
       float v[EQ];
 #pragma unroll
@@ -967,6 +1034,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       }
     }
   }
+  if (Cf::STAGE_OUT && tid == 0) bulk_wait0();  // the last item's store is complete
   tc_fence_before();
   __syncthreads();
   if (warp == DQ_CW) { tc_fence_after(); tmem_dealloc(tm, 512); }
@@ -1004,9 +1072,10 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
                    float* dsum, int B, int T, int C, int NH) {
   using Kv = KvCfg<HS>;
   using Dq = DqCfg<HS>;
-  CUtensorMap tq, tq_s, td, td_s;
+  CUtensorMap tq, tq_s, td, td_s, tout;
   if (!make_tmap_btw(&tq, qkv, B, T, 3 * C, 128) || !make_tmap_btw(&td, dy, B, T, C, 128) ||
-      !make_tmap_btw(&tq_s, qkv, B, T, 3 * C, Kv::QS) || !make_tmap_btw(&td_s, dy, B, T, C, Kv::QS)) {
+      !make_tmap_btw(&tq_s, qkv, B, T, 3 * C, Kv::QS) || !make_tmap_btw(&td_s, dy, B, T, C, Kv::QS) ||
+      !make_tmap_btw(&tout, dqkv, B, T, 3 * C, 128)) {
     c.host_fail = 1;
     return;
   }
@@ -1017,10 +1086,10 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
   const int nitems = ((T + 127) / 128) * B * NH;
   const int grid = std::min(nitems, c.num_sms);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, dqkv, lse,
+  launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, tout, dqkv, lse,
              (const float*)dsum, B, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Dq::SMEM);
-  launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, dqkv, lse,
+  launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, tout, dqkv, lse,
              (const float*)dsum, B, T, C, NH, scale, c.err);
 }
 
