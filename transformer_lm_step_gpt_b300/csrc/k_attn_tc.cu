@@ -185,23 +185,27 @@ __device__ __forceinline__ int snake_item(int r) {
 // query rows, and take key columns 0..63 / 64..127 of a block and head dims
 // 0..HS/2-1 / HS/2..HS-1 of O), warp 8 the MMA issuer, warp 9 the loader.
 // TMEM: S 0..127, P 128..191 (bf16 pairs), O 192..192+HS-1.
-// smem: Q [2] | K ring [2] | V ring [2] | row-max exchange [2][2][128] |
-//       row-sum exchange [2][128] | barriers.
+// smem: Q [QB] | K ring [2] | V ring [2] | y staging (head size 64) |
+//       row-max exchange [2][2][128] | row-sum exchange [2][128] | barriers.
 #define FW_SOFT 8
 #define FW_THREADS (FW_SOFT * 32 + 64)
 template <int HS>
 struct FwdCfg {
   static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;  // [128 x HS]
-  static constexpr int QB = 2, KV = 2;
+  // head size 64: the y tile leaves through a shared-memory staging tile and
+  // one TMA store; to fit it next to a second CTA on the SM, one q buffer
+  static constexpr bool STAGE_OUT = HS == 64;
+  static constexpr int QB = STAGE_OUT ? 1 : 2, KV = 2;
   static constexpr int TMEM = HS > 64 ? 512 : 256;
   static constexpr int PER_SM = HS > 64 ? 1 : 2;
-  static constexpr uint32_t SMEM = 1024 + (QB + 2 * KV) * TILE + 2048 + 1024 + 256;
+  static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 16384u : 0u;
+  static constexpr uint32_t SMEM = 1024 + (QB + 2 * KV) * TILE + OUT_BYTES + 2048 + 1024 + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
-    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, bf16* y, float* lse, int B, int T,
-                       int C, int NH, float scale, int* err) {
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_y,
+                       bf16* y, float* lse, int B, int T, int C, int NH, float scale, int* err) {
   using Cf = FwdCfg<HS>;
   constexpr int QB = Cf::QB, KV = Cf::KV;
   constexpr uint32_t TILE = Cf::TILE;
@@ -210,7 +214,8 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
   uint8_t* sQ = sm;
   uint8_t* sK = sQ + QB * TILE;
   uint8_t* sV = sK + KV * TILE;
-  float* red = reinterpret_cast<float*>(sV + KV * TILE);  // [2][2][128]
+  uint8_t* sOut = sV + KV * TILE;                          // y staging (head size 64)
+  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);  // [2][2][128]
   float* lred = red + 512;                                 // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lred + 256);
   uint64_t* q_full = bars;             // [QB]
@@ -413,15 +418,40 @@ __global__ void __launch_bounds__(FW_THREADS, FwdCfg<HS>::PER_SM)
       lred[half * 128 + row] = l;
       named_bar_sync(1 + quarter, 64);
       const float lt = lred[row] + lred[128 + row];
-      if (q < T) {
+      if (q < T && half == 0) lse[(int64_t)bh * T + q] = -(m * sl2 + log2f(lt));  // minus lse, base-2 units
+      if constexpr (Cf::STAGE_OUT) {
+        // the warp's 32 rows x 32 columns into the 128B-swizzled staging
+        // tile (16-byte chunks 4 half .. 4 half + 3 of each row), then one
+        // TMA store of the [128 x 64] tile (rows past T are not written);
+        // the previous item's store has read the tile before it is rewritten
+        if (tid == 0) bulk_wait_read0();
+        named_bar_sync(5, FW_SOFT * 32);
+        const float inv = 1.f / lt;
+        uint8_t* rowp = sOut + row * 128;
+#pragma unroll
+        for (int qq = 0; qq < 4; qq++) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(o[8 * qq]) * inv, __uint_as_float(o[8 * qq + 1]) * inv);
+          u.y = pack_bf16(__uint_as_float(o[8 * qq + 2]) * inv, __uint_as_float(o[8 * qq + 3]) * inv);
+          u.z = pack_bf16(__uint_as_float(o[8 * qq + 4]) * inv, __uint_as_float(o[8 * qq + 5]) * inv);
+          u.w = pack_bf16(__uint_as_float(o[8 * qq + 6]) * inv, __uint_as_float(o[8 * qq + 7]) * inv);
+          *reinterpret_cast<uint4*>(rowp + (((half * 4 + qq) ^ (row & 7)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(5, FW_SOFT * 32);
+        if (tid == 0) {
+          tma_store_3d(&tm_y, sOut, h * HS, qb * 128, b);
+          bulk_commit();
+        }
+      } else if (q < T) {
         float v[OH];
 #pragma unroll
         for (int i = 0; i < OH; i++) v[i] = __uint_as_float(o[i]);
         store_bf16_row<OH>(y + ((int64_t)b * T + q) * C + h * HS + half * OH, v, 1.f / lt);
-        if (half == 0) lse[(int64_t)bh * T + q] = -(m * sl2 + log2f(lt));  // minus lse, base-2 units
       }
     }
   }
+  if (Cf::STAGE_OUT && tid == 0) bulk_wait0();  // the last item's store is complete
   tc_fence_before();
   __syncthreads();
   if (warp == 0) { tc_fence_after(); tmem_dealloc(tm, Cf::TMEM); }
@@ -1044,15 +1074,15 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
 template <int HS>
 static void fwd_hs(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T, int C, int NH) {
   using Cf = FwdCfg<HS>;
-  CUtensorMap tq;
-  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C, 128)) {
+  CUtensorMap tq, ty;
+  if (!make_tmap_btw(&tq, qkv, B, T, 3 * C, 128) || !make_tmap_btw(&ty, y, B, T, C, 128)) {
     c.host_fail = 1;
     return;
   }
   const int nitems = ((T + 127) / 128) * B * NH;
   const int grid = std::min(nitems, Cf::PER_SM * c.num_sms);
   cudaFuncSetAttribute(attn_fwd_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cf::SMEM);
-  launch_pdl(c, attn_fwd_tc_kernel<HS>, dim3(grid), dim3(FW_THREADS), Cf::SMEM, tq, y, lse, B, T, C, NH,
+  launch_pdl(c, attn_fwd_tc_kernel<HS>, dim3(grid), dim3(FW_THREADS), Cf::SMEM, tq, ty, y, lse, B, T, C, NH,
              1.f / sqrtf((float)HS), c.err);
 }
 
