@@ -282,8 +282,12 @@ size_t layout(gpt2_model* m, char* base) {
   m->datty = b.take<char>(M * C * a);
   m->dsum = b.take<float>((int64_t)m->B * m->NH * m->T);
   m->ln_partial = b.take<float>(ln_partial_floats(m->M, m->C));
-  m->cs_partial = b.take<float>(std::max<int64_t>(colsum_partial_floats(m->M, 4 * m->C),
-                                                  (int64_t)((m->M + 31) / 32) * 4 * m->C));
+  // column-sum partial rows: the fc bias gradient's (one per 32 rows of
+  // fcproj's data gradient), the colsum pass's, and the attention
+  // backward's qkv bias rows (one per batch row and 128-row block)
+  m->cs_partial = b.take<float>(std::max<int64_t>(
+      std::max<int64_t>(colsum_partial_floats(m->M, 4 * m->C), (int64_t)((m->M + 31) / 32) * 4 * m->C),
+      (int64_t)m->B * ((m->T + 127) / 128) * 3 * m->C));
   m->splitk_floats = m->bf ? 16 * C * C : 0;
   m->splitk = b.take<float>(m->splitk_floats);
   m->splitk_flag_count = m->bf ? 8192 : 0;
@@ -552,13 +556,15 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
-    // attention
+    // attention (at head size 64 the tensor-core path also leaves the qkv
+    // bias gradient's partial rows in cs_partial)
+    bool qkvb_partials = false;
     {
       ProfScope ps(m, PC_ATTN_BWD, attn_flop);
       if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
-      else launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
-                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                     lse, m->dsum, B, T, C, NH);
+      else qkvb_partials = launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
+                                                     reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
+                                                     lse, m->dsum, B, T, C, NH, m->cs_partial);
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
@@ -567,7 +573,10 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
     {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
-      launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+      if (qkvb_partials)
+        launch_colsum_reduce(c, m->G(QKVB) + (int64_t)l * 3 * C, m->cs_partial, B * ((T + 127) / 128), 3 * C);
+      else
+        launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);

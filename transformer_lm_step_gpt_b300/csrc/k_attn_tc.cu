@@ -44,9 +44,10 @@
 //   dQ       item (128-query block, b*h), 128-key blocks: S = q k^T, dP =
 //            dy v^T; dS into TMEM; dQ += dS k.
 // No atomics: every output element is written by one CTA, so the results
-// repeat bit for bit.  The qkv bias gradient (column sums of dqkv) is left
-// to a separate coalesced column-sum pass: summing columns across the 32
-// lanes of each warp in these epilogues cost more than re-reading dqkv.
+// repeat bit for bit.  At head size 64 the output tiles leave through
+// shared memory, where the epilogues also take their column sums (the qkv
+// bias gradient's partial rows); other head sizes leave the bias gradient
+// to a column-sum pass over dqkv.
 #include <cuda.h>
 
 #include <cstdio>
@@ -577,15 +578,16 @@ struct KvCfg {
   static constexpr bool STAGE_OUT = HS == 64;
   static constexpr int ST = STAGE_OUT ? 3 : 4;
   static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 2 * 16384u : 0u;
-  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + OUT_BYTES + 256;
+  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 2 * 8 * 64 * 4 : 0u;  // column-sum partials [2][8][64]
+  static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + OUT_BYTES + RED_BYTES + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                            const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_out,
-                           bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH, float scale,
-                           int* err) {
+                           bf16* dqkv, const float* lse, const float* dsum, float* bias_partial, int B, int T, int C,
+                           int NH, float scale, int* err) {
   using Cf = KvCfg<HS>;
   constexpr int QS = Cf::QS, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
   constexpr uint32_t KTILE = Cf::KTILE, QTILE = Cf::QTILE;
@@ -597,7 +599,8 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sD = sQ + ST * QTILE;             // dy [ST]
   float* sLD = reinterpret_cast<float*>(sD + ST * QTILE);  // [ST][lse QS, D QS]
   uint8_t* sOut = reinterpret_cast<uint8_t*>(sLD + ST * 2 * QS);  // dV | dK staging (head size 64)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cf::OUT_BYTES);
+  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);     // [2][8][64] column-sum partials
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + Cf::RED_BYTES);
   uint64_t* kv_full = bars;              // [KVB]
   uint64_t* kv_empty = kv_full + KVB;    // [KVB]: the item's last S^T, dP^T have read k, v
   uint64_t* q_full = kv_empty + KVB;     // [ST]
@@ -794,6 +797,35 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           tma_store_3d(&tm_out, sOut + 16384, C + h * HS, k0, b);    // dK
           bulk_commit();
         }
+        // the tiles' column sums over the block's key rows below T (one
+        // partial row of the qkv bias gradient per (batch row, key block)),
+        // read back from the staging tiles: warp w sums 16 rows of tile
+        // w / 8, lane l columns 2l and 2l + 1; the 8 row groups are then
+        // added in order
+        {
+          const int tt = warp >> 3, rg = warp & 7, c2 = 2 * lane;
+          const uint8_t* tile = sOut + tt * 16384;
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+          for (int r = rg * 16; r < rg * 16 + 16; r++) {
+            if (k0 + r < T) {
+              const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+              s0 += f.x;
+              s1 += f.y;
+            }
+          }
+          red[(tt * 8 + rg) * 64 + c2] = s0;
+          red[(tt * 8 + rg) * 64 + c2 + 1] = s1;
+          named_bar_sync(1, KV_CW * 32);
+          if (tid < 128) {
+            const int t2 = tid >> 6, col = tid & 63;
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; q++) sum += red[(t2 * 8 + q) * 64 + col];
+            bias_partial[((int64_t)b * nkb + kb) * 3 * (int64_t)C + (t2 ? C : 2 * C) + h * HS + col] = sum;
+          }
+        }
       } else {
         constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
         const int64_t C3 = 3 * (int64_t)C;
@@ -837,14 +869,15 @@ struct DqCfg {
   // head size 64: the dQ tile leaves through shared memory and one TMA store
   static constexpr bool STAGE_OUT = HS == 64;
   static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 16384u : 0u;
-  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + OUT_BYTES + 256;
+  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 16 * 64 * 4 : 0u;  // column-sum partials [16][64]
+  static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + OUT_BYTES + RED_BYTES + 256;
 };
 
 template <int HS>
 __global__ void __launch_bounds__(DQ_THREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_dy,
-                          const __grid_constant__ CUtensorMap tm_out, bf16* dqkv, const float* lse, const float* dsum, int B, int T, int C, int NH,
-                          float scale, int* err) {
+                          const __grid_constant__ CUtensorMap tm_out, bf16* dqkv, const float* lse, const float* dsum,
+                          float* bias_partial, int B, int T, int C, int NH, float scale, int* err) {
   using Cf = DqCfg<HS>;
   constexpr int QB = Cf::QB, KST = Cf::KST, VST = Cf::VST;
   constexpr uint32_t TILE = Cf::TILE;
@@ -854,7 +887,8 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint8_t* sK = sQ + QB * 2 * TILE;     // [KST]
   uint8_t* sV = sK + KST * TILE;        // [VST]
   uint8_t* sOut = sV + VST * TILE;  // dQ staging (head size 64)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sOut + Cf::OUT_BYTES);
+  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);  // [16][64] column-sum partials
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + Cf::RED_BYTES);
   uint64_t* qd_full = bars;             // [QB]
   uint64_t* qd_empty = qd_full + QB;    // [QB]: the item's last S, dP have read q, dy
   uint64_t* k_full = qd_empty + QB;     // [KST]
@@ -1046,6 +1080,32 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           tma_store_3d(&tm_out, sOut, h * HS, qb * 128, b);
           bulk_commit();
         }
+        // column sums of the tile over its query rows below T (one partial
+        // row of the qkv bias gradient per (batch row, query block)): warp w
+        // sums 8 rows, lane l columns 2l and 2l + 1, then the 16 row groups
+        // are added in order
+        {
+          const int c2 = 2 * lane;
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int r = warp * 8; r < warp * 8 + 8; r++) {
+            if (qb * 128 + r < T) {
+              const uint32_t u = *reinterpret_cast<const uint32_t*>(sOut + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+              s0 += f.x;
+              s1 += f.y;
+            }
+          }
+          red[warp * 64 + c2] = s0;
+          red[warp * 64 + c2 + 1] = s1;
+          named_bar_sync(1, DQ_CW * 32);
+          if (tid < 64) {
+            float sum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 16; q++) sum += red[q * 64 + tid];
+            bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * HS + tid] = sum;
+          }
+        }
         continue;
       }
       tmem_ld_wait();
@@ -1099,7 +1159,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 
 template <int HS>
 static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, const bf16* qkv, const float* lse,
-                   float* dsum, int B, int T, int C, int NH) {
+                   float* dsum, int B, int T, int C, int NH, float* bias_partial) {
   using Kv = KvCfg<HS>;
   using Dq = DqCfg<HS>;
   CUtensorMap tq, tq_s, td, td_s, tout;
@@ -1117,20 +1177,20 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
   const int grid = std::min(nitems, c.num_sms);
   cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
   launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, tout, dqkv, lse,
-             (const float*)dsum, B, T, C, NH, scale, c.err);
+             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Dq::SMEM);
   launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, tout, dqkv, lse,
-             (const float*)dsum, B, T, C, NH, scale, c.err);
+             (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
 }
 
-void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T,
-                               int C, int NH) {
+                               int C, int NH, float* bias_partial) {
   switch (C / NH) {
-    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
-    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
-    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
-    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH); break;
-    default: c.host_fail = 1;
+    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
+    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
+    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return true;
+    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
+    default: c.host_fail = 1; return false;
   }
 }

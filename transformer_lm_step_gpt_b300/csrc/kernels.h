@@ -197,9 +197,12 @@ int64_t attention_simt_scratch_floats(int B, int T_, int NH);
 void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T_,
                                int C, int NH);
 // qkv, y, dy -> dqkv [B,T,3C] (dq | dk | dv); dsum [B,NH,T] is scratch.
-void launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
+// Returns true when it also wrote the qkv bias gradient's partial rows
+// (head size 64): bias_partial [B * ceil(T/128)][3C], row b * ceil(T/128) +
+// block (launch_colsum_reduce adds them up).
+bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, int B, int T_,
-                               int C, int NH);
+                               int C, int NH, float* bias_partial);
 
 // A tensor map over a [B][T][W] bf16 tensor with box {64, rows, 1},
 // 128-byte swizzle, rows past T read as 0 (false if the driver's encoder is
