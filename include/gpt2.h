@@ -70,8 +70,10 @@ typedef enum { GPT2_FP32 = 0, GPT2_BF16 = 1 } gpt2_precision;
  *   channels % 8 == 0;
  *   head size channels/num_heads in {16, 32, 64, 128};
  *   vocab_size <= padded_vocab_size and padded_vocab_size % 8 == 0;
+ *   padded_vocab_size <= 262144 (token ids fit 18 bits);
  *   1 <= seq_len <= max_seq_len <= 4096; batch_size >= 1;
- *   batch_size * seq_len <= 32768. */
+ *   batch_size * seq_len <= 32768;
+ *   padded_vocab_size * batch_size * seq_len < 2^32. */
 typedef struct gpt2_config {
   int32_t max_seq_len;       /* maxT: rows of the position embedding          */
   int32_t vocab_size;        /* V: real vocabulary, the softmax's width       */

@@ -148,3 +148,11 @@ def test_noalloc_layernorm_backward_checks_arguments_without_gpu():
         bad = list(ptrs)
         bad[i] = p + 2
         assert call(bad) == -1, i
+
+
+def test_build_rejects_a_vocabulary_beyond_18_bit_token_ids():
+    # the encoder backward sorts positions by token id in two 9-bit radix
+    # passes, so Vp is capped at 2^18
+    with pytest.raises(tl.GPT2Error) as e:
+        tl.Model(1, 64, 1, 262152, 262152, 8, 1, 8, precision="bf16")
+    assert e.value.code == -1

@@ -635,6 +635,8 @@ int gpt2_build(const gpt2_config* cfg, uint64_t seed, gpt2_model** out) {
                 "gpt2_build: need L>=1, 8<=C<=1024, C%NH==0, C%8==0, head size in {16,32,64,128}");
   if (k.vocab_size < 1 || k.padded_vocab_size < k.vocab_size || k.padded_vocab_size % 8 != 0)
     return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need 1 <= V <= Vp and Vp % 8 == 0");
+  if (k.padded_vocab_size > (1 << 18))  // the encoder backward's radix sort takes 18-bit token ids
+    return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need Vp <= 262144");
   if (k.seq_len < 1 || k.seq_len > k.max_seq_len || k.max_seq_len > 4096 || k.batch_size < 1 ||
       (int64_t)k.batch_size * k.seq_len > 32768)
     return fail(nullptr, GPT2_ERR_ARG, "gpt2_build: need 1 <= T <= maxT <= 4096, B >= 1, B*T <= 32768");

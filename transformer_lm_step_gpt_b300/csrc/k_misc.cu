@@ -119,40 +119,106 @@ __global__ void encoder_bwd_wpe_kernel(float* dwpe, const float* dout, int B, in
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int t = (int)(idx / C), ch = (int)(idx % C);
     float s = 0.f;
-    for (int b = 0; b < B; b++) s += dout[((int64_t)b * T + t) * C + ch];
+#pragma unroll 8
+    for (int b = 0; b < B; b++) s += __ldg(dout + ((int64_t)b * T + t) * C + ch);  // loads issued ahead, added in b order
     dwpe[idx] += s;
   }
 }
 
-// Sort the keys tok*M + position (one block, bitonic sort in shared memory);
-// equal tokens end up adjacent, in position order.
-__global__ void encoder_sort_kernel(uint32_t* sorted, const int32_t* tok, int M, int Vp, int P) {
+// Sort the keys tok*M + position by token, stably (positions come in
+// increasing order, so equal tokens end up adjacent in position order):
+// one block, a least-significant-digit radix sort on the token in two
+// passes of 9 bits (tokens below 2^18).  In each pass warp w owns the
+// contiguous items [w*S, (w+1)*S) and walks them 32 at a time:
+//   1. per-warp digit counts (__match_any_sync groups the lanes of a digit);
+//   2. one exclusive scan over (digit, warp) in digit-major order gives each
+//      warp's first destination per digit;
+//   3. the same walk scatters each key to its warp's next slot for its
+//      digit (rank among equal digits of the round = lanes below it).
+// keys in `a`, the first pass writes `b`, the second writes `a` back.
+#define ES_THREADS 1024
+#define ES_WARPS (ES_THREADS / 32)
+#define ES_BITS 9
+#define ES_BINS (1 << ES_BITS)
+#define ES_MAX_ROUNDS 32  // 32 x 32 items per warp: M <= 32768
+__global__ void __launch_bounds__(ES_THREADS, 1)
+    encoder_sort_kernel(uint32_t* a, uint32_t* b, const int32_t* tok, int M, int Vp) {
   pdl_trigger();
   pdl_wait();
-  extern __shared__ uint32_t keys[];
-  for (int i = threadIdx.x; i < P; i += blockDim.x) {
-    uint32_t k = 0xFFFFFFFFu;
-    if (i < M) {
-      int id = tok[i];
-      id = id < 0 ? 0 : (id >= Vp ? Vp - 1 : id);
-      k = (uint32_t)id * (uint32_t)M + (uint32_t)i;
-    }
-    keys[i] = k;
+  extern __shared__ int es_cnt[];  // [ES_BINS][ES_WARPS], digit-major
+  __shared__ int es_sums[ES_THREADS];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < M; i += ES_THREADS) {
+    int id = tok[i];
+    id = id < 0 ? 0 : (id >= Vp ? Vp - 1 : id);
+    a[i] = (uint32_t)id * (uint32_t)M + (uint32_t)i;
   }
   __syncthreads();
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = (lo & size) == 0;
-        const uint32_t a = keys[lo], b = keys[hi];
-        if ((a > b) == up) { keys[lo] = b; keys[hi] = a; }
-      }
-      __syncthreads();
+  const int S = (M + ES_WARPS - 1) / ES_WARPS;  // <= 1024 items per warp (M <= 32768)
+  const int w0 = warp * S, w1 = min(M, w0 + S);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int pass = 0; pass < 2; pass++) {
+    const uint32_t* src = pass ? b : a;
+    uint32_t* dst = pass ? a : b;
+    const int shift = pass * ES_BITS;
+    // the warp's keys in registers: round r's key of lane l is item w0 + 32r + l
+    uint32_t key[ES_MAX_ROUNDS];
+#pragma unroll
+    for (int r = 0; r < ES_MAX_ROUNDS; r++) {
+      const int i = w0 + 32 * r + lane;
+      key[r] = i < w1 ? src[i] : 0xFFFFFFFFu;
     }
+    for (int i = threadIdx.x; i < ES_BINS * ES_WARPS; i += ES_THREADS) es_cnt[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < ES_MAX_ROUNDS; r++) {
+      if (w0 + 32 * r >= w1) break;  // warp-uniform
+      const bool on = w0 + 32 * r + lane < w1;
+      const uint32_t d = on ? ((key[r] / (uint32_t)M) >> shift) & (ES_BINS - 1) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (on && (peers & lt) == 0) es_cnt[d * ES_WARPS + warp] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // exclusive scan of the ES_BINS * ES_WARPS counts, 16 per thread
+    {
+      constexpr int PER = ES_BINS * ES_WARPS / ES_THREADS;
+      int run = 0;
+#pragma unroll
+      for (int k = 0; k < PER; k++) run += es_cnt[threadIdx.x * PER + k];
+      es_sums[threadIdx.x] = run;
+      __syncthreads();
+      for (int off = 1; off < ES_THREADS; off <<= 1) {  // inclusive scan of the thread totals
+        const int t = threadIdx.x >= off ? es_sums[threadIdx.x - off] : 0;
+        __syncthreads();
+        es_sums[threadIdx.x] += t;
+        __syncthreads();
+      }
+      int base = es_sums[threadIdx.x] - run;
+#pragma unroll
+      for (int k = 0; k < PER; k++) {
+        const int v = es_cnt[threadIdx.x * PER + k];
+        es_cnt[threadIdx.x * PER + k] = base;
+        base += v;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < ES_MAX_ROUNDS; r++) {
+      if (w0 + 32 * r >= w1) break;
+      const bool on = w0 + 32 * r + lane < w1;
+      const uint32_t d = on ? ((key[r] / (uint32_t)M) >> shift) & (ES_BINS - 1) : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, d);
+      if (on) {
+        const int base = es_cnt[d * ES_WARPS + warp];
+        dst[base + __popc(peers & lt)] = key[r];
+      }
+      __syncwarp();
+      if (on && (peers & lt) == 0) es_cnt[d * ES_WARPS + warp] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
   }
-  for (int i = threadIdx.x; i < M; i += blockDim.x) sorted[i] = keys[i];
 }
 
 __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_t key) {
@@ -165,59 +231,141 @@ __device__ __forceinline__ int lower_bound_u32(const uint32_t* a, int n, uint32_
 }
 
 #define ENC_PIECE 64
-// One block per sorted index; blocks at a piece start (segment start, or 64
-// rows into a segment) sum their piece's rows in order.  Single-piece
-// segments add straight into dwte; longer ones leave a partial per piece.
+#define ENC_RANGE 64  // sorted indices per block
+// Block b looks at the sorted indices [64b, 64b+64): those that start a
+// piece (a segment start, or 64 rows into a segment) sum their piece's rows
+// in order, one warp per piece.  Single-piece segments add straight into
+// dwte; longer ones leave a partial per piece.
 __global__ void encoder_bwd_piece_kernel(float* dwte, float* partial, const float* dout,
                                          const uint32_t* sorted, int M, int C) {
   pdl_trigger();
   pdl_wait();
-  const int i = blockIdx.x;
-  const uint32_t key = sorted[i];
-  const uint32_t id = key / (uint32_t)M;
-  const int seg0 = lower_bound_u32(sorted, M, id * (uint32_t)M);
-  if ((i - seg0) % ENC_PIECE != 0) return;
-  const int seg1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
-  const int end = min(seg1, i + ENC_PIECE);
-  const int C4 = C / 4;
-  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) {
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = i; j < end; j++) {
-      const uint32_t pos = sorted[j] % (uint32_t)M;
-      const float4 v = reinterpret_cast<const float4*>(dout + (int64_t)pos * C)[c4];
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  __shared__ int starts[ENC_RANGE];
+  __shared__ int seg_lo[ENC_RANGE], seg_hi[ENC_RANGE];
+  __shared__ int nstart;
+  const int i0 = blockIdx.x * ENC_RANGE;
+  if (threadIdx.x == 0) nstart = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    for (int k = threadIdx.x; k < ENC_RANGE; k += 32) {  // two rounds of 32, in index order
+      const int i = i0 + k;
+      bool is_start = false;
+      int s0 = 0, s1 = 0;
+      if (i < M) {
+        const uint32_t id = sorted[i] / (uint32_t)M;
+        s0 = lower_bound_u32(sorted, M, id * (uint32_t)M);
+        is_start = (i - s0) % ENC_PIECE == 0;
+        if (is_start) s1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
+      }
+      const uint32_t ball = __ballot_sync(0xffffffffu, is_start);
+      const int slot = nstart + __popc(ball & ((1u << threadIdx.x) - 1u));
+      if (is_start) {
+        starts[slot] = i;
+        seg_lo[slot] = s0;
+        seg_hi[slot] = s1;
+      }
+      __syncwarp();
+      if (threadIdx.x == 0) nstart += __popc(ball);
+      __syncwarp();
     }
-    if (seg1 - seg0 <= ENC_PIECE) {
-      float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
-      float4 o = *d;
-      o.x += s.x; o.y += s.y; o.z += s.z; o.w += s.w;
-      *d = o;
-    } else {
-      reinterpret_cast<float4*>(partial + (int64_t)i * C)[c4] = s;
+  }
+  __syncthreads();
+  const int C4 = C / 4, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int p = warp; p < nstart; p += nwarps) {  // one warp per piece
+    const int i = starts[p], s0 = seg_lo[p], s1 = seg_hi[p];
+    const int end = min(s1, i + ENC_PIECE);
+    const uint32_t id = sorted[i] / (uint32_t)M;
+    // lane l holds the 16-byte columns l, l + 32, ... (C <= 1024: at most 8);
+    // a row's loads are all issued before its additions, rows in order
+    float4 s[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) s[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+    for (int j = i; j < end; j++) {
+      const float4* row = reinterpret_cast<const float4*>(dout + (int64_t)(sorted[j] % (uint32_t)M) * C);
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++) v[k] = lane + 32 * k < C4 ? __ldg(row + lane + 32 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; k++) { s[k].x += v[k].x; s[k].y += v[k].y; s[k].z += v[k].z; s[k].w += v[k].w; }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const int c4 = lane + 32 * k;
+      if (c4 >= C4) break;
+      if (s1 - s0 <= ENC_PIECE) {
+        float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
+        float4 o = *d;
+        o.x += s[k].x; o.y += s[k].y; o.z += s[k].z; o.w += s[k].w;
+        *d = o;
+      } else {
+        reinterpret_cast<float4*>(partial + (int64_t)i * C)[c4] = s[k];
+      }
     }
   }
 }
 
+// Block b: the segments that start in [64b, 64b+64) and have more than one
+// piece add their pieces' partials in order into dwte.
 __global__ void encoder_bwd_combine_kernel(float* dwte, const float* partial,
                                            const uint32_t* sorted, int M, int C) {
   pdl_trigger();
   pdl_wait();
-  const int i = blockIdx.x;
-  const uint32_t id = sorted[i] / (uint32_t)M;
-  if (i > 0 && sorted[i - 1] / (uint32_t)M == id) return;  // not a segment start
-  const int seg1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
-  if (seg1 - i <= ENC_PIECE) return;
-  const int C4 = C / 4;
-  for (int c4 = threadIdx.x; c4 < C4; c4 += blockDim.x) {
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = i; j < seg1; j += ENC_PIECE) {
-      const float4 v = reinterpret_cast<const float4*>(partial + (int64_t)j * C)[c4];
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  __shared__ int starts[ENC_RANGE], ends[ENC_RANGE];
+  __shared__ int nstart;
+  const int i0 = blockIdx.x * ENC_RANGE;
+  if (threadIdx.x == 0) nstart = 0;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    for (int k = threadIdx.x; k < ENC_RANGE; k += 32) {
+      const int i = i0 + k;
+      bool take = false;
+      int s1 = 0;
+      if (i < M) {
+        const uint32_t id = sorted[i] / (uint32_t)M;
+        if (i == 0 || sorted[i - 1] / (uint32_t)M != id) {
+          s1 = lower_bound_u32(sorted, M, (id + 1) * (uint32_t)M);
+          take = s1 - i > ENC_PIECE;
+        }
+      }
+      const uint32_t ball = __ballot_sync(0xffffffffu, take);
+      const int slot = nstart + __popc(ball & ((1u << threadIdx.x) - 1u));
+      if (take) {
+        starts[slot] = i;
+        ends[slot] = s1;
+      }
+      __syncwarp();
+      if (threadIdx.x == 0) nstart += __popc(ball);
+      __syncwarp();
     }
-    float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
-    float4 o = *d;
-    o.x += s.x; o.y += s.y; o.z += s.z; o.w += s.w;
-    *d = o;
+  }
+  __syncthreads();
+  const int C4 = C / 4, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  for (int p = warp; p < nstart; p += nwarps) {  // one warp per segment
+    const int i = starts[p], s1 = ends[p];
+    const uint32_t id = sorted[i] / (uint32_t)M;
+    float4 s[8];
+#pragma unroll
+    for (int k = 0; k < 8; k++) s[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = i; j < s1; j += ENC_PIECE) {  // the pieces' partials, in order
+      const float4* row = reinterpret_cast<const float4*>(partial + (int64_t)j * C);
+      float4 v[8];
+#pragma unroll
+      for (int k = 0; k < 8; k++) v[k] = lane + 32 * k < C4 ? row[lane + 32 * k] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; k++) { s[k].x += v[k].x; s[k].y += v[k].y; s[k].z += v[k].z; s[k].w += v[k].w; }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+      const int c4 = lane + 32 * k;
+      if (c4 >= C4) break;
+      float4* d = reinterpret_cast<float4*>(dwte + (int64_t)id * C) + c4;
+      float4 o = *d;
+      o.x += s[k].x; o.y += s[k].y; o.z += s[k].z; o.w += s[k].w;
+      *d = o;
+    }
   }
 }
 
@@ -230,14 +378,14 @@ void launch_encoder_bwd(LaunchCtx& c, float* dwte, float* dwpe, const float* dou
     int grid = (int)std::min<int64_t>(cdiv(n, 256), (int64_t)c.num_sms * 8);
     launch_pdl(c, encoder_bwd_wpe_kernel, dim3(grid), dim3(256), 0, dwpe, dout, B, T, C);
   }
-  int P = 1;
-  while (P < M) P <<= 1;
-  const size_t smem = (size_t)P * sizeof(uint32_t);
+  // the sort's second key buffer borrows the head of the piece partials,
+  // which are written only after the sort
+  const size_t smem = (size_t)ES_BINS * ES_WARPS * sizeof(int);
   cudaFuncSetAttribute(encoder_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  launch_pdl(c, encoder_sort_kernel, dim3(1), dim3(1024), smem, sorted, tok, M, Vp, P);
-  const int threads = std::min(1024, std::max(32, ((C / 4) + 31) / 32 * 32));
-  launch_pdl(c, encoder_bwd_piece_kernel, dim3(M), dim3(threads), 0, dwte, partial, dout, sorted, M, C);
-  launch_pdl(c, encoder_bwd_combine_kernel, dim3(M), dim3(threads), 0, dwte, partial, sorted, M, C);
+  launch_pdl(c, encoder_sort_kernel, dim3(1), dim3(ES_THREADS), smem, sorted, reinterpret_cast<uint32_t*>(partial),
+             tok, M, Vp);
+  launch_pdl(c, encoder_bwd_piece_kernel, dim3(cdiv(M, ENC_RANGE)), dim3(256), 0, dwte, partial, dout, sorted, M, C);
+  launch_pdl(c, encoder_bwd_combine_kernel, dim3(cdiv(M, ENC_RANGE)), dim3(256), 0, dwte, partial, sorted, M, C);
 }
 
 // ============================================================ LayerNorm
