@@ -391,10 +391,10 @@ GPT2_API const char* gpt2_last_error(const gpt2_model* m);
  * vectors), mean and rstd on 4-byte ones; otherwise GPT2_ERR_ARG.
  * Ordering: the call's first kernel starts only after all work enqueued
  * before it on cuda_stream has finished (no programmatic overlap).
- * Scratch: the partial sums, at most ceil(N/64) * 8 * 3 * C floats, live in one
+ * Scratch: the partial sums, at most ceil(N/64) * 3 * C floats, live in one
  * file-scope __device__ array of 2^21 floats (8 MiB) that every GPU which
  * loads the library holds until the process exits.  Larger sizes are
- * rejected with GPT2_ERR_ARG (N * C must stay below about 5.59 million);
+ * rejected with GPT2_ERR_ARG (N * C must stay below about 44.7 million);
  * also GPT2_ERR_ARG for a NULL input/output or C outside [4, 1024] or
  * C % 4 != 0, GPT2_ERR_CUDA if a launch fails; gpt2_last_error(NULL) has
  * the text.  Every call on a device shares the array and leaves the last

@@ -517,8 +517,8 @@ template void launch_layernorm_fwd<bf16>(LaunchCtx&, bf16*, float*, float*, cons
 #define LNB_STAGES 2        // rows in flight per warp
 #define LNB_ROWS_PER_BLOCK 64  // rows per block at least (grid sizing)
 
-// partial rows: at most one per warp of a grid of cdiv(N, 64) blocks
-int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS_PER_BLOCK) * LNB_WARPS * 3 * C; }
+// partial rows: one per block of a grid of at most cdiv(N, 64) blocks
+int64_t ln_partial_floats(int N, int C) { return (int64_t)cdiv(N, LNB_ROWS_PER_BLOCK) * 3 * C; }
 
 static size_t lnb_smem(int C) {
   return (size_t)LNB_WARPS * LNB_STAGES * 3 * C * sizeof(float) + LNB_WARPS * LNB_STAGES * sizeof(uint64_t);
@@ -530,8 +530,9 @@ static size_t lnb_smem(int C) {
 // rows' loads are in flight while this one is processed from shared memory.
 // Lane l owns the float4 column chunks l, l+32, ... (NCH = C/128 of them)
 // and keeps its gamma / beta / residual-gradient column partials in
-// registers across all of the warp's rows, then writes them as the warp's
-// own partial row; reduce_partials_kernel adds the partial rows in order.
+// registers across all of the warp's rows; the block adds its warps'
+// partials in warp order into one partial row, and reduce_partials_kernel
+// adds the blocks' rows in order.
 //   xhat = (x - mean) rstd, g = dy * gamma,
 //   dx = rstd (g - mean(g) - xhat mean(g xhat)),  dres (+)= dx.
 template <typename ActT, int NCH>
@@ -628,15 +629,30 @@ __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
     m = mn;
     r = rn;
   }
-  float* out = partial + (int64_t)gw * 3 * C;
+  // the block's partial row: each warp leaves its column partials in its own
+  // (now idle) ring area, then the block adds the 8 warps' rows in warp
+  // order (a fixed order) and writes one row of 3C
+  float* mine = ring;
 #pragma unroll
   for (int k = 0; k < NCH; k++) {
     const int c = (lane + 32 * k) * 4;
     if (c < C) {
-      *reinterpret_cast<float4*>(out + c) = pw[k];
-      *reinterpret_cast<float4*>(out + C + c) = pb[k];
-      *reinterpret_cast<float4*>(out + 2 * C + c) = pr[k];
+      *reinterpret_cast<float4*>(mine + c) = pw[k];
+      *reinterpret_cast<float4*>(mine + C + c) = pb[k];
+      *reinterpret_cast<float4*>(mine + 2 * C + c) = pr[k];
     }
+  }
+  __syncthreads();
+  const float* rings = reinterpret_cast<const float*>(lnb_sm);
+  float* out = partial + (int64_t)blockIdx.x * 3 * C;
+  for (int c = threadIdx.x * 4; c < 3 * C; c += LNB_WARPS * 32 * 4) {
+    float4 t = *reinterpret_cast<const float4*>(rings + c);
+#pragma unroll
+    for (int w2 = 1; w2 < LNB_WARPS; w2++) {
+      const float4 u = *reinterpret_cast<const float4*>(rings + (size_t)w2 * LNB_STAGES * 3 * C + c);
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    *reinterpret_cast<float4*>(out + c) = t;
   }
 }
 
@@ -683,9 +699,8 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
                           float* dres_colsum, const float* dy, const float* inp, const float* w,
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial) {
-  int nb = cdiv(N, LNB_ROWS_PER_BLOCK);  // partial rows nb * LNB_WARPS <= ln_partial_floats / (3C)
+  int nb = cdiv(N, LNB_ROWS_PER_BLOCK);  // one partial row per block: nb <= ln_partial_floats / (3C)
   if (c.num_sms > 0) nb = std::min(nb, c.num_sms);
-  const int nparts = nb * LNB_WARPS;
   switch ((C + 127) / 128) {  // C <= 1024 (checked by the callers): partials in registers
     case 1: ln_bwd_launch<ActT, 1>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
     case 2: ln_bwd_launch<ActT, 2>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
@@ -696,7 +711,7 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
     case 7: ln_bwd_launch<ActT, 7>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
     default: ln_bwd_launch<ActT, 8>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
   }
-  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nparts, 3 * C, C);
+  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nb, 3 * C, C);
 }
 template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
                                           const float*, const float*, const float*, const float*,
@@ -944,7 +959,7 @@ void launch_adamw(LaunchCtx& c, float* p, const float* g, float* m, float* v, bf
 // ============================================================ allocation-free LayerNorm backward
 // gpt2_layernorm_backward_noalloc: the LayerNorm backward above for callers
 // that cannot allocate device memory.  Its partial sums (at most
-// ceil(N/64)*8 rows of 3*C floats) live in this file-scope array instead of caller- or
+// ceil(N/64) rows of 3*C floats) live in this file-scope array instead of caller- or
 // model-owned scratch; every GPU that loads the library holds it until the
 // process exits.  Its bounded waits report into g_noalloc_err, which
 // gpt2_noalloc_check reads and clears.
@@ -1001,8 +1016,8 @@ extern "C" int gpt2_layernorm_backward_noalloc(float* dinp, float* dweight, floa
   }
   const int64_t need = ln_partial_floats(N, C);
   if (need > NOALLOC_SCRATCH_FLOATS) {
-    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/64)*8*3*C exceeds the 2^21-float "
-                     "static scratch (N*C must stay below about 5.59 million)");
+    set_global_error("gpt2_layernorm_backward_noalloc: ceil(N/64)*3*C exceeds the 2^21-float "
+                     "static scratch (N*C must stay below about 44.7 million)");
     return GPT2_ERR_ARG;
   }
   int dev = 0;
