@@ -274,8 +274,13 @@ LONG1024 = (1, 128, 2, 1000, 1000, 1024, 4, 1024)
 # T = 4096, one sequence, head size 64: 64 key blocks of 64 per query row
 LONG4096 = (1, 128, 2, 1000, 1000, 4096, 1, 4096)
 # C = 1024, 16 heads (the 350M layer): the LayerNorm kernels' widest rows and
-# every 350M matmul shape, with K = 4096 weight gradients split 6 ways
+# every 350M matmul shape; the attproj weight gradient (4 x 4 tiles of 256 on
+# CTA pairs) splits K = 4096 four ways, reduced inside the matmul in split order
 WIDE1024 = (1, 1024, 16, 1000, 1000, 1024, 4, 1024)
+# C = 256, 4 heads: every weight gradient runs on CTA pairs with one to four
+# 256 x 256 tiles, so K = 4096 splits 8 ways into partial planes that the
+# split-order kernel adds up (the path of the 124M attproj weight gradient)
+MID1024 = (1, 256, 4, 1000, 1000, 1024, 4, 1024)
 
 
 @pytest.mark.parametrize("prec", ["fp32", "bf16"])
@@ -295,6 +300,11 @@ def test_longest_sequence_whole_step(prec):
 def test_widest_layer_whole_step(prec):
     res = run_steps(WIDE1024, prec, 1, 6e-4, 0.9, 0.999, 1e-8, 0.1, "uniform", seed=17)
     assert_parity(res, WIDE1024, prec)
+
+
+def test_pair_split_planes_whole_step():
+    res = run_steps(MID1024, "bf16", 1, 6e-4, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=18)
+    assert_parity(res, MID1024, "bf16")
 
 
 # ---- the edges of what the build accepts (head sizes 32 and 128, single-token

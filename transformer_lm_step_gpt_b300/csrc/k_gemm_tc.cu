@@ -1128,7 +1128,14 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   const int k_tiles = (g.K + TC_BK - 1) / TC_BK;
   int splits = 1;
   if (g.epi == EPI_ACCUM && g.splitk_scratch && tiles < c.num_sms) {
-    splits = std::max(1, std::min((2 * c.num_sms) / tiles, k_tiles / 8));
+    if (BN == 256) {
+      // CTA pairs: as many splits as keep every pair busy in one wave (the
+      // fewest hand-offs for the same balance)
+      const int pair_tiles = ((g.N + PAIR_BN - 1) / PAIR_BN) * ((g.M + 2 * TC_BM - 1) / (2 * TC_BM));
+      splits = std::max(1, std::min((c.num_sms / 2) / pair_tiles, k_tiles / 8));
+    } else {
+      splits = std::max(1, std::min((2 * c.num_sms) / tiles, k_tiles / 8));
+    }
     while (splits > 1 && (int64_t)splits * g.M * g.N > g.splitk_scratch_floats) splits--;
   }
   float* partial = splits > 1 ? g.splitk_scratch : nullptr;
