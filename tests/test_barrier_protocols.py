@@ -18,14 +18,14 @@ from protocol_sim import Sim, find
 
 # warps and ring stages as the kernels are compiled (head size 64): 8
 # softmax warps, 2 query buffers and 2-stage key / value rings (forward);
-# 16 elementwise warps, 2 key/value buffers and a 4-stage query ring
-# (dK/dV); 16 elementwise warps, 2 query buffers, 3 key and 2 value stages
+# 16 elementwise warps, 2 key/value buffers and a 3-stage query ring
+# (dK/dV); 16 elementwise warps, 2 query buffers, 5 key and 3 value stages
 # (dQ).  A CTA walks a list of work items; ITEMS are the item lengths (key
 # or query blocks) of the lists tried, longest first as the kernels order
 # them.
 FWD_WARPS, FWD_QB, FWD_KV = 8, 2, 2
-DKV_WARPS, DKV_KVB, DKV_STAGES = 16, 2, 4
-DQ_WARPS, DQ_QB, DQ_KST, DQ_VST = 16, 2, 3, 2
+DKV_WARPS, DKV_KVB, DKV_STAGES = 16, 2, 3
+DQ_WARPS, DQ_QB, DQ_KST, DQ_VST = 16, 2, 5, 3
 ITEMS = [[1], [3], [8, 5, 2], [4, 4, 1, 1], [2, 1, 1, 1, 1], [16, 9]]
 
 
@@ -145,9 +145,12 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
     interleave with the score issuer's in any order): dV, dK(g) from
     P^T, dS^T(g); an item's last one also commits the accumulators'
     completion.
-    Elementwise warps: copy S^T, dP^T out; (staged) wait for the stage's
-    lse / D; P^T, dS^T into tensor memory once dV, dK(g - 1) have read them;
-    dV, dK read at the end of each item."""
+    Elementwise warps, in two halves of a sub-block's columns: copy one
+    half of S^T, dP^T out, (staged) wait for the stage's lse / D, write its
+    P^T, dS^T once dV, dK(g - 1) have read them; then the other half, after
+    which S^T, dP^T are free.  An item's dV, dK are read one item late, in
+    the next item's first sub-block before its gradient products are
+    released (and the last item's after the loop)."""
     sim = Sim(seed, plant)
     for i in range(kvb):
         sim.bar("kvf%d" % i)
@@ -211,13 +214,13 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
     def compute():
         g = 0
         for it, nsub in enumerate(items):
-            for _ in range(nsub):
+            for j in range(nsub):
                 s = g % stages
                 yield from sim.wait("sf", g)
+                # two halves: each read, computed and written before the next
                 t0 = sim.t
-                yield from sim.work(1, 3)
+                yield from sim.work(1, 2)
                 sim.touch("warp", "r", t0, "St", "dPt")
-                sim.arrive("sfree", phase=g)
                 if staged:  # the stage's lse / D arrive with its q / dy tiles
                     yield from sim.wait("qf%d" % s, g // stages)
                 t1 = sim.t
@@ -227,14 +230,34 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
                 if g > 0 and plant != "p_overwrite_unguarded":
                     yield from sim.wait("pe", g - 1)
                 t2 = sim.t
-                yield from sim.work(1, 3)
+                yield from sim.work(1, 2)
                 sim.touch("warp", "w", t2, "Pt", "dSt")
+                t3 = sim.t
+                yield from sim.work(1, 2)
+                sim.touch("warp", "r", t3, "St", "dPt")
+                sim.arrive("sfree", phase=g)
+                t4 = sim.t
+                yield from sim.work(1, 2)
+                sim.touch("warp", "w", t4, "Pt", "dSt")
+                if j == 0 and it > 0 and plant != "epi_late":
+                    # the previous item's dV, dK read before this item's
+                    # first gradient products overwrite them
+                    yield from sim.wait("acc", it - 1)
+                    t5 = sim.t
+                    yield from sim.work(1, 2)
+                    sim.touch("warp", "r", t5, "dV", "dK")
                 sim.arrive("pf", phase=g)
+                if j == 0 and it > 0 and plant == "epi_late":
+                    yield from sim.wait("acc", it - 1)
+                    t5 = sim.t
+                    yield from sim.work(1, 2)
+                    sim.touch("warp", "r", t5, "dV", "dK")
                 g += 1
-            yield from sim.wait("acc", it)
-            t3 = sim.t
+        if items:  # the last item's accumulators
+            yield from sim.wait("acc", len(items) - 1)
+            t6 = sim.t
             yield from sim.work(1, 3)
-            sim.touch("warp", "r", t3, "dV", "dK")
+            sim.touch("warp", "r", t6, "dV", "dK")
 
     sim.run([loader(), score_mma(), grad_mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
@@ -249,8 +272,11 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
     once the warps have copied out S(g - 1), dP(g - 1).  dQ issuer
     (another thread): dQ(g) from dS(g) (an item's last one also commits
     dQ's completion).
-    Elementwise warps: copy S, dP out; dS into tensor memory once dQ(g - 1)
-    has read it; dQ read at the end of each item."""
+    Elementwise warps, in two halves of a block's columns: copy one half
+    of S, dP out, write its dS once dQ(g - 1) has read dS; then the other
+    half, after which S, dP are free.  An item's dQ is read one item late,
+    in the next item's first block before its dQ products are released
+    (and the last item's after the loop)."""
     sim = Sim(seed, plant)
     for i in range(qb):
         sim.bar("qf%d" % i)
@@ -318,25 +344,40 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
     def compute():
         g = 0
         for it, nk in enumerate(items):
-            for _ in range(nk):
+            for j in range(nk):
                 yield from sim.wait("sf", g)
+                # two halves: each read, computed and its dS written before the next
                 t0 = sim.t
-                yield from sim.work(1, 3)
+                yield from sim.work(1, 2)
                 sim.touch("warp", "r", t0, "S", "dP")
-                sim.arrive("sfree", phase=g)
                 yield from sim.work()
                 if g > 0:
                     k = g - 1 if plant != "ds_wrong_phase" else g
                     yield from sim.wait("dsf", k)
                 t1 = sim.t
-                yield from sim.work(1, 3)
+                yield from sim.work(1, 2)
                 sim.touch("warp", "w", t1, "dS")
+                t2 = sim.t
+                yield from sim.work(1, 2)
+                sim.touch("warp", "r", t2, "S", "dP")
+                sim.arrive("sfree", phase=g)
+                t3 = sim.t
+                yield from sim.work(1, 2)
+                sim.touch("warp", "w", t3, "dS")
+                if j == 0 and it > 0:
+                    # the previous item's dQ read before this item's first
+                    # dQ products overwrite it
+                    yield from sim.wait("dqf", it - 1)
+                    t4 = sim.t
+                    yield from sim.work(1, 2)
+                    sim.touch("warp", "r", t4, "dQ")
                 sim.arrive("pf", phase=g)
                 g += 1
-            yield from sim.wait("dqf", it)
-            t2 = sim.t
+        if items:  # the last item's dQ
+            yield from sim.wait("dqf", len(items) - 1)
+            t5 = sim.t
             yield from sim.work(1, 3)
-            sim.touch("warp", "r", t2, "dQ")
+            sim.touch("warp", "r", t5, "dQ")
 
     sim.run([loader(), score_mma(), dq_mma()] + [compute() for _ in range(ncomp)])
     return sim.errors
@@ -382,7 +423,8 @@ def _find(model, plant, kind, seeds=12, **kw):
     (forward, "q_refill_unguarded", "race on sQ", dict(qb=1)),
     (dkv, "p_overwrite_unguarded", "race on Pt", {}),
     (dkv, "kv_refill_unguarded", "race on sK", dict(kvb=1)),
-    (dq, "k_refill_unguarded", "race on sK", {}),
+    (dkv, "epi_late", "race on dV", {}),
+    (dq, "k_refill_unguarded", "race on sK", dict(kst=2)),
     (dq, "ds_wrong_phase", "no progress", {}),
 ])
 def test_the_checker_finds_a_planted_mistake(model, plant, kind, kw):

@@ -724,77 +724,60 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
     const int quarter = warp & 3, cg = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    int g = 0, it = 0;
-    for (int r = 0;; r++, it++) {
-      const int idx = snake_item(r);
-      if (idx >= nitems) break;
-      const int kb = idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH, k0 = kb * 128;
-      const int key = k0 + row;
-      const int nsub = (T - k0 + QS - 1) / QS;
-      for (int j = 0; j < nsub; j++, g++) {
-        const int s = g % ST, q0 = k0 + j * QS;
-        mbar_wait(s_full, (uint32_t)g & 1u, err);
-        tc_fence_after();
-        uint32_t rs[CPT], rd[CPT];
-        tmem_ld_cols<CPT>(tSt + lb + cg * CPT, rs);
-        tmem_ld_cols<CPT>(tdPt + lb + cg * CPT, rd);
+    // epilogue of an item: warps cg 0, 1 take dV columns 0..HS/2-1, HS/2..;
+    // 2, 3 take dK.  It runs one item late: epi_load reads the accumulators
+    // (everything that must precede the next item's first gradient
+    // products), epi_rest writes them out.
+    constexpr int EH = HS / 2;
+    const int which = cg >> 1, ch = cg & 1;  // which: 0 dV, 1 dK
+    const float mul = which ? scale : 1.f;
+    struct Item { int b, h, kb, k0; };
+    Item pv = {0, 0, 0, 0};
+    uint32_t pr[Cf::STAGE_OUT ? 16 : 1];  // the warp's 32 columns as bf16 pairs, kept for epi_rest
+    auto epi_load = [&](const Item& p) {
+      if constexpr (Cf::STAGE_OUT) {
+        // the warp's 128 key rows x 32 columns, written out by epi_rest
+        uint32_t ra[32];
+        tmem_ld32((which ? tdK : tdV) + lb + ch * 32, ra);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
-        const int c0 = q0 + cg * CPT;  // query of column 0 of this warp
-        if (staged) mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
-        const float* lc = sLD + s * 2 * QS + cg * CPT;  // minus lse, minus D of the columns
-        uint32_t pk[CPT / 2], dk[CPT / 2];
-        if (q0 < k0 + 128 || q0 + QS > T)
-          kv_elementwise<CPT, true>(rs, rd, lc, lc + QS, staged, lse + (int64_t)bh * T, dsum + (int64_t)bh * T, c0, key,
-                                    T, sl2, pk, dk);
-        else
-          kv_elementwise<CPT, false>(rs, rd, lc, lc + QS, staged, lse + (int64_t)bh * T, dsum + (int64_t)bh * T, c0, key,
-                                     T, sl2, pk, dk);
-        if (g > 0) {
-          mbar_wait(p_empty, (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read P^T, dS^T
-          tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < 16; i++) pr[i] = pack_bf16(__uint_as_float(ra[2 * i]) * mul, __uint_as_float(ra[2 * i + 1]) * mul);
+      } else {
+        // rows straight to global memory
+        constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
+        const int64_t C3 = 3 * (int64_t)C;
+#pragma unroll
+        for (int e = 0; e < EH; e += EC) {
+          uint32_t rc[EC];
+          tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, rc);
+          tmem_ld_wait();
+          float v[EC];
+#pragma unroll
+          for (int i = 0; i < EC; i++) v[i] = __uint_as_float(rc[i]);
+          if (p.k0 + row < T)
+            store_bf16_row<EC>(dqkv + ((int64_t)p.b * T + p.k0 + row) * C3 + (which ? C : 2 * C) + p.h * HS + ch * EH + e, v, mul);
         }
-        tmem_st_cols<CPT / 2>(tPt + lb + cg * (CPT / 2), pk);
-        tmem_st_cols<CPT / 2>(tdSt + lb + cg * (CPT / 2), dk);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
       }
-      // epilogue: warps cg 0, 1 take dV columns 0..HS/2-1, HS/2..; 2, 3 take dK
-      mbar_wait(acc_full, (uint32_t)it & 1u, err);
-      tc_fence_after();
-      constexpr int EH = HS / 2;
-      const int which = cg >> 1, ch = cg & 1;  // which: 0 dV, 1 dK
-      const float mul = which ? scale : 1.f;
+    };
+    auto epi_rest = [&](const Item& p) {
       if constexpr (Cf::STAGE_OUT) {
         // the 128 key rows x 32 columns of this warp into the 128B-swizzled
         // staging tile (row = key, 16-byte chunks ch*4 .. ch*4+3), then one
         // thread stores the dV and dK tiles with TMA (rows past T are not
         // written); the staging area was read by the previous item's stores
         // before anyone writes it again
-        uint32_t ra[32];
-        tmem_ld32((which ? tdK : tdV) + lb + ch * 32, ra);
         if (tid == 0) bulk_wait_read0();
         named_bar_sync(1, KV_CW * 32);
-        tmem_ld_wait();
         uint8_t* rowp = sOut + which * 16384 + row * 128;
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-          uint4 u;
-          u.x = pack_bf16(__uint_as_float(ra[8 * q]) * mul, __uint_as_float(ra[8 * q + 1]) * mul);
-          u.y = pack_bf16(__uint_as_float(ra[8 * q + 2]) * mul, __uint_as_float(ra[8 * q + 3]) * mul);
-          u.z = pack_bf16(__uint_as_float(ra[8 * q + 4]) * mul, __uint_as_float(ra[8 * q + 5]) * mul);
-          u.w = pack_bf16(__uint_as_float(ra[8 * q + 6]) * mul, __uint_as_float(ra[8 * q + 7]) * mul);
-          *reinterpret_cast<uint4*>(rowp + (((ch * 4 + q) ^ (row & 7)) << 4)) = u;
-        }
+        for (int q = 0; q < 4; q++)
+          *reinterpret_cast<uint4*>(rowp + (((ch * 4 + q) ^ (row & 7)) << 4)) =
+              make_uint4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
         fence_proxy_async_smem();
         named_bar_sync(1, KV_CW * 32);
         if (tid == 0) {
-          tma_store_3d(&tm_out, sOut, 2 * C + h * HS, k0, b);        // dV
-          tma_store_3d(&tm_out, sOut + 16384, C + h * HS, k0, b);    // dK
+          tma_store_3d(&tm_out, sOut, 2 * C + p.h * HS, p.k0, p.b);        // dV
+          tma_store_3d(&tm_out, sOut + 16384, C + p.h * HS, p.k0, p.b);    // dK
           bulk_commit();
         }
         // the tiles' column sums over the block's key rows below T (one
@@ -808,7 +791,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
           for (int r = rg * 16; r < rg * 16 + 16; r++) {
-            if (k0 + r < T) {
+            if (p.k0 + r < T) {
               const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
               const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
               s0 += f.x;
@@ -823,24 +806,78 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             float sum = 0.f;
 #pragma unroll
             for (int q = 0; q < 8; q++) sum += red[(t2 * 8 + q) * 64 + col];
-            bias_partial[((int64_t)b * nkb + kb) * 3 * (int64_t)C + (t2 ? C : 2 * C) + h * HS + col] = sum;
+            bias_partial[((int64_t)p.b * nkb + p.kb) * 3 * (int64_t)C + (t2 ? C : 2 * C) + p.h * HS + col] = sum;
           }
         }
-      } else {
-        constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
-        const int64_t C3 = 3 * (int64_t)C;
-#pragma unroll
-        for (int e = 0; e < EH; e += EC) {
-          uint32_t ra[EC];
-          tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, ra);
-          tmem_ld_wait();
-          float v[EC];
-#pragma unroll
-          for (int i = 0; i < EC; i++) v[i] = __uint_as_float(ra[i]);
-          if (key < T)
-            store_bf16_row<EC>(dqkv + ((int64_t)b * T + key) * C3 + (which ? C : 2 * C) + h * HS + ch * EH + e, v, mul);
-        }
       }
+    };
+    int g = 0, it = 0;
+    for (int r = 0;; r++, it++) {
+      const int idx = snake_item(r);
+      if (idx >= nitems) break;
+      const int kb = idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH, k0 = kb * 128;
+      const int key = k0 + row;
+      const int nsub = (T - k0 + QS - 1) / QS;
+      for (int j = 0; j < nsub; j++, g++) {
+        const int s = g % ST, q0 = k0 + j * QS;
+        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        tc_fence_after();
+        const int c0 = q0 + cg * CPT;  // query of column 0 of this warp
+        const float* lc = sLD + s * 2 * QS + cg * CPT;  // minus lse, minus D of the columns
+        const bool edge = q0 < k0 + 128 || q0 + QS > T;
+        // two halves of HC columns, each loaded, computed and stored before
+        // the next is loaded (the TMEM loads and stores keep the order), so
+        // that one half's operands and results are live at a time; S^T and
+        // dP^T are free for the next score products once both halves are read
+        constexpr int HC = CPT / 2;
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          uint32_t rs[HC], rd[HC];
+          tmem_ld_cols<HC>(tSt + lb + cg * CPT + hh * HC, rs);
+          tmem_ld_cols<HC>(tdPt + lb + cg * CPT + hh * HC, rd);
+          tmem_ld_wait();
+          if (hh == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+          } else if (staged) {
+            mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
+          }
+          uint32_t pk[HC / 2], dk[HC / 2];
+          if (edge)
+            kv_elementwise<HC, true>(rs, rd, lc + hh * HC, lc + QS + hh * HC, staged, lse + (int64_t)bh * T,
+                                     dsum + (int64_t)bh * T, c0 + hh * HC, key, T, sl2, pk, dk);
+          else
+            kv_elementwise<HC, false>(rs, rd, lc + hh * HC, lc + QS + hh * HC, staged, lse + (int64_t)bh * T,
+                                      dsum + (int64_t)bh * T, c0 + hh * HC, key, T, sl2, pk, dk);
+          if (hh == 0 && g > 0) {
+            mbar_wait(p_empty, (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read P^T, dS^T
+            tc_fence_after();
+          }
+          tmem_st_cols<HC / 2>(tPt + lb + cg * (CPT / 2) + hh * (HC / 2), pk);
+          tmem_st_cols<HC / 2>(tdSt + lb + cg * (CPT / 2) + hh * (HC / 2), dk);
+        }
+        tmem_st_wait();
+        if (j == 0 && it > 0) {
+          // the previous item's dV, dK leave TMEM before this item's first
+          // gradient products overwrite them; the rest of its epilogue runs
+          // while the tensor pipe works on this item
+          mbar_wait(acc_full, (uint32_t)(it - 1) & 1u, err);
+          tc_fence_after();
+          epi_load(pv);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        if (j == 0 && it > 0) epi_rest(pv);
+      }
+      pv = Item{b, h, kb, k0};
+    }
+    if (it > 0) {  // the last item's epilogue
+      mbar_wait(acc_full, (uint32_t)(it - 1) & 1u, err);
+      tc_fence_after();
+      epi_load(pv);
+      epi_rest(pv);
     }
   }
   if (Cf::STAGE_OUT && tid == 0) bulk_wait0();  // the last item's stores are complete
@@ -864,8 +901,10 @@ template <int HS>
 struct DqCfg {
   static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;
   static constexpr int QB = HS > 64 ? 1 : 2;
-  static constexpr int KST = HS > 64 ? 2 : 3;
-  static constexpr int VST = 2;
+  // a key stage is refilled only once dQ of its block has read it, so the
+  // ring must cover the load latency past that point
+  static constexpr int KST = HS > 64 ? 2 : 5;
+  static constexpr int VST = HS > 64 ? 2 : 3;
   // head size 64: the dQ tile leaves through shared memory and one TMA store
   static constexpr bool STAGE_OUT = HS == 64;
   static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 16384u : 0u;
@@ -1005,123 +1044,151 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const float sl2 = scale * LOG2E_F;
-    int g = 0, it = 0;
-    for (int r = 0;; r++, it++) {
-      const int idx = snake_item(r);
-      if (idx >= nitems) break;
-      const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
-      const int q = qb * 128 + row, nk = qb + 1;
-        // minus the row's lse (base 2) and minus its D; rows past T give P = 0
-      const float nl = q < T ? lse[(int64_t)bh * T + q] : -INFINITY;
-      const float nd = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
-      for (int j = 0; j < nk; j++, g++) {
-        mbar_wait(s_full, (uint32_t)g & 1u, err);
-        tc_fence_after();
-        uint32_t rs[32], rd[32];
-        tmem_ld32(tS + lb + cg * 32, rs);
-        tmem_ld32(tdP + lb + cg * 32, rd);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
-        const int c0 = j * 128 + cg * 32;  // key of column 0 of this warp
-        const bool diag = j == nk - 1;
-        uint32_t dk[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, nl2), x0, x1);
-          const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
-          float d0, d1;
-          f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), nd2)), d0, d1);
-          if (diag) {
-            d0 = c0 + i <= q ? d0 : 0.f;
-            d1 = c0 + i + 1 <= q ? d1 : 0.f;
-          }
-          dk[i >> 1] = pack_bf16(d0, d1);
-        }
-        if (g > 0) {
-          mbar_wait(ds_free, (uint32_t)(g - 1) & 1u, err);  // dQ(g-1) has read dS
-          tc_fence_after();
-        }
-        tmem_st16(tdS + lb + cg * 16, dk);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-      }
-      // epilogue: warp cg takes dQ columns cg*HS/4 .. cg*HS/4 + HS/4 - 1
-      mbar_wait(dq_full, (uint32_t)it & 1u, err);
-      tc_fence_after();
-      constexpr int EQ = HS / 4;
+    // epilogue of an item: warp cg takes dQ columns cg*HS/4 .. cg*HS/4 +
+    // HS/4 - 1.  It runs one item late: epi_load reads the accumulator
+    // (everything that must precede the next item's first dQ products),
+    // epi_rest writes it out.
+    constexpr int EQ = HS / 4;
+    struct Item { int b, h, qb; };
+    Item pv = {0, 0, 0};
+    uint32_t pr[Cf::STAGE_OUT ? EQ / 2 : 1];  // the warp's columns as bf16 pairs, kept for epi_rest
+    auto epi_load = [&](const Item& p) {
       uint32_t ra[EQ];
       tmem_ld_cols<EQ>(tdQ + lb + cg * EQ, ra);
+      tmem_ld_wait();
+      if constexpr (Cf::STAGE_OUT) {
+#pragma unroll
+        for (int i = 0; i < EQ / 2; i++) pr[i] = pack_bf16(__uint_as_float(ra[2 * i]) * scale, __uint_as_float(ra[2 * i + 1]) * scale);
+      } else {
+        const int q = p.qb * 128 + row;
+        float v[EQ];
+#pragma unroll
+        for (int i = 0; i < EQ; i++) v[i] = __uint_as_float(ra[i]) * scale;
+        if constexpr (EQ >= 8) {
+          if (q < T) store_bf16_row<EQ>(dqkv + ((int64_t)p.b * T + q) * 3 * (int64_t)C + p.h * HS + cg * EQ, v, 1.f);
+        } else {
+          if (q < T) {  // 4 columns: one 8-byte store
+            uint2 u;
+            u.x = pack_bf16(v[0], v[1]);
+            u.y = pack_bf16(v[2], v[3]);
+            *reinterpret_cast<uint2*>(dqkv + ((int64_t)p.b * T + q) * 3 * (int64_t)C + p.h * HS + cg * EQ) = u;
+          }
+        }
+      }
+    };
+    auto epi_rest = [&](const Item& p) {
       if constexpr (Cf::STAGE_OUT) {
         // 16 columns of the warp's 32 query rows into the 128B-swizzled
         // staging tile (row = query, 16-byte chunks 2cg, 2cg+1), then one
         // TMA store of the [128 x 64] tile (rows past T are not written)
         if (tid == 0) bulk_wait_read0();  // the previous item's store has read the staging tile
         named_bar_sync(1, DQ_CW * 32);
-        tmem_ld_wait();
         uint8_t* rowp = sOut + row * 128;
 #pragma unroll
-        for (int qq = 0; qq < 2; qq++) {
-          uint4 u;
-          u.x = pack_bf16(__uint_as_float(ra[8 * qq]) * scale, __uint_as_float(ra[8 * qq + 1]) * scale);
-          u.y = pack_bf16(__uint_as_float(ra[8 * qq + 2]) * scale, __uint_as_float(ra[8 * qq + 3]) * scale);
-          u.z = pack_bf16(__uint_as_float(ra[8 * qq + 4]) * scale, __uint_as_float(ra[8 * qq + 5]) * scale);
-          u.w = pack_bf16(__uint_as_float(ra[8 * qq + 6]) * scale, __uint_as_float(ra[8 * qq + 7]) * scale);
-          *reinterpret_cast<uint4*>(rowp + (((cg * 2 + qq) ^ (row & 7)) << 4)) = u;
-        }
+        for (int qq = 0; qq < 2; qq++)
+          *reinterpret_cast<uint4*>(rowp + (((cg * 2 + qq) ^ (row & 7)) << 4)) =
+              make_uint4(pr[4 * qq], pr[4 * qq + 1], pr[4 * qq + 2], pr[4 * qq + 3]);
         fence_proxy_async_smem();
         named_bar_sync(1, DQ_CW * 32);
         if (tid == 0) {
-          tma_store_3d(&tm_out, sOut, h * HS, qb * 128, b);
+          tma_store_3d(&tm_out, sOut, p.h * HS, p.qb * 128, p.b);
           bulk_commit();
         }
         // column sums of the tile over its query rows below T (one partial
         // row of the qkv bias gradient per (batch row, query block)): warp w
         // sums 8 rows, lane l columns 2l and 2l + 1, then the 16 row groups
         // are added in order
-        {
-          const int c2 = 2 * lane;
-          float s0 = 0.f, s1 = 0.f;
+        const int c2 = 2 * lane;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-          for (int r = warp * 8; r < warp * 8 + 8; r++) {
-            if (qb * 128 + r < T) {
-              const uint32_t u = *reinterpret_cast<const uint32_t*>(sOut + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-              s0 += f.x;
-              s1 += f.y;
+        for (int r = warp * 8; r < warp * 8 + 8; r++) {
+          if (p.qb * 128 + r < T) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(sOut + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+            s0 += f.x;
+            s1 += f.y;
+          }
+        }
+        red[warp * 64 + c2] = s0;
+        red[warp * 64 + c2 + 1] = s1;
+        named_bar_sync(1, DQ_CW * 32);
+        if (tid < 64) {
+          float sum = 0.f;
+#pragma unroll
+          for (int q = 0; q < 16; q++) sum += red[q * 64 + tid];
+          bias_partial[((int64_t)p.b * nqb + p.qb) * 3 * (int64_t)C + p.h * HS + tid] = sum;
+        }
+      }
+    };
+    int g = 0, it = 0;
+    for (int r = 0;; r++, it++) {
+      const int idx = snake_item(r);
+      if (idx >= nitems) break;
+      const int qb = nqb - 1 - idx / BH, bh = idx % BH, b = bh / NH, h = bh % NH;
+      const int q = qb * 128 + row, nk = qb + 1;
+      // minus the row's lse (base 2) and minus its D; rows past T give P = 0
+      const float nl = q < T ? lse[(int64_t)bh * T + q] : -INFINITY;
+      const float nd = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
+      for (int j = 0; j < nk; j++, g++) {
+        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        tc_fence_after();
+        const bool diag = j == nk - 1;
+        // two halves of 16 columns, each loaded, computed and stored before
+        // the next is loaded; S and dP are free once both halves are read
+#pragma unroll
+        for (int hh = 0; hh < 2; hh++) {
+          uint32_t rs[16], rd[16];
+          tmem_ld16(tS + lb + cg * 32 + hh * 16, rs);
+          tmem_ld16(tdP + lb + cg * 32 + hh * 16, rd);
+          tmem_ld_wait();
+          if (hh == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free);
+          }
+          const int c0 = j * 128 + cg * 32 + hh * 16;  // key of the half's column 0
+          uint32_t dk[8];
+#pragma unroll
+          for (int i = 0; i < 16; i += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, nl2), x0, x1);
+            const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), nd2)), d0, d1);
+            if (diag) {
+              d0 = c0 + i <= q ? d0 : 0.f;
+              d1 = c0 + i + 1 <= q ? d1 : 0.f;
             }
+            dk[i >> 1] = pack_bf16(d0, d1);
           }
-          red[warp * 64 + c2] = s0;
-          red[warp * 64 + c2 + 1] = s1;
-          named_bar_sync(1, DQ_CW * 32);
-          if (tid < 64) {
-            float sum = 0.f;
-#pragma unroll
-            for (int q = 0; q < 16; q++) sum += red[q * 64 + tid];
-            bias_partial[((int64_t)b * nqb + qb) * 3 * (int64_t)C + h * HS + tid] = sum;
+          if (hh == 0 && g > 0) {
+            mbar_wait(ds_free, (uint32_t)(g - 1) & 1u, err);  // dQ(g-1) has read dS
+            tc_fence_after();
           }
+          tmem_st8(tdS + lb + cg * 16 + hh * 8, dk);
         }
-        continue;
-      }
-      tmem_ld_wait();
-      float v[EQ];
-#pragma unroll
-      for (int i = 0; i < EQ; i++) v[i] = q < T ? __uint_as_float(ra[i]) * scale : 0.f;
-      if constexpr (EQ >= 8) {
-        if (q < T) store_bf16_row<EQ>(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * HS + cg * EQ, v, 1.f);
-      } else {
-        if (q < T) {  // 4 columns: one 8-byte store
-          uint2 u;
-          u.x = pack_bf16(v[0], v[1]);
-          u.y = pack_bf16(v[2], v[3]);
-          *reinterpret_cast<uint2*>(dqkv + ((int64_t)b * T + q) * 3 * (int64_t)C + h * HS + cg * EQ) = u;
+        tmem_st_wait();
+        if (j == 0 && it > 0) {
+          // the previous item's dQ leaves TMEM before this item's first dQ
+          // products overwrite it; the rest of its epilogue runs while the
+          // tensor pipe works on this item
+          mbar_wait(dq_full, (uint32_t)(it - 1) & 1u, err);
+          tc_fence_after();
+          epi_load(pv);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        if (j == 0 && it > 0) epi_rest(pv);
       }
+      pv = Item{b, h, qb};
+    }
+    if (it > 0) {  // the last item's epilogue
+      mbar_wait(dq_full, (uint32_t)(it - 1) & 1u, err);
+      tc_fence_after();
+      epi_load(pv);
+      epi_rest(pv);
     }
   }
   if (Cf::STAGE_OUT && tid == 0) bulk_wait0();  // the last item's store is complete
