@@ -550,9 +550,18 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                                  m->G(ATTPROJB) + (int64_t)l * C, m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
                                  m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
     }
-    // attproj: mid = res[l] + atty Wproj^T + b
-    run_gemm(m, c, gemm(M, C, C, dres_act, C, true, w(ATTPROJW, (int64_t)l * C * C), C, false,
-                        EPI_STORE, datty, C, f32), GS_ATTPROJ);
+    // attproj: mid = res[l] + atty Wproj^T + b.  At head size 64 (tensor-core
+    // attention) its data gradient datty also yields the attention backward's
+    // D = rowsum(datty * atty) per head, one head per 64-column group
+    const bool fused_d = !f32 && C / NH == 64;
+    GemmArgs gd = gemm(M, C, C, dres_act, C, true, w(ATTPROJW, (int64_t)l * C * C), C, false,
+                       fused_d ? EPI_DOT_AUX : EPI_STORE, datty, C, f32);
+    if (fused_d) {
+      gd.aux = atty;
+      gd.dot_out = m->dsum;
+      gd.dot_T = T;
+    }
+    run_gemm(m, c, gd, GS_ATTPROJ);
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
@@ -564,7 +573,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
       if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
       else qkvb_partials = launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
                                                      reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                                     lse, m->dsum, B, T, C, NH, m->cs_partial);
+                                                     lse, m->dsum, fused_d, B, T, C, NH, m->cs_partial);
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,

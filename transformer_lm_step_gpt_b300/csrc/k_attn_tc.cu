@@ -1226,7 +1226,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 
 template <int HS>
 static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, const bf16* qkv, const float* lse,
-                   float* dsum, int B, int T, int C, int NH, float* bias_partial) {
+                   float* dsum, bool dsum_ready, int B, int T, int C, int NH, float* bias_partial) {
   using Kv = KvCfg<HS>;
   using Dq = DqCfg<HS>;
   CUtensorMap tq, tq_s, td, td_s, tout;
@@ -1236,9 +1236,11 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
     c.host_fail = 1;
     return;
   }
-  const int64_t chunks = (int64_t)B * T * (C / 8);
-  launch_pdl(c, attn_bwd_dsum_kernel<HS>, dim3((int)std::min<int64_t>((chunks + 255) / 256, (int64_t)c.num_sms * 8)),
-             dim3(256), 0, dsum, dy, y, B, T, C, NH);
+  if (!dsum_ready) {
+    const int64_t chunks = (int64_t)B * T * (C / 8);
+    launch_pdl(c, attn_bwd_dsum_kernel<HS>, dim3((int)std::min<int64_t>((chunks + 255) / 256, (int64_t)c.num_sms * 8)),
+               dim3(256), 0, dsum, dy, y, B, T, C, NH);
+  }
   const float scale = 1.f / sqrtf((float)HS);
   const int nitems = ((T + 127) / 128) * B * NH;
   const int grid = std::min(nitems, c.num_sms);
@@ -1251,13 +1253,13 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
 }
 
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
-                               const bf16* qkv, const float* lse, float* dsum, int B, int T,
+                               const bf16* qkv, const float* lse, float* dsum, bool dsum_ready, int B, int T,
                                int C, int NH, float* bias_partial) {
   switch (C / NH) {
-    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
-    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
-    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return true;
-    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, B, T, C, NH, bias_partial); return false;
+    case 16: bwd_hs<16>(c, dqkv, dy, y, qkv, lse, dsum, dsum_ready, B, T, C, NH, bias_partial); return false;
+    case 32: bwd_hs<32>(c, dqkv, dy, y, qkv, lse, dsum, dsum_ready, B, T, C, NH, bias_partial); return false;
+    case 64: bwd_hs<64>(c, dqkv, dy, y, qkv, lse, dsum, dsum_ready, B, T, C, NH, bias_partial); return true;
+    case 128: bwd_hs<128>(c, dqkv, dy, y, qkv, lse, dsum, dsum_ready, B, T, C, NH, bias_partial); return false;
     default: c.host_fail = 1; return false;
   }
 }

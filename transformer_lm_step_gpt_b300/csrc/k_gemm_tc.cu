@@ -154,6 +154,16 @@ __device__ __forceinline__ float4 load_bias4(const GemmArgs& g, bool use_bias, i
   return b;
 }
 
+// EPI_DOT_AUX: minus the dot product of row m's 64 columns from n (one
+// attention head) into dot_out[(b * (N / 64) + n / 64) * dot_T + t],
+// m = b * dot_T + t
+__device__ __forceinline__ void store_dot(const GemmArgs& g, int m, int n, float dot) {
+  if (m < g.M) {
+    const int b = m / g.dot_T, t = m - b * g.dot_T;
+    g.dot_out[((int64_t)b * (g.N >> 6) + (n >> 6)) * g.dot_T + t] = -dot;
+  }
+}
+
 // Epilogue of one accumulator tile for one epilogue warp: 32 rows (this
 // warp's TMEM lane quarter, global rows mrow..mrow+31) by the warp's column
 // half of the BN columns starting at n0.  taddr: TMEM address of the
@@ -227,6 +237,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       mbar_wait(abar, aux_phase, err);
       aux_phase ^= 1u;
     }
+    float dot = 0.f;  // EPI_DOT_AUX
     // results (and the auxiliary input) in the thread's staging row
     if (f32) {
 #pragma unroll
@@ -244,11 +255,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       for (int c = 0; c < 8; c++) {
         uint8_t* p = stg + stg_off(lane, c);
         float o[8];
-        if (has_aux) {  // EPI_MUL_AUX: out = acc * aux
+        if (has_aux) {  // EPI_MUL_AUX: out = acc * aux; EPI_DOT_AUX: out = acc, dot += out * aux
           float hv[8];
           get8_bf16(p, hv);
+          if (epi == EPI_DOT_AUX) {
 #pragma unroll
-          for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * hv[q];
+            for (int q = 0; q < 8; q++) {
+              o[q] = v[8 * c + q];
+              dot = fmaf(__bfloat162float(__float2bfloat16_rn(o[q])), hv[q], dot);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * hv[q];
+          }
         } else if (epi == EPI_GELU_FWD && !split) {  // out = gelu'(x); v keeps gelu(x) for out2
 #pragma unroll
           for (int q = 0; q < 8; q++) gelu_and_grad_hw(v[8 * c + q], v[8 * c + q], o[q]);
@@ -269,6 +288,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       if (epi == EPI_GELU_FWD && !split && stg2) tma_store_2d(&em.out2, stg2, ncol, mrow);
       bulk_commit();
     }
+    if (epi == EPI_DOT_AUX) store_dot(g, mrow + lane, ncol, dot);
     if (g.colsum_out && !f32 && !split) {
       // column sums of the stored values over the warp's 32 rows, read back
       // from the staging rows (lane l: columns 2l, 2l+1 of the chunk)
@@ -321,7 +341,7 @@ __device__ __forceinline__ EpiFlags epi_flags(const GemmArgs& g, int splits) {
   const int epi = g.epi;
   f.split = splits > 1;
   f.f32 = f.split || epi == EPI_RESIDUAL || epi == EPI_ACCUM || (epi == EPI_STORE && g.out_f32);
-  f.has_aux = !f.split && (epi == EPI_RESIDUAL || epi == EPI_MUL_AUX);
+  f.has_aux = !f.split && (epi == EPI_RESIDUAL || epi == EPI_MUL_AUX || epi == EPI_DOT_AUX);
   f.use_bias = !f.split && g.bias && (epi == EPI_STORE || epi == EPI_GELU_FWD || epi == EPI_RESIDUAL);
   return f;
 }
@@ -388,6 +408,7 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
     }
     mbar_wait(&abar2[c & 1], (aph >> (c & 1)) & 1u, err);
     aph ^= 1u << (c & 1);
+    float dot = 0.f;  // EPI_DOT_AUX
     if (f32) {  // EPI_RESIDUAL: out = residual + (acc + bias)
 #pragma unroll
       for (int q = 0; q < 8; q++) {
@@ -401,8 +422,16 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
         uint8_t* pp = stg + stg_off(lane, q);
         float hv[8], o[8];
         get8_bf16(pp, hv);
+        if (g.epi == EPI_DOT_AUX) {  // out = acc, dot += out * aux
 #pragma unroll
-        for (int k = 0; k < 8; k++) o[k] = v[8 * q + k] * hv[k];
+          for (int k = 0; k < 8; k++) {
+            o[k] = v[8 * q + k];
+            dot = fmaf(__bfloat162float(__float2bfloat16_rn(o[k])), hv[k], dot);
+          }
+        } else {  // EPI_MUL_AUX: out = acc * aux
+#pragma unroll
+          for (int k = 0; k < 8; k++) o[k] = v[8 * q + k] * hv[k];
+        }
         put8_bf16(pp, o);
       }
     }
@@ -412,6 +441,7 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
       tma_store_2d(&em.out, stg, ncol, mrow);
       bulk_commit();
     }
+    if (g.epi == EPI_DOT_AUX) store_dot(g, mrow + lane, ncol, dot);
     if (g.colsum_out && !f32) {
       float s0 = 0.f, s1 = 0.f;
       const int ch = lane >> 2, wo = (lane & 3) * 4;
@@ -803,7 +833,7 @@ static void launch_tc(LaunchCtx& c, const GemmArgs& g, int splits, float* partia
     ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
     if (g.epi == EPI_GELU_FWD) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
     if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
-    if (g.epi == EPI_MUL_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_MUL_AUX || g.epi == EPI_DOT_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
   }
   if (!ok) {
     fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
@@ -847,7 +877,7 @@ static void launch_tc_pair(LaunchCtx& c, const GemmArgs& g, int splits, float* p
     ok = ok && make_tmap(&em.out, g.out, f32, g.N, g.M, g.ldo, f32 ? 32 : 64, 32);
     if (g.epi == EPI_GELU_FWD) ok = ok && make_tmap(&em.out2, g.out2, false, g.N, g.M, g.ldo, 64, 32);
     if (g.epi == EPI_RESIDUAL) ok = ok && make_tmap(&em.aux, g.aux, true, g.N, g.M, g.ldo, 32, 32);
-    if (g.epi == EPI_MUL_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
+    if (g.epi == EPI_MUL_AUX || g.epi == EPI_DOT_AUX) ok = ok && make_tmap(&em.aux, g.aux, false, g.N, g.M, g.ldo, 64, 32);
   }
   if (!ok) {
     fprintf(stderr, "gpt2: tensor map encoding failed (M=%d N=%d K=%d)\n", g.M, g.N, g.K);
@@ -1115,6 +1145,12 @@ void launch_gemm_fp8(LaunchCtx& c, const GemmArgs& g) {
 }
 
 void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
+  if (g.epi == EPI_DOT_AUX && (g.out_f32 || g.N % 64 != 0 || !g.aux || !g.dot_out || g.dot_T <= 0 ||
+                               g.M % g.dot_T != 0)) {
+    fprintf(stderr, "gpt2: EPI_DOT_AUX needs a bf16 output, N %% 64 == 0 and M a multiple of dot_T\n");
+    c.host_fail = 1;
+    return;
+  }
   if (gemm_rows_applies(g)) {  // a few rows of A: the weights stream once, M and N swapped
     launch_gemm_rows(c, g);
     return;
@@ -1147,7 +1183,8 @@ void launch_gemm_bf16(LaunchCtx& c, const GemmArgs& g) {
   if (BN == 256) {
     // epilogues that read an aux tile use the prefetching variant; the model's
     // aux GEMMs (attproj / fcproj forward, fcproj dgrad) are A K-major
-    const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX || g.epi == EPI_GELU_FWD);
+    const bool aux = splits == 1 && (g.epi == EPI_RESIDUAL || g.epi == EPI_MUL_AUX || g.epi == EPI_GELU_FWD ||
+                                     g.epi == EPI_DOT_AUX);
     if (aux && g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, true>(c, g, splits, partial);
     else if (aux && g.a_kmajor) launch_tc_pair<true, false, true>(c, g, splits, partial);
     else if (g.a_kmajor && g.b_kmajor) launch_tc_pair<true, true, false>(c, g, splits, partial);

@@ -129,6 +129,8 @@ enum GemmEpi {
   EPI_RESIDUAL,      // out(f32) = aux(f32) + acc + bias
   EPI_MUL_AUX,       // out(act) = acc * aux(act)  (the GELU backward with aux = gelu')
   EPI_ACCUM,         // out(f32) += acc
+  EPI_DOT_AUX,       // out(act) = acc; per row and 64-column group (an attention
+                     // head): dot_out = -sum(out * aux), out as rounded to act
 };
 struct GemmArgs {
   int M, N, K;
@@ -159,6 +161,10 @@ struct GemmArgs {
   // (*dequant_a) * (*dequant_b), the operands' per-tensor scales (device)
   const float* dequant_a;
   const float* dequant_b;
+  // EPI_DOT_AUX (act = bf16, N a multiple of 64): row m = b * dot_T + t and
+  // column group h = n / 64 write dot_out[(b * (N / 64) + h) * dot_T + t]
+  float* dot_out;
+  int dot_T;
 };
 // E4M3 operands A [M, K], B [N, K] (uint8 codes, K-major, lda / ldb in
 // bytes, multiples of 16), EPI_STORE only (bias allowed), dequant_a / _b set:
@@ -196,13 +202,15 @@ void launch_attention_bwd_simt(LaunchCtx& c, T* dqkv, const T* dy, const T* y, c
 int64_t attention_simt_scratch_floats(int B, int T_, int NH);
 void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qkv, int B, int T_,
                                int C, int NH);
-// qkv, y, dy -> dqkv [B,T,3C] (dq | dk | dv); dsum [B,NH,T] is scratch.
+// qkv, y, dy -> dqkv [B,T,3C] (dq | dk | dv); dsum [B,NH,T] holds minus
+// D = rowsum(dy * y) per head: computed here unless dsum_ready (the matmul
+// that produced dy wrote it, EPI_DOT_AUX).
 // Returns true when it also wrote the qkv bias gradient's partial rows
 // (head size 64): bias_partial [B * ceil(T/128)][3C], row b * ceil(T/128) +
 // block (launch_colsum_reduce adds them up).
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
-                               const bf16* qkv, const float* lse, float* dsum, int B, int T_,
-                               int C, int NH, float* bias_partial);
+                               const bf16* qkv, const float* lse, float* dsum, bool dsum_ready, int B,
+                               int T_, int C, int NH, float* bias_partial);
 
 // A tensor map over a [B][T][W] bf16 tensor with box {64, rows, 1},
 // 128-byte swizzle, rows past T read as 0 (false if the driver's encoder is
