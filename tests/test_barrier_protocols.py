@@ -139,29 +139,32 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
     """attn_bwd_dkv_tc_kernel.  Loader: per item k, v into buffer it % kvb
     once the item kvb back has issued its last S^T, dP^T; per query
     sub-block g q, dy (and, staged, their lse / D) into ring stage
-    g % stages once dV, dK(g - stages) have read it.  Score issuer, over
-    all sub-blocks in turn: S^T(g), dP^T(g) once the warps have copied out
-    S^T(g - 1), dP^T(g - 1).  Gradient issuer (another thread, its MMAs
-    interleave with the score issuer's in any order): dV, dK(g) from
-    P^T, dS^T(g); an item's last one also commits the accumulators'
-    completion.
-    Elementwise warps, in two halves of a sub-block's columns: copy one
-    half of S^T, dP^T out, (staged) wait for the stage's lse / D, write its
-    P^T, dS^T once dV, dK(g - 1) have read them; then the other half, after
-    which S^T, dP^T are free.  An item's dV, dK are read one item late, in
-    the next item's first sub-block before its gradient products are
-    released (and the last item's after the loop)."""
+    g % stages once dV, dK(g - stages) have read it.  Every sub-block is
+    taken in two column halves with their own hand-offs.  Score issuer, over
+    all sub-blocks and halves in turn: S^T, dP^T (g, h) once group h has
+    copied out its half of g - 1.  Gradient issuer (another thread, its MMAs
+    interleave with the score issuer's in any order): dV, dK (g, h) from
+    P^T, dS^T (g, h), half 0 before half 1; the first of an item overwrites
+    the accumulators, its last commits their completion.
+    Elementwise warps, two groups (group h owns half h): copy the half of
+    S^T, dP^T out in two pieces, (staged) wait for the stage's lse / D, write
+    P^T, dS^T once dV, dK (g - 1, h) have read them.  An item's dV, dK are
+    read by group 0, one item late, in the next item's first sub-block
+    before its half-0 products are released (and the last item's after the
+    loop)."""
     sim = Sim(seed, plant)
+    gw = ncomp // 2
     for i in range(kvb):
         sim.bar("kvf%d" % i)
         sim.bar("kve%d" % i)
     for s in range(stages):
         sim.bar("qf%d" % s)
         sim.bar("qe%d" % s)
-    sim.bar("sf")
-    sim.bar("sfree", ncomp)
-    sim.bar("pf", ncomp)
-    sim.bar("pe")
+    for h in range(2):
+        sim.bar("sf%d" % h)
+        sim.bar("sfree%d" % h, gw)
+        sim.bar("pf%d" % h, gw)
+        sim.bar("pe%d" % h)
     sim.bar("acc")
 
     def stage_bufs(s):
@@ -189,12 +192,14 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
             for j in range(nsub):
                 s = g % stages
                 yield from sim.wait("qf%d" % s, g // stages)
-                if g > 0:
-                    yield from sim.wait("sfree", g - 1)
-                sim.mma(reads=("sK%d" % b, "sV%d" % b, "sQ%d" % s, "sD%d" % s), writes=("St", "dPt"))
-                if j == nsub - 1:
-                    sim.commit("kve%d" % b, phase=it // kvb)
-                sim.commit("sf", phase=g)
+                for h in range(2):
+                    if g > 0:
+                        yield from sim.wait("sfree%d" % h, g - 1)
+                    sim.mma(reads=("sK%d" % b, "sV%d" % b, "sQ%d" % s, "sD%d" % s),
+                            writes=("St%d" % h, "dPt%d" % h))
+                    if h == 1 and j == nsub - 1:
+                        sim.commit("kve%d" % b, phase=it // kvb)
+                    sim.commit("sf%d" % h, phase=g)
                 g += 1
 
     def grad_mma():
@@ -202,25 +207,27 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
         for it, nsub in enumerate(items):
             for j in range(nsub):
                 s = g % stages
-                yield from sim.wait("pf", g)
-                acc = () if j == 0 else ("dV", "dK")
-                sim.mma(reads=("Pt", "dSt", "sQ%d" % s, "sD%d" % s) + acc, writes=("dV", "dK"))
-                sim.commit("qe%d" % s, phase=g // stages)
-                sim.commit("pe", phase=g)
-                if j == nsub - 1:
-                    sim.commit("acc", phase=it)
+                for h in range(2):
+                    yield from sim.wait("pf%d" % h, g)
+                    acc = () if (j == 0 and h == 0) else ("dV", "dK")
+                    sim.mma(reads=("Pt%d" % h, "dSt%d" % h, "sQ%d" % s, "sD%d" % s) + acc, writes=("dV", "dK"))
+                    sim.commit("pe%d" % h, phase=g)
+                    if h == 1:
+                        sim.commit("qe%d" % s, phase=g // stages)
+                    if h == 1 and j == nsub - 1:
+                        sim.commit("acc", phase=it)
                 g += 1
 
-    def compute():
+    def compute(h):
         g = 0
         for it, nsub in enumerate(items):
             for j in range(nsub):
                 s = g % stages
-                yield from sim.wait("sf", g)
-                # two halves: each read, computed and written before the next
+                yield from sim.wait("sf%d" % h, g)
+                # two pieces: each read, computed and written before the next
                 t0 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "r", t0, "St", "dPt")
+                sim.touch("warp", "r", t0, "St%d" % h, "dPt%d" % h)
                 if staged:  # the stage's lse / D arrive with its q / dy tiles
                     yield from sim.wait("qf%d" % s, g // stages)
                 t1 = sim.t
@@ -228,38 +235,39 @@ def dkv(items, seed, plant=None, staged=True, ncomp=DKV_WARPS, kvb=DKV_KVB, stag
                 if staged:
                     sim.touch("warp", "r", t1, "sLD%d" % s)
                 if g > 0 and plant != "p_overwrite_unguarded":
-                    yield from sim.wait("pe", g - 1)
+                    yield from sim.wait("pe%d" % h, g - 1)
                 t2 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "w", t2, "Pt", "dSt")
+                sim.touch("warp", "w", t2, "Pt%d" % h, "dSt%d" % h)
                 t3 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "r", t3, "St", "dPt")
-                sim.arrive("sfree", phase=g)
+                sim.touch("warp", "r", t3, "St%d" % h, "dPt%d" % h)
+                sim.arrive("sfree%d" % h, phase=g)
                 t4 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "w", t4, "Pt", "dSt")
-                if j == 0 and it > 0 and plant != "epi_late":
+                sim.touch("warp", "w", t4, "Pt%d" % h, "dSt%d" % h)
+                epi = h == 0 and j == 0 and it > 0
+                if epi and plant != "epi_late":
                     # the previous item's dV, dK read before this item's
                     # first gradient products overwrite them
                     yield from sim.wait("acc", it - 1)
                     t5 = sim.t
                     yield from sim.work(1, 2)
                     sim.touch("warp", "r", t5, "dV", "dK")
-                sim.arrive("pf", phase=g)
-                if j == 0 and it > 0 and plant == "epi_late":
+                sim.arrive("pf%d" % h, phase=g)
+                if epi and plant == "epi_late":
                     yield from sim.wait("acc", it - 1)
                     t5 = sim.t
                     yield from sim.work(1, 2)
                     sim.touch("warp", "r", t5, "dV", "dK")
                 g += 1
-        if items:  # the last item's accumulators
+        if h == 0 and items:  # the last item's accumulators
             yield from sim.wait("acc", len(items) - 1)
             t6 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t6, "dV", "dK")
 
-    sim.run([loader(), score_mma(), grad_mma()] + [compute() for _ in range(ncomp)])
+    sim.run([loader(), score_mma(), grad_mma()] + [compute(w // gw) for w in range(ncomp)])
     return sim.errors
 
 

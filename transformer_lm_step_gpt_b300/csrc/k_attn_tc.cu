@@ -134,12 +134,19 @@ __device__ __forceinline__ void mma_hs_ss(uint32_t d, uint64_t a, int arows, uin
     for (int kk = 0; kk < KS; kk++) tc_mma_bf16(d, a + kstep(arows, kk), b + kstep(brows, kk), idesc, kk > 0 ? 1u : 0u);
   }
 }
-// A chain of NK K steps (a multiple of 4) with A in TMEM from column a and
-// an MN-major B operand (K = rows): dst (+)= A B, accumulating iff acc.
+// A chain of NK K steps (a multiple of 4, or 1 or 2) with A in TMEM from
+// column a (8 columns of bf16 pairs per step) and an MN-major B operand
+// (K = rows): dst (+)= A B, accumulating iff acc.
 template <int NK>
 __device__ __forceinline__ void mma_ts_chain(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, bool acc) {
+  if constexpr (NK % 4 == 0) {
 #pragma unroll
-  for (int c = 0; c < NK / 4; c++) tc_mma4_ts<128>(d, a + 32 * c, b + nstep(4 * c), idesc, (acc || c > 0) ? 1u : 0u);
+    for (int c = 0; c < NK / 4; c++) tc_mma4_ts<128>(d, a + 32 * c, b + nstep(4 * c), idesc, (acc || c > 0) ? 1u : 0u);
+  } else {
+    static_assert(NK == 1 || NK == 2, "K steps");
+#pragma unroll
+    for (int kk = 0; kk < NK; kk++) tc_mma_bf16_ts(d, a + 8 * kk, b + nstep(kk), idesc, (acc || kk > 0) ? 1u : 0u);
+  }
 }
 // TMA of one tile (NB boxes) onto one barrier
 template <int HS>
@@ -550,13 +557,18 @@ __device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_
 }
 
 // Item (128-key block kb, b*h): query sub-blocks of QS rows from k0 = 128 kb
-// to T.  Warps 0..15 elementwise (warps w, w+4, w+8, w+12 share TMEM lane
-// quarter w % 4 = 32 key rows and take QS/4 query columns each), warp 16
-// issues the score products, warp 17 loads, warp 18 issues the gradient
-// products.
-//   S^T = k q^T, dP^T = v dy^T (M = 128 keys, N = QS queries, K = HS);
+// to T, each taken in two column halves of QS/2 queries.  Warps 0..15
+// elementwise in two groups: group h (warps 8h..8h+7) owns half h of every
+// sub-block (warps w and w+4 of a group share TMEM lane quarter w % 4 = 32
+// key rows and take QS/4 query columns each); warp 16 issues the score
+// products, warp 17 loads, warp 18 issues the gradient products.
+//   S^T = k q^T, dP^T = v dy^T (M = 128 keys, N = QS/2 queries per half, K = HS);
 //   P^T = 2^(S^T scale log2e - lse2), dS^T = P^T (dP^T - D), into TMEM;
-//   dV += P^T dy, dK += dS^T q (N = HS, K = QS queries; A from TMEM).
+//   dV += P^T dy, dK += dS^T q (N = HS, K = QS/2 queries per half; A from TMEM).
+// Each half has its own hand-offs (scores in, scores copied out, P^T / dS^T
+// in, P^T / dS^T read), so one group's TMEM loads and arithmetic overlap the
+// other group's, and the tensor pipe works on one half while the warps
+// work on the other.  The item's epilogue is group 0's, one item late.
 // TMEM: S^T 0..QS-1, dP^T QS..2QS-1, P^T 2QS.., dS^T 2.5QS.., dV 3QS..,
 // dK 3QS+HS.. (at most 512 columns).
 // smem: K, V [KVB] | q, dy ring [ST] | lse / D per stage [ST][2][QS] | barriers.
@@ -564,10 +576,12 @@ __device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_
 // multiple of 4 (16-byte aligned rows); otherwise the elementwise warps read
 // them from global memory.
 #define KV_CW 16
+#define KV_GW 8  // warps per elementwise group
 #define KV_THREADS (KV_CW * 32 + 96)
 template <int HS>
 struct KvCfg {
   static constexpr int QS = HS > 64 ? 64 : 128;
+  static constexpr int QH = QS / 2;   // queries per half
   static constexpr int CPT = QS / 4;  // query columns per elementwise thread
   static constexpr uint32_t KTILE = Hs<HS>::NB * 16384u;                  // [128 x HS]
   static constexpr uint32_t QTILE = Hs<HS>::NB * (uint32_t)QS * 128u;     // [QS x HS]
@@ -578,7 +592,7 @@ struct KvCfg {
   static constexpr bool STAGE_OUT = HS == 64;
   static constexpr int ST = STAGE_OUT ? 3 : 4;
   static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 2 * 16384u : 0u;
-  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 2 * 8 * 64 * 4 : 0u;  // column-sum partials [2][8][64]
+  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 2 * 4 * 64 * 4 : 0u;  // column-sum partials [2][4][64]
   static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + OUT_BYTES + RED_BYTES + 256;
 };
 
@@ -589,7 +603,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
                            bf16* dqkv, const float* lse, const float* dsum, float* bias_partial, int B, int T, int C,
                            int NH, float scale, int* err) {
   using Cf = KvCfg<HS>;
-  constexpr int QS = Cf::QS, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
+  constexpr int QS = Cf::QS, QH = Cf::QH, CPT = Cf::CPT, KVB = Cf::KVB, ST = Cf::ST;
   constexpr uint32_t KTILE = Cf::KTILE, QTILE = Cf::QTILE;
   extern __shared__ uint8_t smraw[];
   uint8_t* sm = align1024(smraw);
@@ -599,17 +613,17 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   uint8_t* sD = sQ + ST * QTILE;             // dy [ST]
   float* sLD = reinterpret_cast<float*>(sD + ST * QTILE);  // [ST][lse QS, D QS]
   uint8_t* sOut = reinterpret_cast<uint8_t*>(sLD + ST * 2 * QS);  // dV | dK staging (head size 64)
-  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);     // [2][8][64] column-sum partials
+  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);     // [2][4][64] column-sum partials
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + Cf::RED_BYTES);
   uint64_t* kv_full = bars;              // [KVB]
   uint64_t* kv_empty = kv_full + KVB;    // [KVB]: the item's last S^T, dP^T have read k, v
   uint64_t* q_full = kv_empty + KVB;     // [ST]
   uint64_t* q_empty = q_full + ST;       // [ST]: dV, dK of the sub-block done
-  uint64_t* s_full = q_empty + ST;       // S^T, dP^T in TMEM
-  uint64_t* s_free = s_full + 1;         // copied out by the 16 warps
-  uint64_t* p_full = s_free + 1;         // P^T, dS^T written by the 16 warps
-  uint64_t* p_empty = p_full + 1;        // dV, dK have read them
-  uint64_t* acc_full = p_empty + 1;      // the item's dV, dK complete
+  uint64_t* s_full = q_empty + ST;       // [2] S^T, dP^T of a half in TMEM
+  uint64_t* s_free = s_full + 2;         // [2] copied out by the half's group
+  uint64_t* p_full = s_free + 2;         // [2] P^T, dS^T of a half written by its group
+  uint64_t* p_empty = p_full + 2;        // [2] dV, dK have read them
+  uint64_t* acc_full = p_empty + 2;      // the item's dV, dK complete
   uint32_t* tslot = reinterpret_cast<uint32_t*>(acc_full + 1);
 
   const int nkb = (T + 127) / 128, BH = B * NH, nitems = nkb * BH;
@@ -618,10 +632,12 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   if (tid == 0) {
     for (int i = 0; i < KVB; i++) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < ST; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, KV_CW);
-    mbar_init(p_full, KV_CW);
-    mbar_init(p_empty, 1);
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], KV_GW);
+      mbar_init(&p_full[i], KV_GW);
+      mbar_init(&p_empty[i], 1);
+    }
     mbar_init(acc_full, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -670,7 +686,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
   } else if (warp == KV_CW) {
     // ---------------------------------------------------------------- score MMAs
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, QS, false, false);
+      const uint32_t idS = tc_idesc_bf16(128, QH, false, false);
       int g = 0, it = 0;
       for (int r = 0;; r++, it++) {
         const int idx = snake_item(r);
@@ -683,21 +699,26 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         for (int j = 0; j < nsub; j++, g++) {
           const int s = g % ST;
           mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);
-          if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
-          tc_fence_after();
           const uint64_t dQ = kdesc(smem_u32(sQ + s * QTILE), QS, 0), dD = kdesc(smem_u32(sD + s * QTILE), QS, 0);
-          mma_hs_ss<Hs<HS>::KS>(tSt, dK, 128, dQ, QS, idS);
-          mma_hs_ss<Hs<HS>::KS>(tdPt, dV, 128, dD, QS, idS);
-          if (j == nsub - 1) tc_commit(&kv_empty[kvb]);
-          tc_commit(s_full);
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {
+            // half hf: query rows hf*QH.. of the stage (their 128-byte rows
+            // start hf*QH*128 bytes in, a multiple of the 1 KB swizzle atom)
+            if (g > 0) mbar_wait(&s_free[hf], (uint32_t)(g - 1) & 1u, err);
+            tc_fence_after();
+            const uint64_t off = (uint64_t)((hf * QH * 128) >> 4);
+            mma_hs_ss<Hs<HS>::KS>(tSt + hf * QH, dK, 128, dQ + off, QS, idS);
+            mma_hs_ss<Hs<HS>::KS>(tdPt + hf * QH, dV, 128, dD + off, QS, idS);
+            if (hf == 1 && j == nsub - 1) tc_commit(&kv_empty[kvb]);
+            tc_commit(&s_full[hf]);
+          }
         }
       }
     }
   } else if (warp == KV_CW + 2) {
     // ---------------------------------------------------------------- gradient MMAs
-    // dV, dK (g) once P^T, dS^T (g) are in TMEM; a thread on another
-    // scheduler than the score MMAs' issuer, so that the two instruction
-    // streams compete with different elementwise warps for issue slots
+    // dV, dK (g, half) once P^T, dS^T of the half are in TMEM; a thread on
+    // another scheduler than the score MMAs' issuer
     if (lane == 0) {
       const uint32_t idO = tc_idesc_bf16(128, HS, false, true);
       int g = 0;
@@ -707,41 +728,60 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         const int k0 = (idx / BH) * 128;
         const int nsub = (T - k0 + QS - 1) / QS;
         for (int j = 0; j < nsub; j++, g++) {
-          mbar_wait(p_full, (uint32_t)g & 1u, err);
-          tc_fence_after();
           const int s = g % ST;
           const uint64_t dQn = ndesc(smem_u32(sQ + s * QTILE), QS, 0), dDn = ndesc(smem_u32(sD + s * QTILE), QS, 0);
-          mma_ts_chain<QS / 16>(tdV, tPt, dDn, idO, j > 0);
-          mma_ts_chain<QS / 16>(tdK, tdSt, dQn, idO, j > 0);
-          tc_commit(&q_empty[s]);
-          tc_commit(p_empty);
-          if (j == nsub - 1) tc_commit(acc_full);
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {
+            mbar_wait(&p_full[hf], (uint32_t)g & 1u, err);
+            tc_fence_after();
+            // K = the half's QH queries: P^T / dS^T columns hf*QH/2.., q / dy rows hf*QH..
+            mma_ts_chain<QH / 16>(tdV, tPt + hf * (QH / 2), dDn + nstep(hf * (QH / 16)), idO, j > 0 || hf > 0);
+            mma_ts_chain<QH / 16>(tdK, tdSt + hf * (QH / 2), dQn + nstep(hf * (QH / 16)), idO, j > 0 || hf > 0);
+            tc_commit(&p_empty[hf]);
+            if (hf == 1) tc_commit(&q_empty[s]);
+            if (hf == 1 && j == nsub - 1) tc_commit(acc_full);
+          }
         }
       }
     }
   } else {
     // ---------------------------------------------------------------- elementwise warps
-    const int quarter = warp & 3, cg = warp >> 2;
+    const int quarter = warp & 3, cg = warp >> 2, grp = cg >> 1;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    // epilogue of an item: warps cg 0, 1 take dV columns 0..HS/2-1, HS/2..;
-    // 2, 3 take dK.  It runs one item late: epi_load reads the accumulators
-    // (everything that must precede the next item's first gradient
-    // products), epi_rest writes them out.
-    constexpr int EH = HS / 2;
-    const int which = cg >> 1, ch = cg & 1;  // which: 0 dV, 1 dK
+    // epilogue of an item, by group 0 (warps 0..7): warps with cg 0 take
+    // dV, cg 1 dK, all HS columns of their 32 key rows.  It runs one item
+    // late: epi_load reads the accumulators (everything that must precede
+    // the next item's first gradient products, which wait for group 0),
+    // epi_rest writes them out.
+    constexpr int EH = HS;
+    const int which = cg & 1;  // 0 dV, 1 dK
     const float mul = which ? scale : 1.f;
     struct Item { int b, h, kb, k0; };
     Item pv = {0, 0, 0, 0};
-    uint32_t pr[Cf::STAGE_OUT ? 16 : 1];  // the warp's 32 columns as bf16 pairs, kept for epi_rest
     auto epi_load = [&](const Item& p) {
       if constexpr (Cf::STAGE_OUT) {
-        // the warp's 128 key rows x 32 columns, written out by epi_rest
-        uint32_t ra[32];
-        tmem_ld32((which ? tdK : tdV) + lb + ch * 32, ra);
-        tmem_ld_wait();
+        // the warp's 32 key rows x 64 columns into the 128B-swizzled staging
+        // tile of dV (cg 0) or dK (cg 1), once the previous item's stores
+        // have read the staging area
+        if (tid == 0) bulk_wait_read0();
+        named_bar_sync(1, KV_GW * 32);
+        uint8_t* rowp = sOut + which * 16384 + row * 128;
 #pragma unroll
-        for (int i = 0; i < 16; i++) pr[i] = pack_bf16(__uint_as_float(ra[2 * i]) * mul, __uint_as_float(ra[2 * i + 1]) * mul);
+        for (int e = 0; e < 2; e++) {
+          uint32_t ra[32];
+          tmem_ld32((which ? tdK : tdV) + lb + e * 32, ra);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; q++) {
+            uint4 u;
+            u.x = pack_bf16(__uint_as_float(ra[8 * q]) * mul, __uint_as_float(ra[8 * q + 1]) * mul);
+            u.y = pack_bf16(__uint_as_float(ra[8 * q + 2]) * mul, __uint_as_float(ra[8 * q + 3]) * mul);
+            u.z = pack_bf16(__uint_as_float(ra[8 * q + 4]) * mul, __uint_as_float(ra[8 * q + 5]) * mul);
+            u.w = pack_bf16(__uint_as_float(ra[8 * q + 6]) * mul, __uint_as_float(ra[8 * q + 7]) * mul);
+            *reinterpret_cast<uint4*>(rowp + (((4 * e + q) ^ (row & 7)) << 4)) = u;
+          }
+        }
       } else {
         // rows straight to global memory
         constexpr int EC = EH < 32 ? EH : 32;  // columns per chunk
@@ -749,32 +789,22 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 #pragma unroll
         for (int e = 0; e < EH; e += EC) {
           uint32_t rc[EC];
-          tmem_ld_cols<EC>((which ? tdK : tdV) + lb + ch * EH + e, rc);
+          tmem_ld_cols<EC>((which ? tdK : tdV) + lb + e, rc);
           tmem_ld_wait();
           float v[EC];
 #pragma unroll
           for (int i = 0; i < EC; i++) v[i] = __uint_as_float(rc[i]);
           if (p.k0 + row < T)
-            store_bf16_row<EC>(dqkv + ((int64_t)p.b * T + p.k0 + row) * C3 + (which ? C : 2 * C) + p.h * HS + ch * EH + e, v, mul);
+            store_bf16_row<EC>(dqkv + ((int64_t)p.b * T + p.k0 + row) * C3 + (which ? C : 2 * C) + p.h * HS + e, v, mul);
         }
       }
     };
     auto epi_rest = [&](const Item& p) {
       if constexpr (Cf::STAGE_OUT) {
-        // the 128 key rows x 32 columns of this warp into the 128B-swizzled
-        // staging tile (row = key, 16-byte chunks ch*4 .. ch*4+3), then one
-        // thread stores the dV and dK tiles with TMA (rows past T are not
-        // written); the staging area was read by the previous item's stores
-        // before anyone writes it again
-        if (tid == 0) bulk_wait_read0();
-        named_bar_sync(1, KV_CW * 32);
-        uint8_t* rowp = sOut + which * 16384 + row * 128;
-#pragma unroll
-        for (int q = 0; q < 4; q++)
-          *reinterpret_cast<uint4*>(rowp + (((ch * 4 + q) ^ (row & 7)) << 4)) =
-              make_uint4(pr[4 * q], pr[4 * q + 1], pr[4 * q + 2], pr[4 * q + 3]);
+        // one thread stores the dV and dK tiles with TMA (rows past T are
+        // not written)
         fence_proxy_async_smem();
-        named_bar_sync(1, KV_CW * 32);
+        named_bar_sync(1, KV_GW * 32);
         if (tid == 0) {
           tma_store_3d(&tm_out, sOut, 2 * C + p.h * HS, p.k0, p.b);        // dV
           tma_store_3d(&tm_out, sOut + 16384, C + p.h * HS, p.k0, p.b);    // dK
@@ -782,32 +812,30 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         }
         // the tiles' column sums over the block's key rows below T (one
         // partial row of the qkv bias gradient per (batch row, key block)),
-        // read back from the staging tiles: warp w sums 16 rows of tile
-        // w / 8, lane l columns 2l and 2l + 1; the 8 row groups are then
+        // read back from the staging tiles: warp w sums 32 rows of tile
+        // w / 4, lane l columns 2l and 2l + 1; the 4 row groups are then
         // added in order
-        {
-          const int tt = warp >> 3, rg = warp & 7, c2 = 2 * lane;
-          const uint8_t* tile = sOut + tt * 16384;
-          float s0 = 0.f, s1 = 0.f;
+        const int tt = warp >> 2, rg = warp & 3, c2 = 2 * lane;
+        const uint8_t* tile = sOut + tt * 16384;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
-          for (int r = rg * 16; r < rg * 16 + 16; r++) {
-            if (p.k0 + r < T) {
-              const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
-              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-              s0 += f.x;
-              s1 += f.y;
-            }
+        for (int r = rg * 32; r < rg * 32 + 32; r++) {
+          if (p.k0 + r < T) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
+            s0 += f.x;
+            s1 += f.y;
           }
-          red[(tt * 8 + rg) * 64 + c2] = s0;
-          red[(tt * 8 + rg) * 64 + c2 + 1] = s1;
-          named_bar_sync(1, KV_CW * 32);
-          if (tid < 128) {
-            const int t2 = tid >> 6, col = tid & 63;
-            float sum = 0.f;
+        }
+        red[(tt * 4 + rg) * 64 + c2] = s0;
+        red[(tt * 4 + rg) * 64 + c2 + 1] = s1;
+        named_bar_sync(1, KV_GW * 32);
+        if (tid < 128) {
+          const int t2 = tid >> 6, col = tid & 63;
+          float sum = 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; q++) sum += red[(t2 * 8 + q) * 64 + col];
-            bias_partial[((int64_t)p.b * nkb + p.kb) * 3 * (int64_t)C + (t2 ? C : 2 * C) + p.h * HS + col] = sum;
-          }
+          for (int q = 0; q < 4; q++) sum += red[(t2 * 4 + q) * 64 + col];
+          bias_partial[((int64_t)p.b * nkb + p.kb) * 3 * (int64_t)C + (t2 ? C : 2 * C) + p.h * HS + col] = sum;
         }
       }
     };
@@ -820,15 +848,15 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
       const int nsub = (T - k0 + QS - 1) / QS;
       for (int j = 0; j < nsub; j++, g++) {
         const int s = g % ST, q0 = k0 + j * QS;
-        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        mbar_wait(&s_full[grp], (uint32_t)g & 1u, err);
         tc_fence_after();
         const int c0 = q0 + cg * CPT;  // query of column 0 of this warp
         const float* lc = sLD + s * 2 * QS + cg * CPT;  // minus lse, minus D of the columns
         const bool edge = q0 < k0 + 128 || q0 + QS > T;
         // two halves of HC columns, each loaded, computed and stored before
         // the next is loaded (the TMEM loads and stores keep the order), so
-        // that one half's operands and results are live at a time; S^T and
-        // dP^T are free for the next score products once both halves are read
+        // that one half's operands and results are live at a time; the
+        // group's S^T and dP^T columns are free once both halves are read
         constexpr int HC = CPT / 2;
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
@@ -839,7 +867,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
           if (hh == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(&s_free[grp]);
           } else if (staged) {
             mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
           }
@@ -851,29 +879,30 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             kv_elementwise<HC, false>(rs, rd, lc + hh * HC, lc + QS + hh * HC, staged, lse + (int64_t)bh * T,
                                       dsum + (int64_t)bh * T, c0 + hh * HC, key, T, sl2, pk, dk);
           if (hh == 0 && g > 0) {
-            mbar_wait(p_empty, (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read P^T, dS^T
+            mbar_wait(&p_empty[grp], (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read the half's P^T, dS^T
             tc_fence_after();
           }
           tmem_st_cols<HC / 2>(tPt + lb + cg * (CPT / 2) + hh * (HC / 2), pk);
           tmem_st_cols<HC / 2>(tdSt + lb + cg * (CPT / 2) + hh * (HC / 2), dk);
         }
         tmem_st_wait();
-        if (j == 0 && it > 0) {
+        const bool epi = grp == 0 && j == 0 && it > 0;
+        if (epi) {
           // the previous item's dV, dK leave TMEM before this item's first
-          // gradient products overwrite them; the rest of its epilogue runs
-          // while the tensor pipe works on this item
+          // gradient products (half 0, group 0's) overwrite them; the rest
+          // of its epilogue runs while the tensor pipe works on this item
           mbar_wait(acc_full, (uint32_t)(it - 1) & 1u, err);
           tc_fence_after();
           epi_load(pv);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-        if (j == 0 && it > 0) epi_rest(pv);
+        if (lane == 0) mbar_arrive(&p_full[grp]);
+        if (epi) epi_rest(pv);
       }
       pv = Item{b, h, kb, k0};
     }
-    if (it > 0) {  // the last item's epilogue
+    if (grp == 0 && it > 0) {  // the last item's epilogue
       mbar_wait(acc_full, (uint32_t)(it - 1) & 1u, err);
       tc_fence_after();
       epi_load(pv);
