@@ -506,18 +506,20 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
 // The elementwise step of one key row over N query columns (c0 .. c0+N-1):
 // P^T = 2^(S^T sl2 - lse2), dS^T = P^T (dP^T - D), packed to bf16 pairs.
 // nl, nd: minus lse2 and minus D of the columns, from shared memory
-// (staged) or global memory (gl, gd: the (b, h) rows, read at c0 + i).
+// (STAGED) or global memory (gl, gd: the (b, h) rows, read at c0 + i).
 // MASK: columns before the key or past T give 0 (a masked column may hold
-// a stale lse / D: select, do not scale).
-template <int N, bool MASK>
+// a stale lse / D: select, do not scale).  Each combination is its own
+// instantiation, so that sub-blocks off the diagonal carry no
+// compare-and-select and the staged path no global-load addressing.
+template <int N, bool MASK, bool STAGED>
 __device__ __forceinline__ void kv_elementwise(const uint32_t* rs, const uint32_t* rd, const float* nl, const float* nd,
-                                               bool staged, const float* gl, const float* gd, int c0, int key, int T,
+                                               const float* gl, const float* gd, int c0, int key, int T,
                                                float sl2, uint32_t* pk, uint32_t* dk) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
   for (int i = 0; i < N; i += 4) {
     float4 a, d;
-    if (staged) {
+    if (STAGED) {
       a = *reinterpret_cast<const float4*>(nl + i);
       d = *reinterpret_cast<const float4*>(nd + i);
     } else {
@@ -872,12 +874,18 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
             mbar_wait(&q_full[s], (uint32_t)(g / ST) & 1u, err);  // the stage's lse / D
           }
           uint32_t pk[HC / 2], dk[HC / 2];
-          if (edge)
-            kv_elementwise<HC, true>(rs, rd, lc + hh * HC, lc + QS + hh * HC, staged, lse + (int64_t)bh * T,
-                                     dsum + (int64_t)bh * T, c0 + hh * HC, key, T, sl2, pk, dk);
-          else
-            kv_elementwise<HC, false>(rs, rd, lc + hh * HC, lc + QS + hh * HC, staged, lse + (int64_t)bh * T,
-                                      dsum + (int64_t)bh * T, c0 + hh * HC, key, T, sl2, pk, dk);
+          const float *gl = lse + (int64_t)bh * T, *gd = dsum + (int64_t)bh * T;
+          if (staged) {
+            if (edge)
+              kv_elementwise<HC, true, true>(rs, rd, lc + hh * HC, lc + QS + hh * HC, gl, gd, c0 + hh * HC, key, T, sl2, pk, dk);
+            else
+              kv_elementwise<HC, false, true>(rs, rd, lc + hh * HC, lc + QS + hh * HC, gl, gd, c0 + hh * HC, key, T, sl2, pk, dk);
+          } else {
+            if (edge)
+              kv_elementwise<HC, true, false>(rs, rd, lc + hh * HC, lc + QS + hh * HC, gl, gd, c0 + hh * HC, key, T, sl2, pk, dk);
+            else
+              kv_elementwise<HC, false, false>(rs, rd, lc + hh * HC, lc + QS + hh * HC, gl, gd, c0 + hh * HC, key, T, sl2, pk, dk);
+          }
           if (hh == 0 && g > 0) {
             mbar_wait(&p_empty[grp], (uint32_t)(g - 1) & 1u, err);  // dV, dK(g-1) have read the half's P^T, dS^T
             tc_fence_after();
@@ -916,16 +924,44 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 }
 
 // ============================================================ backward: dQ
-// Item (128-query block, b*h), 128-key blocks.  Warps 0..15 elementwise
-// (warps w, w+4, w+8, w+12 share lane quarter w % 4 = 32 query rows and
-// take 32 key columns each), warp 16 issues the score products, warp 17
-// loads, warp 18 issues the dQ products.
-//   S = q k^T, dP = dy v^T (M = 128 queries, N = 128 keys, K = HS);
-//   dS = P (dP - D) into TMEM; dQ += dS k (N = HS, K = 128 keys).
+// Item (128-query block, b*h), 128-key blocks, each taken in two column
+// halves of 64 keys.  Warps 0..15 elementwise in two groups: group h (warps
+// 8h..8h+7) owns key half h of every block (warps w and w+4 of a group share
+// lane quarter w % 4 = 32 query rows and take 32 key columns each); warp 16
+// issues the score products, warp 17 loads, warp 18 issues the dQ products.
+//   S = q k^T, dP = dy v^T (M = 128 queries, N = 64 keys per half, K = HS);
+//   dS = P (dP - D) into TMEM; dQ += dS k (N = HS, K = 64 keys per half).
+// Each half has its own hand-offs, so one group's TMEM traffic and
+// arithmetic overlap the other's and the tensor pipe; the item's epilogue
+// is group 0's, one item late.
 // TMEM: S 0..127, dP 128..255, dS 256..319, dQ 320..320+HS-1.
-// smem: q, dy [QB] | K ring [KST] | V ring [2] | barriers.
+// smem: q, dy [QB] | K ring [KST] | V ring [VST] | barriers.
 #define DQ_CW 16
+#define DQ_GW 8  // warps per elementwise group
 #define DQ_THREADS (DQ_CW * 32 + 96)
+// The elementwise step of one query row over N key columns (c0 .. c0+N-1):
+// dS = 2^(S sl2 - lse2) (dP - D), packed to bf16 pairs; nl2, nd2: minus
+// lse2 and minus D of the row, paired.  MASK (the diagonal block): keys past
+// the query give 0.  A separate instantiation, so that blocks off the
+// diagonal carry no compare-and-select per element.
+template <int N, bool MASK>
+__device__ __forceinline__ void dq_elementwise(const uint32_t* rs, const uint32_t* rd, uint64_t sl2x2, uint64_t nl2,
+                                               uint64_t nd2, int c0, int q, uint32_t* dk) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, nl2), x0, x1);
+    const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
+    float d0, d1;
+    f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), nd2)), d0, d1);
+    if (MASK) {
+      d0 = c0 + i <= q ? d0 : 0.f;
+      d1 = c0 + i + 1 <= q ? d1 : 0.f;
+    }
+    dk[i >> 1] = pack_bf16(d0, d1);
+  }
+}
+
 template <int HS>
 struct DqCfg {
   static constexpr uint32_t TILE = Hs<HS>::NB * 16384u;
@@ -937,7 +973,7 @@ struct DqCfg {
   // head size 64: the dQ tile leaves through shared memory and one TMA store
   static constexpr bool STAGE_OUT = HS == 64;
   static constexpr uint32_t OUT_BYTES = STAGE_OUT ? 16384u : 0u;
-  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 16 * 64 * 4 : 0u;  // column-sum partials [16][64]
+  static constexpr uint32_t RED_BYTES = STAGE_OUT ? 8 * 64 * 4 : 0u;  // column-sum partials [8][64]
   static constexpr uint32_t SMEM = 1024 + QB * 2 * TILE + (KST + VST) * TILE + OUT_BYTES + RED_BYTES + 256;
 };
 
@@ -955,7 +991,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint8_t* sK = sQ + QB * 2 * TILE;     // [KST]
   uint8_t* sV = sK + KST * TILE;        // [VST]
   uint8_t* sOut = sV + VST * TILE;  // dQ staging (head size 64)
-  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);  // [16][64] column-sum partials
+  float* red = reinterpret_cast<float*>(sOut + Cf::OUT_BYTES);  // [8][64] column-sum partials
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(red) + Cf::RED_BYTES);
   uint64_t* qd_full = bars;             // [QB]
   uint64_t* qd_empty = qd_full + QB;    // [QB]: the item's last S, dP have read q, dy
@@ -963,11 +999,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   uint64_t* k_empty = k_full + KST;     // [KST]: dQ of the block has read k
   uint64_t* v_full = k_empty + KST;     // [VST]
   uint64_t* v_empty = v_full + VST;     // [VST]
-  uint64_t* s_full = v_empty + VST;
-  uint64_t* s_free = s_full + 1;
-  uint64_t* p_full = s_free + 1;
-  uint64_t* ds_free = p_full + 1;       // dQ of the block has read dS
-  uint64_t* dq_full = ds_free + 1;      // the item's dQ complete
+  uint64_t* s_full = v_empty + VST;     // [2] S, dP of a half in TMEM
+  uint64_t* s_free = s_full + 2;        // [2] copied out by the half's group
+  uint64_t* p_full = s_free + 2;        // [2] dS of a half written by its group
+  uint64_t* ds_free = p_full + 2;       // [2] dQ of the block has read the half's dS
+  uint64_t* dq_full = ds_free + 2;      // the item's dQ complete
   uint32_t* tslot = reinterpret_cast<uint32_t*>(dq_full + 1);
 
   const int nqb = (T + 127) / 128, BH = B * NH, nitems = nqb * BH;
@@ -976,10 +1012,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
     for (int i = 0; i < QB; i++) { mbar_init(&qd_full[i], 1); mbar_init(&qd_empty[i], 1); }
     for (int i = 0; i < KST; i++) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
     for (int i = 0; i < VST; i++) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, DQ_CW);
-    mbar_init(p_full, DQ_CW);
-    mbar_init(ds_free, 1);
+    for (int i = 0; i < 2; i++) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], DQ_GW);
+      mbar_init(&p_full[i], DQ_GW);
+      mbar_init(&ds_free[i], 1);
+    }
     mbar_init(dq_full, 1);
     fence_mbar_init();
     tma_prefetch_desc(&tm_qkv);
@@ -1021,7 +1059,7 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
   } else if (warp == DQ_CW) {
     // ---------------------------------------------------------------- score MMAs
     if (lane == 0) {
-      const uint32_t idS = tc_idesc_bf16(128, 128, false, false);
+      const uint32_t idS = tc_idesc_bf16(128, 64, false, false);
       int g = 0, it = 0;
       for (int r = 0;; r++, it++) {
         const int idx = snake_item(r);
@@ -1034,21 +1072,29 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           const int ks = g % KST, vs = g % VST;
           mbar_wait(&k_full[ks], (uint32_t)(g / KST) & 1u, err);
           mbar_wait(&v_full[vs], (uint32_t)(g / VST) & 1u, err);
-          if (g > 0) mbar_wait(s_free, (uint32_t)(g - 1) & 1u, err);
-          tc_fence_after();
           const uint64_t dK = kdesc(smem_u32(sK + ks * TILE), 128, 0), dV = kdesc(smem_u32(sV + vs * TILE), 128, 0);
-          mma_hs_ss<Hs<HS>::KS>(tS, dQ, 128, dK, 128, idS);
-          mma_hs_ss<Hs<HS>::KS>(tdP, dD, 128, dV, 128, idS);
-          tc_commit(&v_empty[vs]);
-          if (j == nk - 1) tc_commit(&qd_empty[ib]);
-          tc_commit(s_full);
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {
+            // key half hf: rows 64 hf.. of the k / v tiles (8 KB in, a
+            // multiple of the 1 KB swizzle atom)
+            if (g > 0) mbar_wait(&s_free[hf], (uint32_t)(g - 1) & 1u, err);
+            tc_fence_after();
+            const uint64_t off = (uint64_t)((hf * 64 * 128) >> 4);
+            mma_hs_ss<Hs<HS>::KS>(tS + hf * 64, dQ, 128, dK + off, 128, idS);
+            mma_hs_ss<Hs<HS>::KS>(tdP + hf * 64, dD, 128, dV + off, 128, idS);
+            if (hf == 1) {
+              tc_commit(&v_empty[vs]);
+              if (j == nk - 1) tc_commit(&qd_empty[ib]);
+            }
+            tc_commit(&s_full[hf]);
+          }
         }
       }
     }
   } else if (warp == DQ_CW + 2) {
     // ---------------------------------------------------------------- dQ MMAs
-    // dQ (+)= dS(g) k(g) once dS(g) is in TMEM, from a thread on another
-    // scheduler than the score MMAs' issuer
+    // dQ (+)= dS(g, half) k(g, half) once the half's dS is in TMEM, from a
+    // thread on another scheduler than the score MMAs' issuer
     if (lane == 0) {
       const uint32_t idQ = tc_idesc_bf16(128, HS, false, true);
       int g = 0;
@@ -1057,80 +1103,89 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         if (idx >= nitems) break;
         const int nk = nqb - idx / BH;
         for (int j = 0; j < nk; j++, g++) {
-          mbar_wait(p_full, (uint32_t)g & 1u, err);
-          tc_fence_after();
           const uint64_t dKn = ndesc(smem_u32(sK + (g % KST) * TILE), 128, 0);
-          mma_ts_chain<8>(tdQ, tdS, dKn, idQ, j > 0);
-          tc_commit(&k_empty[g % KST]);
-          tc_commit(ds_free);
-          if (j == nk - 1) tc_commit(dq_full);
+#pragma unroll
+          for (int hf = 0; hf < 2; hf++) {
+            mbar_wait(&p_full[hf], (uint32_t)g & 1u, err);
+            tc_fence_after();
+            // K = the half's 64 keys: dS columns 32 hf.., k rows 64 hf..
+            mma_ts_chain<4>(tdQ, tdS + hf * 32, dKn + nstep(4 * hf), idQ, j > 0 || hf > 0);
+            tc_commit(&ds_free[hf]);
+            if (hf == 1) {
+              tc_commit(&k_empty[g % KST]);
+              if (j == nk - 1) tc_commit(dq_full);
+            }
+          }
         }
       }
     }
   } else {
     // ---------------------------------------------------------------- elementwise warps
-    const int quarter = warp & 3, cg = warp >> 2;
+    const int quarter = warp & 3, cg = warp >> 2, grp = cg >> 1;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const float sl2 = scale * LOG2E_F;
-    // epilogue of an item: warp cg takes dQ columns cg*HS/4 .. cg*HS/4 +
-    // HS/4 - 1.  It runs one item late: epi_load reads the accumulator
-    // (everything that must precede the next item's first dQ products),
+    // epilogue of an item, by group 0 (warps 0..7): warp cg (0 or 1) takes
+    // dQ columns cg*HS/2 .. cg*HS/2 + HS/2 - 1 of its 32 query rows.  It runs
+    // one item late: epi_load reads the accumulator (everything that must
+    // precede the next item's first dQ products, which wait for group 0),
     // epi_rest writes it out.
-    constexpr int EQ = HS / 4;
+    constexpr int EQ = HS / 2;
     struct Item { int b, h, qb; };
     Item pv = {0, 0, 0};
-    uint32_t pr[Cf::STAGE_OUT ? EQ / 2 : 1];  // the warp's columns as bf16 pairs, kept for epi_rest
     auto epi_load = [&](const Item& p) {
-      uint32_t ra[EQ];
-      tmem_ld_cols<EQ>(tdQ + lb + cg * EQ, ra);
-      tmem_ld_wait();
       if constexpr (Cf::STAGE_OUT) {
+        // 32 columns of the warp's 32 query rows into the 128B-swizzled
+        // staging tile (row = query, 16-byte chunks 4cg .. 4cg+3), once the
+        // previous item's store has read it
+        if (tid == 0) bulk_wait_read0();
+        named_bar_sync(1, DQ_GW * 32);
+        uint32_t ra[32];
+        tmem_ld32(tdQ + lb + cg * 32, ra);
+        tmem_ld_wait();
+        uint8_t* rowp = sOut + row * 128;
 #pragma unroll
-        for (int i = 0; i < EQ / 2; i++) pr[i] = pack_bf16(__uint_as_float(ra[2 * i]) * scale, __uint_as_float(ra[2 * i + 1]) * scale);
+        for (int qq = 0; qq < 4; qq++) {
+          uint4 u;
+          u.x = pack_bf16(__uint_as_float(ra[8 * qq]) * scale, __uint_as_float(ra[8 * qq + 1]) * scale);
+          u.y = pack_bf16(__uint_as_float(ra[8 * qq + 2]) * scale, __uint_as_float(ra[8 * qq + 3]) * scale);
+          u.z = pack_bf16(__uint_as_float(ra[8 * qq + 4]) * scale, __uint_as_float(ra[8 * qq + 5]) * scale);
+          u.w = pack_bf16(__uint_as_float(ra[8 * qq + 6]) * scale, __uint_as_float(ra[8 * qq + 7]) * scale);
+          *reinterpret_cast<uint4*>(rowp + (((cg * 4 + qq) ^ (row & 7)) << 4)) = u;
+        }
       } else {
+        // rows straight to global memory
         const int q = p.qb * 128 + row;
-        float v[EQ];
+        constexpr int EC = EQ < 32 ? EQ : 32;  // columns per chunk
 #pragma unroll
-        for (int i = 0; i < EQ; i++) v[i] = __uint_as_float(ra[i]) * scale;
-        if constexpr (EQ >= 8) {
-          if (q < T) store_bf16_row<EQ>(dqkv + ((int64_t)p.b * T + q) * 3 * (int64_t)C + p.h * HS + cg * EQ, v, 1.f);
-        } else {
-          if (q < T) {  // 4 columns: one 8-byte store
-            uint2 u;
-            u.x = pack_bf16(v[0], v[1]);
-            u.y = pack_bf16(v[2], v[3]);
-            *reinterpret_cast<uint2*>(dqkv + ((int64_t)p.b * T + q) * 3 * (int64_t)C + p.h * HS + cg * EQ) = u;
-          }
+        for (int e = 0; e < EQ; e += EC) {
+          uint32_t ra[EC];
+          tmem_ld_cols<EC>(tdQ + lb + cg * EQ + e, ra);
+          tmem_ld_wait();
+          float v[EC];
+#pragma unroll
+          for (int i = 0; i < EC; i++) v[i] = __uint_as_float(ra[i]) * scale;
+          if (q < T) store_bf16_row<EC>(dqkv + ((int64_t)p.b * T + q) * 3 * (int64_t)C + p.h * HS + cg * EQ + e, v, 1.f);
         }
       }
     };
     auto epi_rest = [&](const Item& p) {
       if constexpr (Cf::STAGE_OUT) {
-        // 16 columns of the warp's 32 query rows into the 128B-swizzled
-        // staging tile (row = query, 16-byte chunks 2cg, 2cg+1), then one
-        // TMA store of the [128 x 64] tile (rows past T are not written)
-        if (tid == 0) bulk_wait_read0();  // the previous item's store has read the staging tile
-        named_bar_sync(1, DQ_CW * 32);
-        uint8_t* rowp = sOut + row * 128;
-#pragma unroll
-        for (int qq = 0; qq < 2; qq++)
-          *reinterpret_cast<uint4*>(rowp + (((cg * 2 + qq) ^ (row & 7)) << 4)) =
-              make_uint4(pr[4 * qq], pr[4 * qq + 1], pr[4 * qq + 2], pr[4 * qq + 3]);
+        // one TMA store of the [128 x 64] tile (rows past T are not written)
         fence_proxy_async_smem();
-        named_bar_sync(1, DQ_CW * 32);
+        named_bar_sync(1, DQ_GW * 32);
         if (tid == 0) {
           tma_store_3d(&tm_out, sOut, p.h * HS, p.qb * 128, p.b);
           bulk_commit();
         }
         // column sums of the tile over its query rows below T (one partial
         // row of the qkv bias gradient per (batch row, query block)): warp w
-        // sums 8 rows, lane l columns 2l and 2l + 1, then the 16 row groups
+        // sums 16 rows, lane l columns 2l and 2l + 1, then the 8 row groups
         // are added in order
         const int c2 = 2 * lane;
         float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int r = warp * 8; r < warp * 8 + 8; r++) {
+#pragma unroll 4
+        for (int r = warp * 16; r < warp * 16 + 16; r++) {
           if (p.qb * 128 + r < T) {
             const uint32_t u = *reinterpret_cast<const uint32_t*>(sOut + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
             const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
@@ -1140,11 +1195,11 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         }
         red[warp * 64 + c2] = s0;
         red[warp * 64 + c2 + 1] = s1;
-        named_bar_sync(1, DQ_CW * 32);
+        named_bar_sync(1, DQ_GW * 32);
         if (tid < 64) {
           float sum = 0.f;
 #pragma unroll
-          for (int q = 0; q < 16; q++) sum += red[q * 64 + tid];
+          for (int q = 0; q < 8; q++) sum += red[q * 64 + tid];
           bias_partial[((int64_t)p.b * nqb + p.qb) * 3 * (int64_t)C + p.h * HS + tid] = sum;
         }
       }
@@ -1160,11 +1215,12 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
       const float nd = q < T ? dsum[(int64_t)bh * T + q] : 0.f;
       const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
       for (int j = 0; j < nk; j++, g++) {
-        mbar_wait(s_full, (uint32_t)g & 1u, err);
+        mbar_wait(&s_full[grp], (uint32_t)g & 1u, err);
         tc_fence_after();
         const bool diag = j == nk - 1;
-        // two halves of 16 columns, each loaded, computed and stored before
-        // the next is loaded; S and dP are free once both halves are read
+        // two pieces of 16 columns, each loaded, computed and stored before
+        // the next is loaded; the group's S and dP columns are free once
+        // both pieces are read
 #pragma unroll
         for (int hh = 0; hh < 2; hh++) {
           uint32_t rs[16], rd[16];
@@ -1174,46 +1230,38 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
           if (hh == 1) {
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
+            if (lane == 0) mbar_arrive(&s_free[grp]);
           }
-          const int c0 = j * 128 + cg * 32 + hh * 16;  // key of the half's column 0
+          const int c0 = j * 128 + cg * 32 + hh * 16;  // key of the piece's column 0
           uint32_t dk[8];
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(rs[i]), __uint_as_float(rs[i + 1])), sl2x2, nl2), x0, x1);
-            const float p0 = ex2_hw(x0), p1 = ex2_hw(x1);
-            float d0, d1;
-            f2_unpack(f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(rd[i]), __uint_as_float(rd[i + 1])), nd2)), d0, d1);
-            if (diag) {
-              d0 = c0 + i <= q ? d0 : 0.f;
-              d1 = c0 + i + 1 <= q ? d1 : 0.f;
-            }
-            dk[i >> 1] = pack_bf16(d0, d1);
-          }
+          if (diag)  // the block on the diagonal: keys past the query give 0
+            dq_elementwise<16, true>(rs, rd, sl2x2, nl2, nd2, c0, q, dk);
+          else
+            dq_elementwise<16, false>(rs, rd, sl2x2, nl2, nd2, c0, q, dk);
           if (hh == 0 && g > 0) {
-            mbar_wait(ds_free, (uint32_t)(g - 1) & 1u, err);  // dQ(g-1) has read dS
+            mbar_wait(&ds_free[grp], (uint32_t)(g - 1) & 1u, err);  // dQ(g-1) has read the half's dS
             tc_fence_after();
           }
           tmem_st8(tdS + lb + cg * 16 + hh * 8, dk);
         }
         tmem_st_wait();
-        if (j == 0 && it > 0) {
+        const bool epi = grp == 0 && j == 0 && it > 0;
+        if (epi) {
           // the previous item's dQ leaves TMEM before this item's first dQ
-          // products overwrite it; the rest of its epilogue runs while the
-          // tensor pipe works on this item
+          // products (half 0, group 0's) overwrite it; the rest of its
+          // epilogue runs while the tensor pipe works on this item
           mbar_wait(dq_full, (uint32_t)(it - 1) & 1u, err);
           tc_fence_after();
           epi_load(pv);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
-        if (j == 0 && it > 0) epi_rest(pv);
+        if (lane == 0) mbar_arrive(&p_full[grp]);
+        if (epi) epi_rest(pv);
       }
       pv = Item{b, h, qb};
     }
-    if (it > 0) {  // the last item's epilogue
+    if (grp == 0 && it > 0) {  // the last item's epilogue
       mbar_wait(dq_full, (uint32_t)(it - 1) & 1u, err);
       tc_fence_after();
       epi_load(pv);
