@@ -276,16 +276,18 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
     """attn_bwd_dq_tc_kernel.  Loader: per item q, dy into buffer it % qb
     once the item qb back has issued its last S, dP; per key block k into
     stage g % kst once dQ(g - kst) has read it, v into stage g % vst once
-    dP(g - vst) has.  Score issuer, over all blocks in turn: S(g), dP(g)
-    once the warps have copied out S(g - 1), dP(g - 1).  dQ issuer
-    (another thread): dQ(g) from dS(g) (an item's last one also commits
-    dQ's completion).
-    Elementwise warps, in two halves of a block's columns: copy one half
-    of S, dP out, write its dS once dQ(g - 1) has read dS; then the other
-    half, after which S, dP are free.  An item's dQ is read one item late,
-    in the next item's first block before its dQ products are released
-    (and the last item's after the loop)."""
+    dP(g - vst) has.  Every block is taken in two key halves with their own
+    hand-offs.  Score issuer, over all blocks and halves in turn: S, dP
+    (g, h) once group h has copied out its half of g - 1.  dQ issuer
+    (another thread): dQ from dS (g, h), half 0 before half 1; the first of
+    an item overwrites dQ, its last commits dQ's completion.
+    Elementwise warps, two groups (group h owns half h): copy the half of S,
+    dP out in two pieces, write its dS once dQ (g - 1, h) has read it.  An
+    item's dQ is read by group 0, one item late, in the next item's first
+    block before its half-0 products are released (and the last item's
+    after the loop)."""
     sim = Sim(seed, plant)
+    gw = ncomp // 2
     for i in range(qb):
         sim.bar("qf%d" % i)
         sim.bar("qe%d" % i)
@@ -295,10 +297,11 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
     for s in range(vst):
         sim.bar("vf%d" % s)
         sim.bar("ve%d" % s)
-    sim.bar("sf")
-    sim.bar("sfree", ncomp)
-    sim.bar("pf", ncomp)
-    sim.bar("dsf")
+    for h in range(2):
+        sim.bar("sf%d" % h)
+        sim.bar("sfree%d" % h, gw)
+        sim.bar("pf%d" % h, gw)
+        sim.bar("dsf%d" % h)
     sim.bar("dqf")
 
     def loader():
@@ -327,13 +330,15 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
                 ks, vs = g % kst, g % vst
                 yield from sim.wait("kf%d" % ks, g // kst)
                 yield from sim.wait("vf%d" % vs, g // vst)
-                if g > 0:
-                    yield from sim.wait("sfree", g - 1)
-                sim.mma(reads=("sQ%d" % b, "sD%d" % b, "sK%d" % ks, "sV%d" % vs), writes=("S", "dP"))
-                sim.commit("ve%d" % vs, phase=g // vst)
-                if j == nk - 1:
-                    sim.commit("qe%d" % b, phase=it // qb)
-                sim.commit("sf", phase=g)
+                for h in range(2):
+                    if g > 0:
+                        yield from sim.wait("sfree%d" % h, g - 1)
+                    sim.mma(reads=("sQ%d" % b, "sD%d" % b, "sK%d" % ks, "sV%d" % vs), writes=("S%d" % h, "dP%d" % h))
+                    if h == 1:
+                        sim.commit("ve%d" % vs, phase=g // vst)
+                        if j == nk - 1:
+                            sim.commit("qe%d" % b, phase=it // qb)
+                    sim.commit("sf%d" % h, phase=g)
                 g += 1
 
     def dq_mma():
@@ -341,53 +346,55 @@ def dq(items, seed, plant=None, ncomp=DQ_WARPS, qb=DQ_QB, kst=DQ_KST, vst=DQ_VST
         for it, nk in enumerate(items):
             for j in range(nk):
                 ks = g % kst
-                yield from sim.wait("pf", g)
-                sim.mma(reads=("dS", "sK%d" % ks) + (() if j == 0 else ("dQ",)), writes=("dQ",))
-                sim.commit("ke%d" % ks, phase=g // kst)
-                sim.commit("dsf", phase=g)
-                if j == nk - 1:
-                    sim.commit("dqf", phase=it)
+                for h in range(2):
+                    k = g if plant != "ds_wrong_phase" else g + 1
+                    yield from sim.wait("pf%d" % h, k)
+                    sim.mma(reads=("dS%d" % h, "sK%d" % ks) + (() if (j == 0 and h == 0) else ("dQ",)), writes=("dQ",))
+                    sim.commit("dsf%d" % h, phase=g)
+                    if h == 1:
+                        sim.commit("ke%d" % ks, phase=g // kst)
+                        if j == nk - 1:
+                            sim.commit("dqf", phase=it)
                 g += 1
 
-    def compute():
+    def compute(h):
         g = 0
         for it, nk in enumerate(items):
             for j in range(nk):
-                yield from sim.wait("sf", g)
-                # two halves: each read, computed and its dS written before the next
+                yield from sim.wait("sf%d" % h, g)
+                # two pieces: each read, computed and its dS written before the next
                 t0 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "r", t0, "S", "dP")
+                sim.touch("warp", "r", t0, "S%d" % h, "dP%d" % h)
                 yield from sim.work()
                 if g > 0:
-                    k = g - 1 if plant != "ds_wrong_phase" else g
-                    yield from sim.wait("dsf", k)
+                    yield from sim.wait("dsf%d" % h, g - 1)
                 t1 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "w", t1, "dS")
+                sim.touch("warp", "w", t1, "dS%d" % h)
                 t2 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "r", t2, "S", "dP")
-                sim.arrive("sfree", phase=g)
+                sim.touch("warp", "r", t2, "S%d" % h, "dP%d" % h)
+                sim.arrive("sfree%d" % h, phase=g)
                 t3 = sim.t
                 yield from sim.work(1, 2)
-                sim.touch("warp", "w", t3, "dS")
-                if j == 0 and it > 0:
+                sim.touch("warp", "w", t3, "dS%d" % h)
+                if h == 0 and j == 0 and it > 0:
                     # the previous item's dQ read before this item's first
                     # dQ products overwrite it
                     yield from sim.wait("dqf", it - 1)
                     t4 = sim.t
                     yield from sim.work(1, 2)
                     sim.touch("warp", "r", t4, "dQ")
-                sim.arrive("pf", phase=g)
+                sim.arrive("pf%d" % h, phase=g)
                 g += 1
-        if items:  # the last item's dQ
+        if h == 0 and items:  # the last item's dQ
             yield from sim.wait("dqf", len(items) - 1)
             t5 = sim.t
             yield from sim.work(1, 3)
             sim.touch("warp", "r", t5, "dQ")
 
-    sim.run([loader(), score_mma(), dq_mma()] + [compute() for _ in range(ncomp)])
+    sim.run([loader(), score_mma(), dq_mma()] + [compute(w // gw) for w in range(ncomp)])
     return sim.errors
 
 
