@@ -194,18 +194,26 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records a timeout) if the time limit passes first.
+// false (and records a timeout) if the time limit passes first.  Between
+// tests only the SM cycle counter is read: the error word (global memory)
+// is looked at about once per 2^20 cycles, so that a wait whose phase
+// completes is not held up behind a load from L2.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = sm_cycles();
+  long long check = t0 + (1ll << 20);
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-    // once any wait of the launch has given up, the others stop early
-    // instead of each spending the full limit
-    if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
-    if (sm_cycles() - t0 > GPT2_WAIT_LIMIT_CYCLES) {
-      record_error(err, DEVERR_TIMEOUT);
-      return false;
+    const long long t = sm_cycles();
+    if (t > check) {
+      // once any wait of the launch has given up, the others stop early
+      // instead of each spending the full limit
+      if (err && (*reinterpret_cast<volatile int*>(err) & DEVERR_TIMEOUT)) return false;
+      if (t - t0 > GPT2_WAIT_LIMIT_CYCLES) {
+        record_error(err, DEVERR_TIMEOUT);
+        return false;
+      }
+      check = t + (1ll << 20);
     }
   }
 }
