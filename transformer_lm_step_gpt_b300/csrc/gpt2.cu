@@ -508,12 +508,14 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
   ActT* dbig = reinterpret_cast<ActT*>(m->dbig);
   ActT* datty = reinterpret_cast<ActT*>(m->datty);
   // tied head: logits = lnf wte^T
-  run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, m->dln, C, true), GS_HEAD);
+  // the LayerNorm input gradients (dln) are in the activation type
+  ActT* dln = reinterpret_cast<ActT*>(m->dln);
+  run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, dln, C, f32), GS_HEAD);
   run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true), GS_HEAD);
   {
     ProfScope ps(m, PC_LN_BWD, lnb_bytes - 4.0 * M * C);
     launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB),
-                               m->G(FCPROJB) + (int64_t)(L - 1) * C, m->dln, m->res[L],
+                               m->G(FCPROJB) + (int64_t)(L - 1) * C, dln, m->res[L],
                                m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
   }
   for (int l = L - 1; l >= 0; l--) {
@@ -536,7 +538,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     // backward that produced dres (LN_f or the next block's LN1)
     // fc: x = ln2 Wfc^T + b
     run_gemm(m, c, gemm(M, C, 4 * C, dbig, 4 * C, true, w(FCW, (int64_t)l * 4 * C * C), C, false,
-                        EPI_STORE, m->dln, C, true), GS_FC);
+                        EPI_STORE, dln, C, f32), GS_FC);
     run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,
                         m->G(FCW) + (int64_t)l * 4 * C * C, C, true), GS_FC);
     {
@@ -547,7 +549,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
       launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
-                                 m->G(ATTPROJB) + (int64_t)l * C, m->dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
+                                 m->G(ATTPROJB) + (int64_t)l * C, dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
                                  m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
     }
     // attproj: mid = res[l] + atty Wproj^T + b.  At head size 64 (tensor-core
@@ -577,7 +579,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
-                        EPI_STORE, m->dln, C, true), GS_QKV);
+                        EPI_STORE, dln, C, f32), GS_QKV);
     run_gemm(m, c, gemm(3 * C, C, M, dbig, 3 * C, false, ln1, C, false, EPI_ACCUM,
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
     {
@@ -590,7 +592,7 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
       launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
-                                 l > 0 ? m->G(FCPROJB) + (int64_t)(l - 1) * C : nullptr, m->dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
+                                 l > 0 ? m->G(FCPROJB) + (int64_t)(l - 1) * C : nullptr, dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
                                  m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
     }
   }

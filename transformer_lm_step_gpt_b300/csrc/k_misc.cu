@@ -535,9 +535,18 @@ static size_t lnb_smem(int C) {
 // adds the blocks' rows in order.
 //   xhat = (x - mean) rstd, g = dy * gamma,
 //   dx = rstd (g - mean(g) - xhat mean(g xhat)),  dres (+)= dx.
+// Four consecutive values as fp32 (a 16-byte fp32 or an 8-byte bf16 load).
+__device__ __forceinline__ float4 load4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4f(const bf16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
 template <typename ActT, int NCH>
 __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
-    layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const float* dy,
+    layernorm_bwd_kernel(float* dres, ActT* dres_act, float* partial, const ActT* dy,
                          const float* inp, const float* w, const float* mean, const float* rstd,
                          int N, int C, int accumulate, int* err) {
   pdl_trigger();
@@ -563,11 +572,11 @@ __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
   }
   pdl_wait();  // from here on global memory written by the previous kernel is read
   const int gw = blockIdx.x * LNB_WARPS + warp, nw = gridDim.x * LNB_WARPS;
-  const uint32_t rowbytes = (uint32_t)C * sizeof(float);
+  const uint32_t rowbytes = (uint32_t)C * sizeof(float), dybytes = (uint32_t)C * sizeof(ActT);
   auto issue = [&](int row, int s) {
-    float* st = ring + (size_t)s * 3 * C;
-    mbar_arrive_expect_tx(&bars[s], (accumulate ? 3u : 2u) * rowbytes);
-    bulk_load(st, dy + (int64_t)row * C, rowbytes, &bars[s]);
+    float* st = ring + (size_t)s * 3 * C;  // dy (C values of ActT) | x | old dres
+    mbar_arrive_expect_tx(&bars[s], (accumulate ? 2u : 1u) * rowbytes + dybytes);
+    bulk_load(st, dy + (int64_t)row * C, dybytes, &bars[s]);
     bulk_load(st + C, inp + (int64_t)row * C, rowbytes, &bars[s]);
     if (accumulate) bulk_load(st + 2 * C, dres + (int64_t)row * C, rowbytes, &bars[s]);
   };
@@ -583,8 +592,8 @@ __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
     float mn = 0.f, rn = 0.f;  // next row's statistics, loaded ahead
     if (nrow < N) { mn = mean[nrow]; rn = rstd[nrow]; }
     mbar_wait(&bars[s], (uint32_t)(it / LNB_STAGES) & 1u, err);
-    const float* g = ring + (size_t)s * 3 * C;
-    const float* x = g + C;
+    const ActT* g = reinterpret_cast<const ActT*>(ring + (size_t)s * 3 * C);
+    const float* x = ring + (size_t)s * 3 * C + C;
     const float* o = x + C;
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
@@ -592,7 +601,7 @@ __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
       const int c = (lane + 32 * k) * 4;
       if (c < C) {
         const float4 xv = *reinterpret_cast<const float4*>(x + c);
-        const float4 gv = *reinterpret_cast<const float4*>(g + c);
+        const float4 gv = load4f(g + c);
         const float h0 = gv.x * wv[k].x, h1 = gv.y * wv[k].y, h2 = gv.z * wv[k].z, h3 = gv.w * wv[k].w;
         s1 += (h0 + h1) + (h2 + h3);
         s2 += (h0 * (xv.x - m) * r + h1 * (xv.y - m) * r) + (h2 * (xv.z - m) * r + h3 * (xv.w - m) * r);
@@ -606,7 +615,7 @@ __global__ void __launch_bounds__(LNB_WARPS * 32, 1)
       const int c = (lane + 32 * k) * 4;
       if (c < C) {
         const float4 xv = *reinterpret_cast<const float4*>(x + c);
-        const float4 gv = *reinterpret_cast<const float4*>(g + c);
+        const float4 gv = load4f(g + c);
         const float x0 = (xv.x - m) * r, x1 = (xv.y - m) * r, x2 = (xv.z - m) * r, x3 = (xv.w - m) * r;
         float4 d;
         d.x = r * (gv.x * wv[k].x - mg - x0 * mgx);
@@ -686,7 +695,7 @@ __global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
 
 template <typename ActT, int NCH>
 static void ln_bwd_launch(LaunchCtx& c, int nb, float* dres, ActT* dres_act, float* partial,
-                          const float* dy, const float* inp, const float* w, const float* mean,
+                          const ActT* dy, const float* inp, const float* w, const float* mean,
                           const float* rstd, int N, int C, bool accumulate) {
   const size_t smem = lnb_smem(C);
   cudaFuncSetAttribute(layernorm_bwd_kernel<ActT, NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -696,7 +705,7 @@ static void ln_bwd_launch(LaunchCtx& c, int nb, float* dres, ActT* dres_act, flo
 
 template <typename ActT>
 void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
-                          float* dres_colsum, const float* dy, const float* inp, const float* w,
+                          float* dres_colsum, const ActT* dy, const float* inp, const float* w,
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial) {
   int nb = cdiv(N, LNB_ROWS_PER_BLOCK);  // one partial row per block: nb <= ln_partial_floats / (3C)
@@ -717,7 +726,7 @@ template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, fl
                                           const float*, const float*, const float*, const float*,
                                           const float*, int, int, bool, float*);
 template void launch_layernorm_bwd<bf16>(LaunchCtx&, float*, bf16*, float*, float*, float*,
-                                         const float*, const float*, const float*, const float*,
+                                         const bf16*, const float*, const float*, const float*,
                                          const float*, int, int, bool, float*);
 
 // ============================================================ column sums

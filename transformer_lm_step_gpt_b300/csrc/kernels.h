@@ -89,10 +89,11 @@ void launch_layernorm_fwd(LaunchCtx& c, OutT* out, float* mean, float* rstd, con
                           const float* w, const float* b, int N, int C);
 // dres (+)= dx; dres_act = dres in ActT (if non-null); dw, db += column
 // sums; dres_colsum (if non-null) += column sums of the updated dres; via
-// partials (float [ln_partial_floats(N, C)]).
+// partials (float [ln_partial_floats(N, C)]).  dy (the gradient of the
+// LayerNorm output) is in ActT too.
 template <typename ActT>
 void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
-                          float* dres_colsum, const float* dy, const float* inp, const float* w,
+                          float* dres_colsum, const ActT* dy, const float* inp, const float* w,
                           const float* mean, const float* rstd, int N, int C, bool accumulate,
                           float* partial);
 int64_t ln_partial_floats(int N, int C);
