@@ -154,6 +154,29 @@ __device__ __forceinline__ float4 load_bias4(const GemmArgs& g, bool use_bias, i
   return b;
 }
 
+// gelu(x) and gelu'(x) (tanh form) of 8 values, in f32x2 pairs with one
+// tanh.approx per value.  With S = sqrt(2/pi), A = 0.044715, x2 = x^2,
+// th = tanh(x (S + S A x2)), h = (1 + th)/2 and m = (1 - th)/2:
+//   gelu(x)  = x h
+//   gelu'(x) = h + x (1 - th^2) (S/2 + 3 S A x2/2) = h + (x (2S + 6 S A x2)) (h m)
+// since 1 - th^2 = 4 h m.
+__device__ __forceinline__ void gelu8_f2(const float* x, float* gl, float* gd) {
+  const uint64_t c_sa = f2_pack(GELU_S * GELU_A, GELU_S * GELU_A), c_s = f2_pack(GELU_S, GELU_S);
+  const uint64_t c_h = f2_pack(0.5f, 0.5f), c_nh = f2_pack(-0.5f, -0.5f);
+  const uint64_t c_sa6 = f2_pack(6.f * GELU_S * GELU_A, 6.f * GELU_S * GELU_A), c_s2 = f2_pack(2.f * GELU_S, 2.f * GELU_S);
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint64_t xx = f2_pack(x[i], x[i + 1]);
+    const uint64_t x2 = f2_mul(xx, xx);
+    float z0, z1;
+    f2_unpack(f2_mul(xx, f2_fma(x2, c_sa, c_s)), z0, z1);
+    const uint64_t th = f2_pack(tanh_hw(z0), tanh_hw(z1));
+    const uint64_t h = f2_fma(th, c_h, c_h), m = f2_fma(th, c_nh, c_h);
+    f2_unpack(f2_mul(xx, h), gl[i], gl[i + 1]);
+    f2_unpack(f2_fma(f2_mul(xx, f2_fma(x2, c_sa6, c_s2)), f2_mul(h, m), h), gd[i], gd[i + 1]);
+  }
+}
+
 // EPI_DOT_AUX: minus the dot product of row m's 64 columns from n (one
 // attention head) into dot_out[(b * (N / 64) + n / 64) * dot_T + t],
 // m = b * dot_T + t
@@ -168,6 +191,9 @@ __device__ __forceinline__ void store_dot(const GemmArgs& g, int m, int n, float
 // warp's TMEM lane quarter, global rows mrow..mrow+31) by the warp's column
 // half of the BN columns starting at n0.  taddr: TMEM address of the
 // accumulator at (lane quarter, column 0); bq: load_bias4 of the tile.
+// The fp32 arithmetic runs in f32x2 pairs: the warps of lane quarter 1
+// share a scheduler with the thread that issues the MMAs, and packed
+// instructions take half the issue slots of scalar ones.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& em, uint8_t* stg,
                                               uint64_t* abar, uint32_t& aux_phase, uint32_t taddr0,
@@ -226,10 +252,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
       for (int j = 0; j < 64; j += 4) {
         if (j < CW) {
           const int src = lb + (j >> 2);
-          v[j] += __shfl_sync(0xffffffffu, bq.x, src);
-          v[j + 1] += __shfl_sync(0xffffffffu, bq.y, src);
-          v[j + 2] += __shfl_sync(0xffffffffu, bq.z, src);
-          v[j + 3] += __shfl_sync(0xffffffffu, bq.w, src);
+          const float b0 = __shfl_sync(0xffffffffu, bq.x, src), b1 = __shfl_sync(0xffffffffu, bq.y, src);
+          const float b2 = __shfl_sync(0xffffffffu, bq.z, src), b3 = __shfl_sync(0xffffffffu, bq.w, src);
+          f2_unpack(f2_add(f2_pack(v[j], v[j + 1]), f2_pack(b0, b1)), v[j], v[j + 1]);
+          f2_unpack(f2_add(f2_pack(v[j + 2], v[j + 3]), f2_pack(b2, b3)), v[j + 2], v[j + 3]);
         }
       }
     }
@@ -246,7 +272,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
         float4 o = make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
         if (has_aux) {  // EPI_RESIDUAL: out = residual + (acc + bias)
           const float4 r = *p;
-          o.x = r.x + o.x; o.y = r.y + o.y; o.z = r.z + o.z; o.w = r.w + o.w;
+          f2_unpack(f2_add(f2_pack(r.x, r.y), f2_pack(o.x, o.y)), o.x, o.y);
+          f2_unpack(f2_add(f2_pack(r.z, r.w), f2_pack(o.z, o.w)), o.z, o.w);
         }
         *p = o;
       }
@@ -266,11 +293,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
             }
           } else {
 #pragma unroll
-            for (int q = 0; q < 8; q++) o[q] = v[8 * c + q] * hv[q];
+            for (int q = 0; q < 8; q += 2)
+              f2_unpack(f2_mul(f2_pack(v[8 * c + q], v[8 * c + q + 1]), f2_pack(hv[q], hv[q + 1])), o[q], o[q + 1]);
           }
         } else if (epi == EPI_GELU_FWD && !split) {  // out = gelu'(x); v keeps gelu(x) for out2
+          {
+            float gl[8];
+            gelu8_f2(&v[8 * c], gl, o);
 #pragma unroll
-          for (int q = 0; q < 8; q++) gelu_and_grad_hw(v[8 * c + q], v[8 * c + q], o[q]);
+            for (int q = 0; q < 8; q++) v[8 * c + q] = gl[q];
+          }
           if (stg2) put8_bf16(stg2 + stg_off(lane, c), &v[8 * c]);  // gelu(x) into the second buffer
         } else {
 #pragma unroll
@@ -292,15 +324,16 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, const EpiMaps& 
     if (g.colsum_out && !f32 && !split) {
       // column sums of the stored values over the warp's 32 rows, read back
       // from the staging rows (lane l: columns 2l, 2l+1 of the chunk)
-      float s0 = 0.f, s1 = 0.f;
+      uint64_t s01 = f2_pack(0.f, 0.f);
       const int ch = lane >> 2, wo = (lane & 3) * 4;
 #pragma unroll 8
       for (int r = 0; r < 32; r++) {
         const uint32_t u = *reinterpret_cast<const uint32_t*>(stg + r * 128 + ((ch ^ (r & 7)) << 4) + wo);
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-        s0 += f.x;
-        s1 += f.y;
+        s01 = f2_add(s01, f2_pack(f.x, f.y));
       }
+      float s0, s1;
+      f2_unpack(s01, s0, s1);
       const int n = ncol + 2 * lane;
       if (mrow < g.M && n < g.N)
         *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);
@@ -399,10 +432,10 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
       for (int j = 0; j < 64; j += 4) {
         if (j < CW) {
           const int src = lb + (j >> 2);
-          v[j] += __shfl_sync(0xffffffffu, bq.x, src);
-          v[j + 1] += __shfl_sync(0xffffffffu, bq.y, src);
-          v[j + 2] += __shfl_sync(0xffffffffu, bq.z, src);
-          v[j + 3] += __shfl_sync(0xffffffffu, bq.w, src);
+          const float b0 = __shfl_sync(0xffffffffu, bq.x, src), b1 = __shfl_sync(0xffffffffu, bq.y, src);
+          const float b2 = __shfl_sync(0xffffffffu, bq.z, src), b3 = __shfl_sync(0xffffffffu, bq.w, src);
+          f2_unpack(f2_add(f2_pack(v[j], v[j + 1]), f2_pack(b0, b1)), v[j], v[j + 1]);
+          f2_unpack(f2_add(f2_pack(v[j + 2], v[j + 3]), f2_pack(b2, b3)), v[j + 2], v[j + 3]);
         }
       }
     }
@@ -414,7 +447,10 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
       for (int q = 0; q < 8; q++) {
         float4* pp = reinterpret_cast<float4*>(stg + stg_off(lane, q));
         const float4 r = *pp;
-        *pp = make_float4(r.x + v[4 * q], r.y + v[4 * q + 1], r.z + v[4 * q + 2], r.w + v[4 * q + 3]);
+        float4 o;
+        f2_unpack(f2_add(f2_pack(r.x, r.y), f2_pack(v[4 * q], v[4 * q + 1])), o.x, o.y);
+        f2_unpack(f2_add(f2_pack(r.z, r.w), f2_pack(v[4 * q + 2], v[4 * q + 3])), o.z, o.w);
+        *pp = o;
       }
     } else {  // EPI_MUL_AUX: out = acc * aux
 #pragma unroll
@@ -430,7 +466,8 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
           }
         } else {  // EPI_MUL_AUX: out = acc * aux
 #pragma unroll
-          for (int k = 0; k < 8; k++) o[k] = v[8 * q + k] * hv[k];
+          for (int k = 0; k < 8; k += 2)
+            f2_unpack(f2_mul(f2_pack(v[8 * q + k], v[8 * q + k + 1]), f2_pack(hv[k], hv[k + 1])), o[k], o[k + 1]);
         }
         put8_bf16(pp, o);
       }
@@ -443,15 +480,16 @@ __device__ __forceinline__ void epilogue_tile_aux(const GemmArgs& g, const EpiMa
     }
     if (g.epi == EPI_DOT_AUX) store_dot(g, mrow + lane, ncol, dot);
     if (g.colsum_out && !f32) {
-      float s0 = 0.f, s1 = 0.f;
+      uint64_t s01 = f2_pack(0.f, 0.f);
       const int ch = lane >> 2, wo = (lane & 3) * 4;
 #pragma unroll 8
       for (int r = 0; r < 32; r++) {
         const uint32_t u = *reinterpret_cast<const uint32_t*>(stg + r * 128 + ((ch ^ (r & 7)) << 4) + wo);
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-        s0 += f.x;
-        s1 += f.y;
+        s01 = f2_add(s01, f2_pack(f.x, f.y));
       }
+      float s0, s1;
+      f2_unpack(s01, s0, s1);
       const int n = ncol + 2 * lane;
       if (mrow < g.M && n < g.N)
         *reinterpret_cast<float2*>(g.colsum_out + (int64_t)(mrow >> 5) * g.N + n) = make_float2(s0, s1);

@@ -388,6 +388,28 @@ void launch_encoder_bwd(LaunchCtx& c, float* dwte, float* dwpe, const float* dou
   launch_pdl(c, encoder_bwd_combine_kernel, dim3(cdiv(M, ENC_RANGE)), dim3(256), 0, dwte, partial, sorted, M, C);
 }
 
+// 8 values at p (16-byte aligned for bf16, 32 for float), one or two 16-byte stores
+template <typename OutT>
+__device__ __forceinline__ void store8(OutT* p, const float* v);
+template <>
+__device__ __forceinline__ void store8<float>(float* p, const float* v) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+template <>
+__device__ __forceinline__ void store8<bf16>(bf16* p, const float* v) {
+  uint4 u;
+  __nv_bfloat162 t = __floats2bfloat162_rn(v[0], v[1]);
+  u.x = *reinterpret_cast<uint32_t*>(&t);
+  t = __floats2bfloat162_rn(v[2], v[3]);
+  u.y = *reinterpret_cast<uint32_t*>(&t);
+  t = __floats2bfloat162_rn(v[4], v[5]);
+  u.z = *reinterpret_cast<uint32_t*>(&t);
+  t = __floats2bfloat162_rn(v[6], v[7]);
+  u.w = *reinterpret_cast<uint32_t*>(&t);
+  *reinterpret_cast<uint4*>(p) = u;
+}
+
 // ============================================================ LayerNorm
 template <typename OutT>
 __device__ __forceinline__ void store4(OutT* p, float a, float b, float c, float d);
@@ -895,9 +917,135 @@ __global__ void __launch_bounds__(512) crossentropy_kernel(T* logits, float* los
   }
 }
 
+// The same computation with the row staged in shared memory: one thread
+// starts bulk copies of the whole row (pieces of CE_PIECE bytes, each on
+// its own mbarrier) before any arithmetic, so that a block keeps the full
+// row in flight; pass 1 folds each group of 8 into (max, sum) once its
+// piece has landed, pass 2 reads the row from shared memory and writes
+// dlogits with coalesced 16-byte stores.  The row is read from HBM once.
+#define CE_PIECE 16384
+#define CE_MAX_PIECES 14
+template <typename T>
+__global__ void __launch_bounds__(512) crossentropy_smem_kernel(T* logits, float* losses, const int32_t* targets,
+                                                                 int V, int Vp, float dscale, int write_dlogits,
+                                                                 int* err) {
+  extern __shared__ __align__(128) uint8_t ce_row[];
+  __shared__ uint64_t bar[CE_MAX_PIECES];
+  __shared__ float sm_m[32], sm_s[32];
+  const int64_t row = blockIdx.x;
+  T* l = logits + row * Vp;
+  const T* r = reinterpret_cast<const T*>(ce_row);
+  const uint32_t rowbytes = (uint32_t)Vp * sizeof(T);
+  const int np = (int)((rowbytes + CE_PIECE - 1) / CE_PIECE);
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < np; q++) mbar_init(&bar[q], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    for (int q = 0; q < np; q++) {
+      const uint32_t b = min((uint32_t)CE_PIECE, rowbytes - (uint32_t)q * CE_PIECE);
+      mbar_arrive_expect_tx(&bar[q], b);
+      bulk_load(ce_row + (size_t)q * CE_PIECE, reinterpret_cast<const uint8_t*>(l) + (size_t)q * CE_PIECE, b, &bar[q]);
+    }
+  }
+  int tg = targets ? targets[row] : -1;
+  if (targets && (tg < 0 || tg >= V)) {
+    if (threadIdx.x == 0) record_error(err, DEVERR_TOKEN);
+    tg = 0;
+  }
+  constexpr int GB = 8 * sizeof(T);  // bytes of a group of 8
+  int landed = 0;                     // pieces this thread has seen complete
+  float m = -INFINITY, s = 0.f;
+  const int nch = Vp / 8;
+  for (int q = threadIdx.x; q < nch; q += blockDim.x) {
+    const int pc = q * GB / CE_PIECE;
+    while (landed <= pc) mbar_wait(&bar[landed++], 0u, err);
+    float v[8];
+    load8<T>(r + q * 8, v);
+    const int base = q * 8;
+    if (base + 8 > V) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) v[j] = base + j < V ? v[j] : -INFINITY;
+    }
+    float cm = v[0];
+#pragma unroll
+    for (int j = 1; j < 8; j++) cm = fmaxf(cm, v[j]);
+    if (cm == -INFINITY) continue;
+    const float nm = fmaxf(m, cm), nl = -nm * LOG2E;
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; j++) a += ex2_hw(fmaf(v[j], LOG2E, nl));
+    s = s * ex2_hw((m - nm) * LOG2E) + a;
+    m = nm;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_combine(m, s, m2, s2);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  if (lane == 0) { sm_m[warp] = m; sm_s[warp] = s; }
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < nw ? sm_m[lane] : -INFINITY;
+    s = lane < nw ? sm_s[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      lse_combine(m, s, m2, s2);
+    }
+    if (lane == 0) { sm_m[0] = m; sm_s[0] = s; }
+  }
+  __syncthreads();
+  const float lse = sm_m[0] + logf(sm_s[0]);
+  if (threadIdx.x == 0 && targets) {
+    const int pc = tg * (int)sizeof(T) / CE_PIECE;
+    while (landed <= pc) mbar_wait(&bar[landed++], 0u, err);
+    losses[row] = lse - to_f(r[tg]);
+  }
+  if (!write_dlogits) return;
+  const float nl = -lse * LOG2E;
+  for (int q = threadIdx.x; q < nch; q += blockDim.x) {
+    const int pc = q * GB / CE_PIECE;
+    while (landed <= pc) mbar_wait(&bar[landed++], 0u, err);
+    float v[8];
+    load8<T>(r + q * 8, v);
+    const int base = q * 8;
+    float o[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) o[j] = ex2_hw(fmaf(v[j], LOG2E, nl)) * dscale;
+    if (base + 8 > V || (base <= tg && tg < base + 8)) {
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        if (base + j >= V) o[j] = 0.f;
+        else if (base + j == tg) o[j] -= dscale;
+      }
+    }
+    store8<T>(l + base, o);
+  }
+}
+
 template <typename T>
 void launch_crossentropy(LaunchCtx& c, T* logits, float* losses, const int32_t* targets, int M,
                          int V, int Vp, float dscale, bool dlogits) {
+  const size_t rowbytes = (size_t)Vp * sizeof(T);
+  if (rowbytes <= (size_t)CE_PIECE * CE_MAX_PIECES && rowbytes % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(logits) % 16 == 0) {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(crossentropy_smem_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           CE_PIECE * CE_MAX_PIECES);
+      attr = true;
+    }
+    launch_pdl(c, crossentropy_smem_kernel<T>, dim3(M), dim3(512), rowbytes, logits, losses, targets, V, Vp,
+               dscale, dlogits ? 1 : 0, c.err);
+    return;
+  }
   launch_pdl(c, crossentropy_kernel<T>, dim3(M), dim3(512), 0, logits, losses, targets, V, Vp, dscale,
                                                   dlogits ? 1 : 0, c.err);
 }
