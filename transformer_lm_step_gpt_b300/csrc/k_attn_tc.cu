@@ -502,6 +502,35 @@ __global__ void attn_bwd_dsum_kernel(float* dsum, const bf16* dy, const bf16* y,
   }
 }
 
+// Column sums of R rows (from r0, a multiple of 8) of a 128B-swizzled
+// [rows x 64] bf16 staging tile: lane l adds columns 2l and 2l + 1; rows at
+// or past `valid` count 0.  Full row groups take the unrolled loop with
+// constant swizzle offsets and f32x2 adds.
+template <int R>
+__device__ __forceinline__ float2 tile_colsum2(const uint8_t* tile, int r0, int valid, int lane) {
+  const int cb = lane >> 2, co = (lane & 3) * 4;
+  const uint8_t* base = tile + r0 * 128 + co;
+  uint64_t s = f2_pack(0.f, 0.f);
+  if (r0 + R <= valid) {
+#pragma unroll 8
+    for (int i = 0; i < R; i++) {
+      const uint32_t u = *reinterpret_cast<const uint32_t*>(base + i * 128 + ((cb ^ (i & 7)) << 4));
+      s = f2_add(s, f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+    }
+  } else {
+#pragma unroll 4
+    for (int i = 0; i < R; i++) {
+      if (r0 + i < valid) {
+        const uint32_t u = *reinterpret_cast<const uint32_t*>(base + i * 128 + ((cb ^ (i & 7)) << 4));
+        s = f2_add(s, f2_pack(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u)));
+      }
+    }
+  }
+  float2 o;
+  f2_unpack(s, o.x, o.y);
+  return o;
+}
+
 // ============================================================ backward: dK, dV
 // The elementwise step of one key row over N query columns (c0 .. c0+N-1):
 // P^T = 2^(S^T sl2 - lse2), dS^T = P^T (dP^T - D), packed to bf16 pairs.
@@ -598,7 +627,7 @@ struct KvCfg {
   static constexpr uint32_t SMEM = 1024 + KVB * 2 * KTILE + ST * 2 * QTILE + ST * 2 * QS * 4 + OUT_BYTES + RED_BYTES + 256;
 };
 
-template <int HS>
+template <int HS, bool STAGED>
 __global__ void __launch_bounds__(KV_THREADS, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                            const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_out,
@@ -630,7 +659,7 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
 
   const int nkb = (T + 127) / 128, BH = B * NH, nitems = nkb * BH;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const bool staged = (T & 3) == 0;
+  constexpr bool staged = STAGED;  // lse, D rows 16-byte aligned: T % 4 == 0
   if (tid == 0) {
     for (int i = 0; i < KVB; i++) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < ST; i++) { mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1); }
@@ -818,19 +847,9 @@ __global__ void __launch_bounds__(KV_THREADS, 1)
         // w / 4, lane l columns 2l and 2l + 1; the 4 row groups are then
         // added in order
         const int tt = warp >> 2, rg = warp & 3, c2 = 2 * lane;
-        const uint8_t* tile = sOut + tt * 16384;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-        for (int r = rg * 32; r < rg * 32 + 32; r++) {
-          if (p.k0 + r < T) {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(tile + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-            s0 += f.x;
-            s1 += f.y;
-          }
-        }
-        red[(tt * 4 + rg) * 64 + c2] = s0;
-        red[(tt * 4 + rg) * 64 + c2 + 1] = s1;
+        const float2 cs = tile_colsum2<32>(sOut + tt * 16384, rg * 32, T - p.k0, lane);
+        red[(tt * 4 + rg) * 64 + c2] = cs.x;
+        red[(tt * 4 + rg) * 64 + c2 + 1] = cs.y;
         named_bar_sync(1, KV_GW * 32);
         if (tid < 128) {
           const int t2 = tid >> 6, col = tid & 63;
@@ -1183,18 +1202,9 @@ __global__ void __launch_bounds__(DQ_THREADS, 1)
         // sums 16 rows, lane l columns 2l and 2l + 1, then the 8 row groups
         // are added in order
         const int c2 = 2 * lane;
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-        for (int r = warp * 16; r < warp * 16 + 16; r++) {
-          if (p.qb * 128 + r < T) {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(sOut + r * 128 + (((c2 >> 3) ^ (r & 7)) << 4) + (c2 & 7) * 2);
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u));
-            s0 += f.x;
-            s1 += f.y;
-          }
-        }
-        red[warp * 64 + c2] = s0;
-        red[warp * 64 + c2 + 1] = s1;
+        const float2 cs = tile_colsum2<16>(sOut, warp * 16, T - p.qb * 128, lane);
+        red[warp * 64 + c2] = cs.x;
+        red[warp * 64 + c2 + 1] = cs.y;
         named_bar_sync(1, DQ_GW * 32);
         if (tid < 64) {
           float sum = 0.f;
@@ -1321,8 +1331,9 @@ static void bwd_hs(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y, cons
   const float scale = 1.f / sqrtf((float)HS);
   const int nitems = ((T + 127) / 128) * B * NH;
   const int grid = std::min(nitems, c.num_sms);
-  cudaFuncSetAttribute(attn_bwd_dkv_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
-  launch_pdl(c, attn_bwd_dkv_tc_kernel<HS>, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, tout, dqkv, lse,
+  auto kv = (T & 3) == 0 ? attn_bwd_dkv_tc_kernel<HS, true> : attn_bwd_dkv_tc_kernel<HS, false>;
+  cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Kv::SMEM);
+  launch_pdl(c, kv, dim3(grid), dim3(KV_THREADS), Kv::SMEM, tq_s, tq, td_s, tout, dqkv, lse,
              (const float*)dsum, bias_partial, B, T, C, NH, scale, c.err);
   cudaFuncSetAttribute(attn_bwd_dq_tc_kernel<HS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Dq::SMEM);
   launch_pdl(c, attn_bwd_dq_tc_kernel<HS>, dim3(grid), dim3(DQ_THREADS), Dq::SMEM, tq, td, tout, dqkv, lse,
