@@ -11,7 +11,8 @@ Asynchronous work completes after random delays:
     issued has read its buffer, wait_group 0 until every store completed;
   * the MMA groups issued by one thread run one after another in issue
     order, reading their operands and writing their accumulators; a commit
-    arrives once every group issued before it has completed.
+    arrives once every group issued before it has completed (a kernel with
+    several issuing threads on separate tensor pipes names each pipe).
 
 Checks, for every interleaving tried:
   * every actor finishes (no deadlock);
@@ -38,6 +39,7 @@ class Sim:
         self.need = {}      # barrier -> arrivals that complete a phase
         self.pending = []   # (time, callback, label)
         self.pipe_t = 0     # completion time of the last MMA group issued
+        self.pipes = {}     # named pipes: pipe -> completion time of its last group
         self.acc = []       # (buffer, "r" | "w", agent, t0, t1)
         self.stores = {}    # warp -> [(read_end, complete_end)]
         self.errors = []
@@ -87,16 +89,23 @@ class Sim:
         while any(d > self.t for _, d in self.stores.get(warp, [])):
             yield
 
-    def mma(self, reads=(), writes=()):  # one group of MMAs, run in issue order
-        t0 = max(self.pipe_t, self.t)
-        self.pipe_t = t0 + self.rnd.randint(1, 30)
+    def mma(self, reads=(), writes=(), pipe=None):  # one group of MMAs, run in issue order
+        t_prev = self.pipe_t if pipe is None else self.pipes.get(pipe, 0)
+        t0 = max(t_prev, self.t)
+        t1 = t0 + self.rnd.randint(1, 30)
+        if pipe is None:
+            self.pipe_t = t1
+        else:
+            self.pipes[pipe] = t1
+        agent = "mma" if pipe is None else "mma " + pipe
         for b in reads:
-            self.acc.append((b, "r", "mma", t0, self.pipe_t))
+            self.acc.append((b, "r", agent, t0, t1))
         for b in writes:
-            self.acc.append((b, "w", "mma", t0, self.pipe_t))
+            self.acc.append((b, "w", agent, t0, t1))
 
-    def commit(self, name, phase=None):
-        self.later(max(self.pipe_t, self.t + 1), lambda: self.arrive(name, phase), "commit -> " + name)
+    def commit(self, name, phase=None, pipe=None):
+        t_last = self.pipe_t if pipe is None else self.pipes.get(pipe, 0)
+        self.later(max(t_last, self.t + 1), lambda: self.arrive(name, phase), "commit -> " + name)
 
     def touch(self, agent, mode, t0, *bufs, until=None):  # an access from t0 until now (or until)
         for b in bufs:

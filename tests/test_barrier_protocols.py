@@ -9,7 +9,8 @@ buffers, and work still in flight at exit.  Warps that run the same code
 are separate actors, so one may run a sub-block ahead of another.
 Planted mistakes in the models show that the checks fire.  The models
 follow attn_fwd_tc_kernel, attn_bwd_dkv_tc_kernel, attn_bwd_dq_tc_kernel
-(csrc/k_attn_tc.cu) and layernorm_bwd_kernel (csrc/k_misc.cu); a change
+(csrc/k_attn_tc.cu), gemm_tc_pair_kernel (csrc/k_gemm_tc.cu) and
+layernorm_bwd_kernel (csrc/k_misc.cu); a change
 to a kernel's hand-offs changes its model.
 """
 import pytest
@@ -487,3 +488,92 @@ def test_layernorm_backward_row_ring():
             errs = ln_bwd_ring(nrows, seed)
             assert not errs, (nrows, seed, errs[:3])
     assert find(ln_bwd_ring, "early_refill", "race on ring", [9, 20])
+
+
+# -------------------------------------------------------------- matmul CTA pairs
+GEMM_STAGES = 6
+
+
+def gemm_pair(ntiles, seed, plant=None, stages=GEMM_STAGES, kt=3):
+    """gemm_tc_pair_kernel: CTA r of the pair loads its A rows and its half
+    of the B tile into stage s; every byte lands on the leader's full[s]
+    (the leader's arrive.expect_tx is one more arrival).  The leader's MMA
+    thread issues a tile's k steps into accumulator a = tile % 2 once both
+    CTAs' epilogues released it, and its commits release stage s in both
+    CTAs (empty[s]) and hand the accumulator to both epilogues."""
+    sim = Sim(seed, plant)
+    for st in range(stages):
+        sim.bar("full_%d" % st, 5)  # expect + 2 A loads + 2 B halves
+        for c in range(2):
+            sim.bar("empty%d_%d" % (c, st))
+    for a in range(2):
+        sim.bar("accf_%d" % a)
+        sim.bar("acce_%d" % a, 2)
+    nsteps = ntiles * kt
+
+    def producer(c):
+        for it in range(nsteps):
+            st, ph = it % stages, it // stages
+            if it >= stages and plant != "refill_unguarded":
+                yield from sim.wait("empty%d_%d" % (c, st), ph - 1)
+            if c == 0:
+                sim.arrive("full_%d" % st, ph)
+            sim.tma("full_%d" % st, "A%d_%d" % (c, st), phase=ph)
+            sim.tma("full_%d" % st, "B%d_%d" % (c, st), phase=ph)
+            yield from sim.work(0, 2)
+        for d in range(max(0, nsteps - stages), nsteps):  # the last releases have landed
+            yield from sim.wait("empty%d_%d" % (c, d % stages), d // stages)
+
+    def issuer():
+        it = 0
+        for ti in range(ntiles):
+            a = ti & 1
+            if ti >= 2:
+                yield from sim.wait("acce_%d" % a, ti // 2 - 1)
+            for _ in range(kt):
+                st, ph = it % stages, it // stages
+                yield from sim.wait("full_%d" % st, ph)
+                reads = ["A%d_%d" % (c, st) for c in range(2)] + ["B%d_%d" % (c, st) for c in range(2)]
+                sim.mma(reads=reads, writes=["acc_%d" % a])
+                for c in range(2):
+                    sim.commit("empty%d_%d" % (c, st), ph)
+                it += 1
+                yield
+            sim.commit("accf_%d" % a, ti // 2)
+        for d in range(max(0, ntiles - 2), ntiles):
+            yield from sim.wait("acce_%d" % (d & 1), d // 2)
+
+    def epilogue(c):
+        for ti in range(ntiles):
+            a = ti & 1
+            yield from sim.wait("accf_%d" % a, ti // 2)
+            t0 = sim.t
+            yield from sim.work(1, 12)
+            if plant == "acc_release_early":  # released before the last TMEM loads are done
+                sim.arrive("acce_%d" % a, ti // 2)
+                sim.touch("epi%d" % c, "r", t0, "acc_%d" % a, until=sim.t + 100)
+            else:
+                sim.touch("epi%d" % c, "r", t0, "acc_%d" % a)
+                sim.arrive("acce_%d" % a, ti // 2)
+
+    sim.run([producer(c) for c in range(2)] + [issuer()] + [epilogue(c) for c in range(2)])
+    return sim.errors
+
+
+def test_matmul_pair_protocol():
+    for ntiles in (1, 2, 3, 7):
+        for kt in (1, 2, 5, 12):
+            for seed in range(3):
+                errs = gemm_pair(ntiles, seed, kt=kt)
+                assert not errs, (ntiles, kt, seed, errs[:3])
+    for seed in range(3):
+        assert not gemm_pair(5, seed, stages=2, kt=3)
+
+
+@pytest.mark.parametrize("plant,kind", [
+    ("refill_unguarded", "race on A"),     # a stage refilled while the MMAs still read it
+    ("acc_release_early", "race on acc"),  # the accumulator handed back before it is read out
+])
+def test_matmul_pair_checker_finds_a_planted_mistake(plant, kind):
+    assert find(lambda n, seed, plant=None: gemm_pair(n, seed, plant=plant, stages=2, kt=1),
+                plant, kind, [3, 7], seeds=12)
