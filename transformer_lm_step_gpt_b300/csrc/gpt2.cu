@@ -110,12 +110,18 @@ struct gpt2_model {
   char* dres_act;  // bf16 copy of dres (bf16 mode); == dres in fp32 mode
   float* dln;
   char *dbig, *datty;
-  float *dsum, *ln_partial, *cs_partial, *splitk;
+  float *dsum, *splitk;
   int64_t splitk_floats;
   int* splitk_flags;  // turnstiles of the in-kernel split-K reduction
   int64_t splitk_flag_count;
   uint32_t* enc_sorted;
   float* enc_partial;
+  // partial rows of the bias and LayerNorm weight gradients, one slot per
+  // reduction of a backward pass, added up by one launch at its end
+  float* red_part;
+  ReduceJob* red_jobs_dev;  // the job list on the device
+  int red_jobs_cap = 0;
+  std::vector<ReduceJob> red_jobs, red_jobs_up;  // this pass's jobs / the list on the device
   int* err;
   int64_t launches = 0;
   ProfState prof;
@@ -281,19 +287,26 @@ size_t layout(gpt2_model* m, char* base) {
   m->dbig = b.take<char>(M * 4 * C * a);
   m->datty = b.take<char>(M * C * a);
   m->dsum = b.take<float>((int64_t)m->B * m->NH * m->T);
-  m->ln_partial = b.take<float>(ln_partial_floats(m->M, m->C));
-  // column-sum partial rows: the fc bias gradient's (one per 32 rows of
-  // fcproj's data gradient), the colsum pass's, and the attention
-  // backward's qkv bias rows (one per batch row and 128-row block)
-  m->cs_partial = b.take<float>(std::max<int64_t>(
-      std::max<int64_t>(colsum_partial_floats(m->M, 4 * m->C), (int64_t)((m->M + 31) / 32) * 4 * m->C),
-      (int64_t)m->B * ((m->T + 127) / 128) * 3 * m->C));
   m->splitk_floats = m->bf ? 16 * C * C : 0;
   m->splitk = b.take<float>(m->splitk_floats);
   m->splitk_flag_count = m->bf ? 8192 : 0;
   m->splitk_flags = b.take<int>(m->splitk_flag_count);
   m->enc_sorted = b.take<uint32_t>(M);
   m->enc_partial = b.take<float>(M * C);
+  {
+    // per layer: the LN2 and LN1 backward partials, the fc bias partials
+    // (one row per 32 rows of the fcproj data gradient, or the column-sum
+    // pass's rows) and the qkv bias partials (one row per batch row and
+    // 128-query block from the attention backward, or the column-sum
+    // pass's); and the final LayerNorm's
+    const int64_t lnp = ln_partial_floats(m->M, m->C);
+    const int64_t fcp = std::max<int64_t>((M + 31) / 32 * 4 * C, colsum_partial_floats(m->M, 4 * m->C));
+    const int64_t qkvp = std::max<int64_t>((int64_t)m->B * ((m->T + 127) / 128) * 3 * C,
+                                           colsum_partial_floats(m->M, 3 * m->C));
+    m->red_part = b.take<float>(L * (2 * lnp + fcp + qkvp) + lnp + 64 * (4 * L + 1));  // + 256-byte slot alignment
+    m->red_jobs_cap = 4 * m->L + 1;
+    m->red_jobs_dev = b.take<ReduceJob>(m->red_jobs_cap);
+  }
   m->dec_x = b.take<float>((int64_t)m->B * C);
   m->dec_mid = b.take<float>((int64_t)m->B * C);
   m->dec_mean = b.take<float>(m->B);
@@ -510,13 +523,34 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
   // tied head: logits = lnf wte^T
   // the LayerNorm input gradients (dln) are in the activation type
   ActT* dln = reinterpret_cast<ActT*>(m->dln);
+  // the bias and LayerNorm weight gradients are column sums: each kernel
+  // that produces them leaves partial rows in a slot of its own, and one
+  // launch at the end of the pass adds every slot up (the reductions feed
+  // nothing inside the pass)
+  float* slot = m->red_part;
+  int red_blocks = 0;
+  m->red_jobs.clear();
+  auto take_slot = [&](int64_t floats) {
+    float* p = slot;
+    slot += (floats + 63) & ~(int64_t)63;
+    return p;
+  };
+  auto add_job = [&](float* d0, float* d1, float* d2, const float* partial, int nb, int W, int seg) {
+    ReduceJob j;
+    j.d[0] = d0; j.d[1] = d1; j.d[2] = d2;
+    j.partial = partial; j.nb = nb; j.W = W; j.seg = seg; j.first_block = red_blocks;
+    red_blocks += reduce_job_blocks(W);
+    m->red_jobs.push_back(j);
+  };
+  const int64_t lnp = ln_partial_floats(M, C);
   run_gemm(m, c, gemm(M, C, Vp, dlogits, Vp, true, m->W(WTE), C, false, EPI_STORE, dln, C, f32), GS_HEAD);
   run_gemm(m, c, gemm(Vp, C, M, dlogits, Vp, false, lnf, C, false, EPI_ACCUM, m->G(WTE), C, true), GS_HEAD);
   {
     ProfScope ps(m, PC_LN_BWD, lnb_bytes - 4.0 * M * C);
-    launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LNFW), m->G(LNFB),
-                               m->G(FCPROJB) + (int64_t)(L - 1) * C, dln, m->res[L],
-                               m->P(LNFW), m->lnf_mean, m->lnf_rstd, M, C, false, m->ln_partial);
+    float* part = take_slot(lnp);
+    const int nb = launch_layernorm_bwd_partials<ActT>(c, m->dres, dres_act_out, dln, m->res[L], m->P(LNFW),
+                                                       m->lnf_mean, m->lnf_rstd, M, C, false, part);
+    add_job(m->G(LNFW), m->G(LNFB), m->G(FCPROJB) + (int64_t)(L - 1) * C, part, nb, 3 * C, C);
   }
   for (int l = L - 1; l >= 0; l--) {
     ActT* ln1 = m->A<ActT>(m->ln1, l, (int64_t)M * C);
@@ -530,7 +564,8 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     GemmArgs g = gemm(M, 4 * C, C, dres_act, C, true, w(FCPROJW, (int64_t)l * C * 4 * C), 4 * C,
                       false, EPI_MUL_AUX, dbig, 4 * C, f32);
     g.aux = fcd;  // d(fc pre-activation) = d(fcg) * gelu'(x)
-    if (!f32) g.colsum_out = m->cs_partial;  // fc bias gradient partials, 32 rows each
+    float* fcb_part = take_slot(std::max<int64_t>((int64_t)(M + 31) / 32 * 4 * C, colsum_partial_floats(M, 4 * C)));
+    if (!f32) g.colsum_out = fcb_part;  // fc bias gradient partials, 32 rows each
     run_gemm(m, c, g, GS_FCPROJ);
     run_gemm(m, c, gemm(C, 4 * C, M, dres_act, C, false, fcg, 4 * C, false, EPI_ACCUM,
                         m->G(FCPROJW) + (int64_t)l * C * 4 * C, 4 * C, true), GS_FCPROJ);
@@ -541,16 +576,20 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
                         EPI_STORE, dln, C, f32), GS_FC);
     run_gemm(m, c, gemm(4 * C, C, M, dbig, 4 * C, false, ln2, C, false, EPI_ACCUM,
                         m->G(FCW) + (int64_t)l * 4 * C * C, C, true), GS_FC);
-    {
+    if (f32) {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 4.0 * C);
-      if (f32) launch_colsum<ActT>(c, m->G(FCB) + (int64_t)l * 4 * C, dbig, M, 4 * C, 4 * C, m->cs_partial);
-      else launch_colsum_reduce(c, m->G(FCB) + (int64_t)l * 4 * C, m->cs_partial, (M + 31) / 32, 4 * C);
+      const int nb = launch_colsum_partials<ActT>(c, fcb_part, dbig, M, 4 * C, 4 * C);
+      add_job(m->G(FCB) + (int64_t)l * 4 * C, nullptr, nullptr, fcb_part, nb, 4 * C, 4 * C);
+    } else {
+      add_job(m->G(FCB) + (int64_t)l * 4 * C, nullptr, nullptr, fcb_part, (M + 31) / 32, 4 * C, 4 * C);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
-      launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN2W) + l * C, m->G(LN2B) + l * C,
-                                 m->G(ATTPROJB) + (int64_t)l * C, dln, m->mid[l], m->P(LN2W) + l * C, m->ln2_mean + (int64_t)l * M,
-                                 m->ln2_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+      float* part = take_slot(lnp);
+      const int nb = launch_layernorm_bwd_partials<ActT>(c, m->dres, dres_act_out, dln, m->mid[l], m->P(LN2W) + l * C,
+                                                         m->ln2_mean + (int64_t)l * M, m->ln2_rstd + (int64_t)l * M,
+                                                         M, C, true, part);
+      add_job(m->G(LN2W) + l * C, m->G(LN2B) + l * C, m->G(ATTPROJB) + (int64_t)l * C, part, nb, 3 * C, C);
     }
     // attproj: mid = res[l] + atty Wproj^T + b.  At head size 64 (tensor-core
     // attention) its data gradient datty also yields the attention backward's
@@ -567,39 +606,60 @@ void backward_layers(gpt2_model* m, LaunchCtx& c) {
     run_gemm(m, c, gemm(C, C, M, dres_act, C, false, atty, C, false, EPI_ACCUM,
                         m->G(ATTPROJW) + (int64_t)l * C * C, C, true), GS_ATTPROJ);
     // attproj bias gradient: taken by the LN2 backward above
-    // attention (at head size 64 the tensor-core path also leaves the qkv
-    // bias gradient's partial rows in cs_partial)
+    // attention (the tensor-core path also leaves the qkv bias gradient's
+    // partial rows in its slot)
     bool qkvb_partials = false;
+    float* qkvb_part = take_slot(std::max<int64_t>((int64_t)B * ((T + 127) / 128) * 3 * C, colsum_partial_floats(M, 3 * C)));
     {
       ProfScope ps(m, PC_ATTN_BWD, attn_flop);
       if (f32) launch_attention_bwd_simt<ActT>(c, dbig, datty, atty, qkv, lse, m->dsum, B, T, C, NH, nullptr);
       else qkvb_partials = launch_attention_bwd_bf16(c, reinterpret_cast<bf16*>(dbig), reinterpret_cast<const bf16*>(datty),
                                                      reinterpret_cast<const bf16*>(atty), reinterpret_cast<const bf16*>(qkv),
-                                                     lse, m->dsum, fused_d, B, T, C, NH, m->cs_partial);
+                                                     lse, m->dsum, fused_d, B, T, C, NH, qkvb_part);
     }
     // qkv: qkv = ln1 Wqkv^T + b
     run_gemm(m, c, gemm(M, C, 3 * C, dbig, 3 * C, true, w(QKVW, (int64_t)l * 3 * C * C), C, false,
                         EPI_STORE, dln, C, f32), GS_QKV);
     run_gemm(m, c, gemm(3 * C, C, M, dbig, 3 * C, false, ln1, C, false, EPI_ACCUM,
                         m->G(QKVW) + (int64_t)l * 3 * C * C, C, true), GS_QKV);
-    {
+    if (qkvb_partials) {
+      add_job(m->G(QKVB) + (int64_t)l * 3 * C, nullptr, nullptr, qkvb_part, B * ((T + 127) / 128), 3 * C, 3 * C);
+    } else {
       ProfScope ps(m, PC_BIAS_GRAD, a * M * 3.0 * C);
-      if (qkvb_partials)
-        launch_colsum_reduce(c, m->G(QKVB) + (int64_t)l * 3 * C, m->cs_partial, B * ((T + 127) / 128), 3 * C);
-      else
-        launch_colsum<ActT>(c, m->G(QKVB) + (int64_t)l * 3 * C, dbig, M, 3 * C, 3 * C, m->cs_partial);
+      const int nb = launch_colsum_partials<ActT>(c, qkvb_part, dbig, M, 3 * C, 3 * C);
+      add_job(m->G(QKVB) + (int64_t)l * 3 * C, nullptr, nullptr, qkvb_part, nb, 3 * C, 3 * C);
     }
     {
       ProfScope ps(m, PC_LN_BWD, lnb_bytes);
-      launch_layernorm_bwd<ActT>(c, m->dres, dres_act_out, m->G(LN1W) + l * C, m->G(LN1B) + l * C,
-                                 l > 0 ? m->G(FCPROJB) + (int64_t)(l - 1) * C : nullptr, dln, m->res[l], m->P(LN1W) + l * C, m->ln1_mean + (int64_t)l * M,
-                                 m->ln1_rstd + (int64_t)l * M, M, C, true, m->ln_partial);
+      float* part = take_slot(lnp);
+      const int nb = launch_layernorm_bwd_partials<ActT>(c, m->dres, dres_act_out, dln, m->res[l], m->P(LN1W) + l * C,
+                                                         m->ln1_mean + (int64_t)l * M, m->ln1_rstd + (int64_t)l * M,
+                                                         M, C, true, part);
+      add_job(m->G(LN1W) + l * C, m->G(LN1B) + l * C, l > 0 ? m->G(FCPROJB) + (int64_t)(l - 1) * C : nullptr, part,
+              nb, 3 * C, C);
     }
   }
   {
     ProfScope ps(m, PC_ENC_BWD, 4.0 * M * C + 8.0 * T * C);
     launch_encoder_bwd(c, m->G(WTE), m->G(WPE), m->dres, m->tok, B, T, C, Vp, m->enc_sorted,
                        m->enc_partial);
+  }
+  {
+    ProfScope ps(m, PC_BIAS_GRAD, 4.0 * (double)(slot - m->red_part));
+    const int nj = (int)m->red_jobs.size();
+    if (nj > m->red_jobs_cap) {
+      c.host_fail = 1;
+      return;
+    }
+    // the list is the same every pass: it goes to the device once
+    if (m->red_jobs_up.size() != m->red_jobs.size() ||
+        std::memcmp(m->red_jobs_up.data(), m->red_jobs.data(), sizeof(ReduceJob) * nj) != 0) {
+      m->red_jobs_up = m->red_jobs;
+      if (cudaMemcpyAsync(m->red_jobs_dev, m->red_jobs_up.data(), sizeof(ReduceJob) * nj, cudaMemcpyHostToDevice,
+                          m->stream) != cudaSuccess)
+        c.host_fail = 1;
+    }
+    launch_reduce_jobs(c, m->red_jobs_dev, nj, red_blocks);
   }
 }
 

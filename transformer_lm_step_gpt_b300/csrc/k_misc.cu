@@ -701,8 +701,10 @@ __global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
   const int lane = threadIdx.x % RP_COLS, grp = threadIdx.x / RP_COLS;
   const int c = blockIdx.x * RP_COLS + lane;
   float s = 0.f;
-  if (c < W)
+  if (c < W) {
+#pragma unroll 4
     for (int b = grp; b < nb; b += RP_GROUPS) s += partial[(int64_t)b * W + c];
+  }
   sm[grp][lane] = s;
   __syncthreads();
   if (grp == 0 && c < W) {
@@ -713,6 +715,55 @@ __global__ void __launch_bounds__(RP_COLS * RP_GROUPS)
     for (int q = 0; q < RP_GROUPS; q++) t += sm[q][lane];
     d[c % seg] += t;
   }
+}
+
+// reduce_partials_kernel over a list of jobs: block b works on the job with
+// the largest first_block <= b, on its column block b - first_block.  Many
+// small reductions in one launch keep more loads in flight than one launch
+// each, and take one step of the stream's dependency chain instead of one
+// per reduction.
+__global__ void __launch_bounds__(RP_COLS * RP_GROUPS) reduce_jobs_kernel(const ReduceJob* jobs, int njobs) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float sm[RP_GROUPS][RP_COLS + 1];
+  __shared__ int sj;
+  if (threadIdx.x == 0) {
+    int lo = 0, hi = njobs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (jobs[mid].first_block <= (int)blockIdx.x) lo = mid;
+      else hi = mid - 1;
+    }
+    sj = lo;
+  }
+  __syncthreads();
+  const ReduceJob& jb = jobs[sj];
+  const int lane = threadIdx.x % RP_COLS, grp = threadIdx.x / RP_COLS;
+  const int W = jb.W, nb = jb.nb, seg = jb.seg;
+  const int c = ((int)blockIdx.x - jb.first_block) * RP_COLS + lane;
+  const float* partial = jb.partial;
+  float s = 0.f;
+  if (c < W) {
+#pragma unroll 4
+    for (int b = grp; b < nb; b += RP_GROUPS) s += partial[(int64_t)b * W + c];
+  }
+  sm[grp][lane] = s;
+  __syncthreads();
+  if (grp == 0 && c < W) {
+    float* d = c < seg ? jb.d[0] : (c < 2 * seg ? jb.d[1] : jb.d[2]);
+    if (!d) return;
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < RP_GROUPS; q++) t += sm[q][lane];
+    d[c % seg] += t;
+  }
+}
+
+int reduce_job_blocks(int W) { return cdiv(W, RP_COLS); }
+
+void launch_reduce_jobs(LaunchCtx& c, const ReduceJob* jobs, int njobs, int blocks) {
+  if (njobs <= 0 || blocks <= 0) return;
+  launch_pdl(c, reduce_jobs_kernel, dim3(blocks), dim3(RP_COLS * RP_GROUPS), 0, jobs, njobs);
 }
 
 template <typename ActT, int NCH>
@@ -726,10 +777,9 @@ static void ln_bwd_launch(LaunchCtx& c, int nb, float* dres, ActT* dres_act, flo
 }
 
 template <typename ActT>
-void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
-                          float* dres_colsum, const ActT* dy, const float* inp, const float* w,
-                          const float* mean, const float* rstd, int N, int C, bool accumulate,
-                          float* partial) {
+int launch_layernorm_bwd_partials(LaunchCtx& c, float* dres, ActT* dres_act, const ActT* dy, const float* inp,
+                                  const float* w, const float* mean, const float* rstd, int N, int C,
+                                  bool accumulate, float* partial) {
   int nb = cdiv(N, LNB_ROWS_PER_BLOCK);  // one partial row per block: nb <= ln_partial_floats / (3C)
   if (c.num_sms > 0) nb = std::min(nb, c.num_sms);
   switch ((C + 127) / 128) {  // C <= 1024 (checked by the callers): partials in registers
@@ -742,6 +792,22 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
     case 7: ln_bwd_launch<ActT, 7>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
     default: ln_bwd_launch<ActT, 8>(c, nb, dres, dres_act, partial, dy, inp, w, mean, rstd, N, C, accumulate); break;
   }
+  return nb;
+}
+template int launch_layernorm_bwd_partials<float>(LaunchCtx&, float*, float*, const float*, const float*,
+                                                  const float*, const float*, const float*, int, int, bool,
+                                                  float*);
+template int launch_layernorm_bwd_partials<bf16>(LaunchCtx&, float*, bf16*, const bf16*, const float*,
+                                                 const float*, const float*, const float*, int, int, bool,
+                                                 float*);
+
+template <typename ActT>
+void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, float* db,
+                          float* dres_colsum, const ActT* dy, const float* inp, const float* w,
+                          const float* mean, const float* rstd, int N, int C, bool accumulate,
+                          float* partial) {
+  const int nb = launch_layernorm_bwd_partials<ActT>(c, dres, dres_act, dy, inp, w, mean, rstd, N, C, accumulate,
+                                                     partial);
   launch_pdl(c, reduce_partials_kernel, dim3(cdiv(3 * C, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, dw, db, dres_colsum, partial, nb, 3 * C, C);
 }
 template void launch_layernorm_bwd<float>(LaunchCtx&, float*, float*, float*, float*, float*,
@@ -809,9 +875,17 @@ __global__ void __launch_bounds__(256) colsum_partial_kernel(float* partial, con
 }
 
 template <typename T>
-void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
+int launch_colsum_partials(LaunchCtx& c, float* partial, const T* x, int M, int N, int64_t ld) {
   dim3 grid(cdiv(N, 256), CS_CHUNKS);
   launch_pdl(c, colsum_partial_kernel<T>, dim3(grid), dim3(256), 0, partial, x, M, N, ld);
+  return CS_CHUNKS;
+}
+template int launch_colsum_partials<float>(LaunchCtx&, float*, const float*, int, int, int64_t);
+template int launch_colsum_partials<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t);
+
+template <typename T>
+void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
+  launch_colsum_partials<T>(c, partial, x, M, N, ld);
   launch_pdl(c, reduce_partials_kernel, dim3(cdiv(N, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
 }
 template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);

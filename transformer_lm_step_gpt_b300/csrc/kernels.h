@@ -106,6 +106,33 @@ int64_t colsum_partial_floats(int M, int N);
 // db[n] += sum over r < rows of partial[r * N + n], rows in order
 void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N);
 
+// ---------------------------------------------------------------- deferred column reductions
+// One reduction of partial rows: sum the nb rows of width W (row stride W)
+// of `partial`, rows in a fixed order, and add columns [i*seg, (i+1)*seg)
+// into d[i] (a null d[i] is skipped).  first_block: the job's first block
+// in a launch of several jobs (ascending over the job list).
+struct ReduceJob {
+  float* d[3];
+  const float* partial;
+  int nb, W, seg, first_block;
+};
+int reduce_job_blocks(int W);
+// Every job of a device-resident list in one launch of `blocks` blocks (the
+// sum of reduce_job_blocks over the jobs); each job's sums are the same, bit
+// for bit, as launch_colsum_reduce's or the LayerNorm backward's.
+void launch_reduce_jobs(LaunchCtx& c, const ReduceJob* jobs, int njobs, int blocks);
+// The LayerNorm backward (as launch_layernorm_bwd) without its reduction:
+// writes its partial rows and returns their number (the job is the
+// caller's: W = 3C, seg = C, d = {dw, db, dres_colsum}).
+template <typename ActT>
+int launch_layernorm_bwd_partials(LaunchCtx& c, float* dres, ActT* dres_act, const ActT* dy, const float* inp,
+                                  const float* w, const float* mean, const float* rstd, int N, int C,
+                                  bool accumulate, float* partial);
+// The column-sum partial rows of launch_colsum without their reduction;
+// returns their number (colsum_partial_floats(M, N) / N).
+template <typename T>
+int launch_colsum_partials(LaunchCtx& c, float* partial, const T* x, int M, int N, int64_t ld);
+
 // ---------------------------------------------------------------- softmax + CE
 // Per row i < M of logits [M, Vp]: loss_i = logsumexp(l[0:V]) - l[target];
 // if dlogits: logits row <- (softmax - onehot(target)) * dscale (pad cols 0).
