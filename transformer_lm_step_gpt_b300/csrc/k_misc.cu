@@ -883,16 +883,7 @@ int launch_colsum_partials(LaunchCtx& c, float* partial, const T* x, int M, int 
 template int launch_colsum_partials<float>(LaunchCtx&, float*, const float*, int, int, int64_t);
 template int launch_colsum_partials<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t);
 
-template <typename T>
-void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial) {
-  launch_colsum_partials<T>(c, partial, x, M, N, ld);
-  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(N, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, db, nullptr, nullptr, partial, CS_CHUNKS, N, N);
-}
-template void launch_colsum<float>(LaunchCtx&, float*, const float*, int, int, int64_t, float*);
-void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N) {
-  launch_pdl(c, reduce_partials_kernel, dim3(cdiv(N, RP_COLS)), dim3(RP_COLS * RP_GROUPS), 0, db, nullptr, nullptr, partial, rows, N, N);
-}
-template void launch_colsum<bf16>(LaunchCtx&, float*, const bf16*, int, int, int64_t, float*);
+
 
 // ============================================================ softmax + cross-entropy
 #define LOG2E 1.4426950408889634f

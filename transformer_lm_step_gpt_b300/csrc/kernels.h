@@ -99,12 +99,8 @@ void launch_layernorm_bwd(LaunchCtx& c, float* dres, ActT* dres_act, float* dw, 
 int64_t ln_partial_floats(int N, int C);
 
 // ---------------------------------------------------------------- column sums
-// db[j] += sum_i x[i*ld + j], i < M, j < N.  partial: float [colsum_partial_floats]
-template <typename T>
-void launch_colsum(LaunchCtx& c, float* db, const T* x, int M, int N, int64_t ld, float* partial);
+// Floats of the partial rows launch_colsum_partials writes for an M x N matrix.
 int64_t colsum_partial_floats(int M, int N);
-// db[n] += sum over r < rows of partial[r * N + n], rows in order
-void launch_colsum_reduce(LaunchCtx& c, float* db, const float* partial, int rows, int N);
 
 // ---------------------------------------------------------------- deferred column reductions
 // One reduction of partial rows: sum the nb rows of width W (row stride W)
@@ -119,7 +115,8 @@ struct ReduceJob {
 int reduce_job_blocks(int W);
 // Every job of a device-resident list in one launch of `blocks` blocks (the
 // sum of reduce_job_blocks over the jobs); each job's sums are the same, bit
-// for bit, as launch_colsum_reduce's or the LayerNorm backward's.
+// for bit, as those of one reduction launch per job (the allocation-free
+// LayerNorm backward's).
 void launch_reduce_jobs(LaunchCtx& c, const ReduceJob* jobs, int njobs, int blocks);
 // The LayerNorm backward (as launch_layernorm_bwd) without its reduction:
 // writes its partial rows and returns their number (the job is the
@@ -128,8 +125,9 @@ template <typename ActT>
 int launch_layernorm_bwd_partials(LaunchCtx& c, float* dres, ActT* dres_act, const ActT* dy, const float* inp,
                                   const float* w, const float* mean, const float* rstd, int N, int C,
                                   bool accumulate, float* partial);
-// The column-sum partial rows of launch_colsum without their reduction;
-// returns their number (colsum_partial_floats(M, N) / N).
+// Column sums of x [M x N] (row stride ld) as R = colsum_partial_floats(M, N)
+// / N partial rows: row r sums the r-th of R contiguous chunks of x's rows
+// (a fixed order); returns R.  A ReduceJob adds the rows up.
 template <typename T>
 int launch_colsum_partials(LaunchCtx& c, float* partial, const T* x, int M, int N, int64_t ld);
 
@@ -178,7 +176,7 @@ struct GemmArgs {
   int64_t splitk_flag_count;
   // EPI_MUL_AUX on the tensor-core path: if set, also the column sums of
   // the stored (bf16) output over each 32-row block, [ceil(M/32)][N] floats
-  // (launch_colsum_reduce adds them up)
+  // (a ReduceJob adds them up)
   float* colsum_out;
   // if set (few-row and CUDA-core kernels only): out and out2 start
   // (*out_row) * out_row_stride elements further, read on the device (the
@@ -235,7 +233,7 @@ void launch_attention_fwd_bf16(LaunchCtx& c, bf16* y, float* lse, const bf16* qk
 // that produced dy wrote it, EPI_DOT_AUX).
 // Returns true when it also wrote the qkv bias gradient's partial rows
 // (head size 64): bias_partial [B * ceil(T/128)][3C], row b * ceil(T/128) +
-// block (launch_colsum_reduce adds them up).
+// block (a ReduceJob adds them up).
 bool launch_attention_bwd_bf16(LaunchCtx& c, bf16* dqkv, const bf16* dy, const bf16* y,
                                const bf16* qkv, const float* lse, float* dsum, bool dsum_ready, int B,
                                int T_, int C, int NH, float* bias_partial);
