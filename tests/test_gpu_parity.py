@@ -310,15 +310,18 @@ def test_pair_split_planes_whole_step():
 # a vocabulary row of 120,000 logits (240 KB in bf16, 480 KB in fp32) is
 # larger than a block's shared memory, so the softmax / cross-entropy takes
 # the streaming kernel (two passes over the row in global memory) instead of
-# the one that stages the row in shared memory
+# the one that stages the row in shared memory; a row of 114,688 bf16 logits
+# is the largest the staged kernel takes (fourteen 16 KB pieces, all full)
 BIGVOCAB = (1, 32, 2, 120000, 120000, 8, 2, 8)
+EDGEVOCAB = (1, 32, 2, 114680, 114688, 8, 2, 8)
 
 
+@pytest.mark.parametrize("shape", [BIGVOCAB, EDGEVOCAB])
 @pytest.mark.parametrize("prec", ["fp32", "bf16"])
-def test_vocabulary_row_larger_than_shared_memory(prec):
-    res = run_steps(BIGVOCAB, prec, 2, 1e-3, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=19,
+def test_vocabulary_row_larger_than_shared_memory(shape, prec):
+    res = run_steps(shape, prec, 2, 1e-3, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=19,
                     check_grads_every_step=True)
-    assert_parity(res, BIGVOCAB, prec)
+    assert_parity(res, shape, prec)
 
 
 # ---- the edges of what the build accepts (head sizes 32 and 128, single-token
