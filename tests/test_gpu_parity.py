@@ -307,6 +307,18 @@ def test_pair_split_planes_whole_step():
     assert_parity(res, MID1024, "bf16")
 
 
+# one layer of the 124M model's width at its throughput batch (B = 16,
+# T = 1024): every product of a layer runs at the step's own shapes (192
+# tiles of 256 x 256 on the N = 768 products, more than two waves of CTA
+# pairs), and every gradient, parameter, m and v is compared
+FULLWIDTH = (1, 768, 12, 1000, 1024, 1024, 16, 1024)
+
+
+def test_full_width_layer_whole_step():
+    res = run_steps(FULLWIDTH, "bf16", 1, 6e-4, 0.9, 0.999, 1e-8, 0.1, "zipf", seed=20)
+    assert_parity(res, FULLWIDTH, "bf16")
+
+
 # a vocabulary row of 120,000 logits (240 KB in bf16, 480 KB in fp32) is
 # larger than a block's shared memory, so the softmax / cross-entropy takes
 # the streaming kernel (two passes over the row in global memory) instead of
